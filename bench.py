@@ -1,0 +1,376 @@
+"""Benchmark: train views/s of the 3D Gaussian Splatting training step (fwd + bwd + Adam).
+
+Workload (default): the 300K-Gaussian object scene at 1236x820, batch 4, 64 views on a
+ring, all fp32, seeded synthetic data (scene generator in scenes/).  One step = one batch
+of 4 views: per view projection, binning + radix sort, compositing, L1 + D-SSIM loss,
+compositing backward, projection backward; then visible sets and the visible-only Adam
+update.  throughput = steps * batch / time.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
+Targets are rendered (untimed) by the CUDA path from means jittered by N(0, 0.02).
+Between timed steps L2 is flushed by writing a 512 MB buffer (outside the timed events).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import scenes  # noqa: E402
+
+METRIC = "train views/s (fwd+bwd+Adam) at N Gaussians x res; % of HBM/FP32 roofline"
+UNIT = "views/s"
+
+# Algorithmic work per unit ("Roofline").
+FWD_FLOPS_PER_PAIR = 20      # compositing forward, FMA = 2 flops
+BWD_FLOPS_PER_PAIR = 46      # compositing backward
+# FP32 peak derived from unit counts: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+HBM_FALLBACK_GBS = 6800.0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as fh:
+                return json.load(fh), "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+def hbm_peak():
+    d, src = measured_peaks()
+    for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+        if k in d and isinstance(d[k], (int, float)):
+            return float(d[k]), src
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- oracle timing
+class OracleSampler:
+    """Times the CPU oracle on a bounded sample of the workload: the top rows of view 0 at
+    full width (same camera, smaller image), batch 1, the whole step (project, bin,
+    composite, loss, backward, Adam).  views/s = (fraction of the view) / seconds."""
+
+    def __init__(self, cfg_idx: int):
+        import oracle
+
+        self.oracle = oracle
+        self.cfg = scenes.CONFIGS[cfg_idx]
+        self.P = scenes.make_params(cfg_idx)
+        self.cam = scenes.make_cameras(cfg_idx)[0]
+        self.jit = scenes.jitter_means(self.P, self.cfg.jitter, 2000 + cfg_idx)
+        self.rows = None
+        self.tgt = None
+
+    def _cam(self, rows):
+        c = self.cam
+        return scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy, c.znear, c.width, rows)
+
+    def _run(self, rows, tgt):
+        t0 = time.perf_counter()
+        self.oracle.step(self.P, np.zeros_like(self.P), np.zeros_like(self.P), [self._cam(rows)], tgt,
+                         lr=self.cfg.lr, eps=self.cfg.eps)
+        return time.perf_counter() - t0
+
+    def calibrate(self, budget_s: float):
+        tgt = self.oracle.render_view(self.jit, self._cam(32))[None]
+        t_small = self._run(32, tgt)
+        rows = int(min(self.cfg.height, 32 * budget_s / max(t_small, 1e-3)))
+        self.rows = max(16, (rows // 16) * 16)
+        self.tgt = self.oracle.render_view(self.jit, self._cam(self.rows))[None]
+        return self.rows
+
+    def step(self):
+        t = self._run(self.rows, self.tgt)
+        return (self.rows / self.cfg.height) / t, t
+
+    def describe(self, t):
+        return (f"rows 0..{self.rows} of view 0 at full width ({t:.1f} s per sample, batch 1): project+bin+"
+                "composite+loss+backward+Adam, single thread, double precision")
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gs", choices=["gs", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = scenes.CONFIGS[args.config]
+    workload = {"workload": cfg.name, "gaussians": cfg.n, "width": cfg.width, "height": cfg.height,
+                "batch": cfg.batch, "views": cfg.n_views, "focal": cfg.focal}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        ncores = 1
+        per_step = []
+        smp = OracleSampler(args.config)
+        smp.calibrate(max(1.0, 120.0 / max(1, args.steps + args.warmup)))
+        t = 0.0
+        for i in range(args.warmup + args.steps):
+            v, t = smp.step()
+            if i >= args.warmup:
+                per_step.append(v)
+        value = statistics.median(per_step)
+        sample = "each step: " + smp.describe(t)
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.batch / value, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {**workload, "l2": "n/a (CPU)"}, "impl": "reference",
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": ncores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from gaussian_splatting_gb300 import Trainer
+
+    P = scenes.make_params(args.config)
+    cams = scenes.make_cameras(args.config)
+    jit = scenes.jitter_means(P, cfg.jitter, 2000 + args.config)
+    params = torch.from_numpy(P).cuda()
+    tr = Trainer(params.clone(), cfg.width, cfg.height, cfg.batch, lr=cfg.lr, betas=(cfg.beta1, cfg.beta2),
+                 eps=cfg.eps, w_l1=cfg.w_l1, w_ssim=cfg.w_ssim)
+    tr.reserve(cams)
+    # targets: render of the jittered scene for every view (untimed setup)
+    jit_dev = torch.from_numpy(jit).cuda()
+    targets = torch.empty((cfg.n_views, 3, cfg.height, cfg.width), dtype=torch.float32, device="cuda")
+    for v, cam in enumerate(cams):
+        tr.render(cam, targets[v], params=jit_dev)
+    torch.cuda.synchronize()
+    del jit_dev
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    def batch_of(step):
+        ids = [((step * world + rank) * cfg.batch + b) % cfg.n_views for b in range(cfg.batch)]
+        return ids, [cams[i] for i in ids]
+
+    def run_step(step):
+        ids, bc = batch_of(step)
+        tgt = targets[ids[0]:ids[0] + cfg.batch] if ids == list(range(ids[0], ids[0] + cfg.batch)) \
+            else targets[torch.tensor(ids, device="cuda")]
+        tr.step_async(bc, tgt)
+
+    for s in range(args.warmup):
+        run_step(s)
+    torch.cuda.synchronize()
+    st = tr.counts.cpu()
+    if int(st[:, 1].abs().sum()) != 0:
+        raise SystemExit(f"binning overflow during warm-up: {st.tolist()}")
+
+    # ---------------- timed region (device time, CUDA events per step)
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    tr.timer = []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.zero_()
+            starts[s].record(stream)
+            run_step(args.warmup + s)
+            ends[s].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    st = tr.counts.cpu()
+    if int(st[:, 1].abs().sum()) != 0:
+        raise SystemExit(f"binning overflow in the timed region: {st.tolist()}")
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    per_call = {}
+    for name, a, b in tr.timer:
+        per_call.setdefault(name, []).append(a.elapsed_time(b))
+    tr.timer = None
+    launches = tr.launches * args.steps
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    views = args.steps * cfg.batch * world
+    value = views / (total_ms / 1000.0)
+
+    # ---------------- work counts of the timed batches (untimed re-run, same views)
+    tr_w = Trainer(params.clone(), cfg.width, cfg.height, cfg.batch, lr=cfg.lr, eps=cfg.eps, capacity=tr.capacity)
+    tr_w.work = []
+    pairs = 0
+    for s in range(args.steps):
+        ids, bc = batch_of(args.warmup + s)
+        tr_w.step_async(bc, targets[torch.tensor(ids, device="cuda")], adam=False)
+        tr_w.grads.zero_()
+    pairs = sum(w for w, _ in tr_w.work)
+    del tr_w
+    n_launch_bwd = len(per_call.get("render_bwd", []))
+    avg = {k: sum(v) / len(v) for k, v in per_call.items()}
+    share = {k: sum(v) / total_ms for k, v in per_call.items()}
+    dominant = max(per_call, key=lambda k: sum(per_call[k]))
+    peak_hbm, hbm_src = hbm_peak()
+    roof = {}
+    pairs_per_launch = pairs / max(1, n_launch_bwd)
+    flops = {"render_fwd": FWD_FLOPS_PER_PAIR * pairs_per_launch, "render_bwd": BWD_FLOPS_PER_PAIR * pairs_per_launch}
+    if dominant in flops:
+        ach = flops[dominant] / (avg[dominant] / 1e3) / 1e12
+        roof = {"kernel": dominant, "bound": "alu", "achieved": ach, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": ach / FP32_PEAK_TFLOPS, "traffic": None,
+                "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 flop x 2.07 GHz",
+                "work": f"{pairs_per_launch:.4g} pixel-Gaussian pairs per launch"}
+    else:
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": None, "peak": peak_hbm, "unit": "GB/s",
+                "frac": None, "traffic": None, "peak_source": hbm_src}
+    others = {}
+    for k in ("render_fwd", "render_bwd"):
+        if k in flops:
+            ach = flops[k] / (avg[k] / 1e3) / 1e12
+            others[k] = {"bound": "alu", "achieved_tflops": round(ach, 3), "frac": round(ach / FP32_PEAK_TFLOPS, 4)}
+    if "sparse_adam" in avg:
+        nu = None
+        try:
+            nu = int(tr.n_union.item())
+        except Exception:
+            pass
+        if nu:
+            gbs = nu * 15 * 16 * 8 / (avg["sparse_adam"] / 1e3) / 1e9
+            others["sparse_adam"] = {"bound": "hbm", "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak_hbm, 4),
+                                     "peak_source": hbm_src}
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_t = torch.empty((cfg.n_views, 3, cfg.height, cfg.width), dtype=torch.float32).pin_memory()
+        host_t.copy_(targets.cpu())
+        for s in range(2):
+            ids, bc = batch_of(s)
+            tr.step(bc, host_t[ids])
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pinned = [host_t[batch_of(args.warmup + s)[0]].pin_memory() for s in range(args.steps)]
+        t_setup = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            ids, bc = batch_of(args.warmup + s)
+            tr.step(bc, pinned[s])
+        torch.cuda.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([t_e2e], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        del t_setup
+        e2e = {"value": views / t_e2e, "unit": UNIT,
+               "h2d_bytes_per_step": cfg.batch * 3 * cfg.height * cfg.width * 4,
+               "d2h_bytes_per_step": 4 + cfg.batch * 16}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = OracleSampler(args.config)
+        smp.calibrate(12.0)
+        v, t = smp.step()
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": smp.describe(t)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {**workload, "l2": "flushed between timed steps (512 MB write)",
+                           "parallelism": "replicas" if world > 1 else "single"},
+                "roofline": roof, "kernels": {"ms_avg": {k: round(v, 4) for k, v in avg.items()},
+                                              "share": {k: round(v, 4) for k, v in share.items()}, **others},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk.summary(), "instances_per_view": int(st[:, 0].float().mean().item())}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

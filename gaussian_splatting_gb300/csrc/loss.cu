@@ -1,0 +1,272 @@
+// L1 + SSIM image loss and its gradient in one fused pass (gs_loss).
+//
+// "Loss" step of the Grendel-GS training flow (训练流程: L1 + SSIM).  Each CTA owns a 32x32
+// output tile of one channel.  It loads the image and target with a 10-pixel halo, blurs
+// the five SSIM statistics (x, y, x^2, y^2, xy) separably with the 11-tap window over the
+// tile plus a 5-pixel halo, forms the SSIM map and its three partial derivatives there
+// (zero outside the image), and blurs those back onto the tile (the window is symmetric,
+// so the adjoint of the zero-padded window sum is the same window sum).  Nothing but the
+// per-CTA partial sums of SSIM and |x - y| goes to global scratch; a last one-CTA kernel
+// reduces them in a fixed order.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kOut = 32;               // output tile edge
+constexpr int kR = 5;                  // window radius
+constexpr int kMid = kOut + 2 * kR;    // 42: SSIM map region
+constexpr int kIn = kOut + 4 * kR;     // 52: input region
+constexpr int kThreads = 256;
+
+struct Window {
+  float w[11];
+};
+
+struct LossSmem {
+  // phase A: inputs; phase B: derivative maps (aliases the inputs)
+  union {
+    struct {
+      float x[kIn][kIn];
+      float y[kIn][kIn];
+    } in;
+    float d[3][kMid][kMid];
+  } u1;
+  // phase A: horizontal blur of 5 statistics; phase C: horizontal blur of 3 maps
+  union {
+    float h5[5][kIn][kMid];
+    float h3[3][kMid][kOut];
+  } u2;
+  float red[2][kThreads / 32];
+};
+
+__global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict__ img, const float* __restrict__ tgt,
+                                                          int W, int H, Window win, float w_l1, float w_ssim,
+                                                          float scale, float inv_n, float* __restrict__ dimg,
+                                                          float* __restrict__ partials) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  LossSmem& S = *reinterpret_cast<LossSmem*>(smem_raw);
+  const int ch = blockIdx.z;
+  const int ox = blockIdx.x * kOut, oy = blockIdx.y * kOut;
+  const int64_t P = (int64_t)W * H;
+  const float* X = img + ch * P;
+  const float* Y = tgt + ch * P;
+  const int tid = threadIdx.x;
+  // ---- A: load with 10-px halo (zero outside the image)
+  for (int e = tid; e < kIn * kIn; e += kThreads) {
+    const int r = e / kIn, c = e % kIn;
+    const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
+    float xv = 0.f, yv = 0.f;
+    if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
+      xv = __ldg(&X[(int64_t)gy * W + gx]);
+      yv = __ldg(&Y[(int64_t)gy * W + gx]);
+    }
+    S.u1.in.x[r][c] = xv;
+    S.u1.in.y[r][c] = yv;
+  }
+  __syncthreads();
+  // horizontal blur of x, y, x^2, y^2, xy: rows 0..51, columns 0..41 of the SSIM region
+  for (int e = tid; e < kIn * kMid; e += kThreads) {
+    const int r = e / kMid, c = e % kMid;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      const float xv = S.u1.in.x[r][c + k], yv = S.u1.in.y[r][c + k], w = win.w[k];
+      a0 = fmaf(w, xv, a0);
+      a1 = fmaf(w, yv, a1);
+      a2 = fmaf(w, xv * xv, a2);
+      a3 = fmaf(w, yv * yv, a3);
+      a4 = fmaf(w, xv * yv, a4);
+    }
+    S.u2.h5[0][r][c] = a0;
+    S.u2.h5[1][r][c] = a1;
+    S.u2.h5[2][r][c] = a2;
+    S.u2.h5[3][r][c] = a3;
+    S.u2.h5[4][r][c] = a4;
+  }
+  __syncthreads();
+  // ---- B: vertical blur -> SSIM statistics on the 42x42 region; map + derivatives
+  constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
+  constexpr int kPerThread = (kMid * kMid + kThreads - 1) / kThreads;  // 7
+  float ssim_sum = 0.f;
+  float dv[kPerThread][3];
+#pragma unroll
+  for (int it = 0; it < kPerThread; ++it) {
+    const int e = tid + it * kThreads;
+    dv[it][0] = dv[it][1] = dv[it][2] = 0.f;
+    if (e >= kMid * kMid) continue;
+    const int r = e / kMid, c = e % kMid;
+    float mx = 0.f, my = 0.f, exx = 0.f, eyy = 0.f, exy = 0.f;
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      const float w = win.w[k];
+      mx = fmaf(w, S.u2.h5[0][r + k][c], mx);
+      my = fmaf(w, S.u2.h5[1][r + k][c], my);
+      exx = fmaf(w, S.u2.h5[2][r + k][c], exx);
+      eyy = fmaf(w, S.u2.h5[3][r + k][c], eyy);
+      exy = fmaf(w, S.u2.h5[4][r + k][c], exy);
+    }
+    const int gy = oy - kR + r, gx = ox - kR + c;
+    float d0 = 0.f, d1 = 0.f, d2 = 0.f;
+    if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
+      const float sxx = exx - mx * mx, syy = eyy - my * my, sxy = exy - mx * my;
+      const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
+      const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
+      const float iB = 1.f / (B1 * B2);
+      const float Sv = A1 * A2 * iB;
+      d0 = 2.f * my * (A2 - A1) * iB - 2.f * mx * Sv * (1.f / B1 - 1.f / B2);  // dS/dmu_x
+      d1 = -Sv / B2;                                                            // dS/dE[x^2]
+      d2 = 2.f * A1 * iB;                                                       // dS/dE[xy]
+      if (r >= kR && r < kR + kOut && c >= kR && c < kR + kOut) ssim_sum += Sv;
+    }
+    dv[it][0] = d0;
+    dv[it][1] = d1;
+    dv[it][2] = d2;
+  }
+  __syncthreads();  // inputs no longer needed: the derivative maps overwrite them
+#pragma unroll
+  for (int it = 0; it < kPerThread; ++it) {
+    const int e = tid + it * kThreads;
+    if (e >= kMid * kMid) continue;
+    const int r = e / kMid, c = e % kMid;
+    S.u1.d[0][r][c] = dv[it][0];
+    S.u1.d[1][r][c] = dv[it][1];
+    S.u1.d[2][r][c] = dv[it][2];
+  }
+  __syncthreads();
+  // ---- C: horizontal blur of the three derivative maps onto the output columns
+  for (int e = tid; e < kMid * kOut; e += kThreads) {
+    const int r = e / kOut, c = e % kOut;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      const float w = win.w[k];
+      a0 = fmaf(w, S.u1.d[0][r][c + k], a0);
+      a1 = fmaf(w, S.u1.d[1][r][c + k], a1);
+      a2 = fmaf(w, S.u1.d[2][r][c + k], a2);
+    }
+    S.u2.h3[0][r][c] = a0;
+    S.u2.h3[1][r][c] = a1;
+    S.u2.h3[2][r][c] = a2;
+  }
+  __syncthreads();
+  // ---- D: vertical blur, combine with the L1 term, write dL/dx
+  float l1_sum = 0.f;
+  for (int e = tid; e < kOut * kOut; e += kThreads) {
+    const int r = e / kOut, c = e % kOut;
+    const int gy = oy + r, gx = ox + c;
+    if (gx >= W || gy >= H) continue;
+    float t0 = 0.f, t1 = 0.f, t2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 11; ++k) {
+      const float w = win.w[k];
+      t0 = fmaf(w, S.u2.h3[0][r + k][c], t0);
+      t1 = fmaf(w, S.u2.h3[1][r + k][c], t1);
+      t2 = fmaf(w, S.u2.h3[2][r + k][c], t2);
+    }
+    const int64_t g = (int64_t)gy * W + gx;
+    const float xv = __ldg(&X[g]), yv = __ldg(&Y[g]);
+    const float diff = xv - yv;
+    l1_sum += fabsf(diff);
+    const float sgn = diff > 0.f ? 1.f : (diff < 0.f ? -1.f : 0.f);
+    const float dssim = t0 + 2.f * xv * t1 + yv * t2;
+    dimg[ch * P + g] = scale * inv_n * (w_l1 * sgn - w_ssim * dssim);
+  }
+  // ---- fixed-order block reduction of the two sums
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ssim_sum += __shfl_xor_sync(0xffffffffu, ssim_sum, o);
+    l1_sum += __shfl_xor_sync(0xffffffffu, l1_sum, o);
+  }
+  if (lane == 0) {
+    S.red[0][warp] = ssim_sum;
+    S.red[1][warp] = l1_sum;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float a = 0.f, b = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      a += S.red[0][w];
+      b += S.red[1][w];
+    }
+    const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    partials[2 * blk] = a;
+    partials[2 * blk + 1] = b;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_loss_final(const float* __restrict__ partials, int64_t nblk, float w_l1,
+                                                     float w_ssim, float scale, double inv_n, float* loss,
+                                                     int accumulate) {
+  __shared__ double s[2][256];
+  double a = 0.0, b = 0.0;
+  for (int64_t i = threadIdx.x; i < nblk; i += 256) {
+    a += (double)partials[2 * i];
+    b += (double)partials[2 * i + 1];
+  }
+  s[0][threadIdx.x] = a;
+  s[1][threadIdx.x] = b;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) {
+      s[0][threadIdx.x] += s[0][threadIdx.x + o];
+      s[1][threadIdx.x] += s[1][threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double ssim = s[0][0] * inv_n, l1 = s[1][0] * inv_n;
+    const float v = (float)((double)scale * ((double)w_l1 * l1 + (double)w_ssim * (1.0 - ssim)));
+    *loss = accumulate ? *loss + v : v;
+  }
+}
+
+int64_t loss_blocks(int W, int H) {
+  return (int64_t)((W + kOut - 1) / kOut) * ((H + kOut - 1) / kOut) * 3;
+}
+
+Window make_window() {
+  double h[11], s = 0;
+  for (int k = 0; k < 11; ++k) {
+    h[k] = std::exp(-double((k - 5) * (k - 5)) / (2.0 * 1.5 * 1.5));
+    s += h[k];
+  }
+  Window w;
+  for (int k = 0; k < 11; ++k) w.w[k] = (float)(h[k] / s);
+  return w;
+}
+
+}  // namespace
+
+extern "C" size_t gs_loss_workspace_size(int width, int height) {
+  if (width <= 0 || height <= 0) return 0;
+  return sizeof(float) * 2 * (size_t)loss_blocks(width, height);
+}
+
+extern "C" gs_status gs_loss(const float* image, const float* target, int width, int height, float w_l1,
+                             float w_ssim, float scale, float* loss_dev, int accumulate, float* dL_dimage,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (width <= 0 || height <= 0 || width > 32768 || height > 32768)
+    return gs::set_error(GS_ERR_INVALID, "gs_loss: bad image size %d x %d", width, height);
+  if (!image || !target || !loss_dev || !dL_dimage || !workspace)
+    return gs::set_error(GS_ERR_INVALID, "gs_loss: NULL pointer");
+  if (!gs::aligned8(workspace)) return gs::set_error(GS_ERR_INVALID, "gs_loss: misaligned workspace");
+  const size_t need = gs_loss_workspace_size(width, height);
+  if (workspace_bytes < need)
+    return gs::set_error(GS_ERR_INVALID, "gs_loss: workspace %zu bytes < %zu needed", workspace_bytes, need);
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
+  if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss: %s", cudaGetErrorString(attr));
+  cudaStream_t st = gs::as_stream(stream);
+  const double n = 3.0 * (double)width * (double)height;
+  dim3 grid((width + kOut - 1) / kOut, (height + kOut - 1) / kOut, 3);
+  float* partials = reinterpret_cast<float*>(workspace);
+  k_loss_fused<<<grid, kThreads, sizeof(LossSmem), st>>>(image, target, width, height, make_window(), w_l1, w_ssim,
+                                                         scale, (float)(1.0 / n), dL_dimage, partials);
+  if (gs_status s = gs::check_launch("gs_loss")) return s;
+  k_loss_final<<<1, 256, 0, st>>>(partials, loss_blocks(width, height), w_l1, w_ssim, scale, 1.0 / n, loss_dev,
+                                  accumulate);
+  return gs::check_launch("gs_loss final");
+}

@@ -1,0 +1,216 @@
+"""One 3D Gaussian Splatting training step on one GPU, driven through libgs.so.
+
+``Trainer`` owns the device state (parameters, gradients, Adam moments, per-view scratch)
+as torch tensors -- torch supplies memory and the stream, every computation is a libgs.so
+kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
+training flow (训练流程): for each view project -> bin/sort -> composite -> loss ->
+composite backward -> projection backward; then the visible sets and the visible-only
+Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch scaling).
+
+The step never synchronises with the host.  The tile-instance buffers have a capacity;
+when a view overflows it, gs_sparse_adam skips the update (it reads the per-view status
+words), ``step`` notices on its one readback of the loss, grows the buffers and runs the
+batch again.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import _native as N
+
+# kernels each entry point launches (memset nodes are not counted)
+LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_bwd": 1, "visible_sets": 7,
+            "sparse_adam": 1}
+
+
+def bin_sort_launches(cam) -> int:
+    tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
+    bits = max(1, (tiles - 1).bit_length())
+    return 4 + (4 + (bits + 7) // 8)  # scan, histogram, digit scan, ranges + radix passes
+
+
+@dataclasses.dataclass
+class StepResult:
+    loss: torch.Tensor       # device scalar (float32)
+    status: torch.Tensor     # device int64 [B, 2]: instance count and status per view
+
+
+class Trainer:
+    def __init__(self, params: torch.Tensor, width: int, height: int, batch: int, lr: float = 1e-3,
+                 betas=(0.9, 0.999), eps: float = 1e-15, w_l1: float = 0.8, w_ssim: float = 0.2,
+                 bg=(0.0, 0.0, 0.0), capacity: int = 0):
+        if params.device.type != "cuda" or params.dtype != torch.float32 or params.dim() != 3 or params.shape[0] != 15 \
+                or params.shape[2] != 4:
+            raise ValueError("params must be a CUDA float32 tensor of shape [15, N, 4]")
+        N.load()
+        dev = params.device
+        self.n = params.shape[1]
+        self.width, self.height, self.batch = width, height, batch
+        self.lr, self.betas, self.eps = lr, betas, eps
+        self.w_l1, self.w_ssim, self.bg = w_l1, w_ssim, tuple(bg)
+        self.params = params.contiguous()
+        self.grads = torch.zeros_like(self.params)
+        self.exp_avg = torch.zeros_like(self.params)
+        self.exp_avg_sq = torch.zeros_like(self.params)
+        self.t = 0
+        n, P = self.n, width * height
+        tiles = ((width + 15) // 16) * ((height + 15) // 16)
+        f32, i32, i64 = torch.float32, torch.int32, torch.int64
+        self.proj = torch.zeros((batch, 3, n, 4), dtype=f32, device=dev)
+        self.grad2d = torch.zeros((n, 12), dtype=f32, device=dev)
+        self.image = torch.zeros((3, height, width), dtype=f32, device=dev)
+        self.T_final = torch.zeros((height, width), dtype=f32, device=dev)
+        self.n_contrib = torch.zeros((height, width), dtype=i32, device=dev)
+        self.dimg = torch.zeros((3, height, width), dtype=f32, device=dev)
+        self.ranges = torch.zeros((tiles, 2), dtype=i32, device=dev)
+        self.counts = torch.zeros((batch, 2), dtype=i64, device=dev)
+        self.loss = torch.zeros(1, dtype=f32, device=dev)
+        self.loss_ws = torch.empty(max(N.gs_loss_workspace_size(width, height), 256), dtype=torch.uint8, device=dev)
+        self.vis_ws = torch.empty(max(N.gs_visible_sets_workspace_size(batch, n), 256), dtype=torch.uint8, device=dev)
+        self.offsets = torch.zeros(batch + 1, dtype=i64, device=dev)
+        self.indices = torch.zeros(max(batch * n, 1), dtype=i32, device=dev)
+        self.union_idx = torch.zeros(max(n, 1), dtype=i32, device=dev)
+        self.n_union = torch.zeros(1, dtype=i64, device=dev)
+        self.inter = torch.zeros((batch, batch), dtype=i64, device=dev)
+        self.jaccard = torch.zeros((batch, batch), dtype=f32, device=dev)
+        self.target_dev = torch.zeros((batch, 3, height, width), dtype=f32, device=dev)
+        self.capacity = 0
+        self.keys = self.vals = self.sort_ws = None
+        self.launches = 0
+        self.timer = None  # list of (name, start event, end event) when timing per call
+        self.work = None   # list of (sum of n_contrib, view) when counting work (synchronises)
+        if capacity:
+            self._alloc_sort(capacity)
+
+    # ------------------------------------------------------------------ buffers
+    def _alloc_sort(self, capacity: int):
+        capacity = int(min(capacity, (1 << 30) - 1))
+        dev = self.params.device
+        self.keys = torch.empty(capacity, dtype=torch.int64, device=dev)
+        self.vals = torch.empty(capacity, dtype=torch.int32, device=dev)
+        self._ws_cam = None
+        self.capacity = capacity
+        self.sort_ws = None
+
+    def _sort_ws(self, cam):
+        need = N.gs_bin_sort_workspace_size(self.n, self.capacity, cam)
+        if self.sort_ws is None or self.sort_ws.numel() < need:
+            self.sort_ws = torch.empty(need, dtype=torch.uint8, device=self.params.device)
+        return self.sort_ws
+
+    def reserve(self, cams, slack: float = 1.25):
+        """Size the instance buffers for these cameras (one synchronising count per view)."""
+        best = 0
+        for cam in cams:
+            N.gs_project(self.params, self.n, cam, self.proj[0])
+            if self.capacity == 0:
+                self._alloc_sort(1024)
+            ws = self._sort_ws(cam)
+            try:
+                m = N.gs_bin_sort(self.proj[0], self.n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity,
+                                  self.ranges, self.counts[0], sync=True)
+            except N.GSError as e:
+                if e.status != N.GS_ERR_CAPACITY:
+                    raise
+                m = int(self.counts[0, 0].item())
+            best = max(best, m)
+        want = int(best * slack) + 4096
+        if want > self.capacity:
+            self._alloc_sort(want)
+        return best
+
+    def render(self, cam, out: torch.Tensor | None = None, params: torch.Tensor | None = None) -> torch.Tensor:
+        """Forward render of one view (project, bin/sort, composite) into ``out`` [3, H, W]."""
+        if self.capacity == 0:
+            self.reserve([cam])
+        params = self.params if params is None else params
+        if out is None:
+            out = torch.empty((3, self.height, self.width), dtype=torch.float32, device=self.params.device)
+        proj = self.proj[0]
+        N.gs_project(params, self.n, cam, proj)
+        ws = self._sort_ws(cam)
+        N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity, self.ranges,
+                      self.counts[0])
+        N.gs_render_fwd(proj, self.n, self.vals, self.ranges, cam, self.bg, out, self.T_final, self.n_contrib)
+        return out
+
+    # ------------------------------------------------------------------ the step
+    def _timed(self, name, fn, *args, **kw):
+        if self.timer is None:
+            return fn(*args, **kw)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn(*args, **kw)
+        e.record()
+        self.timer.append((name, s, e))
+
+    def _enqueue(self, cams, targets: torch.Tensor, adam: bool = True):
+        B = len(cams)
+        n, W, H = self.n, self.width, self.height
+        inv_b = 1.0 / B
+        launches = 0
+        T = self._timed
+        for b, cam in enumerate(cams):
+            proj = self.proj[b]
+            T("project", N.gs_project, self.params, n, cam, proj)
+            ws = self._sort_ws(cam)
+            T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity,
+              self.ranges, self.counts[b])
+            T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
+              self.n_contrib)
+            T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
+              self.dimg, self.loss_ws, self.loss_ws.numel())
+            T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
+              self.n_contrib, self.dimg, self.grad2d)
+            T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d, self.grads)
+            if self.work is not None:
+                self.work.append((int(self.n_contrib.sum()), b))
+            launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in
+                                                     ("project", "render_fwd", "loss", "render_bwd", "project_bwd"))
+        T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
+          self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard)
+        launches += LAUNCHES["visible_sets"]
+        if adam:
+            T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,
+              self.union_idx, self.n_union, n, self.lr, self.betas[0], self.betas[1], self.eps, B, self.t + 1,
+              self.counts, B)
+            launches += LAUNCHES["sparse_adam"]
+        self.launches = launches
+
+    def step_async(self, cams, targets: torch.Tensor, adam: bool = True) -> StepResult:
+        """Enqueue one step on the current stream without any host synchronisation.
+
+        ``targets`` is a device tensor [B, 3, H, W].  The caller must check ``status``
+        (all [:, 1] zero) before trusting the update; ``step`` does that for you.
+        """
+        if self.capacity == 0:
+            self.reserve(cams)
+        self._enqueue(cams, targets, adam)
+        if adam:
+            self.t += 1
+        return StepResult(self.loss, self.counts)
+
+    def step(self, cams, targets: torch.Tensor, adam: bool = True) -> float:
+        """One training step over the views ``cams``; returns the batch loss (host float).
+
+        ``targets`` may be a device tensor or a (pinned) host tensor [B, 3, H, W]; host
+        targets are copied in on the current stream.
+        """
+        if targets.device.type != "cuda":
+            self.target_dev[: len(cams)].copy_(targets, non_blocking=True)
+            targets = self.target_dev
+        while True:
+            res = self.step_async(cams, targets, adam)
+            counts = res.status.cpu()
+            if int(counts[: len(cams), 1].abs().sum()) == 0:
+                return float(res.loss.item())
+            if adam:
+                self.t -= 1
+            if int(counts[:, 1].bitwise_and(2).sum()) != 0:
+                raise RuntimeError("gs_bin_sort: a device-side wait gave up")
+            # overflow: the update was skipped; clear the partial gradients and grow
+            self.grads.zero_()
+            self._alloc_sort(int(int(counts[:, 0].max()) * 1.25) + 4096)

@@ -1,0 +1,220 @@
+/*
+ * gs.h -- C ABI of the GB300 3D Gaussian Splatting training-step library (libgs.so).
+ *
+ * One training step over a batch of B views is, per view:
+ *   gs_project -> gs_bin_sort -> gs_render_fwd -> gs_loss -> gs_render_bwd -> gs_project_bwd
+ * and, once per batch, gs_visible_sets -> gs_sparse_adam.
+ * The step follows the training flow of the Grendel-GS notes ("训练流程": transform,
+ * render by depth-sorted alpha compositing, L1 + SSIM loss, backpropagation, update)
+ * with the visible-only update of the Odin summary ("研究背景与动机": a view renders,
+ * backpropagates and updates only the primitives it sees).
+ *
+ * Conventions shared by every entry point
+ *  - All array arguments are DEVICE pointers owned by the caller unless a comment says
+ *    "host".  The library never allocates device memory in these calls: scratch comes
+ *    from a caller workspace sized by the matching *_workspace_size() call.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) unless it says it synchronises.
+ *  - Arrays of float4 records must be 16-byte aligned; 64-bit arrays 8-byte aligned.
+ *  - Returns GS_OK, or an error code with a message readable by gs_last_error() (per
+ *    host thread).  Argument errors are detected on the host before anything is enqueued.
+ *  - Layouts (float32, plane-major):
+ *      params  [15][N][4]  p0 = (x, y, z, opacity logit), p1 = (log s0, log s1, log s2, 0),
+ *                          p2 = quaternion (w, x, y, z), p3..p14 = SH sh[k][c] flattened as
+ *                          3k + c (k = 0..15 degree<=3 coefficients, c = r, g, b), four per
+ *                          plane -- the 59-float record of the Grendel-GS parameter table.
+ *      proj    [3][N][4]   q0 = (u, v, depth z, opacity), q1 = (conic A, B, C, radius as int32
+ *                          bits), q2 = (r, g, b, tiles touched as int32 bits).  A culled
+ *                          Gaussian has radius 0 and tiles 0.
+ *      grad2d  [N][12]     (du, dv, dopacity, 0, dA, dB, dC, 0, dr, dg, db, 0).
+ *      image   [3][H][W]   channel-major; T_final and n_contrib are [H][W].
+ *  - Pixel (px, py) is sampled at (px + 0.5, py + 0.5); tiles are 16 x 16 pixels
+ *    (Grendel-GS notes §1.2), numbered row-major, Tx = ceil(W/16), Ty = ceil(H/16).
+ */
+#ifndef GS_H_
+#define GS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GS_OK = 0,
+  GS_ERR_INVALID = 1,   /* null pointer, misalignment, negative size, bad dimensions */
+  GS_ERR_CUDA = 2,      /* a CUDA runtime call failed; message from cudaGetErrorString */
+  GS_ERR_CAPACITY = 3,  /* the instance count exceeds the caller's capacity */
+  GS_ERR_TIMEOUT = 4    /* a bounded device-side wait gave up (see gs_bin_sort) */
+} gs_status;
+
+/* Pinhole camera, OpenCV axes (x right, y down, z forward).  p_cam = R p_world + t,
+ * R row-major.  u = fx x/z + cx, v = fy y/z + cy.  Gaussians with z <= znear are culled. */
+typedef struct {
+  float R[9];
+  float t[3];
+  float fx, fy, cx, cy, znear;
+  int32_t width, height;
+} gs_camera;
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* gs_last_error(void);
+
+/* Library ABI version (increments when a signature changes). */
+int gs_version(void);
+
+/* ---------------------------------------------------------------------------
+ * gs_project -- per-Gaussian projection ("transform" step: 3D Gaussian -> screen
+ * position, depth, footprint radius, colour; Grendel-GS notes, 训练流程).
+ * For Gaussian i of params [15][n][4], writes proj [3][n][4]:
+ *   cull if z <= znear; s = exp(log s); opacity = sigmoid(logit); q normalised;
+ *   Sigma = R(q) diag(s^2) R(q)^T; J = perspective Jacobian at the camera-space point
+ *   with x/z, y/z clamped to +-1.3 tan(fov/2); Sigma2D = J R Sigma R^T J^T + 0.3 I;
+ *   conic = Sigma2D^-1 (cull if det <= 0); radius = ceil(3 sqrt(lambda_max));
+ *   tile rectangle [floor((u-r)/16), floor((u+r)/16)+1) clamped to the grid (cull if
+ *   empty); colour = max(0, sum_k sh[k] Y_k(dir) + 0.5) with dir the unit vector from
+ *   the camera centre to the mean and Y_k the real degree-3 SH basis.
+ * n == 0 is a no-op.
+ */
+gs_status gs_project(const float* params, int64_t n, const gs_camera* cam, float* proj, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_bin_sort -- tile binning and depth sort ("find the Gaussians covering a pixel,
+ * sort by depth"; Grendel-GS notes, 训练流程, with 16x16 tiles, §1.2).
+ * Every Gaussian with radius > 0 is duplicated once per tile of its rectangle
+ * (Gaussian index ascending, tiles row-major within the rectangle) with
+ *   key = (tile id << 32) | float bits of z,  value = Gaussian index,
+ * and the M instances are stably radix-sorted by key, i.e. ordered by (tile, depth,
+ * index).  ranges[2t], ranges[2t+1] = [start, end) of tile t in the sorted arrays,
+ * [0, 0) for an empty tile.
+ *   proj       [3][n][4] from gs_project.
+ *   workspace  gs_bin_sort_workspace_size(n, capacity, cam) bytes, 256-byte aligned.
+ *   keys, vals outputs of `capacity` entries.
+ *   ranges     output, 2 * Tx * Ty uint32.
+ *   count      device int64[2]: count[0] = M (the true count even when it exceeds
+ *              capacity), count[1] = status bits (0 = ok, 1 = capacity exceeded,
+ *              2 = a look-back wait gave up).  On any nonzero status the outputs are
+ *              not valid and ranges are left empty.
+ *   count_host optional host int64: if non-NULL the call synchronises the stream, stores
+ *              M there, and returns GS_ERR_CAPACITY / GS_ERR_TIMEOUT per count[1].
+ * capacity must be < 2^30.  The device-side waits of the single-pass scan and of the
+ * radix passes are bounded; none can hang.
+ */
+size_t gs_bin_sort_workspace_size(int64_t n, int64_t capacity, const gs_camera* cam);
+gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
+                      size_t workspace_bytes, uint64_t* keys, uint32_t* vals, int64_t capacity,
+                      uint32_t* ranges, int64_t* count, int64_t* count_host, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_render_fwd -- per-pixel front-to-back alpha compositing of the tile's sorted list
+ * (Grendel-GS notes, 训练流程 "图像渲染").  For pixel p and list entries j in order:
+ *   d = p + 0.5 - (u, v); power = -(A dx^2 + C dy^2)/2 - B dx dy; skip if power > 0;
+ *   alpha = min(0.99, opacity * exp(power)); skip if alpha < 1/255;
+ *   T' = T (1 - alpha); stop before this entry if T' < 1e-4;
+ *   C += colour * alpha * T; T = T'.
+ *   image = C + T bg;  T_final = T;  n_contrib = 1 + list position of the last
+ *   accumulated entry (0 if none).
+ * bg is a host array of 3 floats (may be NULL for black).
+ */
+gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
+                        const gs_camera* cam, const float* bg, float* image, float* T_final,
+                        uint32_t* n_contrib, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_loss -- L1 + SSIM image loss ("损失计算：L1 + SSIM 损失", Grendel-GS notes, 训练流程)
+ * and its gradient.  Per view:
+ *   loss = w_l1 * mean|I - I*| + w_ssim * (1 - mean SSIM),
+ * means over all 3*H*W values; SSIM per channel with an 11x11 Gaussian window
+ * (sigma 1.5, normalised), zero padding, C1 = 0.01^2, C2 = 0.03^2, sigma terms
+ * E[x^2] - mu^2.  Writes dL_dimage = scale * dloss/dimage and
+ *   *loss_dev = scale * loss          (accumulate == 0)
+ *   *loss_dev += scale * loss         (accumulate != 0)
+ * The loss value is reduced in a fixed order (deterministic).
+ * workspace: gs_loss_workspace_size(width, height) bytes.
+ */
+size_t gs_loss_workspace_size(int width, int height);
+gs_status gs_loss(const float* image, const float* target, int width, int height, float w_l1,
+                  float w_ssim, float scale, float* loss_dev, int accumulate, float* dL_dimage,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_render_bwd -- reverse-order backward of gs_render_fwd ("反向传播").  Walks each
+ * pixel's list back to front from n_contrib, recovering T by T / (1 - alpha), and
+ * writes per-Gaussian screen-space gradients into grad2d [n][12] (the call clears
+ * grad2d first; contributions of all pixels are summed with atomics, so the
+ * summation order, and the last bits, vary from run to run).
+ */
+gs_status gs_render_bwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
+                        const gs_camera* cam, const float* bg, const float* T_final,
+                        const uint32_t* n_contrib, const float* dL_dimage, float* grad2d,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_project_bwd -- reverse mode of gs_project: grad2d -> parameter gradients,
+ * ACCUMULATED (+=) into grads [15][n][4] so that a batch's views sum.  Only Gaussians
+ * with radius > 0 in proj are touched.  Exact derivative of the forward, including the
+ * quaternion normalisation, the clamped Jacobian, the view direction of the SH colour
+ * and the colour clamp at 0.
+ */
+gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, const float* proj,
+                         const float* grad2d, float* grads, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_visible_sets -- per-view visible sets and their pairwise overlaps, the inputs of a
+ * primitive-level RAW/WAW/WAR check (Odin summary §1 Jaccard weight w_ij = |Pi n Pj| /
+ * |Pi u Pj|, 0 for an empty union; Odin article: the hook that collects the active
+ * primitives after backward).
+ *   proj_per_view  HOST array of `batch` device pointers to proj [3][n][4].
+ *   V_b = {i : radius_b[i] > 0}.
+ *   offsets  [batch + 1] int64; indices [batch * n] uint32: V_b ascending at
+ *            indices[offsets[b] .. offsets[b+1]).
+ *   union_idx [n] uint32 ascending; *n_union (device int64) = |U|, U = union of V_b.
+ *   inter    [batch][batch] int64 = |V_i n V_j|.
+ *   jaccard  [batch][batch] float = fp32 rounding of the exact ratio inter / |V_i u V_j|
+ *            (computed in double from the integer counts), 0 when the union is empty.
+ * workspace: gs_visible_sets_workspace_size(batch, n) bytes.  batch in [1, 64].
+ */
+size_t gs_visible_sets_workspace_size(int batch, int64_t n);
+gs_status gs_visible_sets(const float* const* proj_per_view, int batch, int64_t n, void* workspace,
+                          size_t workspace_bytes, int64_t* offsets, uint32_t* indices,
+                          uint32_t* union_idx, int64_t* n_union, int64_t* inter, float* jaccard,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_sparse_adam -- Adam on the listed Gaussians only, with the batch scaling rule of
+ * the Grendel-GS notes §4.2: lr' = lr sqrt(batch), beta1' = beta1^batch,
+ * beta2' = beta2^batch.  For every float of the listed Gaussians' 15 planes:
+ *   m = beta1' m + (1 - beta1') g;  v = beta2' v + (1 - beta2') g^2;
+ *   p -= lr' (m / (1 - beta1'^step)) / (sqrt(v / (1 - beta2'^step)) + eps);  g = 0.
+ * Gaussians not listed keep p, m, v and g bit-for-bit.
+ *   idx     union_idx from gs_visible_sets (strictly ascending, each < n).
+ *   n_idx   DEVICE int64 count of idx entries (<= max_idx); read by the kernel so the
+ *           call needs no host synchronisation.
+ *   step    t >= 1, the number of batches applied so far including this one.
+ *   counts  optional DEVICE array of n_counts int64[2] records from gs_bin_sort (one per
+ *           view of the batch); if any record's status word (element [1]) is nonzero the
+ *           whole update is skipped, so a batch whose binning overflowed leaves the
+ *           parameters and moments untouched and can be re-run.  NULL: never skipped.
+ */
+gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp_avg_sq, int64_t n,
+                         const uint32_t* idx, const int64_t* n_idx, int64_t max_idx, float lr,
+                         float beta1, float beta2, float eps, int batch, int64_t step,
+                         const int64_t* counts, int n_counts, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Test hooks (no counterpart in the method).
+ * gs_debug_set_wait_limit: iterations a device-side look-back wait spins before it
+ *   gives up and reports status bit 2 (default 1 << 22; values < 1 restore it).
+ * gs_debug_drop_publish: if nonzero, the next gs_bin_sort call's radix pass 0 never
+ *   publishes tile 0's prefix, so every later tile's wait runs out; used to test
+ *   that the bounded wait reports GS_ERR_TIMEOUT instead of hanging.
+ */
+void gs_debug_set_wait_limit(int64_t iterations);
+void gs_debug_drop_publish(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H_ */
