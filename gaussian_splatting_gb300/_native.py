@@ -66,7 +66,7 @@ def load() -> C.CDLL:
         "gs_project": ([vp, i64, cp, vp, vp], i32),
         "gs_bin_sort_workspace_size": ([i64, i64, cp], sz),
         "gs_bin_sort": ([vp, i64, cp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
-        "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp], i32),
+        "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
         "gs_loss_workspace_size": ([i32, i32], sz),
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
         "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
@@ -140,10 +140,11 @@ def gs_bin_sort(proj, n, cam, workspace, workspace_bytes, keys, vals, capacity, 
     return host.value if sync else None
 
 
-def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, stream=None):
+def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, work=None, stream=None):
     b = _floats3(bg)
     _check(load().gs_render_fwd(_ptr(proj), n, _ptr(vals), _ptr(ranges), _cam(cam), b[0] if b else None,
-                                _ptr(image), _ptr(T_final), _ptr(n_contrib), _stream(stream)), "gs_render_fwd")
+                                _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(work), _stream(stream)),
+           "gs_render_fwd")
 
 
 def gs_loss_workspace_size(width, height) -> int:

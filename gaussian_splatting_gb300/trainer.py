@@ -28,7 +28,9 @@ LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_
 def bin_sort_launches(cam) -> int:
     tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
     bits = max(1, (tiles - 1).bit_length())
-    return 4 + (4 + (bits + 7) // 8)  # scan, histogram, digit scan, ranges + radix passes
+    tile_passes = max(1, (bits + 7) // 8)
+    # depth keys + digit scan, 4 depth passes, scan/dup + histogram + digit scan + ranges, tile passes
+    return 2 + 4 + 4 + tile_passes
 
 
 @dataclasses.dataclass
@@ -80,7 +82,7 @@ class Trainer:
         self.keys = self.vals = self.sort_ws = None
         self.launches = 0
         self.timer = None  # list of (name, start event, end event) when timing per call
-        self.work = None   # list of (sum of n_contrib, view) when counting work (synchronises)
+        self.work = None   # list of per-view work counts when measuring (synchronises)
         if capacity:
             self._alloc_sort(capacity)
 
@@ -159,15 +161,19 @@ class Trainer:
             ws = self._sort_ws(cam)
             T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity,
               self.ranges, self.counts[b])
+            work_buf = None
+            if self.work is not None:
+                work_buf = torch.zeros((2, H, W), dtype=torch.int32, device=self.params.device)
             T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
-              self.n_contrib)
+              self.n_contrib, work_buf)
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               self.dimg, self.loss_ws, self.loss_ws.numel())
             T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
               self.n_contrib, self.dimg, self.grad2d)
             T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d, self.grads)
             if self.work is not None:
-                self.work.append((int(self.n_contrib.sum()), b))
+                # (entries evaluated in the forward, entries accumulated, entries walked by the backward)
+                self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum())))
             launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in
                                                      ("project", "render_fwd", "loss", "render_bwd", "project_bwd"))
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),

@@ -1,0 +1,79 @@
+"""Host-side checks of the C ABI (no GPU needed): every symbol include/gs.h declares is
+exported by libgs.so, and argument errors are rejected on the host before any CUDA call."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gs.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gs_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gaussian_splatting_gb300 import build
+    build.build()
+    from gaussian_splatting_gb300 import _native
+    return _native.load()
+
+
+def test_header_declares_the_eight_step_calls():
+    names = declared_functions()
+    for f in ["gs_project", "gs_bin_sort", "gs_render_fwd", "gs_loss", "gs_render_bwd", "gs_project_bwd",
+              "gs_sparse_adam", "gs_visible_sets"]:
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gaussian_splatting_gb300 import _native
+    names = declared_functions()
+    assert set(names) == set(_native.EXPORTS)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_host_side_argument_errors(lib):
+    from gaussian_splatting_gb300 import _native as N
+    import scenes
+    cam = N.camera(scenes.make_cameras(0)[0])
+    assert lib.gs_version() >= 1
+    # negative n / NULL pointers / bad sizes fail on the host with GS_ERR_INVALID
+    assert lib.gs_project(None, -1, C.byref(cam), None, None) == N.GS_ERR_INVALID
+    assert b"bad n" in lib.gs_last_error()
+    assert lib.gs_project(None, 5, C.byref(cam), None, None) == N.GS_ERR_INVALID
+    assert lib.gs_loss(None, None, 0, 4, 0.8, 0.2, 1.0, None, 0, None, None, 0, None) == N.GS_ERR_INVALID
+    assert lib.gs_visible_sets(None, 0, 10, None, 0, None, None, None, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_sparse_adam(None, None, None, None, 10, None, None, 10, 1e-3, 0.9, 0.999, 1e-15, 0, 1, None, 0,
+                              None) == N.GS_ERR_INVALID
+    bad = N.camera(scenes.make_cameras(0)[0])
+    bad.width = 0
+    assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None) == N.GS_ERR_INVALID
+    # misaligned workspace / capacity bounds for the sort
+    assert lib.gs_bin_sort(None, 0, C.byref(cam), 8, 10, None, None, 1 << 30, 64, 64, None, None) == N.GS_ERR_INVALID
+
+
+def test_workspace_sizes_are_pure_host_functions(lib):
+    from gaussian_splatting_gb300 import _native as N
+    import scenes
+    cam = scenes.make_cameras(1)[0]
+    a = N.gs_bin_sort_workspace_size(300_000, 10_000_000, cam)
+    b = N.gs_bin_sort_workspace_size(300_000, 20_000_000, cam)
+    assert 0 < a < b
+    assert N.gs_loss_workspace_size(1236, 820) > 0
+    assert N.gs_visible_sets_workspace_size(4, 300_000) > 0
+    assert N.gs_visible_sets_workspace_size(65, 10) == 0
+
+
+def test_launch_count_bookkeeping():
+    import scenes
+    from gaussian_splatting_gb300.trainer import bin_sort_launches
+    # 4056 tiles -> 12 tile bits -> 2 tile passes; depth sort has 4
+    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 2 + 4 + 4 + 2
+    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 2 + 4 + 4 + 1
