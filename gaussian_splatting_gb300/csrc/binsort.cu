@@ -7,24 +7,25 @@
 // How: a stable sort by tile of a list that is already in (depth, index) order is the sort
 // by (tile, depth, index).  So the N Gaussians are sorted once by depth (4 stable radix
 // passes over 32-bit keys; equal depths keep index order), the instances are emitted in
-// that order, and only the tile bits of the M instances are radix-sorted
-// (ceil(log2(tiles) / 8) passes: 2 for up to 65,536 tiles) -- about a third of the traffic
-// of sorting all 64 key bits of the M instances.
+// that order as (tile, index) pairs, and only the tile ids of the M instances are
+// radix-sorted (ceil(log2(tiles) / 8) passes: 2 for up to 65,536 tiles) on 8-byte pairs --
+// about a third of the traffic of sorting all 64 key bits of 12-byte pairs.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   k_depth_init  depth keys (0xFFFFFFFF for culled Gaussians) + their digit histograms;
-//                 clears the look-back state of the depth passes.
+//                 clears the look-back state of every pass.
 //   k_digit_scan  exclusive digit offsets per pass.
 //   k_onesweep    one stable radix pass of 8 bits: persistent CTAs take 4096-key tiles in
 //                 order from an atomic counter, rank keys within the tile in shared memory
 //                 (warp match-any ranking), get the tile's global digit offsets by
 //                 decoupled look-back and scatter through shared memory so the global
-//                 writes are digit-contiguous.  Templated on 32- and 64-bit keys.
+//                 writes are digit-contiguous.
 //   k_scan_dup    single-pass scan (decoupled look-back) of tiles-touched over the depth-
-//                 sorted Gaussians; each CTA writes its contiguous run of instances with
-//                 coalesced stores.  The last chunk publishes M.
-//   k_histogram   tile-digit histograms of the instances; clears their look-back state.
-//   k_ranges      [start, end) of every tile from neighbouring keys.
+//                 sorted Gaussians; each CTA writes its contiguous run of (tile, index)
+//                 pairs with coalesced stores and adds the run's tile-digit histograms.
+//                 The last chunk publishes M.
+//   k_finalize    64-bit keys (tile << 32 | depth bits), values, and every tile's
+//                 [start, end) from neighbouring tile ids.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
 #include <mutex>
@@ -34,7 +35,7 @@
 namespace {
 
 constexpr int kScanThreads = 256;
-constexpr int kScanItems = 8;
+constexpr int kScanItems = 2;
 constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
 
 constexpr int kSortThreads = 256;
@@ -57,8 +58,8 @@ constexpr int kSmDigitBase = kSmHist + kSlots * 256;
 constexpr int kSmWords = kSmDigitBase + kSlots * 256;
 
 struct Workspace {
-  uint64_t* keys_alt;
-  uint32_t* vals_alt;
+  uint32_t* tkey[2];               // instance tile ids, ping-pong
+  uint32_t* tval[2];               // instance Gaussian indices, ping-pong
   uint32_t* dkey[2];
   uint32_t* didx[2];
   unsigned long long* scan_state;  // per scan chunk
@@ -86,8 +87,10 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses) {
     return p;
   };
   const int64_t chunks = (n + kScanChunk - 1) / kScanChunk;
-  char* ka = take(sizeof(uint64_t) * (size_t)cap);
-  char* va = take(sizeof(uint32_t) * (size_t)cap);
+  char* tk0 = take(sizeof(uint32_t) * (size_t)cap);
+  char* tk1 = take(sizeof(uint32_t) * (size_t)cap);
+  char* tv0 = take(sizeof(uint32_t) * (size_t)cap);
+  char* tv1 = take(sizeof(uint32_t) * (size_t)cap);
   char* dk0 = take(sizeof(uint32_t) * (size_t)n);
   char* dk1 = take(sizeof(uint32_t) * (size_t)n);
   char* di0 = take(sizeof(uint32_t) * (size_t)n);
@@ -97,8 +100,10 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses) {
   char* lbt = take(sizeof(uint32_t) * 256 * (size_t)tpasses * (size_t)sort_tiles(cap));
   char* sm = take(sizeof(uint32_t) * kSmWords);
   if (w) {
-    w->keys_alt = reinterpret_cast<uint64_t*>(ka);
-    w->vals_alt = reinterpret_cast<uint32_t*>(va);
+    w->tkey[0] = reinterpret_cast<uint32_t*>(tk0);
+    w->tkey[1] = reinterpret_cast<uint32_t*>(tk1);
+    w->tval[0] = reinterpret_cast<uint32_t*>(tv0);
+    w->tval[1] = reinterpret_cast<uint32_t*>(tv1);
     w->dkey[0] = reinterpret_cast<uint32_t*>(dk0);
     w->dkey[1] = reinterpret_cast<uint32_t*>(dk1);
     w->didx[0] = reinterpret_cast<uint32_t*>(di0);
@@ -138,13 +143,15 @@ __device__ __forceinline__ uint32_t wait_u32(const uint32_t* p, int64_t limit, b
 // ------------------------------------------------------------------ depth keys
 __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ proj, int64_t n,
                                                      uint32_t* __restrict__ dkey, uint32_t* __restrict__ didx,
-                                                     uint32_t* small, uint32_t* lb_depth) {
+                                                     uint32_t* small, uint32_t* lb_depth, uint32_t* lb_tile,
+                                                     int64_t lb_tile_words) {
   __shared__ uint32_t s_hist[kDepthPasses][256];
   const float4* q0 = reinterpret_cast<const float4*>(proj);
   const float4* q1 = q0 + n;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t w = gtid; w < (int64_t)kDepthPasses * sort_tiles(n) * 256; w += stride) lb_depth[w] = 0u;
+  for (int64_t w = gtid; w < lb_tile_words; w += stride) lb_tile[w] = 0u;
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
   __syncthreads();
   for (int64_t i = gtid; i < n; i += stride) {
@@ -159,32 +166,6 @@ __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ pr
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) {
     const uint32_t c = (&s_hist[0][0])[i];
     if (c) atomicAdd(&small[kSmHist + i], c);
-  }
-}
-
-// ------------------------------------------------------------------ tile-digit histograms
-__global__ void __launch_bounds__(256) k_histogram(const uint64_t* __restrict__ keys, int64_t cap, int tpasses,
-                                                    uint32_t* small, uint32_t* lb_tile, const int64_t* count) {
-  __shared__ uint32_t s_hist[kMaxTilePasses][256];
-  if (count[1] != 0) return;
-  const int64_t M = min(count[0], cap);
-  const int64_t tiles = sort_tiles(M), tiles_cap = sort_tiles(cap);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t w = gtid; w < (int64_t)tpasses * tiles * 256; w += stride) {
-    const int64_t pass = w / (tiles * 256), rest = w % (tiles * 256);
-    lb_tile[pass * tiles_cap * 256 + rest] = 0u;
-  }
-  for (int i = threadIdx.x; i < kMaxTilePasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
-  __syncthreads();
-  for (int64_t i = gtid; i < M; i += stride) {
-    const uint32_t tile = (uint32_t)(keys[i] >> 32);
-    for (int p = 0; p < tpasses; ++p) atomicAdd(&s_hist[p][(tile >> (8 * p)) & 255u], 1u);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < tpasses * 256; i += blockDim.x) {
-    const uint32_t c = (&s_hist[0][0])[i];
-    if (c) atomicAdd(&small[kSmHist + kDepthPasses * 256 + i], c);
   }
 }
 
@@ -229,7 +210,7 @@ __device__ __forceinline__ uint32_t digit_of(K key, int shift) {
 
 // n_host >= 0: sort n_host keys; otherwise min(count[0], cap) keys.
 template <typename K>
-__global__ void __launch_bounds__(kSortThreads) k_onesweep(const K* __restrict__ kin, const uint32_t* __restrict__ vin,
+__global__ void __launch_bounds__(kSortThreads, 3) k_onesweep(const K* __restrict__ kin, const uint32_t* __restrict__ vin,
                                                             K* __restrict__ kout, uint32_t* __restrict__ vout,
                                                             int64_t n_host, int64_t cap, int shift, int slot,
                                                             uint32_t* small, uint32_t* lookback_pass, int64_t* count,
@@ -355,22 +336,25 @@ __global__ void __launch_bounds__(kSortThreads) k_onesweep(const K* __restrict__
 }
 
 // ------------------------------------------------------------------ scan + duplicate
-// Walks the Gaussians in depth order (skey / sidx: depth-sorted keys and indices).
+// Walks the Gaussians in depth order (skey / sidx: depth-sorted keys and indices) and writes
+// (tile id, Gaussian index) pairs; also accumulates the tile-digit histograms of the pairs.
 __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restrict__ proj, int64_t n,
                                                             const uint32_t* __restrict__ skey,
-                                                            const uint32_t* __restrict__ sidx, gs::Cam k,
-                                                            uint64_t* __restrict__ keys, uint32_t* __restrict__ vals,
+                                                            const uint32_t* __restrict__ sidx, gs::Cam k, int tpasses,
+                                                            uint32_t* __restrict__ tkey, uint32_t* __restrict__ tval,
                                                             int64_t cap, unsigned long long* scan_state,
                                                             uint32_t* small, int64_t* count, int64_t limit) {
   __shared__ uint32_t s_items[kScanChunk];   // tiles touched, then local exclusive offsets
   __shared__ uint32_t s_rect[kScanChunk];    // x0 | y0 << 16
   __shared__ uint32_t s_width[kScanChunk];   // rectangle width in tiles
   __shared__ uint32_t s_gauss[kScanChunk];
+  __shared__ uint32_t s_hist[kMaxTilePasses][256];
   __shared__ uint32_t s_warp[kScanThreads / 32];
   __shared__ unsigned long long s_prefix;
   __shared__ uint32_t s_chunk;
   const int tid = threadIdx.x;
   if (tid == 0) s_chunk = atomicAdd(&small[kSmScanCounter], 1u);
+  for (int i = tid; i < kMaxTilePasses * 256; i += kScanThreads) (&s_hist[0][0])[i] = 0u;
   __syncthreads();
   const int64_t chunk = s_chunk;
   const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
@@ -381,7 +365,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
   for (int j = 0; j < kScanItems; ++j) {
     const int li = j * kScanThreads + tid;
     const int64_t i = base + li;
-    uint32_t cnt = 0, rect = 0, width = 0, g = 0;
+    uint32_t cnt = 0, rect = 0, width = 1, g = 0;
     if (i < n && skey[i] != kCulledKey) {
       g = sidx[i];
       const int r = __float_as_int(__ldg(&q1[g].w));
@@ -402,7 +386,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
     s_gauss[li] = g;
   }
   __syncthreads();
-  // blocked scan: thread t owns items t*8 .. t*8+7
+  // blocked scan: thread t owns items t*kScanItems .. +kScanItems-1
   uint32_t v[kScanItems];
   uint32_t sum = 0;
 #pragma unroll
@@ -469,26 +453,38 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
     const uint32_t j = p - s_items[lo];
     const uint32_t w = s_width[lo];
     const uint32_t rect = s_rect[lo];
-    const uint32_t tx = (rect & 0xffffu) + j % w, ty = (rect >> 16) + j / w;
-    const uint32_t g = s_gauss[lo];
+    const uint32_t row = j / w;
+    const uint32_t tx = (rect & 0xffffu) + (j - row * w), ty = (rect >> 16) + row;
+    const uint32_t tile = ty * (uint32_t)k.Tx + tx;
     const int64_t o = out0 + p;
     if (o < cap) {
-      keys[o] = ((uint64_t)(ty * (uint32_t)k.Tx + tx) << 32) | __float_as_uint(__ldg(&q0[g].z));
-      vals[o] = g;
+      tkey[o] = tile;
+      tval[o] = s_gauss[lo];
     }
+    for (int q = 0; q < tpasses; ++q) atomicAdd(&s_hist[q][(tile >> (8 * q)) & 255u], 1u);
+  }
+  __syncthreads();
+  for (int i = tid; i < tpasses * 256; i += kScanThreads) {
+    const uint32_t c = (&s_hist[0][0])[i];
+    if (c) atomicAdd(&small[kSmHist + kDepthPasses * 256 + i], c);
   }
 }
 
-// ------------------------------------------------------------------ tile ranges
-__global__ void k_ranges(const uint64_t* __restrict__ keys, int64_t cap, uint32_t* __restrict__ ranges,
-                         const int64_t* count) {
+// ------------------------------------------------------------------ keys, values, ranges
+__global__ void __launch_bounds__(256) k_finalize(const float* __restrict__ proj, const uint32_t* __restrict__ tkey,
+                                                   const uint32_t* __restrict__ tval, int64_t cap,
+                                                   uint64_t* __restrict__ keys, uint32_t* __restrict__ vals,
+                                                   uint32_t* __restrict__ ranges, const int64_t* count) {
   if (count[1] != 0) return;
+  const float4* q0 = reinterpret_cast<const float4*>(proj);
   const int64_t M = min(count[0], cap);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride) {
-    const uint32_t t = (uint32_t)(keys[i] >> 32);
-    if (i == 0 || (uint32_t)(keys[i - 1] >> 32) != t) ranges[2 * (int64_t)t] = (uint32_t)i;
-    if (i == M - 1 || (uint32_t)(keys[i + 1] >> 32) != t) ranges[2 * (int64_t)t + 1] = (uint32_t)(i + 1);
+    const uint32_t t = tkey[i], g = tval[i];
+    keys[i] = ((uint64_t)t << 32) | __float_as_uint(__ldg(&q0[g].z));
+    vals[i] = g;
+    if (i == 0 || tkey[i - 1] != t) ranges[2 * (int64_t)t] = (uint32_t)i;
+    if (i == M - 1 || tkey[i + 1] != t) ranges[2 * (int64_t)t + 1] = (uint32_t)(i + 1);
   }
 }
 
@@ -552,7 +548,9 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
       return gs::check_launch("gs_bin_sort memset");
     const int sms = gs::num_sms();
     // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys
-    k_depth_init<<<sms * 4, 256, 0, st>>>(proj, n, w.dkey[0], w.didx[0], w.small, w.lb_depth);
+    const int64_t lb_tile_words = (int64_t)tpasses * sort_tiles(capacity) * 256;
+    k_depth_init<<<sms * 4, 256, 0, st>>>(proj, n, w.dkey[0], w.didx[0], w.small, w.lb_depth, w.lb_tile,
+                                          lb_tile_words);
     k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
     const int grid32 = sms * sort_blocks_per_sm<uint32_t>();
     for (int p = 0; p < kDepthPasses; ++p) {
@@ -561,28 +559,21 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
           w.lb_depth + (size_t)p * sort_tiles(n) * 256, count, limit, p == 0 ? drop : 0);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
-    // 2. instances in depth order; the last tile pass lands in the caller's arrays
-    uint64_t* ka = (tpasses % 2 == 0) ? keys : w.keys_alt;
-    uint32_t* va = (tpasses % 2 == 0) ? vals : w.vals_alt;
-    uint64_t* kb = (tpasses % 2 == 0) ? w.keys_alt : keys;
-    uint32_t* vb = (tpasses % 2 == 0) ? w.vals_alt : vals;
-    k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, ka, va, capacity,
-                                                           w.scan_state, w.small, count, limit);
+    // 2. (tile, index) pairs in depth order, with their tile-digit histograms
+    k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, tpasses, w.tkey[0],
+                                                           w.tval[0], capacity, w.scan_state, w.small, count, limit);
     if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
-    // 3. stable sort of the instances by tile id
-    k_histogram<<<sms * 4, 256, 0, st>>>(ka, capacity, tpasses, w.small, w.lb_tile, count);
+    // 3. stable sort of the pairs by tile id
     k_digit_scan<<<1, 256, 0, st>>>(w.small, kDepthPasses, tpasses, count);
-    const int grid64 = sms * sort_blocks_per_sm<uint64_t>();
     for (int p = 0; p < tpasses; ++p) {
-      k_onesweep<uint64_t><<<grid64, kSortThreads, sizeof(SortSmem<uint64_t>), st>>>(
-          ka, va, kb, vb, -1, capacity, 32 + 8 * p, kDepthPasses + p, w.small,
-          w.lb_tile + (size_t)p * sort_tiles(capacity) * 256, count, limit, 0);
-      std::swap(ka, kb);
-      std::swap(va, vb);
+      k_onesweep<uint32_t><<<grid32, kSortThreads, sizeof(SortSmem<uint32_t>), st>>>(
+          w.tkey[p & 1], w.tval[p & 1], w.tkey[(p + 1) & 1], w.tval[(p + 1) & 1], -1, capacity, 8 * p,
+          kDepthPasses + p, w.small, w.lb_tile + (size_t)p * sort_tiles(capacity) * 256, count, limit, 0);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
-    k_ranges<<<sms * 4, 256, 0, st>>>(keys, capacity, ranges, count);
-    if (gs_status s = gs::check_launch("gs_bin_sort ranges")) return s;
+    k_finalize<<<sms * 8, 256, 0, st>>>(proj, w.tkey[tpasses & 1], w.tval[tpasses & 1], capacity, keys, vals, ranges,
+                                        count);
+    if (gs_status s = gs::check_launch("gs_bin_sort finalize")) return s;
   }
   if (count_host) {
     int64_t hc[2] = {0, 0};

@@ -4,26 +4,30 @@
 // pixel composites the depth-sorted Gaussians of its 16x16 tile front to back; the backward
 // walks the same lists back to front.
 //
-// Layout: one 64-thread CTA per tile, 4 pixels per thread.  Warp 0 owns rows 0-7 and warp 1
-// rows 8-15; lane l owns column l % 16 and the four rows 4 (l / 16) .. +3 of its warp's half,
-// so a thread's pixels share dx and a warp covers a compact 16x8 block (a Gaussian that
-// misses that block is skipped by the whole warp at once).  The tile's list is walked in
-// batches of 256 Gaussians gathered into shared memory (4 per thread) and evaluated from
-// shared memory with broadcast reads.  The conic is stored scaled by -log2(e)/2 so that
-// alpha = opacity * 2^p costs one ex2; a per-Gaussian threshold p_min = log2(1/(255 opacity))
-// rejects pairs below the 1/255 skip before the ex2.  Forward and backward evaluate every
-// (pixel, Gaussian) pair through the same functions, so the backward's T / (1 - alpha)
-// recovery retraces the forward's decisions exactly.
+// Layout: one 128-thread CTA per tile.  Warp w owns the 16x4 block of rows 4w..4w+3; lane l
+// owns column l % 16 and the two rows 4w + 2 (l / 16) + {0, 1}.  The tile's list is walked in
+// batches of 256 Gaussians gathered into shared memory (2 per thread).  While gathering,
+// each Gaussian gets a 4-bit mask of the warp blocks that the bounding box of its
+// alpha >= 1/255 ellipse touches (enlarged by a rounding slack), and every warp compacts the
+// batch, in order, into its own list: a warp never evaluates a Gaussian whose alpha is
+// below the skip threshold on all of its pixels.  Per-pixel results are those of walking the
+// full list.
 //
-// The backward sums each Gaussian's nine gradient terms over a thread's pixels, then over
-// the warp with a transposed butterfly (16 shuffles for 16 lanes of values instead of 45),
-// and one warp-wide atomic add puts the nine sums into grad2d.
+// The conic is stored scaled by -log2(e)/2 so that alpha = opacity * 2^p costs one ex2, and
+// a per-Gaussian threshold p_min = log2(1/(255 opacity)) rejects pairs below the 1/255 skip
+// before the ex2.  Forward and backward evaluate every (pixel, Gaussian) pair through the
+// same functions, so the backward's T / (1 - alpha) recovery retraces the forward exactly.
+//
+// The backward sums a Gaussian's nine gradient terms over a thread's two pixels, then over
+// the warp with a transposed butterfly (16 shuffles instead of 45), and nine lanes add the
+// sums to grad2d with one warp-wide atomic instruction.
 #include "common.cuh"
 
 namespace {
 
-constexpr int kThreads = 64;   // per tile
-constexpr int kPPT = 4;        // pixels per thread
+constexpr int kThreads = 128;  // per tile
+constexpr int kWarps = kThreads / 32;
+constexpr int kPPT = 2;        // pixels per thread
 constexpr int kBatch = 256;    // Gaussians per shared-memory batch
 constexpr int kPerThreadLoad = kBatch / kThreads;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -31,25 +35,61 @@ constexpr float kAlphaMin = 1.0f / 255.0f;
 constexpr float kAlphaMax = 0.99f;
 constexpr float kTMin = 1e-4f;
 
-// Gathered record: s0 = (u, v, a2, b2), s1 = (c2, opacity, p_min, Gaussian index bits),
-// s2 = (r, g, b, 0) with (a2, b2, c2) = log2(e) * (-A/2, -B, -C/2), so that
-// p = a2 dx^2 + b2 dx dy + c2 dy^2 = log2(e) * power.
-struct Rec {
-  float4 s0, s1, s2;
+struct __align__(16) BatchSmem {
+  float4 s0[kBatch];        // (u, v, a2, b2)
+  float4 s1[kBatch];        // (c2, opacity, p_min, Gaussian index bits)
+  float4 s2[kBatch];        // (r, g, b, 0)
+  uint32_t mask[kBatch];    // warp blocks the Gaussian can reach
+  uint8_t list[kWarps][kBatch];
+  uint32_t count[kWarps];
 };
 
-__device__ __forceinline__ Rec gather_record(const float* __restrict__ proj, int64_t n, uint32_t g) {
+// (a2, b2, c2) = log2(e) * (-A/2, -B, -C/2), so p = a2 dx^2 + b2 dx dy + c2 dy^2 = log2(e) power.
+__device__ __forceinline__ void gather_record(const float* __restrict__ proj, int64_t n, uint32_t g, int tile_x0,
+                                              int tile_y0, BatchSmem& S, int slot) {
   const float4 q0 = ldg4(proj, g);
   const float4 q1 = ldg4(proj, n + g);
   const float4 q2 = ldg4(proj, 2 * n + g);
-  Rec r;
-  r.s0 = make_float4(q0.x, q0.y, -0.5f * kLog2e * q1.x, -kLog2e * q1.y);
   // alpha < 1/255  <=>  p < log2(1 / (255 opacity))
   float lg;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(q0.w * 255.0f));
-  r.s1 = make_float4(-0.5f * kLog2e * q1.z, q0.w, -lg, __uint_as_float(g));
-  r.s2 = make_float4(q2.x, q2.y, q2.z, 0.f);
-  return r;
+  S.s0[slot] = make_float4(q0.x, q0.y, -0.5f * kLog2e * q1.x, -kLog2e * q1.y);
+  S.s1[slot] = make_float4(-0.5f * kLog2e * q1.z, q0.w, -lg, __uint_as_float(g));
+  S.s2[slot] = make_float4(q2.x, q2.y, q2.z, 0.f);
+  // bounding box of {d : d^T conic d <= K}, K = 2 ln(255 opacity): half-widths sqrt(K Sigma_xx),
+  // sqrt(K Sigma_yy) with Sigma = conic^-1; enlarged so rounding never drops a reachable pair
+  uint32_t m = 0;
+  const float K = 2.0f * logf(255.0f * q0.w);
+  const float det = q1.x * q1.z - q1.y * q1.y;
+  if (K > 0.f && det > 0.f) {
+    const float hx = sqrtf(K * q1.z / det) * 1.001f + 0.05f;
+    const float hy = sqrtf(K * q1.x / det) * 1.001f + 0.05f;
+    const float xmin = (float)tile_x0 + 0.5f, xmax = (float)tile_x0 + 15.5f;
+    if (q0.x + hx >= xmin && q0.x - hx <= xmax) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float ymin = (float)(tile_y0 + 4 * w) + 0.5f, ymax = ymin + 3.0f;
+        if (q0.y + hy >= ymin && q0.y - hy <= ymax) m |= 1u << w;
+      }
+    }
+  } else if (!(det > 0.f) && K > 0.f) {
+    m = (1u << kWarps) - 1u;  // degenerate record: keep it everywhere
+  }
+  S.mask[slot] = m;
+}
+
+// Ordered compaction of the batch entries whose mask has this warp's bit.
+__device__ __forceinline__ void build_list(BatchSmem& S, int cnt, int warp, int lane) {
+  uint32_t total = 0;
+  for (int base = 0; base < cnt; base += 32) {
+    const int k = base + lane;
+    const bool in = k < cnt && ((S.mask[k] >> warp) & 1u);
+    const uint32_t bal = __ballot_sync(0xffffffffu, in);
+    if (in) S.list[warp][total + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)k;
+    total += __popc(bal);
+  }
+  if (lane == 0) S.count[warp] = total;
+  __syncwarp();
 }
 
 // p at pixel-centre offset (dx, dy), with e = a2 * dx shared by a thread's column.  Explicit
@@ -66,87 +106,87 @@ __device__ __forceinline__ float alpha_of(float opacity, float G) {
 // p passes the skip tests (power <= 0 and alpha >= 1/255 before the clamp)
 __device__ __forceinline__ bool candidate(float p, float pmin) { return p >= pmin && !(p > 0.f); }
 
-__device__ __forceinline__ void pixel_of(int tile, int Tx, int lane, int warp, int& px, int& py0) {
-  const int tx = tile % Tx, ty = tile / Tx;
-  px = tx * gs::kTile + (lane & 15);
-  py0 = ty * gs::kTile + warp * 8 + (lane >> 4) * 4;
-}
-
-__global__ void __launch_bounds__(kThreads) k_render_fwd(const float* __restrict__ proj, int64_t n,
-                                                         const uint32_t* __restrict__ vals,
-                                                         const uint32_t* __restrict__ ranges, int W, int H, int Tx,
-                                                         float3 bg, float* __restrict__ image,
-                                                         float* __restrict__ T_final, uint32_t* __restrict__ n_contrib,
-                                                         uint32_t* __restrict__ work) {
-  __shared__ float4 s0[kBatch];
-  __shared__ float4 s1[kBatch];
-  __shared__ float4 s2[kBatch];
+template <bool kCount>
+__global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restrict__ proj, int64_t n,
+                                                            const uint32_t* __restrict__ vals,
+                                                            const uint32_t* __restrict__ ranges, int W, int H,
+                                                            int Tx, float3 bg, float* __restrict__ image,
+                                                            float* __restrict__ T_final,
+                                                            uint32_t* __restrict__ n_contrib,
+                                                            uint32_t* __restrict__ work) {
+  __shared__ BatchSmem S;
   const int tile = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int px, py0;
-  pixel_of(tile, Tx, lane, warp, px, py0);
+  const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
+  const int px = tile_x0 + (lane & 15), py0 = tile_y0 + 4 * warp + 2 * (lane >> 4);
   const float fx = (float)px + 0.5f;
+  float fy[kPPT];
   const uint32_t start = ranges[2 * tile], end = ranges[2 * tile + 1];
   float T[kPPT], cr[kPPT], cg[kPPT], cb[kPPT];
-  uint32_t last[kPPT], evald[kPPT], used[kPPT];
+  uint32_t last[kPPT], stop[kPPT], used[kPPT];
   bool done[kPPT];
 #pragma unroll
   for (int i = 0; i < kPPT; ++i) {
+    fy[i] = (float)(py0 + i) + 0.5f;
     T[i] = 1.f;
     cr[i] = cg[i] = cb[i] = 0.f;
-    last[i] = evald[i] = used[i] = 0;
+    last[i] = used[i] = 0;
+    stop[i] = end - start;  // entries evaluated if the pixel never saturates
     done[i] = !(px < W && py0 + i < H);
   }
+  bool warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
   for (uint32_t b0 = start; b0 < end; b0 += kBatch) {
-    int mine = 0;
-#pragma unroll
-    for (int i = 0; i < kPPT; ++i) mine += done[i] ? 1 : 0;
-    if (__syncthreads_count(mine == kPPT) == kThreads) break;
+    if (__syncthreads_count(warp_done) == kThreads) break;
+    const int cnt = (int)min((uint32_t)kBatch, end - b0);
 #pragma unroll
     for (int r = 0; r < kPerThreadLoad; ++r) {
       const int slot = r * kThreads + threadIdx.x;
-      const uint32_t j = b0 + slot;
-      if (j < end) {
-        const Rec rec = gather_record(proj, n, __ldg(&vals[j]));
-        s0[slot] = rec.s0;
-        s1[slot] = rec.s1;
-        s2[slot] = rec.s2;
-      }
+      if (slot < cnt) gather_record(proj, n, __ldg(&vals[b0 + slot]), tile_x0, tile_y0, S, slot);
     }
     __syncthreads();
-    const int cnt = (int)min((uint32_t)kBatch, end - b0);
-    for (int k = 0; k < cnt; ++k) {
-      bool all_done = true;
-#pragma unroll
-      for (int i = 0; i < kPPT; ++i) all_done &= done[i];
-      if (all_done) break;
-      const float4 a = s0[k];
-      const float4 c = s1[k];
+    build_list(S, cnt, warp, lane);
+    const int nl = (int)S.count[warp];
+    for (int q = 0; q < nl && !warp_done; ++q) {
+      const int k = S.list[warp][q];
+      const float4 a = S.s0[k];
+      const float4 c = S.s1[k];
       const float dx = fx - a.x;
       const float e = __fmul_rn(a.z, dx);
+      float p[kPPT];
+      bool hit[kPPT];
+      bool any = false;
 #pragma unroll
       for (int i = 0; i < kPPT; ++i) {
-        if (done[i]) continue;
-        ++evald[i];
-        const float dy = ((float)(py0 + i) + 0.5f) - a.y;
-        const float p = power2(a, c, dx, e, dy);
-        if (!candidate(p, c.z)) continue;
-        const float alpha = alpha_of(c.y, fast_exp2(p));
-        if (alpha < kAlphaMin) continue;
-        const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
-        if (Tn < kTMin) {
-          done[i] = true;
-          continue;
-        }
-        const float4 col = s2[k];
-        const float w = alpha * T[i];
-        cr[i] = fmaf(w, col.x, cr[i]);
-        cg[i] = fmaf(w, col.y, cg[i]);
-        cb[i] = fmaf(w, col.z, cb[i]);
-        T[i] = Tn;
-        last[i] = b0 - start + (uint32_t)k + 1u;
-        ++used[i];
+        p[i] = power2(a, c, dx, e, fy[i] - a.y);
+        hit[i] = !done[i] && candidate(p[i], c.z);
+        any |= hit[i];
       }
+      bool ended = false;
+      if (any) {
+        const float4 col = S.s2[k];
+        const uint32_t pos = b0 - start + (uint32_t)k;
+#pragma unroll
+        for (int i = 0; i < kPPT; ++i) {
+          if (!hit[i]) continue;
+          const float alpha = alpha_of(c.y, fast_exp2(p[i]));
+          if (alpha < kAlphaMin) continue;
+          const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
+          if (Tn < kTMin) {
+            done[i] = true;
+            stop[i] = pos + 1u;
+            ended = true;
+            continue;
+          }
+          const float w = alpha * T[i];
+          cr[i] = fmaf(w, col.x, cr[i]);
+          cg[i] = fmaf(w, col.y, cg[i]);
+          cb[i] = fmaf(w, col.z, cb[i]);
+          T[i] = Tn;
+          last[i] = pos + 1u;
+          if (kCount) ++used[i];
+        }
+      }
+      if (__any_sync(0xffffffffu, ended)) warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
     }
     __syncthreads();
   }
@@ -161,8 +201,8 @@ __global__ void __launch_bounds__(kThreads) k_render_fwd(const float* __restrict
       image[2 * P + pix] = cb[i] + T[i] * bg.z;
       T_final[pix] = T[i];
       n_contrib[pix] = last[i];
-      if (work) {
-        work[pix] = evald[i];
+      if (kCount) {
+        work[pix] = stop[i];
         work[P + pix] = used[i];
       }
     }
@@ -188,29 +228,29 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) 
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-__global__ void __launch_bounds__(kThreads) k_render_bwd(const float* __restrict__ proj, int64_t n,
-                                                         const uint32_t* __restrict__ vals,
-                                                         const uint32_t* __restrict__ ranges, int W, int H, int Tx,
-                                                         float3 bg, const float* __restrict__ T_final,
-                                                         const uint32_t* __restrict__ n_contrib,
-                                                         const float* __restrict__ dimg, float* __restrict__ grad2d) {
-  __shared__ float4 s0[kBatch];
-  __shared__ float4 s1[kBatch];
-  __shared__ float4 s2[kBatch];
+__global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restrict__ proj, int64_t n,
+                                                            const uint32_t* __restrict__ vals,
+                                                            const uint32_t* __restrict__ ranges, int W, int H,
+                                                            int Tx, float3 bg, const float* __restrict__ T_final,
+                                                            const uint32_t* __restrict__ n_contrib,
+                                                            const float* __restrict__ dimg,
+                                                            float* __restrict__ grad2d) {
+  __shared__ BatchSmem S;
   __shared__ uint32_t s_max_last;
   const int tile = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int px, py0;
-  pixel_of(tile, Tx, lane, warp, px, py0);
+  const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
+  const int px = tile_x0 + (lane & 15), py0 = tile_y0 + 4 * warp + 2 * (lane >> 4);
   const float fx = (float)px + 0.5f;
   const uint32_t start = ranges[2 * tile], end = ranges[2 * tile + 1];
   const int64_t P = (int64_t)W * H;
-  float T[kPPT], dr[kPPT], dg[kPPT], db[kPPT], Sr[kPPT], Sg[kPPT], Sb[kPPT];
+  float fy[kPPT], T[kPPT], dr[kPPT], dg[kPPT], db[kPPT], Sr[kPPT], Sg[kPPT], Sb[kPPT];
   uint32_t last[kPPT];
   uint32_t my_max = 0;
 #pragma unroll
   for (int i = 0; i < kPPT; ++i) {
     const int py = py0 + i;
+    fy[i] = (float)py + 0.5f;
     T[i] = 1.f;
     dr[i] = dg[i] = db[i] = 0.f;
     last[i] = 0;
@@ -230,76 +270,78 @@ __global__ void __launch_bounds__(kThreads) k_render_bwd(const float* __restrict
   }
   if (threadIdx.x == 0) s_max_last = 0;
   __syncthreads();
-  my_max = __reduce_max_sync(0xffffffffu, my_max);
-  if (lane == 0) atomicMax(&s_max_last, my_max);
+  const uint32_t warp_max = __reduce_max_sync(0xffffffffu, my_max);
+  if (lane == 0) atomicMax(&s_max_last, warp_max);
   __syncthreads();
   const uint32_t max_last = s_max_last;
   // batches aligned to the list start, walked from the back
   for (int bb = (int)((max_last + kBatch - 1) / kBatch) - 1; bb >= 0; --bb) {
     const uint32_t b0 = start + (uint32_t)bb * kBatch;
+    const int cnt = (int)min((uint32_t)kBatch, min(end, start + max_last) - b0);
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < kPerThreadLoad; ++r) {
       const int slot = r * kThreads + threadIdx.x;
-      const uint32_t j = b0 + slot;
-      if (j < end) {
-        const Rec rec = gather_record(proj, n, __ldg(&vals[j]));
-        s0[slot] = rec.s0;
-        s1[slot] = rec.s1;
-        s2[slot] = rec.s2;
-      }
+      if (slot < cnt) gather_record(proj, n, __ldg(&vals[b0 + slot]), tile_x0, tile_y0, S, slot);
     }
     __syncthreads();
-    const int cnt = (int)min((uint32_t)kBatch, min(end, start + max_last) - b0);
-    for (int k = cnt - 1; k >= 0; --k) {
+    build_list(S, cnt, warp, lane);
+    const int nl = (int)S.count[warp];
+    for (int q = nl - 1; q >= 0; --q) {
+      const int k = S.list[warp][q];
       const uint32_t pos = (uint32_t)bb * kBatch + (uint32_t)k;  // list position
-      bool any = false;
-#pragma unroll
-      for (int i = 0; i < kPPT; ++i) any |= pos < last[i];
-      if (!__any_sync(0xffffffffu, any)) continue;
-      const float4 a = s0[k];
-      const float4 c = s1[k];
+      if (pos >= warp_max) continue;                             // warp-uniform
+      const float4 a = S.s0[k];
+      const float4 c = S.s1[k];
       const float dx = fx - a.x;
       const float e = __fmul_rn(a.z, dx);
-      // natural conic from the log2-scaled record
-      const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
-      float acc[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-      bool hit = false;
+      float p[kPPT];
+      bool hit[kPPT];
+      bool any = false;
 #pragma unroll
       for (int i = 0; i < kPPT; ++i) {
-        if (!(pos < last[i])) continue;
-        const float dy = ((float)(py0 + i) + 0.5f) - a.y;
-        const float p = power2(a, c, dx, e, dy);
-        if (!candidate(p, c.z)) continue;
-        const float G = fast_exp2(p);
-        const float alpha = alpha_of(c.y, G);
-        if (alpha < kAlphaMin) continue;
-        hit = true;
-        const float4 col = s2[k];
-        const float om = __fsub_rn(1.f, alpha);
-        T[i] = __fdiv_rn(T[i], om);
-        const float w = alpha * T[i];
-        acc[8] = fmaf(w, dr[i], acc[8]);
-        acc[9] = fmaf(w, dg[i], acc[9]);
-        acc[10] = fmaf(w, db[i], acc[10]);
-        const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
-                             (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) / om;
-        Sr[i] = fmaf(w, col.x, Sr[i]);
-        Sg[i] = fmaf(w, col.y, Sg[i]);
-        Sb[i] = fmaf(w, col.z, Sb[i]);
-        if (__fmul_rn(c.y, G) <= kAlphaMax) {
-          acc[2] = fmaf(dalpha, G, acc[2]);
-          const float dpow = dalpha * alpha;  // d alpha / d power = alpha
-          acc[4] = fmaf(-0.5f * dpow, dx * dx, acc[4]);
-          acc[5] = fmaf(-dpow, dx * dy, acc[5]);
-          acc[6] = fmaf(-0.5f * dpow, dy * dy, acc[6]);
-          acc[0] = fmaf(dpow, A * dx + B * dy, acc[0]);
-          acc[1] = fmaf(dpow, B * dx + C * dy, acc[1]);
+        p[i] = power2(a, c, dx, e, fy[i] - a.y);
+        hit[i] = pos < last[i] && candidate(p[i], c.z);
+        any |= hit[i];
+      }
+      if (!__any_sync(0xffffffffu, any)) continue;
+      float acc[16];
+#pragma unroll
+      for (int qq = 0; qq < 16; ++qq) acc[qq] = 0.f;
+      if (any) {
+        const float4 col = S.s2[k];
+        // natural conic from the log2-scaled record
+        const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
+#pragma unroll
+        for (int i = 0; i < kPPT; ++i) {
+          if (!hit[i]) continue;
+          const float G = fast_exp2(p[i]);
+          const float alpha = alpha_of(c.y, G);
+          if (alpha < kAlphaMin) continue;
+          const float dy = fy[i] - a.y;
+          const float om = __fsub_rn(1.f, alpha);
+          const float iom = 1.f / om;
+          T[i] = __fdiv_rn(T[i], om);
+          const float w = alpha * T[i];
+          acc[8] = fmaf(w, dr[i], acc[8]);
+          acc[9] = fmaf(w, dg[i], acc[9]);
+          acc[10] = fmaf(w, db[i], acc[10]);
+          const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
+                               (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) * iom;
+          Sr[i] = fmaf(w, col.x, Sr[i]);
+          Sg[i] = fmaf(w, col.y, Sg[i]);
+          Sb[i] = fmaf(w, col.z, Sb[i]);
+          if (__fmul_rn(c.y, G) <= kAlphaMax) {
+            acc[2] = fmaf(dalpha, G, acc[2]);
+            const float dpow = dalpha * alpha;  // d alpha / d power = alpha
+            acc[4] = fmaf(-0.5f * dpow, dx * dx, acc[4]);
+            acc[5] = fmaf(-dpow, dx * dy, acc[5]);
+            acc[6] = fmaf(-0.5f * dpow, dy * dy, acc[6]);
+            acc[0] = fmaf(dpow, A * dx + B * dy, acc[0]);
+            acc[1] = fmaf(dpow, B * dx + C * dy, acc[1]);
+          }
         }
       }
-      if (!__any_sync(0xffffffffu, hit)) continue;
       const float tot = warp_transpose_sum16(acc, lane);
       // lane 2k holds value k; k = 0..11 is the [12] record (3, 7 and 11 are padding)
       const int k_val = lane >> 1;
@@ -323,8 +365,13 @@ extern "C" gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t*
   if (proj && !gs::aligned16(proj)) return gs::set_error(GS_ERR_INVALID, "gs_render_fwd: proj must be 16-byte aligned");
   const gs::Cam k = gs::make_cam(*cam);
   const float3 b = bg ? make_float3(bg[0], bg[1], bg[2]) : make_float3(0.f, 0.f, 0.f);
-  k_render_fwd<<<k.Tx * k.Ty, kThreads, 0, gs::as_stream(stream)>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, image,
-                                                                       T_final, n_contrib, work);
+  cudaStream_t st = gs::as_stream(stream);
+  if (work)
+    k_render_fwd<true><<<k.Tx * k.Ty, kThreads, 0, st>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, image, T_final,
+                                                          n_contrib, work);
+  else
+    k_render_fwd<false><<<k.Tx * k.Ty, kThreads, 0, st>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, image, T_final,
+                                                           n_contrib, work);
   return gs::check_launch("gs_render_fwd");
 }
 
