@@ -78,11 +78,21 @@ def test_project_parity(cfg, n, view):
     assert (np.abs(rg[both] - pr["radius"][both]) <= 1).all()
     vis = ok & (pr["radius"] > 0)
     assert vis.sum() > 0
-    # continuous outputs, relative to their own scale
-    for name, a, b, rel in [("u", g[0, vis, 0], pr["uvzo"][vis, 0], 1e-5), ("v", g[0, vis, 1], pr["uvzo"][vis, 1], 1e-5),
-                            ("z", g[0, vis, 2], pr["uvzo"][vis, 2], 1e-6), ("o", g[0, vis, 3], pr["uvzo"][vis, 3], 1e-6)]:
+    # continuous outputs.  The camera-space coordinates come from fp32 sums R mu + t whose
+    # terms can cancel (a mean far to the side, barely in front of the near plane), so the
+    # bound on u, v, z scales with each sum's condition number sum|terms| / |result|.
+    R = cam.R.astype(np.float64)
+    mu = P[0, :, :3].astype(np.float64)
+    terms = np.abs(mu @ R.T) + np.abs(cam.t.astype(np.float64))
+    pc = mu @ R.T + cam.t.astype(np.float64)
+    cond = terms / np.maximum(np.abs(pc), 1e-12)
+    cu = 1.0 + cond[vis, 0] + cond[vis, 2]
+    cv = 1.0 + cond[vis, 1] + cond[vis, 2]
+    for name, a, b, rel in [("u", g[0, vis, 0], pr["uvzo"][vis, 0], 1e-6 * cu), ("v", g[0, vis, 1], pr["uvzo"][vis, 1], 1e-6 * cv),
+                            ("z", g[0, vis, 2], pr["uvzo"][vis, 2], 1e-6 * cond[vis, 2]),
+                            ("o", g[0, vis, 3], pr["uvzo"][vis, 3], 1e-6)]:
         err = np.abs(a - b) / np.maximum(np.abs(b), 1.0)
-        assert err.max() <= rel, (name, err.max())
+        assert (err <= rel).all(), (name, err.max())
     # conic: error relative to the largest entry of the same Gaussian
     scale = np.abs(pr["conic"][vis]).max(axis=1, keepdims=True)
     cerr = np.abs(g[1, vis, :3] - pr["conic"][vis]) / scale
@@ -319,9 +329,11 @@ def test_sparse_adam_parity_and_skip():
     for got, want in zip((tp, tg, tm, tv), ref):
         bad = allclose_grad(host(got), want, RTOL, ATOL)
         assert bad.sum() == 0
-    # the update itself (p_new - p_old) to the same tolerance
-    bad = allclose_grad(host(tp).astype(np.float64) - P, ref[0] - P, RTOL, 1e-9)
-    assert bad.sum() == 0
+    # the update itself (p_new - p_old): relative 1e-3, plus the fp32 rounding of p_new
+    pn = host(tp).astype(np.float64)
+    d_gpu, d_ref = pn - P, ref[0] - P
+    tol = RTOL * np.abs(d_ref) + 2.0 ** -22 * np.maximum(np.abs(P), np.abs(pn))
+    assert (np.abs(d_gpu - d_ref) <= tol).all()
     untouched = np.setdiff1d(np.arange(n), idx)
     assert (host(tp)[:, untouched] == P[:, untouched]).all()
     assert (host(tg)[:, untouched] == G[:, untouched]).all()
