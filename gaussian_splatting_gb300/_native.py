@@ -18,7 +18,7 @@ _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ER
 
 # every symbol include/gs.h declares
 EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_bin_sort_workspace_size", "gs_bin_sort",
-           "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_render_bwd", "gs_project_bwd",
+           "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
@@ -69,6 +69,7 @@ def load() -> C.CDLL:
         "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
         "gs_loss_workspace_size": ([i32, i32], sz),
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
+        "gs_loss_noalloc": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp], i32),
         "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
         "gs_project_bwd": ([vp, i64, cp, vp, vp, vp, vp], i32),
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
@@ -156,6 +157,13 @@ def gs_loss(image, target, width, height, w_l1, w_ssim, scale, loss_dev, accumul
     _check(load().gs_loss(_ptr(image), _ptr(target), width, height, w_l1, w_ssim, scale, _ptr(loss_dev),
                           1 if accumulate else 0, _ptr(dL_dimage), _ptr(workspace), workspace_bytes,
                           _stream(stream)), "gs_loss")
+
+
+def gs_loss_noalloc(image, target, width, height, w_l1, w_ssim, scale, loss_dev, accumulate, dL_dimage,
+                    stream=None):
+    """gs_loss without a workspace (partial sums in a fixed array inside the library)."""
+    _check(load().gs_loss_noalloc(_ptr(image), _ptr(target), width, height, w_l1, w_ssim, scale, _ptr(loss_dev),
+                                  1 if accumulate else 0, _ptr(dL_dimage), _stream(stream)), "gs_loss_noalloc")
 
 
 def gs_render_bwd(proj, n, vals, ranges, cam, bg, T_final, n_contrib, dL_dimage, grad2d, stream=None):

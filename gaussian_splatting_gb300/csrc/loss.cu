@@ -9,6 +9,7 @@
 // per-CTA partial sums of SSIM and |x - y| goes to global scratch; a last one-CTA kernel
 // reduces them in a fixed order.
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -269,4 +270,77 @@ extern "C" gs_status gs_loss(const float* image, const float* target, int width,
   k_loss_final<<<1, 256, 0, st>>>(partials, loss_blocks(width, height), w_l1, w_ssim, scale, 1.0 / n, loss_dev,
                                   accumulate);
   return gs::check_launch("gs_loss final");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant of gs_loss.
+//
+// gs_loss needs a small caller workspace for its per-block partial sums.  Some callers cannot
+// hand one out: code whose device memory is owned by another allocator under a fixed budget,
+// or code that must not call cudaMalloc / cudaFree because those calls can synchronise the
+// whole device.  gs_loss_noalloc keeps the partial sums in a fixed array that lives in this
+// library's own device image instead, so it needs no workspace and allocates nothing.
+//
+// The array holds at most kNoAllocMaxBlocks partial-sum pairs (512 KB; every GPU that loads
+// the library keeps it until the process exits): images with
+// ceil(W/32) * ceil(H/32) * 3 <= 65536, e.g. up to 4096 x 4096.  Larger images are rejected.
+// All calls share the one array: two calls that overlap on the GPU (different streams, no
+// ordering between them) race on it.  Every block of a call rewrites its own pair before the
+// final reduction reads it, so nothing has to be cleared between calls.
+namespace {
+
+constexpr int64_t kNoAllocMaxBlocks = 65536;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_loss_scratch[2 * kNoAllocMaxBlocks];
+
+std::mutex g_scratch_mu;
+float* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_loss_scratch on the current device, looked up once per device (host
+// code cannot use the symbol itself: in host code it names a host-side stand-in).
+gs_status scratch_address(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return gs::set_error(GS_ERR_INVALID, "gs_loss_noalloc: device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_loss_scratch);
+    if (e != cudaSuccess || !p)
+      return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = reinterpret_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return GS_OK;
+}
+
+}  // namespace
+
+extern "C" gs_status gs_loss_noalloc(const float* image, const float* target, int width, int height, float w_l1,
+                                     float w_ssim, float scale, float* loss_dev, int accumulate, float* dL_dimage,
+                                     void* stream) {
+  if (width <= 0 || height <= 0 || width > 32768 || height > 32768)
+    return gs::set_error(GS_ERR_INVALID, "gs_loss_noalloc: bad image size %d x %d", width, height);
+  if (!image || !target || !loss_dev || !dL_dimage) return gs::set_error(GS_ERR_INVALID, "gs_loss_noalloc: NULL pointer");
+  const int64_t nblk = loss_blocks(width, height);
+  if (nblk > kNoAllocMaxBlocks)
+    return gs::set_error(GS_ERR_INVALID,
+                         "gs_loss_noalloc: %d x %d needs %lld partial sums, the built-in scratch holds %lld "
+                         "(ceil(W/32) * ceil(H/32) * 3 must be <= %lld); use gs_loss with a workspace",
+                         width, height, (long long)nblk, (long long)kNoAllocMaxBlocks, (long long)kNoAllocMaxBlocks);
+  float* partials = nullptr;
+  if (gs_status s = scratch_address(&partials)) return s;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
+  if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: %s", cudaGetErrorString(attr));
+  cudaStream_t st = gs::as_stream(stream);
+  const double n = 3.0 * (double)width * (double)height;
+  dim3 grid((width + kOut - 1) / kOut, (height + kOut - 1) / kOut, 3);
+  k_loss_fused<<<grid, kThreads, sizeof(LossSmem), st>>>(image, target, width, height, make_window(), w_l1, w_ssim,
+                                                         scale, (float)(1.0 / n), dL_dimage, partials);
+  if (gs_status s = gs::check_launch("gs_loss_noalloc")) return s;
+  k_loss_final<<<1, 256, 0, st>>>(partials, nblk, w_l1, w_ssim, scale, 1.0 / n, loss_dev, accumulate);
+  return gs::check_launch("gs_loss_noalloc final");
 }

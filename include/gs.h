@@ -142,6 +142,26 @@ gs_status gs_loss(const float* image, const float* target, int width, int height
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_loss_noalloc -- gs_loss without a workspace.  The paper has no counterpart for this
+ * entry point: it is a calling convention of this library, not a step of the method.
+ * For callers that cannot provide device memory: their memory is owned by another
+ * allocator under a fixed budget, or they must not call cudaMalloc / cudaFree, which can
+ * synchronise the whole device.  The partial sums live in a fixed array inside the
+ * library's device image (512 KB, held by every GPU that loads the library until the
+ * process exits), so the call allocates nothing.  Same arguments and results as gs_loss.
+ *  - Limit: ceil(width/32) * ceil(height/32) * 3 <= 65536 (e.g. up to 4096 x 4096);
+ *    larger images return GS_ERR_INVALID with the limit in the message.
+ *  - The first call on a device looks up the array's device address once (a host-side
+ *    runtime query); make that first call before any stream capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (on different
+ *    streams with no ordering between them) race and give wrong results.  Each call
+ *    rewrites the parts it reads, so nothing needs clearing between calls.
+ */
+gs_status gs_loss_noalloc(const float* image, const float* target, int width, int height, float w_l1,
+                          float w_ssim, float scale, float* loss_dev, int accumulate, float* dL_dimage,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------
  * gs_render_bwd -- reverse-order backward of gs_render_fwd ("反向传播").  Walks each
  * pixel's list back to front from n_contrib, recovering T by T / (1 - alpha), and
  * writes per-Gaussian screen-space gradients into grad2d [n][12] (the call clears
