@@ -37,11 +37,13 @@ namespace {
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 2;
 constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
+constexpr int kWin = 4096;                             // output slots per write window
+constexpr int kWinPer = kWin / kScanThreads;
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortItems = 16;
-constexpr int kSortTile = kSortThreads * kSortItems;  // keys per radix tile
+constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N is modest)
+constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
 constexpr int kDepthPasses = 4;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // histogram / counter slots
@@ -69,7 +71,11 @@ struct Workspace {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-__host__ __device__ inline int64_t sort_tiles(int64_t m) { return (m + kSortTile - 1) / kSortTile; }
+template <int ITEMS>
+__host__ __device__ inline int64_t sort_tiles(int64_t m) {
+  constexpr int kTile = kSortThreads * ITEMS;
+  return (m + kTile - 1) / kTile;
+}
 
 int tile_bits(int64_t T) {
   int b = 0;
@@ -96,8 +102,8 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses) {
   char* di0 = take(sizeof(uint32_t) * (size_t)n);
   char* di1 = take(sizeof(uint32_t) * (size_t)n);
   char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
-  char* lbd = take(sizeof(uint32_t) * 256 * kDepthPasses * (size_t)sort_tiles(n));
-  char* lbt = take(sizeof(uint32_t) * 256 * (size_t)tpasses * (size_t)sort_tiles(cap));
+  char* lbd = take(sizeof(uint32_t) * 256 * kDepthPasses * (size_t)sort_tiles<kDepthItems>(n));
+  char* lbt = take(sizeof(uint32_t) * 256 * (size_t)tpasses * (size_t)sort_tiles<kTileItems>(cap));
   char* sm = take(sizeof(uint32_t) * kSmWords);
   if (w) {
     w->tkey[0] = reinterpret_cast<uint32_t*>(tk0);
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ pr
   const float4* q1 = q0 + n;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t w = gtid; w < (int64_t)kDepthPasses * sort_tiles(n) * 256; w += stride) lb_depth[w] = 0u;
+  for (int64_t w = gtid; w < (int64_t)kDepthPasses * sort_tiles<kDepthItems>(n) * 256; w += stride) lb_depth[w] = 0u;
   for (int64_t w = gtid; w < lb_tile_words; w += stride) lb_tile[w] = 0u;
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
   __syncthreads();
@@ -192,10 +198,10 @@ __global__ void k_digit_scan(uint32_t* small, int slot0, int nslots, const int64
 }
 
 // ------------------------------------------------------------------ one stable radix pass
-template <typename K>
+template <int ITEMS>
 struct SortSmem {
-  K keys[kSortTile];
-  uint32_t vals[kSortTile];
+  uint32_t keys[kSortThreads * ITEMS];
+  uint32_t vals[kSortThreads * ITEMS];
   uint32_t whist[kSortWarps][256];
   uint32_t tstart[256];
   uint32_t gbase[256];
@@ -203,23 +209,21 @@ struct SortSmem {
   uint32_t tile;
 };
 
-template <typename K>
-__device__ __forceinline__ uint32_t digit_of(K key, int shift) {
-  return (uint32_t)(key >> shift) & 255u;
-}
-
-// n_host >= 0: sort n_host keys; otherwise min(count[0], cap) keys.
-template <typename K>
-__global__ void __launch_bounds__(kSortThreads, 3) k_onesweep(const K* __restrict__ kin, const uint32_t* __restrict__ vin,
-                                                            K* __restrict__ kout, uint32_t* __restrict__ vout,
-                                                            int64_t n_host, int64_t cap, int shift, int slot,
-                                                            uint32_t* small, uint32_t* lookback_pass, int64_t* count,
-                                                            int64_t limit, int drop_publish) {
+// Stable pass over 32-bit keys (8-bit digit at `shift`).  n_host >= 0: sort n_host keys;
+// otherwise min(count[0], cap) keys.
+template <int ITEMS>
+__global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __restrict__ kin,
+                                                               const uint32_t* __restrict__ vin,
+                                                               uint32_t* __restrict__ kout, uint32_t* __restrict__ vout,
+                                                               int64_t n_host, int64_t cap, int shift, int slot,
+                                                               uint32_t* small, uint32_t* lookback_pass,
+                                                               int64_t* count, int64_t limit, int drop_publish) {
+  constexpr int kTile = kSortThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmem<K>& S = *reinterpret_cast<SortSmem<K>*>(smem_raw);
+  SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
   if (count[1] != 0) return;
   const int64_t M = n_host >= 0 ? n_host : min(count[0], cap);
-  const int64_t ntiles = sort_tiles(M);
+  const int64_t ntiles = sort_tiles<ITEMS>(M);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const uint32_t* digit_base = small + kSmDigitBase + slot * 256;
@@ -229,30 +233,30 @@ __global__ void __launch_bounds__(kSortThreads, 3) k_onesweep(const K* __restric
     __syncthreads();
     const int64_t tile = S.tile;
     if (tile >= ntiles) break;
-    const int64_t base = tile * kSortTile;
-    const int nvalid = (int)min((int64_t)kSortTile, M - base);
+    const int64_t base = tile * kTile;
+    const int nvalid = (int)min((int64_t)kTile, M - base);
+    const bool full = nvalid == kTile;
     // ---- load (warp-striped) and rank stably within the warp
-    K k[kSortItems];
-    uint32_t v[kSortItems], rank[kSortItems];
-    const int wbase = warp * (kSortItems * 32);
+    uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
+    const int wbase = warp * (ITEMS * 32);
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       const int li = wbase + i * 32 + lane;
-      if (li < nvalid) {
+      if (full || li < nvalid) {
         k[i] = kin[base + li];
         v[i] = vin[base + li];
       } else {
-        k[i] = (K)~(K)0;
+        k[i] = 0xFFFFFFFFu;
         v[i] = 0u;
       }
     }
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       const int li = wbase + i * 32 + lane;
-      const bool valid = li < nvalid;
-      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      const bool valid = full || li < nvalid;
+      const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
       if (valid) {
-        const uint32_t d = digit_of(k[i], shift);
+        const uint32_t d = (k[i] >> shift) & 255u;
         const uint32_t peers = __match_any_sync(vmask, d);
         const uint32_t before = S.whist[warp][d];
         __syncwarp(vmask);
@@ -307,10 +311,10 @@ __global__ void __launch_bounds__(kSortThreads, 3) k_onesweep(const K* __restric
     __syncthreads();
     // ---- scatter into shared memory in tile order
 #pragma unroll
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       const int li = wbase + i * 32 + lane;
-      if (li < nvalid) {
-        const uint32_t d = digit_of(k[i], shift);
+      if (full || li < nvalid) {
+        const uint32_t d = (k[i] >> shift) & 255u;
         const uint32_t pos = S.tstart[d] + S.whist[warp][d] + rank[i];
         S.keys[pos] = k[i];
         S.vals[pos] = v[i];
@@ -319,11 +323,11 @@ __global__ void __launch_bounds__(kSortThreads, 3) k_onesweep(const K* __restric
     __syncthreads();
     // ---- digit-contiguous global writes
 #pragma unroll 4
-    for (int i = 0; i < kSortItems; ++i) {
+    for (int i = 0; i < ITEMS; ++i) {
       const int p = i * kSortThreads + tid;
       if (p < nvalid) {
-        const K key = S.keys[p];
-        const uint32_t d = digit_of(key, shift);
+        const uint32_t key = S.keys[p];
+        const uint32_t d = (key >> shift) & 255u;
         const uint32_t g = S.gbase[d] + (uint32_t)p - S.tstart[d];
         if (g < (uint64_t)M) {  // always true unless a look-back wait gave up (status bit set)
           kout[g] = key;
@@ -348,6 +352,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
   __shared__ uint32_t s_rect[kScanChunk];    // x0 | y0 << 16
   __shared__ uint32_t s_width[kScanChunk];   // rectangle width in tiles
   __shared__ uint32_t s_gauss[kScanChunk];
+  __shared__ float s_rcpw[kScanChunk];        // 1 / width
+  __shared__ uint32_t s_owner[kWin];          // owner of each output slot in the window
   __shared__ uint32_t s_hist[kMaxTilePasses][256];
   __shared__ uint32_t s_warp[kScanThreads / 32];
   __shared__ unsigned long long s_prefix;
@@ -383,6 +389,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
     s_items[li] = cnt;
     s_rect[li] = rect;
     s_width[li] = width;
+    s_rcpw[li] = 1.0f / (float)width;
     s_gauss[li] = g;
   }
   __syncthreads();
@@ -440,30 +447,66 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
     }
   }
   __syncthreads();
-  // cooperative, coalesced write of this chunk's instances
+  // Cooperative, coalesced write of this chunk's instances, one window of kWin output slots
+  // at a time: every item whose run meets the window marks its first slot there with its
+  // index + 1, and an inclusive max-scan over the window turns the marks into the owner of
+  // every slot (items are in offset order).
   const int64_t out0 = (int64_t)s_prefix;
-  const int nvalid = (int)min((int64_t)kScanChunk, n - base);
-  for (uint32_t p = tid; p < total; p += kScanThreads) {
-    // last item whose exclusive offset <= p
-    int lo = 0, hi = nvalid - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_items[mid] <= p) lo = mid; else hi = mid - 1;
+  for (uint32_t w0 = 0; w0 < total; w0 += kWin) {
+    const uint32_t wn = min((uint32_t)kWin, total - w0);
+    for (int i = tid; i < kWin; i += kScanThreads) s_owner[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+      const int li = tid * kScanItems + j;
+      const uint32_t off = s_items[li], c = v[j];
+      if (c > 0 && off < w0 + wn && off + c > w0) s_owner[max(off, w0) - w0] = (uint32_t)li + 1u;
     }
-    const uint32_t j = p - s_items[lo];
-    const uint32_t w = s_width[lo];
-    const uint32_t rect = s_rect[lo];
-    const uint32_t row = j / w;
-    const uint32_t tx = (rect & 0xffffu) + (j - row * w), ty = (rect >> 16) + row;
-    const uint32_t tile = ty * (uint32_t)k.Tx + tx;
-    const int64_t o = out0 + p;
-    if (o < cap) {
-      tkey[o] = tile;
-      tval[o] = s_gauss[lo];
+    __syncthreads();
+    {  // inclusive max-scan of s_owner[0 .. kWin): kWinPer consecutive slots per thread
+      uint32_t run = 0;
+#pragma unroll
+      for (int e = 0; e < kWinPer; ++e) run = max(run, s_owner[tid * kWinPer + e]);
+      uint32_t incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = max(incl, y);
+      }
+      if (lane == 31) s_warp[warp] = incl;
+      __syncthreads();
+      uint32_t carry = 0;
+      for (int w = 0; w < warp; ++w) carry = max(carry, s_warp[w]);
+      uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) prev = 0u;
+      run = max(carry, prev);
+#pragma unroll
+      for (int e = 0; e < kWinPer; ++e) {
+        run = max(run, s_owner[tid * kWinPer + e]);
+        s_owner[tid * kWinPer + e] = run;
+      }
     }
-    for (int q = 0; q < tpasses; ++q) atomicAdd(&s_hist[q][(tile >> (8 * q)) & 255u], 1u);
+    __syncthreads();
+    for (uint32_t q = tid; q < wn; q += kScanThreads) {
+      const uint32_t li = s_owner[q] - 1u;
+      const uint32_t j = w0 + q - s_items[li];  // index of the tile inside the item's rectangle
+      const uint32_t w = s_width[li];
+      // j / w from a float estimate, corrected once (|error| <= 1 for j < 2^24)
+      uint32_t row = (uint32_t)__fmul_rz((float)j, s_rcpw[li]);
+      int rem = (int)j - (int)(row * w);
+      if (rem < 0) { --row; rem += (int)w; }
+      if (rem >= (int)w) { ++row; rem -= (int)w; }
+      const uint32_t rect = s_rect[li];
+      const uint32_t tile = ((rect >> 16) + row) * (uint32_t)k.Tx + (rect & 0xffffu) + (uint32_t)rem;
+      const int64_t o = out0 + w0 + q;
+      if (o < cap) {
+        tkey[o] = tile;
+        tval[o] = s_gauss[li];
+      }
+      for (int pp = 0; pp < tpasses; ++pp) atomicAdd(&s_hist[pp][(tile >> (8 * pp)) & 255u], 1u);
+    }
+    __syncthreads();
   }
-  __syncthreads();
   for (int i = tid; i < tpasses * 256; i += kScanThreads) {
     const uint32_t c = (&s_hist[0][0])[i];
     if (c) atomicAdd(&small[kSmHist + kDepthPasses * 256 + i], c);
@@ -488,16 +531,16 @@ __global__ void __launch_bounds__(256) k_finalize(const float* __restrict__ proj
   }
 }
 
-template <typename K>
+template <int ITEMS>
 int sort_blocks_per_sm() {
   static int cached = -1;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (cached < 0) {
     int b = 0;
-    cudaFuncSetAttribute(k_onesweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SortSmem<K>));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<K>, kSortThreads, sizeof(SortSmem<K>)) !=
-            cudaSuccess ||
+    const int bytes = (int)sizeof(SortSmem<ITEMS>);
+    cudaFuncSetAttribute(k_onesweep<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS>, kSortThreads, bytes) != cudaSuccess ||
         b < 1)
       b = 1;
     cached = b;
@@ -548,15 +591,15 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
       return gs::check_launch("gs_bin_sort memset");
     const int sms = gs::num_sms();
     // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys
-    const int64_t lb_tile_words = (int64_t)tpasses * sort_tiles(capacity) * 256;
+    const int64_t lb_tile_words = (int64_t)tpasses * sort_tiles<kTileItems>(capacity) * 256;
     k_depth_init<<<sms * 4, 256, 0, st>>>(proj, n, w.dkey[0], w.didx[0], w.small, w.lb_depth, w.lb_tile,
                                           lb_tile_words);
     k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
-    const int grid32 = sms * sort_blocks_per_sm<uint32_t>();
+    const int grid_d = (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems>(), sort_tiles<kDepthItems>(n));
     for (int p = 0; p < kDepthPasses; ++p) {
-      k_onesweep<uint32_t><<<grid32, kSortThreads, sizeof(SortSmem<uint32_t>), st>>>(
+      k_onesweep<kDepthItems><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
           w.dkey[p & 1], w.didx[p & 1], w.dkey[(p + 1) & 1], w.didx[(p + 1) & 1], n, n, 8 * p, p, w.small,
-          w.lb_depth + (size_t)p * sort_tiles(n) * 256, count, limit, p == 0 ? drop : 0);
+          w.lb_depth + (size_t)p * sort_tiles<kDepthItems>(n) * 256, count, limit, p == 0 ? drop : 0);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. (tile, index) pairs in depth order, with their tile-digit histograms
@@ -565,10 +608,11 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
     // 3. stable sort of the pairs by tile id
     k_digit_scan<<<1, 256, 0, st>>>(w.small, kDepthPasses, tpasses, count);
+    const int grid_t = sms * sort_blocks_per_sm<kTileItems>();
     for (int p = 0; p < tpasses; ++p) {
-      k_onesweep<uint32_t><<<grid32, kSortThreads, sizeof(SortSmem<uint32_t>), st>>>(
+      k_onesweep<kTileItems><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
           w.tkey[p & 1], w.tval[p & 1], w.tkey[(p + 1) & 1], w.tval[(p + 1) & 1], -1, capacity, 8 * p,
-          kDepthPasses + p, w.small, w.lb_tile + (size_t)p * sort_tiles(capacity) * 256, count, limit, 0);
+          kDepthPasses + p, w.small, w.lb_tile + (size_t)p * sort_tiles<kTileItems>(capacity) * 256, count, limit, 0);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
     k_finalize<<<sms * 8, 256, 0, st>>>(proj, w.tkey[tpasses & 1], w.tval[tpasses & 1], capacity, keys, vals, ranges,

@@ -37,7 +37,7 @@ constexpr float kTMin = 1e-4f;
 
 struct __align__(16) BatchSmem {
   float4 s0[kBatch];        // (u, v, a2, b2)
-  float4 s1[kBatch];        // (c2, opacity, p_min, Gaussian index bits)
+  float4 s1[kBatch];        // (c2, opacity, p_min / 2, Gaussian index bits)
   float4 s2[kBatch];        // (r, g, b, 0)
   uint32_t mask[kBatch];    // warp blocks the Gaussian can reach
   uint8_t list[kWarps][kBatch];
@@ -54,7 +54,7 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
   float lg;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(q0.w * 255.0f));
   S.s0[slot] = make_float4(q0.x, q0.y, -0.5f * kLog2e * q1.x, -kLog2e * q1.y);
-  S.s1[slot] = make_float4(-0.5f * kLog2e * q1.z, q0.w, -lg, __uint_as_float(g));
+  S.s1[slot] = make_float4(-0.5f * kLog2e * q1.z, q0.w, -0.5f * lg, __uint_as_float(g));
   S.s2[slot] = make_float4(q2.x, q2.y, q2.z, 0.f);
   // bounding box of {d : d^T conic d <= K}, K = 2 ln(255 opacity): half-widths sqrt(K Sigma_xx),
   // sqrt(K Sigma_yy) with Sigma = conic^-1; enlarged so rounding never drops a reachable pair
@@ -92,19 +92,29 @@ __device__ __forceinline__ void build_list(BatchSmem& S, int cnt, int warp, int 
   __syncwarp();
 }
 
-// p at pixel-centre offset (dx, dy), with e = a2 * dx shared by a thread's column.  Explicit
-// roundings: the forward and backward kernels must evaluate identical bits.
-__device__ __forceinline__ float power2(const float4& s0, const float4& s1, float dx, float e, float dy) {
-  const float t = fmaf(s0.w, dy, e);
-  return fmaf(__fmul_rn(s1.x, dy), dy, __fmul_rn(dx, t));
+// Per-Gaussian, per-column part of p = a2 dx^2 + b2 dx dy + c2 dy^2: f0 = a2 dx^2, g = b2 dx.
+struct Col {
+  float f0, g;
+};
+__device__ __forceinline__ Col column(const float4& s0, float dx) {
+  return Col{__fmul_rn(__fmul_rn(s0.z, dx), dx), __fmul_rn(s0.w, dx)};
+}
+// p at row offset dy: dy (c2 dy + g) + f0.  Explicit roundings: the forward and backward
+// kernels must evaluate identical bits.
+__device__ __forceinline__ float power2(const Col& col, float c2, float dy) {
+  return fmaf(dy, fmaf(c2, dy, col.g), col.f0);
 }
 
 __device__ __forceinline__ float alpha_of(float opacity, float G) {
   return fminf(kAlphaMax, __fmul_rn(opacity, G));
 }
 
-// p passes the skip tests (power <= 0 and alpha >= 1/255 before the clamp)
-__device__ __forceinline__ bool candidate(float p, float pmin) { return p >= pmin && !(p > 0.f); }
+// p passes the skip tests: p_min <= p <= 0 (power <= 0, alpha >= 1/255 before the clamp),
+// written as |p - p_min/2| <= -p_min/2 (hm = p_min / 2)
+__device__ __forceinline__ bool candidate(float p, float hm) { return fabsf(__fsub_rn(p, hm)) <= -hm; }
+
+// A finished pixel's row coordinate is moved here: p becomes about -1e34, never a candidate.
+constexpr float kParkedRow = 1e17f;
 
 template <bool kCount>
 __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restrict__ proj, int64_t n,
@@ -134,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
     stop[i] = end - start;  // entries evaluated if the pixel never saturates
     done[i] = !(px < W && py0 + i < H);
   }
+#pragma unroll
+  for (int i = 0; i < kPPT; ++i)
+    if (done[i]) fy[i] = kParkedRow;
   bool warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
   for (uint32_t b0 = start; b0 < end; b0 += kBatch) {
     if (__syncthreads_count(warp_done) == kThreads) break;
@@ -146,23 +159,22 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
     __syncthreads();
     build_list(S, cnt, warp, lane);
     const int nl = (int)S.count[warp];
-    for (int q = 0; q < nl && !warp_done; ++q) {
-      const int k = S.list[warp][q];
-      const float4 a = S.s0[k];
-      const float4 c = S.s1[k];
-      const float dx = fx - a.x;
-      const float e = __fmul_rn(a.z, dx);
-      float p[kPPT];
-      bool hit[kPPT];
-      bool any = false;
-#pragma unroll
-      for (int i = 0; i < kPPT; ++i) {
-        p[i] = power2(a, c, dx, e, fy[i] - a.y);
-        hit[i] = !done[i] && candidate(p[i], c.z);
-        any |= hit[i];
-      }
+    for (int q0 = 0; q0 < nl && !warp_done; q0 += 16) {
+      const int qend = min(nl, q0 + 16);
       bool ended = false;
-      if (any) {
+      for (int q = q0; q < qend; ++q) {
+        const int k = S.list[warp][q];
+        const float4 a = S.s0[k];
+        const float4 c = S.s1[k];
+        const Col cl = column(a, fx - a.x);
+        float p[kPPT];
+        bool hit[kPPT];
+#pragma unroll
+        for (int i = 0; i < kPPT; ++i) {
+          p[i] = power2(cl, c.x, fy[i] - a.y);
+          hit[i] = candidate(p[i], c.z);
+        }
+        if (!(hit[0] || hit[1])) continue;
         const float4 col = S.s2[k];
         const uint32_t pos = b0 - start + (uint32_t)k;
 #pragma unroll
@@ -173,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
           const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
           if (Tn < kTMin) {
             done[i] = true;
+            fy[i] = kParkedRow;
             stop[i] = pos + 1u;
             ended = true;
             continue;
@@ -209,13 +222,14 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
   }
 }
 
-// Sum of 16 per-lane values over the warp by a transposed butterfly: afterwards lanes 2k and
-// 2k+1 hold the warp total of value k.  16 shuffles instead of 16 * 5.
-__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) {
+// Warp sums of 8 per-lane values by a transposed butterfly: three halving levels (4 + 2 + 1
+// shuffles) leave lane L holding value k = L >> 2 summed over 8 lanes; two plain levels
+// finish it.  Afterwards lanes 4k .. 4k+3 hold the warp total of value k.
+__device__ __forceinline__ float warp_transpose_sum8(float (&v)[8], int lane) {
 #pragma unroll
-  for (int level = 0; level < 4; ++level) {
-    const int off = 16 >> level;  // 16, 8, 4, 2
-    const int half = 8 >> level;  // values kept: 8, 4, 2, 1
+  for (int level = 0; level < 3; ++level) {
+    const int off = 16 >> level;  // 16, 8, 4
+    const int half = 4 >> level;  // values kept: 4, 2, 1
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -225,7 +239,20 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) 
       v[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
     }
   }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+  float t = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return t + __shfl_xor_sync(0xffffffffu, t, 1);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restrict__ proj, int64_t n,
@@ -294,20 +321,19 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
       const float4 a = S.s0[k];
       const float4 c = S.s1[k];
       const float dx = fx - a.x;
-      const float e = __fmul_rn(a.z, dx);
+      const Col cl = column(a, dx);
       float p[kPPT];
       bool hit[kPPT];
-      bool any = false;
 #pragma unroll
       for (int i = 0; i < kPPT; ++i) {
-        p[i] = power2(a, c, dx, e, fy[i] - a.y);
+        p[i] = power2(cl, c.x, fy[i] - a.y);
         hit[i] = pos < last[i] && candidate(p[i], c.z);
-        any |= hit[i];
       }
+      const bool any = hit[0] || hit[1];
       if (!__any_sync(0xffffffffu, any)) continue;
-      float acc[16];
-#pragma unroll
-      for (int qq = 0; qq < 16; ++qq) acc[qq] = 0.f;
+      // acc: du, dv, dopacity, dA, dB, dC, dr, dg (transposed); db separately
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float acc_b = 0.f;
       if (any) {
         const float4 col = S.s2[k];
         // natural conic from the log2-scaled record
@@ -319,13 +345,12 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
           const float alpha = alpha_of(c.y, G);
           if (alpha < kAlphaMin) continue;
           const float dy = fy[i] - a.y;
-          const float om = __fsub_rn(1.f, alpha);
-          const float iom = 1.f / om;
-          T[i] = __fdiv_rn(T[i], om);
+          const float iom = rcp_approx(__fsub_rn(1.f, alpha));
+          T[i] = T[i] * iom;
           const float w = alpha * T[i];
-          acc[8] = fmaf(w, dr[i], acc[8]);
-          acc[9] = fmaf(w, dg[i], acc[9]);
-          acc[10] = fmaf(w, db[i], acc[10]);
+          acc[6] = fmaf(w, dr[i], acc[6]);
+          acc[7] = fmaf(w, dg[i], acc[7]);
+          acc_b = fmaf(w, db[i], acc_b);
           const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
                                (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) * iom;
           Sr[i] = fmaf(w, col.x, Sr[i]);
@@ -334,20 +359,24 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
           if (__fmul_rn(c.y, G) <= kAlphaMax) {
             acc[2] = fmaf(dalpha, G, acc[2]);
             const float dpow = dalpha * alpha;  // d alpha / d power = alpha
-            acc[4] = fmaf(-0.5f * dpow, dx * dx, acc[4]);
-            acc[5] = fmaf(-dpow, dx * dy, acc[5]);
-            acc[6] = fmaf(-0.5f * dpow, dy * dy, acc[6]);
+            acc[3] = fmaf(-0.5f * dpow, dx * dx, acc[3]);
+            acc[4] = fmaf(-dpow, dx * dy, acc[4]);
+            acc[5] = fmaf(-0.5f * dpow, dy * dy, acc[5]);
             acc[0] = fmaf(dpow, A * dx + B * dy, acc[0]);
             acc[1] = fmaf(dpow, B * dx + C * dy, acc[1]);
           }
         }
       }
-      const float tot = warp_transpose_sum16(acc, lane);
-      // lane 2k holds value k; k = 0..11 is the [12] record (3, 7 and 11 are padding)
-      const int k_val = lane >> 1;
-      if ((lane & 1) == 0 && k_val < 12 && (k_val & 3) != 3) {
-        const uint32_t g = __float_as_uint(c.w);
-        atomicAdd(grad2d + 12 * (int64_t)g + k_val, tot);
+      const float tot = warp_transpose_sum8(acc, lane);
+      const float tot_b = warp_sum(acc_b);
+      // lanes 4k hold value k of (du, dv, dopacity, dA, dB, dC, dr, dg); lane 1 adds db
+      const uint32_t g = __float_as_uint(c.w);
+      float* rec = grad2d + 12 * (int64_t)g;
+      if ((lane & 3) == 0) {
+        const int kv = lane >> 2;
+        atomicAdd(rec + kv + (kv >= 3 ? 1 : 0) + (kv >= 6 ? 1 : 0), tot);
+      } else if (lane == 1) {
+        atomicAdd(rec + 10, tot_b);
       }
     }
   }
