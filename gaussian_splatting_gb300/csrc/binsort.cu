@@ -13,19 +13,22 @@
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   k_depth_init  depth keys (0xFFFFFFFF for culled Gaussians) + their digit histograms;
-//                 clears the look-back state of every pass.
-//   k_digit_scan  exclusive digit offsets per pass.
-//   k_onesweep    one stable radix pass of 8 bits: persistent CTAs take 4096-key tiles in
+//                 clears the look-back state and the tile-count grid.
+//   k_digit_scan  exclusive digit offsets of the depth passes.
+//   k_onesweep    one stable radix pass of 8 bits: persistent CTAs take tiles of keys in
 //                 order from an atomic counter, rank keys within the tile in shared memory
 //                 (warp match-any ranking), get the tile's global digit offsets by
 //                 decoupled look-back and scatter through shared memory so the global
-//                 writes are digit-contiguous.
-//   k_scan_dup    single-pass scan (decoupled look-back) of tiles-touched over the depth-
-//                 sorted Gaussians; each CTA writes its contiguous run of (tile, index)
-//                 pairs with coalesced stores and adds the run's tile-digit histograms.
-//                 The last chunk publishes M.
-//   k_finalize    64-bit keys (tile << 32 | depth bits), values, and every tile's
-//                 [start, end) from neighbouring tile ids.
+//                 writes are digit-contiguous.  The last tile pass writes the final
+//                 64-bit keys and the values.
+//   k_scan_dup    single-pass scan (decoupled look-back, 32 predecessors per step) of
+//                 tiles-touched over the depth-sorted Gaussians: every Gaussian's first
+//                 output slot and rectangle record; every Gaussian also adds its rectangle to
+//                 a 2-D difference grid of per-tile counts (4 atomics per Gaussian).
+//   k_dup_write   persistent CTAs over fixed 2048-slot output slices write the (tile, index)
+//                 pairs with coalesced stores (owner of each slot by marks + max-scan).
+//   k_tile_counts prefix sums of the difference grid = instances per tile; their scan gives
+//                 every tile's [start, end) and the digit offsets of the tile passes.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
 #include <mutex>
@@ -35,15 +38,15 @@
 namespace {
 
 constexpr int kScanThreads = 256;
-constexpr int kScanItems = 2;
+constexpr int kScanItems = 4;
 constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
-constexpr int kWin = 4096;                             // output slots per write window
-constexpr int kWinPer = kWin / kScanThreads;
+constexpr int kSlice = 2048;                           // output slots per write slice
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N is modest)
+constexpr int kDepthItems = 8;    // depth passes: 2048 keys per radix tile (N is modest)
 constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
+constexpr int kLookBatch = 4;     // predecessors read per look-back step
 constexpr int kDepthPasses = 4;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // histogram / counter slots
@@ -67,6 +70,11 @@ struct Workspace {
   unsigned long long* scan_state;  // per scan chunk
   uint32_t* lb_depth;              // [pass][tile][256]
   uint32_t* lb_tile;               // [pass][tile][256]
+  uint32_t* grid;                  // (Ty + 1) x (Tx + 1) difference grid of per-tile counts
+  uint32_t* grids;                 // one private difference grid per k_depth_init CTA
+  uint32_t* rstage;                // tile ranges, published to the caller only on success
+  uint32_t* slice_first;           // per output slice of kSlice slots: the item holding its first slot
+  uint4* grec;                     // per depth-ordered Gaussian: (slot, x0 | y0 << 16, width, index)
   uint32_t* small;
 };
 
@@ -85,7 +93,8 @@ int tile_bits(int64_t T) {
 
 int tile_passes(const gs::Cam& k) { return std::max(1, (tile_bits((int64_t)k.Tx * k.Ty) + 7) / 8); }
 
-size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses) {
+size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int64_t grid_words, int64_t n_tiles,
+             int n_grids) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -104,8 +113,18 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses) {
   char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
   char* lbd = take(sizeof(uint32_t) * 256 * kDepthPasses * (size_t)sort_tiles<kDepthItems>(n));
   char* lbt = take(sizeof(uint32_t) * 256 * (size_t)tpasses * (size_t)sort_tiles<kTileItems>(cap));
+  char* gr = take(sizeof(uint32_t) * (size_t)grid_words);
+  char* grs = take(sizeof(uint32_t) * (size_t)grid_words * (size_t)n_grids);
+  char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
+  char* go = take(sizeof(uint32_t) * (size_t)((cap + kSlice - 1) / kSlice));
+  char* gr4 = take(sizeof(uint4) * (size_t)n);
   char* sm = take(sizeof(uint32_t) * kSmWords);
   if (w) {
+    w->grid = reinterpret_cast<uint32_t*>(gr);
+    w->grids = reinterpret_cast<uint32_t*>(grs);
+    w->rstage = reinterpret_cast<uint32_t*>(rs);
+    w->slice_first = reinterpret_cast<uint32_t*>(go);
+    w->grec = reinterpret_cast<uint4*>(gr4);
     w->tkey[0] = reinterpret_cast<uint32_t*>(tk0);
     w->tkey[1] = reinterpret_cast<uint32_t*>(tk1);
     w->tval[0] = reinterpret_cast<uint32_t*>(tv0);
@@ -146,23 +165,42 @@ __device__ __forceinline__ uint32_t wait_u32(const uint32_t* p, int64_t limit, b
   return v;
 }
 
-// ------------------------------------------------------------------ depth keys
-__global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ proj, int64_t n,
+// ------------------------------------------------------------------ depth keys + tile counts
+// Also adds every visible Gaussian's tile rectangle to a difference grid private to the CTA
+// (shared-memory atomics), written out without global atomics and summed by k_grid_sum.
+__global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ proj, int64_t n, gs::Cam k,
                                                      uint32_t* __restrict__ dkey, uint32_t* __restrict__ didx,
                                                      uint32_t* small, uint32_t* lb_depth, uint32_t* lb_tile,
-                                                     int64_t lb_tile_words) {
+                                                     int64_t lb_tile_words, uint32_t* __restrict__ grids) {
+  extern __shared__ uint32_t s_grid[];  // (Ty + 1) x (Tx + 1)
   __shared__ uint32_t s_hist[kDepthPasses][256];
   const float4* q0 = reinterpret_cast<const float4*>(proj);
   const float4* q1 = q0 + n;
+  const int gw = k.Tx + 1, gwords = (k.Tx + 1) * (k.Ty + 1);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t w = gtid; w < (int64_t)kDepthPasses * sort_tiles<kDepthItems>(n) * 256; w += stride) lb_depth[w] = 0u;
   for (int64_t w = gtid; w < lb_tile_words; w += stride) lb_tile[w] = 0u;
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
+  for (int i = threadIdx.x; i < gwords; i += blockDim.x) s_grid[i] = 0u;
   __syncthreads();
   for (int64_t i = gtid; i < n; i += stride) {
     const int r = __float_as_int(__ldg(&q1[i].w));
-    const uint32_t key = r > 0 ? __float_as_uint(__ldg(&q0[i].z)) : kCulledKey;
+    const float4 a = __ldg(&q0[i]);
+    uint32_t key = kCulledKey;
+    if (r > 0) {
+      const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
+      const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
+      const int x0 = min(max((fu - r) >> 4, 0), k.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), k.Tx);
+      const int y0 = min(max((fv - r) >> 4, 0), k.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), k.Ty);
+      key = __float_as_uint(a.z);
+      if (x0 < x1 && y0 < y1) {  // modular arithmetic: -1 = 0xFFFFFFFF
+        atomicAdd(&s_grid[y0 * gw + x0], 1u);
+        atomicAdd(&s_grid[y0 * gw + x1], 0xFFFFFFFFu);
+        atomicAdd(&s_grid[y1 * gw + x0], 0xFFFFFFFFu);
+        atomicAdd(&s_grid[y1 * gw + x1], 1u);
+      }
+    }
     dkey[i] = key;
     didx[i] = (uint32_t)i;
 #pragma unroll
@@ -172,6 +210,23 @@ __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ pr
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) {
     const uint32_t c = (&s_hist[0][0])[i];
     if (c) atomicAdd(&small[kSmHist + i], c);
+  }
+  uint32_t* mine = grids + (size_t)blockIdx.x * gwords;
+  for (int i = threadIdx.x; i < gwords; i += blockDim.x) mine[i] = s_grid[i];
+}
+
+// grid[c] = sum over the CTAs' private difference grids; blockIdx.y picks a group of grids,
+// so each cell receives one atomic add per group
+constexpr int kGridGroups = 16;
+__global__ void __launch_bounds__(256) k_grid_sum(const uint32_t* __restrict__ grids, int ngrids, int gwords,
+                                                   uint32_t* __restrict__ grid) {
+  const int per = (ngrids + kGridGroups - 1) / kGridGroups;
+  const int g0 = blockIdx.y * per, g1 = min(ngrids, g0 + per);
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < gwords; c += gridDim.x * blockDim.x) {
+    uint32_t acc = 0;
+#pragma unroll 4
+    for (int g = g0; g < g1; ++g) acc += __ldg(&grids[(size_t)g * gwords + c]);
+    if (acc) atomicAdd(&grid[c], acc);
   }
 }
 
@@ -211,13 +266,17 @@ struct SortSmem {
 
 // Stable pass over 32-bit keys (8-bit digit at `shift`).  n_host >= 0: sort n_host keys;
 // otherwise min(count[0], cap) keys.
-template <int ITEMS>
+// kFinal: the output is the caller's 64-bit keys, (key << 32) | float bits of the depth of
+// Gaussian value (read from the projection), and the values.
+template <int ITEMS, bool kFinal>
 __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __restrict__ kin,
                                                                const uint32_t* __restrict__ vin,
                                                                uint32_t* __restrict__ kout, uint32_t* __restrict__ vout,
                                                                int64_t n_host, int64_t cap, int shift, int slot,
                                                                uint32_t* small, uint32_t* lookback_pass,
-                                                               int64_t* count, int64_t limit, int drop_publish) {
+                                                               int64_t* count, int64_t limit, int drop_publish,
+                                                               const float4* __restrict__ q0,
+                                                               uint64_t* __restrict__ keys64) {
   constexpr int kTile = kSortThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
@@ -285,11 +344,25 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __
         if (!drop_publish) st_release_u32(my, kFlagPre32 | cnt);
       } else {
         st_release_u32(my, kFlagAgg32 | cnt);
-        for (int64_t p = tile - 1; p >= 0; --p) {
-          const uint32_t s = wait_u32(lookback_pass + p * 256 + d, limit, &to);
-          if (to) break;
-          excl += s & kValMask32;
-          if ((s >> 30) == 2) break;
+        // walk back kLookBatch predecessors per step (independent loads: one memory round trip
+        // per batch), stopping at the nearest inclusive prefix; a predecessor not yet published
+        // is waited for, boundedly
+        int64_t p = tile - 1;
+        bool found = false;
+        while (p >= 0 && !found && !to) {
+          uint32_t sv[kLookBatch];
+#pragma unroll
+          for (int j = 0; j < kLookBatch; ++j)
+            sv[j] = p - j >= 0 ? ld_acquire_u32(lookback_pass + (p - j) * 256 + d) : kFlagPre32;
+#pragma unroll
+          for (int j = 0; j < kLookBatch; ++j) {
+            if (found || to) break;
+            if ((sv[j] >> 30) == 0) sv[j] = wait_u32(lookback_pass + (p - j) * 256 + d, limit, &to);
+            if (to) break;
+            excl += sv[j] & kValMask32;
+            if ((sv[j] >> 30) == 2) found = true;
+          }
+          p -= kLookBatch;
         }
         st_release_u32(my, kFlagPre32 | ((excl + cnt) & kValMask32));
       }
@@ -330,8 +403,10 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __
         const uint32_t d = (key >> shift) & 255u;
         const uint32_t g = S.gbase[d] + (uint32_t)p - S.tstart[d];
         if (g < (uint64_t)M) {  // always true unless a look-back wait gave up (status bit set)
-          kout[g] = key;
-          vout[g] = S.vals[p];
+          const uint32_t val = S.vals[p];
+          if (kFinal) keys64[g] = ((uint64_t)key << 32) | __float_as_uint(__ldg(&q0[val].z));
+          else kout[g] = key;
+          vout[g] = val;
         }
       }
     }
@@ -344,23 +419,17 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __
 // (tile id, Gaussian index) pairs; also accumulates the tile-digit histograms of the pairs.
 __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restrict__ proj, int64_t n,
                                                             const uint32_t* __restrict__ skey,
-                                                            const uint32_t* __restrict__ sidx, gs::Cam k, int tpasses,
-                                                            uint32_t* __restrict__ tkey, uint32_t* __restrict__ tval,
+                                                            const uint32_t* __restrict__ sidx, gs::Cam k,
+                                                            uint32_t* __restrict__ slice_first, uint4* __restrict__ grec,
                                                             int64_t cap, unsigned long long* scan_state,
                                                             uint32_t* small, int64_t* count, int64_t limit) {
   __shared__ uint32_t s_items[kScanChunk];   // tiles touched, then local exclusive offsets
-  __shared__ uint32_t s_rect[kScanChunk];    // x0 | y0 << 16
-  __shared__ uint32_t s_width[kScanChunk];   // rectangle width in tiles
-  __shared__ uint32_t s_gauss[kScanChunk];
-  __shared__ float s_rcpw[kScanChunk];        // 1 / width
-  __shared__ uint32_t s_owner[kWin];          // owner of each output slot in the window
-  __shared__ uint32_t s_hist[kMaxTilePasses][256];
+  __shared__ uint4 s_rec[kScanChunk];         // (offset, x0 | y0 << 16, width, Gaussian)
   __shared__ uint32_t s_warp[kScanThreads / 32];
   __shared__ unsigned long long s_prefix;
   __shared__ uint32_t s_chunk;
   const int tid = threadIdx.x;
   if (tid == 0) s_chunk = atomicAdd(&small[kSmScanCounter], 1u);
-  for (int i = tid; i < kMaxTilePasses * 256; i += kScanThreads) (&s_hist[0][0])[i] = 0u;
   __syncthreads();
   const int64_t chunk = s_chunk;
   const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
@@ -387,10 +456,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
       }
     }
     s_items[li] = cnt;
-    s_rect[li] = rect;
-    s_width[li] = width;
-    s_rcpw[li] = 1.0f / (float)width;
-    s_gauss[li] = g;
+    s_rec[li] = make_uint4(0u, rect, width, g);
   }
   __syncthreads();
   // blocked scan: thread t owns items t*kScanItems .. +kScanItems-1
@@ -420,54 +486,116 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
 #pragma unroll
   for (int j = 0; j < kScanItems; ++j) {
     s_items[tid * kScanItems + j] = run;  // exclusive local offset
+    s_rec[tid * kScanItems + j].x = run;
     run += v[j];
   }
-  // chunk prefix by decoupled look-back
-  if (tid == 0) {
+  // chunk prefix by decoupled look-back, 32 predecessors at a time by warp 0: lane l reads
+  // chunk (p - l); the nearest inclusive prefix ends the walk, aggregates before it are summed
+  if (warp == 0) {
+    if (lane == 0)
+      st_release_u64(&scan_state[chunk], (chunk == 0 ? kFlagPre : kFlagAgg) | (unsigned long long)total);
     unsigned long long excl = 0;
     bool to = false;
-    if (chunk == 0) {
-      st_release_u64(&scan_state[0], kFlagPre | (unsigned long long)total);
-    } else {
-      st_release_u64(&scan_state[chunk], kFlagAgg | (unsigned long long)total);
-      for (int64_t p = chunk - 1; p >= 0; --p) {
-        const unsigned long long s = wait_u64(&scan_state[p], limit, &to);
-        if (to) break;
-        excl += s & kValMask;
-        if ((s >> 62) == 2) break;
+    int64_t p = chunk - 1;
+    while (p >= 0 && !to) {
+      const int64_t q = p - lane;
+      unsigned long long st = q >= 0 ? ld_acquire_u64(&scan_state[q]) : kFlagPre;  // before chunk 0: prefix 0
+      int64_t it = 0;
+      while (true) {  // until every lane up to the nearest prefix has published
+        const uint32_t pre = __ballot_sync(0xffffffffu, (st >> 62) == 2);
+        const uint32_t upto = pre ? (pre & (~pre + 1u)) * 2u - 1u : 0xffffffffu;  // lanes <= nearest prefix
+        const uint32_t missing = __ballot_sync(0xffffffffu, (st >> 62) == 0) & upto;
+        if (!missing) break;
+        if (++it > limit) {
+          to = true;
+          break;
+        }
+        if (it > 32) __nanosleep(64);
+        if ((missing >> lane) & 1u) st = ld_acquire_u64(&scan_state[q]);
       }
-      st_release_u64(&scan_state[chunk], kFlagPre | (excl + total));
+      const uint32_t pre = __ballot_sync(0xffffffffu, (st >> 62) == 2);
+      const int stop = pre ? __ffs(pre) - 1 : 31;
+      unsigned long long v = (lane <= stop && q >= 0) ? (st & kValMask) : 0ull;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      excl += v;
+      if (pre) break;
+      p -= 32;
     }
-    if (to) flag_status(count, gs::kStatusTimeout);
-    s_prefix = excl;
-    if (chunk == nchunks - 1) {
-      const int64_t M = (int64_t)(excl + total);
-      count[0] = M;
-      if (M > cap) flag_status(count, gs::kStatusCapacity);
+    if (lane == 0) {
+      if (chunk > 0) st_release_u64(&scan_state[chunk], kFlagPre | (excl + total));
+      if (to) flag_status(count, gs::kStatusTimeout);
+      s_prefix = excl;
+      if (chunk == nchunks - 1) {
+        const int64_t M = (int64_t)(excl + total);
+        count[0] = M;
+        if (M > cap) flag_status(count, gs::kStatusCapacity);
+      }
     }
   }
   __syncthreads();
-  // Cooperative, coalesced write of this chunk's instances, one window of kWin output slots
-  // at a time: every item whose run meets the window marks its first slot there with its
-  // index + 1, and an inclusive max-scan over the window turns the marks into the owner of
-  // every slot (items are in offset order).
+  // publish every item's global offset and its rectangle record for the write kernel
   const int64_t out0 = (int64_t)s_prefix;
-  for (uint32_t w0 = 0; w0 < total; w0 += kWin) {
-    const uint32_t wn = min((uint32_t)kWin, total - w0);
-    for (int i = tid; i < kWin; i += kScanThreads) s_owner[i] = 0u;
-    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < kScanItems; ++j) {
-      const int li = tid * kScanItems + j;
-      const uint32_t off = s_items[li], c = v[j];
-      if (c > 0 && off < w0 + wn && off + c > w0) s_owner[max(off, w0) - w0] = (uint32_t)li + 1u;
+  for (int j = 0; j < kScanItems; ++j) {
+    const int li = tid * kScanItems + j;
+    const int64_t i = base + li;
+    if (i < n) {
+      uint4 rec = s_rec[li];
+      const int64_t go = out0 + (int64_t)rec.x;  // global exclusive offset
+      rec.x = (uint32_t)min(go, (int64_t)0xFFFFFFFF);
+      grec[i] = rec;
+      // first item of every write slice that starts inside this item's run
+      const int64_t c = v[j];
+      for (int64_t sb = (go + kSlice - 1) / kSlice * kSlice; sb < go + c && sb < cap; sb += kSlice)
+        slice_first[sb / kSlice] = (uint32_t)i;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ instance writes
+// Persistent CTAs take fixed slices of kSlice output slots.  A slice's first item (depth-
+// ordered Gaussian) was recorded by the scan; the items starting in
+// the slice mark their first slot with (item + 1), an inclusive max-scan turns the marks into
+// the owner of every slot, and each slot's (tile, Gaussian) pair is written with coalesced
+// stores.  No CTA waits on another.
+__global__ void __launch_bounds__(kScanThreads) k_dup_write(const uint32_t* __restrict__ slice_first,
+                                                             const uint4* __restrict__ grec, int64_t n, int Tx,
+                                                             uint32_t* __restrict__ tkey, uint32_t* __restrict__ tval,
+                                                             int64_t cap, const int64_t* count) {
+  __shared__ uint32_t s_owner[kSlice];
+  __shared__ uint4 s_item[kSlice];
+  __shared__ uint32_t s_warp[kScanThreads / 32];
+  __shared__ int64_t s_first;
+  if (count[1] != 0) return;
+  const int64_t M = min(count[0], cap);
+  const int64_t nslices = (M + kSlice - 1) / kSlice;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int64_t sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
+    const uint32_t s0 = (uint32_t)(sl * kSlice);
+    const uint32_t sn = (uint32_t)min((int64_t)kSlice, M - (int64_t)s0);
+    if (tid == 0) s_first = __ldg(&slice_first[sl]);  // the item whose run holds slot s0
+    for (int i = tid; i < kSlice; i += kScanThreads) s_owner[i] = 0u;
+    __syncthreads();
+    const int64_t first = s_first;
+    // items first .. first + kSlice - 1 cover the slice (every visible item has >= 1 slot)
+    for (int e = tid; e < kSlice; e += kScanThreads) {
+      const int64_t it = first + e;
+      if (it < n) {
+        const uint4 rec = __ldg(&grec[it]);
+        if (e == 0 || rec.x < s0 + sn) {  // culled items sit at the end with offset M
+          s_item[e] = rec;
+          s_owner[e == 0 ? 0u : rec.x - s0] = (uint32_t)e + 1u;
+        }
+      }
     }
     __syncthreads();
-    {  // inclusive max-scan of s_owner[0 .. kWin): kWinPer consecutive slots per thread
-      uint32_t run = 0;
+    {  // inclusive max-scan of s_owner, kSlice / kScanThreads consecutive slots per thread
+      constexpr int kPer = kSlice / kScanThreads;
+      uint32_t tmax = 0;
 #pragma unroll
-      for (int e = 0; e < kWinPer; ++e) run = max(run, s_owner[tid * kWinPer + e]);
-      uint32_t incl = run;
+      for (int e = 0; e < kPer; ++e) tmax = max(tmax, s_owner[tid * kPer + e]);
+      uint32_t incl = tmax;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -479,59 +607,115 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
       for (int w = 0; w < warp; ++w) carry = max(carry, s_warp[w]);
       uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
       if (lane == 0) prev = 0u;
-      run = max(carry, prev);
+      uint32_t r = max(carry, prev);
 #pragma unroll
-      for (int e = 0; e < kWinPer; ++e) {
-        run = max(run, s_owner[tid * kWinPer + e]);
-        s_owner[tid * kWinPer + e] = run;
+      for (int e = 0; e < kPer; ++e) {
+        r = max(r, s_owner[tid * kPer + e]);
+        s_owner[tid * kPer + e] = r;
       }
     }
     __syncthreads();
-    for (uint32_t q = tid; q < wn; q += kScanThreads) {
-      const uint32_t li = s_owner[q] - 1u;
-      const uint32_t j = w0 + q - s_items[li];  // index of the tile inside the item's rectangle
-      const uint32_t w = s_width[li];
+    for (uint32_t q = tid; q < sn; q += kScanThreads) {
+      const uint4 rec = s_item[s_owner[q] - 1u];
+      const uint32_t j = s0 + q - rec.x;  // index of the tile inside the item's rectangle
+      const uint32_t w = rec.z;
       // j / w from a float estimate, corrected once (|error| <= 1 for j < 2^24)
-      uint32_t row = (uint32_t)__fmul_rz((float)j, s_rcpw[li]);
+      uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));
       int rem = (int)j - (int)(row * w);
       if (rem < 0) { --row; rem += (int)w; }
       if (rem >= (int)w) { ++row; rem -= (int)w; }
-      const uint32_t rect = s_rect[li];
-      const uint32_t tile = ((rect >> 16) + row) * (uint32_t)k.Tx + (rect & 0xffffu) + (uint32_t)rem;
-      const int64_t o = out0 + w0 + q;
-      if (o < cap) {
-        tkey[o] = tile;
-        tval[o] = s_gauss[li];
-      }
-      for (int pp = 0; pp < tpasses; ++pp) atomicAdd(&s_hist[pp][(tile >> (8 * pp)) & 255u], 1u);
+      const int64_t o = (int64_t)s0 + q;
+      tkey[o] = ((rec.y >> 16) + row) * (uint32_t)Tx + (rec.y & 0xffffu) + (uint32_t)rem;
+      tval[o] = rec.w;
     }
     __syncthreads();
   }
-  for (int i = tid; i < tpasses * 256; i += kScanThreads) {
-    const uint32_t c = (&s_hist[0][0])[i];
-    if (c) atomicAdd(&small[kSmHist + kDepthPasses * 256 + i], c);
-  }
 }
 
-// ------------------------------------------------------------------ keys, values, ranges
-__global__ void __launch_bounds__(256) k_finalize(const float* __restrict__ proj, const uint32_t* __restrict__ tkey,
-                                                   const uint32_t* __restrict__ tval, int64_t cap,
-                                                   uint64_t* __restrict__ keys, uint32_t* __restrict__ vals,
-                                                   uint32_t* __restrict__ ranges, const int64_t* count) {
+// ------------------------------------------------------------------ per-tile counts
+// One CTA: 2-D prefix sums of the difference grid (in shared memory) give the instances of
+// every tile; their exclusive scan gives the tile ranges, and their digit sums the exclusive
+// digit offsets of the stable tile passes.
+__global__ void __launch_bounds__(1024) k_tile_counts(const uint32_t* __restrict__ grid, int Tx, int Ty, int tpasses,
+                                                       uint32_t* small, uint32_t* __restrict__ ranges,
+                                                       const int64_t* count) {
+  extern __shared__ uint32_t s_grid[];  // (Ty + 1) x (Tx + 1), then per-pass digit sums
+  __shared__ uint32_t s_warp[32];
   if (count[1] != 0) return;
-  const float4* q0 = reinterpret_cast<const float4*>(proj);
-  const int64_t M = min(count[0], cap);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride) {
-    const uint32_t t = tkey[i], g = tval[i];
-    keys[i] = ((uint64_t)t << 32) | __float_as_uint(__ldg(&q0[g].z));
-    vals[i] = g;
-    if (i == 0 || tkey[i - 1] != t) ranges[2 * (int64_t)t] = (uint32_t)i;
-    if (i == M - 1 || tkey[i + 1] != t) ranges[2 * (int64_t)t + 1] = (uint32_t)(i + 1);
+  const int gw = Tx + 1, gh = Ty + 1, nthreads = blockDim.x, tid = threadIdx.x;
+  const int T = Tx * Ty;
+  uint32_t* s_dig = s_grid + (size_t)gw * gh;  // [kMaxTilePasses][256]
+  for (int i = tid; i < gw * gh; i += nthreads) s_grid[i] = grid[i];
+  for (int i = tid; i < kMaxTilePasses * 256; i += nthreads) s_dig[i] = 0u;
+  __syncthreads();
+  for (int y = tid; y < gh; y += nthreads) {  // prefix along rows
+    uint32_t run = 0;
+    for (int x = 0; x < gw; ++x) {
+      run += s_grid[y * gw + x];
+      s_grid[y * gw + x] = run;
+    }
+  }
+  __syncthreads();
+  for (int x = tid; x < gw; x += nthreads) {  // then along columns
+    uint32_t run = 0;
+    for (int y = 0; y < gh; ++y) {
+      run += s_grid[y * gw + x];
+      s_grid[y * gw + x] = run;
+    }
+  }
+  __syncthreads();
+  // exclusive scan of the T counts in tile order (tile t = (y, x) -> grid cell (y, x))
+  const int per = (T + nthreads - 1) / nthreads;
+  const int t0 = tid * per, t1 = min(T, t0 + per);
+  uint32_t sum = 0;
+  for (int t = t0; t < t1; ++t) sum += s_grid[(t / Tx) * gw + (t % Tx)];
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += s_warp[w];
+  for (int t = t0; t < t1; ++t) {
+    const uint32_t c = s_grid[(t / Tx) * gw + (t % Tx)];
+    ranges[2 * (int64_t)t] = c ? run : 0u;
+    ranges[2 * (int64_t)t + 1] = c ? run + c : 0u;
+    run += c;
+    for (int p = 0; p < tpasses; ++p) atomicAdd(&s_dig[p * 256 + ((t >> (8 * p)) & 255)], c);
+  }
+  __syncthreads();
+  // exclusive digit offsets per tile pass
+  for (int p = 0; p < tpasses; ++p) {
+    if (warp == 0) {
+      uint32_t carry = 0;
+      for (int d0 = 0; d0 < 256; d0 += 32) {
+        const uint32_t c = s_dig[p * 256 + d0 + lane];
+        uint32_t in = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, in, o);
+          if (lane >= o) in += y;
+        }
+        small[kSmDigitBase + (kDepthPasses + p) * 256 + d0 + lane] = carry + in - c;
+        carry += __shfl_sync(0xffffffffu, in, 31);
+      }
+    }
   }
 }
 
-template <int ITEMS>
+// Copies the staged tile ranges to the caller once every pass has finished cleanly.
+__global__ void k_publish_ranges(const uint32_t* __restrict__ rstage, int64_t T, uint32_t* __restrict__ ranges,
+                                 const int64_t* count) {
+  if (count[1] != 0) return;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * T; i += stride) ranges[i] = rstage[i];
+}
+
+template <int ITEMS, bool kFinal>
 int sort_blocks_per_sm() {
   static int cached = -1;
   static std::mutex mu;
@@ -539,8 +723,9 @@ int sort_blocks_per_sm() {
   if (cached < 0) {
     int b = 0;
     const int bytes = (int)sizeof(SortSmem<ITEMS>);
-    cudaFuncSetAttribute(k_onesweep<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS>, kSortThreads, bytes) != cudaSuccess ||
+    cudaFuncSetAttribute(k_onesweep<ITEMS, kFinal>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS, kFinal>, kSortThreads, bytes) !=
+            cudaSuccess ||
         b < 1)
       b = 1;
     cached = b;
@@ -548,12 +733,20 @@ int sort_blocks_per_sm() {
   return cached;
 }
 
+int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); }
+int init_ctas() { return 2 * gs::num_sms(); }
+size_t depth_init_smem(const gs::Cam& k) { return sizeof(uint32_t) * (size_t)grid_words(k); }
+size_t tile_counts_smem(const gs::Cam& k) {
+  return sizeof(uint32_t) * ((size_t)grid_words(k) + (size_t)kMaxTilePasses * 256);
+}
+constexpr size_t kMaxTileCountsSmem = 200 * 1024;
+
 }  // namespace
 
 extern "C" size_t gs_bin_sort_workspace_size(int64_t n, int64_t capacity, const gs_camera* cam) {
   if (!cam || n < 0 || capacity < 0) return 0;
   const gs::Cam k = gs::make_cam(*cam);
-  return carve(nullptr, nullptr, n, capacity, tile_passes(k));
+  return carve(nullptr, nullptr, n, capacity, tile_passes(k), grid_words(k), (int64_t)k.Tx * k.Ty, init_ctas());
 }
 
 extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
@@ -570,14 +763,15 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: misaligned pointer");
   const gs::Cam k = gs::make_cam(*cam);
   const int tpasses = tile_passes(k);
-  if (tpasses > kMaxTilePasses) return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: too many tiles");
-  const size_t need = carve(nullptr, nullptr, n, capacity, tpasses);
+  const int64_t T = (int64_t)k.Tx * k.Ty;
+  if (tpasses > kMaxTilePasses || tile_counts_smem(k) > kMaxTileCountsSmem)
+    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: %d x %d tiles exceed the supported grid", k.Tx, k.Ty);
+  const size_t need = carve(nullptr, nullptr, n, capacity, tpasses, grid_words(k), T, init_ctas());
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: workspace %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w;
-  carve(&w, reinterpret_cast<char*>(workspace), n, capacity, tpasses);
+  carve(&w, reinterpret_cast<char*>(workspace), n, capacity, tpasses, grid_words(k), T, init_ctas());
   cudaStream_t st = gs::as_stream(stream);
-  const int64_t T = (int64_t)k.Tx * k.Ty;
   const int64_t limit = gs::wait_limit();
   const int drop = gs::take_drop_publish();
 
@@ -592,32 +786,58 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     const int sms = gs::num_sms();
     // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys
     const int64_t lb_tile_words = (int64_t)tpasses * sort_tiles<kTileItems>(capacity) * 256;
-    k_depth_init<<<sms * 4, 256, 0, st>>>(proj, n, w.dkey[0], w.didx[0], w.small, w.lb_depth, w.lb_tile,
-                                          lb_tile_words);
+    static const cudaError_t attr_init = cudaFuncSetAttribute(
+        k_depth_init, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxTileCountsSmem);
+    if (attr_init != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr_init));
+    k_depth_init<<<init_ctas(), 256, depth_init_smem(k), st>>>(proj, n, k, w.dkey[0], w.didx[0], w.small, w.lb_depth,
+                                                               w.lb_tile, lb_tile_words, w.grids);
+    if (cudaMemsetAsync(w.grid, 0, sizeof(uint32_t) * (size_t)grid_words(k), st) != cudaSuccess)
+      return gs::check_launch("gs_bin_sort memset");
+    k_grid_sum<<<dim3((unsigned)std::max<int64_t>(1, (grid_words(k) + 255) / 256), kGridGroups), 256, 0, st>>>(
+        w.grids, init_ctas(), (int)grid_words(k), w.grid);
     k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
-    const int grid_d = (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems>(), sort_tiles<kDepthItems>(n));
+    const int grid_d =
+        (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems, false>(), sort_tiles<kDepthItems>(n));
     for (int p = 0; p < kDepthPasses; ++p) {
-      k_onesweep<kDepthItems><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
+      k_onesweep<kDepthItems, false><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
           w.dkey[p & 1], w.didx[p & 1], w.dkey[(p + 1) & 1], w.didx[(p + 1) & 1], n, n, 8 * p, p, w.small,
-          w.lb_depth + (size_t)p * sort_tiles<kDepthItems>(n) * 256, count, limit, p == 0 ? drop : 0);
+          w.lb_depth + (size_t)p * sort_tiles<kDepthItems>(n) * 256, count, limit, p == 0 ? drop : 0, nullptr,
+          nullptr);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
-    // 2. (tile, index) pairs in depth order, with their tile-digit histograms
-    k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, tpasses, w.tkey[0],
-                                                           w.tval[0], capacity, w.scan_state, w.small, count, limit);
+    // 2. (tile, index) pairs in depth order; per-tile counts into the difference grid
+    k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, w.slice_first, w.grec,
+                                                           capacity, w.scan_state, w.small, count, limit);
     if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
-    // 3. stable sort of the pairs by tile id
-    k_digit_scan<<<1, 256, 0, st>>>(w.small, kDepthPasses, tpasses, count);
-    const int grid_t = sms * sort_blocks_per_sm<kTileItems>();
+    const int64_t slices = (capacity + kSlice - 1) / kSlice;
+    k_dup_write<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>(slices, (int64_t)sms * 6)), kScanThreads, 0, st>>>(
+        w.slice_first, w.grec, n, k.Tx, w.tkey[0], w.tval[0], capacity, count);
+    if (gs_status s = gs::check_launch("gs_bin_sort duplicate")) return s;
+    // 3. tile counts -> staged ranges + digit offsets of the tile passes
+    static const cudaError_t attr = cudaFuncSetAttribute(k_tile_counts, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         (int)kMaxTileCountsSmem);
+    if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr));
+    k_tile_counts<<<1, 1024, tile_counts_smem(k), st>>>(w.grid, k.Tx, k.Ty, tpasses, w.small, w.rstage, count);
+    if (gs_status s = gs::check_launch("gs_bin_sort tile counts")) return s;
+    // 4. stable sort of the pairs by tile id; the last pass writes the caller's keys and values
     for (int p = 0; p < tpasses; ++p) {
-      k_onesweep<kTileItems><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
-          w.tkey[p & 1], w.tval[p & 1], w.tkey[(p + 1) & 1], w.tval[(p + 1) & 1], -1, capacity, 8 * p,
-          kDepthPasses + p, w.small, w.lb_tile + (size_t)p * sort_tiles<kTileItems>(capacity) * 256, count, limit, 0);
+      const bool last = p == tpasses - 1;
+      uint32_t* lb = w.lb_tile + (size_t)p * sort_tiles<kTileItems>(capacity) * 256;
+      if (last) {
+        const int grid_t = sms * sort_blocks_per_sm<kTileItems, true>();
+        k_onesweep<kTileItems, true><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
+            w.tkey[p & 1], w.tval[p & 1], nullptr, vals, -1, capacity, 8 * p, kDepthPasses + p, w.small, lb, count,
+            limit, 0, reinterpret_cast<const float4*>(proj), keys);
+      } else {
+        const int grid_t = sms * sort_blocks_per_sm<kTileItems, false>();
+        k_onesweep<kTileItems, false><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
+            w.tkey[p & 1], w.tval[p & 1], w.tkey[(p + 1) & 1], w.tval[(p + 1) & 1], -1, capacity, 8 * p,
+            kDepthPasses + p, w.small, lb, count, limit, 0, nullptr, nullptr);
+      }
     }
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
-    k_finalize<<<sms * 8, 256, 0, st>>>(proj, w.tkey[tpasses & 1], w.tval[tpasses & 1], capacity, keys, vals, ranges,
-                                        count);
-    if (gs_status s = gs::check_launch("gs_bin_sort finalize")) return s;
+    k_publish_ranges<<<sms, 256, 0, st>>>(w.rstage, T, ranges, count);
+    if (gs_status s = gs::check_launch("gs_bin_sort ranges")) return s;
   }
   if (count_host) {
     int64_t hc[2] = {0, 0};
