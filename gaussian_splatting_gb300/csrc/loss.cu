@@ -37,10 +37,17 @@ struct LossSmem {
   // phase A: horizontal blur of 5 statistics; phase C: horizontal blur of 3 maps
   union {
     float h5[5][kIn][kMid];
-    float h3[3][kMid][kOut];
+    float h3[3][kMid][kOut + 1];  // padded row: the row-blocked writes of phase C hit distinct banks
   } u2;
   float red[2][kThreads / 32];
 };
+
+// Register-blocked window sums: a thread produces R consecutive outputs along the blur
+// direction from R + 10 loaded inputs (sliding window), instead of 11 loads per output.
+constexpr int kRA = 6;  // horizontal blur of the statistics: 42 = 7 x 6 outputs per row
+constexpr int kRB = 6;  // vertical blur of the statistics: 42 = 7 x 6 outputs per column
+constexpr int kRC = 4;  // horizontal blur of the derivative maps: 32 = 8 x 4 per row
+constexpr int kRD = 4;  // vertical blur of the derivative maps: 32 = 8 x 4 per column
 
 __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict__ img, const float* __restrict__ tgt,
                                                           int W, int H, Window win, float w_l1, float w_ssim,
@@ -54,6 +61,9 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
   const float* X = img + ch * P;
   const float* Y = tgt + ch * P;
   const int tid = threadIdx.x;
+  float w[11];
+#pragma unroll
+  for (int t = 0; t < 11; ++t) w[t] = win.w[t];
   // ---- A: load with 10-px halo (zero outside the image)
   for (int e = tid; e < kIn * kIn; e += kThreads) {
     const int r = e / kIn, c = e % kIn;
@@ -67,112 +77,158 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
     S.u1.in.y[r][c] = yv;
   }
   __syncthreads();
-  // horizontal blur of x, y, x^2, y^2, xy: rows 0..51, columns 0..41 of the SSIM region
-  for (int e = tid; e < kIn * kMid; e += kThreads) {
-    const int r = e / kMid, c = e % kMid;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f;
+  // horizontal window sums of x, y, x^2, y^2, xy: 52 rows x 42 columns, kRA per thread
+  constexpr int kSegA = kMid / kRA;
+  for (int item = tid; item < kIn * kSegA; item += kThreads) {
+    const int r = item / kSegA, c0 = (item % kSegA) * kRA;
+    float a[5][kRA];
 #pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      const float xv = S.u1.in.x[r][c + k], yv = S.u1.in.y[r][c + k], w = win.w[k];
-      a0 = fmaf(w, xv, a0);
-      a1 = fmaf(w, yv, a1);
-      a2 = fmaf(w, xv * xv, a2);
-      a3 = fmaf(w, yv * yv, a3);
-      a4 = fmaf(w, xv * yv, a4);
+    for (int q = 0; q < kRA; ++q) a[0][q] = a[1][q] = a[2][q] = a[3][q] = a[4][q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kRA + 10; ++e) {
+      const float xv = S.u1.in.x[r][c0 + e], yv = S.u1.in.y[r][c0 + e];
+      const float xx = xv * xv, yy = yv * yv, xy = xv * yv;
+#pragma unroll
+      for (int q = 0; q < kRA; ++q) {
+        const int t = e - q;  // tap index of input e for output q
+        if (t >= 0 && t < 11) {
+          a[0][q] = fmaf(w[t], xv, a[0][q]);
+          a[1][q] = fmaf(w[t], yv, a[1][q]);
+          a[2][q] = fmaf(w[t], xx, a[2][q]);
+          a[3][q] = fmaf(w[t], yy, a[3][q]);
+          a[4][q] = fmaf(w[t], xy, a[4][q]);
+        }
+      }
     }
-    S.u2.h5[0][r][c] = a0;
-    S.u2.h5[1][r][c] = a1;
-    S.u2.h5[2][r][c] = a2;
-    S.u2.h5[3][r][c] = a3;
-    S.u2.h5[4][r][c] = a4;
+#pragma unroll
+    for (int q = 0; q < kRA; ++q)
+#pragma unroll
+      for (int m = 0; m < 5; ++m) S.u2.h5[m][r][c0 + q] = a[m][q];
   }
   __syncthreads();
-  // ---- B: vertical blur -> SSIM statistics on the 42x42 region; map + derivatives
+  // ---- B: vertical window sums -> SSIM statistics on the 42x42 region; map + derivatives
   constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
-  constexpr int kPerThread = (kMid * kMid + kThreads - 1) / kThreads;  // 7
+  constexpr int kSegB = kMid / kRB;
+  constexpr int kItemsB = kMid * kSegB;                         // 294
+  constexpr int kRoundsB = (kItemsB + kThreads - 1) / kThreads;  // 2
   float ssim_sum = 0.f;
-  float dv[kPerThread][3];
+  float dv[kRoundsB][kRB][3];
 #pragma unroll
-  for (int it = 0; it < kPerThread; ++it) {
-    const int e = tid + it * kThreads;
-    dv[it][0] = dv[it][1] = dv[it][2] = 0.f;
-    if (e >= kMid * kMid) continue;
-    const int r = e / kMid, c = e % kMid;
-    float mx = 0.f, my = 0.f, exx = 0.f, eyy = 0.f, exy = 0.f;
+  for (int rd = 0; rd < kRoundsB; ++rd) {
+    const int item = tid + rd * kThreads;
 #pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      const float w = win.w[k];
-      mx = fmaf(w, S.u2.h5[0][r + k][c], mx);
-      my = fmaf(w, S.u2.h5[1][r + k][c], my);
-      exx = fmaf(w, S.u2.h5[2][r + k][c], exx);
-      eyy = fmaf(w, S.u2.h5[3][r + k][c], eyy);
-      exy = fmaf(w, S.u2.h5[4][r + k][c], exy);
+    for (int q = 0; q < kRB; ++q) dv[rd][q][0] = dv[rd][q][1] = dv[rd][q][2] = 0.f;
+    if (item >= kItemsB) continue;
+    const int c = item % kMid, r0 = (item / kMid) * kRB;
+    float a[5][kRB];
+#pragma unroll
+    for (int q = 0; q < kRB; ++q) a[0][q] = a[1][q] = a[2][q] = a[3][q] = a[4][q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kRB + 10; ++e) {
+      float v[5];
+#pragma unroll
+      for (int m = 0; m < 5; ++m) v[m] = S.u2.h5[m][r0 + e][c];
+#pragma unroll
+      for (int q = 0; q < kRB; ++q) {
+        const int t = e - q;
+        if (t >= 0 && t < 11) {
+#pragma unroll
+          for (int m = 0; m < 5; ++m) a[m][q] = fmaf(w[t], v[m], a[m][q]);
+        }
+      }
     }
-    const int gy = oy - kR + r, gx = ox - kR + c;
-    float d0 = 0.f, d1 = 0.f, d2 = 0.f;
-    if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
-      const float sxx = exx - mx * mx, syy = eyy - my * my, sxy = exy - mx * my;
-      const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
-      const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
-      const float iB = 1.f / (B1 * B2);
-      const float Sv = A1 * A2 * iB;
-      d0 = 2.f * my * (A2 - A1) * iB - 2.f * mx * Sv * (1.f / B1 - 1.f / B2);  // dS/dmu_x
-      d1 = -Sv / B2;                                                            // dS/dE[x^2]
-      d2 = 2.f * A1 * iB;                                                       // dS/dE[xy]
-      if (r >= kR && r < kR + kOut && c >= kR && c < kR + kOut) ssim_sum += Sv;
+#pragma unroll
+    for (int q = 0; q < kRB; ++q) {
+      const int r = r0 + q;
+      const int gy = oy - kR + r, gx = ox - kR + c;
+      if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
+        const float mx = a[0][q], my = a[1][q];
+        const float sxx = a[2][q] - mx * mx, syy = a[3][q] - my * my, sxy = a[4][q] - mx * my;
+        const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
+        const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
+        const float iB = 1.f / (B1 * B2);
+        const float Sv = A1 * A2 * iB;
+        dv[rd][q][0] = 2.f * my * (A2 - A1) * iB - 2.f * mx * Sv * (1.f / B1 - 1.f / B2);  // dS/dmu_x
+        dv[rd][q][1] = -Sv / B2;                                                            // dS/dE[x^2]
+        dv[rd][q][2] = 2.f * A1 * iB;                                                       // dS/dE[xy]
+        if (r >= kR && r < kR + kOut && c >= kR && c < kR + kOut) ssim_sum += Sv;
+      }
     }
-    dv[it][0] = d0;
-    dv[it][1] = d1;
-    dv[it][2] = d2;
   }
   __syncthreads();  // inputs no longer needed: the derivative maps overwrite them
 #pragma unroll
-  for (int it = 0; it < kPerThread; ++it) {
-    const int e = tid + it * kThreads;
-    if (e >= kMid * kMid) continue;
-    const int r = e / kMid, c = e % kMid;
-    S.u1.d[0][r][c] = dv[it][0];
-    S.u1.d[1][r][c] = dv[it][1];
-    S.u1.d[2][r][c] = dv[it][2];
-  }
-  __syncthreads();
-  // ---- C: horizontal blur of the three derivative maps onto the output columns
-  for (int e = tid; e < kMid * kOut; e += kThreads) {
-    const int r = e / kOut, c = e % kOut;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+  for (int rd = 0; rd < kRoundsB; ++rd) {
+    const int item = tid + rd * kThreads;
+    if (item >= kItemsB) continue;
+    const int c = item % kMid, r0 = (item / kMid) * kRB;
 #pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      const float w = win.w[k];
-      a0 = fmaf(w, S.u1.d[0][r][c + k], a0);
-      a1 = fmaf(w, S.u1.d[1][r][c + k], a1);
-      a2 = fmaf(w, S.u1.d[2][r][c + k], a2);
-    }
-    S.u2.h3[0][r][c] = a0;
-    S.u2.h3[1][r][c] = a1;
-    S.u2.h3[2][r][c] = a2;
+    for (int q = 0; q < kRB; ++q)
+#pragma unroll
+      for (int m = 0; m < 3; ++m) S.u1.d[m][r0 + q][c] = dv[rd][q][m];
   }
   __syncthreads();
-  // ---- D: vertical blur, combine with the L1 term, write dL/dx
+  // ---- C: horizontal window sums of the three derivative maps onto the output columns
+  constexpr int kSegC = kOut / kRC;
+  for (int item = tid; item < kMid * kSegC; item += kThreads) {
+    const int r = item / kSegC, c0 = (item % kSegC) * kRC;
+    float a[3][kRC];
+#pragma unroll
+    for (int q = 0; q < kRC; ++q) a[0][q] = a[1][q] = a[2][q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kRC + 10; ++e) {
+      float v[3];
+#pragma unroll
+      for (int m = 0; m < 3; ++m) v[m] = S.u1.d[m][r][c0 + e];
+#pragma unroll
+      for (int q = 0; q < kRC; ++q) {
+        const int t = e - q;
+        if (t >= 0 && t < 11) {
+#pragma unroll
+          for (int m = 0; m < 3; ++m) a[m][q] = fmaf(w[t], v[m], a[m][q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kRC; ++q)
+#pragma unroll
+      for (int m = 0; m < 3; ++m) S.u2.h3[m][r][c0 + q] = a[m][q];
+  }
+  __syncthreads();
+  // ---- D: vertical window sums, combine with the L1 term, write dL/dx
   float l1_sum = 0.f;
-  for (int e = tid; e < kOut * kOut; e += kThreads) {
-    const int r = e / kOut, c = e % kOut;
-    const int gy = oy + r, gx = ox + c;
-    if (gx >= W || gy >= H) continue;
-    float t0 = 0.f, t1 = 0.f, t2 = 0.f;
+  constexpr int kSegD = kOut / kRD;
+  for (int item = tid; item < kOut * kSegD; item += kThreads) {
+    const int c = item % kOut, r0 = (item / kOut) * kRD;
+    float a[3][kRD];
 #pragma unroll
-    for (int k = 0; k < 11; ++k) {
-      const float w = win.w[k];
-      t0 = fmaf(w, S.u2.h3[0][r + k][c], t0);
-      t1 = fmaf(w, S.u2.h3[1][r + k][c], t1);
-      t2 = fmaf(w, S.u2.h3[2][r + k][c], t2);
+    for (int q = 0; q < kRD; ++q) a[0][q] = a[1][q] = a[2][q] = 0.f;
+#pragma unroll
+    for (int e = 0; e < kRD + 10; ++e) {
+      float v[3];
+#pragma unroll
+      for (int m = 0; m < 3; ++m) v[m] = S.u2.h3[m][r0 + e][c];
+#pragma unroll
+      for (int q = 0; q < kRD; ++q) {
+        const int t = e - q;
+        if (t >= 0 && t < 11) {
+#pragma unroll
+          for (int m = 0; m < 3; ++m) a[m][q] = fmaf(w[t], v[m], a[m][q]);
+        }
+      }
     }
-    const int64_t g = (int64_t)gy * W + gx;
-    const float xv = __ldg(&X[g]), yv = __ldg(&Y[g]);
-    const float diff = xv - yv;
-    l1_sum += fabsf(diff);
-    const float sgn = diff > 0.f ? 1.f : (diff < 0.f ? -1.f : 0.f);
-    const float dssim = t0 + 2.f * xv * t1 + yv * t2;
-    dimg[ch * P + g] = scale * inv_n * (w_l1 * sgn - w_ssim * dssim);
+    const int gx = ox + c;
+#pragma unroll
+    for (int q = 0; q < kRD; ++q) {
+      const int gy = oy + r0 + q;
+      if (gx >= W || gy >= H) continue;
+      const int64_t g = (int64_t)gy * W + gx;
+      const float xv = __ldg(&X[g]), yv = __ldg(&Y[g]);
+      const float diff = xv - yv;
+      l1_sum += fabsf(diff);
+      const float sgn = diff > 0.f ? 1.f : (diff < 0.f ? -1.f : 0.f);
+      const float dssim = a[0][q] + 2.f * xv * a[1][q] + yv * a[2][q];
+      dimg[ch * P + g] = scale * inv_n * (w_l1 * sgn - w_ssim * dssim);
+    }
   }
   // ---- fixed-order block reduction of the two sums
   const int lane = tid & 31, warp = tid >> 5;
@@ -188,9 +244,9 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
   __syncthreads();
   if (tid == 0) {
     float a = 0.f, b = 0.f;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      a += S.red[0][w];
-      b += S.red[1][w];
+    for (int w2 = 0; w2 < kThreads / 32; ++w2) {
+      a += S.red[0][w2];
+      b += S.red[1][w2];
     }
     const int64_t blk = ((int64_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
     partials[2 * blk] = a;
