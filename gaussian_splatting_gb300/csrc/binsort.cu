@@ -13,22 +13,24 @@
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   k_depth_init  depth keys (0xFFFFFFFF for culled Gaussians) + their digit histograms;
-//                 clears the look-back state and the tile-count grid.
+//                 clears the look-back state; every CTA adds the tile rectangles of its
+//                 Gaussians to a private shared-memory difference grid (4 corners each).
+//   k_grid_sum    sums the private grids into one difference grid of per-tile counts.
 //   k_digit_scan  exclusive digit offsets of the depth passes.
 //   k_onesweep    one stable radix pass of 8 bits: persistent CTAs take tiles of keys in
 //                 order from an atomic counter, rank keys within the tile in shared memory
 //                 (warp match-any ranking), get the tile's global digit offsets by
 //                 decoupled look-back and scatter through shared memory so the global
-//                 writes are digit-contiguous.  The last tile pass writes the final
-//                 64-bit keys and the values.
+//                 writes are digit-contiguous.  The first tile pass generates its
+//                 (tile, index) pairs from the scan's records instead of reading them;
+//                 the last writes the final 64-bit keys and the values.
 //   k_scan_dup    single-pass scan (decoupled look-back, 32 predecessors per step) of
 //                 tiles-touched over the depth-sorted Gaussians: every Gaussian's first
-//                 output slot and rectangle record; every Gaussian also adds its rectangle to
-//                 a 2-D difference grid of per-tile counts (4 atomics per Gaussian).
-//   k_dup_write   persistent CTAs over fixed 2048-slot output slices write the (tile, index)
-//                 pairs with coalesced stores (owner of each slot by marks + max-scan).
+//                 output slot and rectangle record, and for every radix tile of the tile
+//                 passes the Gaussian holding its first slot.
 //   k_tile_counts prefix sums of the difference grid = instances per tile; their scan gives
 //                 every tile's [start, end) and the digit offsets of the tile passes.
+//   k_publish_ranges  copies the staged ranges to the caller's array if nothing failed.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
 #include <mutex>
@@ -40,13 +42,13 @@ namespace {
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 4;
 constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
-constexpr int kSlice = 2048;                           // output slots per write slice
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kDepthItems = 8;    // depth passes: 2048 keys per radix tile (N is modest)
 constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
 constexpr int kLookBatch = 4;     // predecessors read per look-back step
+constexpr int kSlice = kSortThreads * kTileItems;  // instances per generated radix tile
 constexpr int kDepthPasses = 4;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // histogram / counter slots
@@ -268,7 +270,19 @@ struct SortSmem {
 // otherwise min(count[0], cap) keys.
 // kFinal: the output is the caller's 64-bit keys, (key << 32) | float bits of the depth of
 // Gaussian value (read from the projection), and the values.
-template <int ITEMS, bool kFinal>
+// kGen: instead of reading (key, value) pairs, the pass generates them: the pairs are the
+// tile instances in depth order, slot o belonging to the depth-ordered Gaussian whose run
+// [offset, offset + tiles) holds o.  A radix tile is one slice of the scan's slice_first
+// table; the Gaussians starting inside it mark their first slot, an inclusive max-scan turns
+// the marks into each slot's owner, and the owner's rectangle record gives the tile id.
+struct GenSource {
+  const uint32_t* slice_first;  // per radix tile: the Gaussian holding its first slot
+  const uint4* grec;            // per depth-ordered Gaussian: (offset, x0 | y0 << 16, width, index)
+  int64_t n;
+  int Tx;
+};
+
+template <int ITEMS, bool kFinal, bool kGen>
 __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __restrict__ kin,
                                                                const uint32_t* __restrict__ vin,
                                                                uint32_t* __restrict__ kout, uint32_t* __restrict__ vout,
@@ -276,7 +290,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __
                                                                uint32_t* small, uint32_t* lookback_pass,
                                                                int64_t* count, int64_t limit, int drop_publish,
                                                                const float4* __restrict__ q0,
-                                                               uint64_t* __restrict__ keys64) {
+                                                               uint64_t* __restrict__ keys64, GenSource gen) {
   constexpr int kTile = kSortThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
@@ -295,18 +309,79 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __
     const int64_t base = tile * kTile;
     const int nvalid = (int)min((int64_t)kTile, M - base);
     const bool full = nvalid == kTile;
-    // ---- load (warp-striped) and rank stably within the warp
+    // ---- load or generate (warp-striped), then rank stably within the warp
     uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
     const int wbase = warp * (ITEMS * 32);
+    if (kGen) {
+      uint32_t* own = S.keys;  // free until the scatter below
+      const int64_t first = (int64_t)__ldg(&gen.slice_first[tile]);
+      for (int i = tid; i < kTile; i += kSortThreads) own[i] = 0u;
+      __syncthreads();
+      // Offsets rise with e, so the Gaussians starting inside the tile are a prefix of those
+      // after `first`; a Gaussian with no tiles shares its offset with the next one, whence
+      // the max (the last Gaussian at an offset is the one that owns it).
+      const uint32_t end = (uint32_t)(base + nvalid);
+      for (int e0 = 0;; e0 += kSortThreads) {
+        const int64_t it = first + e0 + tid;
+        const uint32_t off = it < gen.n ? __ldg(&gen.grec[it]).x : 0xFFFFFFFFu;
+        const bool in = e0 + tid == 0 || off < end;
+        if (in) atomicMax(&own[e0 + tid == 0 ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
+        if (!__syncthreads_or(in && off < end)) break;
+      }
+      __syncthreads();
+      {  // inclusive max-scan of the marks, ITEMS consecutive slots per thread
+        uint32_t tmax = 0;
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      const int li = wbase + i * 32 + lane;
-      if (full || li < nvalid) {
-        k[i] = kin[base + li];
-        v[i] = vin[base + li];
-      } else {
-        k[i] = 0xFFFFFFFFu;
-        v[i] = 0u;
+        for (int e = 0; e < ITEMS; ++e) tmax = max(tmax, own[tid * ITEMS + e]);
+        uint32_t incl = tmax;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl = max(incl, y);
+        }
+        if (lane == 31) S.wsum[warp] = incl;
+        __syncthreads();
+        uint32_t carry = 0;
+        for (int w = 0; w < warp; ++w) carry = max(carry, S.wsum[w]);
+        uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) prev = 0u;
+        uint32_t r = max(carry, prev);
+#pragma unroll
+        for (int e = 0; e < ITEMS; ++e) {
+          r = max(r, own[tid * ITEMS + e]);
+          own[tid * ITEMS + e] = r;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        if (full || li < nvalid) {
+          const uint4 rec = __ldg(&gen.grec[first + own[li] - 1u]);
+          const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
+          const uint32_t w = rec.z;
+          uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));  // j / w, corrected below
+          int rem = (int)j - (int)(row * w);
+          if (rem < 0) { --row; rem += (int)w; }
+          if (rem >= (int)w) { ++row; rem -= (int)w; }
+          k[i] = ((rec.y >> 16) + row) * (uint32_t)gen.Tx + (rec.y & 0xffffu) + (uint32_t)rem;
+          v[i] = rec.w;
+        } else {
+          k[i] = 0xFFFFFFFFu;
+          v[i] = 0u;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        if (full || li < nvalid) {
+          k[i] = kin[base + li];
+          v[i] = vin[base + li];
+        } else {
+          k[i] = 0xFFFFFFFFu;
+          v[i] = 0u;
+        }
       }
     }
 #pragma unroll
@@ -553,85 +628,6 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
   }
 }
 
-// ------------------------------------------------------------------ instance writes
-// Persistent CTAs take fixed slices of kSlice output slots.  A slice's first item (depth-
-// ordered Gaussian) was recorded by the scan; the items starting in
-// the slice mark their first slot with (item + 1), an inclusive max-scan turns the marks into
-// the owner of every slot, and each slot's (tile, Gaussian) pair is written with coalesced
-// stores.  No CTA waits on another.
-__global__ void __launch_bounds__(kScanThreads) k_dup_write(const uint32_t* __restrict__ slice_first,
-                                                             const uint4* __restrict__ grec, int64_t n, int Tx,
-                                                             uint32_t* __restrict__ tkey, uint32_t* __restrict__ tval,
-                                                             int64_t cap, const int64_t* count) {
-  __shared__ uint32_t s_owner[kSlice];
-  __shared__ uint4 s_item[kSlice];
-  __shared__ uint32_t s_warp[kScanThreads / 32];
-  __shared__ int64_t s_first;
-  if (count[1] != 0) return;
-  const int64_t M = min(count[0], cap);
-  const int64_t nslices = (M + kSlice - 1) / kSlice;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int64_t sl = blockIdx.x; sl < nslices; sl += gridDim.x) {
-    const uint32_t s0 = (uint32_t)(sl * kSlice);
-    const uint32_t sn = (uint32_t)min((int64_t)kSlice, M - (int64_t)s0);
-    if (tid == 0) s_first = __ldg(&slice_first[sl]);  // the item whose run holds slot s0
-    for (int i = tid; i < kSlice; i += kScanThreads) s_owner[i] = 0u;
-    __syncthreads();
-    const int64_t first = s_first;
-    // items first .. first + kSlice - 1 cover the slice (every visible item has >= 1 slot)
-    for (int e = tid; e < kSlice; e += kScanThreads) {
-      const int64_t it = first + e;
-      if (it < n) {
-        const uint4 rec = __ldg(&grec[it]);
-        if (e == 0 || rec.x < s0 + sn) {  // culled items sit at the end with offset M
-          s_item[e] = rec;
-          s_owner[e == 0 ? 0u : rec.x - s0] = (uint32_t)e + 1u;
-        }
-      }
-    }
-    __syncthreads();
-    {  // inclusive max-scan of s_owner, kSlice / kScanThreads consecutive slots per thread
-      constexpr int kPer = kSlice / kScanThreads;
-      uint32_t tmax = 0;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) tmax = max(tmax, s_owner[tid * kPer + e]);
-      uint32_t incl = tmax;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl = max(incl, y);
-      }
-      if (lane == 31) s_warp[warp] = incl;
-      __syncthreads();
-      uint32_t carry = 0;
-      for (int w = 0; w < warp; ++w) carry = max(carry, s_warp[w]);
-      uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) prev = 0u;
-      uint32_t r = max(carry, prev);
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        r = max(r, s_owner[tid * kPer + e]);
-        s_owner[tid * kPer + e] = r;
-      }
-    }
-    __syncthreads();
-    for (uint32_t q = tid; q < sn; q += kScanThreads) {
-      const uint4 rec = s_item[s_owner[q] - 1u];
-      const uint32_t j = s0 + q - rec.x;  // index of the tile inside the item's rectangle
-      const uint32_t w = rec.z;
-      // j / w from a float estimate, corrected once (|error| <= 1 for j < 2^24)
-      uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));
-      int rem = (int)j - (int)(row * w);
-      if (rem < 0) { --row; rem += (int)w; }
-      if (rem >= (int)w) { ++row; rem -= (int)w; }
-      const int64_t o = (int64_t)s0 + q;
-      tkey[o] = ((rec.y >> 16) + row) * (uint32_t)Tx + (rec.y & 0xffffu) + (uint32_t)rem;
-      tval[o] = rec.w;
-    }
-    __syncthreads();
-  }
-}
-
 // ------------------------------------------------------------------ per-tile counts
 // One CTA: 2-D prefix sums of the difference grid (in shared memory) give the instances of
 // every tile; their exclusive scan gives the tile ranges, and their digit sums the exclusive
@@ -715,7 +711,7 @@ __global__ void k_publish_ranges(const uint32_t* __restrict__ rstage, int64_t T,
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * T; i += stride) ranges[i] = rstage[i];
 }
 
-template <int ITEMS, bool kFinal>
+template <int ITEMS, bool kFinal, bool kGen>
 int sort_blocks_per_sm() {
   static int cached = -1;
   static std::mutex mu;
@@ -723,8 +719,8 @@ int sort_blocks_per_sm() {
   if (cached < 0) {
     int b = 0;
     const int bytes = (int)sizeof(SortSmem<ITEMS>);
-    cudaFuncSetAttribute(k_onesweep<ITEMS, kFinal>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS, kFinal>, kSortThreads, bytes) !=
+    cudaFuncSetAttribute(k_onesweep<ITEMS, kFinal, kGen>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS, kFinal, kGen>, kSortThreads, bytes) !=
             cudaSuccess ||
         b < 1)
       b = 1;
@@ -797,42 +793,52 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
         w.grids, init_ctas(), (int)grid_words(k), w.grid);
     k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
     const int grid_d =
-        (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems, false>(), sort_tiles<kDepthItems>(n));
+        (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems, false, false>(), sort_tiles<kDepthItems>(n));
+    const GenSource nogen{nullptr, nullptr, 0, 0};
     for (int p = 0; p < kDepthPasses; ++p) {
-      k_onesweep<kDepthItems, false><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
+      k_onesweep<kDepthItems, false, false><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
           w.dkey[p & 1], w.didx[p & 1], w.dkey[(p + 1) & 1], w.didx[(p + 1) & 1], n, n, 8 * p, p, w.small,
           w.lb_depth + (size_t)p * sort_tiles<kDepthItems>(n) * 256, count, limit, p == 0 ? drop : 0, nullptr,
-          nullptr);
+          nullptr, nogen);
     }
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. (tile, index) pairs in depth order; per-tile counts into the difference grid
     k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, w.slice_first, w.grec,
                                                            capacity, w.scan_state, w.small, count, limit);
     if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
-    const int64_t slices = (capacity + kSlice - 1) / kSlice;
-    k_dup_write<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>(slices, (int64_t)sms * 6)), kScanThreads, 0, st>>>(
-        w.slice_first, w.grec, n, k.Tx, w.tkey[0], w.tval[0], capacity, count);
-    if (gs_status s = gs::check_launch("gs_bin_sort duplicate")) return s;
     // 3. tile counts -> staged ranges + digit offsets of the tile passes
     static const cudaError_t attr = cudaFuncSetAttribute(k_tile_counts, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          (int)kMaxTileCountsSmem);
     if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr));
     k_tile_counts<<<1, 1024, tile_counts_smem(k), st>>>(w.grid, k.Tx, k.Ty, tpasses, w.small, w.rstage, count);
     if (gs_status s = gs::check_launch("gs_bin_sort tile counts")) return s;
-    // 4. stable sort of the pairs by tile id; the last pass writes the caller's keys and values
+    // 4. stable sort of the instances by tile id: the first pass generates the (tile, index)
+    //    pairs in depth order from the scan's records, the last writes the caller's arrays
+    const GenSource gen{w.slice_first, w.grec, n, k.Tx};
+    const float4* q0 = reinterpret_cast<const float4*>(proj);
     for (int p = 0; p < tpasses; ++p) {
-      const bool last = p == tpasses - 1;
       uint32_t* lb = w.lb_tile + (size_t)p * sort_tiles<kTileItems>(capacity) * 256;
-      if (last) {
-        const int grid_t = sms * sort_blocks_per_sm<kTileItems, true>();
-        k_onesweep<kTileItems, true><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
-            w.tkey[p & 1], w.tval[p & 1], nullptr, vals, -1, capacity, 8 * p, kDepthPasses + p, w.small, lb, count,
-            limit, 0, reinterpret_cast<const float4*>(proj), keys);
+      uint32_t* ki = w.tkey[p & 1];
+      uint32_t* vi = w.tval[p & 1];
+      uint32_t* ko = w.tkey[(p + 1) & 1];
+      uint32_t* vo = w.tval[(p + 1) & 1];
+      const size_t sm = sizeof(SortSmem<kTileItems>);
+      const int slot = kDepthPasses + p;
+      if (p == 0 && tpasses == 1) {
+        k_onesweep<kTileItems, true, true><<<sms * sort_blocks_per_sm<kTileItems, true, true>(), kSortThreads, sm, st>>>(
+            ki, vi, nullptr, vals, -1, capacity, 8 * p, slot, w.small, lb, count, limit, 0, q0, keys, gen);
+      } else if (p == 0) {
+        k_onesweep<kTileItems, false, true><<<sms * sort_blocks_per_sm<kTileItems, false, true>(), kSortThreads, sm,
+                                              st>>>(ki, vi, ko, vo, -1, capacity, 8 * p, slot, w.small, lb, count,
+                                                    limit, 0, nullptr, nullptr, gen);
+      } else if (p == tpasses - 1) {
+        k_onesweep<kTileItems, true, false><<<sms * sort_blocks_per_sm<kTileItems, true, false>(), kSortThreads, sm,
+                                              st>>>(ki, vi, nullptr, vals, -1, capacity, 8 * p, slot, w.small, lb,
+                                                    count, limit, 0, q0, keys, nogen);
       } else {
-        const int grid_t = sms * sort_blocks_per_sm<kTileItems, false>();
-        k_onesweep<kTileItems, false><<<grid_t, kSortThreads, sizeof(SortSmem<kTileItems>), st>>>(
-            w.tkey[p & 1], w.tval[p & 1], w.tkey[(p + 1) & 1], w.tval[(p + 1) & 1], -1, capacity, 8 * p,
-            kDepthPasses + p, w.small, lb, count, limit, 0, nullptr, nullptr);
+        k_onesweep<kTileItems, false, false><<<sms * sort_blocks_per_sm<kTileItems, false, false>(), kSortThreads, sm,
+                                               st>>>(ki, vi, ko, vo, -1, capacity, 8 * p, slot, w.small, lb, count,
+                                                     limit, 0, nullptr, nullptr, nogen);
       }
     }
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;

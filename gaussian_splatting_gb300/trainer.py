@@ -29,8 +29,8 @@ def bin_sort_launches(cam) -> int:
     tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
     bits = max(1, (tiles - 1).bit_length())
     tile_passes = max(1, (bits + 7) // 8)
-    # depth keys, grid sum, digit scan, 4 depth passes, scan, duplicate, tile counts, tile passes, ranges
-    return 3 + 4 + 3 + tile_passes + 1
+    # depth keys, grid sum, digit scan, 4 depth passes, scan, tile counts, tile passes, ranges
+    return 3 + 4 + 2 + tile_passes + 1
 
 
 @dataclasses.dataclass

@@ -75,5 +75,5 @@ def test_launch_count_bookkeeping():
     import scenes
     from gaussian_splatting_gb300.trainer import bin_sort_launches
     # 4056 tiles -> 12 tile bits -> 2 tile passes; depth sort has 4
-    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 3 + 4 + 3 + 2 + 1
-    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 3 + 4 + 3 + 1 + 1
+    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 3 + 4 + 2 + 2 + 1
+    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 3 + 4 + 2 + 1 + 1
