@@ -201,5 +201,6 @@ def gs_debug_set_wait_limit(iterations: int):
     load().gs_debug_set_wait_limit(iterations)
 
 
-def gs_debug_drop_publish(enable: bool):
-    load().gs_debug_drop_publish(1 if enable else 0)
+def gs_debug_drop_publish(mode: int):
+    """0 disarms; 1 drops the scan's first look-back publication; 2 drops one grid-barrier arrival."""
+    load().gs_debug_drop_publish(int(mode))

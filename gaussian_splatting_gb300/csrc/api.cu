@@ -54,6 +54,6 @@ void gs_debug_set_wait_limit(int64_t iterations) {
   g_wait_limit.store(iterations < 1 ? (int64_t(1) << 22) : iterations);
 }
 
-void gs_debug_drop_publish(int enable) { g_drop_publish.store(enable ? 1 : 0); }
+void gs_debug_drop_publish(int mode) { g_drop_publish.store(mode == 1 || mode == 2 ? mode : 0); }
 
 }  // extern "C"

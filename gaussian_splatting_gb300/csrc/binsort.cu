@@ -13,21 +13,21 @@
 //
 // Kernels (all on the caller's stream, no host synchronisation):
 //   k_depth_init  depth keys (0xFFFFFFFF for culled Gaussians) + their digit histograms;
-//                 clears the look-back state; every CTA adds the tile rectangles of its
-//                 Gaussians to a private shared-memory difference grid (4 corners each).
+//                 every CTA adds the tile rectangles of its Gaussians to a private
+//                 shared-memory difference grid (4 corners each).
 //   k_grid_sum    sums the private grids into one difference grid of per-tile counts.
 //   k_digit_scan  exclusive digit offsets of the depth passes.
-//   k_onesweep    one stable radix pass of 8 bits: persistent CTAs take tiles of keys in
-//                 order from an atomic counter, rank keys within the tile in shared memory
-//                 (warp match-any ranking), get the tile's global digit offsets by
-//                 decoupled look-back and scatter through shared memory so the global
-//                 writes are digit-contiguous.  The first tile pass generates its
-//                 (tile, index) pairs from the scan's records instead of reading them;
-//                 the last writes the final 64-bit keys and the values.
+//   k_radix_sort  all stable 8-bit passes of one sort in a cooperative launch; each pass
+//                 counts digits per radix tile, scans the counts per digit over the tiles,
+//                 then ranks every tile in shared memory (warp match-any ranking) and
+//                 writes digit-contiguous runs; grid barriers separate the phases.  Used for
+//                 the depth sort and for the tile sort, whose first pass generates its
+//                 (tile, index) pairs from the scan's records instead of reading them and
+//                 whose last pass writes the caller's 64-bit keys and values.
 //   k_scan_dup    single-pass scan (decoupled look-back, 32 predecessors per step) of
 //                 tiles-touched over the depth-sorted Gaussians: every Gaussian's first
 //                 output slot and rectangle record, and for every radix tile of the tile
-//                 passes the Gaussian holding its first slot.
+//                 sort the Gaussian holding its first slot.
 //   k_tile_counts prefix sums of the difference grid = instances per tile; their scan gives
 //                 every tile's [start, end) and the digit offsets of the tile passes.
 //   k_publish_ranges  copies the staged ranges to the caller's array if nothing failed.
@@ -45,22 +45,20 @@ constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kDepthItems = 8;    // depth passes: 2048 keys per radix tile (N is modest)
+constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N is modest)
 constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
-constexpr int kLookBatch = 4;     // predecessors read per look-back step
 constexpr int kSlice = kSortThreads * kTileItems;  // instances per generated radix tile
 constexpr int kDepthPasses = 4;
 constexpr int kMaxTilePasses = 4;
-constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // histogram / counter slots
+constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // digit histogram / base slots
 
 constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
-constexpr uint32_t kFlagAgg32 = 1u << 30, kFlagPre32 = 2u << 30, kValMask32 = (1u << 30) - 1;
 constexpr uint32_t kCulledKey = 0xFFFFFFFFu;
 
 // layout of the small, memset-cleared block of the workspace (32-bit words)
 constexpr int kSmScanCounter = 0;
-constexpr int kSmTileCounters = 1;  // kSlots
-constexpr int kSmHist = 16;         // kSlots * 256
+constexpr int kSmBarrier = 1;        // one arrival counter per sort (depth, tile)
+constexpr int kSmHist = 32;          // kSlots * 256
 constexpr int kSmDigitBase = kSmHist + kSlots * 256;
 constexpr int kSmWords = kSmDigitBase + kSlots * 256;
 
@@ -70,8 +68,8 @@ struct Workspace {
   uint32_t* dkey[2];
   uint32_t* didx[2];
   unsigned long long* scan_state;  // per scan chunk
-  uint32_t* lb_depth;              // [pass][tile][256]
-  uint32_t* lb_tile;               // [pass][tile][256]
+  uint32_t* hist_depth;            // [256][radix tiles of the depth sort]
+  uint32_t* hist_tile;             // [256][radix tiles of the tile sort]
   uint32_t* grid;                  // (Ty + 1) x (Tx + 1) difference grid of per-tile counts
   uint32_t* grids;                 // one private difference grid per k_depth_init CTA
   uint32_t* rstage;                // tile ranges, published to the caller only on success
@@ -113,8 +111,8 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int6
   char* di0 = take(sizeof(uint32_t) * (size_t)n);
   char* di1 = take(sizeof(uint32_t) * (size_t)n);
   char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
-  char* lbd = take(sizeof(uint32_t) * 256 * kDepthPasses * (size_t)sort_tiles<kDepthItems>(n));
-  char* lbt = take(sizeof(uint32_t) * 256 * (size_t)tpasses * (size_t)sort_tiles<kTileItems>(cap));
+  char* lbd = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kDepthItems>(n));
+  char* lbt = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kTileItems>(cap));
   char* gr = take(sizeof(uint32_t) * (size_t)grid_words);
   char* grs = take(sizeof(uint32_t) * (size_t)grid_words * (size_t)n_grids);
   char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
@@ -136,8 +134,8 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int6
     w->didx[0] = reinterpret_cast<uint32_t*>(di0);
     w->didx[1] = reinterpret_cast<uint32_t*>(di1);
     w->scan_state = reinterpret_cast<unsigned long long*>(ss);
-    w->lb_depth = reinterpret_cast<uint32_t*>(lbd);
-    w->lb_tile = reinterpret_cast<uint32_t*>(lbt);
+    w->hist_depth = reinterpret_cast<uint32_t*>(lbd);
+    w->hist_tile = reinterpret_cast<uint32_t*>(lbt);
     w->small = reinterpret_cast<uint32_t*>(sm);
   }
   return off;
@@ -147,33 +145,12 @@ __device__ __forceinline__ void flag_status(int64_t* count, int64_t bits) {
   atomicOr(reinterpret_cast<unsigned long long*>(&count[1]), (unsigned long long)bits);
 }
 
-// Spin on *p until its flag bits are nonzero, at most `limit` iterations.
-__device__ __forceinline__ unsigned long long wait_u64(const unsigned long long* p, int64_t limit, bool* timed_out) {
-  unsigned long long v = ld_acquire_u64(p);
-  for (int64_t it = 0; (v >> 62) == 0; ++it) {
-    if (it >= limit) { *timed_out = true; return v; }
-    if (it > 32) __nanosleep(64);
-    v = ld_acquire_u64(p);
-  }
-  return v;
-}
-__device__ __forceinline__ uint32_t wait_u32(const uint32_t* p, int64_t limit, bool* timed_out) {
-  uint32_t v = ld_acquire_u32(p);
-  for (int64_t it = 0; (v >> 30) == 0; ++it) {
-    if (it >= limit) { *timed_out = true; return v; }
-    if (it > 32) __nanosleep(64);
-    v = ld_acquire_u32(p);
-  }
-  return v;
-}
-
 // ------------------------------------------------------------------ depth keys + tile counts
 // Also adds every visible Gaussian's tile rectangle to a difference grid private to the CTA
 // (shared-memory atomics), written out without global atomics and summed by k_grid_sum.
 __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ proj, int64_t n, gs::Cam k,
                                                      uint32_t* __restrict__ dkey, uint32_t* __restrict__ didx,
-                                                     uint32_t* small, uint32_t* lb_depth, uint32_t* lb_tile,
-                                                     int64_t lb_tile_words, uint32_t* __restrict__ grids) {
+                                                     uint32_t* small, uint32_t* __restrict__ grids) {
   extern __shared__ uint32_t s_grid[];  // (Ty + 1) x (Tx + 1)
   __shared__ uint32_t s_hist[kDepthPasses][256];
   const float4* q0 = reinterpret_cast<const float4*>(proj);
@@ -181,8 +158,6 @@ __global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ pr
   const int gw = k.Tx + 1, gwords = (k.Tx + 1) * (k.Ty + 1);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t w = gtid; w < (int64_t)kDepthPasses * sort_tiles<kDepthItems>(n) * 256; w += stride) lb_depth[w] = 0u;
-  for (int64_t w = gtid; w < lb_tile_words; w += stride) lb_tile[w] = 0u;
   for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
   for (int i = threadIdx.x; i < gwords; i += blockDim.x) s_grid[i] = 0u;
   __syncthreads();
@@ -254,7 +229,16 @@ __global__ void k_digit_scan(uint32_t* small, int slot0, int nslots, const int64
   }
 }
 
-// ------------------------------------------------------------------ one stable radix pass
+// ------------------------------------------------------------------ stable radix sort
+// One cooperative launch runs every pass of a sort.  Each pass is reduce-then-scan over
+// radix tiles of kSortThreads * ITEMS keys, with grid-wide barriers between the phases:
+//   A  every radix tile's digit counts -> hist[digit][tile];
+//   B  per digit, the exclusive scan of its counts over the tiles plus the digit's global
+//      base (digit sums are known beforehand) -> the tile's first output slot for it;
+//   C  every tile ranks its keys stably (warp match-any ranking in shared memory),
+//      scatters them through shared memory and writes digit-contiguous runs.
+// CTA b takes tiles b, b + G, ... in A and C (a tile's offsets no longer depend on the
+// order tiles are processed in), so no CTA ever waits on another inside a phase.
 template <int ITEMS>
 struct SortSmem {
   uint32_t keys[kSortThreads * ITEMS];
@@ -263,18 +247,14 @@ struct SortSmem {
   uint32_t tstart[256];
   uint32_t gbase[256];
   uint32_t wsum[kSortWarps];
-  uint32_t tile;
+  int fail;
 };
 
-// Stable pass over 32-bit keys (8-bit digit at `shift`).  n_host >= 0: sort n_host keys;
-// otherwise min(count[0], cap) keys.
-// kFinal: the output is the caller's 64-bit keys, (key << 32) | float bits of the depth of
-// Gaussian value (read from the projection), and the values.
-// kGen: instead of reading (key, value) pairs, the pass generates them: the pairs are the
-// tile instances in depth order, slot o belonging to the depth-ordered Gaussian whose run
-// [offset, offset + tiles) holds o.  A radix tile is one slice of the scan's slice_first
-// table; the Gaussians starting inside it mark their first slot, an inclusive max-scan turns
-// the marks into each slot's owner, and the owner's rectangle record gives the tile id.
+// Pass 0 of the tile sort generates its pairs: they are the tile instances in depth order,
+// slot o belonging to the depth-ordered Gaussian whose run [offset, offset + tiles) holds o.
+// A radix tile is one slice of the scan's slice_first table; the Gaussians starting inside it
+// mark their first slot, an inclusive max-scan turns the marks into each slot's owner, and
+// the owner's rectangle record gives the tile id.
 struct GenSource {
   const uint32_t* slice_first;  // per radix tile: the Gaussian holding its first slot
   const uint4* grec;            // per depth-ordered Gaussian: (offset, x0 | y0 << 16, width, index)
@@ -282,227 +262,348 @@ struct GenSource {
   int Tx;
 };
 
-template <int ITEMS, bool kFinal, bool kGen>
-__global__ void __launch_bounds__(kSortThreads, 4) k_onesweep(const uint32_t* __restrict__ kin,
-                                                               const uint32_t* __restrict__ vin,
-                                                               uint32_t* __restrict__ kout, uint32_t* __restrict__ vout,
-                                                               int64_t n_host, int64_t cap, int shift, int slot,
-                                                               uint32_t* small, uint32_t* lookback_pass,
-                                                               int64_t* count, int64_t limit, int drop_publish,
-                                                               const float4* __restrict__ q0,
-                                                               uint64_t* __restrict__ keys64, GenSource gen) {
+struct RadixJob {
+  uint32_t* key[2];     // ping-pong: pass p reads key[p & 1] and writes key[(p + 1) & 1]
+  uint32_t* val[2];
+  int64_t n_host;       // >= 0: sort n_host keys; < 0: min(count[0], cap)
+  int64_t cap;
+  int passes;
+  int key_bits;         // significant key bits (pass p sorts bits [8p, min(8p + 8, key_bits)))
+  int slot0;            // digit-base slot of pass 0 in the small block
+  int sort_id;          // selects the barrier word and tile counters in the small block
+  uint32_t* hist;       // [256][hist_stride]
+  int64_t hist_stride;  // radix tiles per digit row
+  uint32_t* small;
+  int64_t* count;
+  int64_t limit;
+  int drop_arrival;     // test hook: CTA 0 never arrives at the first barrier
+  GenSource gen;        // tile sort only (gen.grec != nullptr): pass 0 generates its pairs
+  const float4* q0;     // tile sort only: the last pass writes (key << 32 | depth bits of
+  uint64_t* keys64;     // Gaussian value) to keys64 and the values to vals_out
+  uint32_t* vals_out;
+};
+
+// Grid-wide barrier on a monotonically increasing arrival counter.  Bounded: after `limit`
+// polls, or once another CTA has reported a failure, it sets/keeps status bit 2 and returns
+// false so the caller can leave.
+template <int ITEMS>
+__device__ bool grid_barrier(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t target, bool arrive) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t* bar = J.small + kSmBarrier + J.sort_id;
+    int fail = 0;
+    if (arrive) {
+      __threadfence();
+      atomicAdd(bar, 1u);
+    }
+    for (int64_t it = 0; ld_acquire_u32(bar) < target; ++it) {
+      if (it >= J.limit) {
+        flag_status(J.count, gs::kStatusTimeout);
+        fail = 1;
+        break;
+      }
+      if ((it & 63) == 63 && ld_acquire_u64(reinterpret_cast<const unsigned long long*>(&J.count[1])) != 0) {
+        fail = 1;
+        break;
+      }
+      if (it > 8) __nanosleep(32);
+    }
+    __threadfence();
+    S.fail = fail;
+  }
+  __syncthreads();
+  return S.fail == 0;
+}
+
+// Lanes of vmask whose digit equals this lane's, from one ballot per significant digit bit
+// (cheaper than a match-any when most digits in the warp differ).
+__device__ __forceinline__ uint32_t digit_peers(uint32_t vmask, uint32_t d, int nbits) {
+  uint32_t peers = vmask;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    if (b < nbits) {
+      const uint32_t bit = (d >> b) & 1u;
+      const uint32_t bal = __ballot_sync(vmask, bit);
+      peers &= bit ? bal : ~bal;
+    }
+  }
+  return peers;
+}
+
+// Keys (and values) of radix tile `tile`, warp-striped: item i of lane l of warp w is slot
+// w * ITEMS * 32 + i * 32 + l.  Slots past nvalid get key 0xFFFFFFFF.
+template <int ITEMS>
+__device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J, bool gen, const uint32_t* kin,
+                                          const uint32_t* vin, int64_t tile, int64_t base, int nvalid,
+                                          uint32_t (&k)[ITEMS], uint32_t (&v)[ITEMS]) {
   constexpr int kTile = kSortThreads * ITEMS;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
-  if (count[1] != 0) return;
-  const int64_t M = n_host >= 0 ? n_host : min(count[0], cap);
-  const int64_t ntiles = sort_tiles<ITEMS>(M);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  const uint32_t* digit_base = small + kSmDigitBase + slot * 256;
-  while (true) {
-    if (tid == 0) S.tile = atomicAdd(&small[kSmTileCounters + slot], 1u);
-    for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
-    __syncthreads();
-    const int64_t tile = S.tile;
-    if (tile >= ntiles) break;
-    const int64_t base = tile * kTile;
-    const int nvalid = (int)min((int64_t)kTile, M - base);
-    const bool full = nvalid == kTile;
-    // ---- load or generate (warp-striped), then rank stably within the warp
-    uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
-    const int wbase = warp * (ITEMS * 32);
-    if (kGen) {
-      uint32_t* own = S.keys;  // free until the scatter below
-      const int64_t first = (int64_t)__ldg(&gen.slice_first[tile]);
-      for (int i = tid; i < kTile; i += kSortThreads) own[i] = 0u;
-      __syncthreads();
-      // Offsets rise with e, so the Gaussians starting inside the tile are a prefix of those
-      // after `first`; a Gaussian with no tiles shares its offset with the next one, whence
-      // the max (the last Gaussian at an offset is the one that owns it).
-      const uint32_t end = (uint32_t)(base + nvalid);
-      for (int e0 = 0;; e0 += kSortThreads) {
-        const int64_t it = first + e0 + tid;
-        const uint32_t off = it < gen.n ? __ldg(&gen.grec[it]).x : 0xFFFFFFFFu;
-        const bool in = e0 + tid == 0 || off < end;
-        if (in) atomicMax(&own[e0 + tid == 0 ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
-        if (!__syncthreads_or(in && off < end)) break;
-      }
-      __syncthreads();
-      {  // inclusive max-scan of the marks, ITEMS consecutive slots per thread
-        uint32_t tmax = 0;
-#pragma unroll
-        for (int e = 0; e < ITEMS; ++e) tmax = max(tmax, own[tid * ITEMS + e]);
-        uint32_t incl = tmax;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl = max(incl, y);
-        }
-        if (lane == 31) S.wsum[warp] = incl;
-        __syncthreads();
-        uint32_t carry = 0;
-        for (int w = 0; w < warp; ++w) carry = max(carry, S.wsum[w]);
-        uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) prev = 0u;
-        uint32_t r = max(carry, prev);
-#pragma unroll
-        for (int e = 0; e < ITEMS; ++e) {
-          r = max(r, own[tid * ITEMS + e]);
-          own[tid * ITEMS + e] = r;
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const int li = wbase + i * 32 + lane;
-        if (full || li < nvalid) {
-          const uint4 rec = __ldg(&gen.grec[first + own[li] - 1u]);
-          const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
-          const uint32_t w = rec.z;
-          uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));  // j / w, corrected below
-          int rem = (int)j - (int)(row * w);
-          if (rem < 0) { --row; rem += (int)w; }
-          if (rem >= (int)w) { ++row; rem -= (int)w; }
-          k[i] = ((rec.y >> 16) + row) * (uint32_t)gen.Tx + (rec.y & 0xffffu) + (uint32_t)rem;
-          v[i] = rec.w;
-        } else {
-          k[i] = 0xFFFFFFFFu;
-          v[i] = 0u;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const int li = wbase + i * 32 + lane;
-        if (full || li < nvalid) {
-          k[i] = kin[base + li];
-          v[i] = vin[base + li];
-        } else {
-          k[i] = 0xFFFFFFFFu;
-          v[i] = 0u;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      const int li = wbase + i * 32 + lane;
-      const bool valid = full || li < nvalid;
-      const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const uint32_t d = (k[i] >> shift) & 255u;
-        const uint32_t peers = __match_any_sync(vmask, d);
-        const uint32_t before = S.whist[warp][d];
-        __syncwarp(vmask);
-        const int leader = 31 - __clz(peers);
-        if (lane == leader) S.whist[warp][d] = before + __popc(peers);
-        __syncwarp(vmask);
-        rank[i] = before + __popc(peers & lt_mask);
-      }
-    }
-    __syncthreads();
-    // ---- per digit: prefix over warps, tile count, look-back for the global offset
-    {
-      const int d = tid;  // 256 threads = 256 digits
-      uint32_t run = 0;
-#pragma unroll
-      for (int w = 0; w < kSortWarps; ++w) {
-        const uint32_t c = S.whist[w][d];
-        S.whist[w][d] = run;
-        run += c;
-      }
-      const uint32_t cnt = run;
-      uint32_t* my = lookback_pass + tile * 256 + d;
-      uint32_t excl = 0;
-      bool to = false;
-      if (tile == 0) {
-        if (!drop_publish) st_release_u32(my, kFlagPre32 | cnt);
-      } else {
-        st_release_u32(my, kFlagAgg32 | cnt);
-        // walk back kLookBatch predecessors per step (independent loads: one memory round trip
-        // per batch), stopping at the nearest inclusive prefix; a predecessor not yet published
-        // is waited for, boundedly
-        int64_t p = tile - 1;
-        bool found = false;
-        while (p >= 0 && !found && !to) {
-          uint32_t sv[kLookBatch];
-#pragma unroll
-          for (int j = 0; j < kLookBatch; ++j)
-            sv[j] = p - j >= 0 ? ld_acquire_u32(lookback_pass + (p - j) * 256 + d) : kFlagPre32;
-#pragma unroll
-          for (int j = 0; j < kLookBatch; ++j) {
-            if (found || to) break;
-            if ((sv[j] >> 30) == 0) sv[j] = wait_u32(lookback_pass + (p - j) * 256 + d, limit, &to);
-            if (to) break;
-            excl += sv[j] & kValMask32;
-            if ((sv[j] >> 30) == 2) found = true;
-          }
-          p -= kLookBatch;
-        }
-        st_release_u32(my, kFlagPre32 | ((excl + cnt) & kValMask32));
-      }
-      if (to) flag_status(count, gs::kStatusTimeout);
-      S.gbase[d] = digit_base[d] + excl;
-      // exclusive scan of the tile's digit counts
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) S.wsum[warp] = incl;
-      __syncthreads();
-      uint32_t woff = 0;
-      for (int w = 0; w < warp; ++w) woff += S.wsum[w];
-      S.tstart[d] = woff + incl - cnt;
-    }
-    __syncthreads();
-    // ---- scatter into shared memory in tile order
+  const int wbase = warp * (ITEMS * 32);
+  const bool full = nvalid == kTile;
+  if (!gen) {
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int li = wbase + i * 32 + lane;
       if (full || li < nvalid) {
-        const uint32_t d = (k[i] >> shift) & 255u;
-        const uint32_t pos = S.tstart[d] + S.whist[warp][d] + rank[i];
-        S.keys[pos] = k[i];
-        S.vals[pos] = v[i];
+        k[i] = kin[base + li];
+        v[i] = vin[base + li];
+      } else {
+        k[i] = 0xFFFFFFFFu;
+        v[i] = 0u;
       }
     }
+    return;
+  }
+  uint32_t* own = S.keys;  // free until the scatter
+  const GenSource& G = J.gen;
+  const int64_t first = (int64_t)__ldg(&G.slice_first[tile]);
+  for (int i = tid; i < kTile; i += kSortThreads) own[i] = 0u;
+  __syncthreads();
+  // Offsets rise with e, so the Gaussians starting inside the tile are a prefix of those
+  // after `first`; a Gaussian with no tiles shares its offset with the next one, whence the
+  // max (the last Gaussian at an offset is the one that owns it).
+  const uint32_t end = (uint32_t)(base + nvalid);
+  for (int e0 = 0;; e0 += kSortThreads) {
+    const int64_t it = first + e0 + tid;
+    const uint32_t off = it < G.n ? __ldg(&G.grec[it]).x : 0xFFFFFFFFu;
+    const bool first_item = e0 + tid == 0;
+    const bool in = first_item || off < end;
+    if (in && it < G.n) atomicMax(&own[first_item ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
+    if (!__syncthreads_or(!first_item && off < end)) break;
+  }
+  {  // inclusive max-scan of the marks, ITEMS consecutive slots per thread
+    uint32_t tmax = 0;
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) tmax = max(tmax, own[tid * ITEMS + e]);
+    uint32_t incl = tmax;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl = max(incl, y);
+    }
+    if (lane == 31) S.wsum[warp] = incl;
     __syncthreads();
-    // ---- digit-contiguous global writes
-#pragma unroll 4
-    for (int i = 0; i < ITEMS; ++i) {
-      const int p = i * kSortThreads + tid;
-      if (p < nvalid) {
-        const uint32_t key = S.keys[p];
-        const uint32_t d = (key >> shift) & 255u;
-        const uint32_t g = S.gbase[d] + (uint32_t)p - S.tstart[d];
-        if (g < (uint64_t)M) {  // always true unless a look-back wait gave up (status bit set)
-          const uint32_t val = S.vals[p];
-          if (kFinal) keys64[g] = ((uint64_t)key << 32) | __float_as_uint(__ldg(&q0[val].z));
-          else kout[g] = key;
-          vout[g] = val;
+    uint32_t carry = 0;
+    for (int w = 0; w < warp; ++w) carry = max(carry, S.wsum[w]);
+    uint32_t prev = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) prev = 0u;
+    uint32_t r = max(carry, prev);
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) {
+      r = max(r, own[tid * ITEMS + e]);
+      own[tid * ITEMS + e] = r;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int li = wbase + i * 32 + lane;
+    const uint32_t o = own[li];
+    if ((full || li < nvalid) && o != 0u && first + o - 1u < G.n) {
+      const uint4 rec = __ldg(&G.grec[first + o - 1u]);
+      const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
+      const uint32_t w = max(rec.z, 1u);
+      uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));  // j / w, corrected below
+      int rem = (int)j - (int)(row * w);
+      if (rem < 0) { --row; rem += (int)w; }
+      if (rem >= (int)w) { ++row; rem -= (int)w; }
+      k[i] = ((rec.y >> 16) + row) * (uint32_t)G.Tx + (rec.y & 0xffffu) + (uint32_t)rem;
+      v[i] = rec.w;
+    } else {
+      k[i] = 0xFFFFFFFFu;
+      v[i] = 0u;
+    }
+  }
+  __syncthreads();  // own[] (= S.keys) is reused by the caller
+}
+
+template <int ITEMS, bool kTileSort>
+__global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
+  constexpr int kTile = kSortThreads * ITEMS;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
+  if (J.count[1] != 0) return;
+  const int64_t M = J.n_host >= 0 ? J.n_host : min(J.count[0], J.cap);
+  const int64_t ntiles = sort_tiles<ITEMS>(M);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const uint32_t G = gridDim.x;
+  uint32_t nbar = 0;
+  for (int p = 0; p < J.passes; ++p) {
+    const int shift = 8 * p;
+    const int nbits = min(8, J.key_bits - shift);  // the digit's significant bits
+    const bool gen = kTileSort && p == 0;
+    const bool fin = kTileSort && p == J.passes - 1;
+    const uint32_t* kin = J.key[p & 1];
+    const uint32_t* vin = J.val[p & 1];
+    // ---- A: digit counts of every radix tile
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+      for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
+      __syncthreads();
+      const int64_t base = tile * kTile;
+      const int nvalid = (int)min((int64_t)kTile, M - base);
+      uint32_t k[ITEMS], v[ITEMS];
+      load_tile<ITEMS>(S, J, gen, kin, vin, tile, base, nvalid, k, v);
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = warp * (ITEMS * 32) + i * 32 + lane;
+        if (li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
+      __syncthreads();
+    }
+    ++nbar;
+    if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && blockIdx.x == 0))) return;
+    // ---- B: per digit, exclusive scan over the tiles, plus the digit's global base
+    for (uint32_t d = blockIdx.x; d < 256; d += G) {
+      uint32_t* col = J.hist + (int64_t)d * J.hist_stride;
+      uint32_t carry = J.small[kSmDigitBase + (J.slot0 + p) * 256 + d];
+      constexpr int kPer = 12;
+      for (int64_t c0 = 0; c0 < ntiles; c0 += kSortThreads * kPer) {
+        uint32_t x[kPer];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int64_t t = c0 + tid * kPer + j;
+          x[j] = t < ntiles ? col[t] : 0u;
+          sum += x[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) S.wsum[warp] = incl;
+        __syncthreads();
+        uint32_t run = carry + incl - sum, total = 0;
+        for (int w = 0; w < kSortWarps; ++w) {
+          const uint32_t s = S.wsum[w];
+          if (w < warp) run += s;
+          total += s;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int64_t t = c0 + tid * kPer + j;
+          if (t < ntiles) col[t] = run;
+          run += x[j];
+        }
+        carry += total;
+        __syncthreads();
+      }
+    }
+    if (!grid_barrier(S, J, ++nbar * G, true)) return;
+    // ---- C: rank within the tile, scatter through shared memory, digit-contiguous writes
+    uint32_t* kout = J.key[(p + 1) & 1];
+    uint32_t* vout = fin ? J.vals_out : J.val[(p + 1) & 1];
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+      for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
+      __syncthreads();
+      const int64_t base = tile * kTile;
+      const int nvalid = (int)min((int64_t)kTile, M - base);
+      const bool full = nvalid == kTile;
+      uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
+      load_tile<ITEMS>(S, J, gen, kin, vin, tile, base, nvalid, k, v);
+      const int wbase = warp * (ITEMS * 32);
+      // peer masks of all items first (independent ballots), then the per-warp counts in item
+      // order; rank[] holds the peer mask until it is replaced by the rank
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        const bool valid = full || li < nvalid;
+        const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
+        rank[i] = valid ? digit_peers(vmask, (k[i] >> shift) & 255u, nbits) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        const bool valid = full || li < nvalid;
+        const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+          const uint32_t d = (k[i] >> shift) & 255u;
+          const uint32_t peers = rank[i];
+          const uint32_t before = S.whist[warp][d];
+          __syncwarp(vmask);
+          if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
+          __syncwarp(vmask);
+          rank[i] = before + __popc(peers & lt_mask);
         }
       }
+      __syncthreads();
+      {  // per digit (thread = digit): prefix over warps, the tile's offsets
+        const int d = tid;
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) {
+          const uint32_t c = S.whist[w][d];
+          S.whist[w][d] = run;
+          run += c;
+        }
+        const uint32_t cnt = run;
+        S.gbase[d] = J.hist[(int64_t)d * J.hist_stride + tile];
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) S.wsum[warp] = incl;
+        __syncthreads();
+        uint32_t woff = 0;
+        for (int w = 0; w < warp; ++w) woff += S.wsum[w];
+        S.tstart[d] = woff + incl - cnt;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        if (full || li < nvalid) {
+          const uint32_t d = (k[i] >> shift) & 255u;
+          const uint32_t pos = S.tstart[d] + S.whist[warp][d] + rank[i];
+          S.keys[pos] = k[i];
+          S.vals[pos] = v[i];
+        }
+      }
+      __syncthreads();
+#pragma unroll 4
+      for (int i = 0; i < ITEMS; ++i) {
+        const int q = i * kSortThreads + tid;
+        if (q < nvalid) {
+          const uint32_t key = S.keys[q];
+          const uint32_t d = (key >> shift) & 255u;
+          const uint32_t g = S.gbase[d] + (uint32_t)q - S.tstart[d];
+          if (g < (uint64_t)M) {  // always true unless a barrier gave up (status bit set)
+            const uint32_t val = S.vals[q];
+            if (!fin) kout[g] = key;
+            else if (J.keys64) J.keys64[g] = ((uint64_t)key << 32) | __float_as_uint(__ldg(&J.q0[val].z));
+            vout[g] = val;
+          }
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
+    if (p + 1 < J.passes && !grid_barrier(S, J, ++nbar * G, true)) return;
   }
 }
 
 // ------------------------------------------------------------------ scan + duplicate
 // Walks the Gaussians in depth order (skey / sidx: depth-sorted keys and indices) and writes
-// (tile id, Gaussian index) pairs; also accumulates the tile-digit histograms of the pairs.
+// out every Gaussian's first instance slot and rectangle record, from which the tile sort
+// generates the (tile id, Gaussian index) pairs.
 __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restrict__ proj, int64_t n,
                                                             const uint32_t* __restrict__ skey,
                                                             const uint32_t* __restrict__ sidx, gs::Cam k,
                                                             uint32_t* __restrict__ slice_first, uint4* __restrict__ grec,
                                                             int64_t cap, unsigned long long* scan_state,
-                                                            uint32_t* small, int64_t* count, int64_t limit) {
+                                                            uint32_t* small, int64_t* count, int64_t limit,
+                                                            int drop_publish) {
   __shared__ uint32_t s_items[kScanChunk];   // tiles touched, then local exclusive offsets
   __shared__ uint4 s_rec[kScanChunk];         // (offset, x0 | y0 << 16, width, Gaussian)
   __shared__ uint32_t s_warp[kScanThreads / 32];
   __shared__ unsigned long long s_prefix;
   __shared__ uint32_t s_chunk;
+  if (count[1] != 0) return;  // an earlier stage failed
   const int tid = threadIdx.x;
   if (tid == 0) s_chunk = atomicAdd(&small[kSmScanCounter], 1u);
   __syncthreads();
@@ -568,7 +669,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restri
   // chunk (p - l); the nearest inclusive prefix ends the walk, aggregates before it are summed
   if (warp == 0) {
     if (lane == 0)
-      st_release_u64(&scan_state[chunk], (chunk == 0 ? kFlagPre : kFlagAgg) | (unsigned long long)total);
+      if (!(drop_publish && chunk == 0))
+        st_release_u64(&scan_state[chunk], (chunk == 0 ? kFlagPre : kFlagAgg) | (unsigned long long)total);
     unsigned long long excl = 0;
     bool to = false;
     int64_t p = chunk - 1;
@@ -711,22 +813,31 @@ __global__ void k_publish_ranges(const uint32_t* __restrict__ rstage, int64_t T,
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * T; i += stride) ranges[i] = rstage[i];
 }
 
-template <int ITEMS, bool kFinal, bool kGen>
-int sort_blocks_per_sm() {
+template <int ITEMS, bool kTileSort>
+int radix_blocks_per_sm() {
   static int cached = -1;
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (cached < 0) {
     int b = 0;
-    const int bytes = (int)sizeof(SortSmem<ITEMS>);
-    cudaFuncSetAttribute(k_onesweep<ITEMS, kFinal, kGen>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_onesweep<ITEMS, kFinal, kGen>, kSortThreads, bytes) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_radix_sort<ITEMS, kTileSort>, kSortThreads,
+                                                      sizeof(SortSmem<ITEMS>)) != cudaSuccess ||
         b < 1)
       b = 1;
     cached = b;
   }
   return cached;
+}
+
+// Cooperative launch: every CTA of the grid is resident at once, which the grid barriers need.
+template <int ITEMS, bool kTileSort>
+cudaError_t launch_radix(const RadixJob& job, int64_t max_tiles, cudaStream_t st) {
+  const int64_t cap_ctas = (int64_t)gs::num_sms() * radix_blocks_per_sm<ITEMS, kTileSort>();
+  const int grid = (int)std::max<int64_t>(1, std::min(cap_ctas, max_tiles));
+  RadixJob j = job;
+  void* args[] = {&j};
+  return cudaLaunchCooperativeKernel((const void*)k_radix_sort<ITEMS, kTileSort>, dim3(grid), dim3(kSortThreads), args,
+                                     sizeof(SortSmem<ITEMS>), st);
 }
 
 int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); }
@@ -752,7 +863,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
   if (n < 0 || n >= (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: bad n");
   if (capacity < 0 || capacity >= (int64_t(1) << 30))
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: capacity must be in [0, 2^30)");
-  if (!count || !ranges || (n > 0 && !proj) || (capacity > 0 && (!keys || !vals)) || !workspace)
+  if (!count || !ranges || (n > 0 && !proj) || (capacity > 0 && !vals) || !workspace)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: NULL pointer");
   if ((proj && !gs::aligned16(proj)) || !gs::aligned8(count) || (keys && !gs::aligned8(keys)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -781,30 +892,27 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
       return gs::check_launch("gs_bin_sort memset");
     const int sms = gs::num_sms();
     // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys
-    const int64_t lb_tile_words = (int64_t)tpasses * sort_tiles<kTileItems>(capacity) * 256;
     static const cudaError_t attr_init = cudaFuncSetAttribute(
         k_depth_init, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxTileCountsSmem);
     if (attr_init != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr_init));
-    k_depth_init<<<init_ctas(), 256, depth_init_smem(k), st>>>(proj, n, k, w.dkey[0], w.didx[0], w.small, w.lb_depth,
-                                                               w.lb_tile, lb_tile_words, w.grids);
+    k_depth_init<<<init_ctas(), 256, depth_init_smem(k), st>>>(proj, n, k, w.dkey[0], w.didx[0], w.small, w.grids);
     if (cudaMemsetAsync(w.grid, 0, sizeof(uint32_t) * (size_t)grid_words(k), st) != cudaSuccess)
       return gs::check_launch("gs_bin_sort memset");
     k_grid_sum<<<dim3((unsigned)std::max<int64_t>(1, (grid_words(k) + 255) / 256), kGridGroups), 256, 0, st>>>(
         w.grids, init_ctas(), (int)grid_words(k), w.grid);
     k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
-    const int grid_d =
-        (int)std::min<int64_t>(sms * sort_blocks_per_sm<kDepthItems, false, false>(), sort_tiles<kDepthItems>(n));
-    const GenSource nogen{nullptr, nullptr, 0, 0};
-    for (int p = 0; p < kDepthPasses; ++p) {
-      k_onesweep<kDepthItems, false, false><<<grid_d, kSortThreads, sizeof(SortSmem<kDepthItems>), st>>>(
-          w.dkey[p & 1], w.didx[p & 1], w.dkey[(p + 1) & 1], w.didx[(p + 1) & 1], n, n, 8 * p, p, w.small,
-          w.lb_depth + (size_t)p * sort_tiles<kDepthItems>(n) * 256, count, limit, p == 0 ? drop : 0, nullptr,
-          nullptr, nogen);
-    }
+    RadixJob dj{};
+    dj.key[0] = w.dkey[0]; dj.key[1] = w.dkey[1];
+    dj.val[0] = w.didx[0]; dj.val[1] = w.didx[1];
+    dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.key_bits = 32; dj.slot0 = 0; dj.sort_id = 0;
+    dj.hist = w.hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
+    dj.small = w.small; dj.count = count; dj.limit = limit; dj.drop_arrival = drop == 2;
+    if (cudaError_t e = launch_radix<kDepthItems, false>(dj, sort_tiles<kDepthItems>(n), st))
+      return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. (tile, index) pairs in depth order; per-tile counts into the difference grid
     k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, w.slice_first, w.grec,
-                                                           capacity, w.scan_state, w.small, count, limit);
+                                                           capacity, w.scan_state, w.small, count, limit, drop == 1);
     if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
     // 3. tile counts -> staged ranges + digit offsets of the tile passes
     static const cudaError_t attr = cudaFuncSetAttribute(k_tile_counts, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -814,33 +922,17 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     if (gs_status s = gs::check_launch("gs_bin_sort tile counts")) return s;
     // 4. stable sort of the instances by tile id: the first pass generates the (tile, index)
     //    pairs in depth order from the scan's records, the last writes the caller's arrays
-    const GenSource gen{w.slice_first, w.grec, n, k.Tx};
-    const float4* q0 = reinterpret_cast<const float4*>(proj);
-    for (int p = 0; p < tpasses; ++p) {
-      uint32_t* lb = w.lb_tile + (size_t)p * sort_tiles<kTileItems>(capacity) * 256;
-      uint32_t* ki = w.tkey[p & 1];
-      uint32_t* vi = w.tval[p & 1];
-      uint32_t* ko = w.tkey[(p + 1) & 1];
-      uint32_t* vo = w.tval[(p + 1) & 1];
-      const size_t sm = sizeof(SortSmem<kTileItems>);
-      const int slot = kDepthPasses + p;
-      if (p == 0 && tpasses == 1) {
-        k_onesweep<kTileItems, true, true><<<sms * sort_blocks_per_sm<kTileItems, true, true>(), kSortThreads, sm, st>>>(
-            ki, vi, nullptr, vals, -1, capacity, 8 * p, slot, w.small, lb, count, limit, 0, q0, keys, gen);
-      } else if (p == 0) {
-        k_onesweep<kTileItems, false, true><<<sms * sort_blocks_per_sm<kTileItems, false, true>(), kSortThreads, sm,
-                                              st>>>(ki, vi, ko, vo, -1, capacity, 8 * p, slot, w.small, lb, count,
-                                                    limit, 0, nullptr, nullptr, gen);
-      } else if (p == tpasses - 1) {
-        k_onesweep<kTileItems, true, false><<<sms * sort_blocks_per_sm<kTileItems, true, false>(), kSortThreads, sm,
-                                              st>>>(ki, vi, nullptr, vals, -1, capacity, 8 * p, slot, w.small, lb,
-                                                    count, limit, 0, q0, keys, nogen);
-      } else {
-        k_onesweep<kTileItems, false, false><<<sms * sort_blocks_per_sm<kTileItems, false, false>(), kSortThreads, sm,
-                                               st>>>(ki, vi, ko, vo, -1, capacity, 8 * p, slot, w.small, lb, count,
-                                                     limit, 0, nullptr, nullptr, nogen);
-      }
-    }
+    RadixJob tj{};
+    tj.key[0] = w.tkey[0]; tj.key[1] = w.tkey[1];
+    tj.val[0] = w.tval[0]; tj.val[1] = w.tval[1];
+    tj.n_host = -1; tj.cap = capacity; tj.passes = tpasses; tj.key_bits = std::max(1, tile_bits(T));
+    tj.slot0 = kDepthPasses; tj.sort_id = 1;
+    tj.hist = w.hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
+    tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = 0;
+    tj.gen = GenSource{w.slice_first, w.grec, n, k.Tx};
+    tj.q0 = reinterpret_cast<const float4*>(proj); tj.keys64 = keys; tj.vals_out = vals;
+    if (cudaError_t e = launch_radix<kTileItems, true>(tj, sort_tiles<kTileItems>(capacity), st))
+      return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
     k_publish_ranges<<<sms, 256, 0, st>>>(w.rstage, T, ranges, count);
     if (gs_status s = gs::check_launch("gs_bin_sort ranges")) return s;
@@ -851,7 +943,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
         cudaStreamSynchronize(st) != cudaSuccess)
       return gs::check_launch("gs_bin_sort count readback");
     *count_host = hc[0];
-    if (hc[1] & gs::kStatusTimeout) return gs::set_error(GS_ERR_TIMEOUT, "gs_bin_sort: a look-back wait gave up");
+    if (hc[1] & gs::kStatusTimeout) return gs::set_error(GS_ERR_TIMEOUT, "gs_bin_sort: a bounded device-side wait gave up");
     if (hc[1] & gs::kStatusCapacity)
       return gs::set_error(GS_ERR_CAPACITY, "gs_bin_sort: %lld instances exceed capacity %lld", (long long)hc[0],
                            (long long)capacity);

@@ -26,11 +26,9 @@ LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_
 
 
 def bin_sort_launches(cam) -> int:
-    tiles = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
-    bits = max(1, (tiles - 1).bit_length())
-    tile_passes = max(1, (bits + 7) // 8)
-    # depth keys, grid sum, digit scan, 4 depth passes, scan, tile counts, tile passes, ranges
-    return 3 + 4 + 2 + tile_passes + 1
+    # depth keys, grid sum, digit scan, depth sort (all passes in one cooperative launch),
+    # scan, tile counts, tile sort (likewise), ranges
+    return 8
 
 
 @dataclasses.dataclass
@@ -79,7 +77,7 @@ class Trainer:
         self.jaccard = torch.zeros((batch, batch), dtype=f32, device=dev)
         self.target_dev = torch.zeros((batch, 3, height, width), dtype=f32, device=dev)
         self.capacity = 0
-        self.keys = self.vals = self.sort_ws = None
+        self.vals = self.sort_ws = None
         self.launches = 0
         self.timer = None  # list of (name, start event, end event) when timing per call
         self.work = None   # list of per-view work counts when measuring (synchronises)
@@ -90,7 +88,7 @@ class Trainer:
     def _alloc_sort(self, capacity: int):
         capacity = int(min(capacity, (1 << 30) - 1))
         dev = self.params.device
-        self.keys = torch.empty(capacity, dtype=torch.int64, device=dev)
+        # the sorted keys are not requested: rendering reads the values and the tile ranges
         self.vals = torch.empty(capacity, dtype=torch.int32, device=dev)
         self._ws_cam = None
         self.capacity = capacity
@@ -111,7 +109,7 @@ class Trainer:
                 self._alloc_sort(1024)
             ws = self._sort_ws(cam)
             try:
-                m = N.gs_bin_sort(self.proj[0], self.n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity,
+                m = N.gs_bin_sort(self.proj[0], self.n, cam, ws, ws.numel(), None, self.vals, self.capacity,
                                   self.ranges, self.counts[0], sync=True)
             except N.GSError as e:
                 if e.status != N.GS_ERR_CAPACITY:
@@ -133,7 +131,7 @@ class Trainer:
         proj = self.proj[0]
         N.gs_project(params, self.n, cam, proj)
         ws = self._sort_ws(cam)
-        N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity, self.ranges,
+        N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), None, self.vals, self.capacity, self.ranges,
                       self.counts[0])
         N.gs_render_fwd(proj, self.n, self.vals, self.ranges, cam, self.bg, out, self.T_final, self.n_contrib)
         return out
@@ -159,7 +157,7 @@ class Trainer:
             proj = self.proj[b]
             T("project", N.gs_project, self.params, n, cam, proj)
             ws = self._sort_ws(cam)
-            T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), self.keys, self.vals, self.capacity,
+            T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), None, self.vals, self.capacity,
               self.ranges, self.counts[b])
             work_buf = None
             if self.work is not None:

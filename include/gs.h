@@ -90,11 +90,12 @@ gs_status gs_project(const float* params, int64_t n, const gs_camera* cam, float
  * [0, 0) for an empty tile.
  *   proj       [3][n][4] from gs_project.
  *   workspace  gs_bin_sort_workspace_size(n, capacity, cam) bytes, 256-byte aligned.
- *   keys, vals outputs of `capacity` entries.
+ *   keys, vals outputs of `capacity` entries; keys may be NULL (not written: the
+ *              tile ranges and the values are all that compositing reads).
  *   ranges     output, 2 * Tx * Ty uint32.
  *   count      device int64[2]: count[0] = M (the true count even when it exceeds
  *              capacity), count[1] = status bits (0 = ok, 1 = capacity exceeded,
- *              2 = a look-back wait gave up).  On any nonzero status the outputs are
+ *              2 = a bounded device-side wait gave up).  On any nonzero status the outputs are
  *              not valid and ranges are left empty.
  *   count_host optional host int64: if non-NULL the call synchronises the stream, stores
  *              M there, and returns GS_ERR_CAPACITY / GS_ERR_TIMEOUT per count[1].
@@ -227,14 +228,17 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
 
 /* ---------------------------------------------------------------------------
  * Test hooks (no counterpart in the method).
- * gs_debug_set_wait_limit: iterations a device-side look-back wait spins before it
- *   gives up and reports status bit 2 (default 1 << 22; values < 1 restore it).
- * gs_debug_drop_publish: if nonzero, the next gs_bin_sort call's radix pass 0 never
- *   publishes tile 0's prefix, so every later tile's wait runs out; used to test
- *   that the bounded wait reports GS_ERR_TIMEOUT instead of hanging.
+ * gs_debug_set_wait_limit: iterations a device-side wait (a look-back flag or a grid
+ *   barrier) spins before it gives up and reports status bit 2 (default 1 << 22; values
+ *   < 1 restore it).
+ * gs_debug_drop_publish: arms the next gs_bin_sort call only.  mode 1: the tiles-touched
+ *   scan never publishes chunk 0's prefix, so every later chunk's look-back wait runs out;
+ *   mode 2: CTA 0 of the depth sort never arrives at its first grid barrier, so every
+ *   CTA's barrier wait runs out; 0 disarms.  Used to test that the bounded waits report
+ *   GS_ERR_TIMEOUT instead of hanging.
  */
 void gs_debug_set_wait_limit(int64_t iterations);
-void gs_debug_drop_publish(int enable);
+void gs_debug_drop_publish(int mode);
 
 #ifdef __cplusplus
 }

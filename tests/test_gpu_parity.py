@@ -43,7 +43,7 @@ def gpu_project(P, cam):
     return host(proj)
 
 
-def gpu_bin_sort(planes, cam, capacity=None):
+def gpu_bin_sort(planes, cam, capacity=None, with_keys=True):
     n = planes.shape[1]
     tiles = cam.tiles_x * cam.tiles_y
     if capacity is None:
@@ -54,7 +54,8 @@ def gpu_bin_sort(planes, cam, capacity=None):
     vals = torch.zeros(max(capacity, 1), dtype=torch.int32, device="cuda")
     ranges = torch.full((tiles, 2), 7, dtype=torch.int32, device="cuda")
     count = torch.zeros(2, dtype=torch.int64, device="cuda")
-    M = N.gs_bin_sort(dev(planes), n, cam, ws, ws_bytes, keys, vals, capacity, ranges, count, sync=True)
+    M = N.gs_bin_sort(dev(planes), n, cam, ws, ws_bytes, keys if with_keys else None, vals, capacity, ranges, count,
+                      sync=True)
     return (host(keys)[:M].view(np.uint64), host(vals)[:M].view(np.uint32), host(ranges).view(np.uint32), M,
             host(count))
 
@@ -133,6 +134,10 @@ def test_bin_sort_bit_exact(cfg, n, view):
     assert np.array_equal(keys, keys_o)
     assert np.array_equal(vals, vals_o)
     assert np.array_equal(ranges, ranges_o)
+    if n is None or n > 100_000:  # without the keys output: same values and ranges, keys untouched
+        keys2, vals2, ranges2, M2, count2 = gpu_bin_sort(planes, cam, with_keys=False)
+        assert count2[1] == 0 and M2 == M and not keys2.any()
+        assert np.array_equal(vals2, vals_o) and np.array_equal(ranges2, ranges_o)
 
 
 def test_bin_sort_ties_keep_index_order():
@@ -160,18 +165,20 @@ def test_bin_sort_all_culled_and_overflow():
     assert e.value.status == N.GS_ERR_CAPACITY
 
 
-def test_bin_sort_bounded_wait_reports_timeout():
-    """A look-back flag that nothing sets: the wait gives up and reports, the GPU stays usable."""
+@pytest.mark.parametrize("mode", [1, 2], ids=["scan-look-back", "grid-barrier"])
+def test_bin_sort_bounded_wait_reports_timeout(mode):
+    """A flag that nothing sets (a look-back publication, a barrier arrival): the wait gives
+    up and reports, and the GPU stays usable."""
     P, cam = scene(1, 100_000, 0)
     planes = proj_planes_from_oracle(oracle.project(P, cam))
     N.gs_debug_set_wait_limit(2000)
-    N.gs_debug_drop_publish(True)
+    N.gs_debug_drop_publish(mode)
     try:
         with pytest.raises(N.GSError) as e:
             gpu_bin_sort(planes, cam)
         assert e.value.status == N.GS_ERR_TIMEOUT
     finally:
-        N.gs_debug_drop_publish(False)
+        N.gs_debug_drop_publish(0)
         N.gs_debug_set_wait_limit(0)
     keys, vals, ranges, M, count = gpu_bin_sort(planes, cam)  # next call is clean
     assert count[1] == 0 and M > 0
