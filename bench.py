@@ -325,7 +325,8 @@ def main():
     work_note = (f"per launch: {ev:.4g} pairs evaluated (fwd), {walked:.4g} walked (bwd), {used:.4g} accumulated; "
                  f"fwd {FLOPS_EVAL}/eval + {FWD_FLOPS_USED}/acc, bwd {FLOPS_EVAL}/walked + {BWD_FLOPS_USED}/acc flops")
     # dominant single kernel: the entry points that launch one kernel (gs_bin_sort launches ~11)
-    single = [k for k in ("render_bwd", "render_fwd", "project", "project_bwd", "sparse_adam") if k in per_call]
+    single = [k for k in ("render_bwd", "render_fwd", "project", "project_bwd", "sparse_adam", "project_bwd_adam")
+              if k in per_call]
     dominant = max(single, key=lambda k: sum(per_call[k]))
     roof = {}
     if dominant in flops:
@@ -342,16 +343,17 @@ def main():
         if k in flops:
             ach = flops[k] / (avg[k] / 1e3) / 1e12
             others[k] = {"bound": "alu", "achieved_tflops": round(ach, 3), "frac": round(ach / FP32_PEAK_TFLOPS, 4)}
-    if "sparse_adam" in avg:
-        nu = None
-        try:
-            nu = int(tr.n_union.item())
-        except Exception:
-            pass
-        if nu:
-            gbs = nu * 15 * 16 * 8 / (avg["sparse_adam"] / 1e3) / 1e9
-            others["sparse_adam"] = {"bound": "hbm", "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak_hbm, 4),
-                                     "peak_source": hbm_src}
+    if "project_bwd_adam" in avg:
+        # algorithmic bytes: every view's radius word (16 B per Gaussian) and its visible
+        # Gaussians' screen-space gradients (48 B); for the updated Gaussians, the parameters
+        # (240 B) and moments (480 B) read once and all three written (720 B)
+        nu = int(tr.n_union.item())
+        offs = tr.offsets.cpu().tolist()
+        vis = sum(offs[b + 1] - offs[b] for b in range(cfg.batch))
+        nbytes = cfg.batch * tr.n * 16 + vis * 48 + nu * (240 + 480 + 720)
+        gbs = nbytes / (avg["project_bwd_adam"] / 1e3) / 1e9
+        others["project_bwd_adam"] = {"bound": "hbm", "achieved_gbs": round(gbs, 1),
+                                      "frac": round(gbs / peak_hbm, 4), "bytes": nbytes, "peak_source": hbm_src}
 
     # ---------------- end to end through the public API with host buffers
     e2e = None

@@ -19,7 +19,8 @@ _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ER
 # every symbol include/gs.h declares
 EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_bin_sort_workspace_size", "gs_bin_sort",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
-           "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_debug_set_wait_limit",
+           "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
+           "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
 
@@ -75,6 +76,7 @@ def load() -> C.CDLL:
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
+        "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp], i32),
         "gs_debug_set_wait_limit": ([i64], None),
         "gs_debug_drop_publish": ([i32], None),
     }
@@ -195,6 +197,18 @@ def gs_sparse_adam(params, grads, exp_avg, exp_avg_sq, n, idx, n_idx, max_idx, l
     _check(load().gs_sparse_adam(_ptr(params), _ptr(grads), _ptr(exp_avg), _ptr(exp_avg_sq), n, _ptr(idx),
                                  _ptr(n_idx), max_idx, lr, beta1, beta2, eps, batch, step, _ptr(counts),
                                  n_counts if counts is not None else 0, _stream(stream)), "gs_sparse_adam")
+
+
+def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, step,
+                        counts=None, n_counts=0, stream=None):
+    batch = len(cams)
+    carr = (Camera * batch)(*[camera(c) for c in cams])
+    parr = (C.c_void_p * batch)(*[_ptr(p) for p in projs])
+    garr = (C.c_void_p * batch)(*[_ptr(g) for g in grad2ds])
+    _check(load().gs_project_bwd_adam(_ptr(params), n, C.cast(carr, C.c_void_p), batch, C.cast(parr, C.c_void_p),
+                                      C.cast(garr, C.c_void_p), _ptr(exp_avg), _ptr(exp_avg_sq), lr, beta1, beta2,
+                                      eps, step, _ptr(counts), n_counts if counts is not None else 0,
+                                      _stream(stream)), "gs_project_bwd_adam")
 
 
 def gs_debug_set_wait_limit(iterations: int):

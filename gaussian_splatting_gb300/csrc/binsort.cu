@@ -244,6 +244,7 @@ struct SortSmem {
   uint32_t keys[kSortThreads * ITEMS];
   uint32_t vals[kSortThreads * ITEMS];
   uint32_t whist[kSortWarps][256];
+  uint32_t peer[kSortWarps][256];  // all zero between uses
   uint32_t tstart[256];
   uint32_t gbase[256];
   uint32_t wsum[kSortWarps];
@@ -268,7 +269,6 @@ struct RadixJob {
   int64_t n_host;       // >= 0: sort n_host keys; < 0: min(count[0], cap)
   int64_t cap;
   int passes;
-  int key_bits;         // significant key bits (pass p sorts bits [8p, min(8p + 8, key_bits)))
   int slot0;            // digit-base slot of pass 0 in the small block
   int sort_id;          // selects the barrier word and tile counters in the small block
   uint32_t* hist;       // [256][hist_stride]
@@ -313,21 +313,6 @@ __device__ bool grid_barrier(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t tar
   }
   __syncthreads();
   return S.fail == 0;
-}
-
-// Lanes of vmask whose digit equals this lane's, from one ballot per significant digit bit
-// (cheaper than a match-any when most digits in the warp differ).
-__device__ __forceinline__ uint32_t digit_peers(uint32_t vmask, uint32_t d, int nbits) {
-  uint32_t peers = vmask;
-#pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    if (b < nbits) {
-      const uint32_t bit = (d >> b) & 1u;
-      const uint32_t bal = __ballot_sync(vmask, bit);
-      peers &= bit ? bal : ~bal;
-    }
-  }
-  return peers;
 }
 
 // Keys (and values) of radix tile `tile`, warp-striped: item i of lane l of warp w is slot
@@ -428,10 +413,10 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   const uint32_t G = gridDim.x;
+  for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.peer[0][0])[i] = 0u;
   uint32_t nbar = 0;
   for (int p = 0; p < J.passes; ++p) {
     const int shift = 8 * p;
-    const int nbits = min(8, J.key_bits - shift);  // the digit's significant bits
     const bool gen = kTileSort && p == 0;
     const bool fin = kTileSort && p == J.passes - 1;
     const uint32_t* kin = J.key[p & 1];
@@ -506,14 +491,20 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
       uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
       load_tile<ITEMS>(S, J, gen, kin, vin, tile, base, nvalid, k, v);
       const int wbase = warp * (ITEMS * 32);
-      // peer masks of all items first (independent ballots), then the per-warp counts in item
-      // order; rank[] holds the peer mask until it is replaced by the rank
+      // peer masks of all items first, then the per-warp counts in item order; rank[] holds
+      // the peer mask until it is replaced by the rank.  Peers: every lane ORs its bit into
+      // its digit's word of a per-warp shared-memory table, reads the word back and clears it.
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
         const int li = wbase + i * 32 + lane;
         const bool valid = full || li < nvalid;
-        const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
-        rank[i] = valid ? digit_peers(vmask, (k[i] >> shift) & 255u, nbits) : 0u;
+        const uint32_t d = (k[i] >> shift) & 255u;
+        if (valid) atomicOr(&S.peer[warp][d], 1u << lane);
+        __syncwarp();
+        rank[i] = valid ? S.peer[warp][d] : 0u;
+        __syncwarp();
+        if (valid) S.peer[warp][d] = 0u;
+        __syncwarp();
       }
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
@@ -904,7 +895,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     RadixJob dj{};
     dj.key[0] = w.dkey[0]; dj.key[1] = w.dkey[1];
     dj.val[0] = w.didx[0]; dj.val[1] = w.didx[1];
-    dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.key_bits = 32; dj.slot0 = 0; dj.sort_id = 0;
+    dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
     dj.hist = w.hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
     dj.small = w.small; dj.count = count; dj.limit = limit; dj.drop_arrival = drop == 2;
     if (cudaError_t e = launch_radix<kDepthItems, false>(dj, sort_tiles<kDepthItems>(n), st))
@@ -925,7 +916,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     RadixJob tj{};
     tj.key[0] = w.tkey[0]; tj.key[1] = w.tkey[1];
     tj.val[0] = w.tval[0]; tj.val[1] = w.tval[1];
-    tj.n_host = -1; tj.cap = capacity; tj.passes = tpasses; tj.key_bits = std::max(1, tile_bits(T));
+    tj.n_host = -1; tj.cap = capacity; tj.passes = tpasses;
     tj.slot0 = kDepthPasses; tj.sort_id = 1;
     tj.hist = w.hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
     tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = 0;

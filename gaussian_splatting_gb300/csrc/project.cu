@@ -5,6 +5,8 @@
 // parameter plane is read as one coalesced float4 per thread (512 B per warp), the SH
 // planes only for Gaussians that survive the culls.  HBM-bound: 240 B read + 48 B written
 // per visible Gaussian, 16 B read per culled one.
+#include <cmath>
+
 #include "common.cuh"
 
 namespace {
@@ -90,16 +92,30 @@ struct Fwd {
   int radius, x0, y0, x1, y1;
 };
 
+// Where a Gaussian's parameter planes are read from: global memory (plane pl of Gaussian i
+// at params[pl][i]) or a shared-memory copy ([pl][thread]).
+struct GlobalParams {
+  const float* p;
+  int64_t n, i;
+  __device__ __forceinline__ float4 plane(int pl) const { return ldg4(p, (int64_t)pl * n + i); }
+};
+template <int kThreadsPerCta>
+struct SharedParams {
+  const float4* s;
+  int t;
+  __device__ __forceinline__ float4 plane(int pl) const { return s[pl * kThreadsPerCta + t]; }
+};
+
 // Returns false if the Gaussian is culled.
-__device__ __forceinline__ bool project_core(const float* __restrict__ params, int64_t n, int64_t i, const Cam& k,
-                                             Fwd& f) {
-  const float4 p0 = ldg4(params, i);
+template <class Src>
+__device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& f) {
+  const float4 p0 = src.plane(0);
   f.px = k.R[0] * p0.x + k.R[1] * p0.y + k.R[2] * p0.z + k.t[0];
   f.py = k.R[3] * p0.x + k.R[4] * p0.y + k.R[5] * p0.z + k.t[1];
   f.pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
   if (!(f.pz > k.znear)) return false;
-  const float4 p1 = ldg4(params, n + i);
-  const float4 p2 = ldg4(params, 2 * n + i);
+  const float4 p1 = src.plane(1);
+  const float4 p2 = src.plane(2);
   f.s[0] = expf(p1.x);
   f.s[1] = expf(p1.y);
   f.s[2] = expf(p1.z);
@@ -175,8 +191,9 @@ __global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ p
   if (i >= n) return;
   Fwd f;
   float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, q2 = q0;
-  if (project_core(params, n, i, k, f)) {
-    const float4 p0 = ldg4(params, i);
+  const GlobalParams src{params, n, i};
+  if (project_core(src, k, f)) {
+    const float4 p0 = src.plane(0);
     float dx = p0.x - campos.x, dy = p0.y - campos.y, dz = p0.z - campos.z;
     const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
     dx *= il; dy *= il; dz *= il;
@@ -185,7 +202,7 @@ __global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ p
     float rgb[3] = {0.5f, 0.5f, 0.5f};
 #pragma unroll
     for (int pl = 0; pl < 12; ++pl) {
-      const float4 s = ldg4(params, (int64_t)(3 + pl) * n + i);
+      const float4 s = src.plane(3 + pl);
       const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
       for (int l = 0; l < 4; ++l) {
@@ -203,43 +220,47 @@ __global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ p
   st4(proj, 2 * n + i, q2);
 }
 
-__global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ params, int64_t n, Cam k,
-                                                     float3 campos, const float* __restrict__ proj,
-                                                     const float* __restrict__ grad2d, float* __restrict__ grads) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  if (__float_as_int(ldg4(proj, n + i).w) <= 0) return;  // culled in this view
-  Fwd f;
-  if (!project_core(params, n, i, k, f)) return;
-  const float4 g0 = ldg4(grad2d, 3 * i + 0);  // du, dv, dopacity
-  const float4 g1 = ldg4(grad2d, 3 * i + 1);  // dA, dB, dC
-  const float4 g2 = ldg4(grad2d, 3 * i + 2);  // dr, dg, db
-  const float4 p0 = ldg4(params, i);
+// Reverse mode of the projection of Gaussian i for one camera: parameter gradients from its
+// screen-space gradients g0 = (du, dv, dopacity), g1 = (dA, dB, dC), g2 = (dr, dg, db).
+// The SH-coefficient gradient is rank one, gcol[c] * y[k] for coefficient k and channel c,
+// so it is returned as the clamped colour gradient gcol and the basis y.
+struct BwdOut {
+  float gm[3];     // mean
+  float glogit;    // opacity logit
+  float gls[3];    // log-scales
+  float4 gq;       // quaternion (unnormalised)
+  float gcol[3];   // colour gradient after the clamp at 0
+  SHBasis b;       // SH basis at the view direction
+};
+
+template <class Src>
+__device__ __forceinline__ void project_bwd_core(const Src& src, const Cam& k, float3 campos, const Fwd& f, float4 g0,
+                                                 float4 g1, float4 g2, BwdOut& o) {
+  const float4 p0 = src.plane(0);
 
   // ---- colour: rgb = max(sum_k sh_k Y_k(d) + 0.5, 0), d = (mean - campos)/|.|
   float dx = p0.x - campos.x, dy = p0.y - campos.y, dz = p0.z - campos.z;
   const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
   dx *= il; dy *= il; dz *= il;
-  SHBasis b;
-  sh_eval(dx, dy, dz, b);
+  sh_eval(dx, dy, dz, o.b);
   float sh[48];
 #pragma unroll
   for (int pl = 0; pl < 12; ++pl) {
-    const float4 s = ldg4(params, (int64_t)(3 + pl) * n + i);
+    const float4 s = src.plane(3 + pl);
     sh[4 * pl + 0] = s.x; sh[4 * pl + 1] = s.y; sh[4 * pl + 2] = s.z; sh[4 * pl + 3] = s.w;
   }
-  float gcol[3] = {g2.x, g2.y, g2.z};
+  o.gcol[0] = g2.x; o.gcol[1] = g2.y; o.gcol[2] = g2.z;
 #pragma unroll
   for (int c = 0; c < 3; ++c) {
     float raw = 0.5f;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) raw += sh[3 * kk + c] * b.y[kk];
-    if (raw < 0.f) gcol[c] = 0.f;  // clamped channel passes no gradient
+    for (int kk = 0; kk < 16; ++kk) raw += sh[3 * kk + c] * o.b.y[kk];
+    if (raw < 0.f) o.gcol[c] = 0.f;  // clamped channel passes no gradient
   }
   float wsum[16];
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk)
-    wsum[kk] = gcol[0] * sh[3 * kk] + gcol[1] * sh[3 * kk + 1] + gcol[2] * sh[3 * kk + 2];
+    wsum[kk] = o.gcol[0] * sh[3 * kk] + o.gcol[1] * sh[3 * kk + 1] + o.gcol[2] * sh[3 * kk + 2];
   const float3 gd = sh_grad_dot(dx, dy, dz, wsum);
   const float gdot = gd.x * dx + gd.y * dy + gd.z * dz;
   float gmx = (gd.x - gdot * dx) * il, gmy = (gd.y - gdot * dy) * il, gmz = (gd.z - gdot * dz) * il;
@@ -303,6 +324,7 @@ __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ p
     gmy += k.R[1] * gpx + k.R[4] * gpy + k.R[7] * gpz;
     gmz += k.R[2] * gpx + k.R[5] * gpy + k.R[8] * gpz;
   }
+  o.gm[0] = gmx; o.gm[1] = gmy; o.gm[2] = gmz;
   // ---- Sigma = M M^T, M = Rq diag(s):  dM = 2 dSigma M
   float M[9];
 #pragma unroll
@@ -316,10 +338,10 @@ __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ p
 #pragma unroll
     for (int c = 0; c < 3; ++c)
       dM[3 * r + c] = 2.f * (dSf[3 * r] * M[c] + dSf[3 * r + 1] * M[3 + c] + dSf[3 * r + 2] * M[6 + c]);
-  float gls[3], dR[9];
+  float dR[9];
 #pragma unroll
   for (int c = 0; c < 3; ++c) {
-    gls[c] = (dM[c] * f.Rq[c] + dM[3 + c] * f.Rq[3 + c] + dM[6 + c] * f.Rq[6 + c]) * f.s[c];
+    o.gls[c] = (dM[c] * f.Rq[c] + dM[3 + c] * f.Rq[3 + c] + dM[6 + c] * f.Rq[6 + c]) * f.s[c];
 #pragma unroll
     for (int r = 0; r < 3; ++r) dR[3 * r + c] = dM[3 * r + c] * f.s[c];
   }
@@ -331,21 +353,33 @@ __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ p
   gq[2] = 2.f * (x * (dR[1] + dR[3]) + w * (dR[2] - dR[6]) + z * (dR[5] + dR[7]) - 2.f * y * (dR[0] + dR[8]));
   gq[3] = 2.f * (w * (dR[3] - dR[1]) + x * (dR[2] + dR[6]) + y * (dR[5] + dR[7]) - 2.f * z * (dR[0] + dR[4]));
   const float qd = gq[0] * w + gq[1] * x + gq[2] * y + gq[3] * z;
-  const float4 gqr = make_float4((gq[0] - qd * w) * f.qinv, (gq[1] - qd * x) * f.qinv, (gq[2] - qd * y) * f.qinv,
-                                 (gq[3] - qd * z) * f.qinv);
+  o.gq = make_float4((gq[0] - qd * w) * f.qinv, (gq[1] - qd * x) * f.qinv, (gq[2] - qd * y) * f.qinv,
+                     (gq[3] - qd * z) * f.qinv);
   // ---- opacity = sigmoid(logit)
-  const float glogit = g0.z * f.opac * (1.f - f.opac);
+  o.glogit = g0.z * f.opac * (1.f - f.opac);
+}
 
+__global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ params, int64_t n, Cam k,
+                                                     float3 campos, const float* __restrict__ proj,
+                                                     const float* __restrict__ grad2d, float* __restrict__ grads) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  if (__float_as_int(ldg4(proj, n + i).w) <= 0) return;  // culled in this view
+  Fwd f;
+  const GlobalParams src{params, n, i};
+  if (!project_core(src, k, f)) return;
+  BwdOut o;
+  project_bwd_core(src, k, campos, f, ldg4(grad2d, 3 * i + 0), ldg4(grad2d, 3 * i + 1), ldg4(grad2d, 3 * i + 2), o);
   // ---- accumulate into the gradient planes
   float4* G = reinterpret_cast<float4*>(grads);
   float4 a0 = G[i];
-  a0.x += gmx; a0.y += gmy; a0.z += gmz; a0.w += glogit;
+  a0.x += o.gm[0]; a0.y += o.gm[1]; a0.z += o.gm[2]; a0.w += o.glogit;
   G[i] = a0;
   float4 a1 = G[n + i];
-  a1.x += gls[0]; a1.y += gls[1]; a1.z += gls[2];
+  a1.x += o.gls[0]; a1.y += o.gls[1]; a1.z += o.gls[2];
   G[n + i] = a1;
   float4 a2 = G[2 * n + i];
-  a2.x += gqr.x; a2.y += gqr.y; a2.z += gqr.z; a2.w += gqr.w;
+  a2.x += o.gq.x; a2.y += o.gq.y; a2.z += o.gq.z; a2.w += o.gq.w;
   G[2 * n + i] = a2;
 #pragma unroll
   for (int pl = 0; pl < 12; ++pl) {
@@ -354,9 +388,126 @@ __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ p
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       const int fidx = 4 * pl + l;
-      sv[l] += gcol[fidx % 3] * b.y[fidx / 3];
+      sv[l] += o.gcol[fidx % 3] * o.b.y[fidx / 3];
     }
     G[(int64_t)(3 + pl) * n + i] = s;
+  }
+}
+
+// ------------------------------------------------------------------ batched backward + Adam
+// The composition of gs_project_bwd over the views of a batch (gradients summed in view
+// order) and gs_sparse_adam over the Gaussians visible in at least one of them, without the
+// gradient planes ever reaching global memory: a thread owns one Gaussian, keeps its
+// geometry gradients in registers and its 48 SH-coefficient gradients in shared memory, and
+// applies the update plane by plane.  Reads 240 B of parameters + 64 B per view + 480 B of
+// moments and writes 720 B per updated Gaussian.
+constexpr int kMaxBatchViews = 16;
+constexpr int kAdamThreads = 128;
+
+struct BatchViews {
+  Cam k[kMaxBatchViews];
+  float3 campos[kMaxBatchViews];
+  const float* proj[kMaxBatchViews];
+  const float* grad2d[kMaxBatchViews];
+  int batch;
+};
+
+struct AdamHyper {
+  float b1, b2, lr_b, bc1, bc2, eps;
+};
+
+__device__ __forceinline__ void adam4(float4& p, float4& m, float4& v, float4 g, const AdamHyper& h) {
+  float* pa = &p.x;
+  float* ma = &m.x;
+  float* va = &v.x;
+  const float ga[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+  for (int l = 0; l < 4; ++l) {
+    ma[l] = h.b1 * ma[l] + (1.f - h.b1) * ga[l];
+    va[l] = h.b2 * va[l] + (1.f - h.b2) * ga[l] * ga[l];
+    pa[l] -= h.lr_b * (ma[l] / h.bc1) / (sqrtf(va[l] / h.bc2) + h.eps);
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+struct AdamSmem {
+  float4 par[15][kAdamThreads];  // the CTA's parameter planes
+  float sh[48][kAdamThreads];    // SH-coefficient gradients, [3k + c][thread]
+};
+
+__global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __restrict__ params, int64_t n,
+                                                                      BatchViews bv, float4* __restrict__ m,
+                                                                      float4* __restrict__ v, AdamHyper h,
+                                                                      const int64_t* counts, int n_counts) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  AdamSmem& S = *reinterpret_cast<AdamSmem*>(smem_raw);
+  for (int c = 0; c < n_counts; ++c)
+    if (counts[2 * c + 1] != 0) return;  // a view of this batch overflowed its binning
+  const int t = threadIdx.x;
+  const int64_t i = (int64_t)blockIdx.x * kAdamThreads + t;
+  if (i >= n) return;
+  // the fifteen planes of this Gaussian, copied asynchronously while the visibility is read
+  const float4* P4 = reinterpret_cast<const float4*>(params);
+#pragma unroll
+  for (int pl = 0; pl < 15; ++pl) cp_async16(&S.par[pl][t], &P4[(int64_t)pl * n + i]);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  float (*s_sh)[kAdamThreads] = S.sh;
+#pragma unroll
+  for (int f = 0; f < 48; ++f) s_sh[f][t] = 0.f;
+  float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gl = ga, gq = ga;
+  bool seen = false;
+  uint32_t vis = 0;  // views whose radius word is > 0, all read up front
+  for (int b = 0; b < bv.batch; ++b)
+    if (__float_as_int(__ldg(&reinterpret_cast<const float4*>(bv.proj[b])[n + i].w)) > 0) vis |= 1u << b;
+  asm volatile("cp.async.wait_all;" ::: "memory");  // own copies only: no block barrier needed
+  const SharedParams<kAdamThreads> src{&S.par[0][0], t};
+  for (int b = 0; b < bv.batch; ++b) {
+    if (!((vis >> b) & 1u)) continue;  // culled in this view
+    const float* g2 = bv.grad2d[b];
+    const float4 g0 = ldg4(g2, 3 * i + 0), g1 = ldg4(g2, 3 * i + 1), g2v = ldg4(g2, 3 * i + 2);
+    Fwd f;
+    if (!project_core(src, bv.k[b], f)) continue;
+    seen = true;
+    BwdOut o;
+    project_bwd_core(src, bv.k[b], bv.campos[b], f, g0, g1, g2v, o);
+    ga.x += o.gm[0]; ga.y += o.gm[1]; ga.z += o.gm[2]; ga.w += o.glogit;
+    gl.x += o.gls[0]; gl.y += o.gls[1]; gl.z += o.gls[2];
+    gq.x += o.gq.x; gq.y += o.gq.y; gq.z += o.gq.z; gq.w += o.gq.w;
+#pragma unroll
+    for (int fidx = 0; fidx < 48; ++fidx) s_sh[fidx][t] += o.gcol[fidx % 3] * o.b.y[fidx / 3];
+  }
+  if (!seen) return;  // not visible in any view of the batch: untouched
+  float4* P = reinterpret_cast<float4*>(params);
+  // planes in groups of three: the six moment loads of a group are in flight together
+#pragma unroll 1
+  for (int pl0 = 0; pl0 < 15; pl0 += 3) {
+    float4 pp[3], mm[3], vv[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int64_t e = (int64_t)(pl0 + j) * n + i;
+      pp[j] = S.par[pl0 + j][t];
+      mm[j] = m[e];
+      vv[j] = v[e];
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int pl = pl0 + j;
+      float4 g;
+      if (pl == 0) g = ga;
+      else if (pl == 1) g = gl;
+      else if (pl == 2) g = gq;
+      else g = make_float4(s_sh[4 * (pl - 3)][t], s_sh[4 * (pl - 3) + 1][t], s_sh[4 * (pl - 3) + 2][t],
+                           s_sh[4 * (pl - 3) + 3][t]);
+      adam4(pp[j], mm[j], vv[j], g, h);
+      const int64_t e = (int64_t)pl * n + i;
+      P[e] = pp[j];
+      m[e] = mm[j];
+      v[e] = vv[j];
+    }
   }
 }
 
@@ -397,4 +548,47 @@ extern "C" gs_status gs_project_bwd(const float* params, int64_t n, const gs_cam
   k_project_bwd<<<blocks, threads, 0, gs::as_stream(stream)>>>(params, n, k, camera_centre(*cam), proj, grad2d,
                                                                grads);
   return gs::check_launch("gs_project_bwd");
+}
+
+extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_camera* cams, int batch,
+                                         const float* const* proj_per_view, const float* const* grad2d_per_view,
+                                         float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
+                                         float eps, int64_t step, const int64_t* counts, int n_counts,
+                                         void* stream) {
+  if (batch < 1 || batch > kMaxBatchViews)
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: batch must be 1..%d", kMaxBatchViews);
+  if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: bad n");
+  if (step < 1) return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: step must be >= 1");
+  if (!cams || !proj_per_view || !grad2d_per_view)
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: NULL pointer");
+  if (n == 0) return GS_OK;
+  if (!params || !exp_avg || !exp_avg_sq || (n_counts > 0 && !counts))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: NULL pointer");
+  if (n_counts < 0 || !counts) n_counts = 0;
+  if (!gs::aligned16(params) || !gs::aligned16(exp_avg) || !gs::aligned16(exp_avg_sq))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: planes must be 16-byte aligned");
+  BatchViews bv{};
+  bv.batch = batch;
+  for (int b = 0; b < batch; ++b) {
+    if (gs_status s = gs::check_camera(&cams[b])) return s;
+    if (!proj_per_view[b] || !grad2d_per_view[b] || !gs::aligned16(proj_per_view[b]) ||
+        !gs::aligned16(grad2d_per_view[b]))
+      return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: view %d proj/grad2d NULL or misaligned", b);
+    bv.k[b] = gs::make_cam(cams[b]);
+    bv.campos[b] = camera_centre(cams[b]);
+    bv.proj[b] = proj_per_view[b];
+    bv.grad2d[b] = grad2d_per_view[b];
+  }
+  // batch scaling rule: lr sqrt(b), beta^b; bias corrections with the scaled betas
+  const double b1 = std::pow((double)beta1, batch), b2 = std::pow((double)beta2, batch);
+  const double lr_b = (double)lr * std::sqrt((double)batch);
+  const double bc1 = 1.0 - std::pow(b1, (double)step), bc2 = 1.0 - std::pow(b2, (double)step);
+  const AdamHyper h{(float)b1, (float)b2, (float)lr_b, (float)bc1, (float)bc2, eps};
+  const unsigned blocks = (unsigned)((n + kAdamThreads - 1) / kAdamThreads);
+  static const cudaError_t attr = cudaFuncSetAttribute(k_project_bwd_adam, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)sizeof(AdamSmem));
+  if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_project_bwd_adam: %s", cudaGetErrorString(attr));
+  k_project_bwd_adam<<<blocks, kAdamThreads, sizeof(AdamSmem), gs::as_stream(stream)>>>(
+      params, n, bv, reinterpret_cast<float4*>(exp_avg), reinterpret_cast<float4*>(exp_avg_sq), h, counts, n_counts);
+  return gs::check_launch("gs_project_bwd_adam");
 }

@@ -4,13 +4,16 @@
 as torch tensors -- torch supplies memory and the stream, every computation is a libgs.so
 kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
 training flow (训练流程): for each view project -> bin/sort -> composite -> loss ->
-composite backward -> projection backward; then the visible sets and the visible-only
-Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch scaling).
+composite backward; then the visible sets, and the projection backward of every view
+with the visible-only Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch
+scaling) in one fused pass (gs_project_bwd_adam) whose gradients never leave the chip.
+``step_async(..., adam=False)`` runs the per-view gs_project_bwd instead and leaves the
+summed gradients in ``grads``.
 
 The step never synchronises with the host.  The tile-instance buffers have a capacity;
-when a view overflows it, gs_sparse_adam skips the update (it reads the per-view status
-words), ``step`` notices on its one readback of the loss, grows the buffers and runs the
-batch again.
+when a view overflows it, the update skips itself (it reads the per-view status words),
+``step`` notices on its one readback of the loss, grows the buffers and runs the batch
+again.
 """
 from __future__ import annotations
 
@@ -22,7 +25,10 @@ from . import _native as N
 
 # kernels each entry point launches (memset nodes are not counted)
 LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_bwd": 1, "visible_sets": 7,
-            "sparse_adam": 1}
+            "sparse_adam": 1, "project_bwd_adam": 1}
+
+
+MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
 
 def bin_sort_launches(cam) -> int:
@@ -59,7 +65,7 @@ class Trainer:
         tiles = ((width + 15) // 16) * ((height + 15) // 16)
         f32, i32, i64 = torch.float32, torch.int32, torch.int64
         self.proj = torch.zeros((batch, 3, n, 4), dtype=f32, device=dev)
-        self.grad2d = torch.zeros((n, 12), dtype=f32, device=dev)
+        self.grad2d = torch.zeros((batch, n, 12), dtype=f32, device=dev)  # per view
         self.image = torch.zeros((3, height, width), dtype=f32, device=dev)
         self.T_final = torch.zeros((height, width), dtype=f32, device=dev)
         self.n_contrib = torch.zeros((height, width), dtype=i32, device=dev)
@@ -153,6 +159,7 @@ class Trainer:
         inv_b = 1.0 / B
         launches = 0
         T = self._timed
+        fused = adam and B <= MAX_FUSED_BATCH
         for b, cam in enumerate(cams):
             proj = self.proj[b]
             T("project", N.gs_project, self.params, n, cam, proj)
@@ -167,17 +174,23 @@ class Trainer:
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               self.dimg, self.loss_ws, self.loss_ws.numel())
             T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
-              self.n_contrib, self.dimg, self.grad2d)
-            T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d, self.grads)
+              self.n_contrib, self.dimg, self.grad2d[b])
+            if not fused:
+                T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads)
+                launches += LAUNCHES["project_bwd"]
             if self.work is not None:
                 # (entries evaluated in the forward, entries accumulated, entries walked by the backward)
                 self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum())))
-            launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in
-                                                     ("project", "render_fwd", "loss", "render_bwd", "project_bwd"))
+            launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in ("project", "render_fwd", "loss", "render_bwd"))
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
           self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard)
         launches += LAUNCHES["visible_sets"]
-        if adam:
+        if fused:
+            T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, list(cams), [self.proj[b] for b in range(B)],
+              [self.grad2d[b] for b in range(B)], self.exp_avg, self.exp_avg_sq, self.lr, self.betas[0],
+              self.betas[1], self.eps, self.t + 1, self.counts, B)
+            launches += LAUNCHES["project_bwd_adam"]
+        elif adam:
             T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,
               self.union_idx, self.n_union, n, self.lr, self.betas[0], self.betas[1], self.eps, B, self.t + 1,
               self.counts, B)

@@ -3,7 +3,8 @@
  *
  * One training step over a batch of B views is, per view:
  *   gs_project -> gs_bin_sort -> gs_render_fwd -> gs_loss -> gs_render_bwd -> gs_project_bwd
- * and, once per batch, gs_visible_sets -> gs_sparse_adam.
+ * and, once per batch, gs_visible_sets -> gs_sparse_adam (or, fusing the per-view
+ * gs_project_bwd calls with the update, gs_project_bwd_adam once per batch).
  * The step follows the training flow of the Grendel-GS notes ("训练流程": transform,
  * render by depth-sorted alpha compositing, L1 + SSIM loss, backpropagation, update)
  * with the visible-only update of the Odin summary ("研究背景与动机": a view renders,
@@ -225,6 +226,26 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
                          const uint32_t* idx, const int64_t* n_idx, int64_t max_idx, float lr,
                          float beta1, float beta2, float eps, int batch, int64_t step,
                          const int64_t* counts, int n_counts, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_project_bwd_adam -- the batch's backward projection and its update in one pass:
+ * exactly gs_project_bwd for every view b (gradients summed in view order, starting from
+ * zero) followed by gs_sparse_adam over the Gaussians with radius > 0 in at least one view
+ * (the union of the visible sets), except that the gradient planes are never written.
+ * The pages have no counterpart for this entry point as a separate call: it is the
+ * composition of the two steps above, fused so that the gradients stay on chip.
+ *   cams, proj_per_view, grad2d_per_view  HOST arrays of `batch` entries (the latter two
+ *              hold device pointers); batch in [1, 16].
+ *   exp_avg, exp_avg_sq  Adam moments [15][n][4]; lr, beta1, beta2, eps, step as for
+ *              gs_sparse_adam (batch scaling rule included); counts/n_counts likewise
+ *              (any nonzero status word skips the whole update).
+ * Gaussians visible in no view keep p, m and v bit-for-bit.
+ */
+gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_camera* cams, int batch,
+                              const float* const* proj_per_view, const float* const* grad2d_per_view,
+                              float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
+                              float eps, int64_t step, const int64_t* counts, int n_counts,
+                              void* stream);
 
 /* ---------------------------------------------------------------------------
  * Test hooks (no counterpart in the method).

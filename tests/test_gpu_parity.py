@@ -356,6 +356,73 @@ def test_sparse_adam_parity_and_skip():
     assert (host(tp) == before).all()
 
 
+# ------------------------------------------------------------------ batched backward + Adam
+def test_project_bwd_adam_parity_and_skip():
+    """gs_project_bwd_adam == sum over views of the oracle's projection backward, then the
+    oracle's sparse Adam over the union of the visible sets."""
+    P, cam0 = scene(1, 40_000, 0)
+    P[0, :50, :3] = [0.0, 1e5, 0.0]  # far outside every view: must stay untouched
+    n = P.shape[1]
+    cams = [scenes.make_cameras(1)[v] for v in (0, 9, 17, 30)]
+    rng = np.random.default_rng(21)
+    planes, g2ds, G = [], [], np.zeros((15, n, 4))
+    ok = np.ones(n, bool)
+    vis_any = np.zeros(n, bool)
+    for cam in cams:
+        pr = oracle.project(P, cam)
+        vis = pr["radius"] > 0
+        ok &= pr["margin"] >= MARGIN
+        ok &= (np.abs(pr["raw"]) > 1e-4).all(axis=1) | ~vis
+        vis_any |= vis
+        g2d = (rng.normal(0, 1e-3, size=(n, 9)) * vis[:, None]).astype(np.float32).astype(np.float64)
+        planes.append(proj_planes_from_oracle(pr))
+        g2ds.append(g2d)
+    for cam, g2d in zip(cams, g2ds):
+        g2d[~ok] = 0  # Gaussians near a discrete decision in some view carry no gradient
+        G += oracle.project_bwd(P, cam, g2d)
+    union = np.nonzero(vis_any)[0].astype(np.uint32)
+    M = rng.normal(0, 1e-4, size=(15, n, 4)).astype(np.float32)
+    V = np.abs(rng.normal(0, 1e-6, size=(15, n, 4))).astype(np.float32)
+    ref_p, _, ref_m, ref_v = oracle.sparse_adam(P, G, M, V, union, 1e-3, 0.9, 0.999, 1e-15, len(cams), 5)
+    tp, tm, tv = dev(P), dev(M), dev(V)
+    dplanes = [dev(q) for q in planes]
+    dg = []
+    for g2d in g2ds:
+        lay = np.zeros((n, 12), np.float32)
+        lay[:, [0, 1, 4, 5, 6, 2, 8, 9, 10]] = g2d
+        dg.append(dev(lay))
+    counts = torch.zeros((len(cams), 2), dtype=torch.int64, device="cuda")
+    N.gs_project_bwd_adam(tp, n, cams, dplanes, dg, tm, tv, 1e-3, 0.9, 0.999, 1e-15, 5, counts, len(cams))
+    torch.cuda.synchronize()
+    cmp = ok & vis_any
+    # the gradient floor of the projection backward (ATOL) enters m scaled by 1 - beta1^B and
+    # v by (1 - beta2^B) * 2|g|
+    b1B, b2B = 1 - 0.9 ** len(cams), 1 - 0.999 ** len(cams)
+    for name, got, want, floor in (("m", tm, ref_m, b1B * ATOL), ("v", tv, ref_v, b2B * 2 * np.abs(G) * ATOL + 1e-12)):
+        floor = floor if np.isscalar(floor) else floor[:, cmp]
+        bad = allclose_grad(host(got)[:, cmp], want[:, cmp], RTOL, floor)
+        report(f"project_bwd_adam {name}", int(bad.sum()), bad.size)
+        assert bad.sum() == 0
+    pn = host(tp).astype(np.float64)
+    d_gpu, d_ref = (pn - P)[:, cmp], (ref_p - P)[:, cmp]
+    tol = RTOL * np.abs(d_ref) + 2.0 ** -22 * np.maximum(np.abs(P[:, cmp]), np.abs(pn[:, cmp])) + 1e-9
+    bad = np.abs(d_gpu - d_ref) > tol
+    report("project_bwd_adam params", int(bad.sum()), bad.size)
+    assert bad.sum() == 0
+    # visible in no view: parameters and moments bit-for-bit untouched
+    none = ~vis_any
+    assert none.any()
+    assert (host(tp)[:, none] == P[:, none]).all() and (host(tm)[:, none] == M[:, none]).all()
+    assert (host(tv)[:, none] == V[:, none]).all()
+    # a view with a nonzero status word: the whole update is skipped
+    counts[3, 1] = 1
+    before = [host(t).copy() for t in (tp, tm, tv)]
+    N.gs_project_bwd_adam(tp, n, cams, dplanes, dg, tm, tv, 1e-3, 0.9, 0.999, 1e-15, 6, counts, len(cams))
+    torch.cuda.synchronize()
+    for t, b in zip((tp, tm, tv), before):
+        assert (host(t) == b).all()
+
+
 # ------------------------------------------------------------------ visible sets
 @pytest.mark.parametrize("B,n", [(1, 1000), (4, 70_001), (16, 100_000)])
 def test_visible_sets_bit_exact(B, n):
