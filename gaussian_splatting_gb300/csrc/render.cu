@@ -66,10 +66,26 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
     const float hy = sqrtf(K * q1.x / det) * 1.001f + 0.05f;
     const float xmin = (float)tile_x0 + 0.5f, xmax = (float)tile_x0 + 15.5f;
     if (q0.x + hx >= xmin && q0.x - hx <= xmax) {
+      // Then the exact test: the minimum of q(d) = A dx^2 + 2B dx dy + C dy^2 over the block's
+      // rectangle of pixel centres (d relative to the mean) against K.  q is convex; its
+      // minimum over the column strip [X0, X1] lies at dx = 0 when the strip holds the mean,
+      // else on the nearer edge X at dy = -B X / C; clamping that dy to the block's rows and
+      // then dx to the columns gives the minimum over the rectangle.  The margin keeps every
+      // block whose pixels the fp32 candidate test could accept.
+      const float A = q1.x, B = q1.y, C = q1.z;
+      const float X0 = xmin - q0.x, X1 = xmax - q0.x;
+      const float xe = X0 > 0.f ? X0 : (X1 < 0.f ? X1 : 0.f);
+      const float dys = -B * xe / C, rBA = -B / A;
+      const float Kk = K * 1.001f + 1e-3f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float ymin = (float)(tile_y0 + 4 * w) + 0.5f, ymax = ymin + 3.0f;
-        if (q0.y + hy >= ymin && q0.y - hy <= ymax) m |= 1u << w;
+        if (q0.y + hy >= ymin && q0.y - hy <= ymax) {
+          const float dy = fminf(fmaxf(dys, ymin - q0.y), ymax - q0.y);
+          const float dx = fminf(fmaxf(rBA * dy, X0), X1);
+          const float q = A * dx * dx + 2.f * B * dx * dy + C * dy * dy;
+          if (q <= Kk) m |= 1u << w;
+        }
       }
     }
   } else if (!(det > 0.f) && K > 0.f) {
@@ -162,41 +178,60 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
     for (int q0 = 0; q0 < nl && !warp_done; q0 += 16) {
       const int qend = min(nl, q0 + 16);
       bool ended = false;
-      for (int q = q0; q < qend; ++q) {
-        const int k = S.list[warp][q];
-        const float4 a = S.s0[k];
-        const float4 c = S.s1[k];
-        const Col cl = column(a, fx - a.x);
-        float p[kPPT];
-        bool hit[kPPT];
+      // two entries per iteration: both candidate tests are independent of the compositing
+      // state, so they are issued together; the entries are then composited in list order
+      for (int q = q0; q < qend; q += 2) {
+        const bool has1 = q + 1 < qend;
+        const int k0 = S.list[warp][q];
+        const int k1 = has1 ? S.list[warp][q + 1] : k0;
+        const float4 a0 = S.s0[k0], c0 = S.s1[k0];
+        const float4 a1 = S.s0[k1], c1 = S.s1[k1];
+        const Col cl0 = column(a0, fx - a0.x);
+        const Col cl1 = column(a1, fx - a1.x);
+        float p0[kPPT], p1[kPPT];
+        bool h0[kPPT], h1[kPPT];
 #pragma unroll
         for (int i = 0; i < kPPT; ++i) {
-          p[i] = power2(cl, c.x, fy[i] - a.y);
-          hit[i] = candidate(p[i], c.z);
+          p0[i] = power2(cl0, c0.x, fy[i] - a0.y);
+          p1[i] = power2(cl1, c1.x, fy[i] - a1.y);
+          h0[i] = candidate(p0[i], c0.z);
+          h1[i] = has1 && candidate(p1[i], c1.z);
         }
-        if (!(hit[0] || hit[1])) continue;
-        const float4 col = S.s2[k];
-        const uint32_t pos = b0 - start + (uint32_t)k;
 #pragma unroll
-        for (int i = 0; i < kPPT; ++i) {
-          if (!hit[i]) continue;
-          const float alpha = alpha_of(c.y, fast_exp2(p[i]));
-          if (alpha < kAlphaMin) continue;
-          const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
-          if (Tn < kTMin) {
-            done[i] = true;
-            fy[i] = kParkedRow;
-            stop[i] = pos + 1u;
-            ended = true;
-            continue;
+        for (int e = 0; e < 2; ++e) {
+          const int k = e ? k1 : k0;
+          const float4 c = e ? c1 : c0;
+          bool hit[kPPT];
+          float p[kPPT];
+#pragma unroll
+          for (int i = 0; i < kPPT; ++i) {
+            hit[i] = (e ? h1[i] : h0[i]) && !done[i];  // a pixel may have finished on entry 0
+            p[i] = e ? p1[i] : p0[i];
           }
-          const float w = alpha * T[i];
-          cr[i] = fmaf(w, col.x, cr[i]);
-          cg[i] = fmaf(w, col.y, cg[i]);
-          cb[i] = fmaf(w, col.z, cb[i]);
-          T[i] = Tn;
-          last[i] = pos + 1u;
-          if (kCount) ++used[i];
+          if (!(hit[0] || hit[1])) continue;
+          const float4 col = S.s2[k];
+          const uint32_t pos = b0 - start + (uint32_t)k;
+#pragma unroll
+          for (int i = 0; i < kPPT; ++i) {
+            if (!hit[i]) continue;
+            const float alpha = alpha_of(c.y, fast_exp2(p[i]));
+            if (alpha < kAlphaMin) continue;
+            const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
+            if (Tn < kTMin) {
+              done[i] = true;
+              fy[i] = kParkedRow;
+              stop[i] = pos + 1u;
+              ended = true;
+              continue;
+            }
+            const float w = alpha * T[i];
+            cr[i] = fmaf(w, col.x, cr[i]);
+            cg[i] = fmaf(w, col.y, cg[i]);
+            cb[i] = fmaf(w, col.z, cb[i]);
+            T[i] = Tn;
+            last[i] = pos + 1u;
+            if (kCount) ++used[i];
+          }
         }
       }
       if (__any_sync(0xffffffffu, ended)) warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
