@@ -349,69 +349,96 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
     __syncthreads();
     build_list(S, cnt, warp, lane);
     const int nl = (int)S.count[warp];
-    for (int q = nl - 1; q >= 0; --q) {
-      const int k = S.list[warp][q];
-      const uint32_t pos = (uint32_t)bb * kBatch + (uint32_t)k;  // list position
-      if (pos >= warp_max) continue;                             // warp-uniform
-      const float4 a = S.s0[k];
-      const float4 c = S.s1[k];
-      const float dx = fx - a.x;
-      const Col cl = column(a, dx);
-      float p[kPPT];
-      bool hit[kPPT];
+    // two entries per iteration, walked back to front: both candidate tests first (they do
+    // not depend on the running state), then the entries in reverse list order
+    for (int q = nl - 1; q >= 0; q -= 2) {
+      const bool has1 = q >= 1;
+      const int k0 = S.list[warp][q];
+      const int k1 = has1 ? S.list[warp][q - 1] : k0;
+      const uint32_t pos0 = (uint32_t)bb * kBatch + (uint32_t)k0;  // list positions
+      const uint32_t pos1 = (uint32_t)bb * kBatch + (uint32_t)k1;
+      const float4 a0 = S.s0[k0], c0 = S.s1[k0];
+      const float4 a1 = S.s0[k1], c1 = S.s1[k1];
+      const Col cl0 = column(a0, fx - a0.x);
+      const Col cl1 = column(a1, fx - a1.x);
+      float p0[kPPT], p1[kPPT];
+      bool h0[kPPT], h1[kPPT];
 #pragma unroll
       for (int i = 0; i < kPPT; ++i) {
-        p[i] = power2(cl, c.x, fy[i] - a.y);
-        hit[i] = pos < last[i] && candidate(p[i], c.z);
+        p0[i] = power2(cl0, c0.x, fy[i] - a0.y);
+        p1[i] = power2(cl1, c1.x, fy[i] - a1.y);
+        h0[i] = pos0 < last[i] && candidate(p0[i], c0.z);
+        h1[i] = has1 && pos1 < last[i] && candidate(p1[i], c1.z);
       }
-      const bool any = hit[0] || hit[1];
-      if (!__any_sync(0xffffffffu, any)) continue;
-      // acc: du, dv, dopacity, dA, dB, dC, dr, dg (transposed); db separately
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float acc_b = 0.f;
-      if (any) {
-        const float4 col = S.s2[k];
-        // natural conic from the log2-scaled record
-        const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int k = e ? k1 : k0;
+        const float4 a = e ? a1 : a0;
+        const float4 c = e ? c1 : c0;
+        bool hit[kPPT];
+        float p[kPPT];
 #pragma unroll
         for (int i = 0; i < kPPT; ++i) {
-          if (!hit[i]) continue;
-          const float G = fast_exp2(p[i]);
-          const float alpha = alpha_of(c.y, G);
-          if (alpha < kAlphaMin) continue;
-          const float dy = fy[i] - a.y;
-          const float iom = rcp_approx(__fsub_rn(1.f, alpha));
-          T[i] = T[i] * iom;
-          const float w = alpha * T[i];
-          acc[6] = fmaf(w, dr[i], acc[6]);
-          acc[7] = fmaf(w, dg[i], acc[7]);
-          acc_b = fmaf(w, db[i], acc_b);
-          const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
-                               (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) * iom;
-          Sr[i] = fmaf(w, col.x, Sr[i]);
-          Sg[i] = fmaf(w, col.y, Sg[i]);
-          Sb[i] = fmaf(w, col.z, Sb[i]);
-          if (__fmul_rn(c.y, G) <= kAlphaMax) {
-            acc[2] = fmaf(dalpha, G, acc[2]);
-            const float dpow = dalpha * alpha;  // d alpha / d power = alpha
-            acc[3] = fmaf(-0.5f * dpow, dx * dx, acc[3]);
-            acc[4] = fmaf(-dpow, dx * dy, acc[4]);
-            acc[5] = fmaf(-0.5f * dpow, dy * dy, acc[5]);
-            acc[0] = fmaf(dpow, A * dx + B * dy, acc[0]);
-            acc[1] = fmaf(dpow, B * dx + C * dy, acc[1]);
-          }
+          hit[i] = e ? h1[i] : h0[i];
+          p[i] = e ? p1[i] : p0[i];
         }
-      }
-      const float tot = warp_transpose_sum8(acc, lane);
-      const float tot_b = warp_sum(acc_b);
-      // lanes 4k hold value k of (du, dv, dopacity, dA, dB, dC, dr, dg); lane 1 adds db
-      const uint32_t g = __float_as_uint(c.w);
-      float* rec = grad2d + 12 * (int64_t)g;
-      if ((lane & 3) == 0) {
-        const int kv = lane >> 2;
-        atomicAdd(rec + kv + (kv >= 3 ? 1 : 0) + (kv >= 6 ? 1 : 0), tot);
-      } else if (lane == 1) {
-        atomicAdd(rec + 10, tot_b);
+        const bool any = hit[0] || hit[1];
+        if (!__any_sync(0xffffffffu, any)) continue;
+        // acc: du, dv, dopacity, dA, dB, dC, dr, dg (transposed); db separately
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float acc_b = 0.f;
+        if (any) {
+          const float4 col = S.s2[k];
+          const float dx = fx - a.x;
+          // moments over the thread's pixels (one column): sum dpow, dpow dy, dpow dy^2
+          float m0 = 0.f, m1 = 0.f, m2 = 0.f;
+#pragma unroll
+          for (int i = 0; i < kPPT; ++i) {
+            if (!hit[i]) continue;
+            const float G = fast_exp2(p[i]);
+            const float alpha = alpha_of(c.y, G);
+            if (alpha < kAlphaMin) continue;
+            const float dy = fy[i] - a.y;
+            const float iom = rcp_approx(__fsub_rn(1.f, alpha));
+            T[i] = T[i] * iom;
+            const float w = alpha * T[i];
+            acc[6] = fmaf(w, dr[i], acc[6]);
+            acc[7] = fmaf(w, dg[i], acc[7]);
+            acc_b = fmaf(w, db[i], acc_b);
+            const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
+                                 (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) * iom;
+            Sr[i] = fmaf(w, col.x, Sr[i]);
+            Sg[i] = fmaf(w, col.y, Sg[i]);
+            Sb[i] = fmaf(w, col.z, Sb[i]);
+            if (__fmul_rn(c.y, G) <= kAlphaMax) {
+              acc[2] = fmaf(dalpha, G, acc[2]);
+              const float dpow = dalpha * alpha;  // d alpha / d power = alpha
+              const float t = dpow * dy;
+              m0 += dpow;
+              m1 += t;
+              m2 = fmaf(t, dy, m2);
+            }
+          }
+          // power = -(A dx^2 + C dy^2)/2 - B dx dy, natural conic from the log2-scaled record
+          const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
+          const float dxm0 = dx * m0;
+          acc[3] = -0.5f * dx * dxm0;
+          acc[4] = -dx * m1;
+          acc[5] = -0.5f * m2;
+          acc[0] = fmaf(A, dxm0, B * m1);
+          acc[1] = fmaf(B, dxm0, C * m1);
+        }
+        const float tot = warp_transpose_sum8(acc, lane);
+        const float tot_b = warp_sum(acc_b);
+        // lanes 4k hold value k of (du, dv, dopacity, dA, dB, dC, dr, dg); lane 1 adds db
+        const uint32_t g = __float_as_uint(c.w);
+        float* rec = grad2d + 12 * (int64_t)g;
+        if ((lane & 3) == 0) {
+          const int kv = lane >> 2;
+          atomicAdd(rec + kv + (kv >= 3 ? 1 : 0) + (kv >= 6 ? 1 : 0), tot);
+        } else if (lane == 1) {
+          atomicAdd(rec + 10, tot_b);
+        }
       }
     }
   }
