@@ -39,13 +39,14 @@ struct LossSmem {
     float h5[5][kIn][kMid];
     float h3[3][kMid][kOut + 1];  // padded row: the row-blocked writes of phase C hit distinct banks
   } u2;
+  float core[2][kOut][kOut];  // image and target on the output tile
   float red[2][kThreads / 32];
 };
 
 // Register-blocked window sums: a thread produces R consecutive outputs along the blur
 // direction from R + 10 loaded inputs (sliding window), instead of 11 loads per output.
 constexpr int kRA = 6;  // horizontal blur of the statistics: 42 = 7 x 6 outputs per row
-constexpr int kRB = 6;  // vertical blur of the statistics: 42 = 7 x 6 outputs per column
+constexpr int kRB = 7;  // vertical blur of the statistics: 42 = 6 x 7 outputs per column
 constexpr int kRC = 4;  // horizontal blur of the derivative maps: 32 = 8 x 4 per row
 constexpr int kRD = 4;  // vertical blur of the derivative maps: 32 = 8 x 4 per column
 
@@ -64,17 +65,36 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
   float w[11];
 #pragma unroll
   for (int t = 0; t < 11; ++t) w[t] = win.w[t];
-  // ---- A: load with 10-px halo (zero outside the image)
-  for (int e = tid; e < kIn * kIn; e += kThreads) {
-    const int r = e / kIn, c = e % kIn;
-    const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
-    float xv = 0.f, yv = 0.f;
-    if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
-      xv = __ldg(&X[(int64_t)gy * W + gx]);
-      yv = __ldg(&Y[(int64_t)gy * W + gx]);
+  // ---- A: load with 10-px halo (zero outside the image); all loads of a thread in flight
+  // together, the output tile's own pixels also kept aside for the last stage
+  constexpr int kLoadIters = (kIn * kIn + kThreads - 1) / kThreads;
+  {
+    float xv[kLoadIters], yv[kLoadIters];
+#pragma unroll
+    for (int it = 0; it < kLoadIters; ++it) {
+      const int e = tid + it * kThreads;
+      const int r = e / kIn, c = e % kIn;
+      const int gy = oy - 2 * kR + r, gx = ox - 2 * kR + c;
+      xv[it] = yv[it] = 0.f;
+      if (e < kIn * kIn && gx >= 0 && gx < W && gy >= 0 && gy < H) {
+        xv[it] = __ldg(&X[(int64_t)gy * W + gx]);
+        yv[it] = __ldg(&Y[(int64_t)gy * W + gx]);
+      }
     }
-    S.u1.in.x[r][c] = xv;
-    S.u1.in.y[r][c] = yv;
+#pragma unroll
+    for (int it = 0; it < kLoadIters; ++it) {
+      const int e = tid + it * kThreads;
+      if (e < kIn * kIn) {
+        const int r = e / kIn, c = e % kIn;
+        S.u1.in.x[r][c] = xv[it];
+        S.u1.in.y[r][c] = yv[it];
+        const int cr = r - 2 * kR, cc = c - 2 * kR;
+        if (cr >= 0 && cr < kOut && cc >= 0 && cc < kOut) {
+          S.core[0][cr][cc] = xv[it];
+          S.core[1][cr][cc] = yv[it];
+        }
+      }
+    }
   }
   __syncthreads();
   // horizontal window sums of x, y, x^2, y^2, xy: 52 rows x 42 columns, kRA per thread
@@ -109,8 +129,8 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
   // ---- B: vertical window sums -> SSIM statistics on the 42x42 region; map + derivatives
   constexpr float C1 = 0.01f * 0.01f, C2 = 0.03f * 0.03f;
   constexpr int kSegB = kMid / kRB;
-  constexpr int kItemsB = kMid * kSegB;                         // 294
-  constexpr int kRoundsB = (kItemsB + kThreads - 1) / kThreads;  // 2
+  constexpr int kItemsB = kMid * kSegB;                         // 252
+  constexpr int kRoundsB = (kItemsB + kThreads - 1) / kThreads;  // 1
   float ssim_sum = 0.f;
   float dv[kRoundsB][kRB][3];
 #pragma unroll
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
       const int gy = oy + r0 + q;
       if (gx >= W || gy >= H) continue;
       const int64_t g = (int64_t)gy * W + gx;
-      const float xv = __ldg(&X[g]), yv = __ldg(&Y[g]);
+      const float xv = S.core[0][r0 + q][c], yv = S.core[1][r0 + q][c];
       const float diff = xv - yv;
       l1_sum += fabsf(diff);
       const float sgn = diff > 0.f ? 1.f : (diff < 0.f ? -1.f : 0.f);
