@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
   const float fx = (float)px + 0.5f;
   const uint32_t start = ranges[2 * tile], end = ranges[2 * tile + 1];
   const int64_t P = (int64_t)W * H;
-  float fy[kPPT], T[kPPT], dr[kPPT], dg[kPPT], db[kPPT], Sr[kPPT], Sg[kPPT], Sb[kPPT];
+  float fy[kPPT], T[kPPT], dr[kPPT], dg[kPPT], db[kPPT], U[kPPT];
   uint32_t last[kPPT];
   uint32_t my_max = 0;
 #pragma unroll
@@ -324,10 +324,9 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
       dg[i] = dimg[P + pix];
       db[i] = dimg[2 * P + pix];
     }
-    // colour composited behind the current entry, starting with the background
-    Sr[i] = T[i] * bg.x;
-    Sg[i] = T[i] * bg.y;
-    Sb[i] = T[i] * bg.z;
+    // U = (colour composited behind the current entry) . dL/dpixel, starting with the
+    // background; the colour itself is never needed, only its dot product with dL/dpixel
+    U[i] = T[i] * (bg.x * dr[i] + bg.y * dg[i] + bg.z * db[i]);
     my_max = max(my_max, last[i]);
   }
   if (threadIdx.x == 0) s_max_last = 0;
@@ -405,11 +404,9 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
             acc[6] = fmaf(w, dr[i], acc[6]);
             acc[7] = fmaf(w, dg[i], acc[7]);
             acc_b = fmaf(w, db[i], acc_b);
-            const float dalpha = T[i] * (col.x * dr[i] + col.y * dg[i] + col.z * db[i]) -
-                                 (Sr[i] * dr[i] + Sg[i] * dg[i] + Sb[i] * db[i]) * iom;
-            Sr[i] = fmaf(w, col.x, Sr[i]);
-            Sg[i] = fmaf(w, col.y, Sg[i]);
-            Sb[i] = fmaf(w, col.z, Sb[i]);
+            const float cd = col.x * dr[i] + col.y * dg[i] + col.z * db[i];
+            const float dalpha = T[i] * cd - U[i] * iom;
+            U[i] = fmaf(w, cd, U[i]);
             if (__fmul_rn(c.y, G) <= kAlphaMax) {
               acc[2] = fmaf(dalpha, G, acc[2]);
               const float dpow = dalpha * alpha;  // d alpha / d power = alpha
