@@ -35,9 +35,13 @@ UNIT = "views/s"
 # Algorithmic FP32 work of the compositing kernels (FMA = 2 flops), per pixel-Gaussian pair:
 # every evaluated pair costs the offset and the quadratic form (9); an accumulated pair adds
 # the forward blend (10) or the backward chain rule and pixel sum (49).
-FLOPS_EVAL = 9
-FWD_FLOPS_USED = 10
-BWD_FLOPS_USED = 49
+# Algorithmic flops per unit of work (FMA = 2): per pixel-Gaussian pair that the pixel itself
+# evaluates through its termination point, 15 for the forward compositing and 40 for the
+# backward (plus one ex2 each, not counted); about 1.3 kflop per pixel for the loss
+# (5 statistics x 2 passes x 11 taps x 2 flops x 3 channels forward, as much again backward).
+FWD_FLOPS_PER_PAIR = 15
+BWD_FLOPS_PER_PAIR = 40
+LOSS_FLOPS_PER_PIXEL = 1320
 # FP32 peak derived from unit counts: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 HBM_FALLBACK_GBS = 6800.0
@@ -235,6 +239,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     from gaussian_splatting_gb300 import Trainer
+    from gaussian_splatting_gb300 import _native as N
 
     P = scenes.make_params(args.config)
     cams = scenes.make_cameras(args.config)
@@ -268,6 +273,24 @@ def main():
     st = tr.counts.cpu()
     if int(st[:, 1].abs().sum()) != 0:
         raise SystemExit(f"binning overflow during warm-up: {st.tolist()}")
+
+    # ---------------- measured FP32 throughput (FFMA probe), best of three launches
+    fp32_meas = None
+    try:
+        probe_blocks = torch.cuda.get_device_properties(0).multi_processor_count * 8
+        probe_out = torch.empty(probe_blocks * 256, dtype=torch.float32, device="cuda")
+        best = None
+        for _ in range(4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            N.gs_probe_ffma(probe_out, probe_blocks, 4096)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best or 1e9, a.elapsed_time(b))
+        fp32_meas = probe_blocks * 256 * 4096 * 16 / (best / 1e3) / 1e12
+        del probe_out
+    except Exception:
+        fp32_meas = None
 
     # ---------------- timed region (device time, CUDA events per step)
     stream = torch.cuda.current_stream()
@@ -320,10 +343,11 @@ def main():
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
     peak_hbm, hbm_src = hbm_peak()
-    flops = {"render_fwd": FLOPS_EVAL * ev + FWD_FLOPS_USED * used,
-             "render_bwd": FLOPS_EVAL * walked + BWD_FLOPS_USED * used}
-    work_note = (f"per launch: {ev:.4g} pairs evaluated (fwd), {walked:.4g} walked (bwd), {used:.4g} accumulated; "
-                 f"fwd {FLOPS_EVAL}/eval + {FWD_FLOPS_USED}/acc, bwd {FLOPS_EVAL}/walked + {BWD_FLOPS_USED}/acc flops")
+    flops = {"render_fwd": FWD_FLOPS_PER_PAIR * ev, "render_bwd": BWD_FLOPS_PER_PAIR * ev,
+             "loss": LOSS_FLOPS_PER_PIXEL * cfg.width * cfg.height}
+    work_note = (f"per launch: {ev:.4g} pixel-Gaussian pairs evaluated through termination "
+                 f"({used:.4g} accumulated, {walked:.4g} walked back); fwd {FWD_FLOPS_PER_PAIR}, "
+                 f"bwd {BWD_FLOPS_PER_PAIR} flops per evaluated pair")
     # dominant single kernel: the entry points that launch one kernel (gs_bin_sort launches ~11)
     single = [k for k in ("render_bwd", "render_fwd", "project", "project_bwd", "sparse_adam", "project_bwd_adam")
               if k in per_call]
@@ -333,16 +357,19 @@ def main():
         ach = flops[dominant] / (avg[dominant] / 1e3) / 1e12
         roof = {"kernel": "k_" + dominant, "bound": "alu", "achieved": ach, "peak": FP32_PEAK_TFLOPS,
                 "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": measured_traffic(dominant),
-                "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 flop x 2.07 GHz (no measured FP32 peak)",
+                "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 flop x 2.07 GHz",
+                "measured_peak": fp32_meas, "frac_of_measured": ach / fp32_meas if fp32_meas else None,
+                "measured_peak_source": "gs_probe_ffma in this run: 8 FFMA chains per thread, full occupancy",
                 "work": work_note}
     else:
         roof = {"kernel": "k_" + dominant, "bound": "hbm", "achieved": None, "peak": peak_hbm, "unit": "GB/s",
                 "frac": None, "traffic": measured_traffic(dominant), "peak_source": hbm_src}
     others = {}
-    for k in ("render_fwd", "render_bwd"):
-        if k in flops:
+    for k in ("render_fwd", "render_bwd", "loss"):
+        if k in flops and k in avg:
             ach = flops[k] / (avg[k] / 1e3) / 1e12
-            others[k] = {"bound": "alu", "achieved_tflops": round(ach, 3), "frac": round(ach / FP32_PEAK_TFLOPS, 4)}
+            others[k] = {"bound": "alu", "achieved_tflops": round(ach, 3), "frac": round(ach / FP32_PEAK_TFLOPS, 4),
+                         "frac_of_measured": round(ach / fp32_meas, 4) if fp32_meas else None}
     if "project_bwd_adam" in avg:
         # algorithmic bytes: every view's radius word (16 B per Gaussian) and its visible
         # Gaussians' screen-space gradients (48 B); for the updated Gaussians, the parameters

@@ -20,7 +20,7 @@ _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ER
 EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_bin_sort_workspace_size", "gs_bin_sort",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
-           "gs_debug_set_wait_limit",
+           "gs_probe_ffma", "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
 
@@ -77,6 +77,7 @@ def load() -> C.CDLL:
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
         "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp], i32),
+        "gs_probe_ffma": ([vp, i32, i32, vp], i32),
         "gs_debug_set_wait_limit": ([i64], None),
         "gs_debug_drop_publish": ([i32], None),
     }
@@ -209,6 +210,10 @@ def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr
                                       C.cast(garr, C.c_void_p), _ptr(exp_avg), _ptr(exp_avg_sq), lr, beta1, beta2,
                                       eps, step, _ptr(counts), n_counts if counts is not None else 0,
                                       _stream(stream)), "gs_project_bwd_adam")
+
+
+def gs_probe_ffma(out, blocks, iters, stream=None):
+    _check(load().gs_probe_ffma(_ptr(out), blocks, iters, _stream(stream)), "gs_probe_ffma")
 
 
 def gs_debug_set_wait_limit(iterations: int):

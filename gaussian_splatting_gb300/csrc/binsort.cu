@@ -248,6 +248,7 @@ struct SortSmem {
   uint32_t tstart[256];
   uint32_t gbase[256];
   uint32_t wsum[kSortWarps];
+  uint32_t full;  // first tile pass, counts: full cycles of 256 digits
   int fail;
 };
 
@@ -402,6 +403,74 @@ __device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J,
   __syncthreads();  // own[] (= S.keys) is reused by the caller
 }
 
+// Low-byte digit counts of the tile ids that radix tile `tile` of the first tile pass
+// generates, without generating them: the tile holds whole or partial rectangle rows of the
+// Gaussians starting in it (and of the one holding its first slot); a row segment is a run
+// of consecutive tile ids, i.e. a cyclic run of digits, added to a difference array (every
+// full cycle of 256 adds one to every digit).  Leaves the counts in S.tstart.
+template <int ITEMS>
+__device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const RadixJob& J, int64_t tile, int64_t base,
+                                                 int nvalid, int64_t M) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const GenSource& G = J.gen;
+  uint32_t* diff = S.tstart;  // zeroed by the caller
+  if (tid == 0) S.full = 0u;
+  __syncthreads();
+  const int64_t first = (int64_t)__ldg(&G.slice_first[tile]);
+  const uint32_t lo = (uint32_t)base, end = (uint32_t)(base + nvalid);
+  for (int e0 = 0;; e0 += kSortThreads) {
+    const int64_t it = first + e0 + tid;
+    bool more = false;
+    if (it < G.n) {
+      const uint4 rec = __ldg(&G.grec[it]);
+      const uint32_t off = rec.x;
+      more = off < end;
+      if (more || e0 + tid == 0) {
+        const uint32_t next = it + 1 < G.n ? __ldg(&G.grec[it + 1]).x : (uint32_t)M;
+        const uint32_t s_lo = max(off, lo), s_hi = min(next, end);
+        const uint32_t w = max(rec.z, 1u);
+        if (s_lo < s_hi) {
+          const uint32_t x0 = rec.y & 0xffffu, y0 = rec.y >> 16;
+          const uint32_t r0 = (s_lo - off) / w, r1 = (s_hi - 1u - off) / w;
+          for (uint32_t r = r0; r <= r1; ++r) {
+            const uint32_t j_lo = r == r0 ? s_lo - off - r * w : 0u;
+            const uint32_t j_hi = r == r1 ? s_hi - 1u - off - r * w : w - 1u;
+            const uint32_t t_lo = (y0 + r) * (uint32_t)G.Tx + x0 + j_lo;
+            const uint32_t len = j_hi - j_lo + 1u;
+            if (len >> 8) atomicAdd(&S.full, len >> 8);
+            const uint32_t rem = len & 255u, a = t_lo & 255u;
+            if (rem) {
+              atomicAdd(&diff[a], 1u);
+              if (a + rem < 256u) atomicAdd(&diff[a + rem], 0xFFFFFFFFu);
+              else if (a + rem > 256u) {  // wraps: [a, 256) and [0, a + rem - 256)
+                atomicAdd(&diff[0], 1u);
+                atomicAdd(&diff[a + rem - 256u], 0xFFFFFFFFu);
+              }
+            }
+          }
+        }
+      }
+    }
+    if (!__syncthreads_or(more)) break;
+  }
+  // counts = inclusive prefix of the difference array (one digit per thread) + full cycles
+  const uint32_t dv = diff[tid];
+  uint32_t incl = dv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) S.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t woff = 0;
+  for (int w2 = 0; w2 < warp; ++w2) woff += S.wsum[w2];
+  const uint32_t cnt = woff + incl + S.full;
+  __syncthreads();
+  diff[tid] = cnt;
+  __syncthreads();
+}
+
 template <int ITEMS, bool kTileSort>
 __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   constexpr int kTile = kSortThreads * ITEMS;
@@ -427,14 +496,18 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
       __syncthreads();
       const int64_t base = tile * kTile;
       const int nvalid = (int)min((int64_t)kTile, M - base);
-      uint32_t k[ITEMS], v[ITEMS];
-      load_tile<ITEMS>(S, J, gen, kin, vin, tile, base, nvalid, k, v);
+      if (gen) {
+        gen_digit_counts(S, J, tile, base, nvalid, M);
+      } else {
+        uint32_t k[ITEMS], v[ITEMS];
+        load_tile<ITEMS>(S, J, false, kin, vin, tile, base, nvalid, k, v);
 #pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const int li = warp * (ITEMS * 32) + i * 32 + lane;
-        if (li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
+        for (int i = 0; i < ITEMS; ++i) {
+          const int li = warp * (ITEMS * 32) + i * 32 + lane;
+          if (li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
+        }
+        __syncthreads();
       }
-      __syncthreads();
       J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
       __syncthreads();
     }

@@ -248,6 +248,15 @@ gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_camera* cams, i
                               void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_probe_ffma -- measurement utility with no counterpart in the method: `blocks` CTAs of
+ * 256 threads each run `iters` iterations of eight independent fused multiply-adds and
+ * write one float per thread to out[blocks * 256].  The caller times the launch:
+ * blocks * 256 * iters * 16 flops over the elapsed time is the FP32 throughput the
+ * compositing and loss fractions are reported against.
+ */
+gs_status gs_probe_ffma(float* out, int blocks, int iters, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Test hooks (no counterpart in the method).
  * gs_debug_set_wait_limit: iterations a device-side wait (a look-back flag or a grid
  *   barrier) spins before it gives up and reports status bit 2 (default 1 << 22; values
