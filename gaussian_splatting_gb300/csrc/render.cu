@@ -4,8 +4,9 @@
 // pixel composites the depth-sorted Gaussians of its 16x16 tile front to back; the backward
 // walks the same lists back to front.
 //
-// Layout: one 128-thread CTA per tile.  Warp w owns the 16x4 block of rows 4w..4w+3; lane l
-// owns column l % 16 and the two rows 4w + 2 (l / 16) + {0, 1}.  The tile's list is walked in
+// Layout: one 128-thread CTA per tile.  Warp w owns the 8x8 block at column band w % 2 and
+// row band w / 2 (a square block meets fewer footprints than a 16x4 one); lane l owns column
+// l % 8 of the block and its two rows 2 (l / 8) + {0, 1}.  The tile's list is walked in
 // batches of 256 Gaussians gathered into shared memory (2 per thread).  While gathering,
 // each Gaussian gets a 4-bit mask of the warp blocks that the bounding box of its
 // alpha >= 1/255 ellipse touches (enlarged by a rounding slack), and every warp compacts the
@@ -64,27 +65,30 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
   if (K > 0.f && det > 0.f) {
     const float hx = sqrtf(K * q1.z / det) * 1.001f + 0.05f;
     const float hy = sqrtf(K * q1.x / det) * 1.001f + 0.05f;
-    const float xmin = (float)tile_x0 + 0.5f, xmax = (float)tile_x0 + 15.5f;
-    if (q0.x + hx >= xmin && q0.x - hx <= xmax) {
-      // Then the exact test: the minimum of q(d) = A dx^2 + 2B dx dy + C dy^2 over the block's
-      // rectangle of pixel centres (d relative to the mean) against K.  q is convex; its
-      // minimum over the column strip [X0, X1] lies at dx = 0 when the strip holds the mean,
-      // else on the nearer edge X at dy = -B X / C; clamping that dy to the block's rows and
-      // then dx to the columns gives the minimum over the rectangle.  The margin keeps every
-      // block whose pixels the fp32 candidate test could accept.
-      const float A = q1.x, B = q1.y, C = q1.z;
+    // Per warp block (8x8 pixels, block w at column band w & 1, row band w >> 1): the box test,
+    // then the exact test: the minimum of q(d) = A dx^2 + 2B dx dy + C dy^2 over the block's
+    // rectangle of pixel centres (d relative to the mean) against K.  q is convex; its minimum
+    // over the column strip [X0, X1] lies at dx = 0 when the strip holds the mean, else on the
+    // nearer edge X at dy = -B X / C; clamping that dy to the block's rows and then dx to the
+    // columns gives the minimum over the rectangle.  The margin keeps every block whose pixels
+    // the fp32 candidate test could accept.
+    const float A = q1.x, B = q1.y, C = q1.z;
+    const float rBA = -B / A, Kk = K * 1.001f + 1e-3f;
+#pragma unroll
+    for (int bx = 0; bx < 2; ++bx) {
+      const float xmin = (float)(tile_x0 + 8 * bx) + 0.5f, xmax = xmin + 7.0f;
+      if (!(q0.x + hx >= xmin && q0.x - hx <= xmax)) continue;
       const float X0 = xmin - q0.x, X1 = xmax - q0.x;
       const float xe = X0 > 0.f ? X0 : (X1 < 0.f ? X1 : 0.f);
-      const float dys = -B * xe / C, rBA = -B / A;
-      const float Kk = K * 1.001f + 1e-3f;
+      const float dys = -B * xe / C;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float ymin = (float)(tile_y0 + 4 * w) + 0.5f, ymax = ymin + 3.0f;
+      for (int by = 0; by < 2; ++by) {
+        const float ymin = (float)(tile_y0 + 8 * by) + 0.5f, ymax = ymin + 7.0f;
         if (q0.y + hy >= ymin && q0.y - hy <= ymax) {
           const float dy = fminf(fmaxf(dys, ymin - q0.y), ymax - q0.y);
           const float dx = fminf(fmaxf(rBA * dy, X0), X1);
           const float q = A * dx * dx + 2.f * B * dx * dy + C * dy * dy;
-          if (q <= Kk) m |= 1u << w;
+          if (q <= Kk) m |= 1u << (bx + 2 * by);
         }
       }
     }
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
   const int tile = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
-  const int px = tile_x0 + (lane & 15), py0 = tile_y0 + 4 * warp + 2 * (lane >> 4);
+  const int px = tile_x0 + 8 * (warp & 1) + (lane & 7), py0 = tile_y0 + 8 * (warp >> 1) + 2 * (lane >> 3);
   const float fx = (float)px + 0.5f;
   float fy[kPPT];
   const uint32_t start = ranges[2 * tile], end = ranges[2 * tile + 1];
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
   const int tile = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
-  const int px = tile_x0 + (lane & 15), py0 = tile_y0 + 4 * warp + 2 * (lane >> 4);
+  const int px = tile_x0 + 8 * (warp & 1) + (lane & 7), py0 = tile_y0 + 8 * (warp >> 1) + 2 * (lane >> 3);
   const float fx = (float)px + 0.5f;
   const uint32_t start = ranges[2 * tile], end = ranges[2 * tile + 1];
   const int64_t P = (int64_t)W * H;

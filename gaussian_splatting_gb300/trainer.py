@@ -84,6 +84,7 @@ class Trainer:
         self.target_dev = torch.zeros((batch, 3, height, width), dtype=f32, device=dev)
         self.capacity = 0
         self.vals = self.sort_ws = None
+        self.copy_stream = None
         self.launches = 0
         self.timer = None  # list of (name, start event, end event) when timing per call
         self.work = None   # list of per-view work counts when measuring (synchronises)
@@ -153,7 +154,7 @@ class Trainer:
         e.record()
         self.timer.append((name, s, e))
 
-    def _enqueue(self, cams, targets: torch.Tensor, adam: bool = True):
+    def _enqueue(self, cams, targets: torch.Tensor, adam: bool = True, ready=None):
         B = len(cams)
         n, W, H = self.n, self.width, self.height
         inv_b = 1.0 / B
@@ -171,6 +172,8 @@ class Trainer:
                 work_buf = torch.zeros((2, H, W), dtype=torch.int32, device=self.params.device)
             T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
               self.n_contrib, work_buf)
+            if ready is not None:
+                torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               self.dimg, self.loss_ws, self.loss_ws.numel())
             T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
@@ -203,24 +206,44 @@ class Trainer:
         ``targets`` is a device tensor [B, 3, H, W].  The caller must check ``status``
         (all [:, 1] zero) before trusting the update; ``step`` does that for you.
         """
+        return self._step_async(cams, targets, adam, None)
+
+    def _step_async(self, cams, targets, adam, ready):
         if self.capacity == 0:
             self.reserve(cams)
-        self._enqueue(cams, targets, adam)
+        self._enqueue(cams, targets, adam, ready)
         if adam:
             self.t += 1
         return StepResult(self.loss, self.counts)
 
+    def _upload(self, targets: torch.Tensor, B: int):
+        """Copy host targets into target_dev on the side stream; returns one event per view."""
+        if self.copy_stream is None:
+            self.copy_stream = torch.cuda.Stream(device=self.params.device)
+        cs = self.copy_stream
+        cs.wait_stream(torch.cuda.current_stream())  # target_dev no longer read by earlier work
+        events = []
+        with torch.cuda.stream(cs):
+            for b in range(B):
+                self.target_dev[b].copy_(targets[b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                events.append(ev)
+        return events
+
     def step(self, cams, targets: torch.Tensor, adam: bool = True) -> float:
         """One training step over the views ``cams``; returns the batch loss (host float).
 
-        ``targets`` may be a device tensor or a (pinned) host tensor [B, 3, H, W]; host
-        targets are copied in on the current stream.
+        ``targets`` may be a device tensor or a (pinned) host tensor [B, 3, H, W].  Host
+        targets are copied in view by view on a side stream; view b's loss waits only for its
+        own copy, so the uploads overlap the projection, binning and compositing.
         """
+        ready = None
         if targets.device.type != "cuda":
-            self.target_dev[: len(cams)].copy_(targets, non_blocking=True)
+            ready = self._upload(targets, len(cams))
             targets = self.target_dev
         while True:
-            res = self.step_async(cams, targets, adam)
+            res = self._step_async(cams, targets, adam, ready)
             counts = res.status.cpu()
             if int(counts[: len(cams), 1].abs().sum()) == 0:
                 return float(res.loss.item())

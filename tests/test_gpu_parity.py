@@ -484,3 +484,25 @@ def test_full_step_parity_config0():
     bad = allclose_grad(Pn - P, ref["params"] - P, RTOL, 1e-6)[clear]
     report("step params cfg0", int(bad.sum()), bad.size)
     assert bad.sum() <= 1e-4 * bad.size
+
+
+def test_step_with_host_targets_matches_device_targets():
+    """Host targets are uploaded on a side stream, each view's loss waiting for its own copy:
+    the loss is bit-identical to a step given device targets, and the update agrees up to
+    the order of the backward's float atomics."""
+    P = scenes.make_params(1, n=30_000)
+    cams = [scenes.make_cameras(1)[v] for v in (2, 11, 23, 40)]
+    rng = np.random.default_rng(4)
+    tgt = rng.uniform(0, 1, size=(4, 3, cams[0].height, cams[0].width)).astype(np.float32)
+    results = []
+    for on_host in (False, True):
+        tr = Trainer(dev(P), cams[0].width, cams[0].height, 4)
+        t = torch.from_numpy(tgt).pin_memory() if on_host else dev(tgt)
+        loss = tr.step(cams, t)
+        torch.cuda.synchronize()
+        results.append((loss, host(tr.params).astype(np.float64)))
+    assert results[0][0] == results[1][0]
+    d0, d1 = results[0][1] - P, results[1][1] - P
+    bad = np.abs(d1 - d0) > RTOL * np.abs(d0) + 1e-7
+    report("host-target step params", int(bad.sum()), bad.size)
+    assert bad.sum() <= 1e-4 * bad.size
