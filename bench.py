@@ -50,10 +50,10 @@ HBM_FALLBACK_GBS = 6800.0
 # the benchmark workload, keyed by entry point, valid only for the kernel source it was measured
 # on: when the source file's hash differs the figure is reported as null.
 NCU_TRAFFIC = {
-    # profiles/render_object-300k-1236x820.md: 38.292 MB read + 0.005 MB written per launch
+    # profiles/render_object-300k-1236x820.md: 38.334 MB read + 0.014 MB written per launch
     "render_bwd": {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                   "sha256": "5dc2abd692fe4e48424c409df0d9b15387ed179875e532b7e93c674f598178b6",
-                   "bytes": 38297088},
+                   "sha256": "0e30770754b79ca21250eee8fdf0e18b64bf8b3a15c92e6f8a13a914e36ba331",
+                   "bytes": 38348544},
 }
 
 
@@ -90,7 +90,7 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -104,7 +104,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
