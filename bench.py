@@ -339,6 +339,7 @@ def main():
     ev = sum(w[0] for w in tr_w.work) / n_views
     used = sum(w[1] for w in tr_w.work) / n_views
     walked = sum(w[2] for w in tr_w.work) / n_views
+    warp_pairs = sum(w[3] for w in tr_w.work) / n_views
     del tr_w
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
@@ -346,8 +347,8 @@ def main():
     flops = {"render_fwd": FWD_FLOPS_PER_PAIR * ev, "render_bwd": BWD_FLOPS_PER_PAIR * ev,
              "loss": LOSS_FLOPS_PER_PIXEL * cfg.width * cfg.height}
     work_note = (f"per launch: {ev:.4g} pixel-Gaussian pairs evaluated through termination "
-                 f"({used:.4g} accumulated, {walked:.4g} walked back); fwd {FWD_FLOPS_PER_PAIR}, "
-                 f"bwd {BWD_FLOPS_PER_PAIR} flops per evaluated pair")
+                 f"({used:.4g} accumulated, {walked:.4g} walked back; the forward's warps evaluated "
+                 f"{warp_pairs:.4g}); fwd {FWD_FLOPS_PER_PAIR}, bwd {BWD_FLOPS_PER_PAIR} flops per evaluated pair")
     # dominant single kernel: the entry points that launch one kernel (gs_bin_sort launches ~11)
     single = [k for k in ("render_bwd", "render_fwd", "project", "project_bwd", "sparse_adam", "project_bwd_adam")
               if k in per_call]

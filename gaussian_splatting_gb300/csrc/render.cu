@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
   for (int i = 0; i < kPPT; ++i)
     if (done[i]) fy[i] = kParkedRow;
   bool warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
+  uint32_t walked = 0;  // entries of this warp's culled lists walked (the same in every lane)
   for (uint32_t b0 = start; b0 < end; b0 += kBatch) {
     if (__syncthreads_count(warp_done) == kThreads) break;
     const int cnt = (int)min((uint32_t)kBatch, end - b0);
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
       bool ended = false;
       // two entries per iteration: both candidate tests are independent of the compositing
       // state, so they are issued together; the entries are then composited in list order
+      if (kCount) walked += (uint32_t)(qend - q0);
       for (int q = q0; q < qend; q += 2) {
         const bool has1 = q + 1 < qend;
         const int k0 = S.list[warp][q];
@@ -212,29 +214,29 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
             hit[i] = (e ? h1[i] : h0[i]) && !done[i];  // a pixel may have finished on entry 0
             p[i] = e ? p1[i] : p0[i];
           }
-          if (!(hit[0] || hit[1])) continue;
+          if (!__any_sync(0xffffffffu, hit[0] || hit[1])) continue;  // warp-uniform skip
           const float4 col = S.s2[k];
           const uint32_t pos = b0 - start + (uint32_t)k;
+          // branch-free per pixel: a pixel that does not take the entry gets weight 0 and
+          // keeps its state (fmaf(0, c, x) == x)
 #pragma unroll
           for (int i = 0; i < kPPT; ++i) {
-            if (!hit[i]) continue;
             const float alpha = alpha_of(c.y, fast_exp2(p[i]));
-            if (alpha < kAlphaMin) continue;
             const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
-            if (Tn < kTMin) {
-              done[i] = true;
-              fy[i] = kParkedRow;
-              stop[i] = pos + 1u;
-              ended = true;
-              continue;
-            }
-            const float w = alpha * T[i];
+            const bool take = hit[i] && alpha >= kAlphaMin;
+            const bool term = take && Tn < kTMin;  // stop before this entry
+            const bool acc = take && !term;
+            const float w = acc ? alpha * T[i] : 0.f;
             cr[i] = fmaf(w, col.x, cr[i]);
             cg[i] = fmaf(w, col.y, cg[i]);
             cb[i] = fmaf(w, col.z, cb[i]);
-            T[i] = Tn;
-            last[i] = pos + 1u;
-            if (kCount) ++used[i];
+            T[i] = acc ? Tn : T[i];
+            last[i] = acc ? pos + 1u : last[i];
+            if (kCount) used[i] += acc ? 1u : 0u;
+            done[i] = done[i] || term;
+            fy[i] = term ? kParkedRow : fy[i];
+            stop[i] = term ? pos + 1u : stop[i];
+            ended = ended || term;
           }
         }
       }
@@ -256,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
       if (kCount) {
         work[pix] = stop[i];
         work[P + pix] = used[i];
+        work[2 * P + pix] = walked;
       }
     }
   }
@@ -385,49 +388,51 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
           hit[i] = e ? h1[i] : h0[i];
           p[i] = e ? p1[i] : p0[i];
         }
-        const bool any = hit[0] || hit[1];
-        if (!__any_sync(0xffffffffu, any)) continue;
+        if (!__any_sync(0xffffffffu, hit[0] || hit[1])) continue;
         // acc: du, dv, dopacity, dA, dB, dC, dr, dg (transposed); db separately
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float acc[8];
         float acc_b = 0.f;
-        if (any) {
+        {
           const float4 col = S.s2[k];
           const float dx = fx - a.x;
-          // moments over the thread's pixels (one column): sum dpow, dpow dy, dpow dy^2
-          float m0 = 0.f, m1 = 0.f, m2 = 0.f;
+          // moments over the thread's pixels (one column): sum dpow, dpow dy, dpow dy^2.
+          // Branch-free per pixel: a pixel that does not take the entry contributes zeros and
+          // keeps its state.
+          float m0 = 0.f, m1 = 0.f, m2 = 0.f, a6 = 0.f, a7 = 0.f, a2 = 0.f;
 #pragma unroll
           for (int i = 0; i < kPPT; ++i) {
-            if (!hit[i]) continue;
             const float G = fast_exp2(p[i]);
             const float alpha = alpha_of(c.y, G);
-            if (alpha < kAlphaMin) continue;
+            const bool take = hit[i] && alpha >= kAlphaMin;
             const float dy = fy[i] - a.y;
             const float iom = rcp_approx(__fsub_rn(1.f, alpha));
-            T[i] = T[i] * iom;
-            const float w = alpha * T[i];
-            acc[6] = fmaf(w, dr[i], acc[6]);
-            acc[7] = fmaf(w, dg[i], acc[7]);
+            T[i] = take ? T[i] * iom : T[i];
+            const float w = take ? alpha * T[i] : 0.f;
+            a6 = fmaf(w, dr[i], a6);
+            a7 = fmaf(w, dg[i], a7);
             acc_b = fmaf(w, db[i], acc_b);
             const float cd = col.x * dr[i] + col.y * dg[i] + col.z * db[i];
             const float dalpha = T[i] * cd - U[i] * iom;
             U[i] = fmaf(w, cd, U[i]);
-            if (__fmul_rn(c.y, G) <= kAlphaMax) {
-              acc[2] = fmaf(dalpha, G, acc[2]);
-              const float dpow = dalpha * alpha;  // d alpha / d power = alpha
-              const float t = dpow * dy;
-              m0 += dpow;
-              m1 += t;
-              m2 = fmaf(t, dy, m2);
-            }
+            const bool unclamped = take && __fmul_rn(c.y, G) <= kAlphaMax;
+            const float dpow = unclamped ? dalpha * alpha : 0.f;  // d alpha / d power = alpha
+            a2 = unclamped ? fmaf(dalpha, G, a2) : a2;
+            const float t = dpow * dy;
+            m0 += dpow;
+            m1 += t;
+            m2 = fmaf(t, dy, m2);
           }
           // power = -(A dx^2 + C dy^2)/2 - B dx dy, natural conic from the log2-scaled record
           const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
           const float dxm0 = dx * m0;
+          acc[0] = fmaf(A, dxm0, B * m1);
+          acc[1] = fmaf(B, dxm0, C * m1);
+          acc[2] = a2;
           acc[3] = -0.5f * dx * dxm0;
           acc[4] = -dx * m1;
           acc[5] = -0.5f * m2;
-          acc[0] = fmaf(A, dxm0, B * m1);
-          acc[1] = fmaf(B, dxm0, C * m1);
+          acc[6] = a6;
+          acc[7] = a7;
         }
         const float tot = warp_transpose_sum8(acc, lane);
         const float tot_b = warp_sum(acc_b);

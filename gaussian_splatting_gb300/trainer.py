@@ -169,7 +169,7 @@ class Trainer:
               self.ranges, self.counts[b])
             work_buf = None
             if self.work is not None:
-                work_buf = torch.zeros((2, H, W), dtype=torch.int32, device=self.params.device)
+                work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
             T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
               self.n_contrib, work_buf)
             if ready is not None:
@@ -182,8 +182,10 @@ class Trainer:
                 T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads)
                 launches += LAUNCHES["project_bwd"]
             if self.work is not None:
-                # (entries evaluated in the forward, entries accumulated, entries walked by the backward)
-                self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum())))
+                # (entries evaluated in the forward, entries accumulated, entries walked by the backward,
+                #  pairs the forward's warps evaluated)
+                self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum()),
+                                  int(work_buf[2].sum())))
             launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in ("project", "render_fwd", "loss", "render_bwd"))
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
           self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard)

@@ -118,9 +118,10 @@ gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* 
  *   image = C + T bg;  T_final = T;  n_contrib = 1 + list position of the last
  *   accumulated entry (0 if none).
  * bg is a host array of 3 floats (may be NULL for black).
- * work is optional (NULL: not written), [2][H][W] uint32: work[0] = list entries the pixel
- *   evaluated (through its termination point), work[1] = entries it accumulated -- the
- *   per-pixel work counts behind the compositing kernels' roofline figures.
+ * work is optional (NULL: not written), [3][H][W] uint32: work[0] = list entries the pixel
+ *   evaluated (through its termination point), work[1] = entries it accumulated, work[2] =
+ *   entries its warp walked (the warp-culled list up to the point where all of the warp's
+ *   pixels were done) -- the work counts behind the compositing kernels' roofline figures.
  */
 gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                         const gs_camera* cam, const float* bg, float* image, float* T_final,
