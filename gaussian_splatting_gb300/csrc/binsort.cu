@@ -12,18 +12,16 @@
 // about a third of the traffic of sorting all 64 key bits of 12-byte pairs.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   k_depth_init  depth keys (0xFFFFFFFF for culled Gaussians) + their digit histograms;
-//                 every CTA adds the tile rectangles of its Gaussians to a private
-//                 shared-memory difference grid (4 corners each).
-//   k_grid_sum    sums the private grids into one difference grid of per-tile counts.
-//   k_digit_scan  exclusive digit offsets of the depth passes.
 //   k_radix_sort  all stable 8-bit passes of one sort in a cooperative launch; each pass
 //                 counts digits per radix tile, scans the counts per digit over the tiles,
-//                 then ranks every tile in shared memory (warp match-any ranking) and
-//                 writes digit-contiguous runs; grid barriers separate the phases.  Used for
-//                 the depth sort and for the tile sort, whose first pass generates its
-//                 (tile, index) pairs from the scan's records instead of reading them and
-//                 whose last pass writes the caller's 64-bit keys and values.
+//                 then ranks every tile in shared memory and writes digit-contiguous runs;
+//                 grid barriers separate the phases.  Used for the depth sort, whose phase 0
+//                 makes the depth keys (0xFFFFFFFF for culled Gaussians), their digit totals
+//                 and, per CTA, a difference grid of per-tile instance counts (4 corners per
+//                 visible Gaussian, summed into one grid in the next phase); and for the tile
+//                 sort, whose first pass generates its (tile, index) pairs from the scan's
+//                 records instead of reading them and whose last pass writes the caller's
+//                 values (and 64-bit keys if asked for).
 //   k_scan_dup    single-pass scan (decoupled look-back, 32 predecessors per step) of
 //                 tiles-touched over the depth-sorted Gaussians: every Gaussian's first
 //                 output slot and rectangle record, and for every radix tile of the tile
@@ -71,7 +69,7 @@ struct Workspace {
   uint32_t* hist_depth;            // [256][radix tiles of the depth sort]
   uint32_t* hist_tile;             // [256][radix tiles of the tile sort]
   uint32_t* grid;                  // (Ty + 1) x (Tx + 1) difference grid of per-tile counts
-  uint32_t* grids;                 // one private difference grid per k_depth_init CTA
+  uint32_t* grids;                 // one private difference grid per depth-sort CTA
   uint32_t* rstage;                // tile ranges, published to the caller only on success
   uint32_t* slice_first;           // per output slice of kSlice slots: the item holding its first slot
   uint4* grec;                     // per depth-ordered Gaussian: (slot, x0 | y0 << 16, width, index)
@@ -145,90 +143,6 @@ __device__ __forceinline__ void flag_status(int64_t* count, int64_t bits) {
   atomicOr(reinterpret_cast<unsigned long long*>(&count[1]), (unsigned long long)bits);
 }
 
-// ------------------------------------------------------------------ depth keys + tile counts
-// Also adds every visible Gaussian's tile rectangle to a difference grid private to the CTA
-// (shared-memory atomics), written out without global atomics and summed by k_grid_sum.
-__global__ void __launch_bounds__(256) k_depth_init(const float* __restrict__ proj, int64_t n, gs::Cam k,
-                                                     uint32_t* __restrict__ dkey, uint32_t* __restrict__ didx,
-                                                     uint32_t* small, uint32_t* __restrict__ grids) {
-  extern __shared__ uint32_t s_grid[];  // (Ty + 1) x (Tx + 1)
-  __shared__ uint32_t s_hist[kDepthPasses][256];
-  const float4* q0 = reinterpret_cast<const float4*>(proj);
-  const float4* q1 = q0 + n;
-  const int gw = k.Tx + 1, gwords = (k.Tx + 1) * (k.Ty + 1);
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
-  for (int i = threadIdx.x; i < gwords; i += blockDim.x) s_grid[i] = 0u;
-  __syncthreads();
-  for (int64_t i = gtid; i < n; i += stride) {
-    const int r = __float_as_int(__ldg(&q1[i].w));
-    const float4 a = __ldg(&q0[i]);
-    uint32_t key = kCulledKey;
-    if (r > 0) {
-      const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
-      const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
-      const int x0 = min(max((fu - r) >> 4, 0), k.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), k.Tx);
-      const int y0 = min(max((fv - r) >> 4, 0), k.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), k.Ty);
-      key = __float_as_uint(a.z);
-      if (x0 < x1 && y0 < y1) {  // modular arithmetic: -1 = 0xFFFFFFFF
-        atomicAdd(&s_grid[y0 * gw + x0], 1u);
-        atomicAdd(&s_grid[y0 * gw + x1], 0xFFFFFFFFu);
-        atomicAdd(&s_grid[y1 * gw + x0], 0xFFFFFFFFu);
-        atomicAdd(&s_grid[y1 * gw + x1], 1u);
-      }
-    }
-    dkey[i] = key;
-    didx[i] = (uint32_t)i;
-#pragma unroll
-    for (int p = 0; p < kDepthPasses; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 255u], 1u);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kDepthPasses * 256; i += blockDim.x) {
-    const uint32_t c = (&s_hist[0][0])[i];
-    if (c) atomicAdd(&small[kSmHist + i], c);
-  }
-  uint32_t* mine = grids + (size_t)blockIdx.x * gwords;
-  for (int i = threadIdx.x; i < gwords; i += blockDim.x) mine[i] = s_grid[i];
-}
-
-// grid[c] = sum over the CTAs' private difference grids; blockIdx.y picks a group of grids,
-// so each cell receives one atomic add per group
-constexpr int kGridGroups = 16;
-__global__ void __launch_bounds__(256) k_grid_sum(const uint32_t* __restrict__ grids, int ngrids, int gwords,
-                                                   uint32_t* __restrict__ grid) {
-  const int per = (ngrids + kGridGroups - 1) / kGridGroups;
-  const int g0 = blockIdx.y * per, g1 = min(ngrids, g0 + per);
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < gwords; c += gridDim.x * blockDim.x) {
-    uint32_t acc = 0;
-#pragma unroll 4
-    for (int g = g0; g < g1; ++g) acc += __ldg(&grids[(size_t)g * gwords + c]);
-    if (acc) atomicAdd(&grid[c], acc);
-  }
-}
-
-// exclusive digit offsets of slots [slot0, slot0 + nslots)
-__global__ void k_digit_scan(uint32_t* small, int slot0, int nslots, const int64_t* count) {
-  __shared__ uint32_t s_warp[8];
-  if (count[1] != 0) return;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  for (int p = slot0; p < slot0 + nslots; ++p) {
-    const uint32_t c = small[kSmHist + p * 256 + t];
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    uint32_t woff = 0;
-    for (int w = 0; w < warp; ++w) woff += s_warp[w];
-    small[kSmDigitBase + p * 256 + t] = woff + incl - c;
-    __syncthreads();
-  }
-}
-
 // ------------------------------------------------------------------ stable radix sort
 // One cooperative launch runs every pass of a sort.  Each pass is reduce-then-scan over
 // radix tiles of kSortThreads * ITEMS keys, with grid-wide barriers between the phases:
@@ -282,6 +196,12 @@ struct RadixJob {
   const float4* q0;     // tile sort only: the last pass writes (key << 32 | depth bits of
   uint64_t* keys64;     // Gaussian value) to keys64 and the values to vals_out
   uint32_t* vals_out;
+  // depth sort only: phase 0 makes the keys from the projection and adds every visible
+  // Gaussian's tile rectangle to a per-CTA difference grid, summed into `grid` in phase B0
+  const float* proj;
+  int Tx, Ty, gwords;
+  uint32_t* grids;      // [gridDim.x][gwords]
+  uint32_t* grid;       // [gwords], zeroed by the host
 };
 
 // Grid-wide barrier on a monotonically increasing arrival counter.  Bounded: after `limit`
@@ -471,6 +391,73 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
   __syncthreads();
 }
 
+// Depth sort, phase 0 (replaces phase A of pass 0): radix tile by radix tile, the depth key of
+// every Gaussian (float bits of z; 0xFFFFFFFF if culled) and its index, the tile's pass-0
+// digit counts, the CTA's digit totals of all four passes (added to the small block once) and
+// the CTA's private difference grid of tile counts (4 corners per visible Gaussian, shared
+// memory atomics), written out for phase B0 to sum.
+template <int ITEMS>
+__device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid,
+                                             uint32_t* s_tot, int64_t n, int64_t ntiles, uint32_t G) {
+  constexpr int kTile = kSortThreads * ITEMS;
+  const int tid = threadIdx.x;
+  const float4* q0 = reinterpret_cast<const float4*>(J.proj);
+  const float4* q1 = q0 + n;
+  const int gw = J.Tx + 1;
+  for (int i = tid; i < J.gwords; i += kSortThreads) s_grid[i] = 0u;
+  for (int i = tid; i < kDepthPasses * 256; i += kSortThreads) s_tot[i] = 0u;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+    for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
+    __syncthreads();
+    for (int j = tid; j < kTile; j += kSortThreads) {
+      const int64_t i = tile * kTile + j;
+      if (i >= n) break;
+      const int r = __float_as_int(__ldg(&q1[i].w));
+      const float4 a = __ldg(&q0[i]);
+      uint32_t key = kCulledKey;
+      if (r > 0) {
+        const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
+        const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
+        const int x0 = min(max((fu - r) >> 4, 0), J.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), J.Tx);
+        const int y0 = min(max((fv - r) >> 4, 0), J.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), J.Ty);
+        key = __float_as_uint(a.z);
+        if (x0 < x1 && y0 < y1) {  // modular arithmetic: -1 = 0xFFFFFFFF
+          atomicAdd(&s_grid[y0 * gw + x0], 1u);
+          atomicAdd(&s_grid[y0 * gw + x1], 0xFFFFFFFFu);
+          atomicAdd(&s_grid[y1 * gw + x0], 0xFFFFFFFFu);
+          atomicAdd(&s_grid[y1 * gw + x1], 1u);
+        }
+      }
+      J.key[0][i] = key;
+      J.val[0][i] = (uint32_t)i;
+      atomicAdd(&S.tstart[key & 255u], 1u);
+#pragma unroll
+      for (int p = 0; p < kDepthPasses; ++p) atomicAdd(&s_tot[p * 256 + ((key >> (8 * p)) & 255u)], 1u);
+    }
+    __syncthreads();
+    J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
+    __syncthreads();
+  }
+  for (int i = tid; i < kDepthPasses * 256; i += kSortThreads)
+    if (s_tot[i]) atomicAdd(&J.small[kSmHist + i], s_tot[i]);
+  uint32_t* mine = J.grids + (size_t)blockIdx.x * J.gwords;
+  for (int i = tid; i < J.gwords; i += kSortThreads) mine[i] = s_grid[i];
+}
+
+// Depth sort, phase B0 side job: grid[c] = sum over the CTAs' private grids, 16 grids per
+// work item (one atomic add per item).
+__device__ __forceinline__ void depth_grid_sum(const RadixJob& J, uint32_t G) {
+  const int64_t groups = (G + 15) / 16;
+  const int64_t items = (int64_t)J.gwords * groups;
+  for (int64_t it = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; it < items; it += (int64_t)G * kSortThreads) {
+    const int c = (int)(it % J.gwords);
+    const uint32_t g0 = (uint32_t)(it / J.gwords) * 16u, g1 = min(G, g0 + 16u);
+    uint32_t acc = 0;
+    for (uint32_t g = g0; g < g1; ++g) acc += J.grids[(size_t)g * J.gwords + c];
+    if (acc) atomicAdd(&J.grid[c], acc);
+  }
+}
+
 template <int ITEMS, bool kTileSort>
 __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   constexpr int kTile = kSortThreads * ITEMS;
@@ -491,7 +478,11 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     const uint32_t* kin = J.key[p & 1];
     const uint32_t* vin = J.val[p & 1];
     // ---- A: digit counts of every radix tile
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+    if (!kTileSort && p == 0) {
+      uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
+      depth_phase0(S, J, s_grid, s_grid + J.gwords, J.n_host, ntiles, G);
+    }
+    for (int64_t tile = blockIdx.x; tile < ntiles && (kTileSort || p > 0); tile += G) {
       for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
       __syncthreads();
       const int64_t base = tile * kTile;
@@ -514,9 +505,26 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     ++nbar;
     if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && blockIdx.x == 0))) return;
     // ---- B: per digit, exclusive scan over the tiles, plus the digit's global base
+    if (!kTileSort) {
+      if (p == 0) depth_grid_sum(J, G);
+      // the digit bases of this pass: exclusive scan of the digit totals of phase 0
+      const uint32_t c = J.small[kSmHist + p * 256 + tid];
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) S.wsum[warp] = incl;
+      __syncthreads();
+      uint32_t woff = 0;
+      for (int w = 0; w < warp; ++w) woff += S.wsum[w];
+      S.gbase[tid] = woff + incl - c;
+      __syncthreads();
+    }
     for (uint32_t d = blockIdx.x; d < 256; d += G) {
       uint32_t* col = J.hist + (int64_t)d * J.hist_stride;
-      uint32_t carry = J.small[kSmDigitBase + (J.slot0 + p) * 256 + d];
+      uint32_t carry = kTileSort ? J.small[kSmDigitBase + (J.slot0 + p) * 256 + d] : S.gbase[d];
       constexpr int kPer = 12;
       for (int64_t c0 = 0; c0 < ntiles; c0 += kSortThreads * kPer) {
         uint32_t x[kPer];
@@ -877,36 +885,54 @@ __global__ void k_publish_ranges(const uint32_t* __restrict__ rstage, int64_t T,
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * T; i += stride) ranges[i] = rstage[i];
 }
 
+// Resident CTAs per SM of a radix kernel for a given dynamic shared-memory size (cached).
 template <int ITEMS, bool kTileSort>
-int radix_blocks_per_sm() {
-  static int cached = -1;
+int radix_blocks_per_sm(size_t smem) {
   static std::mutex mu;
+  static size_t cached_smem = 0;
+  static int cached = -1;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached < 0) {
+  if (cached < 0 || cached_smem != smem) {
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_radix_sort<ITEMS, kTileSort>, kSortThreads,
-                                                      sizeof(SortSmem<ITEMS>)) != cudaSuccess ||
+    cudaFuncSetAttribute(k_radix_sort<ITEMS, kTileSort>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_radix_sort<ITEMS, kTileSort>, kSortThreads, smem) !=
+            cudaSuccess ||
         b < 1)
       b = 1;
     cached = b;
+    cached_smem = smem;
   }
   return cached;
 }
 
+template <int ITEMS, bool kTileSort>
+int radix_grid(size_t smem, int64_t max_tiles) {
+  const int64_t cap_ctas = (int64_t)gs::num_sms() * radix_blocks_per_sm<ITEMS, kTileSort>(smem);
+  return (int)std::max<int64_t>(1, std::min(cap_ctas, max_tiles));
+}
+
 // Cooperative launch: every CTA of the grid is resident at once, which the grid barriers need.
 template <int ITEMS, bool kTileSort>
-cudaError_t launch_radix(const RadixJob& job, int64_t max_tiles, cudaStream_t st) {
-  const int64_t cap_ctas = (int64_t)gs::num_sms() * radix_blocks_per_sm<ITEMS, kTileSort>();
-  const int grid = (int)std::max<int64_t>(1, std::min(cap_ctas, max_tiles));
+cudaError_t launch_radix(const RadixJob& job, int grid, size_t smem, cudaStream_t st) {
   RadixJob j = job;
   void* args[] = {&j};
   return cudaLaunchCooperativeKernel((const void*)k_radix_sort<ITEMS, kTileSort>, dim3(grid), dim3(kSortThreads), args,
-                                     sizeof(SortSmem<ITEMS>), st);
+                                     smem, st);
 }
 
 int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); }
-int init_ctas() { return 2 * gs::num_sms(); }
-size_t depth_init_smem(const gs::Cam& k) { return sizeof(uint32_t) * (size_t)grid_words(k); }
+// depth sort: the sort's shared memory, then the CTA's difference grid and digit totals
+size_t depth_sort_smem(const gs::Cam& k) {
+  return sizeof(SortSmem<kDepthItems>) + sizeof(uint32_t) * ((size_t)grid_words(k) + kDepthPasses * 256);
+}
+int depth_sort_grid(const gs::Cam& k, int64_t n) {
+  return radix_grid<kDepthItems, false>(depth_sort_smem(k), sort_tiles<kDepthItems>(n));
+}
+// private difference grids the workspace holds: at most one per resident CTA (2048 threads
+// per SM), at most one per radix tile of the depth sort
+int64_t depth_grids_bound(int64_t n) {
+  return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n), (int64_t)gs::num_sms() * 8));
+}
 size_t tile_counts_smem(const gs::Cam& k) {
   return sizeof(uint32_t) * ((size_t)grid_words(k) + (size_t)kMaxTilePasses * 256);
 }
@@ -917,7 +943,8 @@ constexpr size_t kMaxTileCountsSmem = 200 * 1024;
 extern "C" size_t gs_bin_sort_workspace_size(int64_t n, int64_t capacity, const gs_camera* cam) {
   if (!cam || n < 0 || capacity < 0) return 0;
   const gs::Cam k = gs::make_cam(*cam);
-  return carve(nullptr, nullptr, n, capacity, tile_passes(k), grid_words(k), (int64_t)k.Tx * k.Ty, init_ctas());
+  return carve(nullptr, nullptr, n, capacity, tile_passes(k), grid_words(k), (int64_t)k.Tx * k.Ty,
+               depth_grids_bound(n));
 }
 
 extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
@@ -937,11 +964,11 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
   const int64_t T = (int64_t)k.Tx * k.Ty;
   if (tpasses > kMaxTilePasses || tile_counts_smem(k) > kMaxTileCountsSmem)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: %d x %d tiles exceed the supported grid", k.Tx, k.Ty);
-  const size_t need = carve(nullptr, nullptr, n, capacity, tpasses, grid_words(k), T, init_ctas());
+  const size_t need = carve(nullptr, nullptr, n, capacity, tpasses, grid_words(k), T, depth_grids_bound(n));
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: workspace %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w;
-  carve(&w, reinterpret_cast<char*>(workspace), n, capacity, tpasses, grid_words(k), T, init_ctas());
+  carve(&w, reinterpret_cast<char*>(workspace), n, capacity, tpasses, grid_words(k), T, depth_grids_bound(n));
   cudaStream_t st = gs::as_stream(stream);
   const int64_t limit = gs::wait_limit();
   const int drop = gs::take_drop_publish();
@@ -955,23 +982,20 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     if (cudaMemsetAsync(w.scan_state, 0, sizeof(unsigned long long) * chunks, st) != cudaSuccess)
       return gs::check_launch("gs_bin_sort memset");
     const int sms = gs::num_sms();
-    // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys
-    static const cudaError_t attr_init = cudaFuncSetAttribute(
-        k_depth_init, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxTileCountsSmem);
-    if (attr_init != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr_init));
-    k_depth_init<<<init_ctas(), 256, depth_init_smem(k), st>>>(proj, n, k, w.dkey[0], w.didx[0], w.small, w.grids);
+    // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys; phase 0 also
+    //    builds the difference grid of per-tile instance counts
     if (cudaMemsetAsync(w.grid, 0, sizeof(uint32_t) * (size_t)grid_words(k), st) != cudaSuccess)
       return gs::check_launch("gs_bin_sort memset");
-    k_grid_sum<<<dim3((unsigned)std::max<int64_t>(1, (grid_words(k) + 255) / 256), kGridGroups), 256, 0, st>>>(
-        w.grids, init_ctas(), (int)grid_words(k), w.grid);
-    k_digit_scan<<<1, 256, 0, st>>>(w.small, 0, kDepthPasses, count);
+    const size_t dsmem = depth_sort_smem(k);
+    const int dgrid = (int)std::min<int64_t>(depth_sort_grid(k, n), depth_grids_bound(n));
     RadixJob dj{};
     dj.key[0] = w.dkey[0]; dj.key[1] = w.dkey[1];
     dj.val[0] = w.didx[0]; dj.val[1] = w.didx[1];
     dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
     dj.hist = w.hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
     dj.small = w.small; dj.count = count; dj.limit = limit; dj.drop_arrival = drop == 2;
-    if (cudaError_t e = launch_radix<kDepthItems, false>(dj, sort_tiles<kDepthItems>(n), st))
+    dj.proj = proj; dj.Tx = k.Tx; dj.Ty = k.Ty; dj.gwords = (int)grid_words(k); dj.grids = w.grids; dj.grid = w.grid;
+    if (cudaError_t e = launch_radix<kDepthItems, false>(dj, dgrid, dsmem, st))
       return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. (tile, index) pairs in depth order; per-tile counts into the difference grid
@@ -995,7 +1019,9 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = 0;
     tj.gen = GenSource{w.slice_first, w.grec, n, k.Tx};
     tj.q0 = reinterpret_cast<const float4*>(proj); tj.keys64 = keys; tj.vals_out = vals;
-    if (cudaError_t e = launch_radix<kTileItems, true>(tj, sort_tiles<kTileItems>(capacity), st))
+    if (cudaError_t e = launch_radix<kTileItems, true>(
+            tj, radix_grid<kTileItems, true>(sizeof(SortSmem<kTileItems>), sort_tiles<kTileItems>(capacity)),
+            sizeof(SortSmem<kTileItems>), st))
       return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
     k_publish_ranges<<<sms, 256, 0, st>>>(w.rstage, T, ranges, count);

@@ -32,9 +32,9 @@ MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
 
 def bin_sort_launches(cam) -> int:
-    # depth keys, grid sum, digit scan, depth sort (all passes in one cooperative launch),
-    # scan, tile counts, tile sort (likewise), ranges
-    return 8
+    # depth sort (keys, tile-count grid and all four passes in one cooperative launch), scan,
+    # tile counts, tile sort (both passes in one cooperative launch), ranges
+    return 5
 
 
 @dataclasses.dataclass
