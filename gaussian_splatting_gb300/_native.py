@@ -221,5 +221,5 @@ def gs_debug_set_wait_limit(iterations: int):
 
 
 def gs_debug_drop_publish(mode: int):
-    """0 disarms; 1 drops the scan's first look-back publication; 2 drops one grid-barrier arrival."""
+    """0 disarms; 1 drops CTA 0's first barrier arrival in the tile sort, 2 in the depth sort."""
     load().gs_debug_drop_publish(int(mode))

@@ -22,12 +22,12 @@
 //                 sort, whose first pass generates its (tile, index) pairs from the scan's
 //                 records instead of reading them and whose last pass writes the caller's
 //                 values (and 64-bit keys if asked for).
-//   k_scan_dup    single-pass scan (decoupled look-back, 32 predecessors per step) of
-//                 tiles-touched over the depth-sorted Gaussians: every Gaussian's first
-//                 output slot and rectangle record, and for every radix tile of the tile
-//                 sort the Gaussian holding its first slot.
-//   k_tile_counts prefix sums of the difference grid = instances per tile; their scan gives
-//                 every tile's [start, end) and the digit offsets of the tile passes.
+//                 After the depth passes the same launch runs the tiles-touched scan over
+//                 the sorted Gaussians (reduce, scan of the chunk sums, then each chunk's
+//                 records: first slot, rectangle, index; and for every radix tile of the
+//                 tile sort the Gaussian holding its first slot) and, on one CTA, the tile
+//                 counts (2-D prefix sums of the grid, their scan = staged ranges, digit
+//                 bases of the tile passes).
 //   k_publish_ranges  copies the staged ranges to the caller's array if nothing failed.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
@@ -37,9 +37,7 @@
 
 namespace {
 
-constexpr int kScanThreads = 256;
-constexpr int kScanItems = 4;
-constexpr int kScanChunk = kScanThreads * kScanItems;  // Gaussians per scan CTA
+constexpr int kScanChunk = 1024;  // sorted Gaussians per chunk of the tiles-touched scan
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
@@ -50,11 +48,9 @@ constexpr int kDepthPasses = 4;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // digit histogram / base slots
 
-constexpr uint64_t kFlagAgg = 1ull << 62, kFlagPre = 2ull << 62, kValMask = (1ull << 62) - 1;
 constexpr uint32_t kCulledKey = 0xFFFFFFFFu;
 
 // layout of the small, memset-cleared block of the workspace (32-bit words)
-constexpr int kSmScanCounter = 0;
 constexpr int kSmBarrier = 1;        // one arrival counter per sort (depth, tile)
 constexpr int kSmHist = 32;          // kSlots * 256
 constexpr int kSmDigitBase = kSmHist + kSlots * 256;
@@ -65,7 +61,7 @@ struct Workspace {
   uint32_t* tval[2];               // instance Gaussian indices, ping-pong
   uint32_t* dkey[2];
   uint32_t* didx[2];
-  unsigned long long* scan_state;  // per scan chunk
+  unsigned long long* chunk_tot;   // per scan chunk: tiles touched, then its first slot
   uint32_t* hist_depth;            // [256][radix tiles of the depth sort]
   uint32_t* hist_tile;             // [256][radix tiles of the tile sort]
   uint32_t* grid;                  // (Ty + 1) x (Tx + 1) difference grid of per-tile counts
@@ -131,7 +127,7 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int6
     w->dkey[1] = reinterpret_cast<uint32_t*>(dk1);
     w->didx[0] = reinterpret_cast<uint32_t*>(di0);
     w->didx[1] = reinterpret_cast<uint32_t*>(di1);
-    w->scan_state = reinterpret_cast<unsigned long long*>(ss);
+    w->chunk_tot = reinterpret_cast<unsigned long long*>(ss);
     w->hist_depth = reinterpret_cast<uint32_t*>(lbd);
     w->hist_tile = reinterpret_cast<uint32_t*>(lbt);
     w->small = reinterpret_cast<uint32_t*>(sm);
@@ -202,6 +198,14 @@ struct RadixJob {
   int Tx, Ty, gwords;
   uint32_t* grids;      // [gridDim.x][gwords]
   uint32_t* grid;       // [gwords], zeroed by the host
+  // depth sort only, after the last pass: the tiles-touched scan over the depth-sorted
+  // Gaussians and the per-tile counts
+  unsigned long long* chunk_tot;  // per scan chunk of kScanChunk sorted Gaussians
+  uint4* grec;          // per sorted Gaussian: (first slot, x0 | y0 << 16, width, index)
+  uint32_t* slice_first;  // per radix tile of the tile sort: the Gaussian holding its first slot
+  int64_t tcap;         // instance capacity
+  uint32_t* rstage;     // staged tile ranges
+  int tpasses;          // tile passes (their digit bases go to the small block)
 };
 
 // Grid-wide barrier on a monotonically increasing arrival counter.  Bounded: after `limit`
@@ -458,6 +462,271 @@ __device__ __forceinline__ void depth_grid_sum(const RadixJob& J, uint32_t G) {
   }
 }
 
+// Tiles touched by the Gaussian at a depth-sorted position (key, index), and its rectangle
+// record (first slot left 0).
+__device__ __forceinline__ uint32_t touched(const RadixJob& J, int64_t n, uint32_t key, uint32_t g, uint4& rec) {
+  rec = make_uint4(0u, 0u, 1u, g);
+  if (key == kCulledKey) return 0u;
+  const float4* q0 = reinterpret_cast<const float4*>(J.proj);
+  const int r = __float_as_int(__ldg(&q0[n + g].w));
+  const float4 a = __ldg(&q0[g]);
+  const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
+  const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
+  const int x0 = min(max((fu - r) >> 4, 0), J.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), J.Tx);
+  const int y0 = min(max((fv - r) >> 4, 0), J.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), J.Ty);
+  if (!(r > 0 && x0 < x1 && y0 < y1)) return 0u;
+  rec.y = (uint32_t)x0 | ((uint32_t)y0 << 16);
+  rec.z = (uint32_t)(x1 - x0);
+  return (uint32_t)((x1 - x0) * (y1 - y0));
+}
+
+// Block-wide sum over the 256 threads (result in every thread).
+template <int ITEMS>
+__device__ __forceinline__ unsigned long long block_sum(SortSmem<ITEMS>& S, uint32_t v) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) S.wsum[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int w = 0; w < kSortWarps; ++w) t += S.wsum[w];
+  return t;
+}
+
+// One CTA: 2-D prefix sums of the difference grid give the instances of every tile; their
+// scan in tile order gives the staged ranges, and their digit sums the exclusive digit bases
+// of the tile passes.  s_grid holds gwords words, s_dig 2 x 256.
+template <int ITEMS>
+__device__ void tile_counts_cta(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid, uint32_t* s_dig) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Tx = J.Tx, Ty = J.Ty, gw = Tx + 1, gh = Ty + 1, T = Tx * Ty;
+  for (int i = tid; i < gw * gh; i += kSortThreads) s_grid[i] = ld_acquire_u32(&J.grid[i]);
+  __syncthreads();
+  for (int y = warp; y < gh; y += kSortWarps) {  // prefix along each row, a warp per row
+    uint32_t carry = 0;
+    for (int x0 = 0; x0 < gw; x0 += 32) {
+      const int x = x0 + lane;
+      uint32_t v = x < gw ? s_grid[y * gw + x] : 0u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (x < gw) s_grid[y * gw + x] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  for (int x = warp; x < gw; x += kSortWarps) {  // then along each column
+    uint32_t carry = 0;
+    for (int y0 = 0; y0 < gh; y0 += 32) {
+      const int y = y0 + lane;
+      uint32_t v = y < gh ? s_grid[y * gw + x] : 0u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (y < gh) s_grid[y * gw + x] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  // the count of tile t = (y, x) is grid cell (y, x), walked in tile order by stepping x
+  // (one division per walk)
+  auto cell = [&](int t) { return s_grid[(t / Tx) * gw + (t % Tx)]; };
+  // digit sums: pass 0 holds the tiles d, d + 256, ...; pass 1 the tiles [256 d, 256 d + 256)
+  {
+    uint32_t sum = 0;
+    if (tid < T) {
+      int y = tid / Tx, x = tid % Tx;
+      for (int t = tid; t < T; t += 256) {
+        sum += s_grid[y * gw + x];
+        x += 256;
+        while (x >= Tx) { x -= Tx; ++y; }
+      }
+    }
+    s_dig[tid] = sum;
+  }
+  if (J.tpasses > 1) {
+    for (int d = warp; d < 256; d += kSortWarps) {
+      uint32_t sum = 0;
+      if ((d << 8) < T) {
+        for (int t = (d << 8) + lane; t < min(T, (d + 1) << 8); t += 32) sum += cell(t);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      }
+      if (lane == 0) s_dig[256 + d] = sum;
+    }
+  }
+  // exclusive scan of the T counts in tile order, consecutive tiles per thread
+  const int per = (T + kSortThreads - 1) / kSortThreads;
+  const int t0 = tid * per, t1 = min(T, t0 + per);
+  const int y0 = t0 < T ? t0 / Tx : 0, x0 = t0 < T ? t0 % Tx : 0;
+  uint32_t sum = 0;
+  for (int t = t0, y = y0, x = x0; t < t1; ++t) {
+    sum += s_grid[y * gw + x];
+    if (++x == Tx) { x = 0; ++y; }
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();
+  if (lane == 31) S.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += S.wsum[w];
+  for (int t = t0, y = y0, x = x0; t < t1; ++t) {
+    const uint32_t c = s_grid[y * gw + x];
+    J.rstage[2 * (int64_t)t] = c ? run : 0u;
+    J.rstage[2 * (int64_t)t + 1] = c ? run + c : 0u;
+    run += c;
+    if (++x == Tx) { x = 0; ++y; }
+  }
+  __syncthreads();
+  if (warp < J.tpasses) {  // exclusive digit bases, a warp per pass
+    uint32_t carry = 0;
+    for (int d0 = 0; d0 < 256; d0 += 32) {
+      const uint32_t c = s_dig[warp * 256 + d0 + lane];
+      uint32_t in = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, in, o);
+        if (lane >= o) in += u;
+      }
+      J.small[kSmDigitBase + (kDepthPasses + warp) * 256 + d0 + lane] = carry + in - c;
+      carry += __shfl_sync(0xffffffffu, in, 31);
+    }
+  }
+}
+
+// After the depth passes: the tiles-touched scan over the sorted Gaussians and the tile counts.
+// S1: the sum of every chunk of kScanChunk sorted Gaussians, while the last CTA (which has no
+// chunk when the grid has a spare CTA) computes the tile counts.  S2 (only for more than
+// kDirectChunks chunks): CTA 0 turns the sums into exclusive prefixes.  S3: every chunk's
+// records (its prefix summed directly from the chunk sums when there are few chunks).
+// Returns false if a barrier failed.
+constexpr int64_t kDirectChunks = 4096;
+
+template <int ITEMS>
+__device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid, uint32_t* s_tot, uint32_t G,
+                           uint32_t& nbar) {
+  constexpr int kPer = kScanChunk / kSortThreads;  // 4 consecutive Gaussians per thread
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = J.n_host;
+  const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
+  const bool direct = nchunks <= kDirectChunks;
+  const uint32_t* skey = J.key[kDepthPasses & 1];
+  const uint32_t* sidx = J.val[kDepthPasses & 1];
+  unsigned long long* wsum64 = reinterpret_cast<unsigned long long*>(S.gbase);  // free in these phases
+  // S1: chunk sums; tile counts on the last CTA
+  for (int64_t c = blockIdx.x; c < nchunks; c += G) {
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t i = c * kScanChunk + tid * kPer + j;
+      if (i < n) {
+        uint4 rec;
+        sum += touched(J, n, skey[i], sidx[i], rec);
+      }
+    }
+    const unsigned long long t = block_sum(S, sum);
+    if (tid == 0) J.chunk_tot[c] = t;
+  }
+  if (blockIdx.x == G - 1) tile_counts_cta(S, J, s_grid, s_tot);
+  if (!grid_barrier(S, J, ++nbar * G, true)) return false;
+  // S2: exclusive prefixes of the chunk sums and the instance count M (CTA 0)
+  if (!direct) {
+    if (blockIdx.x == 0) {
+      unsigned long long carry = 0;
+      for (int64_t c0 = 0; c0 < nchunks; c0 += kSortThreads) {
+        const int64_t c = c0 + tid;
+        const unsigned long long v = c < nchunks ? J.chunk_tot[c] : 0ull;
+        unsigned long long in = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long u = __shfl_up_sync(0xffffffffu, in, o);
+          if (lane >= o) in += u;
+        }
+        __syncthreads();
+        if (lane == 31) wsum64[warp] = in;
+        __syncthreads();
+        unsigned long long woff = 0, tot = 0;
+        for (int w = 0; w < kSortWarps; ++w) {
+          if (w < warp) woff += wsum64[w];
+          tot += wsum64[w];
+        }
+        if (c < nchunks) J.chunk_tot[c] = carry + woff + in - v;
+        carry += tot;
+      }
+      if (tid == 0) {
+        J.count[0] = (int64_t)carry;
+        if ((int64_t)carry > J.tcap) flag_status(J.count, gs::kStatusCapacity);
+      }
+    }
+    if (!grid_barrier(S, J, ++nbar * G, true)) return false;
+  }
+  // S3: every chunk's records and the first Gaussian of every radix tile of the tile sort
+  for (int64_t c = blockIdx.x; c < nchunks; c += G) {
+    unsigned long long prefix;
+    if (direct) {  // sum of the chunk sums before c (and, for the last chunk, M)
+      unsigned long long part = 0;
+      for (int64_t c2 = tid; c2 < c; c2 += kSortThreads) part += J.chunk_tot[c2];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      __syncthreads();
+      if (lane == 0) wsum64[warp] = part;
+      __syncthreads();
+      prefix = 0;
+      for (int w = 0; w < kSortWarps; ++w) prefix += wsum64[w];
+      if (c == nchunks - 1 && tid == 0) {
+        const int64_t M = (int64_t)(prefix + J.chunk_tot[c]);
+        J.count[0] = M;
+        if (M > J.tcap) flag_status(J.count, gs::kStatusCapacity);
+      }
+    } else {
+      prefix = J.chunk_tot[c];
+    }
+    uint32_t cnt[kPer];
+    uint4 rec[kPer];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t i = c * kScanChunk + tid * kPer + j;
+      cnt[j] = i < n ? touched(J, n, skey[i], sidx[i], rec[j]) : 0u;
+      sum += cnt[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    __syncthreads();
+    if (lane == 31) S.wsum[warp] = incl;
+    __syncthreads();
+    uint32_t woff = 0;
+    for (int w = 0; w < warp; ++w) woff += S.wsum[w];
+    int64_t go = (int64_t)prefix + woff + incl - sum;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t i = c * kScanChunk + tid * kPer + j;
+      if (i < n) {
+        rec[j].x = (uint32_t)min(go, (int64_t)0xFFFFFFFF);
+        J.grec[i] = rec[j];
+        for (int64_t sb = (go + kSlice - 1) / kSlice * kSlice; sb < go + cnt[j] && sb < J.tcap; sb += kSlice)
+          J.slice_first[sb / kSlice] = (uint32_t)i;
+      }
+      go += cnt[j];
+    }
+  }
+  return true;
+}
+
 template <int ITEMS, bool kTileSort>
 __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   constexpr int kTile = kSortThreads * ITEMS;
@@ -657,223 +926,10 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     }
     if (p + 1 < J.passes && !grid_barrier(S, J, ++nbar * G, true)) return;
   }
-}
-
-// ------------------------------------------------------------------ scan + duplicate
-// Walks the Gaussians in depth order (skey / sidx: depth-sorted keys and indices) and writes
-// out every Gaussian's first instance slot and rectangle record, from which the tile sort
-// generates the (tile id, Gaussian index) pairs.
-__global__ void __launch_bounds__(kScanThreads) k_scan_dup(const float* __restrict__ proj, int64_t n,
-                                                            const uint32_t* __restrict__ skey,
-                                                            const uint32_t* __restrict__ sidx, gs::Cam k,
-                                                            uint32_t* __restrict__ slice_first, uint4* __restrict__ grec,
-                                                            int64_t cap, unsigned long long* scan_state,
-                                                            uint32_t* small, int64_t* count, int64_t limit,
-                                                            int drop_publish) {
-  __shared__ uint32_t s_items[kScanChunk];   // tiles touched, then local exclusive offsets
-  __shared__ uint4 s_rec[kScanChunk];         // (offset, x0 | y0 << 16, width, Gaussian)
-  __shared__ uint32_t s_warp[kScanThreads / 32];
-  __shared__ unsigned long long s_prefix;
-  __shared__ uint32_t s_chunk;
-  if (count[1] != 0) return;  // an earlier stage failed
-  const int tid = threadIdx.x;
-  if (tid == 0) s_chunk = atomicAdd(&small[kSmScanCounter], 1u);
-  __syncthreads();
-  const int64_t chunk = s_chunk;
-  const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
-  const int64_t base = chunk * kScanChunk;
-  const float4* q0 = reinterpret_cast<const float4*>(proj);
-  const float4* q1 = q0 + n;
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    const int li = j * kScanThreads + tid;
-    const int64_t i = base + li;
-    uint32_t cnt = 0, rect = 0, width = 1, g = 0;
-    if (i < n && skey[i] != kCulledKey) {
-      g = sidx[i];
-      const int r = __float_as_int(__ldg(&q1[g].w));
-      const float4 a = __ldg(&q0[g]);
-      const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
-      const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
-      const int x0 = min(max((fu - r) >> 4, 0), k.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), k.Tx);
-      const int y0 = min(max((fv - r) >> 4, 0), k.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), k.Ty);
-      if (r > 0 && x0 < x1 && y0 < y1) {
-        cnt = (uint32_t)((x1 - x0) * (y1 - y0));
-        rect = (uint32_t)x0 | ((uint32_t)y0 << 16);
-        width = (uint32_t)(x1 - x0);
-      }
-    }
-    s_items[li] = cnt;
-    s_rec[li] = make_uint4(0u, rect, width, g);
-  }
-  __syncthreads();
-  // blocked scan: thread t owns items t*kScanItems .. +kScanItems-1
-  uint32_t v[kScanItems];
-  uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    v[j] = s_items[tid * kScanItems + j];
-    sum += v[j];
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = sum;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += y;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  uint32_t warp_off = 0, total = 0;
-  for (int w = 0; w < kScanThreads / 32; ++w) {
-    const uint32_t x = s_warp[w];
-    if (w < warp) warp_off += x;
-    total += x;
-  }
-  uint32_t run = warp_off + incl - sum;
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    s_items[tid * kScanItems + j] = run;  // exclusive local offset
-    s_rec[tid * kScanItems + j].x = run;
-    run += v[j];
-  }
-  // chunk prefix by decoupled look-back, 32 predecessors at a time by warp 0: lane l reads
-  // chunk (p - l); the nearest inclusive prefix ends the walk, aggregates before it are summed
-  if (warp == 0) {
-    if (lane == 0)
-      if (!(drop_publish && chunk == 0))
-        st_release_u64(&scan_state[chunk], (chunk == 0 ? kFlagPre : kFlagAgg) | (unsigned long long)total);
-    unsigned long long excl = 0;
-    bool to = false;
-    int64_t p = chunk - 1;
-    while (p >= 0 && !to) {
-      const int64_t q = p - lane;
-      unsigned long long st = q >= 0 ? ld_acquire_u64(&scan_state[q]) : kFlagPre;  // before chunk 0: prefix 0
-      int64_t it = 0;
-      while (true) {  // until every lane up to the nearest prefix has published
-        const uint32_t pre = __ballot_sync(0xffffffffu, (st >> 62) == 2);
-        const uint32_t upto = pre ? (pre & (~pre + 1u)) * 2u - 1u : 0xffffffffu;  // lanes <= nearest prefix
-        const uint32_t missing = __ballot_sync(0xffffffffu, (st >> 62) == 0) & upto;
-        if (!missing) break;
-        if (++it > limit) {
-          to = true;
-          break;
-        }
-        if (it > 32) __nanosleep(64);
-        if ((missing >> lane) & 1u) st = ld_acquire_u64(&scan_state[q]);
-      }
-      const uint32_t pre = __ballot_sync(0xffffffffu, (st >> 62) == 2);
-      const int stop = pre ? __ffs(pre) - 1 : 31;
-      unsigned long long v = (lane <= stop && q >= 0) ? (st & kValMask) : 0ull;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      excl += v;
-      if (pre) break;
-      p -= 32;
-    }
-    if (lane == 0) {
-      if (chunk > 0) st_release_u64(&scan_state[chunk], kFlagPre | (excl + total));
-      if (to) flag_status(count, gs::kStatusTimeout);
-      s_prefix = excl;
-      if (chunk == nchunks - 1) {
-        const int64_t M = (int64_t)(excl + total);
-        count[0] = M;
-        if (M > cap) flag_status(count, gs::kStatusCapacity);
-      }
-    }
-  }
-  __syncthreads();
-  // publish every item's global offset and its rectangle record for the write kernel
-  const int64_t out0 = (int64_t)s_prefix;
-#pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    const int li = tid * kScanItems + j;
-    const int64_t i = base + li;
-    if (i < n) {
-      uint4 rec = s_rec[li];
-      const int64_t go = out0 + (int64_t)rec.x;  // global exclusive offset
-      rec.x = (uint32_t)min(go, (int64_t)0xFFFFFFFF);
-      grec[i] = rec;
-      // first item of every write slice that starts inside this item's run
-      const int64_t c = v[j];
-      for (int64_t sb = (go + kSlice - 1) / kSlice * kSlice; sb < go + c && sb < cap; sb += kSlice)
-        slice_first[sb / kSlice] = (uint32_t)i;
-    }
-  }
-}
-
-// ------------------------------------------------------------------ per-tile counts
-// One CTA: 2-D prefix sums of the difference grid (in shared memory) give the instances of
-// every tile; their exclusive scan gives the tile ranges, and their digit sums the exclusive
-// digit offsets of the stable tile passes.
-__global__ void __launch_bounds__(1024) k_tile_counts(const uint32_t* __restrict__ grid, int Tx, int Ty, int tpasses,
-                                                       uint32_t* small, uint32_t* __restrict__ ranges,
-                                                       const int64_t* count) {
-  extern __shared__ uint32_t s_grid[];  // (Ty + 1) x (Tx + 1), then per-pass digit sums
-  __shared__ uint32_t s_warp[32];
-  if (count[1] != 0) return;
-  const int gw = Tx + 1, gh = Ty + 1, nthreads = blockDim.x, tid = threadIdx.x;
-  const int T = Tx * Ty;
-  uint32_t* s_dig = s_grid + (size_t)gw * gh;  // [kMaxTilePasses][256]
-  for (int i = tid; i < gw * gh; i += nthreads) s_grid[i] = grid[i];
-  for (int i = tid; i < kMaxTilePasses * 256; i += nthreads) s_dig[i] = 0u;
-  __syncthreads();
-  for (int y = tid; y < gh; y += nthreads) {  // prefix along rows
-    uint32_t run = 0;
-    for (int x = 0; x < gw; ++x) {
-      run += s_grid[y * gw + x];
-      s_grid[y * gw + x] = run;
-    }
-  }
-  __syncthreads();
-  for (int x = tid; x < gw; x += nthreads) {  // then along columns
-    uint32_t run = 0;
-    for (int y = 0; y < gh; ++y) {
-      run += s_grid[y * gw + x];
-      s_grid[y * gw + x] = run;
-    }
-  }
-  __syncthreads();
-  // exclusive scan of the T counts in tile order (tile t = (y, x) -> grid cell (y, x))
-  const int per = (T + nthreads - 1) / nthreads;
-  const int t0 = tid * per, t1 = min(T, t0 + per);
-  uint32_t sum = 0;
-  for (int t = t0; t < t1; ++t) sum += s_grid[(t / Tx) * gw + (t % Tx)];
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  uint32_t run = incl - sum;
-  for (int w = 0; w < warp; ++w) run += s_warp[w];
-  for (int t = t0; t < t1; ++t) {
-    const uint32_t c = s_grid[(t / Tx) * gw + (t % Tx)];
-    ranges[2 * (int64_t)t] = c ? run : 0u;
-    ranges[2 * (int64_t)t + 1] = c ? run + c : 0u;
-    run += c;
-    for (int p = 0; p < tpasses; ++p) atomicAdd(&s_dig[p * 256 + ((t >> (8 * p)) & 255)], c);
-  }
-  __syncthreads();
-  // exclusive digit offsets per tile pass
-  for (int p = 0; p < tpasses; ++p) {
-    if (warp == 0) {
-      uint32_t carry = 0;
-      for (int d0 = 0; d0 < 256; d0 += 32) {
-        const uint32_t c = s_dig[p * 256 + d0 + lane];
-        uint32_t in = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, in, o);
-          if (lane >= o) in += y;
-        }
-        small[kSmDigitBase + (kDepthPasses + p) * 256 + d0 + lane] = carry + in - c;
-        carry += __shfl_sync(0xffffffffu, in, 31);
-      }
-    }
+  if (!kTileSort) {
+    if (!grid_barrier(S, J, ++nbar * G, true)) return;
+    uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
+    depth_scan(S, J, s_grid, s_grid + J.gwords, G, nbar);
   }
 }
 
@@ -925,18 +981,15 @@ int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); 
 size_t depth_sort_smem(const gs::Cam& k) {
   return sizeof(SortSmem<kDepthItems>) + sizeof(uint32_t) * ((size_t)grid_words(k) + kDepthPasses * 256);
 }
-int depth_sort_grid(const gs::Cam& k, int64_t n) {
-  return radix_grid<kDepthItems, false>(depth_sort_smem(k), sort_tiles<kDepthItems>(n));
+int depth_sort_grid(const gs::Cam& k, int64_t n) {  // one CTA more than radix tiles if it fits
+  return radix_grid<kDepthItems, false>(depth_sort_smem(k), sort_tiles<kDepthItems>(n) + 1);
 }
 // private difference grids the workspace holds: at most one per resident CTA (2048 threads
 // per SM), at most one per radix tile of the depth sort
 int64_t depth_grids_bound(int64_t n) {
-  return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n), (int64_t)gs::num_sms() * 8));
+  return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n) + 1, (int64_t)gs::num_sms() * 8));
 }
-size_t tile_counts_smem(const gs::Cam& k) {
-  return sizeof(uint32_t) * ((size_t)grid_words(k) + (size_t)kMaxTilePasses * 256);
-}
-constexpr size_t kMaxTileCountsSmem = 200 * 1024;
+constexpr size_t kMaxSortSmem = 227 * 1024;  // shared memory a CTA may have
 
 }  // namespace
 
@@ -962,7 +1015,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
   const gs::Cam k = gs::make_cam(*cam);
   const int tpasses = tile_passes(k);
   const int64_t T = (int64_t)k.Tx * k.Ty;
-  if (tpasses > kMaxTilePasses || tile_counts_smem(k) > kMaxTileCountsSmem)
+  if (tpasses > 2 || depth_sort_smem(k) > kMaxSortSmem)  // the tile counts handle two passes
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: %d x %d tiles exceed the supported grid", k.Tx, k.Ty);
   const size_t need = carve(nullptr, nullptr, n, capacity, tpasses, grid_words(k), T, depth_grids_bound(n));
   if (workspace_bytes < need)
@@ -978,12 +1031,11 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
       cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * T, st) != cudaSuccess)
     return gs::check_launch("gs_bin_sort memset");
   if (n > 0) {
-    const int64_t chunks = (n + kScanChunk - 1) / kScanChunk;
-    if (cudaMemsetAsync(w.scan_state, 0, sizeof(unsigned long long) * chunks, st) != cudaSuccess)
-      return gs::check_launch("gs_bin_sort memset");
     const int sms = gs::num_sms();
     // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys; phase 0 also
-    //    builds the difference grid of per-tile instance counts
+    //    builds the difference grid of per-tile instance counts, and after the passes the
+    //    tiles-touched scan gives every sorted Gaussian's first slot (and M), the tile counts
+    //    the staged ranges and the digit bases of the tile passes
     if (cudaMemsetAsync(w.grid, 0, sizeof(uint32_t) * (size_t)grid_words(k), st) != cudaSuccess)
       return gs::check_launch("gs_bin_sort memset");
     const size_t dsmem = depth_sort_smem(k);
@@ -995,20 +1047,12 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     dj.hist = w.hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
     dj.small = w.small; dj.count = count; dj.limit = limit; dj.drop_arrival = drop == 2;
     dj.proj = proj; dj.Tx = k.Tx; dj.Ty = k.Ty; dj.gwords = (int)grid_words(k); dj.grids = w.grids; dj.grid = w.grid;
+    dj.chunk_tot = w.chunk_tot; dj.grec = w.grec; dj.slice_first = w.slice_first; dj.tcap = capacity;
+    dj.rstage = w.rstage; dj.tpasses = tpasses;
     if (cudaError_t e = launch_radix<kDepthItems, false>(dj, dgrid, dsmem, st))
       return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
-    // 2. (tile, index) pairs in depth order; per-tile counts into the difference grid
-    k_scan_dup<<<(unsigned)chunks, kScanThreads, 0, st>>>(proj, n, w.dkey[0], w.didx[0], k, w.slice_first, w.grec,
-                                                           capacity, w.scan_state, w.small, count, limit, drop == 1);
-    if (gs_status s = gs::check_launch("gs_bin_sort scan")) return s;
-    // 3. tile counts -> staged ranges + digit offsets of the tile passes
-    static const cudaError_t attr = cudaFuncSetAttribute(k_tile_counts, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         (int)kMaxTileCountsSmem);
-    if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_bin_sort: %s", cudaGetErrorString(attr));
-    k_tile_counts<<<1, 1024, tile_counts_smem(k), st>>>(w.grid, k.Tx, k.Ty, tpasses, w.small, w.rstage, count);
-    if (gs_status s = gs::check_launch("gs_bin_sort tile counts")) return s;
-    // 4. stable sort of the instances by tile id: the first pass generates the (tile, index)
+    // 2. stable sort of the instances by tile id: the first pass generates the (tile, index)
     //    pairs in depth order from the scan's records, the last writes the caller's arrays
     RadixJob tj{};
     tj.key[0] = w.tkey[0]; tj.key[1] = w.tkey[1];
@@ -1016,7 +1060,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     tj.n_host = -1; tj.cap = capacity; tj.passes = tpasses;
     tj.slot0 = kDepthPasses; tj.sort_id = 1;
     tj.hist = w.hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
-    tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = 0;
+    tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = drop == 1;
     tj.gen = GenSource{w.slice_first, w.grec, n, k.Tx};
     tj.q0 = reinterpret_cast<const float4*>(proj); tj.keys64 = keys; tj.vals_out = vals;
     if (cudaError_t e = launch_radix<kTileItems, true>(

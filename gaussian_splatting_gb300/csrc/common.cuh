@@ -79,7 +79,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-// Bounded-wait loads/stores for single-pass (decoupled look-back) algorithms.
+// Acquire loads / release stores for flags other CTAs poll (grid barriers).
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

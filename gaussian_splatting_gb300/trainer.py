@@ -32,9 +32,9 @@ MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
 
 def bin_sort_launches(cam) -> int:
-    # depth sort (keys, tile-count grid and all four passes in one cooperative launch), scan,
-    # tile counts, tile sort (both passes in one cooperative launch), ranges
-    return 5
+    # depth sort (keys, tile-count grid, the four passes, the tiles-touched scan and the tile
+    # counts in one cooperative launch), tile sort (both passes, likewise), ranges
+    return 3
 
 
 @dataclasses.dataclass

@@ -100,8 +100,8 @@ gs_status gs_project(const float* params, int64_t n, const gs_camera* cam, float
  *              not valid and ranges are left empty.
  *   count_host optional host int64: if non-NULL the call synchronises the stream, stores
  *              M there, and returns GS_ERR_CAPACITY / GS_ERR_TIMEOUT per count[1].
- * capacity must be < 2^30.  The device-side waits of the single-pass scan and of the
- * radix passes are bounded; none can hang.
+ * capacity must be < 2^30.  The device-side waits (grid barriers) are bounded; none can
+ * hang.
  */
 size_t gs_bin_sort_workspace_size(int64_t n, int64_t capacity, const gs_camera* cam);
 gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
@@ -259,14 +259,13 @@ gs_status gs_probe_ffma(float* out, int blocks, int iters, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Test hooks (no counterpart in the method).
- * gs_debug_set_wait_limit: iterations a device-side wait (a look-back flag or a grid
- *   barrier) spins before it gives up and reports status bit 2 (default 1 << 22; values
- *   < 1 restore it).
- * gs_debug_drop_publish: arms the next gs_bin_sort call only.  mode 1: the tiles-touched
- *   scan never publishes chunk 0's prefix, so every later chunk's look-back wait runs out;
- *   mode 2: CTA 0 of the depth sort never arrives at its first grid barrier, so every
- *   CTA's barrier wait runs out; 0 disarms.  Used to test that the bounded waits report
- *   GS_ERR_TIMEOUT instead of hanging.
+ * gs_debug_set_wait_limit: iterations a device-side wait (a grid barrier of gs_bin_sort's
+ *   cooperative launches) spins before it gives up and reports status bit 2 (default
+ *   1 << 22; values < 1 restore it).
+ * gs_debug_drop_publish: arms the next gs_bin_sort call only.  mode 1: CTA 0 of the tile
+ *   sort never arrives at its first grid barrier; mode 2: the same in the depth sort; every
+ *   other CTA's barrier wait then runs out; 0 disarms.  Used to test that the bounded waits
+ *   report GS_ERR_TIMEOUT instead of hanging.
  */
 void gs_debug_set_wait_limit(int64_t iterations);
 void gs_debug_drop_publish(int mode);

@@ -75,5 +75,5 @@ def test_launch_count_bookkeeping():
     import scenes
     from gaussian_splatting_gb300.trainer import bin_sort_launches
     # every radix pass of a sort runs inside one cooperative launch
-    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 5
-    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 5
+    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 3
+    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 3

@@ -165,10 +165,10 @@ def test_bin_sort_all_culled_and_overflow():
     assert e.value.status == N.GS_ERR_CAPACITY
 
 
-@pytest.mark.parametrize("mode", [1, 2], ids=["scan-look-back", "grid-barrier"])
+@pytest.mark.parametrize("mode", [1, 2], ids=["tile-sort-barrier", "depth-sort-barrier"])
 def test_bin_sort_bounded_wait_reports_timeout(mode):
-    """A flag that nothing sets (a look-back publication, a barrier arrival): the wait gives
-    up and reports, and the GPU stays usable."""
+    """A flag that nothing sets (a grid-barrier arrival): every other CTA's wait gives up and
+    reports, and the GPU stays usable."""
     P, cam = scene(1, 100_000, 0)
     planes = proj_planes_from_oracle(oracle.project(P, cam))
     N.gs_debug_set_wait_limit(2000)
