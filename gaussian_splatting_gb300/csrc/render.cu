@@ -8,20 +8,23 @@
 // row band w / 2 (a square block meets fewer footprints than a 16x4 one); lane l owns column
 // l % 8 of the block and its two rows 2 (l / 8) + {0, 1}.  The tile's list is walked in
 // batches of 256 Gaussians gathered into shared memory (2 per thread).  While gathering,
-// each Gaussian gets a 4-bit mask of the warp blocks that the bounding box of its
-// alpha >= 1/255 ellipse touches (enlarged by a rounding slack), and every warp compacts the
-// batch, in order, into its own list: a warp never evaluates a Gaussian whose alpha is
-// below the skip threshold on all of its pixels.  Per-pixel results are those of walking the
-// full list.
+// each Gaussian gets a 4-bit mask of the warp blocks that its alpha >= 1/255 ellipse meets
+// (a box test, then the exact minimum of the quadratic form over the block, with a rounding
+// margin), and every warp compacts the batch, in order, into its own list: a warp never
+// evaluates a Gaussian whose alpha is below the skip threshold on all of its pixels.
+// Per-pixel results are those of walking the full list.  The per-pixel compositing is
+// branch-free: a pixel that does not take an entry gets weight zero and keeps its state.
 //
 // The conic is stored scaled by -log2(e)/2 so that alpha = opacity * 2^p costs one ex2, and
 // a per-Gaussian threshold p_min = log2(1/(255 opacity)) rejects pairs below the 1/255 skip
 // before the ex2.  Forward and backward evaluate every (pixel, Gaussian) pair through the
 // same functions, so the backward's T / (1 - alpha) recovery retraces the forward exactly.
 //
-// The backward sums a Gaussian's nine gradient terms over a thread's two pixels, then over
-// the warp with a transposed butterfly (16 shuffles instead of 45), and nine lanes add the
-// sums to grad2d with one warp-wide atomic instruction.
+// The backward takes two list entries per iteration: for each, a Gaussian's nine gradient
+// terms are summed over a thread's two pixels; then both entries' terms are summed over the
+// warp together (a 16-value transposed butterfly, 16 shuffles, and a 2-value one for the two
+// blue terms, 5 shuffles, instead of 90 for plain butterflies) and eighteen lanes add the sums
+// to grad2d with one warp-wide atomic instruction.
 #include "common.cuh"
 
 namespace {
@@ -264,31 +267,32 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
   }
 }
 
-// Warp sums of 8 per-lane values by a transposed butterfly: three halving levels (4 + 2 + 1
-// shuffles) leave lane L holding value k = L >> 2 summed over 8 lanes; two plain levels
-// finish it.  Afterwards lanes 4k .. 4k+3 hold the warp total of value k.
-__device__ __forceinline__ float warp_transpose_sum8(float (&v)[8], int lane) {
+// Warp sums of 16 per-lane values by a transposed butterfly: four halving levels (8 + 4 + 2 + 1 shuffles) leave lane L holding
+// value (L >> 1) summed over 16 lanes; one plain level finishes it, in lanes 2k and 2k + 1.
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int level = 0; level < 3; ++level) {
-    const int off = 16 >> level;  // 16, 8, 4
-    const int half = 4 >> level;  // values kept: 4, 2, 1
+  for (int level = 0; level < 4; ++level) {
+    const int off = 16 >> level;  // 16, 8, 4, 2
+    const int half = 8 >> level;  // values kept: 8, 4, 2, 1
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
-      // give away the half the partner keeps; add the partner's copy of the half kept here
       const float give = upper ? v[i] : v[i + half];
       const float keep = upper ? v[i + half] : v[i];
       v[i] = keep + __shfl_xor_sync(0xffffffffu, give, off);
     }
   }
-  float t = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
-  return t + __shfl_xor_sync(0xffffffffu, t, 1);
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Two values: one halving level leaves lanes 0..15 with value 0 and 16..31 with value 1,
+// four plain levels finish the sums.
+__device__ __forceinline__ float warp_transpose_sum2(const float (&v)[2], int lane) {
+  const bool upper = (lane & 16) != 0;
+  float t = (upper ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, upper ? v[0] : v[1], 16);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
 }
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -376,9 +380,14 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
         h0[i] = pos0 < last[i] && candidate(p0[i], c0.z);
         h1[i] = has1 && pos1 < last[i] && candidate(p1[i], c1.z);
       }
+      const bool any0 = __any_sync(0xffffffffu, h0[0] || h0[1]);
+      const bool any1 = __any_sync(0xffffffffu, h1[0] || h1[1]);
+      if (!(any0 || any1)) continue;
+      // per entry e: acc[8e + (du, dv, dopacity, dA, dB, dC, dr, dg)] and accb[e] = db
+      float acc[16];
+      float accb[2] = {0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int k = e ? k1 : k0;
         const float4 a = e ? a1 : a0;
         const float4 c = e ? c1 : c0;
         bool hit[kPPT];
@@ -388,63 +397,64 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
           hit[i] = e ? h1[i] : h0[i];
           p[i] = e ? p1[i] : p0[i];
         }
-        if (!__any_sync(0xffffffffu, hit[0] || hit[1])) continue;
-        // acc: du, dv, dopacity, dA, dB, dC, dr, dg (transposed); db separately
-        float acc[8];
-        float acc_b = 0.f;
-        {
-          const float4 col = S.s2[k];
-          const float dx = fx - a.x;
-          // moments over the thread's pixels (one column): sum dpow, dpow dy, dpow dy^2.
-          // Branch-free per pixel: a pixel that does not take the entry contributes zeros and
-          // keeps its state.
-          float m0 = 0.f, m1 = 0.f, m2 = 0.f, a6 = 0.f, a7 = 0.f, a2 = 0.f;
 #pragma unroll
-          for (int i = 0; i < kPPT; ++i) {
-            const float G = fast_exp2(p[i]);
-            const float alpha = alpha_of(c.y, G);
-            const bool take = hit[i] && alpha >= kAlphaMin;
-            const float dy = fy[i] - a.y;
-            const float iom = rcp_approx(__fsub_rn(1.f, alpha));
-            T[i] = take ? T[i] * iom : T[i];
-            const float w = take ? alpha * T[i] : 0.f;
-            a6 = fmaf(w, dr[i], a6);
-            a7 = fmaf(w, dg[i], a7);
-            acc_b = fmaf(w, db[i], acc_b);
-            const float cd = col.x * dr[i] + col.y * dg[i] + col.z * db[i];
-            const float dalpha = T[i] * cd - U[i] * iom;
-            U[i] = fmaf(w, cd, U[i]);
-            const bool unclamped = take && __fmul_rn(c.y, G) <= kAlphaMax;
-            const float dpow = unclamped ? dalpha * alpha : 0.f;  // d alpha / d power = alpha
-            a2 = unclamped ? fmaf(dalpha, G, a2) : a2;
-            const float t = dpow * dy;
-            m0 += dpow;
-            m1 += t;
-            m2 = fmaf(t, dy, m2);
-          }
-          // power = -(A dx^2 + C dy^2)/2 - B dx dy, natural conic from the log2-scaled record
-          const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
-          const float dxm0 = dx * m0;
-          acc[0] = fmaf(A, dxm0, B * m1);
-          acc[1] = fmaf(B, dxm0, C * m1);
-          acc[2] = a2;
-          acc[3] = -0.5f * dx * dxm0;
-          acc[4] = -dx * m1;
-          acc[5] = -0.5f * m2;
-          acc[6] = a6;
-          acc[7] = a7;
+        for (int v = 0; v < 8; ++v) acc[8 * e + v] = 0.f;
+        if (!(e ? any1 : any0)) continue;  // warp-uniform
+        const float4 col = S.s2[e ? k1 : k0];
+        const float dx = fx - a.x;
+        // moments over the thread's pixels (one column): sum dpow, dpow dy, dpow dy^2.
+        // Branch-free per pixel: a pixel that does not take the entry contributes zeros and
+        // keeps its state.
+        float m0 = 0.f, m1 = 0.f, m2 = 0.f, a6 = 0.f, a7 = 0.f, a2 = 0.f, ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPPT; ++i) {
+          const float G = fast_exp2(p[i]);
+          const float alpha = alpha_of(c.y, G);
+          const bool take = hit[i] && alpha >= kAlphaMin;
+          const float dy = fy[i] - a.y;
+          const float iom = rcp_approx(__fsub_rn(1.f, alpha));
+          T[i] = take ? T[i] * iom : T[i];
+          const float w = take ? alpha * T[i] : 0.f;
+          a6 = fmaf(w, dr[i], a6);
+          a7 = fmaf(w, dg[i], a7);
+          ab = fmaf(w, db[i], ab);
+          const float cd = col.x * dr[i] + col.y * dg[i] + col.z * db[i];
+          const float dalpha = T[i] * cd - U[i] * iom;
+          U[i] = fmaf(w, cd, U[i]);
+          const bool unclamped = take && __fmul_rn(c.y, G) <= kAlphaMax;
+          const float dpow = unclamped ? dalpha * alpha : 0.f;  // d alpha / d power = alpha
+          a2 = unclamped ? fmaf(dalpha, G, a2) : a2;
+          const float t = dpow * dy;
+          m0 += dpow;
+          m1 += t;
+          m2 = fmaf(t, dy, m2);
         }
-        const float tot = warp_transpose_sum8(acc, lane);
-        const float tot_b = warp_sum(acc_b);
-        // lanes 4k hold value k of (du, dv, dopacity, dA, dB, dC, dr, dg); lane 1 adds db
-        const uint32_t g = __float_as_uint(c.w);
-        float* rec = grad2d + 12 * (int64_t)g;
-        if ((lane & 3) == 0) {
-          const int kv = lane >> 2;
+        // power = -(A dx^2 + C dy^2)/2 - B dx dy, natural conic from the log2-scaled record
+        const float A = a.z * (-2.f / kLog2e), B = a.w * (-1.f / kLog2e), C = c.x * (-2.f / kLog2e);
+        const float dxm0 = dx * m0;
+        acc[8 * e + 0] = fmaf(A, dxm0, B * m1);
+        acc[8 * e + 1] = fmaf(B, dxm0, C * m1);
+        acc[8 * e + 2] = a2;
+        acc[8 * e + 3] = -0.5f * dx * dxm0;
+        acc[8 * e + 4] = -dx * m1;
+        acc[8 * e + 5] = -0.5f * m2;
+        acc[8 * e + 6] = a6;
+        acc[8 * e + 7] = a7;
+        accb[e] = ab;
+      }
+      // both entries' sixteen values in one transposed reduction: lanes 2k, 2k+1 hold value k;
+      // the two db values in a second one: lanes 0..15 hold entry 0's, 16..31 entry 1's
+      const float tot = warp_transpose_sum16(acc, lane);
+      const float tot_b = warp_transpose_sum2(accb, lane);
+      if ((lane & 1) == 0) {
+        const int kk = lane >> 1, e = kk >> 3, kv = kk & 7;
+        if (e ? any1 : any0) {
+          float* rec = grad2d + 12 * (int64_t)__float_as_uint(e ? c1.w : c0.w);
           atomicAdd(rec + kv + (kv >= 3 ? 1 : 0) + (kv >= 6 ? 1 : 0), tot);
-        } else if (lane == 1) {
-          atomicAdd(rec + 10, tot_b);
         }
+      } else if (lane == 1 || lane == 17) {
+        const int e = lane >> 4;
+        if (e ? any1 : any0) atomicAdd(grad2d + 12 * (int64_t)__float_as_uint(e ? c1.w : c0.w) + 10, tot_b);
       }
     }
   }
