@@ -236,10 +236,12 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
             T[i] = acc ? Tn : T[i];
             last[i] = acc ? pos + 1u : last[i];
             if (kCount) used[i] += acc ? 1u : 0u;
-            done[i] = done[i] || term;
-            fy[i] = term ? kParkedRow : fy[i];
-            stop[i] = term ? pos + 1u : stop[i];
-            ended = ended || term;
+            if (term) {  // at most once per pixel: a branch that is almost never taken
+              done[i] = true;
+              fy[i] = kParkedRow;
+              stop[i] = pos + 1u;
+              ended = true;
+            }
           }
         }
       }
