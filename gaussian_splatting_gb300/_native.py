@@ -203,7 +203,7 @@ def gs_sparse_adam(params, grads, exp_avg, exp_avg_sq, n, idx, n_idx, max_idx, l
 def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, step,
                         counts=None, n_counts=0, stream=None):
     batch = len(cams)
-    carr = (Camera * batch)(*[camera(c) for c in cams])
+    carr = (Camera * batch)(*[c if isinstance(c, Camera) else camera(c) for c in cams])
     parr = (C.c_void_p * batch)(*[_ptr(p) for p in projs])
     garr = (C.c_void_p * batch)(*[_ptr(g) for g in grad2ds])
     _check(load().gs_project_bwd_adam(_ptr(params), n, C.cast(carr, C.c_void_p), batch, C.cast(parr, C.c_void_p),

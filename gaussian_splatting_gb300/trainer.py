@@ -102,7 +102,11 @@ class Trainer:
         self.sort_ws = None
 
     def _sort_ws(self, cam):
-        need = N.gs_bin_sort_workspace_size(self.n, self.capacity, cam)
+        # every view of a trainer has the same image size: the size depends on the capacity only
+        if self._ws_cam != self.capacity:
+            self._ws_need = N.gs_bin_sort_workspace_size(self.n, self.capacity, cam)
+            self._ws_cam = self.capacity
+        need = self._ws_need
         if self.sort_ws is None or self.sort_ws.numel() < need:
             self.sort_ws = torch.empty(need, dtype=torch.uint8, device=self.params.device)
         return self.sort_ws
@@ -161,25 +165,28 @@ class Trainer:
         launches = 0
         T = self._timed
         fused = adam and B <= MAX_FUSED_BATCH
-        for b, cam in enumerate(cams):
+        # marshal once per step: the cameras as gs_camera structs, the stream as a handle
+        ccams = [N.camera(c) for c in cams]
+        st = torch.cuda.current_stream().cuda_stream
+        for b, cam in enumerate(ccams):
             proj = self.proj[b]
-            T("project", N.gs_project, self.params, n, cam, proj)
+            T("project", N.gs_project, self.params, n, cam, proj, stream=st)
             ws = self._sort_ws(cam)
             T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), None, self.vals, self.capacity,
-              self.ranges, self.counts[b])
+              self.ranges, self.counts[b], stream=st)
             work_buf = None
             if self.work is not None:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
             T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
-              self.n_contrib, work_buf)
+              self.n_contrib, work_buf, stream=st)
             if ready is not None:
                 torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
-              self.dimg, self.loss_ws, self.loss_ws.numel())
+              self.dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
             T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
-              self.n_contrib, self.dimg, self.grad2d[b])
+              self.n_contrib, self.dimg, self.grad2d[b], stream=st)
             if not fused:
-                T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads)
+                T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads, stream=st)
                 launches += LAUNCHES["project_bwd"]
             if self.work is not None:
                 # (entries evaluated in the forward, entries accumulated, entries walked by the backward,
@@ -188,17 +195,17 @@ class Trainer:
                                   int(work_buf[2].sum())))
             launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in ("project", "render_fwd", "loss", "render_bwd"))
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
-          self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard)
+          self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard, stream=st)
         launches += LAUNCHES["visible_sets"]
         if fused:
-            T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, list(cams), [self.proj[b] for b in range(B)],
+            T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, ccams, [self.proj[b] for b in range(B)],
               [self.grad2d[b] for b in range(B)], self.exp_avg, self.exp_avg_sq, self.lr, self.betas[0],
-              self.betas[1], self.eps, self.t + 1, self.counts, B)
+              self.betas[1], self.eps, self.t + 1, self.counts, B, stream=st)
             launches += LAUNCHES["project_bwd_adam"]
         elif adam:
             T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,
               self.union_idx, self.n_union, n, self.lr, self.betas[0], self.betas[1], self.eps, B, self.t + 1,
-              self.counts, B)
+              self.counts, B, stream=st)
             launches += LAUNCHES["sparse_adam"]
         self.launches = launches
 
