@@ -19,6 +19,8 @@ from __future__ import annotations
 
 import dataclasses
 
+import numpy as np
+
 import torch
 
 from . import _native as N
@@ -85,6 +87,8 @@ class Trainer:
         self.capacity = 0
         self.vals = self.sort_ws = None
         self.copy_stream = None
+        self.host_out = None
+        self._cam_cache = {}
         self.launches = 0
         self.timer = None  # list of (name, start event, end event) when timing per call
         self.work = None   # list of per-view work counts when measuring (synchronises)
@@ -100,6 +104,19 @@ class Trainer:
         self._ws_cam = None
         self.capacity = capacity
         self.sort_ws = None
+
+    def _camera(self, cam):
+        """gs_camera struct of a camera, converted once per distinct camera (keyed by content)."""
+        if isinstance(cam, N.Camera):
+            return cam
+        key = (np.asarray(cam.R, np.float32).tobytes(), np.asarray(cam.t, np.float32).tobytes(), cam.fx, cam.fy,
+               cam.cx, cam.cy, cam.znear, cam.width, cam.height)
+        hit = self._cam_cache.get(key)
+        if hit is None:
+            if len(self._cam_cache) > 4096:
+                self._cam_cache.clear()
+            hit = self._cam_cache[key] = N.camera(cam)
+        return hit
 
     def _sort_ws(self, cam):
         # every view of a trainer has the same image size: the size depends on the capacity only
@@ -158,7 +175,7 @@ class Trainer:
         e.record()
         self.timer.append((name, s, e))
 
-    def _enqueue(self, cams, targets: torch.Tensor, adam: bool = True, ready=None):
+    def _enqueue(self, cams, targets: torch.Tensor, adam: bool = True, ready=None, host_targets=None):
         B = len(cams)
         n, W, H = self.n, self.width, self.height
         inv_b = 1.0 / B
@@ -166,8 +183,12 @@ class Trainer:
         T = self._timed
         fused = adam and B <= MAX_FUSED_BATCH
         # marshal once per step: the cameras as gs_camera structs, the stream as a handle
-        ccams = [N.camera(c) for c in cams]
+        ccams = [self._camera(c) for c in cams]
         st = torch.cuda.current_stream().cuda_stream
+        step_start = None
+        if host_targets is not None:  # marks the point the target uploads may start from
+            step_start = torch.cuda.Event()
+            step_start.record()
         for b, cam in enumerate(ccams):
             proj = self.proj[b]
             T("project", N.gs_project, self.params, n, cam, proj, stream=st)
@@ -179,6 +200,8 @@ class Trainer:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
             T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
               self.n_contrib, work_buf, stream=st)
+            if host_targets is not None and ready is None:  # after the first view's compositing
+                ready = self._upload(host_targets, B, step_start)
             if ready is not None:
                 torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
@@ -217,20 +240,21 @@ class Trainer:
         """
         return self._step_async(cams, targets, adam, None)
 
-    def _step_async(self, cams, targets, adam, ready):
+    def _step_async(self, cams, targets, adam, ready, host_targets=None):
         if self.capacity == 0:
             self.reserve(cams)
-        self._enqueue(cams, targets, adam, ready)
+        self._enqueue(cams, targets, adam, ready, host_targets)
         if adam:
             self.t += 1
         return StepResult(self.loss, self.counts)
 
-    def _upload(self, targets: torch.Tensor, B: int):
-        """Copy host targets into target_dev on the side stream; returns one event per view."""
+    def _upload(self, targets: torch.Tensor, B: int, after: torch.cuda.Event):
+        """Copy host targets into target_dev on the side stream once `after` (recorded before the
+        step's first kernel) has passed; returns one event per view."""
         if self.copy_stream is None:
             self.copy_stream = torch.cuda.Stream(device=self.params.device)
         cs = self.copy_stream
-        cs.wait_stream(torch.cuda.current_stream())  # target_dev no longer read by earlier work
+        cs.wait_event(after)  # target_dev no longer read by earlier steps
         events = []
         with torch.cuda.stream(cs):
             for b in range(B):
@@ -244,18 +268,26 @@ class Trainer:
         """One training step over the views ``cams``; returns the batch loss (host float).
 
         ``targets`` may be a device tensor or a (pinned) host tensor [B, 3, H, W].  Host
-        targets are copied in view by view on a side stream; view b's loss waits only for its
-        own copy, so the uploads overlap the projection, binning and compositing.
+        targets are copied in view by view on a side stream, enqueued once the first view's
+        projection, binning and compositing are; view b's loss waits only for its own copy.
+        The status words and the loss come back in one synchronisation.
         """
-        ready = None
-        if targets.device.type != "cuda":
-            ready = self._upload(targets, len(cams))
+        host = targets if targets.device.type != "cuda" else None
+        if host is not None:
             targets = self.target_dev
+        if self.host_out is None:
+            self.host_out = (torch.empty((self.batch, 2), dtype=torch.int64).pin_memory(),
+                             torch.empty(1, dtype=torch.float32).pin_memory())
         while True:
-            res = self._step_async(cams, targets, adam, ready)
-            counts = res.status.cpu()
+            res = self._step_async(cams, targets, adam, None, host)
+            host = None  # a re-run reuses the uploaded targets
+            hc, hl = self.host_out
+            hc.copy_(res.status, non_blocking=True)
+            hl.copy_(res.loss, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            counts = hc
             if int(counts[: len(cams), 1].abs().sum()) == 0:
-                return float(res.loss.item())
+                return float(hl[0])
             if adam:
                 self.t -= 1
             if int(counts[:, 1].bitwise_and(2).sum()) != 0:
