@@ -833,6 +833,8 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     uint32_t* kout = J.key[(p + 1) & 1];
     uint32_t* vout = fin ? J.vals_out : J.val[(p + 1) & 1];
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+      // this tile's global digit offsets, loaded now and used after the ranking
+      const uint32_t tile_base = J.hist[(int64_t)tid * J.hist_stride + tile];
       for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
       __syncthreads();
       const int64_t base = tile * kTile;
@@ -882,7 +884,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
           run += c;
         }
         const uint32_t cnt = run;
-        S.gbase[d] = J.hist[(int64_t)d * J.hist_stride + tile];
+        S.gbase[d] = tile_base;
         uint32_t incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
