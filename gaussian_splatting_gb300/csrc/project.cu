@@ -106,14 +106,11 @@ struct SharedParams {
   __device__ __forceinline__ float4 plane(int pl) const { return s[pl * kThreadsPerCta + t]; }
 };
 
-// Returns false if the Gaussian is culled.
+// The view-independent part of the forward: scales, opacity, normalised quaternion, its
+// rotation and the 3-D covariance.
 template <class Src>
-__device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& f) {
+__device__ __forceinline__ void project_intrinsics(const Src& src, Fwd& f) {
   const float4 p0 = src.plane(0);
-  f.px = k.R[0] * p0.x + k.R[1] * p0.y + k.R[2] * p0.z + k.t[0];
-  f.py = k.R[3] * p0.x + k.R[4] * p0.y + k.R[5] * p0.z + k.t[1];
-  f.pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
-  if (!(f.pz > k.znear)) return false;
   const float4 p1 = src.plane(1);
   const float4 p2 = src.plane(2);
   f.s[0] = expf(p1.x);
@@ -138,6 +135,17 @@ __device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& 
   f.Sg[3] = M[3] * M[3] + M[4] * M[4] + M[5] * M[5];
   f.Sg[4] = M[3] * M[6] + M[4] * M[7] + M[5] * M[8];
   f.Sg[5] = M[6] * M[6] + M[7] * M[7] + M[8] * M[8];
+}
+
+// The view-dependent part, on a Fwd whose intrinsics are set.  Returns false if the Gaussian
+// is culled in this view.
+template <class Src>
+__device__ __forceinline__ bool project_view(const Src& src, const Cam& k, Fwd& f) {
+  const float4 p0 = src.plane(0);
+  f.px = k.R[0] * p0.x + k.R[1] * p0.y + k.R[2] * p0.z + k.t[0];
+  f.py = k.R[3] * p0.x + k.R[4] * p0.y + k.R[5] * p0.z + k.t[1];
+  f.pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
+  if (!(f.pz > k.znear)) return false;
   const float iz = 1.f / f.pz;
   const float limx = 1.3f * (0.5f * (float)k.W / k.fx), limy = 1.3f * (0.5f * (float)k.H / k.fy);
   const float rx = f.px * iz, ry = f.py * iz;
@@ -183,6 +191,16 @@ __device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& 
   f.y0 = min(max((fv - r) >> 4, 0), k.Ty);
   f.y1 = min(max(((fv + r) >> 4) + 1, 0), k.Ty);
   return f.x0 < f.x1 && f.y0 < f.y1;
+}
+
+// The whole forward of one Gaussian in one view.  Returns false if it is culled.
+template <class Src>
+__device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& f) {
+  const float4 p0 = src.plane(0);
+  const float pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
+  if (!(pz > k.znear)) return false;  // the near-plane cull needs only the mean
+  project_intrinsics(src, f);
+  return project_view(src, k, f);
 }
 
 __global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ params, int64_t n, Cam k,
@@ -469,6 +487,8 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
     if (!((vis >> b) & 1u)) continue;  // culled in this view
     const float* g2 = bv.grad2d[b];
     const float4 g0 = ldg4(g2, 3 * i + 0), g1 = ldg4(g2, 3 * i + 1), g2v = ldg4(g2, 3 * i + 2);
+    // the view-independent part is recomputed per view: keeping it live across the views
+    // costs more in spilled registers than it saves
     Fwd f;
     if (!project_core(src, bv.k[b], f)) continue;
     seen = true;
