@@ -230,9 +230,11 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
 
 /* ---------------------------------------------------------------------------
  * gs_project_bwd_adam -- the batch's backward projection and its update in one pass:
- * exactly gs_project_bwd for every view b (gradients summed in view order, starting from
- * zero) followed by gs_sparse_adam over the Gaussians with radius > 0 in at least one view
- * (the union of the visible sets), except that the gradient planes are never written.
+ * gs_project_bwd for every view b (gradients summed in view order, starting from zero)
+ * followed by gs_sparse_adam over the Gaussians with radius > 0 in at least one view (the
+ * union of the visible sets), except that the gradient planes are never written and the
+ * update's quotient is formed with host-computed bias-correction factors and one fast
+ * division (a few ulp of the update).
  * The pages have no counterpart for this entry point as a separate call: it is the
  * composition of the two steps above, fused so that the gradients stay on chip.
  *   cams, proj_per_view, grad2d_per_view  HOST arrays of `batch` entries (the latter two
