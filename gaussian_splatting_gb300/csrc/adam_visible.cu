@@ -210,8 +210,8 @@ __global__ void k_vis_jaccard(int B, int64_t* inter, float* jac) {
 __global__ void __launch_bounds__(256) k_sparse_adam(float4* __restrict__ p, float4* __restrict__ g,
                                                      float4* __restrict__ m, float4* __restrict__ v, int64_t n,
                                                      const uint32_t* __restrict__ idx, const int64_t* n_idx,
-                                                     int64_t max_idx, float b1, float b2, float lr_b, float bc1,
-                                                     float bc2, float eps, const int64_t* counts, int n_counts) {
+                                                     int64_t max_idx, float b1, float b2, float lr_c, float ibc2,
+                                                     float eps, const int64_t* counts, int n_counts) {
   for (int c = 0; c < n_counts; ++c)
     if (counts[2 * c + 1] != 0) return;  // a view of this batch overflowed its binning
   const int64_t nu = min(*n_idx, max_idx);
@@ -229,7 +229,9 @@ __global__ void __launch_bounds__(256) k_sparse_adam(float4* __restrict__ p, flo
     for (int l = 0; l < 4; ++l) {
       ma[l] = b1 * ma[l] + (1.f - b1) * ga[l];
       va[l] = b2 * va[l] + (1.f - b2) * ga[l] * ga[l];
-      pa[l] -= lr_b * (ma[l] / bc1) / (sqrtf(va[l] / bc2) + eps);
+      // lr_c = lr' / (1 - beta1'^step), ibc2 = 1 / (1 - beta2'^step): host-computed factors and
+      // one fast division instead of two IEEE divisions (a few ulp of the update)
+      pa[l] -= __fdividef(lr_c * ma[l], sqrtf(va[l] * ibc2) + eps);
     }
     p[e] = pp;
     m[e] = mm;
@@ -316,7 +318,7 @@ extern "C" gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg,
   dim3 grid((unsigned)((per_plane + 255) / 256), 15);
   k_sparse_adam<<<grid, 256, 0, gs::as_stream(stream)>>>(
       reinterpret_cast<float4*>(params), reinterpret_cast<float4*>(grads), reinterpret_cast<float4*>(exp_avg),
-      reinterpret_cast<float4*>(exp_avg_sq), n, idx, n_idx, max_idx, (float)b1, (float)b2, (float)lr_b, (float)bc1,
-      (float)bc2, eps, counts, n_counts);
+      reinterpret_cast<float4*>(exp_avg_sq), n, idx, n_idx, max_idx, (float)b1, (float)b2, (float)(lr_b / bc1),
+      (float)(1.0 / bc2), eps, counts, n_counts);
   return gs::check_launch("gs_sparse_adam");
 }

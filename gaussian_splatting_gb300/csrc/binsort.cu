@@ -313,7 +313,7 @@ __device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J,
       const uint4 rec = __ldg(&G.grec[first + o - 1u]);
       const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
       const uint32_t w = max(rec.z, 1u);
-      uint32_t row = (uint32_t)__fmul_rz((float)j, __frcp_rn((float)w));  // j / w, corrected below
+      uint32_t row = (uint32_t)__fmul_rz((float)j, __fdividef(1.f, (float)w));  // j / w within 1, corrected below
       int rem = (int)j - (int)(row * w);
       if (rem < 0) { --row; rem += (int)w; }
       if (rem >= (int)w) { ++row; rem -= (int)w; }

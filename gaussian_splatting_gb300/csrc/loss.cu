@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kThreads) k_loss_fused(const float* __restrict
         const float sxx = a[2][q] - mx * mx, syy = a[3][q] - my * my, sxy = a[4][q] - mx * my;
         const float A1 = 2.f * mx * my + C1, A2 = 2.f * sxy + C2;
         const float B1 = mx * mx + my * my + C1, B2 = sxx + syy + C2;
-        const float iB1 = 1.f / B1, iB2 = 1.f / B2;  // two reciprocals serve all four quotients
+        // two fast reciprocals (B1 >= C1, B2 >= C2 - rounding: far from zero) serve all four quotients
+        const float iB1 = __fdividef(1.f, B1), iB2 = __fdividef(1.f, B2);
         const float iB = iB1 * iB2;
         const float Sv = A1 * A2 * iB;
         dv[rd][q][0] = 2.f * my * (A2 - A1) * iB - 2.f * mx * Sv * (iB1 - iB2);  // dS/dmu_x

@@ -63,11 +63,15 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
   // bounding box of {d : d^T conic d <= K}, K = 2 ln(255 opacity): half-widths sqrt(K Sigma_xx),
   // sqrt(K Sigma_yy) with Sigma = conic^-1; enlarged so rounding never drops a reachable pair
   uint32_t m = 0;
-  const float K = 2.0f * logf(255.0f * q0.w);
+  // (fast intrinsics: the 0.1 % + 0.05 px box slack and the exact test's margin absorb their
+  // few-ulp errors, and culling only ever skips pairs no pixel can accept)
+  const float Kr = 2.0f * __logf(255.0f * q0.w);
+  const float K = fmaxf(Kr, 0.f);  // opacity at the 1/255 threshold within the log's error: keep it
   const float det = q1.x * q1.z - q1.y * q1.y;
-  if (K > 0.f && det > 0.f) {
-    const float hx = sqrtf(K * q1.z / det) * 1.001f + 0.05f;
-    const float hy = sqrtf(K * q1.x / det) * 1.001f + 0.05f;
+  if (Kr > -1e-5f && det > 0.f) {
+    const float idet = __fdividef(1.f, det);
+    const float hx = sqrtf(K * q1.z * idet) * 1.001f + 0.05f;
+    const float hy = sqrtf(K * q1.x * idet) * 1.001f + 0.05f;
     // Per warp block (8x8 pixels, block w at column band w & 1, row band w >> 1): the box test,
     // then the exact test: the minimum of q(d) = A dx^2 + 2B dx dy + C dy^2 over the block's
     // rectangle of pixel centres (d relative to the mean) against K.  q is convex; its minimum
@@ -76,14 +80,14 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
     // columns gives the minimum over the rectangle.  The margin keeps every block whose pixels
     // the fp32 candidate test could accept.
     const float A = q1.x, B = q1.y, C = q1.z;
-    const float rBA = -B / A, Kk = K * 1.001f + 1e-3f;
+    const float rBA = -__fdividef(B, A), rBC = -__fdividef(B, C), Kk = K * 1.001f + 1e-3f;
 #pragma unroll
     for (int bx = 0; bx < 2; ++bx) {
       const float xmin = (float)(tile_x0 + 8 * bx) + 0.5f, xmax = xmin + 7.0f;
       if (!(q0.x + hx >= xmin && q0.x - hx <= xmax)) continue;
       const float X0 = xmin - q0.x, X1 = xmax - q0.x;
       const float xe = X0 > 0.f ? X0 : (X1 < 0.f ? X1 : 0.f);
-      const float dys = -B * xe / C;
+      const float dys = rBC * xe;
 #pragma unroll
       for (int by = 0; by < 2; ++by) {
         const float ymin = (float)(tile_y0 + 8 * by) + 0.5f, ymax = ymin + 7.0f;
@@ -95,7 +99,7 @@ __device__ __forceinline__ void gather_record(const float* __restrict__ proj, in
         }
       }
     }
-  } else if (!(det > 0.f) && K > 0.f) {
+  } else if (!(det > 0.f) && Kr > -1e-5f) {
     m = (1u << kWarps) - 1u;  // degenerate record: keep it everywhere
   }
   S.mask[slot] = m;

@@ -212,7 +212,9 @@ gs_status gs_visible_sets(const float* const* proj_per_view, int batch, int64_t 
  * the Grendel-GS notes §4.2: lr' = lr sqrt(batch), beta1' = beta1^batch,
  * beta2' = beta2^batch.  For every float of the listed Gaussians' 15 planes:
  *   m = beta1' m + (1 - beta1') g;  v = beta2' v + (1 - beta2') g^2;
- *   p -= lr' (m / (1 - beta1'^step)) / (sqrt(v / (1 - beta2'^step)) + eps);  g = 0.
+ *   p -= lr' (m / (1 - beta1'^step)) / (sqrt(v / (1 - beta2'^step)) + eps);  g = 0
+ * (the two bias corrections are applied as host-computed factors and the quotient by a
+ * fast division: the update is exact to a few ulp).
  * Gaussians not listed keep p, m, v and g bit-for-bit.
  *   idx     union_idx from gs_visible_sets (strictly ascending, each < n).
  *   n_idx   DEVICE int64 count of idx entries (<= max_idx); read by the kernel so the
@@ -232,9 +234,7 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
  * gs_project_bwd_adam -- the batch's backward projection and its update in one pass:
  * gs_project_bwd for every view b (gradients summed in view order, starting from zero)
  * followed by gs_sparse_adam over the Gaussians with radius > 0 in at least one view (the
- * union of the visible sets), except that the gradient planes are never written and the
- * update's quotient is formed with host-computed bias-correction factors and one fast
- * division (a few ulp of the update).
+ * union of the visible sets), except that the gradient planes are never written.
  * The pages have no counterpart for this entry point as a separate call: it is the
  * composition of the two steps above, fused so that the gradients stay on chip.
  *   cams, proj_per_view, grad2d_per_view  HOST arrays of `batch` entries (the latter two
