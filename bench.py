@@ -50,10 +50,10 @@ HBM_FALLBACK_GBS = 6800.0
 # the benchmark workload, keyed by entry point, valid only for the kernel source it was measured
 # on: when the source file's hash differs the figure is reported as null.
 NCU_TRAFFIC = {
-    # profiles/render_object-300k-1236x820.md: 38.318 MB read + 0.017 MB written per launch
+    # profiles/render_object-300k-1236x820.md: 38.313 MB read + 0.032 MB written per launch
     "render_bwd": {"source": "gaussian_splatting_gb300/csrc/render.cu",
                    "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
-                   "bytes": 38334976},
+                   "bytes": 38345472},
 }
 
 
@@ -349,7 +349,7 @@ def main():
     work_note = (f"per launch: {ev:.4g} pixel-Gaussian pairs evaluated through termination "
                  f"({used:.4g} accumulated, {walked:.4g} walked back; the forward's warps evaluated "
                  f"{warp_pairs:.4g}); fwd {FWD_FLOPS_PER_PAIR}, bwd {BWD_FLOPS_PER_PAIR} flops per evaluated pair")
-    # dominant single kernel: the entry points that launch one kernel (gs_bin_sort launches ~11)
+    # dominant single kernel: the entry points that launch one kernel (gs_bin_sort_batch launches several)
     single = [k for k in ("render_bwd", "render_fwd", "project", "project_bwd", "sparse_adam", "project_bwd_adam")
               if k in per_call]
     dominant = max(single, key=lambda k: sum(per_call[k]))
@@ -425,8 +425,10 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": {**workload, "l2": "flushed between timed steps (512 MB write)",
                            "parallelism": "replicas" if world > 1 else "single"},
-                "roofline": roof, "kernels": {"ms_avg": {k: round(v, 4) for k, v in avg.items()},
-                                              "share": {k: round(v, 4) for k, v in share.items()}, **others},
+                "roofline": roof,
+                "kernels": {"ms_avg": {k: round(v, 4) for k, v in avg.items()},
+                            "calls": "bin_sort, visible_sets and project_bwd_adam once per batch, the rest once per view",
+                            "share": {k: round(v, 4) for k, v in share.items()}, **others},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk.summary(), "instances_per_view": int(st[:, 0].float().mean().item())}
         print(json.dumps(line), flush=True)

@@ -18,6 +18,7 @@ _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ER
 
 # every symbol include/gs.h declares
 EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_bin_sort_workspace_size", "gs_bin_sort",
+           "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
            "gs_probe_ffma", "gs_debug_set_wait_limit",
@@ -67,6 +68,8 @@ def load() -> C.CDLL:
         "gs_project": ([vp, i64, cp, vp, vp], i32),
         "gs_bin_sort_workspace_size": ([i64, i64, cp], sz),
         "gs_bin_sort": ([vp, i64, cp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
+        "gs_bin_sort_batch_workspace_size": ([i32, i64, i64, vp], sz),
+        "gs_bin_sort_batch": ([vp, i32, i64, vp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
         "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
         "gs_loss_workspace_size": ([i32, i32], sz),
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
@@ -142,6 +145,35 @@ def gs_bin_sort(proj, n, cam, workspace, workspace_bytes, keys, vals, capacity, 
                               capacity, _ptr(ranges), _ptr(count), C.byref(host) if sync else None,
                               _stream(stream)), "gs_bin_sort")
     return host.value if sync else None
+
+
+def _cams(cams):
+    arr = (Camera * len(cams))(*[c if isinstance(c, Camera) else camera(c) for c in cams])
+    return C.cast(arr, C.c_void_p), arr
+
+
+def _ptrs(xs):
+    arr = (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    return C.cast(arr, C.c_void_p), arr
+
+
+def gs_bin_sort_batch_workspace_size(batch, n, capacity, cams) -> int:
+    c = _cams(cams[:batch])
+    return load().gs_bin_sort_batch_workspace_size(batch, n, capacity, c[0])
+
+
+def gs_bin_sort_batch(projs, n, cams, workspace, workspace_bytes, keys, vals, capacity, ranges, counts, sync=False,
+                      stream=None):
+    """gs_bin_sort for len(cams) views; keys may be None or a list with None entries.  Returns
+    the per-view M (host list) when sync=True, else None."""
+    batch = len(cams)
+    c, p, v, r = _cams(cams), _ptrs(projs), _ptrs(vals), _ptrs(ranges)
+    k = _ptrs(keys) if keys is not None else (None, None)
+    host = (C.c_int64 * batch)()
+    _check(load().gs_bin_sort_batch(p[0], batch, n, c[0], _ptr(workspace), workspace_bytes, k[0], v[0], capacity,
+                                    r[0], _ptr(counts), C.cast(host, C.c_void_p) if sync else None,
+                                    _stream(stream)), "gs_bin_sort_batch")
+    return list(host) if sync else None
 
 
 def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, work=None, stream=None):

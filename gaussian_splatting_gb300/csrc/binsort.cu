@@ -12,26 +12,30 @@
 // about a third of the traffic of sorting all 64 key bits of 12-byte pairs.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   k_radix_sort  all stable 8-bit passes of one sort in a cooperative launch; each pass
-//                 counts digits per radix tile, scans the counts per digit over the tiles,
-//                 then ranks every tile in shared memory and writes digit-contiguous runs;
-//                 grid barriers separate the phases.  Used for the depth sort, whose phase 0
-//                 makes the depth keys (0xFFFFFFFF for culled Gaussians), their digit totals
+//   k_sort_init   zeroes the status words, the small block, the difference grid and the
+//                 caller's ranges of every view of a group (one launch instead of memsets).
+//   k_depth_sort  all stable 8-bit passes of the depth sorts of up to 8 views in one
+//                 cooperative launch (a group of CTAs per view, so the views' latency-bound
+//                 phases overlap).  Each pass counts digits per radix tile, scans the counts
+//                 per digit over the tiles, then ranks every tile in shared memory and writes
+//                 digit-contiguous runs; grid barriers (per view) separate the phases.  Phase
+//                 0 makes the depth keys (0xFFFFFFFF for culled Gaussians), their digit totals
 //                 and, per CTA, a difference grid of per-tile instance counts (4 corners per
-//                 visible Gaussian, summed into one grid in the next phase); and for the tile
-//                 sort, whose first pass generates its (tile, index) pairs from the scan's
-//                 records instead of reading them and whose last pass writes the caller's
-//                 values (and 64-bit keys if asked for).
-//                 After the depth passes the same launch runs the tiles-touched scan over
-//                 the sorted Gaussians (reduce, scan of the chunk sums, then each chunk's
-//                 records: first slot, rectangle, index; and for every radix tile of the
-//                 tile sort the Gaussian holding its first slot) and, on one CTA, the tile
-//                 counts (2-D prefix sums of the grid, their scan = staged ranges, digit
-//                 bases of the tile passes).
-//   k_publish_ranges  copies the staged ranges to the caller's array if nothing failed.
+//                 visible Gaussian, summed into one grid in the next phase).  After the passes
+//                 the same launch runs the tiles-touched scan over the sorted Gaussians
+//                 (reduce, scan of the chunk sums, then each chunk's records: first slot,
+//                 rectangle, index; and for every radix tile of the tile sort the Gaussian
+//                 holding its first slot) and, on one CTA, the tile counts (2-D prefix sums of
+//                 the grid, their scan = staged ranges, digit bases of the tile passes).
+//   k_tile_sort   the same passes for one view's instances by tile id: the first pass
+//                 generates its (tile, index) pairs from the scan's records instead of reading
+//                 them, the last writes the caller's values (and 64-bit keys if asked for).
+//   k_publish_ranges  copies each view's staged ranges to the caller's array if nothing failed.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -87,8 +91,11 @@ int tile_bits(int64_t T) {
 
 int tile_passes(const gs::Cam& k) { return std::max(1, (tile_bits((int64_t)k.Tx * k.Ty) + 7) / 8); }
 
-size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int64_t grid_words, int64_t n_tiles,
-             int n_grids) {
+// Workspace layout: the tile-sort buffers (capacity-sized, shared by the views, whose tile
+// sorts run one after another), then per view the depth-sort buffers and the scan's records.
+// w (if not NULL) receives `views` entries.
+size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_t grid_words, int64_t n_tiles,
+             int64_t n_grids) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -100,37 +107,40 @@ size_t carve(Workspace* w, char* base, int64_t n, int64_t cap, int tpasses, int6
   char* tk1 = take(sizeof(uint32_t) * (size_t)cap);
   char* tv0 = take(sizeof(uint32_t) * (size_t)cap);
   char* tv1 = take(sizeof(uint32_t) * (size_t)cap);
-  char* dk0 = take(sizeof(uint32_t) * (size_t)n);
-  char* dk1 = take(sizeof(uint32_t) * (size_t)n);
-  char* di0 = take(sizeof(uint32_t) * (size_t)n);
-  char* di1 = take(sizeof(uint32_t) * (size_t)n);
-  char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
-  char* lbd = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kDepthItems>(n));
   char* lbt = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kTileItems>(cap));
-  char* gr = take(sizeof(uint32_t) * (size_t)grid_words);
-  char* grs = take(sizeof(uint32_t) * (size_t)grid_words * (size_t)n_grids);
-  char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
-  char* go = take(sizeof(uint32_t) * (size_t)((cap + kSlice - 1) / kSlice));
-  char* gr4 = take(sizeof(uint4) * (size_t)n);
-  char* sm = take(sizeof(uint32_t) * kSmWords);
-  if (w) {
-    w->grid = reinterpret_cast<uint32_t*>(gr);
-    w->grids = reinterpret_cast<uint32_t*>(grs);
-    w->rstage = reinterpret_cast<uint32_t*>(rs);
-    w->slice_first = reinterpret_cast<uint32_t*>(go);
-    w->grec = reinterpret_cast<uint4*>(gr4);
-    w->tkey[0] = reinterpret_cast<uint32_t*>(tk0);
-    w->tkey[1] = reinterpret_cast<uint32_t*>(tk1);
-    w->tval[0] = reinterpret_cast<uint32_t*>(tv0);
-    w->tval[1] = reinterpret_cast<uint32_t*>(tv1);
-    w->dkey[0] = reinterpret_cast<uint32_t*>(dk0);
-    w->dkey[1] = reinterpret_cast<uint32_t*>(dk1);
-    w->didx[0] = reinterpret_cast<uint32_t*>(di0);
-    w->didx[1] = reinterpret_cast<uint32_t*>(di1);
-    w->chunk_tot = reinterpret_cast<unsigned long long*>(ss);
-    w->hist_depth = reinterpret_cast<uint32_t*>(lbd);
-    w->hist_tile = reinterpret_cast<uint32_t*>(lbt);
-    w->small = reinterpret_cast<uint32_t*>(sm);
+  for (int v = 0; v < views; ++v) {
+    char* dk0 = take(sizeof(uint32_t) * (size_t)n);
+    char* dk1 = take(sizeof(uint32_t) * (size_t)n);
+    char* di0 = take(sizeof(uint32_t) * (size_t)n);
+    char* di1 = take(sizeof(uint32_t) * (size_t)n);
+    char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
+    char* lbd = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kDepthItems>(n));
+    char* gr = take(sizeof(uint32_t) * (size_t)grid_words);
+    char* grs = take(sizeof(uint32_t) * (size_t)grid_words * (size_t)n_grids);
+    char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
+    char* go = take(sizeof(uint32_t) * (size_t)((cap + kSlice - 1) / kSlice));
+    char* gr4 = take(sizeof(uint4) * (size_t)n);
+    char* sm = take(sizeof(uint32_t) * kSmWords);
+    if (w) {
+      Workspace& x = w[v];
+      x.tkey[0] = reinterpret_cast<uint32_t*>(tk0);
+      x.tkey[1] = reinterpret_cast<uint32_t*>(tk1);
+      x.tval[0] = reinterpret_cast<uint32_t*>(tv0);
+      x.tval[1] = reinterpret_cast<uint32_t*>(tv1);
+      x.hist_tile = reinterpret_cast<uint32_t*>(lbt);
+      x.dkey[0] = reinterpret_cast<uint32_t*>(dk0);
+      x.dkey[1] = reinterpret_cast<uint32_t*>(dk1);
+      x.didx[0] = reinterpret_cast<uint32_t*>(di0);
+      x.didx[1] = reinterpret_cast<uint32_t*>(di1);
+      x.chunk_tot = reinterpret_cast<unsigned long long*>(ss);
+      x.hist_depth = reinterpret_cast<uint32_t*>(lbd);
+      x.grid = reinterpret_cast<uint32_t*>(gr);
+      x.grids = reinterpret_cast<uint32_t*>(grs);
+      x.rstage = reinterpret_cast<uint32_t*>(rs);
+      x.slice_first = reinterpret_cast<uint32_t*>(go);
+      x.grec = reinterpret_cast<uint4*>(gr4);
+      x.small = reinterpret_cast<uint32_t*>(sm);
+    }
   }
   return off;
 }
@@ -196,7 +206,7 @@ struct RadixJob {
   // Gaussian's tile rectangle to a per-CTA difference grid, summed into `grid` in phase B0
   const float* proj;
   int Tx, Ty, gwords;
-  uint32_t* grids;      // [gridDim.x][gwords]
+  uint32_t* grids;      // [CTAs of the job][gwords]
   uint32_t* grid;       // [gwords], zeroed by the host
   // depth sort only, after the last pass: the tiles-touched scan over the depth-sorted
   // Gaussians and the per-tile counts
@@ -207,6 +217,15 @@ struct RadixJob {
   uint32_t* rstage;     // staged tile ranges
   int tpasses;          // tile passes (their digit bases go to the small block)
 };
+
+// The depth-sort jobs of one launch (kernel parameter space: 8 jobs stay under 4 KB).
+constexpr int kMaxSortViews = 8;
+struct RadixBatch {
+  RadixJob job[kMaxSortViews];
+  int views;
+};
+static_assert(sizeof(RadixBatch) <= 4000, "depth-sort jobs must fit the kernel parameter space");
+static_assert(sizeof(RadixJob) % 4 == 0, "jobs are copied as 32-bit words");
 
 // Grid-wide barrier on a monotonically increasing arrival counter.  Bounded: after `limit`
 // polls, or once another CTA has reported a failure, it sets/keeps status bit 2 and returns
@@ -402,7 +421,8 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
 // memory atomics), written out for phase B0 to sum.
 template <int ITEMS>
 __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid,
-                                             uint32_t* s_tot, int64_t n, int64_t ntiles, uint32_t G) {
+                                             uint32_t* s_tot, int64_t n, int64_t ntiles, uint32_t G,
+                                             uint32_t bid) {
   constexpr int kTile = kSortThreads * ITEMS;
   const int tid = threadIdx.x;
   const float4* q0 = reinterpret_cast<const float4*>(J.proj);
@@ -410,7 +430,7 @@ __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob&
   const int gw = J.Tx + 1;
   for (int i = tid; i < J.gwords; i += kSortThreads) s_grid[i] = 0u;
   for (int i = tid; i < kDepthPasses * 256; i += kSortThreads) s_tot[i] = 0u;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+  for (int64_t tile = bid; tile < ntiles; tile += G) {
     for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
     __syncthreads();
     for (int j = tid; j < kTile; j += kSortThreads) {
@@ -444,16 +464,16 @@ __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob&
   }
   for (int i = tid; i < kDepthPasses * 256; i += kSortThreads)
     if (s_tot[i]) atomicAdd(&J.small[kSmHist + i], s_tot[i]);
-  uint32_t* mine = J.grids + (size_t)blockIdx.x * J.gwords;
+  uint32_t* mine = J.grids + (size_t)bid * J.gwords;
   for (int i = tid; i < J.gwords; i += kSortThreads) mine[i] = s_grid[i];
 }
 
 // Depth sort, phase B0 side job: grid[c] = sum over the CTAs' private grids, 16 grids per
 // work item (one atomic add per item).
-__device__ __forceinline__ void depth_grid_sum(const RadixJob& J, uint32_t G) {
+__device__ __forceinline__ void depth_grid_sum(const RadixJob& J, uint32_t G, uint32_t bid) {
   const int64_t groups = (G + 15) / 16;
   const int64_t items = (int64_t)J.gwords * groups;
-  for (int64_t it = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; it < items; it += (int64_t)G * kSortThreads) {
+  for (int64_t it = (int64_t)bid * kSortThreads + threadIdx.x; it < items; it += (int64_t)G * kSortThreads) {
     const int c = (int)(it % J.gwords);
     const uint32_t g0 = (uint32_t)(it / J.gwords) * 16u, g1 = min(G, g0 + 16u);
     uint32_t acc = 0;
@@ -614,7 +634,7 @@ constexpr int64_t kDirectChunks = 4096;
 
 template <int ITEMS>
 __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid, uint32_t* s_tot, uint32_t G,
-                           uint32_t& nbar) {
+                           uint32_t bid, uint32_t& nbar) {
   constexpr int kPer = kScanChunk / kSortThreads;  // 4 consecutive Gaussians per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = J.n_host;
@@ -624,7 +644,7 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
   const uint32_t* sidx = J.val[kDepthPasses & 1];
   unsigned long long* wsum64 = reinterpret_cast<unsigned long long*>(S.gbase);  // free in these phases
   // S1: chunk sums; tile counts on the last CTA
-  for (int64_t c = blockIdx.x; c < nchunks; c += G) {
+  for (int64_t c = bid; c < nchunks; c += G) {
     uint32_t sum = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -637,11 +657,11 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
     const unsigned long long t = block_sum(S, sum);
     if (tid == 0) J.chunk_tot[c] = t;
   }
-  if (blockIdx.x == G - 1) tile_counts_cta(S, J, s_grid, s_tot);
+  if (bid == G - 1) tile_counts_cta(S, J, s_grid, s_tot);
   if (!grid_barrier(S, J, ++nbar * G, true)) return false;
   // S2: exclusive prefixes of the chunk sums and the instance count M (CTA 0)
   if (!direct) {
-    if (blockIdx.x == 0) {
+    if (bid == 0) {
       unsigned long long carry = 0;
       for (int64_t c0 = 0; c0 < nchunks; c0 += kSortThreads) {
         const int64_t c = c0 + tid;
@@ -671,7 +691,7 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
     if (!grid_barrier(S, J, ++nbar * G, true)) return false;
   }
   // S3: every chunk's records and the first Gaussian of every radix tile of the tile sort
-  for (int64_t c = blockIdx.x; c < nchunks; c += G) {
+  for (int64_t c = bid; c < nchunks; c += G) {
     unsigned long long prefix;
     if (direct) {  // sum of the chunk sums before c (and, for the last chunk, M)
       unsigned long long part = 0;
@@ -727,8 +747,9 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
   return true;
 }
 
+// All passes of one sort, run by the G CTAs bid = 0 .. G-1 that the job owns.
 template <int ITEMS, bool kTileSort>
-__global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
+__device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, const uint32_t bid) {
   constexpr int kTile = kSortThreads * ITEMS;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
@@ -737,7 +758,6 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   const int64_t ntiles = sort_tiles<ITEMS>(M);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  const uint32_t G = gridDim.x;
   for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.peer[0][0])[i] = 0u;
   uint32_t nbar = 0;
   for (int p = 0; p < J.passes; ++p) {
@@ -749,9 +769,9 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     // ---- A: digit counts of every radix tile
     if (!kTileSort && p == 0) {
       uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
-      depth_phase0(S, J, s_grid, s_grid + J.gwords, J.n_host, ntiles, G);
+      depth_phase0(S, J, s_grid, s_grid + J.gwords, J.n_host, ntiles, G, bid);
     }
-    for (int64_t tile = blockIdx.x; tile < ntiles && (kTileSort || p > 0); tile += G) {
+    for (int64_t tile = bid; tile < ntiles && (kTileSort || p > 0); tile += G) {
       for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
       __syncthreads();
       const int64_t base = tile * kTile;
@@ -772,10 +792,10 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
       __syncthreads();
     }
     ++nbar;
-    if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && blockIdx.x == 0))) return;
+    if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && bid == 0))) return;
     // ---- B: per digit, exclusive scan over the tiles, plus the digit's global base
     if (!kTileSort) {
-      if (p == 0) depth_grid_sum(J, G);
+      if (p == 0) depth_grid_sum(J, G, bid);
       // the digit bases of this pass: exclusive scan of the digit totals of phase 0
       const uint32_t c = J.small[kSmHist + p * 256 + tid];
       uint32_t incl = c;
@@ -791,7 +811,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
       S.gbase[tid] = woff + incl - c;
       __syncthreads();
     }
-    for (uint32_t d = blockIdx.x; d < 256; d += G) {
+    for (uint32_t d = bid; d < 256; d += G) {
       uint32_t* col = J.hist + (int64_t)d * J.hist_stride;
       uint32_t carry = kTileSort ? J.small[kSmDigitBase + (J.slot0 + p) * 256 + d] : S.gbase[d];
       constexpr int kPer = 12;
@@ -832,7 +852,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
     // ---- C: rank within the tile, scatter through shared memory, digit-contiguous writes
     uint32_t* kout = J.key[(p + 1) & 1];
     uint32_t* vout = fin ? J.vals_out : J.val[(p + 1) & 1];
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += G) {
+    for (int64_t tile = bid; tile < ntiles; tile += G) {
       // this tile's global digit offsets, loaded now and used after the ranking
       const uint32_t tile_base = J.hist[(int64_t)tid * J.hist_stride + tile];
       for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
@@ -931,51 +951,89 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_radix_sort(RadixJob J) {
   if (!kTileSort) {
     if (!grid_barrier(S, J, ++nbar * G, true)) return;
     uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
-    depth_scan(S, J, s_grid, s_grid + J.gwords, G, nbar);
+    depth_scan(S, J, s_grid, s_grid + J.gwords, G, bid, nbar);
   }
 }
 
-// Copies the staged tile ranges to the caller once every pass has finished cleanly.
-__global__ void k_publish_ranges(const uint32_t* __restrict__ rstage, int64_t T, uint32_t* __restrict__ ranges,
-                                 const int64_t* count) {
-  if (count[1] != 0) return;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * T; i += stride) ranges[i] = rstage[i];
+// The tile sort of one view: every CTA of the grid works on the job.
+__global__ void __launch_bounds__(kSortThreads, 4) k_tile_sort(RadixJob J) {
+  radix_body<kTileItems, true>(J, gridDim.x, blockIdx.x);
 }
 
-// Resident CTAs per SM of a radix kernel for a given dynamic shared-memory size (cached).
-template <int ITEMS, bool kTileSort>
+// The depth sorts of up to kMaxSortViews views in one launch: CTAs [v G, (v + 1) G) sort view
+// v, with their own barrier counter and workspace, so the views' latency-bound phases overlap.
+// A CTA reads its view's job from parameter space once, into shared memory.
+__global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort(const __grid_constant__ RadixBatch B) {
+  __shared__ RadixJob s_job;
+  const uint32_t G = gridDim.x / (uint32_t)B.views;
+  const uint32_t view = blockIdx.x / G;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&B.job[view]);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(&s_job);
+  for (int i = threadIdx.x; i < (int)(sizeof(RadixJob) / 4); i += kSortThreads) dst[i] = src[i];
+  __syncthreads();
+  radix_body<kDepthItems, false>(s_job, G, blockIdx.x - view * G);
+}
+
+// Per view of a batch: the buffers zeroed before the sorts (the status words, the small
+// block, the difference grid, the caller's ranges) and the staged ranges published after.
+struct ViewBuffers {
+  uint32_t* zero[kMaxSortViews][4];
+  int64_t zero_words[kMaxSortViews][4];
+  const uint32_t* rstage[kMaxSortViews];
+  uint32_t* ranges[kMaxSortViews];
+  const int64_t* count[kMaxSortViews];
+  int64_t words2T[kMaxSortViews];  // 2 x tiles of the view
+  int views;
+};
+
+// blockIdx.y = view * 4 + buffer
+__global__ void k_sort_init(const __grid_constant__ ViewBuffers B) {
+  const int v = blockIdx.y >> 2, b = blockIdx.y & 3;
+  uint32_t* p = B.zero[v][b];
+  const int64_t words = B.zero_words[v][b];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0u;
+}
+
+// Copies every view's staged tile ranges to the caller once all its passes finished cleanly
+// (blockIdx.y = view).
+__global__ void k_publish_ranges(const __grid_constant__ ViewBuffers B) {
+  const int v = blockIdx.y;
+  if (B.count[v][1] != 0) return;
+  const uint32_t* src = B.rstage[v];
+  uint32_t* dst = B.ranges[v];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < B.words2T[v]; i += stride) dst[i] = src[i];
+}
+
+// Resident CTAs per SM of a sort kernel for a given dynamic shared-memory size (cached).
+template <bool kTileSort>
 int radix_blocks_per_sm(size_t smem) {
   static std::mutex mu;
   static size_t cached_smem = 0;
   static int cached = -1;
   std::lock_guard<std::mutex> lock(mu);
   if (cached < 0 || cached_smem != smem) {
+    const void* fn = kTileSort ? (const void*)k_tile_sort : (const void*)k_depth_sort;
     int b = 0;
-    cudaFuncSetAttribute(k_radix_sort<ITEMS, kTileSort>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_radix_sort<ITEMS, kTileSort>, kSortThreads, smem) !=
-            cudaSuccess ||
-        b < 1)
-      b = 1;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kSortThreads, smem) != cudaSuccess || b < 1) b = 1;
     cached = b;
     cached_smem = smem;
   }
   return cached;
 }
 
-template <int ITEMS, bool kTileSort>
-int radix_grid(size_t smem, int64_t max_tiles) {
-  const int64_t cap_ctas = (int64_t)gs::num_sms() * radix_blocks_per_sm<ITEMS, kTileSort>(smem);
-  return (int)std::max<int64_t>(1, std::min(cap_ctas, max_tiles));
-}
-
-// Cooperative launch: every CTA of the grid is resident at once, which the grid barriers need.
-template <int ITEMS, bool kTileSort>
-cudaError_t launch_radix(const RadixJob& job, int grid, size_t smem, cudaStream_t st) {
+// Cooperative launches: every CTA of the grid is resident at once, which the grid barriers need.
+cudaError_t launch_tile_sort(const RadixJob& job, int grid, size_t smem, cudaStream_t st) {
   RadixJob j = job;
   void* args[] = {&j};
-  return cudaLaunchCooperativeKernel((const void*)k_radix_sort<ITEMS, kTileSort>, dim3(grid), dim3(kSortThreads), args,
-                                     smem, st);
+  return cudaLaunchCooperativeKernel((const void*)k_tile_sort, dim3(grid), dim3(kSortThreads), args, smem, st);
+}
+cudaError_t launch_depth_sort(const RadixBatch& batch, int grid, size_t smem, cudaStream_t st) {
+  RadixBatch b = batch;
+  void* args[] = {&b};
+  return cudaLaunchCooperativeKernel((const void*)k_depth_sort, dim3(grid), dim3(kSortThreads), args, smem, st);
 }
 
 int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); }
@@ -983,106 +1041,226 @@ int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); 
 size_t depth_sort_smem(const gs::Cam& k) {
   return sizeof(SortSmem<kDepthItems>) + sizeof(uint32_t) * ((size_t)grid_words(k) + kDepthPasses * 256);
 }
-int depth_sort_grid(const gs::Cam& k, int64_t n) {  // one CTA more than radix tiles if it fits
-  return radix_grid<kDepthItems, false>(depth_sort_smem(k), sort_tiles<kDepthItems>(n) + 1);
-}
-// private difference grids the workspace holds: at most one per resident CTA (2048 threads
-// per SM), at most one per radix tile of the depth sort
+// private difference grids a view's workspace holds: at most one per resident CTA (2048
+// threads per SM), at most one per radix tile of the depth sort plus one
 int64_t depth_grids_bound(int64_t n) {
   return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n) + 1, (int64_t)gs::num_sms() * 8));
 }
 constexpr size_t kMaxSortSmem = 227 * 1024;  // shared memory a CTA may have
 
+// Largest grid words and tiles over a batch of cameras.
+void batch_dims(const gs::Cam* k, int views, int64_t* gw, int64_t* T) {
+  *gw = 1;
+  *T = 1;
+  for (int v = 0; v < views; ++v) {
+    *gw = std::max(*gw, grid_words(k[v]));
+    *T = std::max(*T, (int64_t)k[v].Tx * k[v].Ty);
+  }
+}
+
+struct SortView {
+  const float* proj;
+  gs::Cam k;
+  uint64_t* keys;
+  uint32_t* vals;
+  uint32_t* ranges;
+  int64_t* count;
+};
+
+// Enqueues the sorts of `views` views that share n and capacity.  Views go in groups of up
+// to kMaxSortViews: one zeroing launch, one depth-sort launch, one tile sort per view, one
+// publishing launch.  A group's depth buffers are w[0 .. group size), reused by the next group
+// once the tile sorts before it (which read them) are enqueued.
+gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, const Workspace* w,
+                    cudaStream_t st) {
+  const int64_t limit = gs::wait_limit();
+  const int drop = gs::take_drop_publish();
+  const int sms = gs::num_sms();
+  for (int g0 = 0; g0 < views; g0 += kMaxSortViews) {
+    const int gv = std::min(kMaxSortViews, views - g0);
+    ViewBuffers vb{};
+    vb.views = gv;
+    int64_t max_words = 0;
+    for (int v = 0; v < gv; ++v) {
+      const gs::Cam& k = V[g0 + v].k;
+      const int64_t T = (int64_t)k.Tx * k.Ty;
+      uint32_t* z[4] = {reinterpret_cast<uint32_t*>(V[g0 + v].count), w[v].small, w[v].grid, V[g0 + v].ranges};
+      const int64_t zw[4] = {4, kSmWords, grid_words(k), 2 * T};
+      for (int b = 0; b < 4; ++b) {
+        vb.zero[v][b] = z[b];
+        vb.zero_words[v][b] = zw[b];
+        max_words = std::max(max_words, zw[b]);
+      }
+      vb.rstage[v] = w[v].rstage;
+      vb.ranges[v] = V[g0 + v].ranges;
+      vb.count[v] = V[g0 + v].count;
+      vb.words2T[v] = 2 * T;
+    }
+    const int zx = (int)std::min<int64_t>(std::max<int64_t>(1, (max_words + 1023) / 1024), 64);
+    k_sort_init<<<dim3(zx, 4 * gv), 256, 0, st>>>(vb);
+    if (gs_status s = gs::check_launch("gs_bin_sort init")) return s;
+    if (n == 0) continue;
+    // 1. per view, Gaussians by (depth, index): 4 stable passes over 32-bit depth keys; phase
+    //    0 also builds the difference grid of per-tile instance counts, and after the passes
+    //    the tiles-touched scan gives every sorted Gaussian's first slot (and M), the tile
+    //    counts the staged ranges and the digit bases of the tile passes
+    RadixBatch db{};
+    db.views = gv;
+    size_t dsmem = 0;
+    for (int v = 0; v < gv; ++v) {
+      const SortView& sv = V[g0 + v];
+      dsmem = std::max(dsmem, depth_sort_smem(sv.k));
+      RadixJob& dj = db.job[v];
+      dj.key[0] = w[v].dkey[0]; dj.key[1] = w[v].dkey[1];
+      dj.val[0] = w[v].didx[0]; dj.val[1] = w[v].didx[1];
+      dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
+      dj.hist = w[v].hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
+      dj.small = w[v].small; dj.count = sv.count; dj.limit = limit; dj.drop_arrival = drop == 2 && g0 + v == 0;
+      dj.proj = sv.proj; dj.Tx = sv.k.Tx; dj.Ty = sv.k.Ty; dj.gwords = (int)grid_words(sv.k);
+      dj.grids = w[v].grids; dj.grid = w[v].grid;
+      dj.chunk_tot = w[v].chunk_tot; dj.grec = w[v].grec; dj.slice_first = w[v].slice_first; dj.tcap = capacity;
+      dj.rstage = w[v].rstage; dj.tpasses = tile_passes(sv.k);
+    }
+    // CTAs per view: one more than the radix tiles if the group fits, else an equal share of
+    // the resident CTAs
+    const int64_t resident = (int64_t)sms * radix_blocks_per_sm<false>(dsmem);
+    const int64_t G = std::max<int64_t>(
+        1, std::min({sort_tiles<kDepthItems>(n) + 1, resident / gv, depth_grids_bound(n)}));
+    if (cudaError_t e = launch_depth_sort(db, (int)(G * gv), dsmem, st))
+      return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
+    if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
+    // 2. per view, the stable sort of the instances by tile id: the first pass generates the
+    //    (tile, index) pairs in depth order from the scan's records, the last writes the
+    //    caller's arrays
+    const size_t tsmem = sizeof(SortSmem<kTileItems>);
+    const int tgrid = (int)std::max<int64_t>(
+        1, std::min<int64_t>((int64_t)sms * radix_blocks_per_sm<true>(tsmem), sort_tiles<kTileItems>(capacity)));
+    for (int v = 0; v < gv; ++v) {
+      const SortView& sv = V[g0 + v];
+      RadixJob tj{};
+      tj.key[0] = w[v].tkey[0]; tj.key[1] = w[v].tkey[1];
+      tj.val[0] = w[v].tval[0]; tj.val[1] = w[v].tval[1];
+      tj.n_host = -1; tj.cap = capacity; tj.passes = tile_passes(sv.k);
+      tj.slot0 = kDepthPasses; tj.sort_id = 1;
+      tj.hist = w[v].hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
+      tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
+      tj.gen = GenSource{w[v].slice_first, w[v].grec, n, sv.k.Tx};
+      tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
+      if (cudaError_t e = launch_tile_sort(tj, tgrid, tsmem, st))
+        return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
+      if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
+    }
+    k_publish_ranges<<<dim3(sms, gv), 256, 0, st>>>(vb);
+    if (gs_status s = gs::check_launch("gs_bin_sort ranges")) return s;
+  }
+  return GS_OK;
+}
+
+// Reads back the status words of `views` views (count[2v], count[2v + 1]) after a sort.
+gs_status read_counts(const int64_t* const* count, int views, int64_t* count_host, cudaStream_t st) {
+  std::vector<int64_t> hc(2 * (size_t)views, 0);
+  for (int v = 0; v < views; ++v)
+    if (cudaMemcpyAsync(&hc[2 * v], count[v], 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return gs::check_launch("gs_bin_sort count readback");
+  if (cudaStreamSynchronize(st) != cudaSuccess) return gs::check_launch("gs_bin_sort count readback");
+  int64_t bits = 0;
+  for (int v = 0; v < views; ++v) {
+    count_host[v] = hc[2 * v];
+    bits |= hc[2 * v + 1];
+  }
+  if (bits & gs::kStatusTimeout) return gs::set_error(GS_ERR_TIMEOUT, "gs_bin_sort: a bounded device-side wait gave up");
+  if (bits & gs::kStatusCapacity) {
+    int64_t worst = 0;
+    for (int v = 0; v < views; ++v) worst = std::max(worst, count_host[v]);
+    return gs::set_error(GS_ERR_CAPACITY, "gs_bin_sort: %lld instances exceed the capacity", (long long)worst);
+  }
+  return GS_OK;
+}
+
+gs_status check_sort_args(int64_t n, int64_t capacity, const gs::Cam& k, const char* fn) {
+  if (n < 0 || n >= (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "%s: bad n", fn);
+  if (capacity < 0 || capacity >= (int64_t(1) << 30))
+    return gs::set_error(GS_ERR_INVALID, "%s: capacity must be in [0, 2^30)", fn);
+  if (tile_passes(k) > 2 || depth_sort_smem(k) > kMaxSortSmem)  // the tile counts handle two passes
+    return gs::set_error(GS_ERR_INVALID, "%s: %d x %d tiles exceed the supported grid", fn, k.Tx, k.Ty);
+  return GS_OK;
+}
+
 }  // namespace
 
 extern "C" size_t gs_bin_sort_workspace_size(int64_t n, int64_t capacity, const gs_camera* cam) {
-  if (!cam || n < 0 || capacity < 0) return 0;
-  const gs::Cam k = gs::make_cam(*cam);
-  return carve(nullptr, nullptr, n, capacity, tile_passes(k), grid_words(k), (int64_t)k.Tx * k.Ty,
-               depth_grids_bound(n));
+  return gs_bin_sort_batch_workspace_size(1, n, capacity, cam);
+}
+
+extern "C" size_t gs_bin_sort_batch_workspace_size(int batch, int64_t n, int64_t capacity, const gs_camera* cams) {
+  if (!cams || batch < 1 || n < 0 || capacity < 0) return 0;
+  std::vector<gs::Cam> k((size_t)batch);
+  for (int v = 0; v < batch; ++v) k[v] = gs::make_cam(cams[v]);
+  int64_t gw, T;
+  batch_dims(k.data(), batch, &gw, &T);
+  return carve(nullptr, nullptr, std::min(batch, kMaxSortViews), n, capacity, gw, T, depth_grids_bound(n));
 }
 
 extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
                                  size_t workspace_bytes, uint64_t* keys, uint32_t* vals, int64_t capacity,
                                  uint32_t* ranges, int64_t* count, int64_t* count_host, void* stream) {
   if (gs_status s = gs::check_camera(cam)) return s;
-  if (n < 0 || n >= (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: bad n");
-  if (capacity < 0 || capacity >= (int64_t(1) << 30))
-    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: capacity must be in [0, 2^30)");
+  const gs::Cam k = gs::make_cam(*cam);
+  if (gs_status s = check_sort_args(n, capacity, k, "gs_bin_sort")) return s;
   if (!count || !ranges || (n > 0 && !proj) || (capacity > 0 && !vals) || !workspace)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: NULL pointer");
   if ((proj && !gs::aligned16(proj)) || !gs::aligned8(count) || (keys && !gs::aligned8(keys)) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: misaligned pointer");
-  const gs::Cam k = gs::make_cam(*cam);
-  const int tpasses = tile_passes(k);
-  const int64_t T = (int64_t)k.Tx * k.Ty;
-  if (tpasses > 2 || depth_sort_smem(k) > kMaxSortSmem)  // the tile counts handle two passes
-    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: %d x %d tiles exceed the supported grid", k.Tx, k.Ty);
-  const size_t need = carve(nullptr, nullptr, n, capacity, tpasses, grid_words(k), T, depth_grids_bound(n));
+  const size_t need = gs_bin_sort_workspace_size(n, capacity, cam);
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: workspace %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w;
-  carve(&w, reinterpret_cast<char*>(workspace), n, capacity, tpasses, grid_words(k), T, depth_grids_bound(n));
+  carve(&w, reinterpret_cast<char*>(workspace), 1, n, capacity, grid_words(k), (int64_t)k.Tx * k.Ty,
+        depth_grids_bound(n));
   cudaStream_t st = gs::as_stream(stream);
-  const int64_t limit = gs::wait_limit();
-  const int drop = gs::take_drop_publish();
+  const SortView view{proj, k, keys, vals, ranges, count};
+  if (gs_status s = run_sorts(&view, 1, n, capacity, &w, st)) return s;
+  if (!count_host) return GS_OK;
+  const int64_t* c = count;
+  return read_counts(&c, 1, count_host, st);
+}
 
-  if (cudaMemsetAsync(count, 0, 2 * sizeof(int64_t), st) != cudaSuccess ||
-      cudaMemsetAsync(w.small, 0, sizeof(uint32_t) * kSmWords, st) != cudaSuccess ||
-      cudaMemsetAsync(ranges, 0, sizeof(uint32_t) * 2 * T, st) != cudaSuccess)
-    return gs::check_launch("gs_bin_sort memset");
-  if (n > 0) {
-    const int sms = gs::num_sms();
-    // 1. Gaussians by (depth, index): 4 stable passes over 32-bit depth keys; phase 0 also
-    //    builds the difference grid of per-tile instance counts, and after the passes the
-    //    tiles-touched scan gives every sorted Gaussian's first slot (and M), the tile counts
-    //    the staged ranges and the digit bases of the tile passes
-    if (cudaMemsetAsync(w.grid, 0, sizeof(uint32_t) * (size_t)grid_words(k), st) != cudaSuccess)
-      return gs::check_launch("gs_bin_sort memset");
-    const size_t dsmem = depth_sort_smem(k);
-    const int dgrid = (int)std::min<int64_t>(depth_sort_grid(k, n), depth_grids_bound(n));
-    RadixJob dj{};
-    dj.key[0] = w.dkey[0]; dj.key[1] = w.dkey[1];
-    dj.val[0] = w.didx[0]; dj.val[1] = w.didx[1];
-    dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
-    dj.hist = w.hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
-    dj.small = w.small; dj.count = count; dj.limit = limit; dj.drop_arrival = drop == 2;
-    dj.proj = proj; dj.Tx = k.Tx; dj.Ty = k.Ty; dj.gwords = (int)grid_words(k); dj.grids = w.grids; dj.grid = w.grid;
-    dj.chunk_tot = w.chunk_tot; dj.grec = w.grec; dj.slice_first = w.slice_first; dj.tcap = capacity;
-    dj.rstage = w.rstage; dj.tpasses = tpasses;
-    if (cudaError_t e = launch_radix<kDepthItems, false>(dj, dgrid, dsmem, st))
-      return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
-    if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
-    // 2. stable sort of the instances by tile id: the first pass generates the (tile, index)
-    //    pairs in depth order from the scan's records, the last writes the caller's arrays
-    RadixJob tj{};
-    tj.key[0] = w.tkey[0]; tj.key[1] = w.tkey[1];
-    tj.val[0] = w.tval[0]; tj.val[1] = w.tval[1];
-    tj.n_host = -1; tj.cap = capacity; tj.passes = tpasses;
-    tj.slot0 = kDepthPasses; tj.sort_id = 1;
-    tj.hist = w.hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
-    tj.small = w.small; tj.count = count; tj.limit = limit; tj.drop_arrival = drop == 1;
-    tj.gen = GenSource{w.slice_first, w.grec, n, k.Tx};
-    tj.q0 = reinterpret_cast<const float4*>(proj); tj.keys64 = keys; tj.vals_out = vals;
-    if (cudaError_t e = launch_radix<kTileItems, true>(
-            tj, radix_grid<kTileItems, true>(sizeof(SortSmem<kTileItems>), sort_tiles<kTileItems>(capacity)),
-            sizeof(SortSmem<kTileItems>), st))
-      return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
-    if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
-    k_publish_ranges<<<sms, 256, 0, st>>>(w.rstage, T, ranges, count);
-    if (gs_status s = gs::check_launch("gs_bin_sort ranges")) return s;
+extern "C" gs_status gs_bin_sort_batch(const float* const* projs, int batch, int64_t n, const gs_camera* cams,
+                                       void* workspace, size_t workspace_bytes, uint64_t* const* keys,
+                                       uint32_t* const* vals, int64_t capacity, uint32_t* const* ranges,
+                                       int64_t* counts, int64_t* counts_host, void* stream) {
+  if (batch < 1) return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: batch must be >= 1");
+  if (!projs || !cams || !vals || !ranges || !counts || !workspace)
+    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: NULL pointer");
+  std::vector<SortView> V((size_t)batch);
+  for (int v = 0; v < batch; ++v) {
+    if (gs_status s = gs::check_camera(&cams[v])) return s;
+    SortView& sv = V[v];
+    sv = SortView{projs[v], gs::make_cam(cams[v]), keys ? keys[v] : nullptr, vals[v], ranges[v], counts + 2 * v};
+    if (gs_status s = check_sort_args(n, capacity, sv.k, "gs_bin_sort_batch")) return s;
+    if (!sv.ranges || (n > 0 && !sv.proj) || (capacity > 0 && !sv.vals))
+      return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: NULL pointer (view %d)", v);
+    if ((sv.proj && !gs::aligned16(sv.proj)) || (sv.keys && !gs::aligned8(sv.keys)))
+      return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: misaligned pointer (view %d)", v);
   }
-  if (count_host) {
-    int64_t hc[2] = {0, 0};
-    if (cudaMemcpyAsync(hc, count, sizeof(hc), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-      return gs::check_launch("gs_bin_sort count readback");
-    *count_host = hc[0];
-    if (hc[1] & gs::kStatusTimeout) return gs::set_error(GS_ERR_TIMEOUT, "gs_bin_sort: a bounded device-side wait gave up");
-    if (hc[1] & gs::kStatusCapacity)
-      return gs::set_error(GS_ERR_CAPACITY, "gs_bin_sort: %lld instances exceed capacity %lld", (long long)hc[0],
-                           (long long)capacity);
-  }
-  return GS_OK;
+  if (!gs::aligned8(counts) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: misaligned pointer");
+  const size_t need = gs_bin_sort_batch_workspace_size(batch, n, capacity, cams);
+  if (workspace_bytes < need)
+    return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: workspace %zu bytes < %zu needed", workspace_bytes,
+                         need);
+  int64_t gw, T;
+  std::vector<gs::Cam> k((size_t)batch);
+  for (int v = 0; v < batch; ++v) k[v] = V[v].k;
+  batch_dims(k.data(), batch, &gw, &T);
+  Workspace w[kMaxSortViews];
+  carve(w, reinterpret_cast<char*>(workspace), std::min(batch, kMaxSortViews), n, capacity, gw, T,
+        depth_grids_bound(n));
+  cudaStream_t st = gs::as_stream(stream);
+  if (gs_status s = run_sorts(V.data(), batch, n, capacity, w, st)) return s;
+  if (!counts_host) return GS_OK;
+  std::vector<const int64_t*> c((size_t)batch);
+  for (int v = 0; v < batch; ++v) c[v] = counts + 2 * v;
+  return read_counts(c.data(), batch, counts_host, st);
 }

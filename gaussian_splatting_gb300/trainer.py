@@ -3,8 +3,9 @@
 ``Trainer`` owns the device state (parameters, gradients, Adam moments, per-view scratch)
 as torch tensors -- torch supplies memory and the stream, every computation is a libgs.so
 kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
-training flow (训练流程): for each view project -> bin/sort -> composite -> loss ->
-composite backward; then the visible sets, and the projection backward of every view
+training flow (训练流程): project every view, bin/sort them all (gs_bin_sort_batch: the
+views' depth sorts share one launch), then for each view composite -> loss -> composite
+backward; then the visible sets, and the projection backward of every view
 with the visible-only Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch
 scaling) in one fused pass (gs_project_bwd_adam) whose gradients never leave the chip.
 ``step_async(..., adam=False)`` runs the per-view gs_project_bwd instead and leaves the
@@ -33,10 +34,12 @@ LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_
 MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
 
-def bin_sort_launches(cam) -> int:
-    # depth sort (keys, tile-count grid, the four passes, the tiles-touched scan and the tile
-    # counts in one cooperative launch), tile sort (both passes, likewise), ranges
-    return 3
+def bin_sort_launches(views: int) -> int:
+    # per group of up to 8 views: zeroing, the depth sorts (keys, tile-count grids, the four
+    # passes, the tiles-touched scans and the tile counts in one cooperative launch), ranges;
+    # per view: the tile sort (both passes in one cooperative launch)
+    groups = (views + 7) // 8
+    return 3 * groups + views
 
 
 @dataclasses.dataclass
@@ -72,7 +75,7 @@ class Trainer:
         self.T_final = torch.zeros((height, width), dtype=f32, device=dev)
         self.n_contrib = torch.zeros((height, width), dtype=i32, device=dev)
         self.dimg = torch.zeros((3, height, width), dtype=f32, device=dev)
-        self.ranges = torch.zeros((tiles, 2), dtype=i32, device=dev)
+        self.ranges = torch.zeros((batch, tiles, 2), dtype=i32, device=dev)  # per view
         self.counts = torch.zeros((batch, 2), dtype=i64, device=dev)
         self.loss = torch.zeros(1, dtype=f32, device=dev)
         self.loss_ws = torch.empty(max(N.gs_loss_workspace_size(width, height), 256), dtype=torch.uint8, device=dev)
@@ -100,7 +103,8 @@ class Trainer:
         capacity = int(min(capacity, (1 << 30) - 1))
         dev = self.params.device
         # the sorted keys are not requested: rendering reads the values and the tile ranges
-        self.vals = torch.empty(capacity, dtype=torch.int32, device=dev)
+        # (one set per view: the views are sorted together before any is composited)
+        self.vals = torch.empty((self.batch, capacity), dtype=torch.int32, device=dev)
         self._ws_cam = None
         self.capacity = capacity
         self.sort_ws = None
@@ -120,8 +124,9 @@ class Trainer:
 
     def _sort_ws(self, cam):
         # every view of a trainer has the same image size: the size depends on the capacity only
+        # (sized for a full batch, which also covers a single view)
         if self._ws_cam != self.capacity:
-            self._ws_need = N.gs_bin_sort_workspace_size(self.n, self.capacity, cam)
+            self._ws_need = N.gs_bin_sort_batch_workspace_size(self.batch, self.n, self.capacity, [cam] * self.batch)
             self._ws_cam = self.capacity
         need = self._ws_need
         if self.sort_ws is None or self.sort_ws.numel() < need:
@@ -137,8 +142,8 @@ class Trainer:
                 self._alloc_sort(1024)
             ws = self._sort_ws(cam)
             try:
-                m = N.gs_bin_sort(self.proj[0], self.n, cam, ws, ws.numel(), None, self.vals, self.capacity,
-                                  self.ranges, self.counts[0], sync=True)
+                m = N.gs_bin_sort(self.proj[0], self.n, cam, ws, ws.numel(), None, self.vals[0], self.capacity,
+                                  self.ranges[0], self.counts[0], sync=True)
             except N.GSError as e:
                 if e.status != N.GS_ERR_CAPACITY:
                     raise
@@ -159,9 +164,9 @@ class Trainer:
         proj = self.proj[0]
         N.gs_project(params, self.n, cam, proj)
         ws = self._sort_ws(cam)
-        N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), None, self.vals, self.capacity, self.ranges,
+        N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), None, self.vals[0], self.capacity, self.ranges[0],
                       self.counts[0])
-        N.gs_render_fwd(proj, self.n, self.vals, self.ranges, cam, self.bg, out, self.T_final, self.n_contrib)
+        N.gs_render_fwd(proj, self.n, self.vals[0], self.ranges[0], cam, self.bg, out, self.T_final, self.n_contrib)
         return out
 
     # ------------------------------------------------------------------ the step
@@ -190,15 +195,18 @@ class Trainer:
             step_start = torch.cuda.Event()
             step_start.record()
         for b, cam in enumerate(ccams):
-            proj = self.proj[b]
-            T("project", N.gs_project, self.params, n, cam, proj, stream=st)
-            ws = self._sort_ws(cam)
-            T("bin_sort", N.gs_bin_sort, proj, n, cam, ws, ws.numel(), None, self.vals, self.capacity,
-              self.ranges, self.counts[b], stream=st)
+            T("project", N.gs_project, self.params, n, cam, self.proj[b], stream=st)
+        ws = self._sort_ws(ccams[0])
+        T("bin_sort", N.gs_bin_sort_batch, [self.proj[b] for b in range(B)], n, ccams, ws, ws.numel(), None,
+          [self.vals[b] for b in range(B)], self.capacity, [self.ranges[b] for b in range(B)], self.counts,
+          stream=st)
+        launches += B * LAUNCHES["project"] + bin_sort_launches(B)
+        for b, cam in enumerate(ccams):
+            proj, vals, ranges = self.proj[b], self.vals[b], self.ranges[b]
             work_buf = None
             if self.work is not None:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
-            T("render_fwd", N.gs_render_fwd, proj, n, self.vals, self.ranges, cam, self.bg, self.image, self.T_final,
+            T("render_fwd", N.gs_render_fwd, proj, n, vals, ranges, cam, self.bg, self.image, self.T_final,
               self.n_contrib, work_buf, stream=st)
             if host_targets is not None and ready is None:  # after the first view's compositing
                 ready = self._upload(host_targets, B, step_start)
@@ -206,7 +214,7 @@ class Trainer:
                 torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               self.dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
-            T("render_bwd", N.gs_render_bwd, proj, n, self.vals, self.ranges, cam, self.bg, self.T_final,
+            T("render_bwd", N.gs_render_bwd, proj, n, vals, ranges, cam, self.bg, self.T_final,
               self.n_contrib, self.dimg, self.grad2d[b], stream=st)
             if not fused:
                 T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads, stream=st)
@@ -216,7 +224,7 @@ class Trainer:
                 #  pairs the forward's warps evaluated)
                 self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum()),
                                   int(work_buf[2].sum())))
-            launches += bin_sort_launches(cam) + sum(LAUNCHES[k] for k in ("project", "render_fwd", "loss", "render_bwd"))
+            launches += sum(LAUNCHES[k] for k in ("render_fwd", "loss", "render_bwd"))
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
           self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard, stream=st)
         launches += LAUNCHES["visible_sets"]

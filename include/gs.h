@@ -109,6 +109,30 @@ gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* 
                       uint32_t* ranges, int64_t* count, int64_t* count_host, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_bin_sort_batch -- gs_bin_sort for the `batch` views of one training step (the
+ * Grendel-GS notes' batch of images, §4.2), with results identical to `batch` separate
+ * gs_bin_sort calls.  The depth sorts of up to 8 views run in one launch, so their short,
+ * barrier-bound phases overlap; the tile sorts follow view by view.
+ *   projs      host array of `batch` device pointers, [3][n][4] each (one n for all views).
+ *   cams       host array of `batch` cameras (image sizes may differ).
+ *   workspace  gs_bin_sort_batch_workspace_size(batch, n, capacity, cams) bytes, 256-byte
+ *              aligned: one set of capacity-sized tile-sort buffers plus depth-sort buffers
+ *              for min(batch, 8) views.
+ *   keys       host array of `batch` device pointers (entries may be NULL), or NULL.
+ *   vals, ranges  host arrays of `batch` device pointers: view v's outputs, as gs_bin_sort's.
+ *   counts     device int64 [batch][2]: view v's count[0], count[1] as gs_bin_sort's.
+ *   counts_host optional host int64 [batch]: if non-NULL the call synchronises the stream,
+ *              stores every M there and returns GS_ERR_CAPACITY / GS_ERR_TIMEOUT if any view
+ *              reported it.
+ * Argument checks are gs_bin_sort's, per view; batch must be >= 1.
+ */
+size_t gs_bin_sort_batch_workspace_size(int batch, int64_t n, int64_t capacity, const gs_camera* cams);
+gs_status gs_bin_sort_batch(const float* const* projs, int batch, int64_t n, const gs_camera* cams,
+                            void* workspace, size_t workspace_bytes, uint64_t* const* keys,
+                            uint32_t* const* vals, int64_t capacity, uint32_t* const* ranges,
+                            int64_t* counts, int64_t* counts_host, void* stream);
+
+/* ---------------------------------------------------------------------------
  * gs_render_fwd -- per-pixel front-to-back alpha compositing of the tile's sorted list
  * (Grendel-GS notes, 训练流程 "图像渲染").  For pixel p and list entries j in order:
  *   d = p + 0.5 - (u, v); power = -(A dx^2 + C dy^2)/2 - B dx dy; skip if power > 0;

@@ -57,6 +57,11 @@ def test_host_side_argument_errors(lib):
     assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None) == N.GS_ERR_INVALID
     # misaligned workspace / capacity bounds for the sort
     assert lib.gs_bin_sort(None, 0, C.byref(cam), 8, 10, None, None, 1 << 30, 64, 64, None, None) == N.GS_ERR_INVALID
+    # the batched sort: batch < 1, NULL pointer arrays
+    assert lib.gs_bin_sort_batch(None, 0, 0, C.byref(cam), 256, 10, None, None, 0, None, 64, None, None) \
+        == N.GS_ERR_INVALID
+    assert lib.gs_bin_sort_batch(None, 1, 0, C.byref(cam), 256, 10, None, None, 0, None, 64, None, None) \
+        == N.GS_ERR_INVALID
 
 
 def test_workspace_sizes_are_pure_host_functions(lib):
@@ -66,6 +71,13 @@ def test_workspace_sizes_are_pure_host_functions(lib):
     a = N.gs_bin_sort_workspace_size(300_000, 10_000_000, cam)
     b = N.gs_bin_sort_workspace_size(300_000, 20_000_000, cam)
     assert 0 < a < b
+    # a batch shares the capacity-sized tile-sort buffers and holds depth buffers for up to 8 views
+    b1 = N.gs_bin_sort_batch_workspace_size(1, 300_000, 10_000_000, [cam])
+    b4 = N.gs_bin_sort_batch_workspace_size(4, 300_000, 10_000_000, [cam] * 4)
+    b8 = N.gs_bin_sort_batch_workspace_size(8, 300_000, 10_000_000, [cam] * 8)
+    b16 = N.gs_bin_sort_batch_workspace_size(16, 300_000, 10_000_000, [cam] * 16)
+    assert b1 == a and a < b4 < 4 * a and b8 == b16
+    assert (b4 - a) * 7 == (b8 - a) * 3  # equal per-view depth parts
     assert N.gs_loss_workspace_size(1236, 820) > 0
     assert N.gs_visible_sets_workspace_size(4, 300_000) > 0
     assert N.gs_visible_sets_workspace_size(65, 10) == 0
@@ -74,6 +86,8 @@ def test_workspace_sizes_are_pure_host_functions(lib):
 def test_launch_count_bookkeeping():
     import scenes
     from gaussian_splatting_gb300.trainer import bin_sort_launches
-    # every radix pass of a sort runs inside one cooperative launch
-    assert bin_sort_launches(scenes.make_cameras(1)[0]) == 3
-    assert bin_sort_launches(scenes.make_cameras(0)[0]) == 3
+    # every radix pass of a sort runs inside one cooperative launch; per group of up to 8 views
+    # one zeroing, one depth-sort and one publishing launch, per view one tile sort
+    assert bin_sort_launches(1) == 4
+    assert bin_sort_launches(4) == 7
+    assert bin_sort_launches(16) == 22

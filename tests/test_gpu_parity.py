@@ -184,6 +184,71 @@ def test_bin_sort_bounded_wait_reports_timeout(mode):
     assert count[1] == 0 and M > 0
 
 
+def gpu_bin_sort_batch(planes_list, cams, capacity=None, with_keys=True):
+    n = planes_list[0].shape[1]
+    B = len(cams)
+    if capacity is None:
+        capacity = max(int(p[2, :, 3].view(np.int32).astype(np.int64).sum()) for p in planes_list) + 1
+    ws_bytes = N.gs_bin_sort_batch_workspace_size(B, n, capacity, cams)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    projs = [dev(p) for p in planes_list]
+    keys = [torch.zeros(max(capacity, 1), dtype=torch.int64, device="cuda") for _ in range(B)]
+    vals = [torch.zeros(max(capacity, 1), dtype=torch.int32, device="cuda") for _ in range(B)]
+    ranges = [torch.full((c.tiles_x * c.tiles_y, 2), 7, dtype=torch.int32, device="cuda") for c in cams]
+    counts = torch.zeros((B, 2), dtype=torch.int64, device="cuda")
+    Ms = N.gs_bin_sort_batch(projs, n, cams, ws, ws_bytes, keys if with_keys else None, vals, capacity, ranges,
+                             counts, sync=True)
+    return [(host(keys[b])[:Ms[b]].view(np.uint64), host(vals[b])[:Ms[b]].view(np.uint32),
+             host(ranges[b]).view(np.uint32), Ms[b]) for b in range(B)], host(counts)
+
+
+def _batch_case(case):
+    if case == "small-10-views":  # two launch groups: the second reuses the first's depth buffers
+        P = scenes.make_params(1, n=2048)
+        return P, scenes.make_cameras(1)[:10]
+    if case == "300k-4-views":  # fewer CTAs per view than radix tiles of the depth sort
+        P = scenes.make_params(1, n=300_000)
+        return P, [scenes.make_cameras(1)[v] for v in (0, 5, 11, 23)]
+    # image sizes differ inside the batch (1236x820 and 1920x1080 cameras on one scene)
+    P = scenes.make_params(1, n=50_000)
+    return P, [scenes.make_cameras(1)[2], scenes.make_cameras(3)[0], scenes.make_cameras(1)[7]]
+
+
+@pytest.mark.parametrize("case", ["small-10-views", "300k-4-views", "mixed-sizes"])
+def test_bin_sort_batch_bit_exact(case):
+    P, cams = _batch_case(case)
+    planes_list = [proj_planes_from_oracle(oracle.project(P, c)) for c in cams]
+    out, counts = gpu_bin_sort_batch(planes_list, cams)
+    assert (counts[:, 1] == 0).all()
+    for b, (planes, cam) in enumerate(zip(planes_list, cams)):
+        uvzo, conic, radius, rgb = oracle_inputs_from_planes(planes)
+        keys_o, vals_o, ranges_o = oracle.bin_sort(uvzo, radius, cam.width, cam.height)
+        keys, vals, ranges, M = out[b]
+        assert M == len(keys_o) == counts[b, 0], b
+        assert np.array_equal(keys, keys_o), b
+        assert np.array_equal(vals, vals_o), b
+        assert np.array_equal(ranges, ranges_o), b
+
+
+def test_bin_sort_batch_timeout_is_per_view():
+    """View 0's depth-sort barrier never completes: view 0 reports the timeout, the other
+    views of the launch finish cleanly and the next call is clean."""
+    P = scenes.make_params(1, n=100_000)
+    cams = [scenes.make_cameras(1)[v] for v in (0, 1, 2)]
+    planes_list = [proj_planes_from_oracle(oracle.project(P, c)) for c in cams]
+    N.gs_debug_set_wait_limit(2000)
+    N.gs_debug_drop_publish(2)
+    try:
+        with pytest.raises(N.GSError) as e:
+            gpu_bin_sort_batch(planes_list, cams)
+        assert e.value.status == N.GS_ERR_TIMEOUT
+    finally:
+        N.gs_debug_drop_publish(0)
+        N.gs_debug_set_wait_limit(0)
+    out, counts = gpu_bin_sort_batch(planes_list, cams)
+    assert (counts[:, 1] == 0).all() and all(o[3] > 0 for o in out)
+
+
 # ------------------------------------------------------------------ compositing forward
 def oracle_stage_chain(P, cam):
     pr = oracle.project(P, cam)
