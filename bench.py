@@ -427,7 +427,7 @@ def main():
                            "parallelism": "replicas" if world > 1 else "single"},
                 "roofline": roof,
                 "kernels": {"ms_avg": {k: round(v, 4) for k, v in avg.items()},
-                            "calls": "bin_sort, visible_sets and project_bwd_adam once per batch, the rest once per view",
+                            "calls": "project, bin_sort, visible_sets and project_bwd_adam once per batch, the rest once per view",
                             "share": {k: round(v, 4) for k, v in share.items()}, **others},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk.summary(), "instances_per_view": int(st[:, 0].float().mean().item())}

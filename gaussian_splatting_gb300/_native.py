@@ -17,7 +17,7 @@ GS_OK, GS_ERR_INVALID, GS_ERR_CUDA, GS_ERR_CAPACITY, GS_ERR_TIMEOUT = 0, 1, 2, 3
 _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ERR_TIMEOUT"}
 
 # every symbol include/gs.h declares
-EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_bin_sort_workspace_size", "gs_bin_sort",
+EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_project_batch", "gs_bin_sort_workspace_size", "gs_bin_sort",
            "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
@@ -66,6 +66,7 @@ def load() -> C.CDLL:
         "gs_last_error": ([], C.c_char_p),
         "gs_version": ([], C.c_int),
         "gs_project": ([vp, i64, cp, vp, vp], i32),
+        "gs_project_batch": ([vp, i64, vp, i32, vp, vp], i32),
         "gs_bin_sort_workspace_size": ([i64, i64, cp], sz),
         "gs_bin_sort": ([vp, i64, cp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
         "gs_bin_sort_batch_workspace_size": ([i32, i64, i64, vp], sz),
@@ -131,6 +132,12 @@ def version() -> int:
 
 def gs_project(params, n, cam, proj, stream=None):
     _check(load().gs_project(_ptr(params), n, _cam(cam), _ptr(proj), _stream(stream)), "gs_project")
+
+
+def gs_project_batch(params, n, cams, projs, stream=None):
+    """gs_project for len(cams) views; projs is a list of per-view [3][n][4] outputs."""
+    c, p = _cams(cams), _ptrs(projs)
+    _check(load().gs_project_batch(_ptr(params), n, c[0], len(cams), p[0], _stream(stream)), "gs_project_batch")
 
 
 def gs_bin_sort_workspace_size(n, capacity, cam) -> int:

@@ -5,6 +5,7 @@
 // parameter plane is read as one coalesced float4 per thread (512 B per warp), the SH
 // planes only for Gaussians that survive the culls.  HBM-bound: 240 B read + 48 B written
 // per visible Gaussian, 16 B read per culled one.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -203,14 +204,11 @@ __device__ __forceinline__ bool project_core(const Src& src, const Cam& k, Fwd& 
   return project_view(src, k, f);
 }
 
-__global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ params, int64_t n, Cam k,
-                                                     float3 campos, float* __restrict__ proj) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  Fwd f;
-  float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, q2 = q0;
-  const GlobalParams src{params, n, i};
-  if (project_core(src, k, f)) {
+// Colour and the three records of Gaussian i in a view that does not cull it.
+template <class Src>
+__device__ __forceinline__ void emit_projection(const Src& src, const Fwd& f, float3 campos, float* __restrict__ proj,
+                                                int64_t n, int64_t i) {
+  {
     const float4 p0 = src.plane(0);
     float dx = p0.x - campos.x, dy = p0.y - campos.y, dz = p0.z - campos.z;
     const float il = rsqrtf(dx * dx + dy * dy + dz * dz);
@@ -228,14 +226,64 @@ __global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ p
         rgb[fidx % 3] += sv[l] * b.y[fidx / 3];
       }
     }
-    q0 = make_float4(f.u, f.v, f.pz, f.opac);
-    q1 = make_float4(f.A, f.B, f.C, __int_as_float(f.radius));
-    q2 = make_float4(fmaxf(rgb[0], 0.f), fmaxf(rgb[1], 0.f), fmaxf(rgb[2], 0.f),
-                     __int_as_float((f.x1 - f.x0) * (f.y1 - f.y0)));
+    st4(proj, i, make_float4(f.u, f.v, f.pz, f.opac));
+    st4(proj, n + i, make_float4(f.A, f.B, f.C, __int_as_float(f.radius)));
+    st4(proj, 2 * n + i, make_float4(fmaxf(rgb[0], 0.f), fmaxf(rgb[1], 0.f), fmaxf(rgb[2], 0.f),
+                                     __int_as_float((f.x1 - f.x0) * (f.y1 - f.y0))));
   }
-  st4(proj, i, q0);
-  st4(proj, n + i, q1);
-  st4(proj, 2 * n + i, q2);
+}
+
+// Zero records: Gaussian i is culled in this view.
+__device__ __forceinline__ void emit_culled(float* __restrict__ proj, int64_t n, int64_t i) {
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  st4(proj, i, z);
+  st4(proj, n + i, z);
+  st4(proj, 2 * n + i, z);
+}
+
+__global__ void __launch_bounds__(256) k_project_fwd(const float* __restrict__ params, int64_t n, Cam k,
+                                                     float3 campos, float* __restrict__ proj) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  Fwd f;
+  const GlobalParams src{params, n, i};
+  if (project_core(src, k, f)) emit_projection(src, f, campos, proj, n, i);
+  else emit_culled(proj, n, i);
+}
+
+// Up to 16 views of one batch in one launch: the parameters are read once and the
+// view-independent part (scales, opacity, rotation, 3-D covariance) is computed once, at the
+// first view that does not cull the Gaussian at the near plane.
+constexpr int kMaxProjViews = 16;
+struct ProjViews {
+  Cam k[kMaxProjViews];
+  float3 campos[kMaxProjViews];
+  float* proj[kMaxProjViews];
+  int batch;
+};
+
+__global__ void __launch_bounds__(256) k_project_fwd_batch(const float* __restrict__ params, int64_t n,
+                                                           const __grid_constant__ ProjViews pv) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const GlobalParams src{params, n, i};
+  const float4 p0 = src.plane(0);
+  Fwd f;
+  bool intrinsics = false;
+  for (int b = 0; b < pv.batch; ++b) {
+    const Cam& k = pv.k[b];
+    const float pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
+    bool visible = false;
+    if (pz > k.znear) {  // the near-plane cull needs only the mean
+      if (!intrinsics) {
+        project_intrinsics(src, f);
+        intrinsics = true;
+      }
+      visible = project_view(src, k, f);
+    }
+    if (visible) emit_projection(src, f, pv.campos[b], pv.proj[b], n, i);
+    else emit_culled(pv.proj[b], n, i);
+  }
 }
 
 // Reverse mode of the projection of Gaussian i for one camera: parameter gradients from its
@@ -556,6 +604,36 @@ extern "C" gs_status gs_project(const float* params, int64_t n, const gs_camera*
   const unsigned blocks = (unsigned)((n + threads - 1) / threads);
   k_project_fwd<<<blocks, threads, 0, gs::as_stream(stream)>>>(params, n, k, camera_centre(*cam), proj);
   return gs::check_launch("gs_project");
+}
+
+extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_camera* cams, int batch,
+                                      float* const* projs, void* stream) {
+  if (batch < 1) return gs::set_error(GS_ERR_INVALID, "gs_project_batch: batch must be >= 1");
+  if (n < 0 || n > (int64_t(1) << 31))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_batch: bad n %lld", (long long)n);
+  if (!cams || !projs) return gs::set_error(GS_ERR_INVALID, "gs_project_batch: NULL pointer");
+  for (int b = 0; b < batch; ++b) {
+    if (gs_status s = gs::check_camera(&cams[b])) return s;
+    if (n > 0 && (!projs[b] || !gs::aligned16(projs[b])))
+      return gs::set_error(GS_ERR_INVALID, "gs_project_batch: view %d proj NULL or misaligned", b);
+  }
+  if (n == 0) return GS_OK;
+  if (!params || !gs::aligned16(params))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_batch: params NULL or misaligned");
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+  for (int b0 = 0; b0 < batch; b0 += kMaxProjViews) {
+    ProjViews pv{};
+    pv.batch = std::min(kMaxProjViews, batch - b0);
+    for (int b = 0; b < pv.batch; ++b) {
+      pv.k[b] = gs::make_cam(cams[b0 + b]);
+      pv.campos[b] = camera_centre(cams[b0 + b]);
+      pv.proj[b] = projs[b0 + b];
+    }
+    k_project_fwd_batch<<<blocks, threads, 0, gs::as_stream(stream)>>>(params, n, pv);
+    if (gs_status s = gs::check_launch("gs_project_batch")) return s;
+  }
+  return GS_OK;
 }
 
 extern "C" gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, const float* proj,

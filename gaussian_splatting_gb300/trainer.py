@@ -3,7 +3,7 @@
 ``Trainer`` owns the device state (parameters, gradients, Adam moments, per-view scratch)
 as torch tensors -- torch supplies memory and the stream, every computation is a libgs.so
 kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
-training flow (训练流程): project every view, bin/sort them all (gs_bin_sort_batch: the
+training flow (训练流程): project every view (gs_project_batch), bin/sort them all (gs_bin_sort_batch: the
 views' depth sorts share one launch), then for each view composite -> loss -> composite
 backward; then the visible sets, and the projection backward of every view
 with the visible-only Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch
@@ -194,13 +194,12 @@ class Trainer:
         if host_targets is not None:  # marks the point the target uploads may start from
             step_start = torch.cuda.Event()
             step_start.record()
-        for b, cam in enumerate(ccams):
-            T("project", N.gs_project, self.params, n, cam, self.proj[b], stream=st)
+        T("project", N.gs_project_batch, self.params, n, ccams, [self.proj[b] for b in range(B)], stream=st)
         ws = self._sort_ws(ccams[0])
         T("bin_sort", N.gs_bin_sort_batch, [self.proj[b] for b in range(B)], n, ccams, ws, ws.numel(), None,
           [self.vals[b] for b in range(B)], self.capacity, [self.ranges[b] for b in range(B)], self.counts,
           stream=st)
-        launches += B * LAUNCHES["project"] + bin_sort_launches(B)
+        launches += (B + 15) // 16 * LAUNCHES["project"] + bin_sort_launches(B)
         for b, cam in enumerate(ccams):
             proj, vals, ranges = self.proj[b], self.vals[b], self.ranges[b]
             work_buf = None

@@ -80,6 +80,17 @@ int gs_version(void);
  */
 gs_status gs_project(const float* params, int64_t n, const gs_camera* cam, float* proj, void* stream);
 
+/* gs_project_batch -- gs_project for the `batch` views of one training step (the Grendel-GS
+ * notes' batch of images, §4.2), results identical to `batch` gs_project calls.  One launch
+ * per 16 views reads each Gaussian's parameters once and computes the view-independent part
+ * (scales, opacity, rotation, 3-D covariance) once.
+ *   cams   host array of `batch` cameras.
+ *   projs  host array of `batch` device pointers, [3][n][4] each, 16-byte aligned.
+ * batch must be >= 1; n == 0 is a no-op.
+ */
+gs_status gs_project_batch(const float* params, int64_t n, const gs_camera* cams, int batch,
+                           float* const* projs, void* stream);
+
 /* ---------------------------------------------------------------------------
  * gs_bin_sort -- tile binning and depth sort ("find the Gaussians covering a pixel,
  * sort by depth"; Grendel-GS notes, 训练流程, with 16x16 tiles, §1.2).

@@ -119,6 +119,28 @@ def test_project_empty_and_single():
         N.gs_project(dev(P), -1, cam, proj)
 
 
+@pytest.mark.parametrize("case", ["60k-mixed-sizes", "2k-18-views"])
+def test_project_batch_matches_per_view(case):
+    """gs_project_batch equals gs_project view by view, bit for bit (18 views: two launches)."""
+    if case == "60k-mixed-sizes":
+        P = scenes.make_params(1, n=60_000)
+        cams = [scenes.make_cameras(1)[v] for v in (0, 17, 33)] + [scenes.make_cameras(3)[1]]
+    else:
+        P = scenes.make_params(1, n=2048)
+        cams = scenes.make_cameras(1)[:18]
+    n = P.shape[1]
+    projs = [torch.full((3, n, 4), 7.0, dtype=torch.float32, device="cuda") for _ in cams]
+    N.gs_project_batch(dev(P), n, cams, projs)
+    torch.cuda.synchronize()
+    for b, cam in enumerate(cams):
+        single = gpu_project(P, cam)
+        assert np.array_equal(host(projs[b]).view(np.uint32), single.view(np.uint32)), b
+    # and the first view against the oracle's integer decisions
+    pr = oracle.project(P, cams[0])
+    ok = pr["margin"] >= MARGIN
+    assert np.array_equal(host(projs[0])[1, ok, 3].view(np.int32), pr["radius"][ok])
+
+
 # ------------------------------------------------------------------ binning + sort
 @pytest.mark.parametrize("cfg,n,view", [(0, None, 0), (0, 1, 0), (0, 2047, 0), (0, 2049, 0), (1, 300_000, 5),
                                         (2, 200_000, 3)])
