@@ -49,6 +49,10 @@ constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N i
 constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
 constexpr int kSlice = kSortThreads * kTileItems;  // instances per generated radix tile
 constexpr int kDepthPasses = 4;
+constexpr int kMaxSortViews = 8;  // views per sort launch
+// views whose tile sorts share a launch: as many as have their own capacity-sized ping-pong
+// buffers within this budget (at least one, at most kMaxSortViews)
+constexpr double kTileBudgetBytes = 1024.0 * 1024.0 * 1024.0;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // digit histogram / base slots
 
@@ -91,11 +95,11 @@ int tile_bits(int64_t T) {
 
 int tile_passes(const gs::Cam& k) { return std::max(1, (tile_bits((int64_t)k.Tx * k.Ty) + 7) / 8); }
 
-// Workspace layout: the tile-sort buffers (capacity-sized, shared by the views, whose tile
-// sorts run one after another), then per view the depth-sort buffers and the scan's records.
-// w (if not NULL) receives `views` entries.
+// Workspace layout: `tile_slots` sets of tile-sort buffers (capacity-sized; view v uses set
+// v % tile_slots, the views of one tile-sort launch having sets of their own), then per view
+// the depth-sort buffers and the scan's records.  w (if not NULL) receives `views` entries.
 size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_t grid_words, int64_t n_tiles,
-             int64_t n_grids) {
+             int64_t n_grids, int tile_slots) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -103,11 +107,11 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
     return p;
   };
   const int64_t chunks = (n + kScanChunk - 1) / kScanChunk;
-  char* tk0 = take(sizeof(uint32_t) * (size_t)cap);
-  char* tk1 = take(sizeof(uint32_t) * (size_t)cap);
-  char* tv0 = take(sizeof(uint32_t) * (size_t)cap);
-  char* tv1 = take(sizeof(uint32_t) * (size_t)cap);
-  char* lbt = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kTileItems>(cap));
+  char* tk[kMaxSortViews][5];
+  for (int t = 0; t < tile_slots; ++t) {
+    for (int j = 0; j < 4; ++j) tk[t][j] = take(sizeof(uint32_t) * (size_t)cap);
+    tk[t][4] = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kTileItems>(cap));
+  }
   for (int v = 0; v < views; ++v) {
     char* dk0 = take(sizeof(uint32_t) * (size_t)n);
     char* dk1 = take(sizeof(uint32_t) * (size_t)n);
@@ -123,11 +127,12 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
     char* sm = take(sizeof(uint32_t) * kSmWords);
     if (w) {
       Workspace& x = w[v];
-      x.tkey[0] = reinterpret_cast<uint32_t*>(tk0);
-      x.tkey[1] = reinterpret_cast<uint32_t*>(tk1);
-      x.tval[0] = reinterpret_cast<uint32_t*>(tv0);
-      x.tval[1] = reinterpret_cast<uint32_t*>(tv1);
-      x.hist_tile = reinterpret_cast<uint32_t*>(lbt);
+      char* const* t = tk[v % tile_slots];
+      x.tkey[0] = reinterpret_cast<uint32_t*>(t[0]);
+      x.tkey[1] = reinterpret_cast<uint32_t*>(t[1]);
+      x.tval[0] = reinterpret_cast<uint32_t*>(t[2]);
+      x.tval[1] = reinterpret_cast<uint32_t*>(t[3]);
+      x.hist_tile = reinterpret_cast<uint32_t*>(t[4]);
       x.dkey[0] = reinterpret_cast<uint32_t*>(dk0);
       x.dkey[1] = reinterpret_cast<uint32_t*>(dk1);
       x.didx[0] = reinterpret_cast<uint32_t*>(di0);
@@ -218,8 +223,7 @@ struct RadixJob {
   int tpasses;          // tile passes (their digit bases go to the small block)
 };
 
-// The depth-sort jobs of one launch (kernel parameter space: 8 jobs stay under 4 KB).
-constexpr int kMaxSortViews = 8;
+// The sort jobs of one launch (kernel parameter space: 8 jobs stay under 4 KB).
 struct RadixBatch {
   RadixJob job[kMaxSortViews];
   int views;
@@ -955,23 +959,19 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
   }
 }
 
-// The tile sort of one view: every CTA of the grid works on the job.
-__global__ void __launch_bounds__(kSortThreads, 4) k_tile_sort(RadixJob J) {
-  radix_body<kTileItems, true>(J, gridDim.x, blockIdx.x);
-}
-
-// The depth sorts of up to kMaxSortViews views in one launch: CTAs [v G, (v + 1) G) sort view
-// v, with their own barrier counter and workspace, so the views' latency-bound phases overlap.
-// A CTA reads its view's job from parameter space once, into shared memory.
+// The sorts of up to kMaxSortViews views in one launch: CTAs [v G, (v + 1) G) sort view v,
+// with their own barrier counter and workspace, so the views' barrier waits and uneven phases
+// overlap.  A CTA reads its view's job in place, from kernel parameter space.
 __global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort(const __grid_constant__ RadixBatch B) {
-  __shared__ RadixJob s_job;
   const uint32_t G = gridDim.x / (uint32_t)B.views;
   const uint32_t view = blockIdx.x / G;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(&B.job[view]);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(&s_job);
-  for (int i = threadIdx.x; i < (int)(sizeof(RadixJob) / 4); i += kSortThreads) dst[i] = src[i];
-  __syncthreads();
-  radix_body<kDepthItems, false>(s_job, G, blockIdx.x - view * G);
+  radix_body<kDepthItems, false>(B.job[view], G, blockIdx.x - view * G);
+}
+
+__global__ void __launch_bounds__(kSortThreads, 4) k_tile_sort(const __grid_constant__ RadixBatch B) {
+  const uint32_t G = gridDim.x / (uint32_t)B.views;
+  const uint32_t view = blockIdx.x / G;
+  radix_body<kTileItems, true>(B.job[view], G, blockIdx.x - view * G);
 }
 
 // Per view of a batch: the buffers zeroed before the sorts (the status words, the small
@@ -1025,9 +1025,9 @@ int radix_blocks_per_sm(size_t smem) {
 }
 
 // Cooperative launches: every CTA of the grid is resident at once, which the grid barriers need.
-cudaError_t launch_tile_sort(const RadixJob& job, int grid, size_t smem, cudaStream_t st) {
-  RadixJob j = job;
-  void* args[] = {&j};
+cudaError_t launch_tile_sort(const RadixBatch& batch, int grid, size_t smem, cudaStream_t st) {
+  RadixBatch b = batch;
+  void* args[] = {&b};
   return cudaLaunchCooperativeKernel((const void*)k_tile_sort, dim3(grid), dim3(kSortThreads), args, smem, st);
 }
 cudaError_t launch_depth_sort(const RadixBatch& batch, int grid, size_t smem, cudaStream_t st) {
@@ -1047,6 +1047,13 @@ int64_t depth_grids_bound(int64_t n) {
   return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n) + 1, (int64_t)gs::num_sms() * 8));
 }
 constexpr size_t kMaxSortSmem = 227 * 1024;  // shared memory a CTA may have
+
+// Views per tile-sort launch for a capacity (see kTileBudgetBytes).
+int tile_group(int views, int64_t cap) {
+  const double per_view = 16.0 * (double)std::max<int64_t>(cap, 1) + 1024.0 * (double)sort_tiles<kTileItems>(cap);
+  const int fit = (int)std::min<double>(kMaxSortViews, std::floor(kTileBudgetBytes / per_view));
+  return std::max(1, std::min({fit, views, kMaxSortViews}));
+}
 
 // Largest grid words and tiles over a batch of cameras.
 void batch_dims(const gs::Cam* k, int views, int64_t* gw, int64_t* T) {
@@ -1071,7 +1078,7 @@ struct SortView {
 // to kMaxSortViews: one zeroing launch, one depth-sort launch, one tile sort per view, one
 // publishing launch.  A group's depth buffers are w[0 .. group size), reused by the next group
 // once the tile sorts before it (which read them) are enqueued.
-gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, const Workspace* w,
+gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, const Workspace* w, int tg,
                     cudaStream_t st) {
   const int64_t limit = gs::wait_limit();
   const int drop = gs::take_drop_publish();
@@ -1131,22 +1138,28 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. per view, the stable sort of the instances by tile id: the first pass generates the
     //    (tile, index) pairs in depth order from the scan's records, the last writes the
-    //    caller's arrays
+    //    caller's arrays; tg views per launch, each with its own ping-pong buffers
     const size_t tsmem = sizeof(SortSmem<kTileItems>);
-    const int tgrid = (int)std::max<int64_t>(
-        1, std::min<int64_t>((int64_t)sms * radix_blocks_per_sm<true>(tsmem), sort_tiles<kTileItems>(capacity)));
-    for (int v = 0; v < gv; ++v) {
-      const SortView& sv = V[g0 + v];
-      RadixJob tj{};
-      tj.key[0] = w[v].tkey[0]; tj.key[1] = w[v].tkey[1];
-      tj.val[0] = w[v].tval[0]; tj.val[1] = w[v].tval[1];
-      tj.n_host = -1; tj.cap = capacity; tj.passes = tile_passes(sv.k);
-      tj.slot0 = kDepthPasses; tj.sort_id = 1;
-      tj.hist = w[v].hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
-      tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
-      tj.gen = GenSource{w[v].slice_first, w[v].grec, n, sv.k.Tx};
-      tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
-      if (cudaError_t e = launch_tile_sort(tj, tgrid, tsmem, st))
+    const int64_t tresident = (int64_t)sms * radix_blocks_per_sm<true>(tsmem);
+    for (int t0 = 0; t0 < gv; t0 += tg) {
+      const int tv = std::min(tg, gv - t0);
+      RadixBatch tb{};
+      tb.views = tv;
+      for (int j = 0; j < tv; ++j) {
+        const int v = t0 + j;
+        const SortView& sv = V[g0 + v];
+        RadixJob& tj = tb.job[j];
+        tj.key[0] = w[v].tkey[0]; tj.key[1] = w[v].tkey[1];
+        tj.val[0] = w[v].tval[0]; tj.val[1] = w[v].tval[1];
+        tj.n_host = -1; tj.cap = capacity; tj.passes = tile_passes(sv.k);
+        tj.slot0 = kDepthPasses; tj.sort_id = 1;
+        tj.hist = w[v].hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
+        tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
+        tj.gen = GenSource{w[v].slice_first, w[v].grec, n, sv.k.Tx};
+        tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
+      }
+      const int64_t TG = std::max<int64_t>(1, std::min<int64_t>(tresident / tv, sort_tiles<kTileItems>(capacity)));
+      if (cudaError_t e = launch_tile_sort(tb, (int)(TG * tv), tsmem, st))
         return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
       if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
     }
@@ -1198,7 +1211,8 @@ extern "C" size_t gs_bin_sort_batch_workspace_size(int batch, int64_t n, int64_t
   for (int v = 0; v < batch; ++v) k[v] = gs::make_cam(cams[v]);
   int64_t gw, T;
   batch_dims(k.data(), batch, &gw, &T);
-  return carve(nullptr, nullptr, std::min(batch, kMaxSortViews), n, capacity, gw, T, depth_grids_bound(n));
+  return carve(nullptr, nullptr, std::min(batch, kMaxSortViews), n, capacity, gw, T, depth_grids_bound(n),
+               tile_group(batch, capacity));
 }
 
 extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* cam, void* workspace,
@@ -1217,10 +1231,10 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: workspace %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w;
   carve(&w, reinterpret_cast<char*>(workspace), 1, n, capacity, grid_words(k), (int64_t)k.Tx * k.Ty,
-        depth_grids_bound(n));
+        depth_grids_bound(n), 1);
   cudaStream_t st = gs::as_stream(stream);
   const SortView view{proj, k, keys, vals, ranges, count};
-  if (gs_status s = run_sorts(&view, 1, n, capacity, &w, st)) return s;
+  if (gs_status s = run_sorts(&view, 1, n, capacity, &w, 1, st)) return s;
   if (!count_host) return GS_OK;
   const int64_t* c = count;
   return read_counts(&c, 1, count_host, st);
@@ -1256,9 +1270,9 @@ extern "C" gs_status gs_bin_sort_batch(const float* const* projs, int batch, int
   batch_dims(k.data(), batch, &gw, &T);
   Workspace w[kMaxSortViews];
   carve(w, reinterpret_cast<char*>(workspace), std::min(batch, kMaxSortViews), n, capacity, gw, T,
-        depth_grids_bound(n));
+        depth_grids_bound(n), tile_group(batch, capacity));
   cudaStream_t st = gs::as_stream(stream);
-  if (gs_status s = run_sorts(V.data(), batch, n, capacity, w, st)) return s;
+  if (gs_status s = run_sorts(V.data(), batch, n, capacity, w, tile_group(batch, capacity), st)) return s;
   if (!counts_host) return GS_OK;
   std::vector<const int64_t*> c((size_t)batch);
   for (int v = 0; v < batch; ++v) c[v] = counts + 2 * v;

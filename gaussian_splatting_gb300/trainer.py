@@ -19,6 +19,7 @@ again.
 from __future__ import annotations
 
 import dataclasses
+import math
 
 import numpy as np
 
@@ -34,12 +35,24 @@ LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_
 MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
 
-def bin_sort_launches(views: int) -> int:
+def tile_group(views: int, capacity: int) -> int:
+    """Views whose tile sorts share one launch in gs_bin_sort_batch: as many as have their own
+    capacity-sized ping-pong buffers (16 B per instance) within 1 GiB, 1..8."""
+    per_view = 16.0 * max(capacity, 1) + 1024.0 * ((capacity + 3071) // 3072)
+    fit = min(8, int(math.floor(float(1 << 30) / per_view)))
+    return max(1, min(fit, views, 8))
+
+
+def bin_sort_launches(views: int, capacity: int) -> int:
     # per group of up to 8 views: zeroing, the depth sorts (keys, tile-count grids, the four
-    # passes, the tiles-touched scans and the tile counts in one cooperative launch), ranges;
-    # per view: the tile sort (both passes in one cooperative launch)
-    groups = (views + 7) // 8
-    return 3 * groups + views
+    # passes, the tiles-touched scans and the tile counts in one cooperative launch), the tile
+    # sorts (both passes of tile_group views per cooperative launch), ranges
+    total = 0
+    for g0 in range(0, views, 8):
+        gv = min(8, views - g0)
+        tg = tile_group(views, capacity)
+        total += 3 + (gv + tg - 1) // tg
+    return total
 
 
 @dataclasses.dataclass
@@ -199,7 +212,7 @@ class Trainer:
         T("bin_sort", N.gs_bin_sort_batch, [self.proj[b] for b in range(B)], n, ccams, ws, ws.numel(), None,
           [self.vals[b] for b in range(B)], self.capacity, [self.ranges[b] for b in range(B)], self.counts,
           stream=st)
-        launches += (B + 15) // 16 * LAUNCHES["project"] + bin_sort_launches(B)
+        launches += (B + 15) // 16 * LAUNCHES["project"] + bin_sort_launches(B, self.capacity)
         for b, cam in enumerate(ccams):
             proj, vals, ranges = self.proj[b], self.vals[b], self.ranges[b]
             work_buf = None

@@ -71,13 +71,15 @@ def test_workspace_sizes_are_pure_host_functions(lib):
     a = N.gs_bin_sort_workspace_size(300_000, 10_000_000, cam)
     b = N.gs_bin_sort_workspace_size(300_000, 20_000_000, cam)
     assert 0 < a < b
-    # a batch shares the capacity-sized tile-sort buffers and holds depth buffers for up to 8 views
-    b1 = N.gs_bin_sort_batch_workspace_size(1, 300_000, 10_000_000, [cam])
-    b4 = N.gs_bin_sort_batch_workspace_size(4, 300_000, 10_000_000, [cam] * 4)
-    b8 = N.gs_bin_sort_batch_workspace_size(8, 300_000, 10_000_000, [cam] * 8)
-    b16 = N.gs_bin_sort_batch_workspace_size(16, 300_000, 10_000_000, [cam] * 16)
-    assert b1 == a and a < b4 < 4 * a and b8 == b16
-    assert (b4 - a) * 7 == (b8 - a) * 3  # equal per-view depth parts
+    # a batch holds depth buffers for up to 8 views and capacity-sized tile-sort buffers for the
+    # views that share a tile-sort launch (as many as fit 1 GiB): one set at 100M instances...
+    big = [N.gs_bin_sort_batch_workspace_size(b, 300_000, 100_000_000, [cam] * b) for b in (1, 4, 8, 16)]
+    assert big[0] == N.gs_bin_sort_workspace_size(300_000, 100_000_000, cam)
+    assert (big[1] - big[0]) * 7 == (big[2] - big[0]) * 3 and big[2] == big[3]  # equal per-view depth parts
+    # ... six sets at 10M (160 MB each), so a batch of 4 holds four and one of 8 or 16 six
+    b = [N.gs_bin_sort_batch_workspace_size(k, 300_000, 10_000_000, [cam] * k) for k in (1, 4, 8, 16)]
+    assert b[0] == a and b[2] == b[3]
+    assert b[1] - b[0] == 3 * b[0]  # four views: four depth parts and four tile sets
     assert N.gs_loss_workspace_size(1236, 820) > 0
     assert N.gs_visible_sets_workspace_size(4, 300_000) > 0
     assert N.gs_visible_sets_workspace_size(65, 10) == 0
@@ -87,7 +89,10 @@ def test_launch_count_bookkeeping():
     import scenes
     from gaussian_splatting_gb300.trainer import bin_sort_launches
     # every radix pass of a sort runs inside one cooperative launch; per group of up to 8 views
-    # one zeroing, one depth-sort and one publishing launch, per view one tile sort
-    assert bin_sort_launches(1) == 4
-    assert bin_sort_launches(4) == 7
-    assert bin_sort_launches(16) == 22
+    # one zeroing, one depth-sort and one publishing launch, and the tile sorts of as many views
+    # per launch as have ping-pong buffers within 1 GiB (six at 10M instances, one at 100M)
+    assert bin_sort_launches(1, 10_000_000) == 4
+    assert bin_sort_launches(4, 10_000_000) == 4
+    assert bin_sort_launches(4, 100_000_000) == 7
+    assert bin_sort_launches(16, 10_000_000) == 2 * (3 + 2)
+    assert bin_sort_launches(16, 100_000_000) == 22
