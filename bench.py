@@ -50,10 +50,10 @@ HBM_FALLBACK_GBS = 6800.0
 # the benchmark workload, keyed by entry point, valid only for the kernel source it was measured
 # on: when the source file's hash differs the figure is reported as null.
 NCU_TRAFFIC = {
-    # profiles/render_object-300k-1236x820.md: 38.313 MB read + 0.032 MB written per launch
+    # profiles/render_object-300k-1236x820.md: 38.308 MB read + 0.052 MB written per launch
     "render_bwd": {"source": "gaussian_splatting_gb300/csrc/render.cu",
                    "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
-                   "bytes": 38345472},
+                   "bytes": 38359552},
 }
 
 
@@ -328,19 +328,20 @@ def main():
     views = args.steps * cfg.batch * world
     value = views / (total_ms / 1000.0)
 
-    # ---------------- work counts of the timed batches (untimed re-run, same views)
-    tr_w = Trainer(params.clone(), cfg.width, cfg.height, cfg.batch, lr=cfg.lr, eps=cfg.eps, capacity=tr.capacity)
-    tr_w.work = []
+    # ---------------- work counts of the timed batches (untimed re-run of the same views on the
+    # same trainer, gradients only: the parameters do not move; the gradients are cleared)
+    tr.work = []
     for s in range(args.steps):
         ids, bc = batch_of(args.warmup + s)
-        tr_w.step_async(bc, targets[torch.tensor(ids, device="cuda")], adam=False)
-        tr_w.grads.zero_()
-    n_views = max(1, len(tr_w.work))
-    ev = sum(w[0] for w in tr_w.work) / n_views
-    used = sum(w[1] for w in tr_w.work) / n_views
-    walked = sum(w[2] for w in tr_w.work) / n_views
-    warp_pairs = sum(w[3] for w in tr_w.work) / n_views
-    del tr_w
+        tr.step_async(bc, targets[torch.tensor(ids, device="cuda")], adam=False)
+        tr.grads.zero_()
+    work = tr.work
+    tr.work = None
+    n_views = max(1, len(work))
+    ev = sum(w[0] for w in work) / n_views
+    used = sum(w[1] for w in work) / n_views
+    walked = sum(w[2] for w in work) / n_views
+    warp_pairs = sum(w[3] for w in work) / n_views
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
     peak_hbm, hbm_src = hbm_peak()
