@@ -66,6 +66,10 @@ def lib():
         L.oracle_step.restype = dbl
         L.oracle_sh_basis.argtypes = [dp, dp, dp]
         L.oracle_sh_basis.restype = None
+        L.oracle_tile_split.argtypes = [up, i32, i32, i32, u64p, u64p, i64p]
+        L.oracle_tile_split.restype = None
+        L.oracle_view_order.argtypes = [fp, i32, i32, ip, fp]
+        L.oracle_view_order.restype = None
         _lib = L
     return _lib
 
@@ -196,6 +200,30 @@ def visible_sets(radii):
     lib().oracle_visible_sets(_p(R, C.c_int32), B, N, _p(off, C.c_int64), _p(ind, C.c_uint32), _p(uni, C.c_uint32),
                               _p(nu, C.c_int64), _p(inter, C.c_int64), _p(jac, C.c_float))
     return off, ind[:tot], uni[: int(nu[0])], inter, jac
+
+
+def tile_split(cost_px, parts):
+    """cost_px: H x W uint32 per-pixel costs.  Returns (tile_cost [T] uint64, cum [T] uint64,
+    bounds [parts + 1] int64): block k of the split holds tiles [bounds[k], bounds[k + 1])."""
+    c = np.ascontiguousarray(cost_px, np.uint32)
+    H, W = c.shape
+    T = ((W + 15) // 16) * ((H + 15) // 16)
+    tc = np.zeros(T, np.uint64)
+    cum = np.zeros(T, np.uint64)
+    bounds = np.zeros(parts + 1, np.int64)
+    lib().oracle_tile_split(_p(c, C.c_uint32), W, H, parts, _p(tc, C.c_uint64), _p(cum, C.c_uint64),
+                            _p(bounds, C.c_int64))
+    return tc, cum, bounds
+
+
+def view_order(weights, unit=1):
+    """weights: B x B float32 (the Jaccard matrix).  Returns (order [B] int32, score [B] float32)."""
+    w = np.ascontiguousarray(weights, np.float32)
+    B = w.shape[0]
+    order = np.zeros(B, np.int32)
+    score = np.zeros(B, np.float32)
+    lib().oracle_view_order(_p(w, C.c_float), B, unit, _p(order, C.c_int32), _p(score, C.c_float))
+    return order, score
 
 
 def step(params, m, v, cams, targets, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-15, t=1, w_l1=0.8, w_ssim=0.2,

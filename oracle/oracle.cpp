@@ -30,7 +30,9 @@
 // Parity pins (see tests/test_oracle_*.py): closed form of one isotropic
 // Gaussian, SH against scipy's complex harmonics and by quadrature, brute-force
 // per-pixel compositing, compositing invariants, central finite differences of
-// the whole forward, SSIM identities, Adam closed form at t = 1, set identities.
+// the whole forward, SSIM identities, Adam closed form at t = 1, set identities,
+// balanced splits of known cost profiles, worked view orders on block-structured
+// weights.
 
 #include <algorithm>
 #include <cmath>
@@ -684,6 +686,73 @@ void visible_sets(const int32_t* radius, int B, int64_t N, int64_t* offsets, uin
     }
 }
 
+// Grendel-GS notes §3.1 (pixel-wise load balancing): the render time ET[i] of every 16x16
+// pixel block, CumSum = cumsum(ET), a target of Total / K per GPU, split points by
+// searchsorted.  The per-block "time" here is an integer cost (a per-pixel work count summed
+// over the block), so the sums and the split points are exact.  Split k is the number of
+// blocks whose inclusive cumulative cost is at most k Total / K (searchsorted on the right:
+// a block that ends exactly on a target stays in the earlier part, so equal costs split
+// equally), compared exactly as K C[i] <= k Total.  Part k holds tiles [bounds[k],
+// bounds[k + 1]).
+void tile_split(const uint32_t* cost_px, int W, int H, int K, uint64_t* tile_cost, uint64_t* cum, int64_t* bounds) {
+  const int Tx = (W + 15) / 16, Ty = (H + 15) / 16;
+  const int64_t T = (int64_t)Tx * Ty;
+  for (int ty = 0; ty < Ty; ++ty)
+    for (int tx = 0; tx < Tx; ++tx) {
+      uint64_t s = 0;
+      for (int y = ty * 16; y < std::min(H, ty * 16 + 16); ++y)
+        for (int x = tx * 16; x < std::min(W, tx * 16 + 16); ++x) s += cost_px[(int64_t)y * W + x];
+      tile_cost[(int64_t)ty * Tx + tx] = s;
+    }
+  uint64_t run = 0;
+  for (int64_t i = 0; i < T; ++i) {
+    run += tile_cost[i];
+    cum[i] = run;
+  }
+  const uint64_t total = run;
+  bounds[0] = 0;
+  for (int k = 1; k < K; ++k) {
+    int64_t c = 0;
+    for (int64_t i = 0; i < T; ++i)
+      if ((unsigned __int128)K * cum[i] <= (unsigned __int128)k * total) ++c;
+    bounds[k] = c;
+  }
+  bounds[K] = T;
+}
+
+// Odin summary: the relative locality graph over views with Jaccard edge weights w_uv, and
+// the scheduling score s(v | U_prev) = sum of w_uv over the previous set U_prev; static
+// data scheduling orders the task units so that weakly coupled transitions follow one
+// another.  Views are taken one at a time into task units of `unit` views; the next view is
+// the unscheduled one with the smallest score against the previous unit (ties: the lower
+// index), the first unit's scores being 0.  The scores are float32 sums over the previous
+// unit in its scheduling order -- the precision and order the kernel decides in.
+void view_order(const float* w, int B, int unit, int32_t* order, float* score) {
+  std::vector<int> prev, cur;
+  std::vector<char> done(B, 0);
+  for (int k = 0; k < B; ++k) {
+    int best = -1;
+    float best_s = 0.f;
+    for (int v = 0; v < B; ++v) {
+      if (done[v]) continue;
+      float s = 0.f;
+      for (int u : prev) s += w[(int64_t)u * B + v];
+      if (best < 0 || s < best_s) {
+        best = v;
+        best_s = s;
+      }
+    }
+    done[best] = 1;
+    order[k] = best;
+    score[k] = best_s;
+    cur.push_back(best);
+    if ((int)cur.size() == unit) {
+      prev = cur;
+      cur.clear();
+    }
+  }
+}
+
 }  // namespace
 
 // ======================================================================= C ABI
@@ -767,6 +836,18 @@ void oracle_sparse_adam(double* params, double* grads, double* m, double* v, int
 void oracle_visible_sets(const int32_t* radius, int B, int64_t N, int64_t* offsets, uint32_t* indices,
                          uint32_t* uni, int64_t* n_union, int64_t* inter, float* jac) {
   visible_sets(radius, B, N, offsets, indices, uni, n_union, inter, jac);
+}
+
+// Per-tile costs, their inclusive cumulative sum and the K + 1 split points (Grendel-GS
+// notes §3.1).  cost_px: H x W.  tile_cost, cum: ceil(W/16) ceil(H/16).  bounds: K + 1.
+void oracle_tile_split(const uint32_t* cost_px, int W, int H, int K, uint64_t* tile_cost, uint64_t* cum,
+                       int64_t* bounds) {
+  tile_split(cost_px, W, H, K, tile_cost, cum, bounds);
+}
+
+// Greedy view order by the Odin scheduling score.  w: B x B float32 weights (Jaccard).
+void oracle_view_order(const float* w, int B, int unit, int32_t* order, float* score) {
+  view_order(w, B, unit, order, score);
 }
 
 // One whole training step over B views.  cams: B x 17.  targets: B x 3 x H x W.
