@@ -342,6 +342,52 @@ def main():
     used = sum(w[1] for w in work) / n_views
     walked = sum(w[2] for w in work) / n_views
     warp_pairs = sum(w[3] for w in work) / n_views
+    # ---------------- the scheduling helpers on this workload (untimed by the step): Grendel's
+    # balanced tile split of one view's per-pixel cost (the entries each pixel's warp walked),
+    # and the Odin view order on the batch's Jaccard weights
+    schedule = None
+    try:
+        ids, bc = batch_of(args.warmup + args.steps - 1)
+        H, W, B = cfg.height, cfg.width, cfg.batch
+        wk = torch.zeros((3, H, W), dtype=torch.int32, device="cuda")
+        img = torch.empty((3, H, W), dtype=torch.float32, device="cuda")
+        Tf = torch.empty((H, W), dtype=torch.float32, device="cuda")
+        nc = torch.empty((H, W), dtype=torch.int32, device="cuda")
+        N.gs_render_fwd(tr.proj[0], tr.n, tr.vals[0], tr.ranges[0], bc[0], tr.bg, img, Tf, nc, wk)
+        K = 8
+        T = ((W + 15) // 16) * ((H + 15) // 16)
+        tcost = torch.empty(T, dtype=torch.int64, device="cuda")
+        cum = torch.empty(T, dtype=torch.int64, device="cuda")
+        bounds = torch.empty(K + 1, dtype=torch.int64, device="cuda")
+        order = torch.empty(B, dtype=torch.int32, device="cuda")
+        score = torch.empty(B, dtype=torch.float32, device="cuda")
+        reps = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        N.gs_tile_split(wk[2], W, H, K, tcost, cum, bounds)
+        a.record()
+        for _ in range(reps):
+            N.gs_tile_split(wk[2], W, H, K, tcost, cum, bounds)
+        b.record()
+        torch.cuda.synchronize()
+        split_us = a.elapsed_time(b) / reps * 1e3
+        a.record()
+        for _ in range(reps):
+            N.gs_view_order(tr.jaccard, B, 1, order, score)
+        b.record()
+        torch.cuda.synchronize()
+        order_us = a.elapsed_time(b) / reps * 1e3
+        bl = bounds.cpu().tolist()
+        tc = tcost.cpu()
+        parts = [int(tc[bl[k]:bl[k + 1]].sum()) for k in range(K)]
+        mean = max(1.0, sum(parts) / K)
+        schedule = {"tile_split": {"parts": K, "tiles": T, "us": round(split_us, 2),
+                                   "max_part_over_mean": round(max(parts) / mean, 4),
+                                   "cost": "entries each pixel's warp walked (gs_render_fwd work[2]), one view"},
+                    "view_order": {"views": B, "unit": 1, "us": round(order_us, 2),
+                                   "order": order.cpu().tolist()}}
+    except Exception as e:  # reported, never fatal to the benchmark line
+        schedule = {"error": str(e)[:200]}
+
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
     peak_hbm, hbm_src = hbm_peak()
@@ -430,7 +476,7 @@ def main():
                 "kernels": {"ms_avg": {k: round(v, 4) for k, v in avg.items()},
                             "calls": "project, bin_sort, visible_sets and project_bwd_adam once per batch, the rest once per view",
                             "share": {k: round(v, 4) for k, v in share.items()}, **others},
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "schedule": schedule,
                 "clocks": clk.summary(), "instances_per_view": int(st[:, 0].float().mean().item())}
         print(json.dumps(line), flush=True)
     if dist:

@@ -21,7 +21,7 @@ EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_project_batch", "gs_
            "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
-           "gs_probe_ffma", "gs_debug_set_wait_limit",
+           "gs_tile_split", "gs_view_order", "gs_probe_ffma", "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
 
@@ -81,6 +81,8 @@ def load() -> C.CDLL:
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
         "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp], i32),
+        "gs_tile_split": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
+        "gs_view_order": ([vp, i32, i32, vp, vp, vp], i32),
         "gs_probe_ffma": ([vp, i32, i32, vp], i32),
         "gs_debug_set_wait_limit": ([i64], None),
         "gs_debug_drop_publish": ([i32], None),
@@ -249,6 +251,16 @@ def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr
                                       C.cast(garr, C.c_void_p), _ptr(exp_avg), _ptr(exp_avg_sq), lr, beta1, beta2,
                                       eps, step, _ptr(counts), n_counts if counts is not None else 0,
                                       _stream(stream)), "gs_project_bwd_adam")
+
+
+def gs_tile_split(cost_px, width, height, parts, tile_cost, cum, bounds, stream=None):
+    _check(load().gs_tile_split(_ptr(cost_px), width, height, parts, _ptr(tile_cost), _ptr(cum), _ptr(bounds),
+                                _stream(stream)), "gs_tile_split")
+
+
+def gs_view_order(weights, batch, unit, order, score, stream=None):
+    _check(load().gs_view_order(_ptr(weights), batch, unit, _ptr(order), _ptr(score), _stream(stream)),
+           "gs_view_order")
 
 
 def gs_probe_ffma(out, blocks, iters, stream=None):

@@ -307,6 +307,39 @@ gs_status gs_probe_ffma(float* out, int blocks, int iters, void* stream);
 void gs_debug_set_wait_limit(int64_t iterations);
 void gs_debug_drop_publish(int mode);
 
+/* ---------------------------------------------------------------------------
+ * gs_tile_split -- pixel-wise load balancing of the Grendel-GS notes (§3.1: record each
+ * 16x16 block's render time ET, CumSum = cumsum(ET), a target of Total / K per GPU, split
+ * points by searchsorted).  The block "time" is an integer cost: the per-pixel costs in
+ * cost_px (e.g. work[2] of gs_render_fwd, the entries each pixel's warp walked) summed over
+ * the block, so the sums and the split points are exact.
+ *   cost_px    [H][W] uint32 per-pixel costs.
+ *   tile_cost  output, Tx * Ty uint64: each block's cost (row-major tiles).
+ *   cum        output, Tx * Ty uint64: inclusive cumulative sum of tile_cost.
+ *   bounds     output, parts + 1 int64: part k holds tiles [bounds[k], bounds[k + 1]);
+ *              bounds[k] = number of tiles with parts * cum[i] <= k * Total (searchsorted on
+ *              the right: a tile ending exactly on a target stays in the earlier part; a zero
+ *              total puts every tile in part 0).
+ * parts in 1..1024; 64-bit arrays 8-byte aligned.  Two kernels; no workspace.
+ */
+gs_status gs_tile_split(const uint32_t* cost_px, int width, int height, int parts, uint64_t* tile_cost,
+                        uint64_t* cum, int64_t* bounds, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_view_order -- greedy schedule of a batch's views by the Odin summary's scheduling score
+ * s(v | U_prev) = sum of w_uv over the previous set, with w the Jaccard weights of the
+ * relative locality graph (gs_visible_sets' jaccard output).  The static schedule places
+ * weakly coupled transitions next to each other: views are taken one at a time into task
+ * units of `unit` views, the next being the unscheduled view with the smallest score against
+ * the previous unit (ties: the lower index; the first unit's scores are 0).  Scores are
+ * float32 sums over the previous unit in its scheduling order.
+ *   weights  [batch][batch] float32.
+ *   order    output, batch int32: the views in schedule order.
+ *   score    output, batch float32: each scheduled view's score when it was taken.
+ * batch in 1..64, unit in 1..batch.
+ */
+gs_status gs_view_order(const float* weights, int batch, int unit, int32_t* order, float* score, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

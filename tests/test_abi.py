@@ -57,6 +57,13 @@ def test_host_side_argument_errors(lib):
     assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None) == N.GS_ERR_INVALID
     # misaligned workspace / capacity bounds for the sort
     assert lib.gs_bin_sort(None, 0, C.byref(cam), 8, 10, None, None, 1 << 30, 64, 64, None, None) == N.GS_ERR_INVALID
+    # the scheduling helpers: parts, batch and unit out of range, NULL pointers
+    assert lib.gs_tile_split(None, 64, 64, 0, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_split(None, 64, 64, 1025, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_split(None, 64, 64, 4, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_view_order(None, 65, 1, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_view_order(None, 4, 5, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_view_order(None, 4, 1, None, None, None) == N.GS_ERR_INVALID
     # the batched sort: batch < 1, NULL pointer arrays
     assert lib.gs_bin_sort_batch(None, 0, 0, C.byref(cam), 256, 10, None, None, 0, None, 64, None, None) \
         == N.GS_ERR_INVALID
