@@ -70,6 +70,8 @@ def lib():
         L.oracle_tile_split.restype = None
         L.oracle_view_order.argtypes = [fp, i32, i32, ip, fp]
         L.oracle_view_order.restype = None
+        L.oracle_prune.argtypes = [C.c_void_p, i32, i64, C.c_float, C.c_void_p, i64]
+        L.oracle_prune.restype = i64
         _lib = L
     return _lib
 
@@ -224,6 +226,20 @@ def view_order(weights, unit=1):
     score = np.zeros(B, np.float32)
     lib().oracle_view_order(_p(w, C.c_float), B, unit, _p(order, C.c_int32), _p(score, C.c_float))
     return order, score
+
+
+def prune(plane_sets, min_logit):
+    """plane_sets: list of float32 [15, N, 4] arrays (parameters first: its plane 0, w is the
+    opacity logit).  Returns (kept count, list of [15, kept, 4] arrays)."""
+    sets = [np.ascontiguousarray(p, np.float32) for p in plane_sets]
+    n = sets[0].shape[1]
+    outs = [np.zeros((15, max(n, 1), 4), np.float32) for _ in sets]
+    ins = (C.c_void_p * len(sets))(*[p.ctypes.data for p in sets])
+    ous = (C.c_void_p * len(sets))(*[o.ctypes.data for o in outs])
+    k = lib().oracle_prune(C.cast(ins, C.c_void_p), len(sets), n, C.c_float(min_logit), C.cast(ous, C.c_void_p),
+                           max(n, 1))
+    # the kernel layout keeps the plane stride; re-pack to a stride of k
+    return k, [np.ascontiguousarray(o[:, :k]) for o in outs]
 
 
 def step(params, m, v, cams, targets, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-15, t=1, w_l1=0.8, w_ssim=0.2,

@@ -753,6 +753,26 @@ void view_order(const float* w, int B, int unit, int32_t* order, float* score) {
   }
 }
 
+// Grendel-GS notes, 训练流程 (densification: "prune low-opacity Gaussians"): keep Gaussian i
+// when its opacity logit (plane 0, w) is at least min_logit -- sigmoid is increasing, so
+// this is opacity >= sigmoid(min_logit) -- and copy its 15 parameter planes and both Adam
+// moment planes to the next free slot, in index order.  planes: `n_sets` arrays of
+// [15][n][4]; out: the same sets as [15][out_stride][4].  Returns the number kept.
+int64_t prune(const float* const* planes, int n_sets, int64_t n, float min_logit, float* const* out,
+              int64_t out_stride) {
+  int64_t k = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const float logit = planes[0][(0 * n + i) * 4 + 3];
+    if (!(logit >= min_logit)) continue;
+    if (k < out_stride)
+      for (int s = 0; s < n_sets; ++s)
+        for (int pl = 0; pl < 15; ++pl)
+          for (int c = 0; c < 4; ++c) out[s][((int64_t)pl * out_stride + k) * 4 + c] = planes[s][((int64_t)pl * n + i) * 4 + c];
+    ++k;
+  }
+  return k;
+}
+
 }  // namespace
 
 // ======================================================================= C ABI
@@ -848,6 +868,12 @@ void oracle_tile_split(const uint32_t* cost_px, int W, int H, int K, uint64_t* t
 // Greedy view order by the Odin scheduling score.  w: B x B float32 weights (Jaccard).
 void oracle_view_order(const float* w, int B, int unit, int32_t* order, float* score) {
   view_order(w, B, unit, order, score);
+}
+
+// Opacity pruning: planes / out are arrays of n_sets pointers (parameters, then moments).
+int64_t oracle_prune(const float* const* planes, int n_sets, int64_t n, float min_logit, float* const* out,
+                     int64_t out_stride) {
+  return prune(planes, n_sets, n, min_logit, out, out_stride);
 }
 
 // One whole training step over B views.  cams: B x 17.  targets: B x 3 x H x W.

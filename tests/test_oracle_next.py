@@ -94,3 +94,30 @@ def test_view_order_single_view_and_unit_covering_all():
     w = np.random.default_rng(4).random((6, 6)).astype(np.float32)
     order, _ = oracle.view_order(w, unit=6)  # one unit: no previous set, index order
     assert order.tolist() == list(range(6))
+
+
+# ------------------------------------------------------------------ opacity pruning
+def test_prune_matches_boolean_indexing():
+    rng = np.random.default_rng(5)
+    P = rng.standard_normal((15, 1000, 4)).astype(np.float32)
+    M = rng.standard_normal((15, 1000, 4)).astype(np.float32)
+    V = rng.random((15, 1000, 4)).astype(np.float32)
+    P[0, 7, 3] = np.nan  # a NaN logit is not >= any threshold
+    t = np.float32(-0.3)
+    P[0, 11, 3] = t  # exactly on the threshold: kept
+    k, (Po, Mo, Vo) = oracle.prune([P, M, V], float(t))
+    keep = P[0, :, 3] >= t
+    assert keep[11] and not keep[7]
+    assert k == int(keep.sum())
+    for got, src in ((Po, P), (Mo, M), (Vo, V)):
+        assert np.array_equal(got, src[:, keep])
+
+
+def test_prune_closed_forms():
+    P = np.random.default_rng(6).standard_normal((15, 50, 4)).astype(np.float32)
+    k, (Po,) = oracle.prune([P], -np.inf)
+    assert k == 50 and np.array_equal(Po, P)  # nothing below -inf: identity
+    k, (Po,) = oracle.prune([P], np.inf)
+    assert k == 0 and Po.shape == (15, 0, 4)
+    k, _ = oracle.prune([np.zeros((15, 0, 4), np.float32)], 0.0)
+    assert k == 0
