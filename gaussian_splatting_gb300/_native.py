@@ -21,7 +21,8 @@ EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_project_batch", "gs_
            "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
-           "gs_tile_split", "gs_view_order", "gs_probe_ffma", "gs_debug_set_wait_limit",
+           "gs_tile_split", "gs_view_order", "gs_prune_workspace_size", "gs_prune", "gs_probe_ffma",
+           "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
 
@@ -83,6 +84,8 @@ def load() -> C.CDLL:
         "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp], i32),
         "gs_tile_split": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
         "gs_view_order": ([vp, i32, i32, vp, vp, vp], i32),
+        "gs_prune_workspace_size": ([i64], sz),
+        "gs_prune": ([vp, i32, i64, f32, vp, i64, vp, sz, vp, vp, vp], i32),
         "gs_probe_ffma": ([vp, i32, i32, vp], i32),
         "gs_debug_set_wait_limit": ([i64], None),
         "gs_debug_drop_publish": ([i32], None),
@@ -261,6 +264,21 @@ def gs_tile_split(cost_px, width, height, parts, tile_cost, cum, bounds, stream=
 def gs_view_order(weights, batch, unit, order, score, stream=None):
     _check(load().gs_view_order(_ptr(weights), batch, unit, _ptr(order), _ptr(score), _stream(stream)),
            "gs_view_order")
+
+
+def gs_prune_workspace_size(n) -> int:
+    return load().gs_prune_workspace_size(n)
+
+
+def gs_prune(planes_in, n, min_logit, planes_out, out_stride, workspace, n_keep, sync=False, stream=None):
+    """Returns the kept count (host int) when sync=True, else None (it stays in n_keep)."""
+    pin = _ptrs(planes_in)
+    pout = _ptrs(planes_out) if planes_out is not None else (None, None)
+    host = C.c_int64(0)
+    _check(load().gs_prune(pin[0], len(planes_in), n, min_logit, pout[0], out_stride, _ptr(workspace),
+                           workspace.numel() if workspace is not None else 0, _ptr(n_keep),
+                           C.byref(host) if sync else None, _stream(stream)), "gs_prune")
+    return host.value if sync else None
 
 
 def gs_probe_ffma(out, blocks, iters, stream=None):

@@ -182,6 +182,43 @@ class Trainer:
         N.gs_render_fwd(proj, self.n, self.vals[0], self.ranges[0], cam, self.bg, out, self.T_final, self.n_contrib)
         return out
 
+    def prune(self, min_opacity: float) -> int:
+        """Drop the Gaussians whose opacity is below ``min_opacity`` (the pruning half of
+        densification): parameters and Adam moments are compacted in index order by gs_prune,
+        the per-Gaussian scratch is resized, the gradients start from zero.  Synchronises;
+        returns the new count."""
+        if min_opacity <= 0.0:
+            logit = -math.inf
+        elif min_opacity >= 1.0:
+            logit = math.inf
+        else:
+            logit = math.log(min_opacity / (1.0 - min_opacity))
+        dev, n = self.params.device, self.n
+        ws = torch.empty(max(N.gs_prune_workspace_size(n), 256), dtype=torch.uint8, device=dev)
+        nk = torch.zeros(1, dtype=torch.int64, device=dev)
+        sets = [self.params, self.exp_avg, self.exp_avg_sq]
+        k = N.gs_prune(sets, n, logit, None, 0, ws, nk, sync=True)  # the count
+        outs = [torch.empty((15, k, 4), dtype=torch.float32, device=dev) for _ in sets]
+        if k > 0:
+            N.gs_prune(sets, n, logit, outs, k, ws, nk, sync=True)
+        self.params, self.exp_avg, self.exp_avg_sq = outs
+        self._alloc_gaussians(k)
+        return k
+
+    def _alloc_gaussians(self, n: int):
+        """(Re)allocate the per-Gaussian scratch for n Gaussians."""
+        dev, batch = self.params.device, self.batch
+        f32, i32 = torch.float32, torch.int32
+        self.n = n
+        self.grads = torch.zeros_like(self.params)
+        self.proj = torch.zeros((batch, 3, n, 4), dtype=f32, device=dev)
+        self.grad2d = torch.zeros((batch, n, 12), dtype=f32, device=dev)
+        self.vis_ws = torch.empty(max(N.gs_visible_sets_workspace_size(batch, n), 256), dtype=torch.uint8, device=dev)
+        self.indices = torch.zeros(max(batch * n, 1), dtype=i32, device=dev)
+        self.union_idx = torch.zeros(max(n, 1), dtype=i32, device=dev)
+        self.sort_ws = None
+        self._ws_cam = None
+
     # ------------------------------------------------------------------ the step
     def _timed(self, name, fn, *args, **kw):
         if self.timer is None:

@@ -340,6 +340,27 @@ gs_status gs_tile_split(const uint32_t* cost_px, int width, int height, int part
  */
 gs_status gs_view_order(const float* weights, int batch, int unit, int32_t* order, float* score, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * gs_prune -- the pruning half of densification (Grendel-GS notes, 训练流程: "prune
+ * low-opacity Gaussians").  Gaussian i is kept when its opacity logit (plane 0, w of the
+ * first set) is >= min_logit, i.e. opacity >= sigmoid(min_logit) (a NaN logit is dropped),
+ * and its 15 planes of every set move to the next free slot, index order preserved.
+ *   planes_in   host array of n_sets (1..4) device pointers, [15][n][4] each; set 0 is the
+ *               parameters (its logit decides), the others e.g. the Adam moments.
+ *   planes_out  host array of n_sets device pointers, [15][out_stride][4] each, not
+ *               overlapping the inputs; may be NULL when out_stride == 0 (count only).
+ *   workspace   gs_prune_workspace_size(n) bytes, 256-byte aligned.
+ *   n_keep      device int64[1]: the number kept (the true count even above out_stride;
+ *               slots at or beyond out_stride are not written).
+ *   n_keep_host optional host int64: if non-NULL the call synchronises, stores the count and
+ *               returns GS_ERR_CAPACITY if it exceeds a nonzero out_stride.
+ * A usual pass: once with out_stride = 0 to learn the count, then with out_stride = count.
+ */
+size_t gs_prune_workspace_size(int64_t n);
+gs_status gs_prune(const float* const* planes_in, int n_sets, int64_t n, float min_logit,
+                   float* const* planes_out, int64_t out_stride, void* workspace, size_t workspace_bytes,
+                   int64_t* n_keep, int64_t* n_keep_host, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -64,6 +64,9 @@ def test_host_side_argument_errors(lib):
     assert lib.gs_view_order(None, 65, 1, None, None, None) == N.GS_ERR_INVALID
     assert lib.gs_view_order(None, 4, 5, None, None, None) == N.GS_ERR_INVALID
     assert lib.gs_view_order(None, 4, 1, None, None, None) == N.GS_ERR_INVALID
+    # pruning: set count out of range, NULL output with a nonzero stride
+    assert lib.gs_prune(None, 0, 10, C.c_float(0.0), None, 0, None, 0, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_prune(None, 5, 10, C.c_float(0.0), None, 0, None, 0, None, None, None) == N.GS_ERR_INVALID
     # the batched sort: batch < 1, NULL pointer arrays
     assert lib.gs_bin_sort_batch(None, 0, 0, C.byref(cam), 256, 10, None, None, 0, None, 64, None, None) \
         == N.GS_ERR_INVALID

@@ -109,3 +109,71 @@ def test_view_order_random_weights(B, unit, seed):
     o_w, s_w = oracle.view_order(w, unit)
     assert np.array_equal(o_g, o_w)
     assert np.array_equal(s_g.view(np.uint32), s_w.view(np.uint32))
+
+
+# ------------------------------------------------------------------ opacity pruning
+def _random_sets(n, seed):
+    rng = np.random.default_rng(seed)
+    sets = [rng.standard_normal((15, n, 4)).astype(np.float32) for _ in range(3)]
+    if n > 7:
+        sets[0][0, 3, 3] = np.nan          # dropped
+        sets[0][0, 7, 3] = np.float32(-0.5)  # exactly on the threshold below: kept
+    return sets
+
+
+def gpu_prune(sets, min_logit):
+    n = sets[0].shape[1]
+    ins = [torch.from_numpy(s).cuda() for s in sets]
+    ws = torch.empty(max(N.gs_prune_workspace_size(n), 256), dtype=torch.uint8, device="cuda")
+    nk = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    k = N.gs_prune(ins, n, min_logit, None, 0, ws, nk, sync=True)
+    outs = [torch.full((15, max(k, 1), 4), 7.0, dtype=torch.float32, device="cuda") for _ in sets]
+    if k > 0:
+        assert N.gs_prune(ins, n, min_logit, outs, k, ws, nk, sync=True) == k
+    return k, [o.cpu().numpy()[:, :k] for o in outs]
+
+
+@pytest.mark.parametrize("n,seed", [(1, 0), (255, 1), (256, 2), (257, 3), (100_000, 4), (1_000_003, 5)])
+def test_prune_matches_oracle(n, seed):
+    sets = _random_sets(n, seed)
+    t = float(np.float32(-0.5))
+    k, got = gpu_prune(sets, t)
+    kw, want = oracle.prune(sets, t)
+    assert k == kw
+    for g, w in zip(got, want):
+        assert np.array_equal(g.view(np.uint32), w.view(np.uint32))
+
+
+def test_prune_capacity_and_empty():
+    sets = _random_sets(1000, 6)
+    n = 1000
+    ins = [torch.from_numpy(s).cuda() for s in sets]
+    ws = torch.empty(max(N.gs_prune_workspace_size(n), 256), dtype=torch.uint8, device="cuda")
+    nk = torch.zeros(1, dtype=torch.int64, device="cuda")
+    outs = [torch.zeros((15, 10, 4), dtype=torch.float32, device="cuda") for _ in sets]
+    with pytest.raises(N.GSError) as e:
+        N.gs_prune(ins, n, -np.inf, outs, 10, ws, nk, sync=True)
+    keep = ~np.isnan(sets[0][0, :, 3])  # everything but the NaN logit is >= -inf
+    assert e.value.status == N.GS_ERR_CAPACITY and int(nk.item()) == int(keep.sum()) == 999
+    assert np.array_equal(outs[0].cpu().numpy(), sets[0][:, keep][:, :10])  # the slots that fit
+    empty = torch.zeros((15, 0, 4), dtype=torch.float32, device="cuda")
+    assert N.gs_prune([empty], 0, 0.0, None, 0, None, nk, sync=True) == 0
+
+
+def test_trainer_prune_then_step():
+    from gaussian_splatting_gb300.trainer import Trainer
+    P = scenes.make_params(1, n=20_000)
+    P[0, ::3, 3] = -6.0  # a third of the Gaussians at opacity ~0.0025
+    cams = scenes.make_cameras(1)[:2]
+    tr = Trainer(torch.from_numpy(P).cuda(), cams[0].width, cams[0].height, 2)
+    tr.exp_avg.normal_()
+    tr.exp_avg_sq.uniform_()
+    sets = [tr.params.cpu().numpy(), tr.exp_avg.cpu().numpy(), tr.exp_avg_sq.cpu().numpy()]
+    k = tr.prune(0.005)
+    kw, want = oracle.prune(sets, float(np.float32(np.log(0.005 / 0.995))))
+    assert k == kw == tr.n and 0 < k < 20_000
+    for g, w in zip((tr.params, tr.exp_avg, tr.exp_avg_sq), want):
+        assert np.array_equal(g.cpu().numpy().view(np.uint32), w.view(np.uint32))
+    targets = torch.rand((2, 3, cams[0].height, cams[0].width), device="cuda")
+    loss = tr.step(cams, targets)  # the resized trainer runs a whole step
+    assert np.isfinite(loss) and int(tr.counts[:, 1].abs().sum()) == 0
