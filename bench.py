@@ -387,6 +387,39 @@ def main():
                                    "order": order.cpu().tolist()}}
     except Exception as e:  # reported, never fatal to the benchmark line
         schedule = {"error": str(e)[:200]}
+    # opacity pruning of the trained state into scratch outputs (the trainer is left as is):
+    # count pass, then the timed compaction of parameters and both moments
+    try:
+        n = tr.n
+        min_opacity = 0.005
+        min_logit = math.log(min_opacity / (1.0 - min_opacity))
+        ws_p = torch.empty(max(N.gs_prune_workspace_size(n), 256), dtype=torch.uint8, device="cuda")
+        nk = torch.zeros(1, dtype=torch.int64, device="cuda")
+        sets = [tr.params, tr.exp_avg, tr.exp_avg_sq]
+        k = N.gs_prune(sets, n, min_logit, None, 0, ws_p, nk, sync=True)
+        free, _ = torch.cuda.mem_get_info()
+        if 3 * 240 * max(k, 1) > free // 2:
+            raise RuntimeError("not enough free device memory for the pruning outputs")
+        outs = [torch.empty((15, max(k, 1), 4), dtype=torch.float32, device="cuda") for _ in sets]
+        reps = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        N.gs_prune(sets, n, min_logit, outs, max(k, 1), ws_p, nk)
+        a.record()
+        for _ in range(reps):
+            N.gs_prune(sets, n, min_logit, outs, max(k, 1), ws_p, nk)
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / reps * 1e3
+        # algorithmic bytes: every Gaussian's opacity logit read twice (count and scatter
+        # passes, 4 B each) and, per kept Gaussian, 3 x 240 B read and written
+        nbytes = 2 * 4 * n + k * 3 * 240 * 2
+        del outs
+        prune = {"min_opacity": min_opacity, "kept": k, "of": n, "us": round(us, 2),
+                 "achieved_gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+    except Exception as e:
+        prune = {"error": str(e)[:200]}
+    schedule = dict(schedule or {})
+    schedule["prune"] = prune
 
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
