@@ -188,6 +188,22 @@ class OracleSampler:
 
 
 # ---------------------------------------------------------------------- main
+def rank_views(step: int, rank: int, world: int, batch: int, n_views: int) -> list[int]:
+    """The views rank `rank` trains in step `step`: consecutive batches dealt round-robin over
+    the ranks (replicas: every rank its own views, no exchange)."""
+    return [((step * world + rank) * batch + b) % n_views for b in range(batch)]
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over the ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -258,7 +274,7 @@ def main():
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
     def batch_of(step):
-        ids = [((step * world + rank) * cfg.batch + b) % cfg.n_views for b in range(cfg.batch)]
+        ids = rank_views(step, rank, world, cfg.batch, cfg.n_views)
         return ids, [cams[i] for i in ids]
 
     def run_step(step):
@@ -321,10 +337,7 @@ def main():
         per_call.setdefault(name, []).append(a.elapsed_time(b))
     tr.timer = None
     launches = tr.launches * args.steps
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     views = args.steps * cfg.batch * world
     value = views / (total_ms / 1000.0)
 
@@ -483,10 +496,7 @@ def main():
             tr.step(bc, pinned[s])
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([t_e2e], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = max_over_ranks(t_e2e, dist, "cuda")
         del t_setup
         e2e = {"value": views / t_e2e, "unit": UNIT,
                "h2d_bytes_per_step": cfg.batch * 3 * cfg.height * cfg.width * 4,
