@@ -18,6 +18,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# a test may point the wrapper at another build of the oracle (its mutation checks compile
+# deliberately broken copies of oracle.cpp elsewhere and expect the pins to fail on them)
+_OVERRIDE = os.environ.get("GS_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -36,8 +39,11 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        build()
-        L = C.CDLL(_LIB)
+        if _OVERRIDE:
+            L = C.CDLL(_OVERRIDE)
+        else:
+            build()
+            L = C.CDLL(_LIB)
         dp = C.POINTER(C.c_double)
         ip = C.POINTER(C.c_int32)
         up = C.POINTER(C.c_uint32)

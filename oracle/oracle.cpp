@@ -28,11 +28,16 @@
 // ulp-level difference could flip.
 //
 // Parity pins (see tests/test_oracle_*.py): closed form of one isotropic
-// Gaussian, SH against scipy's complex harmonics and by quadrature, brute-force
+// Gaussian; anisotropic, rotated, off-axis Gaussians against scipy's quaternion
+// rotation, a numpy covariance product and a finite-difference Jacobian of the
+// pinhole map; hand-worked closed forms off the axis, for quarter turns and
+// beyond the field-of-view clamp; the view-dependent colour from two opposite
+// cameras; SH against scipy's complex harmonics and by quadrature, brute-force
 // per-pixel compositing, compositing invariants, central finite differences of
-// the whole forward, SSIM identities, Adam closed form at t = 1, set identities,
-// balanced splits of known cost profiles, worked view orders on block-structured
-// weights.
+// the whole forward (also from an oblique camera with a clamped Gaussian), SSIM
+// identities, Adam closed form at t = 1, set identities, balanced splits of known
+// cost profiles, worked view orders on block-structured weights.  A mutation
+// test plants mistakes in copies of this file and checks that the pins fail.
 
 #include <algorithm>
 #include <cmath>
