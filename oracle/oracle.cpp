@@ -245,11 +245,23 @@ Proj project_one(const Gauss& g, const Cam& k) {
   p.v = k.fy * y / z + k.cy;
   p.z = z;
   rect_of(p.u, p.v, p.r, k, p.rect);
-  {  // a floor(u) or floor(v) one step away would give another rectangle?
+  {  // could a floor(u) or floor(v) one step away give another rectangle?  The kernels round
+     // u = fx x / z + cx in fp32; |u_fp32 - u| stays within 1e-6 (|u - cx| (1 + cond_x +
+     // cond_z) + |cx|), cond_i = (sum_j |R_ij mu_j| + |t_i|) / |p_i| being the condition
+     // number of the camera-space coordinate (four times the roundings of the fma chain,
+     // the division, the scaling and the offset), so only a screen position that close to an
+     // integer can be floored differently.
+    double cond[3];
+    for (int i = 0; i < 3; ++i) {
+      const double terms = std::fabs(k.R[i][0] * g.mu[0]) + std::fabs(k.R[i][1] * g.mu[1]) +
+                           std::fabs(k.R[i][2] * g.mu[2]) + std::fabs(k.t[i]);
+      cond[i] = terms / std::max(std::fabs(p.pc[i]), 1e-30);
+    }
     for (int ax = 0; ax < 2; ++ax) {
       double q = ax == 0 ? p.u : p.v;
+      const double c0 = ax == 0 ? k.cx : k.cy;
       double fr = q - std::floor(q);
-      double eps = 1e-5 * std::max(1.0, std::fabs(q));
+      double eps = 1e-6 * (std::fabs(q - c0) * (1.0 + cond[ax] + cond[2]) + std::fabs(c0));
       if (fr < eps || fr > 1.0 - eps) {
         int alt[4];
         double q2 = fr < eps ? q - 0.5 : q + 0.5;
