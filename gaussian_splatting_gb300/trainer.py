@@ -64,7 +64,7 @@ class StepResult:
 class Trainer:
     def __init__(self, params: torch.Tensor, width: int, height: int, batch: int, lr: float = 1e-3,
                  betas=(0.9, 0.999), eps: float = 1e-15, w_l1: float = 0.8, w_ssim: float = 0.2,
-                 bg=(0.0, 0.0, 0.0), capacity: int = 0):
+                 bg=(0.0, 0.0, 0.0), capacity: int = 0, keep_views: bool = False):
         if params.device.type != "cuda" or params.dtype != torch.float32 or params.dim() != 3 or params.shape[0] != 15 \
                 or params.shape[2] != 4:
             raise ValueError("params must be a CUDA float32 tensor of shape [15, N, 4]")
@@ -88,6 +88,10 @@ class Trainer:
         self.T_final = torch.zeros((height, width), dtype=f32, device=dev)
         self.n_contrib = torch.zeros((height, width), dtype=i32, device=dev)
         self.dimg = torch.zeros((3, height, width), dtype=f32, device=dev)
+        # keep_views: every view of a step keeps its own image and image gradient (for
+        # inspection); otherwise the views share one buffer of each
+        self.images = torch.zeros((batch, 3, height, width), dtype=f32, device=dev) if keep_views else None
+        self.dimgs = torch.zeros((batch, 3, height, width), dtype=f32, device=dev) if keep_views else None
         self.ranges = torch.zeros((batch, tiles, 2), dtype=i32, device=dev)  # per view
         self.counts = torch.zeros((batch, 2), dtype=i64, device=dev)
         self.loss = torch.zeros(1, dtype=f32, device=dev)
@@ -252,19 +256,21 @@ class Trainer:
         launches += (B + 15) // 16 * LAUNCHES["project"] + bin_sort_launches(B, self.capacity)
         for b, cam in enumerate(ccams):
             proj, vals, ranges = self.proj[b], self.vals[b], self.ranges[b]
+            image = self.image if self.images is None else self.images[b]
+            dimg = self.dimg if self.dimgs is None else self.dimgs[b]
             work_buf = None
             if self.work is not None:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
-            T("render_fwd", N.gs_render_fwd, proj, n, vals, ranges, cam, self.bg, self.image, self.T_final,
+            T("render_fwd", N.gs_render_fwd, proj, n, vals, ranges, cam, self.bg, image, self.T_final,
               self.n_contrib, work_buf, stream=st)
             if host_targets is not None and ready is None:  # after the first view's compositing
                 ready = self._upload(host_targets, B, step_start)
             if ready is not None:
                 torch.cuda.current_stream().wait_event(ready[b])
-            T("loss", N.gs_loss, self.image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
-              self.dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
+            T("loss", N.gs_loss, image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
+              dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
             T("render_bwd", N.gs_render_bwd, proj, n, vals, ranges, cam, self.bg, self.T_final,
-              self.n_contrib, self.dimg, self.grad2d[b], stream=st)
+              self.n_contrib, dimg, self.grad2d[b], stream=st)
             if not fused:
                 T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads, stream=st)
                 launches += LAUNCHES["project_bwd"]

@@ -240,6 +240,27 @@ def batch_views(cfg: SceneConfig, step: int) -> list[int]:
     return [((step * cfg.batch) + b) % cfg.n_views for b in range(cfg.batch)]
 
 
+def synthetic_targets(batch: int, width: int, height: int, seed: int) -> np.ndarray:
+    """Seeded target images [batch, 3, H, W] float32 in [0.1, 0.9]: per channel, a sum of four
+    plane waves of random direction, wavelength (8 to 200 px) and phase, rescaled.  Stands in
+    for the photographs a training step compares against where rendering a target is too
+    costly for the CPU oracle."""
+    rng = _rng(seed)
+    y, x = np.mgrid[0:height, 0:width].astype(np.float32)
+    out = np.empty((batch, 3, height, width), np.float32)
+    for b in range(batch):
+        for c in range(3):
+            acc = np.zeros((height, width), np.float32)
+            for _ in range(4):
+                th = rng.uniform(0.0, 2 * math.pi)
+                lam = math.exp(rng.uniform(math.log(8.0), math.log(200.0)))
+                ph = rng.uniform(0.0, 2 * math.pi)
+                k = 2 * math.pi / lam
+                acc += np.cos(np.float32(k * math.cos(th)) * x + np.float32(k * math.sin(th)) * y + np.float32(ph))
+            out[b, c] = 0.5 + 0.1 * acc
+    return out
+
+
 def tiny_scene(n: int, seed: int, width: int = 32, height: int = 32, focal: float = 40.0,
                spread: float = 0.6, logscale=(-2.2, -1.6), opacity=(0.1, 1.2)):
     """Few-Gaussian scene for finite-difference and brute-force checks.

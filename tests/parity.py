@@ -5,14 +5,22 @@ Tolerances (stated once, used everywhere):
   * images: |gpu - oracle| <= 1e-5 (fp32 compositing vs a double oracle);
   * gradients and updated parameters: |gpu - oracle| <= 1e-3 |oracle| + floor, floor = 1e-6
     for parameter-sized quantities; for per-pixel image gradients, whose scale is 1/(3HW),
-    the floor is 1e-6 of the largest magnitude;
-  * elements whose discrete decision (a cull, the radius ceiling, the tile rectangle, the
-    1/255 skip, the 0.99 clamp, the 1e-4 termination) lies within a relative margin of 1e-5
-    of its threshold in the oracle are set aside from the exact comparison and counted; the
-    count must stay below 1% of the elements (it is reported: with lists of hundreds of
-    entries per pixel a few 1e-4 of the pixels carry one near-threshold decision).  A
-    flagged pixel is still bounded -- it may differ by at most 4/255, the weight of a few
-    entries whose alpha sits at the 1/255 skip -- and a flagged radius by one pixel.
+    the floor is 1e-6 of the largest magnitude.
+
+Discrete decisions.  An element whose discrete decision (a cull, the radius ceiling, the tile
+rectangle, the 1/255 skip, the 0.99 clamp, the 1e-4 termination) lies within a relative
+margin of MARGIN = 1e-5 of its threshold in the oracle can come out the other way in fp32
+(the kernels' alpha carries a relative rounding error of a few 1e-6: the prescaled conic, the
+quadratic form, ex2.approx).  Such elements are set aside from the exact comparison and
+counted:
+  * Gaussians (projection decisions, one element per Gaussian and view): at most
+    FLAG_FRAC_GAUSSIANS = 1e-4 of them;
+  * pixels: a pixel carries one decision per list entry it evaluates (about 150 on the
+    300K-Gaussian benchmark view), so at the same per-decision margin about 3e-4 of its
+    pixels are flagged; the bar is FLAG_FRAC_PIXELS = 1e-3 of the pixels.
+A flagged pixel is still bounded by what one flipped decision can change (flag_img_bound).
+The backward tests set nothing aside: the image gradient is zeroed on flagged pixels on both
+sides, so a flipped decision there cannot reach any Gaussian's gradient.
 """
 from __future__ import annotations
 
@@ -20,11 +28,28 @@ import numpy as np
 import torch
 
 MARGIN = 1e-5
-FLAG_FRAC = 1e-2
-FLAG_IMG_BOUND = 4.0 / 255.0
+FLAG_FRAC_GAUSSIANS = 1e-4
+FLAG_FRAC_PIXELS = 1e-3
 IMG_ATOL = 1e-5
 RTOL = 1e-3
 ATOL = 1e-6
+
+
+def flag_img_bound(rgb, bg=(0.0, 0.0, 0.0)) -> float:
+    """Largest change one flipped compositing decision can make to a pixel.
+
+    With c = the largest colour magnitude (Gaussian colours and background) every composite
+    C_rest of the entries behind an entry lies in [0, c], so:
+      * the 1/255 skip: including or skipping entry j moves the pixel by
+        T_j alpha_j |c_j - C_rest| <= (1/255)(1 + MARGIN) c;
+      * the 1e-4 termination: stopping before entry j or not moves it by at most
+        T_j |...| <= T_j c, and a flagged stop has T_j (1 - alpha_j) ~ 1e-4 with
+        alpha_j <= 0.99, so T_j <= 1e-2 (1 + MARGIN);
+      * the 0.99 clamp: alpha moves by MARGIN relative: negligible.
+    The bound is the largest of these."""
+    c = max(float(np.abs(np.asarray(rgb)).max(initial=0.0)), float(np.abs(np.asarray(bg)).max(initial=0.0)))
+    # (the entries a late stop lets through add at most T ~ 1e-4 of c more)
+    return (max(1.0 / 255.0, 1e-2) * (1.0 + MARGIN) + 1e-4) * c + IMG_ATOL
 
 
 def dev(a, dtype=None):
@@ -68,7 +93,12 @@ def allclose_grad(gpu, ref, rtol=RTOL, atol=ATOL):
     return bad
 
 
+def grad2d_oracle_layout(g):
+    """gs_render_bwd's [n][12] record as the oracle's n x 9 (du, dv, dA, dB, dC, dop, dr, dg, db)."""
+    return np.stack([g[:, 0], g[:, 1], g[:, 4], g[:, 5], g[:, 6], g[:, 2], g[:, 8], g[:, 9], g[:, 10]], axis=1)
+
+
 def report(name, bad, total):
     frac = bad / max(total, 1)
-    print(f"[parity] {name}: {bad} / {total} outside tolerance ({frac:.2e})")
+    print(f"[parity] {name}: {bad} / {total} ({frac:.2e})")
     return frac

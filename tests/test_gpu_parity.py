@@ -18,8 +18,9 @@ import scenes  # noqa: E402
 from gaussian_splatting_gb300 import _native as N  # noqa: E402
 from gaussian_splatting_gb300.trainer import Trainer  # noqa: E402
 
-from parity import (ATOL, FLAG_FRAC, FLAG_IMG_BOUND, IMG_ATOL, MARGIN, RTOL, allclose_grad, dev, host, oracle_inputs_from_planes,  # noqa: E402
-                    proj_planes_from_oracle, report)
+from parity import (ATOL, FLAG_FRAC_GAUSSIANS, FLAG_FRAC_PIXELS, IMG_ATOL, MARGIN, RTOL, allclose_grad, dev,  # noqa: E402
+                    flag_img_bound, grad2d_oracle_layout, host, oracle_inputs_from_planes, proj_planes_from_oracle,
+                    report)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,7 +72,7 @@ def test_project_parity(cfg, n, view):
     tg = g[2, :, 3].view(np.int32)
     flagged = int((~ok).sum())
     report(f"project cfg{cfg} flagged", flagged, P.shape[1])
-    assert flagged <= max(2, FLAG_FRAC * P.shape[1])
+    assert flagged <= max(2, FLAG_FRAC_GAUSSIANS * P.shape[1])
     assert np.array_equal(rg[ok], pr["radius"][ok])
     assert np.array_equal(tg[ok], pr["tiles"][ok])
     # a flagged decision moves the radius by at most one pixel
@@ -302,11 +303,11 @@ def test_render_fwd_parity(cfg, n, view, bg):
     ok = mg >= MARGIN
     flagged = int((~ok).sum())
     report(f"render_fwd cfg{cfg} flagged pixels", flagged, ok.size)
-    assert flagged <= max(2, FLAG_FRAC * ok.size)
+    assert flagged <= max(2, FLAG_FRAC_PIXELS * ok.size)
     assert np.abs(img - img_o)[:, ok].max() <= IMG_ATOL
-    # a flagged pixel differs by at most the weight of a few skipped (< 1/255) entries
+    # a flagged pixel differs by at most what one flipped decision can change
     if flagged:
-        assert np.abs(img - img_o)[:, ~ok].max() <= FLAG_IMG_BOUND
+        assert np.abs(img - img_o)[:, ~ok].max() <= flag_img_bound(rgb, bg)
     assert np.abs(T - T_o)[ok].max() <= IMG_ATOL
     assert np.array_equal(nc[ok], nc_o[ok])
     # compositing invariants on the CUDA output itself
@@ -333,7 +334,8 @@ def test_render_fwd_ragged_image():
 
 
 # ------------------------------------------------------------------ loss
-@pytest.mark.parametrize("H,W,scale", [(128, 128, 1.0), (37, 53, 0.25), (820, 1236, 0.25), (7, 5, 1.0)])
+@pytest.mark.parametrize("H,W,scale", [(128, 128, 1.0), (37, 53, 0.25), (820, 1236, 0.25), (7, 5, 1.0),
+                                     (1080, 1920, 0.25), (2160, 3840, 1.0 / 16)])
 def test_loss_parity(H, W, scale):
     rng = np.random.default_rng(H * 1000 + W)
     x = rng.uniform(0, 1, size=(3, H, W)).astype(np.float32)
@@ -361,7 +363,11 @@ def test_render_bwd_parity_config0():
     img_o, T_o, nc_o, mg = oracle.render_fwd(uvzo, conic, rgb, vals, ranges, cam.width, cam.height)
     tgt = oracle.render_view(scenes.jitter_means(P, 0.02, 2000), cam)
     _, dimg = oracle.loss(img_o.astype(np.float32), tgt.astype(np.float32))
-    dimg32 = dimg.astype(np.float32)
+    # the image gradient is zeroed on both sides where a compositing decision sits on its
+    # threshold: a decision flipped there then reaches no Gaussian, and nothing is set aside
+    flagged = mg < MARGIN
+    report("render_bwd cfg0 flagged pixels (gradient zeroed)", int(flagged.sum()), flagged.size)
+    dimg32 = (dimg * ~flagged[None]).astype(np.float32)
     g_o = oracle.render_bwd(uvzo, conic, rgb, vals, ranges, cam.width, cam.height, dimg32.astype(np.float64))
     n = P.shape[1]
     grad2d = torch.full((n, 12), 3.0, dtype=torch.float32, device="cuda")  # the call clears it
@@ -370,15 +376,10 @@ def test_render_bwd_parity_config0():
     torch.cuda.synchronize()
     g = host(grad2d)
     # columns: oracle (du, dv, dA, dB, dC, dop, dr, dg, db) vs gs (du, dv, dop, 0, dA, dB, dC, 0, dr, dg, db, 0)
-    gm = np.stack([g[:, 0], g[:, 1], g[:, 4], g[:, 5], g[:, 6], g[:, 2], g[:, 8], g[:, 9], g[:, 10]], axis=1)
+    gm = grad2d_oracle_layout(g)
     assert (g[:, [3, 7, 11]] == 0).all()
-    # set aside Gaussians seen by pixels whose decisions sit on a threshold
-    suspect = np.zeros(n, bool)
-    for py, px in zip(*np.nonzero(mg < MARGIN)):
-        t = (py // 16) * cam.tiles_x + px // 16
-        suspect[vals[ranges[t, 0]:ranges[t, 1]]] = True
-    bad = allclose_grad(gm, g_o)[~suspect]
-    report("render_bwd cfg0", int(bad.sum()), bad.size)
+    bad = allclose_grad(gm, g_o)
+    report("render_bwd cfg0 (every Gaussian)", int(bad.sum()), bad.size)
     assert bad.sum() == 0
 
 
@@ -557,12 +558,18 @@ def test_full_step_parity_config0():
     assert float(res.loss.item()) == pytest.approx(ref["loss"], rel=1e-5)
     grads_before = host(tr.grads).astype(np.float64)
     G = ref["grads"]
+    # set aside only Gaussians whose own projection decision (cull, radius ceiling, tile
+    # rectangle) sits within the margin of its threshold; every other entry must agree
     pr = oracle.project(P, cam)
     ok = pr["margin"] >= MARGIN
+    report("step cfg0: Gaussians set aside", int((~ok).sum()), ok.size)
+    assert (~ok).sum() <= max(2, FLAG_FRAC_GAUSSIANS * ok.size)
     bad = allclose_grad(grads_before, G)[:, ok]
+    bad[1, :, 3] = False  # padding lane
     report("step grads cfg0", int(bad.sum()), bad.size)
-    assert bad.sum() <= 1e-4 * bad.size
-    # the update: compare where the oracle gradient is clear of the floor
+    assert bad.sum() == 0
+    # the update: at t = 1 each entry moves by lr' sign(g) (reading h3), so entries whose
+    # oracle gradient lies within the 1e-6 floor of zero are not compared
     tr.grads.zero_()
     loss = tr.step([cam], dev(tgt[None]))
     assert loss == pytest.approx(ref["loss"], rel=1e-5)
@@ -570,7 +577,7 @@ def test_full_step_parity_config0():
     clear = (np.abs(G) > 1e-6) & ok[None, :, None]
     bad = allclose_grad(Pn - P, ref["params"] - P, RTOL, 1e-6)[clear]
     report("step params cfg0", int(bad.sum()), bad.size)
-    assert bad.sum() <= 1e-4 * bad.size
+    assert bad.sum() == 0
 
 
 def test_step_with_host_targets_matches_device_targets():
@@ -589,7 +596,14 @@ def test_step_with_host_targets_matches_device_targets():
         torch.cuda.synchronize()
         results.append((loss, host(tr.params).astype(np.float64)))
     assert results[0][0] == results[1][0]
+    # the gradient of the same batch: entries within the 1e-6 floor of zero can change sign
+    # with the order of the backward's atomics, and at t = 1 Adam moves them by lr' sign(g)
+    tr = Trainer(dev(P), cams[0].width, cams[0].height, 4)
+    tr.step_async(cams, dev(tgt), adam=False)
+    torch.cuda.synchronize()
+    g = host(tr.grads)
     d0, d1 = results[0][1] - P, results[1][1] - P
-    bad = np.abs(d1 - d0) > RTOL * np.abs(d0) + 1e-7
-    report("host-target step params", int(bad.sum()), bad.size)
-    assert bad.sum() <= 1e-4 * bad.size
+    clear = np.abs(g) > 1e-6
+    bad = (np.abs(d1 - d0) > RTOL * np.abs(d0) + 1e-7) & clear
+    report("host-target step params", int(bad.sum()), int(clear.sum()))
+    assert bad.sum() == 0
