@@ -1006,22 +1006,28 @@ __global__ void k_publish_ranges(const __grid_constant__ ViewBuffers B) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < B.words2T[v]; i += stride) dst[i] = src[i];
 }
 
-// Resident CTAs per SM of a sort kernel for a given dynamic shared-memory size (cached).
+// Resident CTAs per SM of a sort kernel for a given dynamic shared-memory size on the current
+// device.  The shared-memory attribute is set on every call (it belongs to the device and is
+// lost if the device resets); the occupancy answer is cached per device and size.
 template <bool kTileSort>
 int radix_blocks_per_sm(size_t smem) {
+  constexpr int kMaxDev = 64;
   static std::mutex mu;
-  static size_t cached_smem = 0;
-  static int cached = -1;
+  static size_t cached_smem[kMaxDev] = {0};
+  static int cached[kMaxDev] = {0};
+  const void* fn = kTileSort ? (const void*)k_tile_sort : (const void*)k_depth_sort;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
   std::lock_guard<std::mutex> lock(mu);
-  if (cached < 0 || cached_smem != smem) {
-    const void* fn = kTileSort ? (const void*)k_tile_sort : (const void*)k_depth_sort;
-    int b = 0;
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kSortThreads, smem) != cudaSuccess || b < 1) b = 1;
-    cached = b;
-    cached_smem = smem;
+  if (dev >= 0 && cached[dev] > 0 && cached_smem[dev] == smem) return cached[dev];
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kSortThreads, smem) != cudaSuccess || b < 1) b = 1;
+  if (dev >= 0) {
+    cached[dev] = b;
+    cached_smem[dev] = smem;
   }
-  return cached;
+  return b;
 }
 
 // Cooperative launches: every CTA of the grid is resident at once, which the grid barriers need.

@@ -9,7 +9,6 @@
 // per-CTA partial sums of SSIM and |x - y| goes to global scratch; a last one-CTA kernel
 // reduces them in a fixed order.
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -335,7 +334,8 @@ extern "C" gs_status gs_loss(const float* image, const float* target, int width,
   const size_t need = gs_loss_workspace_size(width, height);
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_loss: workspace %zu bytes < %zu needed", workspace_bytes, need);
-  static const cudaError_t attr =
+  // set on every call: the attribute belongs to the current device (and is lost if it resets)
+  const cudaError_t attr =
       cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss: %s", cudaGetErrorString(attr));
   cudaStream_t st = gs::as_stream(stream);
@@ -368,29 +368,25 @@ extern "C" gs_status gs_loss(const float* image, const float* target, int width,
 namespace {
 
 constexpr int64_t kNoAllocMaxBlocks = 65536;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_loss_scratch[2 * kNoAllocMaxBlocks];
 
-std::mutex g_scratch_mu;
-float* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_loss_scratch on the current device, looked up once per device (host
-// code cannot use the symbol itself: in host code it names a host-side stand-in).
+// Device address of g_loss_scratch on the current device.  Host code cannot use the symbol
+// itself (in host code it names a host-side stand-in), so the address is asked for with the
+// device current.  It is asked for on every call -- a host-side lookup that allocates nothing
+// -- rather than cached: a cached address would outlive a cudaDeviceReset, after which the
+// library's device image is loaded again at another address.  The first call on a device
+// also loads the library's device code there, so that first call should come before any
+// stream capture.
 gs_status scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return gs::set_error(GS_ERR_INVALID, "gs_loss_noalloc: device %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_loss_scratch);
-    if (e != cudaSuccess || !p)
-      return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = reinterpret_cast<float*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_loss_scratch);
+  if (e != cudaSuccess || !p)
+    return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+  *out = reinterpret_cast<float*>(p);
   return GS_OK;
 }
 
@@ -410,7 +406,7 @@ extern "C" gs_status gs_loss_noalloc(const float* image, const float* target, in
                          width, height, (long long)nblk, (long long)kNoAllocMaxBlocks, (long long)kNoAllocMaxBlocks);
   float* partials = nullptr;
   if (gs_status s = scratch_address(&partials)) return s;
-  static const cudaError_t attr =
+  const cudaError_t attr =
       cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: %s", cudaGetErrorString(attr));
   cudaStream_t st = gs::as_stream(stream);

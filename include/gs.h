@@ -189,8 +189,10 @@ gs_status gs_loss(const float* image, const float* target, int width, int height
  * process exits), so the call allocates nothing.  Same arguments and results as gs_loss.
  *  - Limit: ceil(width/32) * ceil(height/32) * 3 <= 65536 (e.g. up to 4096 x 4096);
  *    larger images return GS_ERR_INVALID with the limit in the message.
- *  - The first call on a device looks up the array's device address once (a host-side
- *    runtime query); make that first call before any stream capture.
+ *  - Every call looks up the array's device address on the current device (a host-side
+ *    runtime query that allocates nothing; not cached, so a device reset cannot leave a
+ *    stale address).  The first call on a device also loads the library's device code
+ *    there: make that first call before any stream capture.
  *  - Every call shares the one array: calls that overlap on the GPU (on different
  *    streams with no ordering between them) race and give wrong results.  Each call
  *    rewrites the parts it reads, so nothing needs clearing between calls.
