@@ -1,9 +1,11 @@
 """Benchmark: train views/s of the 3D Gaussian Splatting training step (fwd + bwd + Adam).
 
-Workload (default): the 300K-Gaussian object scene at 1236x820, batch 4, 64 views on a
-ring, all fp32, seeded synthetic data (scene generator in scenes/).  One step = one batch
-of 4 views: per view projection, binning + radix sort, compositing, L1 + D-SSIM loss,
-compositing backward, projection backward; then visible sets and the visible-only Adam
+Workload (default, ``--config 4``): the largest single-GPU scene, 40M Gaussians in a city
+layout of 1024 box clusters, 3840x2160 views, batch 16, 64 views on an orbit, all fp32,
+seeded synthetic data (scene generator in scenes/).  ``--config 1`` is the 300K-Gaussian
+object scene at 1236x820, batch 4.  One step = one batch of views: projection, binning +
+radix sort of every view, then per view compositing, L1 + D-SSIM loss and compositing
+backward; then the visible sets and the projection backward with the visible-only Adam
 update.  throughput = steps * batch / time.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
@@ -42,24 +44,34 @@ UNIT = "views/s"
 FWD_FLOPS_PER_PAIR = 15
 BWD_FLOPS_PER_PAIR = 40
 LOSS_FLOPS_PER_PIXEL = 1320
-# FP32 peak derived from unit counts: 152 SMs x 128 FP32 lanes x 2 flops x 2.07 GHz
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# FP32 lanes per SM of this architecture (4 sub-partitions x 32); the peak is derived from the
+# device's SM count and its maximum SM clock (FMA = 2 flops)
+FP32_LANES_PER_SM = 128
 HBM_FALLBACK_GBS = 6800.0
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# the benchmark workload, keyed by entry point, valid only for the kernel source it was measured
-# on: when the source file's hash differs the figure is reported as null.
-NCU_TRAFFIC = {
-    # profiles/render_object-300k-1236x820.md: 38.308 MB read + 0.052 MB written per launch
-    "render_bwd": {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                   "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
-                   "bytes": 38359552},
-}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
+# keyed by entry point and workload, valid only for the kernel source it was measured on: when
+# the source file's hash differs the figure is reported as null.
+NCU_TRAFFIC = {}
 
 
-def measured_traffic(name):
+def fp32_peak_tflops(sm_count: int, sm_max_mhz: float) -> float:
+    return sm_count * FP32_LANES_PER_SM * 2 * sm_max_mhz * 1e6 / 1e12
+
+
+def max_sm_mhz(gpu_index: int) -> float:
+    """Maximum SM clock reported by nvidia-smi (2070 MHz on GB300 if it cannot be read)."""
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20).stdout
+        return float(out.strip().splitlines()[0])
+    except Exception:
+        return 2070.0
+
+
+def measured_traffic(name, workload):
     import hashlib
-    rec = NCU_TRAFFIC.get(name)
+    rec = NCU_TRAFFIC.get((name, workload))
     if not rec or not rec["sha256"] or rec["bytes"] is None:
         return None
     path = os.path.join(ROOT, rec["source"])
@@ -144,47 +156,137 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- oracle timing
-class OracleSampler:
-    """Times the CPU oracle on a bounded sample of the workload: the top rows of view 0 at
-    full width (same camera, smaller image), batch 1, the whole step (project, bin,
-    composite, loss, backward, Adam).  views/s = (fraction of the view) / seconds."""
+def _reach(P, cam):
+    """Screen position and a bound on the reach of every Gaussian's tile rectangle in a view:
+    r = ceil(3 sqrt(lambda_max)) <= 3 sqrt((f/z)^2 (2 + xr^2 + yr^2) s_max^2 + 0.3) + 1, and the
+    rectangle's tile rounding adds at most 17 pixels.  Returns (u, v, reach, in front)."""
+    R = np.asarray(cam.R, np.float64)
+    t = np.asarray(cam.t, np.float64)
+    limx = 1.3 * (cam.width / 2.0) / cam.fx
+    limy = 1.3 * (cam.height / 2.0) / cam.fy
+    out = []
+    for a in range(0, P.shape[1], 4_000_000):  # chunks bound the float64 temporaries
+        pc = P[0, a:a + 4_000_000, :3].astype(np.float64) @ R.T + t
+        z = pc[:, 2]
+        front = z > 0.99 * cam.znear
+        zs = np.where(front, z, 1.0)
+        xr = np.clip(pc[:, 0] / zs, -limx, limx)
+        yr = np.clip(pc[:, 1] / zs, -limy, limy)
+        smax = np.exp(P[1, a:a + 4_000_000, :3].astype(np.float64).max(axis=1))
+        lam = (max(cam.fx, cam.fy) / zs) ** 2 * (2.0 + xr * xr + yr * yr) * smax * smax + 0.3
+        r = 3.0 * np.sqrt(lam) + 18.0
+        u = cam.fx * pc[:, 0] / zs + cam.cx
+        v = cam.fy * pc[:, 1] / zs + cam.cy
+        out.append((u.astype(np.float32), v.astype(np.float32), r.astype(np.float32), front))
+    return tuple(np.concatenate([o[k] for o in out]) for k in range(4))
 
-    def __init__(self, cfg_idx: int):
-        import oracle
 
-        self.oracle = oracle
-        self.cfg = scenes.CONFIGS[cfg_idx]
-        self.P = scenes.make_params(cfg_idx)
-        self.cam = scenes.make_cameras(cfg_idx)[0]
-        self.jit = scenes.jitter_means(self.P, self.cfg.jitter, 2000 + cfg_idx)
-        self.rows = None
-        self.tgt = None
+def _band_reach(info, width, r0, rows):
+    """Indices of every Gaussian whose tile rectangle can meet rows [r0, r0 + rows) (a
+    superset), so a band rendered from them alone equals those rows of the whole view."""
+    u, v, r, front = info
+    hit = front & (u + r >= 0) & (u - r <= width) & (v + r >= r0) & (v - r <= r0 + rows)
+    return np.nonzero(hit)[0]
 
-    def _cam(self, rows):
-        c = self.cam
-        return scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy, c.znear, c.width, rows)
 
-    def _run(self, rows, tgt):
+def _oracle_worker(conn, P, jit, cam, lr, eps):
+    """One host core's share of the CPU baseline: the oracle's whole step (project, bin,
+    composite, loss, backward, Adam) on its band, once per request.  The band's target is
+    the oracle's render of the jittered scene (untimed)."""
+    import oracle
+
+    tgt = oracle.render_view(jit, cam)[None]
+    zeros = np.zeros_like(P)
+    conn.send("ready")
+    while conn.recv() == "go":
         t0 = time.perf_counter()
-        self.oracle.step(self.P, np.zeros_like(self.P), np.zeros_like(self.P), [self._cam(rows)], tgt,
-                         lr=self.cfg.lr, eps=self.cfg.eps)
-        return time.perf_counter() - t0
+        oracle.step(P, zeros, zeros, [cam], tgt, lr=lr, eps=eps)
+        conn.send(time.perf_counter() - t0)
+    conn.close()
+
+
+class OracleSampler:
+    """Times the CPU oracle, as it stands, on the host cores: one spawned process per core,
+    each running the oracle's whole step (batch 1) on its own band of `rows` image rows at full
+    width (consecutive bands of view 0, then of the next views), on the Gaussians that can
+    reach the band.  One round = every process takes one step; throughput = (bands x rows /
+    height) views / wall time of the round."""
+
+    def __init__(self, cfg_idx: int, P=None, cams=None, workers: int | None = None):
+        self.cfg = scenes.CONFIGS[cfg_idx]
+        self.P = scenes.make_params(cfg_idx) if P is None else P
+        self.cams = scenes.make_cameras(cfg_idx) if cams is None else cams
+        self.jit = scenes.jitter_means(self.P, self.cfg.jitter, 2000 + cfg_idx)
+        self.workers = workers or max(1, len(os.sched_getaffinity(0)))
+        self.rows = None
+        self.procs = []
+        self._info = {}
+
+    def _band(self, k):
+        H = self.cfg.height
+        per_view = max(1, H // self.rows)
+        view = (k // per_view) % len(self.cams)
+        r0 = (k % per_view) * self.rows
+        rows = min(self.rows, H - r0)
+        c = self.cams[view]
+        cam = scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy - r0, c.znear, c.width, rows)
+        if view not in self._info:
+            self._info[view] = _reach(self.P, c)
+        idx = _band_reach(self._info[view], c.width, r0, rows)
+        return self.P[:, idx], self.jit[:, idx], cam, rows
 
     def calibrate(self, budget_s: float):
-        tgt = self.oracle.render_view(self.jit, self._cam(32))[None]
-        t_small = self._run(32, tgt)
-        rows = int(min(self.cfg.height, 32 * budget_s / max(t_small, 1e-3)))
-        self.rows = max(16, (rows // 16) * 16)
-        self.tgt = self.oracle.render_view(self.jit, self._cam(self.rows))[None]
+        """Band height (a multiple of 16) whose step takes about budget_s on one core."""
+        import oracle
+
+        self.rows = 16
+        P, jit, cam, rows = self._band(0)
+        tgt = oracle.render_view(jit, cam)[None]
+        t0 = time.perf_counter()
+        oracle.step(P, np.zeros_like(P), np.zeros_like(P), [cam], tgt, lr=self.cfg.lr, eps=self.cfg.eps)
+        t16 = max(time.perf_counter() - t0, 1e-3)
+        self.rows = int(max(16, min(self.cfg.height, 16 * math.floor(budget_s / t16))))
+        self.rows = max(16, self.rows // 16 * 16)
         return self.rows
 
-    def step(self):
-        t = self._run(self.rows, self.tgt)
-        return (self.rows / self.cfg.height) / t, t
+    def start(self):
+        import multiprocessing as mp
 
-    def describe(self, t):
-        return (f"rows 0..{self.rows} of view 0 at full width ({t:.1f} s per sample, batch 1): project+bin+"
-                "composite+loss+backward+Adam, single thread, double precision")
+        ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+        for k in range(self.workers):
+            P, jit, cam, rows = self._band(k)
+            a, b = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(b, P, jit, cam, self.cfg.lr, self.cfg.eps), daemon=True)
+            pr.start()
+            self.procs.append((pr, a, rows))
+        for _, a, _ in self.procs:
+            assert a.recv() == "ready"
+
+    def round(self):
+        """One timed round: (views/s, wall seconds, views)."""
+        t0 = time.perf_counter()
+        for _, a, _ in self.procs:
+            a.send("go")
+        for _, a, _ in self.procs:
+            a.recv()
+        wall = time.perf_counter() - t0
+        views = sum(rows for _, _, rows in self.procs) / self.cfg.height
+        return views / wall, wall, views
+
+    def stop(self):
+        for pr, a, _ in self.procs:
+            try:
+                a.send("stop")
+            except Exception:
+                pass
+            pr.join(timeout=30)
+        self.procs = []
+
+    def describe(self, wall):
+        return (f"{self.workers} processes (one per host core), each the oracle's whole step (project, bin, "
+                f"composite, loss, backward, Adam; batch 1, double precision) on its own band of {self.rows} rows "
+                f"at full width (bands of view 0, then the next views) with the Gaussians that can reach it; "
+                f"{wall:.1f} s per round")
 
 
 # ---------------------------------------------------------------------- main
@@ -210,7 +312,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gs", choices=["gs", "reference"])
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -225,22 +327,27 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        ncores = 1
-        per_step = []
+        # each step is one round of the oracle on every host core (a bounded sample of the
+        # workload: one band of rows per core); the rounds are sized so that the whole run
+        # takes about two minutes
         smp = OracleSampler(args.config)
         smp.calibrate(max(1.0, 120.0 / max(1, args.steps + args.warmup)))
-        t = 0.0
+        smp.start()
+        per_step, walls, views = [], [], 0.0
         for i in range(args.warmup + args.steps):
-            v, t = smp.step()
+            v, wall, views = smp.round()
             if i >= args.warmup:
                 per_step.append(v)
-        value = statistics.median(per_step)
-        sample = "each step: " + smp.describe(t)
+                walls.append(wall)
+        smp.stop()
+        value = views * len(walls) / sum(walls)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": 1000.0 * cfg.batch / value, "higher_is_better": True,
+                "warmup": args.warmup, "ms_per_step": 1000.0 * sum(walls) / len(walls), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {**workload, "l2": "n/a (CPU)"}, "impl": "reference",
-                "cpu_baseline": {"value": value, "unit": UNIT, "cores": ncores, "kind": "oracle", "sample": sample},
+                "sample_views_per_step": views,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.workers, "kind": "oracle",
+                                 "sample": "each step: " + smp.describe(statistics.median(walls))},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
@@ -341,11 +448,13 @@ def main():
     views = args.steps * cfg.batch * world
     value = views / (total_ms / 1000.0)
 
-    # ---------------- work counts of the timed batches (untimed re-run of the same views on the
-    # same trainer, gradients only: the parameters do not move; the gradients are cleared)
+    # ---------------- work counts over exactly one orbit (every view once, the batches the timed
+    # steps cycle through), untimed, gradients only: the parameters do not move and the
+    # gradients are cleared.  The timed steps weight the views (almost) evenly too.
     tr.work = []
-    for s in range(min(args.steps, 20)):  # twenty batches give the averages
-        ids, bc = batch_of(args.warmup + s)
+    orbit = (cfg.n_views + cfg.batch * world - 1) // (cfg.batch * world)
+    for s in range(orbit):
+        ids, bc = batch_of(s)
         tr.step_async(bc, targets[torch.tensor(ids, device="cuda")], adam=False)
         tr.grads.zero_()
     work = tr.work
@@ -434,6 +543,17 @@ def main():
     schedule = dict(schedule or {})
     schedule["prune"] = prune
 
+    # projected footprints of one view (the GPU's radii): the fraction below 2 % of the image
+    # width, the property the large workloads are drawn to have
+    rad = tr.proj[0][1, :, 3].contiguous().view(torch.int32)
+    vis_r = rad[rad > 0].float()
+    footprint = {"view": batch_of(0)[0][0], "visible": int(vis_r.numel()),
+                 "frac_radius_below_2pct_width": round(float((vis_r < 0.02 * cfg.width).float().mean()), 5)
+                 if vis_r.numel() else None,
+                 "radius_p90_px": float(torch.quantile(vis_r[:1 << 24], 0.9)) if vis_r.numel() else None}
+    sm_count = torch.cuda.get_device_properties(local).multi_processor_count
+    FP32_PEAK_TFLOPS = fp32_peak_tflops(sm_count, max_sm_mhz(local))
+    fp32_src = f"derived: {sm_count} SM x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x the maximum SM clock"
     avg = {k: sum(v) / len(v) for k, v in per_call.items()}
     share = {k: sum(v) / total_ms for k, v in per_call.items()}
     peak_hbm, hbm_src = hbm_peak()
@@ -450,14 +570,14 @@ def main():
     if dominant in flops:
         ach = flops[dominant] / (avg[dominant] / 1e3) / 1e12
         roof = {"kernel": "k_" + dominant, "bound": "alu", "achieved": ach, "peak": FP32_PEAK_TFLOPS,
-                "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": measured_traffic(dominant),
-                "peak_source": "derived: 152 SM x 128 FP32 lanes x 2 flop x 2.07 GHz",
+                "unit": "TFLOP/s", "frac": ach / FP32_PEAK_TFLOPS, "traffic": measured_traffic(dominant, cfg.name),
+                "peak_source": fp32_src,
                 "measured_peak": fp32_meas, "frac_of_measured": ach / fp32_meas if fp32_meas else None,
                 "measured_peak_source": "gs_probe_ffma in this run: 8 FFMA chains per thread, full occupancy",
                 "work": work_note}
     else:
         roof = {"kernel": "k_" + dominant, "bound": "hbm", "achieved": None, "peak": peak_hbm, "unit": "GB/s",
-                "frac": None, "traffic": measured_traffic(dominant), "peak_source": hbm_src}
+                "frac": None, "traffic": measured_traffic(dominant, cfg.name), "peak_source": hbm_src}
     others = {}
     for k in ("render_fwd", "render_bwd", "loss"):
         if k in flops and k in avg:
@@ -509,10 +629,13 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        smp = OracleSampler(args.config)
-        smp.calibrate(12.0)
-        v, t = smp.step()
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": smp.describe(t)}
+        smp = OracleSampler(args.config, P=P, cams=cams)
+        smp.calibrate(10.0)
+        smp.start()
+        v, wall, views = smp.round()
+        smp.stop()
+        cpu = {"value": v, "unit": UNIT, "cores": smp.workers, "kind": "oracle",
+               "sample": f"one round ({views:.3f} views): " + smp.describe(wall)}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -525,6 +648,7 @@ def main():
                             "calls": "project, bin_sort, visible_sets and project_bwd_adam once per batch, the rest once per view",
                             "share": {k: round(v, 4) for k, v in share.items()}, **others},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "schedule": schedule,
+                "footprint": footprint, "work_counts": f"one orbit: {orbit} batches, every view once",
                 "clocks": clk.summary(), "instances_per_view": int(st[:, 0].float().mean().item())}
         print(json.dumps(line), flush=True)
     if dist:
