@@ -51,7 +51,7 @@ def lib():
         i64p = C.POINTER(C.c_int64)
         fp = C.POINTER(C.c_float)
         i64, i32, dbl = C.c_int64, C.c_int, C.c_double
-        L.oracle_project.argtypes = [dp, i64, dp, i32, i32, dp, dp, ip, dp, ip, ip, dp, dp]
+        L.oracle_project.argtypes = [dp, i64, dp, i32, i32, dp, dp, ip, dp, ip, ip, dp, dp, dp]
         L.oracle_project.restype = None
         L.oracle_bin_sort.argtypes = [dp, ip, i64, i32, i32, u64p, up, i64, up]
         L.oracle_bin_sort.restype = i64
@@ -96,17 +96,21 @@ def cam_array(cam) -> np.ndarray:
 
 
 def project(params, cam):
-    """Projection of every Gaussian.  Returns a dict of arrays (double / int32)."""
+    """Projection of every Gaussian.  Returns a dict of arrays (double / int32).  ``margin``:
+    relative distance of the nearest decision that can change an output from its threshold
+    (culls; the tile rectangle where it would add or drop a tile the Gaussian reaches);
+    ``rmargin``: that of the radius ceiling, 0 where the tile rectangle's value may differ
+    (the integer outputs radius and tiles)."""
     P = _d(params)
     N = P.shape[1]
     out = dict(uvzo=np.zeros((N, 4)), conic=np.zeros((N, 3)), radius=np.zeros(N, np.int32),
                rgb=np.zeros((N, 3)), rect=np.zeros((N, 4), np.int32), tiles=np.zeros(N, np.int32),
-               raw=np.zeros((N, 3)), margin=np.zeros(N))
+               raw=np.zeros((N, 3)), margin=np.zeros(N), rmargin=np.zeros(N))
     ca = cam_array(cam)
     lib().oracle_project(_p(P, C.c_double), N, _p(ca, C.c_double), cam.width, cam.height,
                          _p(out["uvzo"], C.c_double), _p(out["conic"], C.c_double), _p(out["radius"], C.c_int32),
                          _p(out["rgb"], C.c_double), _p(out["rect"], C.c_int32), _p(out["tiles"], C.c_int32),
-                         _p(out["raw"], C.c_double), _p(out["margin"], C.c_double))
+                         _p(out["raw"], C.c_double), _p(out["margin"], C.c_double), _p(out["rmargin"], C.c_double))
     return out
 
 

@@ -160,7 +160,8 @@ struct Proj {
   int rect[4] = {0, 0, 0, 0};
   int tiles = 0;
   double dir[3], dlen, d[3], Y[16], dY[16][3], raw[3], rgb[3] = {0, 0, 0};
-  double margin = 1e30;
+  double margin = 1e30;   // nearest decision that can change an output (see project_one)
+  double rmargin = 1e30;  // the integer radius and tile rectangle values (0: either may differ)
 };
 
 void rect_of(double u, double v, int r, const Cam& k, int rect[4]) {
@@ -174,6 +175,36 @@ void rect_of(double u, double v, int r, const Cam& k, int rect[4]) {
   rect[1] = (int)std::min<int64_t>(std::max<int64_t>(y0, 0), k.Ty);
   rect[2] = (int)std::min<int64_t>(std::max<int64_t>(x1, 0), k.Tx);
   rect[3] = (int)std::min<int64_t>(std::max<int64_t>(y1, 0), k.Ty);
+}
+
+// Relative margin below which a discrete decision counts as undecided (the parity tests'
+// threshold; the kernels' fp32 operands carry relative errors of a few 1e-6).
+constexpr double kDecisionMargin = 1e-5;
+
+// Would the tile rectangle `alt` instead of `rect` change any output?  Only through the tiles
+// in one and not the other, and there only at a pixel where the Gaussian passes the
+// compositing skip tests (power <= 0, alpha >= 1/255), both taken with the decision margin so
+// that a pixel on the edge of the skip counts.  The Gaussian's conic, opacity and screen
+// position must be set in p.
+bool reaches(const Proj& p, const Gauss& g, const Cam& k, const int rect[4], const int alt[4]) {
+  (void)g;
+  if (std::memcmp(rect, alt, 4 * sizeof(int)) == 0) return false;
+  const int x0 = std::min(rect[0], alt[0]), x1 = std::max(rect[2], alt[2]);
+  const int y0 = std::min(rect[1], alt[1]), y1 = std::max(rect[3], alt[3]);
+  auto in = [](const int r[4], int tx, int ty) { return tx >= r[0] && tx < r[2] && ty >= r[1] && ty < r[3]; };
+  const double a_min = (double)(1.0f / 255.0f) * (1.0 - kDecisionMargin);
+  for (int ty = y0; ty < y1; ++ty)
+    for (int tx = x0; tx < x1; ++tx) {
+      if (in(rect, tx, ty) == in(alt, tx, ty)) continue;
+      for (int py = ty * TILE; py < std::min(ty * TILE + TILE, k.H); ++py)
+        for (int px = tx * TILE; px < std::min(tx * TILE + TILE, k.W); ++px) {
+          const double dx = (px + 0.5) - p.u, dy = (py + 0.5) - p.v;
+          const double power = -0.5 * (p.conic[0] * dx * dx + p.conic[2] * dy * dy) - p.conic[1] * dx * dy;
+          if (power > kDecisionMargin) continue;
+          if (std::min(0.99, p.o * std::exp(power)) >= a_min) return true;
+        }
+    }
+  return false;
 }
 
 Proj project_one(const Gauss& g, const Cam& k) {
@@ -236,15 +267,21 @@ Proj project_one(const Gauss& g, const Cam& k) {
   const double mid = 0.5 * (p.a + p.c);
   const double lam = mid + std::sqrt(std::max(mid * mid - p.det, 0.0));
   const double r3 = 3.0 * std::sqrt(lam);
-  {
-    double fr = r3 - std::floor(r3);
-    p.margin = std::min(p.margin, std::min(fr, 1.0 - fr) / r3);
-  }
+  const double rfr = r3 - std::floor(r3);
+  p.rmargin = std::min(rfr, 1.0 - rfr) / r3;
   p.r = (int)std::ceil(f32(r3));
   p.u = k.fx * x / z + k.cx;
   p.v = k.fy * y / z + k.cy;
   p.z = z;
   rect_of(p.u, p.v, p.r, k, p.rect);
+  // The radius reaches the rest of the step only through the tile rectangle: a ceiling within
+  // the margin counts as a decision if the neighbouring radius gives a rectangle that adds or
+  // drops a tile where the Gaussian has a pixel with alpha >= 1/255 (see reaches()).
+  if (p.rmargin < kDecisionMargin) {
+    int alt[4];
+    rect_of(p.u, p.v, rfr < 0.5 ? p.r - 1 : p.r + 1, k, alt);
+    if (reaches(p, g, k, p.rect, alt)) p.margin = std::min(p.margin, p.rmargin);
+  }
   {  // could a floor(u) or floor(v) one step away give another rectangle?  The kernels round
      // u = fx x / z + cx in fp32; |u_fp32 - u| stays within 1e-6 (|u - cx| (1 + cond_x +
      // cond_z) + |cx|), cond_i = (sum_j |R_ij mu_j| + |t_i|) / |p_i| being the condition
@@ -266,7 +303,8 @@ Proj project_one(const Gauss& g, const Cam& k) {
         int alt[4];
         double q2 = fr < eps ? q - 0.5 : q + 0.5;
         rect_of(ax == 0 ? q2 : p.u, ax == 0 ? p.v : q2, p.r, k, alt);
-        if (std::memcmp(alt, p.rect, sizeof(alt)) != 0) p.margin = 0.0;
+        if (std::memcmp(alt, p.rect, sizeof(alt)) != 0) p.rmargin = 0.0;
+        if (reaches(p, g, k, p.rect, alt)) p.margin = 0.0;
       }
     }
   }
@@ -798,10 +836,14 @@ extern "C" {
 // Projection of N Gaussians.  params: [15][N][4] doubles.  cam: 17 doubles
 // (R row-major, t, fx, fy, cx, cy, znear).  Outputs (any may be null except
 // uvzo / conic / radius / rgb): uvzo N x 4, conic N x 3, radius N, rgb N x 3,
-// rect N x 4, tiles N, raw N x 3 (colour before the clamp), margin N.
+// rect N x 4, tiles N, raw N x 3 (colour before the clamp), margin N (relative margin of the
+// nearest decision that can change an output: culls, and the tile rectangle -- through the
+// screen position or the radius -- where it adds or drops a tile the Gaussian reaches),
+// rmargin N (relative margin of the radius ceiling; 0 where a floor of the screen position
+// within its rounding bound would give another rectangle: the values that may differ).
 void oracle_project(const double* params, int64_t N, const double* cam, int W, int H, double* uvzo,
                     double* conic, int32_t* radius, double* rgb, int32_t* rect, int32_t* tiles, double* raw,
-                    double* margin) {
+                    double* margin, double* rmargin) {
   const Cam k = load_cam(cam, W, H);
   for (int64_t i = 0; i < N; ++i) {
     const Proj p = project_one(load_gauss(params, N, i), k);
@@ -817,6 +859,7 @@ void oracle_project(const double* params, int64_t N, const double* cam, int W, i
     if (raw)
       for (int l = 0; l < 3; ++l) raw[3 * i + l] = v ? p.raw[l] : 0;
     if (margin) margin[i] = p.margin;
+    if (rmargin) rmargin[i] = v ? p.rmargin : 1e30;
   }
 }
 

@@ -13,8 +13,14 @@ margin of MARGIN = 1e-5 of its threshold in the oracle can come out the other wa
 (the kernels' alpha carries a relative rounding error of a few 1e-6: the prescaled conic, the
 quadratic form, ex2.approx).  Such elements are set aside from the exact comparison and
 counted:
-  * Gaussians (projection decisions, one element per Gaussian and view): at most
-    FLAG_FRAC_GAUSSIANS = 1e-4 of them;
+  * Gaussians whose projection decision can change an output (a cull; a tile rectangle that
+    would add or drop a tile the Gaussian reaches with alpha >= 1/255): at most
+    FLAG_FRAC_GAUSSIANS = 1e-4 of them per view;
+  * Gaussians whose integer radius or tile rectangle value may differ without changing any
+    image or gradient (a radius ceiling within the margin: about 2 MARGIN r3 of them, 6e-4
+    at the benchmark's median r3 of 31 px and about 2e-3 where radii reach 100 px; a floor
+    of the screen position within its rounding bound): at most FLAG_FRAC_VALUES = 3e-3 of
+    them, each radius still within one pixel;
   * pixels: a pixel carries one decision per list entry it evaluates (about 150 on the
     300K-Gaussian benchmark view), so at the same per-decision margin about 3e-4 of its
     pixels are flagged; the bar is FLAG_FRAC_PIXELS = 1e-3 of the pixels.
@@ -29,6 +35,7 @@ import torch
 
 MARGIN = 1e-5
 FLAG_FRAC_GAUSSIANS = 1e-4
+FLAG_FRAC_VALUES = 3e-3
 FLAG_FRAC_PIXELS = 1e-3
 IMG_ATOL = 1e-5
 RTOL = 1e-3

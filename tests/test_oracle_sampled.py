@@ -34,7 +34,7 @@ def test_sampled_step_equals_whole_step(layout_cfg, seed):
         g2d_whole.append(oracle.render_bwd(pr["uvzo"], pr["conic"], pr["rgb"], vals, ranges, W, H, d))
     sample = np.union1d(pick_sample(P, cams[0], 6, seed, rmax=14), pick_sample(P, cams[1], 6, seed + 1, rmax=14))
     assert sample.size >= 8
-    got = sampled_step(P, cams, tg, sample, lr=cfg.lr, eps=cfg.eps)
+    got = sampled_step(P, cams, tg, sample, lr=cfg.lr, eps=cfg.eps, workers=2 if layout_cfg == 2 else 1)
     for b in range(len(cams)):
         ref = g2d_whole[b][sample]
         assert np.allclose(got["g2d"][b], ref, rtol=1e-9, atol=1e-15 * max(1.0, np.abs(ref).max()))
