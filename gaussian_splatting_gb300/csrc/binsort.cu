@@ -12,24 +12,24 @@
 // about a third of the traffic of sorting all 64 key bits of 12-byte pairs.
 //
 // Kernels (all on the caller's stream, no host synchronisation):
-//   k_sort_init   zeroes the status words, the small block, the difference grid and the
+//   k_sort_init   zeroes the status words, the small block, the staged ranges and the
 //                 caller's ranges of every view of a group (one launch instead of memsets).
 //   k_depth_sort  all stable 8-bit passes of the depth sorts of up to 8 views in one
 //                 cooperative launch (a group of CTAs per view, so the views' latency-bound
 //                 phases overlap).  Each pass counts digits per radix tile, scans the counts
-//                 per digit over the tiles, then ranks every tile in shared memory and writes
-//                 digit-contiguous runs; grid barriers (per view) separate the phases.  Phase
-//                 0 makes the depth keys (0xFFFFFFFF for culled Gaussians), their digit totals
-//                 and, per CTA, a difference grid of per-tile instance counts (4 corners per
-//                 visible Gaussian, summed into one grid in the next phase).  After the passes
-//                 the same launch runs the tiles-touched scan over the sorted Gaussians
-//                 (reduce, scan of the chunk sums, then each chunk's records: first slot,
-//                 rectangle, index; and for every radix tile of the tile sort the Gaussian
-//                 holding its first slot) and, on one CTA, the tile counts (2-D prefix sums of
-//                 the grid, their scan = staged ranges, digit bases of the tile passes).
+//                 per digit over the tiles (the column sums are the digit totals), then ranks
+//                 every tile in shared memory and writes digit-contiguous runs at the digit's
+//                 base (an exclusive scan of the totals) plus its column offset; grid
+//                 barriers (per view) separate the phases.  Phase 0 makes the depth keys
+//                 (0xFFFFFFFF for culled Gaussians) and an 8-byte tile-rectangle record per
+//                 Gaussian.  After the passes the same launch runs the tiles-touched scan over
+//                 the sorted Gaussians (reduce, scan of the chunk sums, then each chunk's
+//                 records: first slot, rectangle, index; and for every radix tile of the tile
+//                 sort the Gaussian holding its first slot).
 //   k_tile_sort   the same passes for one view's instances by tile id: the first pass
 //                 generates its (tile, index) pairs from the scan's records instead of reading
-//                 them, the last writes the caller's values (and 64-bit keys if asked for).
+//                 them, the last writes the caller's values (and 64-bit keys if asked for) and
+//                 the sorted tile ids, from whose boundaries a final phase stages the ranges.
 //   k_publish_ranges  copies each view's staged ranges to the caller's array if nothing failed.
 // Every device-side wait is bounded (gs_debug_set_wait_limit); on expiry the kernel sets
 // status bit 2 in count[1] and carries on, so nothing can hang.
@@ -46,6 +46,7 @@ constexpr int kScanChunk = 1024;  // sorted Gaussians per chunk of the tiles-tou
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N is modest)
+constexpr int64_t kWideDepthN = 2000000;  // from this many Gaussians on, 3072 keys per radix tile
 constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
 constexpr int kSlice = kSortThreads * kTileItems;  // instances per generated radix tile
 constexpr int kDepthPasses = 4;
@@ -60,9 +61,8 @@ constexpr uint32_t kCulledKey = 0xFFFFFFFFu;
 
 // layout of the small, memset-cleared block of the workspace (32-bit words)
 constexpr int kSmBarrier = 1;        // one arrival counter per sort (depth, tile)
-constexpr int kSmHist = 32;          // kSlots * 256
-constexpr int kSmDigitBase = kSmHist + kSlots * 256;
-constexpr int kSmWords = kSmDigitBase + kSlots * 256;
+constexpr int kSmHist = 32;          // kSlots * 256 digit totals (the column sums of phase B)
+constexpr int kSmWords = kSmHist + kSlots * 256;
 
 struct Workspace {
   uint32_t* tkey[2];               // instance tile ids, ping-pong
@@ -72,11 +72,10 @@ struct Workspace {
   unsigned long long* chunk_tot;   // per scan chunk: tiles touched, then its first slot
   uint32_t* hist_depth;            // [256][radix tiles of the depth sort]
   uint32_t* hist_tile;             // [256][radix tiles of the tile sort]
-  uint32_t* grid;                  // (Ty + 1) x (Tx + 1) difference grid of per-tile counts
-  uint32_t* grids;                 // one private difference grid per depth-sort CTA
+  uint2* rrec;                     // per Gaussian (index order): (x0 | y0 << 16, w | h << 16)
   uint32_t* rstage;                // tile ranges, published to the caller only on success
   uint32_t* slice_first;           // per output slice of kSlice slots: the item holding its first slot
-  uint4* grec;                     // per depth-ordered Gaussian: (slot, x0 | y0 << 16, width, index)
+  uint4* grec;                     // per depth-ordered Gaussian: (slot, x0 | y0 << 16, w | h << 16, index)
   uint32_t* small;
 };
 
@@ -98,8 +97,7 @@ int tile_passes(const gs::Cam& k) { return std::max(1, (tile_bits((int64_t)k.Tx 
 // Workspace layout: `tile_slots` sets of tile-sort buffers (capacity-sized; view v uses set
 // v % tile_slots, the views of one tile-sort launch having sets of their own), then per view
 // the depth-sort buffers and the scan's records.  w (if not NULL) receives `views` entries.
-size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_t grid_words, int64_t n_tiles,
-             int64_t n_grids, int tile_slots) {
+size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_t n_tiles, int tile_slots) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char* p = base ? base + off : nullptr;
@@ -119,8 +117,7 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
     char* di1 = take(sizeof(uint32_t) * (size_t)n);
     char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
     char* lbd = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kDepthItems>(n));
-    char* gr = take(sizeof(uint32_t) * (size_t)grid_words);
-    char* grs = take(sizeof(uint32_t) * (size_t)grid_words * (size_t)n_grids);
+    char* rr = take(sizeof(uint2) * (size_t)n);
     char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
     char* go = take(sizeof(uint32_t) * (size_t)((cap + kSlice - 1) / kSlice));
     char* gr4 = take(sizeof(uint4) * (size_t)n);
@@ -139,8 +136,7 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
       x.didx[1] = reinterpret_cast<uint32_t*>(di1);
       x.chunk_tot = reinterpret_cast<unsigned long long*>(ss);
       x.hist_depth = reinterpret_cast<uint32_t*>(lbd);
-      x.grid = reinterpret_cast<uint32_t*>(gr);
-      x.grids = reinterpret_cast<uint32_t*>(grs);
+      x.rrec = reinterpret_cast<uint2*>(rr);
       x.rstage = reinterpret_cast<uint32_t*>(rs);
       x.slice_first = reinterpret_cast<uint32_t*>(go);
       x.grec = reinterpret_cast<uint4*>(gr4);
@@ -172,6 +168,7 @@ struct SortSmem {
   uint32_t peer[kSortWarps][256];  // all zero between uses
   uint32_t tstart[256];
   uint32_t gbase[256];
+  uint32_t dbase[256];  // the pass's digit bases
   uint32_t wsum[kSortWarps];
   uint32_t full;  // first tile pass, counts: full cycles of 256 digits
   int fail;
@@ -184,7 +181,7 @@ struct SortSmem {
 // the owner's rectangle record gives the tile id.
 struct GenSource {
   const uint32_t* slice_first;  // per radix tile: the Gaussian holding its first slot
-  const uint4* grec;            // per depth-ordered Gaussian: (offset, x0 | y0 << 16, width, index)
+  const uint4* grec;            // per depth-ordered Gaussian: (offset, x0 | y0 << 16, w | h << 16, index)
   int64_t n;
   int Tx;
 };
@@ -207,20 +204,19 @@ struct RadixJob {
   const float4* q0;     // tile sort only: the last pass writes (key << 32 | depth bits of
   uint64_t* keys64;     // Gaussian value) to keys64 and the values to vals_out
   uint32_t* vals_out;
-  // depth sort only: phase 0 makes the keys from the projection and adds every visible
-  // Gaussian's tile rectangle to a per-CTA difference grid, summed into `grid` in phase B0
+  // depth sort only: phase 0 makes the keys and the rectangle records from the projection
   const float* proj;
-  int Tx, Ty, gwords;
-  uint32_t* grids;      // [CTAs of the job][gwords]
-  uint32_t* grid;       // [gwords], zeroed by the host
+  int Tx, Ty;
+  uint2* rrec;          // per Gaussian, index order: (x0 | y0 << 16, w | h << 16); 0 if culled
   // depth sort only, after the last pass: the tiles-touched scan over the depth-sorted
-  // Gaussians and the per-tile counts
+  // Gaussians
   unsigned long long* chunk_tot;  // per scan chunk of kScanChunk sorted Gaussians
-  uint4* grec;          // per sorted Gaussian: (first slot, x0 | y0 << 16, width, index)
+  uint4* grec;          // per sorted Gaussian: (first slot, x0 | y0 << 16, w | h << 16, index)
   uint32_t* slice_first;  // per radix tile of the tile sort: the Gaussian holding its first slot
   int64_t tcap;         // instance capacity
-  uint32_t* rstage;     // staged tile ranges
-  int tpasses;          // tile passes (their digit bases go to the small block)
+  // tile sort only: after the last pass, the staged ranges from the sorted tile ids (zeroed by
+  // the host, published to the caller if nothing failed)
+  uint32_t* rstage;
 };
 
 // The sort jobs of one launch (kernel parameter space: 8 jobs stay under 4 KB).
@@ -335,7 +331,7 @@ __device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J,
     if ((full || li < nvalid) && o != 0u && first + o - 1u < G.n) {
       const uint4 rec = __ldg(&G.grec[first + o - 1u]);
       const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
-      const uint32_t w = max(rec.z, 1u);
+      const uint32_t w = max(rec.z & 0xffffu, 1u);
       uint32_t row = (uint32_t)__fmul_rz((float)j, __fdividef(1.f, (float)w));  // j / w within 1, corrected below
       int rem = (int)j - (int)(row * w);
       if (rem < 0) { --row; rem += (int)w; }
@@ -375,7 +371,7 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
       if (more || e0 + tid == 0) {
         const uint32_t next = it + 1 < G.n ? __ldg(&G.grec[it + 1]).x : (uint32_t)M;
         const uint32_t s_lo = max(off, lo), s_hi = min(next, end);
-        const uint32_t w = max(rec.z, 1u);
+        const uint32_t w = max(rec.z & 0xffffu, 1u);
         if (s_lo < s_hi) {
           const uint32_t x0 = rec.y & 0xffffu, y0 = rec.y >> 16;
           const uint32_t r0 = (s_lo - off) / w, r1 = (s_hi - 1u - off) / w;
@@ -419,21 +415,15 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
 }
 
 // Depth sort, phase 0 (replaces phase A of pass 0): radix tile by radix tile, the depth key of
-// every Gaussian (float bits of z; 0xFFFFFFFF if culled) and its index, the tile's pass-0
-// digit counts, the CTA's digit totals of all four passes (added to the small block once) and
-// the CTA's private difference grid of tile counts (4 corners per visible Gaussian, shared
-// memory atomics), written out for phase B0 to sum.
+// every Gaussian (float bits of z; 0xFFFFFFFF if culled), its index, its tile-rectangle record
+// and the tile's pass-0 digit counts.
 template <int ITEMS>
-__device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid,
-                                             uint32_t* s_tot, int64_t n, int64_t ntiles, uint32_t G,
-                                             uint32_t bid) {
+__device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, int64_t ntiles,
+                                             uint32_t G, uint32_t bid) {
   constexpr int kTile = kSortThreads * ITEMS;
   const int tid = threadIdx.x;
   const float4* q0 = reinterpret_cast<const float4*>(J.proj);
   const float4* q1 = q0 + n;
-  const int gw = J.Tx + 1;
-  for (int i = tid; i < J.gwords; i += kSortThreads) s_grid[i] = 0u;
-  for (int i = tid; i < kDepthPasses * 256; i += kSortThreads) s_tot[i] = 0u;
   for (int64_t tile = bid; tile < ntiles; tile += G) {
     for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
     __syncthreads();
@@ -443,65 +433,33 @@ __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob&
       const int r = __float_as_int(__ldg(&q1[i].w));
       const float4 a = __ldg(&q0[i]);
       uint32_t key = kCulledKey;
+      uint2 rec = make_uint2(0u, 0u);
       if (r > 0) {
         const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
         const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
         const int x0 = min(max((fu - r) >> 4, 0), J.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), J.Tx);
         const int y0 = min(max((fv - r) >> 4, 0), J.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), J.Ty);
         key = __float_as_uint(a.z);
-        if (x0 < x1 && y0 < y1) {  // modular arithmetic: -1 = 0xFFFFFFFF
-          atomicAdd(&s_grid[y0 * gw + x0], 1u);
-          atomicAdd(&s_grid[y0 * gw + x1], 0xFFFFFFFFu);
-          atomicAdd(&s_grid[y1 * gw + x0], 0xFFFFFFFFu);
-          atomicAdd(&s_grid[y1 * gw + x1], 1u);
-        }
+        if (x0 < x1 && y0 < y1)
+          rec = make_uint2((uint32_t)x0 | ((uint32_t)y0 << 16), (uint32_t)(x1 - x0) | ((uint32_t)(y1 - y0) << 16));
       }
       J.key[0][i] = key;
       J.val[0][i] = (uint32_t)i;
+      J.rrec[i] = rec;
       atomicAdd(&S.tstart[key & 255u], 1u);
-#pragma unroll
-      for (int p = 0; p < kDepthPasses; ++p) atomicAdd(&s_tot[p * 256 + ((key >> (8 * p)) & 255u)], 1u);
     }
     __syncthreads();
     J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
     __syncthreads();
   }
-  for (int i = tid; i < kDepthPasses * 256; i += kSortThreads)
-    if (s_tot[i]) atomicAdd(&J.small[kSmHist + i], s_tot[i]);
-  uint32_t* mine = J.grids + (size_t)bid * J.gwords;
-  for (int i = tid; i < J.gwords; i += kSortThreads) mine[i] = s_grid[i];
 }
 
-// Depth sort, phase B0 side job: grid[c] = sum over the CTAs' private grids, 16 grids per
-// work item (one atomic add per item).
-__device__ __forceinline__ void depth_grid_sum(const RadixJob& J, uint32_t G, uint32_t bid) {
-  const int64_t groups = (G + 15) / 16;
-  const int64_t items = (int64_t)J.gwords * groups;
-  for (int64_t it = (int64_t)bid * kSortThreads + threadIdx.x; it < items; it += (int64_t)G * kSortThreads) {
-    const int c = (int)(it % J.gwords);
-    const uint32_t g0 = (uint32_t)(it / J.gwords) * 16u, g1 = min(G, g0 + 16u);
-    uint32_t acc = 0;
-    for (uint32_t g = g0; g < g1; ++g) acc += J.grids[(size_t)g * J.gwords + c];
-    if (acc) atomicAdd(&J.grid[c], acc);
-  }
-}
-
-// Tiles touched by the Gaussian at a depth-sorted position (key, index), and its rectangle
-// record (first slot left 0).
-__device__ __forceinline__ uint32_t touched(const RadixJob& J, int64_t n, uint32_t key, uint32_t g, uint4& rec) {
-  rec = make_uint4(0u, 0u, 1u, g);
-  if (key == kCulledKey) return 0u;
-  const float4* q0 = reinterpret_cast<const float4*>(J.proj);
-  const int r = __float_as_int(__ldg(&q0[n + g].w));
-  const float4 a = __ldg(&q0[g]);
-  const int fu = (int)floorf(fminf(fmaxf(a.x, -1e9f), 1e9f));
-  const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
-  const int x0 = min(max((fu - r) >> 4, 0), J.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), J.Tx);
-  const int y0 = min(max((fv - r) >> 4, 0), J.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), J.Ty);
-  if (!(r > 0 && x0 < x1 && y0 < y1)) return 0u;
-  rec.y = (uint32_t)x0 | ((uint32_t)y0 << 16);
-  rec.z = (uint32_t)(x1 - x0);
-  return (uint32_t)((x1 - x0) * (y1 - y0));
+// Tiles touched by Gaussian g (from its rectangle record) and its scan record (first slot
+// left 0; z = width | height << 16).
+__device__ __forceinline__ uint32_t touched(const RadixJob& J, uint32_t g, uint4& rec) {
+  const uint2 r = __ldcg(&J.rrec[g]);  // written by other CTAs of this launch
+  rec = make_uint4(0u, r.x, r.y, g);
+  return (r.y & 0xffffu) * (r.y >> 16);
 }
 
 // Block-wide sum over the 256 threads (result in every thread).
@@ -518,136 +476,24 @@ __device__ __forceinline__ unsigned long long block_sum(SortSmem<ITEMS>& S, uint
   return t;
 }
 
-// One CTA: 2-D prefix sums of the difference grid give the instances of every tile; their
-// scan in tile order gives the staged ranges, and their digit sums the exclusive digit bases
-// of the tile passes.  s_grid holds gwords words, s_dig 2 x 256.
-template <int ITEMS>
-__device__ void tile_counts_cta(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid, uint32_t* s_dig) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Tx = J.Tx, Ty = J.Ty, gw = Tx + 1, gh = Ty + 1, T = Tx * Ty;
-  for (int i = tid; i < gw * gh; i += kSortThreads) s_grid[i] = ld_acquire_u32(&J.grid[i]);
-  __syncthreads();
-  for (int y = warp; y < gh; y += kSortWarps) {  // prefix along each row, a warp per row
-    uint32_t carry = 0;
-    for (int x0 = 0; x0 < gw; x0 += 32) {
-      const int x = x0 + lane;
-      uint32_t v = x < gw ? s_grid[y * gw + x] : 0u;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (x < gw) s_grid[y * gw + x] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  __syncthreads();
-  for (int x = warp; x < gw; x += kSortWarps) {  // then along each column
-    uint32_t carry = 0;
-    for (int y0 = 0; y0 < gh; y0 += 32) {
-      const int y = y0 + lane;
-      uint32_t v = y < gh ? s_grid[y * gw + x] : 0u;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (y < gh) s_grid[y * gw + x] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  __syncthreads();
-  // the count of tile t = (y, x) is grid cell (y, x), walked in tile order by stepping x
-  // (one division per walk)
-  auto cell = [&](int t) { return s_grid[(t / Tx) * gw + (t % Tx)]; };
-  // digit sums: pass 0 holds the tiles d, d + 256, ...; pass 1 the tiles [256 d, 256 d + 256)
-  {
-    uint32_t sum = 0;
-    if (tid < T) {
-      int y = tid / Tx, x = tid % Tx;
-      for (int t = tid; t < T; t += 256) {
-        sum += s_grid[y * gw + x];
-        x += 256;
-        while (x >= Tx) { x -= Tx; ++y; }
-      }
-    }
-    s_dig[tid] = sum;
-  }
-  if (J.tpasses > 1) {
-    for (int d = warp; d < 256; d += kSortWarps) {
-      uint32_t sum = 0;
-      if ((d << 8) < T) {
-        for (int t = (d << 8) + lane; t < min(T, (d + 1) << 8); t += 32) sum += cell(t);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      }
-      if (lane == 0) s_dig[256 + d] = sum;
-    }
-  }
-  // exclusive scan of the T counts in tile order, consecutive tiles per thread
-  const int per = (T + kSortThreads - 1) / kSortThreads;
-  const int t0 = tid * per, t1 = min(T, t0 + per);
-  const int y0 = t0 < T ? t0 / Tx : 0, x0 = t0 < T ? t0 % Tx : 0;
-  uint32_t sum = 0;
-  for (int t = t0, y = y0, x = x0; t < t1; ++t) {
-    sum += s_grid[y * gw + x];
-    if (++x == Tx) { x = 0; ++y; }
-  }
-  uint32_t incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  __syncthreads();
-  if (lane == 31) S.wsum[warp] = incl;
-  __syncthreads();
-  uint32_t run = incl - sum;
-  for (int w = 0; w < warp; ++w) run += S.wsum[w];
-  for (int t = t0, y = y0, x = x0; t < t1; ++t) {
-    const uint32_t c = s_grid[y * gw + x];
-    J.rstage[2 * (int64_t)t] = c ? run : 0u;
-    J.rstage[2 * (int64_t)t + 1] = c ? run + c : 0u;
-    run += c;
-    if (++x == Tx) { x = 0; ++y; }
-  }
-  __syncthreads();
-  if (warp < J.tpasses) {  // exclusive digit bases, a warp per pass
-    uint32_t carry = 0;
-    for (int d0 = 0; d0 < 256; d0 += 32) {
-      const uint32_t c = s_dig[warp * 256 + d0 + lane];
-      uint32_t in = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xffffffffu, in, o);
-        if (lane >= o) in += u;
-      }
-      J.small[kSmDigitBase + (kDepthPasses + warp) * 256 + d0 + lane] = carry + in - c;
-      carry += __shfl_sync(0xffffffffu, in, 31);
-    }
-  }
-}
-
-// After the depth passes: the tiles-touched scan over the sorted Gaussians and the tile counts.
-// S1: the sum of every chunk of kScanChunk sorted Gaussians, while the last CTA (which has no
-// chunk when the grid has a spare CTA) computes the tile counts.  S2 (only for more than
-// kDirectChunks chunks): CTA 0 turns the sums into exclusive prefixes.  S3: every chunk's
-// records (its prefix summed directly from the chunk sums when there are few chunks).
-// Returns false if a barrier failed.
+// After the depth passes: the tiles-touched scan over the sorted Gaussians.  S1: every sorted
+// Gaussian's record (gathered once, by index, from the rectangle records) and the sum of every
+// chunk of kScanChunk of them.  S2 (only for more than kDirectChunks chunks): CTA 0 turns the
+// sums into exclusive prefixes.  S3: every chunk's first slots (its prefix summed directly from
+// the chunk sums when there are few chunks), the records read back in order.  Returns false if
+// a barrier failed.
 constexpr int64_t kDirectChunks = 4096;
 
 template <int ITEMS>
-__device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_grid, uint32_t* s_tot, uint32_t G,
-                           uint32_t bid, uint32_t& nbar) {
+__device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t G, uint32_t bid, uint32_t& nbar) {
   constexpr int kPer = kScanChunk / kSortThreads;  // 4 consecutive Gaussians per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n = J.n_host;
   const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
   const bool direct = nchunks <= kDirectChunks;
-  const uint32_t* skey = J.key[kDepthPasses & 1];
   const uint32_t* sidx = J.val[kDepthPasses & 1];
   unsigned long long* wsum64 = reinterpret_cast<unsigned long long*>(S.gbase);  // free in these phases
-  // S1: chunk sums; tile counts on the last CTA
+  // S1: records and chunk sums (a thread keeps its kPer Gaussians for S3)
   for (int64_t c = bid; c < nchunks; c += G) {
     uint32_t sum = 0;
 #pragma unroll
@@ -655,13 +501,13 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
       const int64_t i = c * kScanChunk + tid * kPer + j;
       if (i < n) {
         uint4 rec;
-        sum += touched(J, n, skey[i], sidx[i], rec);
+        sum += touched(J, __ldcg(&sidx[i]), rec);
+        J.grec[i] = rec;
       }
     }
     const unsigned long long t = block_sum(S, sum);
     if (tid == 0) J.chunk_tot[c] = t;
   }
-  if (bid == G - 1) tile_counts_cta(S, J, s_grid, s_tot);
   if (!grid_barrier(S, J, ++nbar * G, true)) return false;
   // S2: exclusive prefixes of the chunk sums and the instance count M (CTA 0)
   if (!direct) {
@@ -721,7 +567,8 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t* s_gr
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int64_t i = c * kScanChunk + tid * kPer + j;
-      cnt[j] = i < n ? touched(J, n, skey[i], sidx[i], rec[j]) : 0u;
+      rec[j] = i < n ? J.grec[i] : make_uint4(0u, 0u, 0u, 0u);  // this thread's own S1 writes
+      cnt[j] = (rec[j].z & 0xffffu) * (rec[j].z >> 16);
       sum += cnt[j];
     }
     uint32_t incl = sum;
@@ -771,10 +618,7 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     const uint32_t* kin = J.key[p & 1];
     const uint32_t* vin = J.val[p & 1];
     // ---- A: digit counts of every radix tile
-    if (!kTileSort && p == 0) {
-      uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
-      depth_phase0(S, J, s_grid, s_grid + J.gwords, J.n_host, ntiles, G, bid);
-    }
+    if (!kTileSort && p == 0) depth_phase0(S, J, J.n_host, ntiles, G, bid);
     for (int64_t tile = bid; tile < ntiles && (kTileSort || p > 0); tile += G) {
       for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
       __syncthreads();
@@ -783,12 +627,12 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       if (gen) {
         gen_digit_counts(S, J, tile, base, nvalid, M);
       } else {
-        uint32_t k[ITEMS], v[ITEMS];
-        load_tile<ITEMS>(S, J, false, kin, vin, tile, base, nvalid, k, v);
+        // the counts need the keys only
+        const bool full = nvalid == kTile;
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i) {
           const int li = warp * (ITEMS * 32) + i * 32 + lane;
-          if (li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
+          if (full || li < nvalid) atomicAdd(&S.tstart[(__ldcg(&kin[base + li]) >> shift) & 255u], 1u);
         }
         __syncthreads();
       }
@@ -797,27 +641,11 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     }
     ++nbar;
     if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && bid == 0))) return;
-    // ---- B: per digit, exclusive scan over the tiles, plus the digit's global base
-    if (!kTileSort) {
-      if (p == 0) depth_grid_sum(J, G, bid);
-      // the digit bases of this pass: exclusive scan of the digit totals of phase 0
-      const uint32_t c = J.small[kSmHist + p * 256 + tid];
-      uint32_t incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) S.wsum[warp] = incl;
-      __syncthreads();
-      uint32_t woff = 0;
-      for (int w = 0; w < warp; ++w) woff += S.wsum[w];
-      S.gbase[tid] = woff + incl - c;
-      __syncthreads();
-    }
+    // ---- B: per digit, exclusive scan of its counts over the tiles; the column's sum is the
+    // digit's total, from which phase C takes the digit bases
     for (uint32_t d = bid; d < 256; d += G) {
       uint32_t* col = J.hist + (int64_t)d * J.hist_stride;
-      uint32_t carry = kTileSort ? J.small[kSmDigitBase + (J.slot0 + p) * 256 + d] : S.gbase[d];
+      uint32_t carry = 0;
       constexpr int kPer = 12;
       for (int64_t c0 = 0; c0 < ntiles; c0 += kSortThreads * kPer) {
         uint32_t x[kPer];
@@ -851,14 +679,30 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         carry += total;
         __syncthreads();
       }
+      if (tid == 0) J.small[kSmHist + (J.slot0 + p) * 256 + d] = carry;
     }
     if (!grid_barrier(S, J, ++nbar * G, true)) return;
+    {  // the digit bases: exclusive scan of the digit totals (thread = digit)
+      const uint32_t c = __ldcg(&J.small[kSmHist + (J.slot0 + p) * 256 + tid]);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) S.wsum[warp] = incl;
+      __syncthreads();
+      uint32_t woff = 0;
+      for (int w = 0; w < warp; ++w) woff += S.wsum[w];
+      S.dbase[tid] = woff + incl - c;
+      __syncthreads();
+    }
     // ---- C: rank within the tile, scatter through shared memory, digit-contiguous writes
     uint32_t* kout = J.key[(p + 1) & 1];
     uint32_t* vout = fin ? J.vals_out : J.val[(p + 1) & 1];
     for (int64_t tile = bid; tile < ntiles; tile += G) {
       // this tile's global digit offsets, loaded now and used after the ranking
-      const uint32_t tile_base = J.hist[(int64_t)tid * J.hist_stride + tile];
+      const uint32_t tile_base = S.dbase[tid] + __ldcg(&J.hist[(int64_t)tid * J.hist_stride + tile]);
       for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
       __syncthreads();
       const int64_t base = tile * kTile;
@@ -942,8 +786,8 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
           const uint32_t g = S.gbase[d] + (uint32_t)q - S.tstart[d];
           if (g < (uint64_t)M) {  // always true unless a barrier gave up (status bit set)
             const uint32_t val = S.vals[q];
-            if (!fin) kout[g] = key;
-            else if (J.keys64) J.keys64[g] = ((uint64_t)key << 32) | __float_as_uint(__ldg(&J.q0[val].z));
+            kout[g] = key;  // the last tile pass keeps the sorted tile ids for the ranges
+            if (fin && J.keys64) J.keys64[g] = ((uint64_t)key << 32) | __float_as_uint(__ldg(&J.q0[val].z));
             vout[g] = val;
           }
         }
@@ -952,10 +796,25 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     }
     if (p + 1 < J.passes && !grid_barrier(S, J, ++nbar * G, true)) return;
   }
+  if (!grid_barrier(S, J, ++nbar * G, true)) return;
   if (!kTileSort) {
-    if (!grid_barrier(S, J, ++nbar * G, true)) return;
-    uint32_t* s_grid = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SortSmem<ITEMS>));
-    depth_scan(S, J, s_grid, s_grid + J.gwords, G, bid, nbar);
+    depth_scan(S, J, G, bid, nbar);
+  } else {
+    // the staged ranges: tile t's run of sorted instances starts where the tile id changes
+    // (the host zeroed them, so empty tiles keep [0, 0)); a lane's neighbours come from the
+    // lanes beside it, the warp's edges from one more load
+    const uint32_t* skey = J.key[J.passes & 1];
+    const int64_t span = (M + 31) / 32 * 32;  // whole warps, so the shuffles see every lane
+    for (int64_t g = (int64_t)bid * kSortThreads + tid; g < span; g += (int64_t)G * kSortThreads) {
+      const bool in = g < M;
+      const uint32_t t = in ? __ldcg(&skey[g]) : 0xFFFFFFFFu;
+      uint32_t prev = __shfl_up_sync(0xffffffffu, t, 1);
+      uint32_t next = __shfl_down_sync(0xffffffffu, t, 1);
+      if (lane == 0) prev = g > 0 && g - 1 < M ? __ldcg(&skey[g - 1]) : 0xFFFFFFFFu;
+      if (lane == 31) next = g + 1 < M ? __ldcg(&skey[g + 1]) : 0xFFFFFFFFu;
+      if (in && (g == 0 || prev != t)) J.rstage[2 * (int64_t)t] = (uint32_t)g;
+      if (in && (g == M - 1 || next != t)) J.rstage[2 * (int64_t)t + 1] = (uint32_t)(g + 1);
+    }
   }
 }
 
@@ -966,6 +825,14 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort(const __grid_con
   const uint32_t G = gridDim.x / (uint32_t)B.views;
   const uint32_t view = blockIdx.x / G;
   radix_body<kDepthItems, false>(B.job[view], G, blockIdx.x - view * G);
+}
+
+// The same with radix tiles of kTileItems keys, for large N: fewer tiles, so fewer digit
+// counts to scan and less fixed work per key.
+__global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort_wide(const __grid_constant__ RadixBatch B) {
+  const uint32_t G = gridDim.x / (uint32_t)B.views;
+  const uint32_t view = blockIdx.x / G;
+  radix_body<kTileItems, false>(B.job[view], G, blockIdx.x - view * G);
 }
 
 __global__ void __launch_bounds__(kSortThreads, 4) k_tile_sort(const __grid_constant__ RadixBatch B) {
@@ -1009,13 +876,14 @@ __global__ void k_publish_ranges(const __grid_constant__ ViewBuffers B) {
 // Resident CTAs per SM of a sort kernel for a given dynamic shared-memory size on the current
 // device.  The shared-memory attribute is set on every call (it belongs to the device and is
 // lost if the device resets); the occupancy answer is cached per device and size.
-template <bool kTileSort>
+template <int kKernel>  // 0: depth sort, 1: tile sort, 2: depth sort with wide radix tiles
 int radix_blocks_per_sm(size_t smem) {
   constexpr int kMaxDev = 64;
   static std::mutex mu;
   static size_t cached_smem[kMaxDev] = {0};
   static int cached[kMaxDev] = {0};
-  const void* fn = kTileSort ? (const void*)k_tile_sort : (const void*)k_depth_sort;
+  const void* fn = kKernel == 1 ? (const void*)k_tile_sort
+                                : (kKernel == 2 ? (const void*)k_depth_sort_wide : (const void*)k_depth_sort);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
@@ -1036,23 +904,13 @@ cudaError_t launch_tile_sort(const RadixBatch& batch, int grid, size_t smem, cud
   void* args[] = {&b};
   return cudaLaunchCooperativeKernel((const void*)k_tile_sort, dim3(grid), dim3(kSortThreads), args, smem, st);
 }
-cudaError_t launch_depth_sort(const RadixBatch& batch, int grid, size_t smem, cudaStream_t st) {
+cudaError_t launch_depth_sort(const RadixBatch& batch, int grid, size_t smem, cudaStream_t st, bool wide) {
   RadixBatch b = batch;
   void* args[] = {&b};
-  return cudaLaunchCooperativeKernel((const void*)k_depth_sort, dim3(grid), dim3(kSortThreads), args, smem, st);
+  return cudaLaunchCooperativeKernel(wide ? (const void*)k_depth_sort_wide : (const void*)k_depth_sort, dim3(grid),
+                                     dim3(kSortThreads), args, smem, st);
 }
 
-int64_t grid_words(const gs::Cam& k) { return (int64_t)(k.Tx + 1) * (k.Ty + 1); }
-// depth sort: the sort's shared memory, then the CTA's difference grid and digit totals
-size_t depth_sort_smem(const gs::Cam& k) {
-  return sizeof(SortSmem<kDepthItems>) + sizeof(uint32_t) * ((size_t)grid_words(k) + kDepthPasses * 256);
-}
-// private difference grids a view's workspace holds: at most one per resident CTA (2048
-// threads per SM), at most one per radix tile of the depth sort plus one
-int64_t depth_grids_bound(int64_t n) {
-  return std::max<int64_t>(1, std::min<int64_t>(sort_tiles<kDepthItems>(n) + 1, (int64_t)gs::num_sms() * 8));
-}
-constexpr size_t kMaxSortSmem = 227 * 1024;  // shared memory a CTA may have
 
 // Views per tile-sort launch for a capacity (see kTileBudgetBytes).
 int tile_group(int views, int64_t cap) {
@@ -1061,14 +919,11 @@ int tile_group(int views, int64_t cap) {
   return std::max(1, std::min({fit, views, kMaxSortViews}));
 }
 
-// Largest grid words and tiles over a batch of cameras.
-void batch_dims(const gs::Cam* k, int views, int64_t* gw, int64_t* T) {
-  *gw = 1;
-  *T = 1;
-  for (int v = 0; v < views; ++v) {
-    *gw = std::max(*gw, grid_words(k[v]));
-    *T = std::max(*T, (int64_t)k[v].Tx * k[v].Ty);
-  }
+// Largest tile count over a batch of cameras.
+int64_t batch_tiles(const gs::Cam* k, int views) {
+  int64_t T = 1;
+  for (int v = 0; v < views; ++v) T = std::max(T, (int64_t)k[v].Tx * k[v].Ty);
+  return T;
 }
 
 struct SortView {
@@ -1097,8 +952,8 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
     for (int v = 0; v < gv; ++v) {
       const gs::Cam& k = V[g0 + v].k;
       const int64_t T = (int64_t)k.Tx * k.Ty;
-      uint32_t* z[4] = {reinterpret_cast<uint32_t*>(V[g0 + v].count), w[v].small, w[v].grid, V[g0 + v].ranges};
-      const int64_t zw[4] = {4, kSmWords, grid_words(k), 2 * T};
+      uint32_t* z[4] = {reinterpret_cast<uint32_t*>(V[g0 + v].count), w[v].small, w[v].rstage, V[g0 + v].ranges};
+      const int64_t zw[4] = {4, kSmWords, 2 * T, 2 * T};
       for (int b = 0; b < 4; ++b) {
         vb.zero[v][b] = z[b];
         vb.zero_words[v][b] = zw[b];
@@ -1114,39 +969,36 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
     if (gs_status s = gs::check_launch("gs_bin_sort init")) return s;
     if (n == 0) continue;
     // 1. per view, Gaussians by (depth, index): 4 stable passes over 32-bit depth keys; phase
-    //    0 also builds the difference grid of per-tile instance counts, and after the passes
-    //    the tiles-touched scan gives every sorted Gaussian's first slot (and M), the tile
-    //    counts the staged ranges and the digit bases of the tile passes
+    //    0 also writes every Gaussian's tile-rectangle record, and after the passes the
+    //    tiles-touched scan gives every sorted Gaussian's first slot (and M)
     RadixBatch db{};
     db.views = gv;
-    size_t dsmem = 0;
+    const bool wide = n >= kWideDepthN;
+    const size_t dsmem = wide ? sizeof(SortSmem<kTileItems>) : sizeof(SortSmem<kDepthItems>);
+    const int64_t dtiles = wide ? sort_tiles<kTileItems>(n) : sort_tiles<kDepthItems>(n);
     for (int v = 0; v < gv; ++v) {
       const SortView& sv = V[g0 + v];
-      dsmem = std::max(dsmem, depth_sort_smem(sv.k));
       RadixJob& dj = db.job[v];
       dj.key[0] = w[v].dkey[0]; dj.key[1] = w[v].dkey[1];
       dj.val[0] = w[v].didx[0]; dj.val[1] = w[v].didx[1];
       dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
-      dj.hist = w[v].hist_depth; dj.hist_stride = sort_tiles<kDepthItems>(n);
+      dj.hist = w[v].hist_depth; dj.hist_stride = dtiles;
       dj.small = w[v].small; dj.count = sv.count; dj.limit = limit; dj.drop_arrival = drop == 2 && g0 + v == 0;
-      dj.proj = sv.proj; dj.Tx = sv.k.Tx; dj.Ty = sv.k.Ty; dj.gwords = (int)grid_words(sv.k);
-      dj.grids = w[v].grids; dj.grid = w[v].grid;
+      dj.proj = sv.proj; dj.Tx = sv.k.Tx; dj.Ty = sv.k.Ty; dj.rrec = w[v].rrec;
       dj.chunk_tot = w[v].chunk_tot; dj.grec = w[v].grec; dj.slice_first = w[v].slice_first; dj.tcap = capacity;
-      dj.rstage = w[v].rstage; dj.tpasses = tile_passes(sv.k);
     }
-    // CTAs per view: one more than the radix tiles if the group fits, else an equal share of
-    // the resident CTAs
-    const int64_t resident = (int64_t)sms * radix_blocks_per_sm<false>(dsmem);
-    const int64_t G = std::max<int64_t>(
-        1, std::min({sort_tiles<kDepthItems>(n) + 1, resident / gv, depth_grids_bound(n)}));
-    if (cudaError_t e = launch_depth_sort(db, (int)(G * gv), dsmem, st))
+    // CTAs per view: as many as the radix tiles if the group fits, else an equal share of the
+    // resident CTAs
+    const int64_t resident = (int64_t)sms * (wide ? radix_blocks_per_sm<2>(dsmem) : radix_blocks_per_sm<0>(dsmem));
+    const int64_t G = std::max<int64_t>(1, std::min<int64_t>(dtiles, resident / gv));
+    if (cudaError_t e = launch_depth_sort(db, (int)(G * gv), dsmem, st, wide))
       return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
     // 2. per view, the stable sort of the instances by tile id: the first pass generates the
     //    (tile, index) pairs in depth order from the scan's records, the last writes the
     //    caller's arrays; tg views per launch, each with its own ping-pong buffers
     const size_t tsmem = sizeof(SortSmem<kTileItems>);
-    const int64_t tresident = (int64_t)sms * radix_blocks_per_sm<true>(tsmem);
+    const int64_t tresident = (int64_t)sms * radix_blocks_per_sm<1>(tsmem);
     for (int t0 = 0; t0 < gv; t0 += tg) {
       const int tv = std::min(tg, gv - t0);
       RadixBatch tb{};
@@ -1163,6 +1015,7 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
         tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
         tj.gen = GenSource{w[v].slice_first, w[v].grec, n, sv.k.Tx};
         tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
+        tj.rstage = w[v].rstage;
       }
       const int64_t TG = std::max<int64_t>(1, std::min<int64_t>(tresident / tv, sort_tiles<kTileItems>(capacity)));
       if (cudaError_t e = launch_tile_sort(tb, (int)(TG * tv), tsmem, st))
@@ -1200,7 +1053,7 @@ gs_status check_sort_args(int64_t n, int64_t capacity, const gs::Cam& k, const c
   if (n < 0 || n >= (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "%s: bad n", fn);
   if (capacity < 0 || capacity >= (int64_t(1) << 30))
     return gs::set_error(GS_ERR_INVALID, "%s: capacity must be in [0, 2^30)", fn);
-  if (tile_passes(k) > 2 || depth_sort_smem(k) > kMaxSortSmem)  // the tile counts handle two passes
+  if (tile_passes(k) > kMaxTilePasses || k.Tx > 65535 || k.Ty > 65535)  // 16-bit rectangle fields
     return gs::set_error(GS_ERR_INVALID, "%s: %d x %d tiles exceed the supported grid", fn, k.Tx, k.Ty);
   return GS_OK;
 }
@@ -1215,9 +1068,7 @@ extern "C" size_t gs_bin_sort_batch_workspace_size(int batch, int64_t n, int64_t
   if (!cams || batch < 1 || n < 0 || capacity < 0) return 0;
   std::vector<gs::Cam> k((size_t)batch);
   for (int v = 0; v < batch; ++v) k[v] = gs::make_cam(cams[v]);
-  int64_t gw, T;
-  batch_dims(k.data(), batch, &gw, &T);
-  return carve(nullptr, nullptr, std::min(batch, kMaxSortViews), n, capacity, gw, T, depth_grids_bound(n),
+  return carve(nullptr, nullptr, std::min(batch, kMaxSortViews), n, capacity, batch_tiles(k.data(), batch),
                tile_group(batch, capacity));
 }
 
@@ -1236,8 +1087,7 @@ extern "C" gs_status gs_bin_sort(const float* proj, int64_t n, const gs_camera* 
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort: workspace %zu bytes < %zu needed", workspace_bytes, need);
   Workspace w;
-  carve(&w, reinterpret_cast<char*>(workspace), 1, n, capacity, grid_words(k), (int64_t)k.Tx * k.Ty,
-        depth_grids_bound(n), 1);
+  carve(&w, reinterpret_cast<char*>(workspace), 1, n, capacity, (int64_t)k.Tx * k.Ty, 1);
   cudaStream_t st = gs::as_stream(stream);
   const SortView view{proj, k, keys, vals, ranges, count};
   if (gs_status s = run_sorts(&view, 1, n, capacity, &w, 1, st)) return s;
@@ -1270,13 +1120,11 @@ extern "C" gs_status gs_bin_sort_batch(const float* const* projs, int batch, int
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_bin_sort_batch: workspace %zu bytes < %zu needed", workspace_bytes,
                          need);
-  int64_t gw, T;
   std::vector<gs::Cam> k((size_t)batch);
   for (int v = 0; v < batch; ++v) k[v] = V[v].k;
-  batch_dims(k.data(), batch, &gw, &T);
   Workspace w[kMaxSortViews];
-  carve(w, reinterpret_cast<char*>(workspace), std::min(batch, kMaxSortViews), n, capacity, gw, T,
-        depth_grids_bound(n), tile_group(batch, capacity));
+  carve(w, reinterpret_cast<char*>(workspace), std::min(batch, kMaxSortViews), n, capacity,
+        batch_tiles(k.data(), batch), tile_group(batch, capacity));
   cudaStream_t st = gs::as_stream(stream);
   if (gs_status s = run_sorts(V.data(), batch, n, capacity, w, tile_group(batch, capacity), st)) return s;
   if (!counts_host) return GS_OK;
