@@ -205,6 +205,18 @@ def _oracle_worker(conn, P, jit, cam, lr, eps):
     conn.close()
 
 
+def available_host_bytes() -> int:
+    """MemAvailable of /proc/meminfo (64 GB if it cannot be read)."""
+    try:
+        with open("/proc/meminfo") as fh:
+            for line in fh:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 64 << 30
+
+
 class OracleSampler:
     """Times the CPU oracle, as it stands, on the host cores: one spawned process per core,
     each running the oracle's whole step (batch 1) on its own band of `rows` image rows at full
@@ -212,11 +224,15 @@ class OracleSampler:
     reach the band.  One round = every process takes one step; throughput = (bands x rows /
     height) views / wall time of the round."""
 
-    def __init__(self, cfg_idx: int, P=None, cams=None, workers: int | None = None):
+    # host memory the oracle's step holds per Gaussian it is given (double-precision parameters,
+    # moments and gradients, and its per-Gaussian records), with slack
+    BYTES_PER_GAUSSIAN = 5000
+
+    def __init__(self, cfg_idx: int, P=None, cams=None, jit=None, workers: int | None = None):
         self.cfg = scenes.CONFIGS[cfg_idx]
         self.P = scenes.make_params(cfg_idx) if P is None else P
         self.cams = scenes.make_cameras(cfg_idx) if cams is None else cams
-        self.jit = scenes.jitter_means(self.P, self.cfg.jitter, 2000 + cfg_idx)
+        self.jit = scenes.jitter_means(self.P, self.cfg.jitter, 2000 + cfg_idx) if jit is None else jit
         self.workers = workers or max(1, len(os.sched_getaffinity(0)))
         self.rows = None
         self.procs = []
@@ -252,9 +268,15 @@ class OracleSampler:
     def start(self):
         import multiprocessing as mp
 
+        # as many processes as host cores, and as the available memory holds
+        bands = [self._band(k) for k in range(self.workers)]
+        need = max(b[0].shape[1] for b in bands) * self.BYTES_PER_GAUSSIAN
+        fit = max(1, int(0.6 * available_host_bytes() // max(need, 1)))
+        if fit < self.workers:
+            self.workers = fit
+            bands = bands[:fit]
         ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
-        for k in range(self.workers):
-            P, jit, cam, rows = self._band(k)
+        for P, jit, cam, rows in bands:
             a, b = ctx.Pipe()
             pr = ctx.Process(target=_oracle_worker, args=(b, P, jit, cam, self.cfg.lr, self.cfg.eps), daemon=True)
             pr.start()
@@ -600,36 +622,42 @@ def main():
     e2e = None
     if not args.no_e2e:
         host_t = torch.empty((cfg.n_views, 3, cfg.height, cfg.width), dtype=torch.float32).pin_memory()
-        host_t.copy_(targets.cpu())
+        host_t.copy_(targets)  # device -> pinned host, no pageable temporary
+
+        def host_batch(ids):
+            # a batch of consecutive views is a slice of the pinned array (itself pinned);
+            # otherwise one pinned gather per distinct batch, made before the timed steps
+            if ids == list(range(ids[0], ids[0] + len(ids))):
+                return host_t[ids[0]:ids[0] + len(ids)]
+            key = tuple(ids)
+            if key not in gathered:
+                gathered[key] = host_t[list(ids)].pin_memory()
+            return gathered[key]
+
+        gathered = {}
+        for s in range(args.steps):
+            host_batch(batch_of(args.warmup + s)[0])
         for s in range(2):
             ids, bc = batch_of(s)
-            tr.step(bc, host_t[ids])
+            tr.step(bc, host_batch(ids))
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        # one pinned copy per distinct batch of views (batches repeat once the views are dealt)
-        pinned = {}
-        for s in range(args.steps):
-            ids = tuple(batch_of(args.warmup + s)[0])
-            if ids not in pinned:
-                pinned[ids] = host_t[list(ids)].pin_memory()
-        t_setup = time.perf_counter() - t0
-        t0 = time.perf_counter()
         for s in range(args.steps):
             ids, bc = batch_of(args.warmup + s)
-            tr.step(bc, pinned[tuple(ids)])
+            tr.step(bc, host_batch(ids))
         torch.cuda.synchronize()
         t_e2e = time.perf_counter() - t0
         t_e2e = max_over_ranks(t_e2e, dist, "cuda")
-        del t_setup
+        del host_t, gathered
         e2e = {"value": views / t_e2e, "unit": UNIT,
                "h2d_bytes_per_step": cfg.batch * 3 * cfg.height * cfg.width * 4,
                "d2h_bytes_per_step": 4 + cfg.batch * 16}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        smp = OracleSampler(args.config, P=P, cams=cams)
+        smp = OracleSampler(args.config, P=P, cams=cams, jit=jit)
         smp.calibrate(10.0)
         smp.start()
         v, wall, views = smp.round()
