@@ -227,6 +227,7 @@ class OracleSampler:
     # host memory the oracle's step holds per Gaussian it is given (double-precision parameters,
     # moments and gradients, and its per-Gaussian records), with slack
     BYTES_PER_GAUSSIAN = 5000
+    MAX_BAND_GAUSSIANS = 1_500_000
 
     def __init__(self, cfg_idx: int, P=None, cams=None, jit=None, workers: int | None = None):
         self.cfg = scenes.CONFIGS[cfg_idx]
@@ -252,7 +253,8 @@ class OracleSampler:
         return self.P[:, idx], self.jit[:, idx], cam, rows
 
     def calibrate(self, budget_s: float):
-        """Band height (a multiple of 16) whose step takes about budget_s on one core."""
+        """Band height (a multiple of 16) whose step takes about budget_s on one core, and at
+        most as tall as keeps a band's Gaussians within MAX_BAND_GAUSSIANS."""
         import oracle
 
         self.rows = 16
@@ -261,26 +263,29 @@ class OracleSampler:
         t0 = time.perf_counter()
         oracle.step(P, np.zeros_like(P), np.zeros_like(P), [cam], tgt, lr=self.cfg.lr, eps=self.cfg.eps)
         t16 = max(time.perf_counter() - t0, 1e-3)
+        del P, jit, tgt
         self.rows = int(max(16, min(self.cfg.height, 16 * math.floor(budget_s / t16))))
         self.rows = max(16, self.rows // 16 * 16)
+        while self.rows > 16 and self._band(0)[0].shape[1] > self.MAX_BAND_GAUSSIANS:
+            self.rows = max(16, (self.rows // 2) // 16 * 16)
         return self.rows
 
     def start(self):
         import multiprocessing as mp
 
-        # as many processes as host cores, and as the available memory holds
-        bands = [self._band(k) for k in range(self.workers)]
-        need = max(b[0].shape[1] for b in bands) * self.BYTES_PER_GAUSSIAN
-        fit = max(1, int(0.6 * available_host_bytes() // max(need, 1)))
-        if fit < self.workers:
-            self.workers = fit
-            bands = bands[:fit]
+        # as many processes as host cores, and as the available memory holds (a band is made,
+        # handed to its process and dropped before the next one)
+        need = self._band(0)[0].shape[1] * self.BYTES_PER_GAUSSIAN
+        fit = max(1, int(0.5 * available_host_bytes() // max(need, 1)))
+        self.workers = min(self.workers, fit)
         ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
-        for P, jit, cam, rows in bands:
+        for k in range(self.workers):
+            P, jit, cam, rows = self._band(k)
             a, b = ctx.Pipe()
             pr = ctx.Process(target=_oracle_worker, args=(b, P, jit, cam, self.cfg.lr, self.cfg.eps), daemon=True)
             pr.start()
             self.procs.append((pr, a, rows))
+            del P, jit
         for _, a, _ in self.procs:
             assert a.recv() == "ready"
 
@@ -326,6 +331,14 @@ def max_over_ranks(x: float, dist, device) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+_T0 = time.perf_counter()
+
+
+def log(msg: str):
+    """Progress on stderr (the JSON line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
 
 
 def main():
@@ -386,9 +399,11 @@ def main():
     from gaussian_splatting_gb300 import Trainer
     from gaussian_splatting_gb300 import _native as N
 
+    log(f"workload {cfg.name}: drawing the scene")
     P = scenes.make_params(args.config)
     cams = scenes.make_cameras(args.config)
     jit = scenes.jitter_means(P, cfg.jitter, 2000 + args.config)
+    log("scene drawn; rendering the targets")
     params = torch.from_numpy(P).cuda()
     tr = Trainer(params.clone(), cfg.width, cfg.height, cfg.batch, lr=cfg.lr, betas=(cfg.beta1, cfg.beta2),
                  eps=cfg.eps, w_l1=cfg.w_l1, w_ssim=cfg.w_ssim)
@@ -412,6 +427,7 @@ def main():
             else targets[torch.tensor(ids, device="cuda")]
         tr.step_async(bc, tgt)
 
+    log("targets rendered; warm-up")
     for s in range(args.warmup):
         run_step(s)
     torch.cuda.synchronize()
@@ -437,6 +453,7 @@ def main():
     except Exception:
         fp32_meas = None
 
+    log("timed steps")
     # ---------------- timed region (device time, CUDA events per step)
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -621,6 +638,7 @@ def main():
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
+        log("end to end")
         host_t = torch.empty((cfg.n_views, 3, cfg.height, cfg.width), dtype=torch.float32).pin_memory()
         host_t.copy_(targets)  # device -> pinned host, no pageable temporary
 
@@ -657,9 +675,12 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
+        log("CPU baseline: calibrating")
         smp = OracleSampler(args.config, P=P, cams=cams, jit=jit)
         smp.calibrate(10.0)
+        log(f"CPU baseline: bands of {smp.rows} rows; starting the processes")
         smp.start()
+        log(f"CPU baseline: {smp.workers} processes; one round")
         v, wall, views = smp.round()
         smp.stop()
         cpu = {"value": v, "unit": UNIT, "cores": smp.workers, "kind": "oracle",

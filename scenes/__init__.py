@@ -156,19 +156,22 @@ def make_params(cfg: SceneConfig | int, seed: int | None = None, n: int | None =
         seed = 0
     n = cfg.n if n is None else n
     rng = _rng(seed)
-    mu = _means(cfg.layout, n, rng)
-    ls = rng.uniform(-4.5, -2.5, size=(n, 3))
+    P = np.zeros((N_PLANES, n, 4), dtype=np.float32)
+    P[0, :, :3] = _means(cfg.layout, n, rng)
+    P[1, :, :3] = rng.uniform(-4.5, -2.5, size=(n, 3))
     q = rng.standard_normal((n, 4))
     q /= np.linalg.norm(q, axis=1, keepdims=True)
-    logit = rng.standard_normal(n)
-    dc = rng.normal(0.5, 0.2, size=(n, 3))
-    rest = rng.normal(0.0, 0.05, size=(n, 45))
-    P = np.zeros((N_PLANES, n, 4), dtype=np.float32)
-    P[0, :, :3] = mu
-    P[0, :, 3] = logit
-    P[1, :, :3] = ls
     P[2] = q
-    sh = np.concatenate([dc, rest], axis=1).astype(np.float32)  # (n, 48), index 3k + c
+    del q
+    P[0, :, 3] = rng.standard_normal(n)
+    # the SH coefficients, drawn in blocks of Gaussians (the same stream as one draw of all of
+    # them) so that no float64 copy of the whole [n, 48] array is ever held
+    sh = P[3:].transpose(1, 0, 2).reshape(n, 48) if n else np.zeros((0, 48), np.float32)
+    chunk = 1 << 20
+    for a in range(0, n, chunk):
+        sh[a:a + chunk, :3] = rng.normal(0.5, 0.2, size=(min(chunk, n - a), 3))
+    for a in range(0, n, chunk):
+        sh[a:a + chunk, 3:] = rng.normal(0.0, 0.05, size=(min(chunk, n - a), 45))
     P[3:] = sh.reshape(n, 12, 4).transpose(1, 0, 2)
     return P
 
