@@ -78,6 +78,10 @@ def lib():
         L.oracle_view_order.restype = None
         L.oracle_prune.argtypes = [C.c_void_p, i32, i64, C.c_float, C.c_void_p, i64]
         L.oracle_prune.restype = i64
+        L.oracle_densify_stat.argtypes = [dp, ip, i64, dp]
+        L.oracle_densify_stat.restype = None
+        L.oracle_densify.argtypes = [fp, fp, fp, fp, i64, C.c_float, C.c_float, fp, dp, dp, dp, i64, i64p, i64p]
+        L.oracle_densify.restype = i64
         _lib = L
     return _lib
 
@@ -250,6 +254,37 @@ def prune(plane_sets, min_logit):
                            max(n, 1))
     # the kernel layout keeps the plane stride; re-pack to a stride of k
     return k, [np.ascontiguousarray(o[:, :k]) for o in outs]
+
+
+def densify_stat(g2d, radius, stat=None):
+    """Adds one view's densification statistic: for radius > 0, |(du, dv)| and one view.
+    g2d: N x 9 (oracle layout); returns the N x 2 statistic (a new array unless given)."""
+    G = _d(g2d)
+    R = np.ascontiguousarray(radius, np.int32)
+    N = R.shape[0]
+    out = np.zeros((N, 2)) if stat is None else np.ascontiguousarray(stat, np.float64)
+    lib().oracle_densify_stat(_p(G, C.c_double), _p(R, C.c_int32), N, _p(out, C.c_double))
+    return out
+
+
+def densify(params, m, v, stat, grad_threshold, log_scale_threshold, normals):
+    """Clone / split.  params, m, v: float32 [15, N, 4]; stat: float32 N x 2 (sum of screen
+    gradient lengths, views); normals: float32 N x 6.  Returns (params, m, v) as double
+    [15, n_out, 4] arrays and (n_clone, n_split)."""
+    P, Mm, Vv = (np.ascontiguousarray(a, np.float32) for a in (params, m, v))
+    S = np.ascontiguousarray(stat, np.float32)
+    Z = np.ascontiguousarray(normals, np.float32)
+    N = P.shape[1]
+    nc, ns = np.zeros(1, np.int64), np.zeros(1, np.int64)
+    args = lambda op, om, ov, stride: (_p(P, C.c_float), _p(Mm, C.c_float), _p(Vv, C.c_float), _p(S, C.c_float), N,
+                                       C.c_float(grad_threshold), C.c_float(log_scale_threshold), _p(Z, C.c_float),
+                                       _p(op, C.c_double), _p(om, C.c_double), _p(ov, C.c_double), stride,
+                                       _p(nc, C.c_int64), _p(ns, C.c_int64))
+    dummy = np.zeros(1)
+    n_out = lib().oracle_densify(*args(dummy, dummy, dummy, 0))
+    outs = [np.zeros((15, max(n_out, 1), 4)) for _ in range(3)]
+    lib().oracle_densify(*args(outs[0], outs[1], outs[2], n_out))
+    return tuple(o[:, :n_out] for o in outs), (int(nc[0]), int(ns[0]))
 
 
 def step(params, m, v, cams, targets, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-15, t=1, w_l1=0.8, w_ssim=0.2,

@@ -828,6 +828,99 @@ int64_t prune(const float* const* planes, int n_sets, int64_t n, float min_logit
   return k;
 }
 
+// Grendel-GS notes, 训练流程 ("致密化": clone or split the Gaussians that need more detail,
+// prune the transparent ones).  The pages give no criterion; the readings taken:
+//  * statistic: per Gaussian, the sum over the views that see it (radius > 0) of the length of
+//    its screen-space mean gradient |(dL/du, dL/dv)| in that view, and the number of those
+//    views (densify_stat);
+//  * selected: seen at least once and sum / count >= grad_threshold, compared in fp32 (the
+//    precision the kernel decides in);
+//  * split if the largest log-scale exceeds log_scale_threshold (compared in fp32, no exp
+//    evaluated), else clone;
+//  * the output: the Gaussians not split, in index order, then for every selected Gaussian in
+//    index order its new ones: a clone (an exact copy), or two split children with means
+//    mu + R(q / |q|) (s * z_k) (s = exp(log-scale), z_k the caller's standard normals k = 0, 1)
+//    and log-scales lowered by ln 1.6, the other parameters copied; new Gaussians start with
+//    zero Adam moments, kept ones keep theirs.
+void densify_stat(const double* g2d, const int32_t* radius, int64_t N, double* stat) {
+  for (int64_t i = 0; i < N; ++i) {
+    if (radius[i] <= 0) continue;
+    const double du = g2d[9 * i + 0], dv = g2d[9 * i + 1];
+    stat[2 * i + 0] += std::sqrt(du * du + dv * dv);
+    stat[2 * i + 1] += 1.0;
+  }
+}
+
+void quat_rotation(const double q[4], double R[3][3]) {
+  const double len = std::sqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+  const double w = q[0] / len, x = q[1] / len, y = q[2] / len, z = q[3] / len;
+  R[0][0] = 1 - 2 * (y * y + z * z); R[0][1] = 2 * (x * y - w * z);     R[0][2] = 2 * (x * z + w * y);
+  R[1][0] = 2 * (x * y + w * z);     R[1][1] = 1 - 2 * (x * x + z * z); R[1][2] = 2 * (y * z - w * x);
+  R[2][0] = 2 * (x * z - w * y);     R[2][1] = 2 * (y * z + w * x);     R[2][2] = 1 - 2 * (x * x + y * y);
+}
+
+int64_t densify(const float* params, const float* m, const float* v, const float* stat, int64_t N,
+                float grad_threshold, float log_scale_threshold, const float* normals, double* out_p,
+                double* out_m, double* out_v, int64_t out_stride, int64_t* n_clone, int64_t* n_split) {
+  auto at = [&](const float* a, int pl, int64_t i, int c) { return (double)a[((int64_t)pl * N + i) * 4 + c]; };
+  std::vector<int> kind(N, 0);  // 0 untouched, 1 clone, 2 split
+  int64_t clones = 0, splits = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    const float sum = stat[2 * i], cnt = stat[2 * i + 1];
+    if (!(cnt > 0.0f)) continue;
+    const float avg = sum / cnt;
+    if (!(avg >= grad_threshold)) continue;
+    const float lmax = std::max(std::max(params[(1 * N + i) * 4 + 0], params[(1 * N + i) * 4 + 1]),
+                                params[(1 * N + i) * 4 + 2]);
+    kind[i] = lmax > log_scale_threshold ? 2 : 1;
+    if (kind[i] == 2) ++splits; else ++clones;
+  }
+  *n_clone = clones;
+  *n_split = splits;
+  const int64_t n_out = N - splits + clones + 2 * splits;
+  int64_t k = 0;
+  auto put = [&](int64_t dst, const double p[15][4], bool keep_moments, int64_t src) {
+    if (dst >= out_stride) return;
+    for (int pl = 0; pl < 15; ++pl)
+      for (int c = 0; c < 4; ++c) {
+        out_p[((int64_t)pl * out_stride + dst) * 4 + c] = p[pl][c];
+        out_m[((int64_t)pl * out_stride + dst) * 4 + c] = keep_moments ? at(m, pl, src, c) : 0.0;
+        out_v[((int64_t)pl * out_stride + dst) * 4 + c] = keep_moments ? at(v, pl, src, c) : 0.0;
+      }
+  };
+  double p[15][4];
+  for (int64_t i = 0; i < N; ++i) {  // the Gaussians not split, in index order
+    if (kind[i] == 2) continue;
+    for (int pl = 0; pl < 15; ++pl)
+      for (int c = 0; c < 4; ++c) p[pl][c] = at(params, pl, i, c);
+    put(k++, p, true, i);
+  }
+  for (int64_t i = 0; i < N; ++i) {  // then the new ones of every selected Gaussian
+    if (kind[i] == 0) continue;
+    for (int pl = 0; pl < 15; ++pl)
+      for (int c = 0; c < 4; ++c) p[pl][c] = at(params, pl, i, c);
+    if (kind[i] == 1) {
+      put(k++, p, false, i);
+      continue;
+    }
+    double q[4] = {p[2][0], p[2][1], p[2][2], p[2][3]}, R[3][3];
+    quat_rotation(q, R);
+    const double s[3] = {std::exp(p[1][0]), std::exp(p[1][1]), std::exp(p[1][2])};
+    for (int child = 0; child < 2; ++child) {
+      double c[15][4];
+      std::memcpy(c, p, sizeof(c));
+      for (int r = 0; r < 3; ++r) {
+        double off = 0;
+        for (int j = 0; j < 3; ++j) off += R[r][j] * s[j] * (double)normals[6 * i + 3 * child + j];
+        c[0][r] = p[0][r] + off;
+      }
+      for (int j = 0; j < 3; ++j) c[1][j] = p[1][j] - std::log(1.6);
+      put(k++, c, false, i);
+    }
+  }
+  return n_out;
+}
+
 }  // namespace
 
 // ======================================================================= C ABI
@@ -928,6 +1021,21 @@ void oracle_tile_split(const uint32_t* cost_px, int W, int H, int K, uint64_t* t
 // Greedy view order by the Odin scheduling score.  w: B x B float32 weights (Jaccard).
 void oracle_view_order(const float* w, int B, int unit, int32_t* order, float* score) {
   view_order(w, B, unit, order, score);
+}
+
+// Densification statistic of one view (+= into stat, N x 2: sum of |(du, dv)|, views).
+void oracle_densify_stat(const double* g2d, const int32_t* radius, int64_t N, double* stat) {
+  densify_stat(g2d, radius, N, stat);
+}
+
+// Clone / split (readings above densify_stat).  params, m, v: float32 [15][N][4]; stat:
+// float32 N x 2; normals: float32 N x 6.  Outputs [15][out_stride][4] doubles (slots past
+// out_stride not written).  Returns the output count; n_clone / n_split receive the counts.
+int64_t oracle_densify(const float* params, const float* m, const float* v, const float* stat, int64_t N,
+                       float grad_threshold, float log_scale_threshold, const float* normals, double* out_p,
+                       double* out_m, double* out_v, int64_t out_stride, int64_t* n_clone, int64_t* n_split) {
+  return densify(params, m, v, stat, N, grad_threshold, log_scale_threshold, normals, out_p, out_m, out_v,
+                 out_stride, n_clone, n_split);
 }
 
 // Opacity pruning: planes / out are arrays of n_sets pointers (parameters, then moments).

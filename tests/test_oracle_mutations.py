@@ -1,9 +1,9 @@
-"""The projection pins bite: each plausible mistake, planted in a copy of the oracle's source
+"""The projection and densification pins bite: each plausible mistake, planted in a copy of the oracle's source
 on the CPU, makes at least one pin fail.
 
 Every mutation names a text that occurs exactly once in oracle.cpp and its replacement; the
-copy is compiled into a temporary directory and the pins of
-``test_oracle_projection.py`` and ``test_oracle_pins.py`` run against it in a child process
+copy is compiled into a temporary directory and the pins of ``test_oracle_projection.py``,
+``test_oracle_densify.py`` and ``test_oracle_pins.py`` run against it in a child process
 (``GS_ORACLE_LIB`` points the wrapper at the copy).  The child must fail.  Nothing here
 touches the oracle the other tests use.
 """
@@ -50,6 +50,14 @@ MUTATIONS = {
     # backward: view-direction gradient with the wrong sign
     "bwd_sh_direction_sign": ("dmu[l] += (dd[l] - p.d[l] * ddot) / p.dlen;",
                               "dmu[l] -= (dd[l] - p.d[l] * ddot) / p.dlen;"),
+    # densification: split offset along the transposed rotation
+    "split_rotation_transposed": ("off += R[r][j] * s[j] * (double)normals[6 * i + 3 * child + j];",
+                                  "off += R[j][r] * s[j] * (double)normals[6 * i + 3 * child + j];"),
+    # densification: children scaled up instead of down
+    "split_scale_sign": ("for (int j = 0; j < 3; ++j) c[1][j] = p[1][j] - std::log(1.6);",
+                         "for (int j = 0; j < 3; ++j) c[1][j] = p[1][j] + std::log(1.6);"),
+    # densification: a mean exactly at the threshold not selected
+    "densify_threshold_strict": ("if (!(avg >= grad_threshold)) continue;", "if (!(avg > grad_threshold)) continue;"),
 }
 
 
@@ -67,6 +75,7 @@ def _run_pins(lib):
     env = dict(os.environ, GS_ORACLE_LIB=lib)
     cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
            os.path.join(ROOT, "tests", "test_oracle_projection.py"),
+           os.path.join(ROOT, "tests", "test_oracle_densify.py"),
            os.path.join(ROOT, "tests", "test_oracle_pins.py") + "::test_single_isotropic_gaussian_closed_form"]
     return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
