@@ -21,7 +21,8 @@ EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_project_batch", "gs_
            "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
            "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
-           "gs_tile_split", "gs_view_order", "gs_prune_workspace_size", "gs_prune", "gs_probe_ffma",
+           "gs_tile_split", "gs_view_order", "gs_prune_workspace_size", "gs_prune", "gs_densify_workspace_size",
+           "gs_densify", "gs_probe_ffma",
            "gs_debug_set_wait_limit",
            "gs_debug_drop_publish"]
 
@@ -77,15 +78,17 @@ def load() -> C.CDLL:
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
         "gs_loss_noalloc": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp], i32),
         "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
-        "gs_project_bwd": ([vp, i64, cp, vp, vp, vp, vp], i32),
+        "gs_project_bwd": ([vp, i64, cp, vp, vp, vp, vp, vp], i32),
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
-        "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp], i32),
+        "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp, vp], i32),
         "gs_tile_split": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
         "gs_view_order": ([vp, i32, i32, vp, vp, vp], i32),
         "gs_prune_workspace_size": ([i64], sz),
         "gs_prune": ([vp, i32, i64, f32, vp, i64, vp, sz, vp, vp, vp], i32),
+        "gs_densify_workspace_size": ([i64], sz),
+        "gs_densify": ([vp, vp, vp, i64, vp, f32, f32, vp, vp, vp, vp, i64, vp, sz, vp, vp, vp], i32),
         "gs_probe_ffma": ([vp, i32, i32, vp], i32),
         "gs_debug_set_wait_limit": ([i64], None),
         "gs_debug_drop_publish": ([i32], None),
@@ -220,9 +223,9 @@ def gs_render_bwd(proj, n, vals, ranges, cam, bg, T_final, n_contrib, dL_dimage,
            "gs_render_bwd")
 
 
-def gs_project_bwd(params, n, cam, proj, grad2d, grads, stream=None):
+def gs_project_bwd(params, n, cam, proj, grad2d, grads, densify_stat=None, stream=None):
     _check(load().gs_project_bwd(_ptr(params), n, _cam(cam), _ptr(proj), _ptr(grad2d), _ptr(grads),
-                                 _stream(stream)), "gs_project_bwd")
+                                 _ptr(densify_stat), _stream(stream)), "gs_project_bwd")
 
 
 def gs_visible_sets_workspace_size(batch, n) -> int:
@@ -245,7 +248,7 @@ def gs_sparse_adam(params, grads, exp_avg, exp_avg_sq, n, idx, n_idx, max_idx, l
 
 
 def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, step,
-                        counts=None, n_counts=0, stream=None):
+                        counts=None, n_counts=0, densify_stat=None, stream=None):
     batch = len(cams)
     carr = (Camera * batch)(*[c if isinstance(c, Camera) else camera(c) for c in cams])
     parr = (C.c_void_p * batch)(*[_ptr(p) for p in projs])
@@ -253,7 +256,7 @@ def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr
     _check(load().gs_project_bwd_adam(_ptr(params), n, C.cast(carr, C.c_void_p), batch, C.cast(parr, C.c_void_p),
                                       C.cast(garr, C.c_void_p), _ptr(exp_avg), _ptr(exp_avg_sq), lr, beta1, beta2,
                                       eps, step, _ptr(counts), n_counts if counts is not None else 0,
-                                      _stream(stream)), "gs_project_bwd_adam")
+                                      _ptr(densify_stat), _stream(stream)), "gs_project_bwd_adam")
 
 
 def gs_tile_split(cost_px, width, height, parts, tile_cost, cum, bounds, stream=None):
@@ -279,6 +282,23 @@ def gs_prune(planes_in, n, min_logit, planes_out, out_stride, workspace, n_keep,
                            workspace.numel() if workspace is not None else 0, _ptr(n_keep),
                            C.byref(host) if sync else None, _stream(stream)), "gs_prune")
     return host.value if sync else None
+
+
+def gs_densify_workspace_size(n) -> int:
+    return load().gs_densify_workspace_size(n)
+
+
+def gs_densify(params, exp_avg, exp_avg_sq, n, densify_stat, grad_threshold, log_scale_threshold, normals, outs,
+               out_stride, workspace, counts, sync=False, stream=None):
+    """outs: (params_out, exp_avg_out, exp_avg_sq_out) or None (count only).  Returns the host
+    counts (output, clones, splits) when sync=True, else None (they stay in counts)."""
+    host = (C.c_int64 * 3)()
+    po, mo, vo = outs if outs is not None else (None, None, None)
+    _check(load().gs_densify(_ptr(params), _ptr(exp_avg), _ptr(exp_avg_sq), n, _ptr(densify_stat), grad_threshold,
+                             log_scale_threshold, _ptr(normals), _ptr(po), _ptr(mo), _ptr(vo), out_stride,
+                             _ptr(workspace), workspace.numel() if workspace is not None else 0, _ptr(counts),
+                             C.cast(host, C.c_void_p) if sync else None, _stream(stream)), "gs_densify")
+    return tuple(host) if sync else None
 
 
 def gs_probe_ffma(out, blocks, iters, stream=None):

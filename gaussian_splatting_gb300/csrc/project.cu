@@ -427,7 +427,8 @@ __device__ __forceinline__ void project_bwd_core(const Src& src, const Cam& k, f
 
 __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ params, int64_t n, Cam k,
                                                      float3 campos, const float* __restrict__ proj,
-                                                     const float* __restrict__ grad2d, float* __restrict__ grads) {
+                                                     const float* __restrict__ grad2d, float* __restrict__ grads,
+                                                     float2* __restrict__ stat) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   if (__float_as_int(ldg4(proj, n + i).w) <= 0) return;  // culled in this view
@@ -435,7 +436,14 @@ __global__ void __launch_bounds__(256) k_project_bwd(const float* __restrict__ p
   const GlobalParams src{params, n, i};
   if (!project_core(src, k, f)) return;
   BwdOut o;
-  project_bwd_core(src, k, campos, f, ldg4(grad2d, 3 * i + 0), ldg4(grad2d, 3 * i + 1), ldg4(grad2d, 3 * i + 2), o);
+  const float4 g0 = ldg4(grad2d, 3 * i + 0);
+  project_bwd_core(src, k, campos, f, g0, ldg4(grad2d, 3 * i + 1), ldg4(grad2d, 3 * i + 2), o);
+  if (stat) {  // densification statistic: this view's screen-space mean-gradient length
+    float2 s2 = stat[i];
+    s2.x += sqrtf(g0.x * g0.x + g0.y * g0.y);
+    s2.y += 1.f;
+    stat[i] = s2;
+  }
   // ---- accumulate into the gradient planes
   float4* G = reinterpret_cast<float4*>(grads);
   float4 a0 = G[i];
@@ -512,7 +520,8 @@ struct AdamSmem {
 __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __restrict__ params, int64_t n,
                                                                       BatchViews bv, float4* __restrict__ m,
                                                                       float4* __restrict__ v, AdamHyper h,
-                                                                      const int64_t* counts, int n_counts) {
+                                                                      const int64_t* counts, int n_counts,
+                                                                      float2* __restrict__ stat) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AdamSmem& S = *reinterpret_cast<AdamSmem*>(smem_raw);
   for (int c = 0; c < n_counts; ++c)
@@ -530,6 +539,7 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
   for (int f = 0; f < 48; ++f) s_sh[f][t] = 0.f;
   float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gl = ga, gq = ga;
   bool seen = false;
+  float dsum = 0.f, dcnt = 0.f;  // densification statistic of the batch's views
   uint32_t vis = 0;  // views whose radius word is > 0, all read up front
   for (int b = 0; b < bv.batch; ++b)
     if (__float_as_int(__ldg(&reinterpret_cast<const float4*>(bv.proj[b])[n + i].w)) > 0) vis |= 1u << b;
@@ -544,6 +554,8 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
     Fwd f;
     if (!project_core(src, bv.k[b], f)) continue;
     seen = true;
+    dsum += sqrtf(g0.x * g0.x + g0.y * g0.y);
+    dcnt += 1.f;
     BwdOut o;
     project_bwd_core(src, bv.k[b], bv.campos[b], f, g0, g1, g2v, o);
     ga.x += o.gm[0]; ga.y += o.gm[1]; ga.z += o.gm[2]; ga.w += o.glogit;
@@ -553,6 +565,12 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
     for (int fidx = 0; fidx < 48; ++fidx) s_sh[fidx][t] += o.gcol[fidx % 3] * o.b.y[fidx / 3];
   }
   if (!seen) return;  // not visible in any view of the batch: untouched
+  if (stat) {
+    float2 s2 = stat[i];
+    s2.x += dsum;
+    s2.y += dcnt;
+    stat[i] = s2;
+  }
   float4* P = reinterpret_cast<float4*>(params);
   // planes in groups of three: the six moment loads of a group are in flight together
 #pragma unroll 1
@@ -637,7 +655,7 @@ extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_c
 }
 
 extern "C" gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, const float* proj,
-                                    const float* grad2d, float* grads, void* stream) {
+                                    const float* grad2d, float* grads, float* densify_stat, void* stream) {
   if (gs_status s = gs::check_camera(cam)) return s;
   if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_project_bwd: bad n");
   if (n == 0) return GS_OK;
@@ -647,8 +665,10 @@ extern "C" gs_status gs_project_bwd(const float* params, int64_t n, const gs_cam
   const gs::Cam k = gs::make_cam(*cam);
   const int threads = 256;
   const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+  if (densify_stat && !gs::aligned8(densify_stat))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd: densify_stat must be 8-byte aligned");
   k_project_bwd<<<blocks, threads, 0, gs::as_stream(stream)>>>(params, n, k, camera_centre(*cam), proj, grad2d,
-                                                               grads);
+                                                               grads, reinterpret_cast<float2*>(densify_stat));
   return gs::check_launch("gs_project_bwd");
 }
 
@@ -656,7 +676,7 @@ extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_came
                                          const float* const* proj_per_view, const float* const* grad2d_per_view,
                                          float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
                                          float eps, int64_t step, const int64_t* counts, int n_counts,
-                                         void* stream) {
+                                         float* densify_stat, void* stream) {
   if (batch < 1 || batch > kMaxBatchViews)
     return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: batch must be 1..%d", kMaxBatchViews);
   if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: bad n");
@@ -691,7 +711,10 @@ extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_came
   const cudaError_t attr = cudaFuncSetAttribute(k_project_bwd_adam, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        (int)sizeof(AdamSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_project_bwd_adam: %s", cudaGetErrorString(attr));
+  if (densify_stat && !gs::aligned8(densify_stat))
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: densify_stat must be 8-byte aligned");
   k_project_bwd_adam<<<blocks, kAdamThreads, sizeof(AdamSmem), gs::as_stream(stream)>>>(
-      params, n, bv, reinterpret_cast<float4*>(exp_avg), reinterpret_cast<float4*>(exp_avg_sq), h, counts, n_counts);
+      params, n, bv, reinterpret_cast<float4*>(exp_avg), reinterpret_cast<float4*>(exp_avg_sq), h, counts, n_counts,
+      reinterpret_cast<float2*>(densify_stat));
   return gs::check_launch("gs_project_bwd_adam");
 }

@@ -78,6 +78,9 @@ class Trainer:
         self.grads = torch.zeros_like(self.params)
         self.exp_avg = torch.zeros_like(self.params)
         self.exp_avg_sq = torch.zeros_like(self.params)
+        # densification statistic (sum of screen-space mean-gradient lengths, views), gathered by
+        # every training step's projection backward and read by densify()
+        self.dstat = torch.zeros((self.n, 2), dtype=torch.float32, device=dev)
         self.t = 0
         n, P = self.n, width * height
         tiles = ((width + 15) // 16) * ((height + 15) // 16)
@@ -209,12 +212,40 @@ class Trainer:
         self._alloc_gaussians(k)
         return k
 
+    def densify(self, grad_threshold: float, scale_threshold: float, seed: int = 0):
+        """Clone / split (the growing half of densification) by gs_densify: the Gaussians whose
+        mean screen-space mean-gradient length over the views that saw them since the last
+        densify() reaches grad_threshold are cloned, or split in two if their largest scale
+        exceeds scale_threshold (world units); the children's offsets use standard normals
+        drawn from `seed`.  New Gaussians start with zero moments, the statistic and the
+        gradients restart from zero.  Synchronises; returns (count, clones, splits)."""
+        dev, n = self.params.device, self.n
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(int(seed))
+        normals = torch.randn((max(n, 1), 6), generator=gen, device=dev, dtype=torch.float32)
+        ws = torch.empty(max(N.gs_densify_workspace_size(n), 256), dtype=torch.uint8, device=dev)
+        counts = torch.zeros(3, dtype=torch.int64, device=dev)
+        lthr = math.log(scale_threshold) if scale_threshold > 0 else -math.inf
+        total, clones, splits = N.gs_densify(self.params, self.exp_avg, self.exp_avg_sq, n, self.dstat,
+                                             grad_threshold, lthr, normals, None, 0, ws, counts, sync=True)
+        outs = [torch.empty((15, max(total, 1), 4), dtype=torch.float32, device=dev) for _ in range(3)]
+        if total > 0:
+            N.gs_densify(self.params, self.exp_avg, self.exp_avg_sq, n, self.dstat, grad_threshold, lthr, normals,
+                         outs, total, ws, counts, sync=True)
+        self.params, self.exp_avg, self.exp_avg_sq = (o[:, :total] if total else o[:, :0] for o in outs)
+        self.params = self.params.contiguous()
+        self.exp_avg = self.exp_avg.contiguous()
+        self.exp_avg_sq = self.exp_avg_sq.contiguous()
+        self._alloc_gaussians(total)
+        return total, clones, splits
+
     def _alloc_gaussians(self, n: int):
         """(Re)allocate the per-Gaussian scratch for n Gaussians."""
         dev, batch = self.params.device, self.batch
         f32, i32 = torch.float32, torch.int32
         self.n = n
         self.grads = torch.zeros_like(self.params)
+        self.dstat = torch.zeros((n, 2), dtype=f32, device=dev)
         self.proj = torch.zeros((batch, 3, n, 4), dtype=f32, device=dev)
         self.grad2d = torch.zeros((batch, n, 12), dtype=f32, device=dev)
         self.vis_ws = torch.empty(max(N.gs_visible_sets_workspace_size(batch, n), 256), dtype=torch.uint8, device=dev)
@@ -272,7 +303,8 @@ class Trainer:
             T("render_bwd", N.gs_render_bwd, proj, n, vals, ranges, cam, self.bg, self.T_final,
               self.n_contrib, dimg, self.grad2d[b], stream=st)
             if not fused:
-                T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads, stream=st)
+                T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads,
+                  self.dstat if adam else None, stream=st)
                 launches += LAUNCHES["project_bwd"]
             if self.work is not None:
                 # (entries evaluated in the forward, entries accumulated, entries walked by the backward,
@@ -286,7 +318,7 @@ class Trainer:
         if fused:
             T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, ccams, [self.proj[b] for b in range(B)],
               [self.grad2d[b] for b in range(B)], self.exp_avg, self.exp_avg_sq, self.lr, self.betas[0],
-              self.betas[1], self.eps, self.t + 1, self.counts, B, stream=st)
+              self.betas[1], self.eps, self.t + 1, self.counts, B, self.dstat, stream=st)
             launches += LAUNCHES["project_bwd_adam"]
         elif adam:
             T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,
@@ -341,6 +373,9 @@ class Trainer:
         if self.host_out is None:
             self.host_out = (torch.empty((self.batch, 2), dtype=torch.int64).pin_memory(),
                              torch.empty(1, dtype=torch.float32).pin_memory())
+        # the unfused path (more than 16 views) adds to the statistic before the overflow check
+        # can skip anything: keep a copy to restore if the batch has to run again
+        dstat0 = self.dstat.clone() if adam and len(cams) > MAX_FUSED_BATCH else None
         while True:
             res = self._step_async(cams, targets, adam, None, host)
             host = None  # a re-run reuses the uploaded targets
@@ -357,4 +392,6 @@ class Trainer:
                 raise RuntimeError("gs_bin_sort: a device-side wait gave up")
             # overflow: the update was skipped; clear the partial gradients and grow
             self.grads.zero_()
+            if dstat0 is not None:
+                self.dstat.copy_(dstat0)
             self._alloc_sort(int(int(counts[:, 0].max()) * 1.25) + 4096)

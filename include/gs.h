@@ -219,9 +219,13 @@ gs_status gs_render_bwd(const float* proj, int64_t n, const uint32_t* vals, cons
  * with radius > 0 in proj are touched.  Exact derivative of the forward, including the
  * quaternion normalisation, the clamped Jacobian, the view direction of the SH colour
  * and the colour clamp at 0.
+ *   densify_stat  optional device float [n][2] (8-byte aligned), ACCUMULATED: for every
+ *                 Gaussian with radius > 0 in this view, [0] += |(dL/du, dL/dv)| (the length of
+ *                 its screen-space mean gradient, from grad2d) and [1] += 1 -- the statistic
+ *                 gs_densify reads.  NULL: not accumulated.
  */
 gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, const float* proj,
-                         const float* grad2d, float* grads, void* stream);
+                         const float* grad2d, float* grads, float* densify_stat, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_visible_sets -- per-view visible sets and their pairwise overlaps, the inputs of a
@@ -279,13 +283,15 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
  *   exp_avg, exp_avg_sq  Adam moments [15][n][4]; lr, beta1, beta2, eps, step as for
  *              gs_sparse_adam (batch scaling rule included); counts/n_counts likewise
  *              (any nonzero status word skips the whole update).
+ *   densify_stat  optional, as for gs_project_bwd, summed over the batch's views (in view
+ *              order); not touched when the update is skipped.
  * Gaussians visible in no view keep p, m and v bit-for-bit.
  */
 gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_camera* cams, int batch,
                               const float* const* proj_per_view, const float* const* grad2d_per_view,
                               float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
                               float eps, int64_t step, const int64_t* counts, int n_counts,
-                              void* stream);
+                              float* densify_stat, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_probe_ffma -- measurement utility with no counterpart in the method: `blocks` CTAs of
@@ -362,6 +368,39 @@ size_t gs_prune_workspace_size(int64_t n);
 gs_status gs_prune(const float* const* planes_in, int n_sets, int64_t n, float min_logit,
                    float* const* planes_out, int64_t out_stride, void* workspace, size_t workspace_bytes,
                    int64_t* n_keep, int64_t* n_keep_host, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_densify -- the clone / split half of densification (Grendel-GS notes, 训练流程:
+ * "致密化", clone or split the Gaussians that need more detail).  The pages give no
+ * criterion; this library's reading, in its own terms:
+ *   selected   densify_stat[i][1] > 0 and densify_stat[i][0] / densify_stat[i][1] >=
+ *              grad_threshold (fp32): the mean, over the views that saw Gaussian i since the
+ *              statistic was last cleared, of its screen-space mean-gradient length;
+ *   split      a selected Gaussian whose largest log-scale is > log_scale_threshold; the
+ *              others are cloned.
+ * Output, [15][out_stride][4] planes of parameters and both Adam moments: the Gaussians not
+ * split, in index order, moments kept; then, for every selected Gaussian in index order, its
+ * new ones with zero moments: a clone (exact copy of the parameters), or two split children
+ * k = 0, 1 with mean mu + R(q / |q|) (exp(log-scale) * z_k), z_k = normals[i][3k .. 3k + 2],
+ * and log-scales lowered by ln 1.6, the other parameters copied.
+ *   params, exp_avg, exp_avg_sq  [15][n][4], 16-byte aligned.
+ *   densify_stat  [n][2] float (see gs_project_bwd); normals  [n][6] float, the caller's
+ *              standard normal draws (two 3-vectors per Gaussian; only split ones are read).
+ *   *_out      [15][out_stride][4], not overlapping the inputs; NULL with out_stride == 0
+ *              (count only).  Slots at or beyond out_stride are not written.
+ *   workspace  gs_densify_workspace_size(n) bytes, 256-byte aligned.
+ *   counts     device int64[3]: output count, clones, splits (the true counts even above
+ *              out_stride).  counts_host: optional host int64[3]; if non-NULL the call
+ *              synchronises, stores them and returns GS_ERR_CAPACITY if the output count
+ *              exceeds a nonzero out_stride.
+ * A usual pass: once with out_stride = 0 to learn the count, then with out_stride = count.
+ */
+size_t gs_densify_workspace_size(int64_t n);
+gs_status gs_densify(const float* params, const float* exp_avg, const float* exp_avg_sq, int64_t n,
+                     const float* densify_stat, float grad_threshold, float log_scale_threshold,
+                     const float* normals, float* params_out, float* exp_avg_out, float* exp_avg_sq_out,
+                     int64_t out_stride, void* workspace, size_t workspace_bytes, int64_t* counts,
+                     int64_t* counts_host, void* stream);
 
 #ifdef __cplusplus
 }

@@ -177,3 +177,117 @@ def test_trainer_prune_then_step():
     targets = torch.rand((2, 3, cams[0].height, cams[0].width), device="cuda")
     loss = tr.step(cams, targets)  # the resized trainer runs a whole step
     assert np.isfinite(loss) and int(tr.counts[:, 1].abs().sum()) == 0
+
+
+# ------------------------------------------------------------------ densification: clone / split
+def _densify_inputs(n, seed):
+    rng = np.random.default_rng(seed)
+    P = rng.normal(size=(15, n, 4)).astype(np.float32)
+    P[1, :, :3] = rng.uniform(-4.0, -1.0, size=(n, 3))
+    P[1, :, 3] = 0.0
+    M = rng.normal(size=(15, n, 4)).astype(np.float32)
+    V = np.abs(rng.normal(size=(15, n, 4))).astype(np.float32)
+    stat = np.zeros((n, 2), np.float32)
+    stat[:, 1] = rng.integers(0, 5, size=n)
+    stat[:, 0] = (rng.uniform(0, 2e-3, size=n) * stat[:, 1]).astype(np.float32)
+    Z = rng.standard_normal((n, 6)).astype(np.float32)
+    return P, M, V, stat, Z
+
+
+def gpu_densify(P, M, V, stat, thr, lthr, Z):
+    n = P.shape[1]
+    d = [torch.from_numpy(a).cuda() for a in (P, M, V, stat, Z)]
+    ws = torch.empty(max(N.gs_densify_workspace_size(n), 256), dtype=torch.uint8, device="cuda")
+    counts = torch.full((3,), -1, dtype=torch.int64, device="cuda")
+    total, nc, ns = N.gs_densify(d[0], d[1], d[2], n, d[3], thr, lthr, d[4], None, 0, ws, counts, sync=True)
+    outs = [torch.full((15, max(total, 1), 4), 7.0, dtype=torch.float32, device="cuda") for _ in range(3)]
+    if total:
+        N.gs_densify(d[0], d[1], d[2], n, d[3], thr, lthr, d[4], outs, total, ws, counts, sync=True)
+    return (total, nc, ns), [o.cpu().numpy()[:, :total] for o in outs]
+
+
+@pytest.mark.parametrize("n,seed", [(1, 0), (255, 1), (257, 2), (100_000, 3), (1_000_003, 4)])
+def test_densify_matches_oracle(n, seed):
+    """Counts and layout bit-exact (kept Gaussians and clones are copies, new moments zero),
+    split children within the parameter tolerance."""
+    P, M, V, stat, Z = _densify_inputs(n, seed)
+    thr, lthr = float(np.float32(8e-4)), float(np.float32(-2.5))
+    (total, nc, ns), (gp, gm, gv) = gpu_densify(P, M, V, stat, thr, lthr, Z)
+    (op, om, ov), (onc, ons) = oracle.densify(P, M, V, stat, thr, lthr, Z)
+    assert (total, nc, ns) == (op.shape[1], onc, ons)
+    if n >= 1000:
+        assert nc > 0 and ns > 0
+    kept = n - ns
+    n_plain = kept + nc  # kept Gaussians, then the clones and split children in index order
+    new_kind = []
+    cnt = stat[:, 1]
+    avg = np.where(cnt > 0, stat[:, 0] / np.where(cnt > 0, cnt, 1), 0).astype(np.float32)
+    sel = np.nonzero((cnt > 0) & (avg >= np.float32(thr)))[0]
+    for i in sel:
+        new_kind += [1] if P[1, i, :3].max() <= np.float32(lthr) else [2, 2]
+    exact = np.ones(total, bool)
+    exact[kept:][np.array(new_kind, int) == 2] = False  # split children are recomputed in fp32
+    assert np.array_equal(gp[:, exact].astype(np.float64), op[:, exact])
+    assert np.array_equal(gm.astype(np.float64), om) and np.array_equal(gv.astype(np.float64), ov)
+    if (~exact).any():
+        bad = np.abs(gp[:, ~exact] - op[:, ~exact]) > 1e-6 * np.abs(op[:, ~exact]) + 1e-6
+        assert bad.sum() == 0
+    del n_plain
+
+
+def test_densify_statistic_from_the_backward_passes():
+    """gs_project_bwd and the fused gs_project_bwd_adam add |(dL/du, dL/dv)| and one view per
+    visible Gaussian, as the oracle's statistic does on the same screen-space gradients."""
+    P = scenes.make_params(1, n=50_000)
+    cams = [scenes.make_cameras(1)[v] for v in (1, 9, 30)]
+    n = P.shape[1]
+    rng = np.random.default_rng(12)
+    planes, g2ds, want = [], [], np.zeros((n, 2))
+    ok = np.ones(n, bool)  # the kernels recompute the projection: skip decisions on a threshold
+    for cam in cams:
+        pr = oracle.project(P, cam)
+        ok &= pr["margin"] >= 1e-5
+        g2d = (rng.normal(0, 1e-3, size=(n, 9)) * (pr["radius"] > 0)[:, None]).astype(np.float32)
+        planes.append(proj_planes_from_oracle(pr))
+        g2ds.append(g2d)
+        want = oracle.densify_stat(g2d.astype(np.float64), pr["radius"], want)
+    lay = lambda g: np.ascontiguousarray(np.pad(g, ((0, 0), (0, 3)))[:, [0, 1, 5, 9, 2, 3, 4, 10, 6, 7, 8, 11]])
+    dP = torch.from_numpy(P).cuda()
+    stat = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+    grads = torch.zeros((15, n, 4), dtype=torch.float32, device="cuda")
+    for cam, pl, g in zip(cams, planes, g2ds):
+        N.gs_project_bwd(dP, n, cam, torch.from_numpy(pl).cuda(), torch.from_numpy(lay(g)).cuda(), grads, stat)
+    s_seq = stat.cpu().numpy()
+    stat2 = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+    m, v = torch.zeros_like(dP), torch.zeros_like(dP)
+    N.gs_project_bwd_adam(dP.clone(), n, cams, [torch.from_numpy(pl).cuda() for pl in planes],
+                          [torch.from_numpy(lay(g)).cuda() for g in g2ds], m, v, 1e-3, 0.9, 0.999, 1e-15, 1,
+                          densify_stat=stat2)
+    s_fused = stat2.cpu().numpy()
+    torch.cuda.synchronize()
+    for s in (s_seq, s_fused):
+        assert np.array_equal(s[ok, 1], want[ok, 1])
+        assert np.allclose(s[ok, 0], want[ok, 0], rtol=1e-6, atol=1e-12)
+    assert (want[:, 1] == 3).sum() > 1000
+
+
+def test_trainer_densify_then_step():
+    from gaussian_splatting_gb300.trainer import Trainer
+    P = scenes.make_params(1, n=30_000)
+    cams = scenes.make_cameras(1)[:4]
+    tr = Trainer(torch.from_numpy(P).cuda(), cams[0].width, cams[0].height, 4)
+    targets = torch.rand((4, 3, cams[0].height, cams[0].width), device="cuda")
+    for _ in range(2):
+        tr.step(cams, targets)
+    st = tr.dstat.cpu().numpy()
+    assert (st[:, 1] == 8).sum() > 1000  # seen in all four views of both steps
+    avg = st[:, 0] / np.maximum(st[:, 1], 1)
+    thr = float(np.quantile(avg[st[:, 1] > 0], 0.9))  # about a tenth of the seen Gaussians
+    params0 = tr.params.cpu().numpy()
+    total, nc, ns = tr.densify(thr, 0.03, seed=5)
+    assert nc > 0 and ns > 0 and total == 30_000 + nc + ns == tr.n
+    assert tr.params.shape == (15, total, 4) and float(tr.dstat.abs().sum()) == 0.0
+    kept = tr.params.cpu().numpy()[:, : total - nc - 2 * ns]
+    assert np.isin(kept[0, :, 0], params0[0, :, 0]).all()
+    loss = tr.step(cams, targets)  # the grown trainer runs a whole step
+    assert np.isfinite(loss) and int(tr.counts[:, 1].abs().sum()) == 0
