@@ -226,7 +226,7 @@ class OracleSampler:
 
     # host memory the oracle's step holds per Gaussian it is given (double-precision parameters,
     # moments and gradients, and its per-Gaussian records), with slack
-    BYTES_PER_GAUSSIAN = 5000
+    BYTES_PER_GAUSSIAN = 7000
     MAX_BAND_GAUSSIANS = 1_500_000
 
     def __init__(self, cfg_idx: int, P=None, cams=None, jit=None, workers: int | None = None):
@@ -239,7 +239,8 @@ class OracleSampler:
         self.procs = []
         self._info = {}
 
-    def _band(self, k):
+    def _band_idx(self, k):
+        """Band k: its camera, its height and the indices of the Gaussians that can reach it."""
         H = self.cfg.height
         per_view = max(1, H // self.rows)
         view = (k // per_view) % len(self.cams)
@@ -249,7 +250,10 @@ class OracleSampler:
         cam = scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy - r0, c.znear, c.width, rows)
         if view not in self._info:
             self._info[view] = _reach(self.P, c)
-        idx = _band_reach(self._info[view], c.width, r0, rows)
+        return cam, rows, _band_reach(self._info[view], c.width, r0, rows)
+
+    def _band(self, k):
+        cam, rows, idx = self._band_idx(k)
         return self.P[:, idx], self.jit[:, idx], cam, rows
 
     def calibrate(self, budget_s: float):
@@ -266,16 +270,19 @@ class OracleSampler:
         del P, jit, tgt
         self.rows = int(max(16, min(self.cfg.height, 16 * math.floor(budget_s / t16))))
         self.rows = max(16, self.rows // 16 * 16)
-        while self.rows > 16 and self._band(0)[0].shape[1] > self.MAX_BAND_GAUSSIANS:
+        while self.rows > 16 and self._largest_band() > self.MAX_BAND_GAUSSIANS:
             self.rows = max(16, (self.rows // 2) // 16 * 16)
         return self.rows
+
+    def _largest_band(self):
+        return max(len(self._band_idx(k)[2]) for k in range(self.workers))
 
     def start(self):
         import multiprocessing as mp
 
         # as many processes as host cores, and as the available memory holds (a band is made,
         # handed to its process and dropped before the next one)
-        need = self._band(0)[0].shape[1] * self.BYTES_PER_GAUSSIAN
+        need = self._largest_band() * self.BYTES_PER_GAUSSIAN
         fit = max(1, int(0.5 * available_host_bytes() // max(need, 1)))
         self.workers = min(self.workers, fit)
         ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
