@@ -242,9 +242,11 @@ class OracleSampler:
     def _band_idx(self, k):
         """Band k: its camera, its height and the indices of the Gaussians that can reach it."""
         H = self.cfg.height
-        per_view = max(1, H // self.rows)
+        # the processes' bands spread evenly over the image height (the content of a view is not
+        # uniform: the top rows of a city view see little), then over the next views
+        per_view = max(1, min(H // self.rows, self.workers))
         view = (k // per_view) % len(self.cams)
-        r0 = (k % per_view) * self.rows
+        r0 = min(((k % per_view) * H // per_view) // 16 * 16, max(0, H - self.rows))
         rows = min(self.rows, H - r0)
         c = self.cams[view]
         cam = scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy - r0, c.znear, c.width, rows)
@@ -262,7 +264,7 @@ class OracleSampler:
         import oracle
 
         self.rows = 16
-        P, jit, cam, rows = self._band(0)
+        P, jit, cam, rows = self._band(self.workers // 2)  # a band in the middle of the view
         tgt = oracle.render_view(jit, cam)[None]
         t0 = time.perf_counter()
         oracle.step(P, np.zeros_like(P), np.zeros_like(P), [cam], tgt, lr=self.cfg.lr, eps=self.cfg.eps)
@@ -319,8 +321,8 @@ class OracleSampler:
     def describe(self, wall):
         return (f"{self.workers} processes (one per host core), each the oracle's whole step (project, bin, "
                 f"composite, loss, backward, Adam; batch 1, double precision) on its own band of {self.rows} rows "
-                f"at full width (bands of view 0, then the next views) with the Gaussians that can reach it; "
-                f"{wall:.1f} s per round")
+                f"at full width (bands spread evenly over the height of view 0, then of the next views) with the "
+                f"Gaussians that can reach it; {wall:.1f} s per round")
 
 
 # ---------------------------------------------------------------------- main
