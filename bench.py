@@ -52,7 +52,17 @@ HBM_FALLBACK_GBS = 6800.0
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
 # keyed by entry point and workload, valid only for the kernel source it was measured on: when
 # the source file's hash differs the figure is reported as null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # one launch on the 300K-Gaussian 1236x820 view: 38.308 MB read + 0.052 MB written
+    ("render_bwd", "object-300k-1236x820"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
+                                             "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
+                                             "bytes": 38359552},
+    # one launch on a 10M-Gaussian 3840x2160 view of the city layout (55.2M instances): 1.875 GB
+    # read + 0.146 GB written, scaled by the instances to the 40M view's 216.2M (x 3.914)
+    ("render_bwd", "city-40m-3840x2160"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
+                                           "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
+                                           "bytes": 7910000000, "scaled_from": "10M-Gaussian capture, by instances"},
+}
 
 
 def fp32_peak_tflops(sm_count: int, sm_max_mhz: float) -> float:
@@ -350,6 +360,78 @@ def log(msg: str):
     print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
 
 
+def kernels_mode(args):
+    """One view of the workload's first camera (project, bin and sort, composite, loss,
+    composite backward), every call timed on its own with CUDA events (best of --steps after
+    --warmup).  The scene can be drawn smaller (--gaussians) so that a profiler capture holds
+    a few GB on the device.  Prints one JSON line of per-call milliseconds."""
+    import torch
+    from gaussian_splatting_gb300 import _native as N
+
+    cfg = scenes.CONFIGS[args.config]
+    n = args.gaussians or cfg.n
+    P = scenes.make_params(args.config, n=n)
+    cam = scenes.make_cameras(args.config)[0]
+    W, H = cam.width, cam.height
+    Pd = torch.from_numpy(P).cuda()
+    proj = torch.zeros((3, n, 4), dtype=torch.float32, device="cuda")
+    N.gs_project(Pd, n, cam, proj)
+    torch.cuda.synchronize()
+    M = int(proj[2, :, 3].contiguous().view(torch.int32).long().sum())
+    cap = M + 4096
+    vals = torch.empty(cap, dtype=torch.int32, device="cuda")
+    ranges = torch.zeros((cam.tiles_x * cam.tiles_y, 2), dtype=torch.int32, device="cuda")
+    counts = torch.zeros((1, 2), dtype=torch.int64, device="cuda")
+    wsb = N.gs_bin_sort_batch_workspace_size(1, n, cap, [cam])
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    img = torch.empty((3, H, W), device="cuda")
+    Tf = torch.empty((H, W), device="cuda")
+    nc = torch.empty((H, W), dtype=torch.int32, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3000 + args.config)
+    tgt = torch.rand((3, H, W), device="cuda", generator=gen)
+    dimg = torch.empty((3, H, W), device="cuda")
+    lws = torch.empty(N.gs_loss_workspace_size(W, H), dtype=torch.uint8, device="cuda")
+    loss = torch.zeros(1, device="cuda")
+    g2d = torch.zeros((n, 12), device="cuda")
+    calls = {
+        "project": lambda: N.gs_project(Pd, n, cam, proj),
+        "bin_sort": lambda: N.gs_bin_sort_batch([proj], n, [cam], ws, wsb, None, [vals], cap, [ranges], counts),
+        "render_fwd": lambda: N.gs_render_fwd(proj, n, vals, ranges, cam, None, img, Tf, nc),
+        "loss": lambda: N.gs_loss(img, tgt, W, H, 0.8, 0.2, 1.0, loss, False, dimg, lws, lws.numel()),
+        "render_bwd": lambda: N.gs_render_bwd(proj, n, vals, ranges, cam, None, Tf, nc, dimg, g2d),
+    }
+    # the batch's fused projection backward + Adam, every view with its own projection and a
+    # copy of view 0's screen-space gradients
+    B = min(cfg.batch, 16)
+    bcams = scenes.make_cameras(args.config)[:B]
+    bprojs = [torch.zeros((3, n, 4), dtype=torch.float32, device="cuda") for _ in range(B)]
+    N.gs_project_batch(Pd, n, bcams, bprojs)
+    g2ds = [g2d.clone() for _ in range(B)]
+    m_, v_ = torch.zeros_like(Pd), torch.zeros_like(Pd)
+    Pu = Pd.clone()
+    stat = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+    calls["project_bwd_adam"] = lambda: N.gs_project_bwd_adam(Pu, n, bcams, bprojs, g2ds, m_, v_, 1e-3, 0.9, 0.999,
+                                                              1e-15, 1, densify_stat=stat)
+    for _ in range(max(1, args.warmup)):
+        for f in calls.values():
+            f()
+    torch.cuda.synchronize()
+    res = {"workload": cfg.name, "gaussians": n, "instances": M, "status": counts.cpu().tolist()}
+    for name, f in calls.items():
+        best = None
+        for _ in range(max(1, args.steps)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            best = a.elapsed_time(b) if best is None else min(best, a.elapsed_time(b))
+        res[name + "_ms"] = round(best, 4)
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,7 +441,12 @@ def main():
     ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernels", action="store_true",
+                    help="time the stage calls of one view of the workload (for profiler captures)")
+    ap.add_argument("--gaussians", type=int, default=0, help="with --kernels: draw this many Gaussians instead")
     args = ap.parse_args()
+    if args.kernels:
+        return kernels_mode(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
