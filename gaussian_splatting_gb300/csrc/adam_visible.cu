@@ -288,8 +288,7 @@ extern "C" gs_status gs_visible_sets(const float* const* proj_per_view, int batc
     dim3 gw((unsigned)nblk, (unsigned)(batch + 1));
     k_vis_write<<<gw, kWordsPerBlock, 0, st>>>(batch, nwords, nblk, w.bits, w.blkcnt, offsets, indices, union_idx);
     const size_t smem = sizeof(uint32_t) * 256 * batch;
-    const cudaError_t attr =  // per call: the attribute belongs to the current device
-        cudaFuncSetAttribute(k_vis_inter, cudaFuncAttributeMaxDynamicSharedMemorySize, 256 * 4 * kMaxViews);
+    const cudaError_t attr = gs::max_dynamic_smem((const void*)k_vis_inter, 256 * 4 * kMaxViews);
     if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_visible_sets: %s", cudaGetErrorString(attr));
     k_vis_inter<<<(unsigned)((nwords + 255) / 256), 256, smem, st>>>(batch, nwords, w.bits,
                                                                      reinterpret_cast<unsigned long long*>(inter));

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -34,6 +35,35 @@ gs_status check_launch(const char* what) {
 int64_t wait_limit() { return g_wait_limit.load(); }
 
 int take_drop_publish() { return g_drop_publish.exchange(0); }
+
+cudaError_t max_dynamic_smem(const void* fn, int bytes) {
+  // the attribute belongs to a device: remembered per device (and kernel, and size), so
+  // that the driver call is made once per device rather than on every launch
+  constexpr int kMaxDev = 64, kMaxEntries = 32;
+  struct Entry {
+    const void* fn;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Entry done[kMaxDev][kMaxEntries];
+  static int used[kMaxDev] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used[dev]; ++i)
+    if (done[dev][i].fn == fn && done[dev][i].bytes >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) {
+    for (int i = 0; i < used[dev]; ++i)
+      if (done[dev][i].fn == fn) {
+        done[dev][i].bytes = bytes;
+        return e;
+      }
+    if (used[dev] < kMaxEntries) done[dev][used[dev]++] = Entry{fn, bytes};
+  }
+  return e;
+}
 
 int num_sms() {
   int dev = 0, n = 0;

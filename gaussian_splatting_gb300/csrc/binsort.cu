@@ -47,7 +47,13 @@ constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kDepthItems = 4;    // depth passes: 1024 keys per radix tile (N is modest)
 constexpr int64_t kWideDepthN = 2000000;  // from this many Gaussians on, 3072 keys per radix tile
-constexpr int kTileItems = 12;    // tile passes: 3072 keys per radix tile (M is large)
+#ifndef GS_TILE_ITEMS
+#define GS_TILE_ITEMS 12
+#endif
+#ifndef GS_SORT_MIN_BLOCKS
+#define GS_SORT_MIN_BLOCKS 4
+#endif
+constexpr int kTileItems = GS_TILE_ITEMS;  // tile passes: 3072 keys per radix tile (M is large)
 constexpr int kSlice = kSortThreads * kTileItems;  // instances per generated radix tile
 constexpr int kDepthPasses = 4;
 constexpr int kMaxSortViews = 8;  // views per sort launch
@@ -627,12 +633,18 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       if (gen) {
         gen_digit_counts(S, J, tile, base, nvalid, M);
       } else {
-        // the counts need the keys only
+        // the counts need the keys only: all of a thread's loads in flight, then the counts
         const bool full = nvalid == kTile;
+        uint32_t k[ITEMS];
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i) {
           const int li = warp * (ITEMS * 32) + i * 32 + lane;
-          if (full || li < nvalid) atomicAdd(&S.tstart[(__ldcg(&kin[base + li]) >> shift) & 255u], 1u);
+          k[i] = (full || li < nvalid) ? __ldcg(&kin[base + li]) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+          const int li = warp * (ITEMS * 32) + i * 32 + lane;
+          if (full || li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
         }
         __syncthreads();
       }
@@ -801,19 +813,30 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     depth_scan(S, J, G, bid, nbar);
   } else {
     // the staged ranges: tile t's run of sorted instances starts where the tile id changes
-    // (the host zeroed them, so empty tiles keep [0, 0)); a lane's neighbours come from the
-    // lanes beside it, the warp's edges from one more load
+    // (the host zeroed them, so empty tiles keep [0, 0)).  Four sorted ids per thread in one
+    // 16-byte load (the buffer is 256-byte aligned and its padding covers the last group); a
+    // thread's neighbours come from the lanes beside it, a warp's edges from one more load.
     const uint32_t* skey = J.key[J.passes & 1];
-    const int64_t span = (M + 31) / 32 * 32;  // whole warps, so the shuffles see every lane
-    for (int64_t g = (int64_t)bid * kSortThreads + tid; g < span; g += (int64_t)G * kSortThreads) {
-      const bool in = g < M;
-      const uint32_t t = in ? __ldcg(&skey[g]) : 0xFFFFFFFFu;
-      uint32_t prev = __shfl_up_sync(0xffffffffu, t, 1);
-      uint32_t next = __shfl_down_sync(0xffffffffu, t, 1);
-      if (lane == 0) prev = g > 0 && g - 1 < M ? __ldcg(&skey[g - 1]) : 0xFFFFFFFFu;
-      if (lane == 31) next = g + 1 < M ? __ldcg(&skey[g + 1]) : 0xFFFFFFFFu;
-      if (in && (g == 0 || prev != t)) J.rstage[2 * (int64_t)t] = (uint32_t)g;
-      if (in && (g == M - 1 || next != t)) J.rstage[2 * (int64_t)t + 1] = (uint32_t)(g + 1);
+    const uint4* sk4 = reinterpret_cast<const uint4*>(skey);
+    const int64_t n4 = (M + 3) / 4;
+    const int64_t span = (n4 + 31) / 32 * 32;  // whole warps, so the shuffles see every lane
+    for (int64_t q = (int64_t)bid * kSortThreads + tid; q < span; q += (int64_t)G * kSortThreads) {
+      const bool in = q < n4;
+      const uint4 v4 = in ? __ldcg(&sk4[q]) : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+      uint32_t e[6];
+      e[0] = __shfl_up_sync(0xffffffffu, v4.w, 1);
+      e[5] = __shfl_down_sync(0xffffffffu, v4.x, 1);
+      if (lane == 0) e[0] = in && q > 0 ? __ldcg(&skey[4 * q - 1]) : 0xFFFFFFFFu;
+      if (lane == 31) e[5] = in && 4 * q + 4 < M ? __ldcg(&skey[4 * q + 4]) : 0xFFFFFFFFu;
+      e[1] = v4.x; e[2] = v4.y; e[3] = v4.z; e[4] = v4.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t g = 4 * q + j;
+        if (!in || g >= M) break;
+        const uint32_t t = e[j + 1];
+        if (g == 0 || e[j] != t) J.rstage[2 * (int64_t)t] = (uint32_t)g;
+        if (g == M - 1 || e[j + 2] != t) J.rstage[2 * (int64_t)t + 1] = (uint32_t)(g + 1);
+      }
     }
   }
 }
@@ -829,13 +852,16 @@ __global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort(const __grid_con
 
 // The same with radix tiles of kTileItems keys, for large N: fewer tiles, so fewer digit
 // counts to scan and less fixed work per key.
-__global__ void __launch_bounds__(kSortThreads, 4) k_depth_sort_wide(const __grid_constant__ RadixBatch B) {
+__global__ void __launch_bounds__(kSortThreads, GS_SORT_MIN_BLOCKS) k_depth_sort_wide(const __grid_constant__ RadixBatch B) {
   const uint32_t G = gridDim.x / (uint32_t)B.views;
   const uint32_t view = blockIdx.x / G;
   radix_body<kTileItems, false>(B.job[view], G, blockIdx.x - view * G);
 }
 
-__global__ void __launch_bounds__(kSortThreads, 4) k_tile_sort(const __grid_constant__ RadixBatch B) {
+#ifndef GS_TILE_MIN_BLOCKS
+#define GS_TILE_MIN_BLOCKS GS_SORT_MIN_BLOCKS
+#endif
+__global__ void __launch_bounds__(kSortThreads, GS_TILE_MIN_BLOCKS) k_tile_sort(const __grid_constant__ RadixBatch B) {
   const uint32_t G = gridDim.x / (uint32_t)B.views;
   const uint32_t view = blockIdx.x / G;
   radix_body<kTileItems, true>(B.job[view], G, blockIdx.x - view * G);
@@ -874,8 +900,7 @@ __global__ void k_publish_ranges(const __grid_constant__ ViewBuffers B) {
 }
 
 // Resident CTAs per SM of a sort kernel for a given dynamic shared-memory size on the current
-// device.  The shared-memory attribute is set on every call (it belongs to the device and is
-// lost if the device resets); the occupancy answer is cached per device and size.
+// device (the shared-memory attribute and the occupancy answer are both kept per device).
 template <int kKernel>  // 0: depth sort, 1: tile sort, 2: depth sort with wide radix tiles
 int radix_blocks_per_sm(size_t smem) {
   constexpr int kMaxDev = 64;
@@ -884,7 +909,7 @@ int radix_blocks_per_sm(size_t smem) {
   static int cached[kMaxDev] = {0};
   const void* fn = kKernel == 1 ? (const void*)k_tile_sort
                                 : (kKernel == 2 ? (const void*)k_depth_sort_wide : (const void*)k_depth_sort);
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  gs::max_dynamic_smem(fn, (int)smem);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
   std::lock_guard<std::mutex> lock(mu);

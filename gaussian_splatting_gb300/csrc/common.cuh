@@ -17,6 +17,9 @@ gs_status check_launch(const char* what);
 int64_t wait_limit();
 int take_drop_publish();
 int num_sms();
+// cudaFuncSetAttribute(fn, MaxDynamicSharedMemorySize, bytes) for the current device, made once
+// per device (and kernel) -- the attribute is per device, so a second device gets its own call
+cudaError_t max_dynamic_smem(const void* fn, int bytes);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }

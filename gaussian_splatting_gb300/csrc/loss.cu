@@ -334,9 +334,7 @@ extern "C" gs_status gs_loss(const float* image, const float* target, int width,
   const size_t need = gs_loss_workspace_size(width, height);
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_loss: workspace %zu bytes < %zu needed", workspace_bytes, need);
-  // set on every call: the attribute belongs to the current device (and is lost if it resets)
-  const cudaError_t attr =
-      cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
+  const cudaError_t attr = gs::max_dynamic_smem((const void*)k_loss_fused, (int)sizeof(LossSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss: %s", cudaGetErrorString(attr));
   cudaStream_t st = gs::as_stream(stream);
   const double n = 3.0 * (double)width * (double)height;
@@ -406,8 +404,7 @@ extern "C" gs_status gs_loss_noalloc(const float* image, const float* target, in
                          width, height, (long long)nblk, (long long)kNoAllocMaxBlocks, (long long)kNoAllocMaxBlocks);
   float* partials = nullptr;
   if (gs_status s = scratch_address(&partials)) return s;
-  const cudaError_t attr =
-      cudaFuncSetAttribute(k_loss_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(LossSmem));
+  const cudaError_t attr = gs::max_dynamic_smem((const void*)k_loss_fused, (int)sizeof(LossSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_loss_noalloc: %s", cudaGetErrorString(attr));
   cudaStream_t st = gs::as_stream(stream);
   const double n = 3.0 * (double)width * (double)height;

@@ -707,9 +707,7 @@ extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_came
   const double bc1 = 1.0 - std::pow(b1, (double)step), bc2 = 1.0 - std::pow(b2, (double)step);
   const AdamHyper h{(float)b1, (float)b2, eps, (float)(lr_b / bc1), (float)(1.0 / bc2)};
   const unsigned blocks = (unsigned)((n + kAdamThreads - 1) / kAdamThreads);
-  // set on every call: the attribute belongs to the current device
-  const cudaError_t attr = cudaFuncSetAttribute(k_project_bwd_adam, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       (int)sizeof(AdamSmem));
+  const cudaError_t attr = gs::max_dynamic_smem((const void*)k_project_bwd_adam, (int)sizeof(AdamSmem));
   if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_project_bwd_adam: %s", cudaGetErrorString(attr));
   if (densify_stat && !gs::aligned8(densify_stat))
     return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: densify_stat must be 8-byte aligned");
