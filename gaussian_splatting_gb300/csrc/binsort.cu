@@ -21,9 +21,10 @@
 //                 every tile in shared memory and writes digit-contiguous runs at the digit's
 //                 base (an exclusive scan of the totals) plus its column offset; grid
 //                 barriers (per view) separate the phases.  Phase 0 makes the depth keys
-//                 (0xFFFFFFFF for culled Gaussians) and an 8-byte tile-rectangle record per
-//                 Gaussian.  After the passes the same launch runs the tiles-touched scan over
-//                 the sorted Gaussians (reduce, scan of the chunk sums, then each chunk's
+//                 and an 8-byte tile-rectangle record per visible Gaussian; pass 0 leaves the
+//                 culled ones out, so the later passes move only the visible keys.  After the
+//                 passes the same launch runs the tiles-touched scan over the sorted visible
+//                 Gaussians (reduce, scan of the chunk sums, then each chunk's
 //                 records: first slot, rectangle, index; and for every radix tile of the tile
 //                 sort the Gaussian holding its first slot).
 //   k_tile_sort   the same passes for one view's instances by tile id: the first pass
@@ -59,7 +60,10 @@ constexpr int kDepthPasses = 4;
 constexpr int kMaxSortViews = 8;  // views per sort launch
 // views whose tile sorts share a launch: as many as have their own capacity-sized ping-pong
 // buffers within this budget (at least one, at most kMaxSortViews)
-constexpr double kTileBudgetBytes = 1024.0 * 1024.0 * 1024.0;
+#ifndef GS_TILE_BUDGET_MB
+#define GS_TILE_BUDGET_MB 1024
+#endif
+constexpr double kTileBudgetBytes = GS_TILE_BUDGET_MB * 1024.0 * 1024.0;
 constexpr int kMaxTilePasses = 4;
 constexpr int kSlots = kDepthPasses + kMaxTilePasses;  // digit histogram / base slots
 
@@ -67,6 +71,7 @@ constexpr uint32_t kCulledKey = 0xFFFFFFFFu;
 
 // layout of the small, memset-cleared block of the workspace (32-bit words)
 constexpr int kSmBarrier = 1;        // one arrival counter per sort (depth, tile)
+constexpr int kSmVisible = 3;        // the depth sort's count of visible Gaussians, for the tile sort
 constexpr int kSmHist = 32;          // kSlots * 256 digit totals (the column sums of phase B)
 constexpr int kSmWords = kSmHist + kSlots * 256;
 
@@ -176,7 +181,9 @@ struct SortSmem {
   uint32_t gbase[256];
   uint32_t dbase[256];  // the pass's digit bases
   uint32_t wsum[kSortWarps];
-  uint32_t full;  // first tile pass, counts: full cycles of 256 digits
+  uint32_t full;    // first tile pass, counts: full cycles of 256 digits
+  uint32_t total;   // the pass's key count (sum of the digit totals)
+  uint32_t tvalid;  // phase C: keys of the current radix tile that take part in the pass
   int fail;
 };
 
@@ -187,8 +194,7 @@ struct SortSmem {
 // the owner's rectangle record gives the tile id.
 struct GenSource {
   const uint32_t* slice_first;  // per radix tile: the Gaussian holding its first slot
-  const uint4* grec;            // per depth-ordered Gaussian: (offset, x0 | y0 << 16, w | h << 16, index)
-  int64_t n;
+  const uint4* grec;            // per depth-ordered visible Gaussian: (offset, x0 | y0 << 16, w | h << 16, index)
   int Tx;
 };
 
@@ -265,32 +271,34 @@ __device__ bool grid_barrier(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t tar
   return S.fail == 0;
 }
 
-// Keys (and values) of radix tile `tile`, warp-striped: item i of lane l of warp w is slot
-// w * ITEMS * 32 + i * 32 + l.  Slots past nvalid get key 0xFFFFFFFF.
+// 32-bit words of radix tile `tile` of an M-word array, warp-striped: item i of lane l of warp
+// w is slot w * ITEMS * 32 + i * 32 + l; slots past M read nothing and get 0.
 template <int ITEMS>
-__device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J, bool gen, const uint32_t* kin,
-                                          const uint32_t* vin, int64_t tile, int64_t base, int nvalid,
-                                          uint32_t (&k)[ITEMS], uint32_t (&v)[ITEMS]) {
+__device__ __forceinline__ void load_words(const uint32_t* in, int64_t tile, int64_t M, uint32_t (&x)[ITEMS]) {
+  constexpr int kTile = kSortThreads * ITEMS;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t base = tile * kTile;
+  const int64_t nvalid = min((int64_t)kTile, M - base);
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int li = warp * (ITEMS * 32) + i * 32 + lane;
+    x[i] = li < nvalid ? __ldcg(&in[base + li]) : 0u;
+  }
+}
+
+// The keys (tile ids) and values (Gaussian indices) of radix tile `tile` of the first tile
+// pass, generated in the warp-striped order of load_words.  Slots past nvalid get key
+// 0xFFFFFFFF.
+template <int ITEMS>
+__device__ __forceinline__ void gen_tile(SortSmem<ITEMS>& S, const RadixJob& J, int64_t tile, int64_t base,
+                                         int nvalid, uint32_t (&k)[ITEMS], uint32_t (&v)[ITEMS]) {
   constexpr int kTile = kSortThreads * ITEMS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int wbase = warp * (ITEMS * 32);
   const bool full = nvalid == kTile;
-  if (!gen) {
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      const int li = wbase + i * 32 + lane;
-      if (full || li < nvalid) {
-        k[i] = kin[base + li];
-        v[i] = vin[base + li];
-      } else {
-        k[i] = 0xFFFFFFFFu;
-        v[i] = 0u;
-      }
-    }
-    return;
-  }
   uint32_t* own = S.keys;  // free until the scatter
   const GenSource& G = J.gen;
+  const int64_t gn = __ldg(&J.small[kSmVisible]);  // depth-ordered visible Gaussians (previous launch)
   const int64_t first = (int64_t)__ldg(&G.slice_first[tile]);
   for (int i = tid; i < kTile; i += kSortThreads) own[i] = 0u;
   __syncthreads();
@@ -300,10 +308,10 @@ __device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J,
   const uint32_t end = (uint32_t)(base + nvalid);
   for (int e0 = 0;; e0 += kSortThreads) {
     const int64_t it = first + e0 + tid;
-    const uint32_t off = it < G.n ? __ldg(&G.grec[it]).x : 0xFFFFFFFFu;
+    const uint32_t off = it < gn ? __ldg(&G.grec[it]).x : 0xFFFFFFFFu;
     const bool first_item = e0 + tid == 0;
     const bool in = first_item || off < end;
-    if (in && it < G.n) atomicMax(&own[first_item ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
+    if (in && it < gn) atomicMax(&own[first_item ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
     if (!__syncthreads_or(!first_item && off < end)) break;
   }
   {  // inclusive max-scan of the marks, ITEMS consecutive slots per thread
@@ -334,7 +342,7 @@ __device__ __forceinline__ void load_tile(SortSmem<ITEMS>& S, const RadixJob& J,
   for (int i = 0; i < ITEMS; ++i) {
     const int li = wbase + i * 32 + lane;
     const uint32_t o = own[li];
-    if ((full || li < nvalid) && o != 0u && first + o - 1u < G.n) {
+    if ((full || li < nvalid) && o != 0u && first + o - 1u < gn) {
       const uint4 rec = __ldg(&G.grec[first + o - 1u]);
       const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
       const uint32_t w = max(rec.z & 0xffffu, 1u);
@@ -362,6 +370,7 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
                                                  int nvalid, int64_t M) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GenSource& G = J.gen;
+  const int64_t gn = __ldg(&J.small[kSmVisible]);  // depth-ordered visible Gaussians (previous launch)
   uint32_t* diff = S.tstart;  // zeroed by the caller
   if (tid == 0) S.full = 0u;
   __syncthreads();
@@ -370,12 +379,12 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
   for (int e0 = 0;; e0 += kSortThreads) {
     const int64_t it = first + e0 + tid;
     bool more = false;
-    if (it < G.n) {
+    if (it < gn) {
       const uint4 rec = __ldg(&G.grec[it]);
       const uint32_t off = rec.x;
       more = off < end;
       if (more || e0 + tid == 0) {
-        const uint32_t next = it + 1 < G.n ? __ldg(&G.grec[it + 1]).x : (uint32_t)M;
+        const uint32_t next = it + 1 < gn ? __ldg(&G.grec[it + 1]).x : (uint32_t)M;
         const uint32_t s_lo = max(off, lo), s_hi = min(next, end);
         const uint32_t w = max(rec.z & 0xffffu, 1u);
         if (s_lo < s_hi) {
@@ -421,8 +430,9 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
 }
 
 // Depth sort, phase 0 (replaces phase A of pass 0): radix tile by radix tile, the depth key of
-// every Gaussian (float bits of z; 0xFFFFFFFF if culled), its index, its tile-rectangle record
-// and the tile's pass-0 digit counts.
+// every Gaussian (float bits of z; 0xFFFFFFFF if culled), its index, the tile-rectangle record
+// of every visible one and the tile's pass-0 digit counts of the visible keys only: pass 0
+// drops the culled Gaussians, so the later passes and the scan see only the visible ones.
 template <int ITEMS>
 __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, int64_t ntiles,
                                              uint32_t G, uint32_t bid) {
@@ -445,14 +455,14 @@ __device__ __forceinline__ void depth_phase0(SortSmem<ITEMS>& S, const RadixJob&
         const int fv = (int)floorf(fminf(fmaxf(a.y, -1e9f), 1e9f));
         const int x0 = min(max((fu - r) >> 4, 0), J.Tx), x1 = min(max(((fu + r) >> 4) + 1, 0), J.Tx);
         const int y0 = min(max((fv - r) >> 4, 0), J.Ty), y1 = min(max(((fv + r) >> 4) + 1, 0), J.Ty);
-        key = __float_as_uint(a.z);
+        key = __float_as_uint(a.z);  // finite and positive: never the culled key
         if (x0 < x1 && y0 < y1)
           rec = make_uint2((uint32_t)x0 | ((uint32_t)y0 << 16), (uint32_t)(x1 - x0) | ((uint32_t)(y1 - y0) << 16));
+        J.rrec[i] = rec;
+        atomicAdd(&S.tstart[key & 255u], 1u);
       }
       J.key[0][i] = key;
       J.val[0][i] = (uint32_t)i;
-      J.rrec[i] = rec;
-      atomicAdd(&S.tstart[key & 255u], 1u);
     }
     __syncthreads();
     J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
@@ -482,7 +492,7 @@ __device__ __forceinline__ unsigned long long block_sum(SortSmem<ITEMS>& S, uint
   return t;
 }
 
-// After the depth passes: the tiles-touched scan over the sorted Gaussians.  S1: every sorted
+// After the depth passes: the tiles-touched scan over the n sorted visible Gaussians.  S1: every sorted
 // Gaussian's record (gathered once, by index, from the rectangle records) and the sum of every
 // chunk of kScanChunk of them.  S2 (only for more than kDirectChunks chunks): CTA 0 turns the
 // sums into exclusive prefixes.  S3: every chunk's first slots (its prefix summed directly from
@@ -491,10 +501,10 @@ __device__ __forceinline__ unsigned long long block_sum(SortSmem<ITEMS>& S, uint
 constexpr int64_t kDirectChunks = 4096;
 
 template <int ITEMS>
-__device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t G, uint32_t bid, uint32_t& nbar) {
+__device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, uint32_t G, uint32_t bid,
+                           uint32_t& nbar) {
   constexpr int kPer = kScanChunk / kSortThreads;  // 4 consecutive Gaussians per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t n = J.n_host;
   const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
   const bool direct = nchunks <= kDirectChunks;
   const uint32_t* sidx = J.val[kDepthPasses & 1];
@@ -611,8 +621,8 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmem<ITEMS>& S = *reinterpret_cast<SortSmem<ITEMS>*>(smem_raw);
   if (J.count[1] != 0) return;
-  const int64_t M = J.n_host >= 0 ? J.n_host : min(J.count[0], J.cap);
-  const int64_t ntiles = sort_tiles<ITEMS>(M);
+  int64_t M = J.n_host >= 0 ? J.n_host : min(J.count[0], J.cap);  // keys of the pass (depth: visible after pass 0)
+  int64_t ntiles = sort_tiles<ITEMS>(M);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.peer[0][0])[i] = 0u;
@@ -621,35 +631,42 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     const int shift = 8 * p;
     const bool gen = kTileSort && p == 0;
     const bool fin = kTileSort && p == J.passes - 1;
+    const bool compact = !kTileSort && p == 0;  // drops the culled keys
     const uint32_t* kin = J.key[p & 1];
     const uint32_t* vin = J.val[p & 1];
     // ---- A: digit counts of every radix tile
     if (!kTileSort && p == 0) depth_phase0(S, J, J.n_host, ntiles, G, bid);
-    for (int64_t tile = bid; tile < ntiles && (kTileSort || p > 0); tile += G) {
-      for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
-      __syncthreads();
-      const int64_t base = tile * kTile;
-      const int nvalid = (int)min((int64_t)kTile, M - base);
-      if (gen) {
-        gen_digit_counts(S, J, tile, base, nvalid, M);
-      } else {
-        // the counts need the keys only: all of a thread's loads in flight, then the counts
-        const bool full = nvalid == kTile;
-        uint32_t k[ITEMS];
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) {
-          const int li = warp * (ITEMS * 32) + i * 32 + lane;
-          k[i] = (full || li < nvalid) ? __ldcg(&kin[base + li]) : 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) {
-          const int li = warp * (ITEMS * 32) + i * 32 + lane;
-          if (full || li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
-        }
+    if (gen) {
+      for (int64_t tile = bid; tile < ntiles; tile += G) {
+        for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
+        __syncthreads();
+        const int64_t base = tile * kTile;
+        gen_digit_counts(S, J, tile, base, (int)min((int64_t)kTile, M - base), M);
+        J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
         __syncthreads();
       }
-      J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
-      __syncthreads();
+    } else if (kTileSort || p > 0) {
+      // the counts need the keys only; the next radix tile's keys are in flight while this
+      // one's are counted
+      uint32_t k[ITEMS];
+      load_words<ITEMS>(kin, bid, M, k);
+      for (int64_t tile = bid; tile < ntiles; tile += G) {
+        for (int i = tid; i < 256; i += kSortThreads) S.tstart[i] = 0u;
+        __syncthreads();
+        const int nvalid = (int)min((int64_t)kTile, M - tile * kTile);
+        uint32_t kn[ITEMS];
+        load_words<ITEMS>(kin, tile + G, M, kn);
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+          const int li = warp * (ITEMS * 32) + i * 32 + lane;
+          if (li < nvalid) atomicAdd(&S.tstart[(k[i] >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        J.hist[(int64_t)tid * J.hist_stride + tile] = S.tstart[tid];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) k[i] = kn[i];
+      }
     }
     ++nbar;
     if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && bid == 0))) return;
@@ -707,6 +724,10 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       uint32_t woff = 0;
       for (int w = 0; w < warp; ++w) woff += S.wsum[w];
       S.dbase[tid] = woff + incl - c;
+      if (tid == 255) {
+        S.total = woff + incl;
+        if (compact && bid == 0) J.small[kSmVisible] = woff + incl;
+      }
       __syncthreads();
     }
     // ---- C: rank within the tile, scatter through shared memory, digit-contiguous writes
@@ -719,17 +740,29 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       __syncthreads();
       const int64_t base = tile * kTile;
       const int nvalid = (int)min((int64_t)kTile, M - base);
-      const bool full = nvalid == kTile;
+      const bool full = nvalid == kTile && !compact;
+      // (loading the next tile's keys during this one's write-out was measured slower: the
+      // extra live registers spill)
       uint32_t k[ITEMS], v[ITEMS], rank[ITEMS];
-      load_tile<ITEMS>(S, J, gen, kin, vin, tile, base, nvalid, k, v);
+      if (gen) {
+        gen_tile<ITEMS>(S, J, tile, base, nvalid, k, v);
+      } else {
+        load_words<ITEMS>(kin, tile, M, k);
+        load_words<ITEMS>(vin, tile, M, v);
+      }
       const int wbase = warp * (ITEMS * 32);
+      uint32_t vbits = 0;  // bit i: item i takes part (in range; in pass 0 of the depth sort, visible)
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) {
+        const int li = wbase + i * 32 + lane;
+        if (full || (li < nvalid && !(compact && k[i] == kCulledKey))) vbits |= 1u << i;
+      }
       // peer masks of all items first, then the per-warp counts in item order; rank[] holds
       // the peer mask until it is replaced by the rank.  Peers: every lane ORs its bit into
       // its digit's word of a per-warp shared-memory table, reads the word back and clears it.
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
-        const int li = wbase + i * 32 + lane;
-        const bool valid = full || li < nvalid;
+        const bool valid = (vbits >> i) & 1u;
         const uint32_t d = (k[i] >> shift) & 255u;
         if (valid) atomicOr(&S.peer[warp][d], 1u << lane);
         __syncwarp();
@@ -740,8 +773,7 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       }
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
-        const int li = wbase + i * 32 + lane;
-        const bool valid = full || li < nvalid;
+        const bool valid = (vbits >> i) & 1u;
         const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
         if (valid) {
           const uint32_t d = (k[i] >> shift) & 255u;
@@ -776,12 +808,12 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         uint32_t woff = 0;
         for (int w = 0; w < warp; ++w) woff += S.wsum[w];
         S.tstart[d] = woff + incl - cnt;
+        if (d == 255) S.tvalid = woff + incl;
       }
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
-        const int li = wbase + i * 32 + lane;
-        if (full || li < nvalid) {
+        if ((vbits >> i) & 1u) {
           const uint32_t d = (k[i] >> shift) & 255u;
           const uint32_t pos = S.tstart[d] + S.whist[warp][d] + rank[i];
           S.keys[pos] = k[i];
@@ -789,10 +821,11 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         }
       }
       __syncthreads();
+
 #pragma unroll 4
       for (int i = 0; i < ITEMS; ++i) {
         const int q = i * kSortThreads + tid;
-        if (q < nvalid) {
+        if (q < (int)S.tvalid) {
           const uint32_t key = S.keys[q];
           const uint32_t d = (key >> shift) & 255u;
           const uint32_t g = S.gbase[d] + (uint32_t)q - S.tstart[d];
@@ -806,11 +839,15 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       }
       __syncthreads();
     }
+    if (compact) {  // the later passes sort the visible keys, written to [0, total) by this one
+      M = S.total;
+      ntiles = sort_tiles<ITEMS>(M);
+    }
     if (p + 1 < J.passes && !grid_barrier(S, J, ++nbar * G, true)) return;
   }
   if (!grid_barrier(S, J, ++nbar * G, true)) return;
   if (!kTileSort) {
-    depth_scan(S, J, G, bid, nbar);
+    depth_scan(S, J, M, G, bid, nbar);
   } else {
     // the staged ranges: tile t's run of sorted instances starts where the tile id changes
     // (the host zeroed them, so empty tiles keep [0, 0)).  Four sorted ids per thread in one
@@ -1038,7 +1075,7 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
         tj.slot0 = kDepthPasses; tj.sort_id = 1;
         tj.hist = w[v].hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
         tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
-        tj.gen = GenSource{w[v].slice_first, w[v].grec, n, sv.k.Tx};
+        tj.gen = GenSource{w[v].slice_first, w[v].grec, sv.k.Tx};
         tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
         tj.rstage = w[v].rstage;
       }
