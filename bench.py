@@ -394,12 +394,19 @@ def kernels_mode(args):
     lws = torch.empty(N.gs_loss_workspace_size(W, H), dtype=torch.uint8, device="cuda")
     loss = torch.zeros(1, device="cuda")
     g2d = torch.zeros((n, 12), device="cuda")
+    T = cam.tiles_x * cam.tiles_y
+    order = torch.zeros((2, T), dtype=torch.int32, device="cuda")
+    tcost = torch.zeros(T, dtype=torch.int32, device="cuda")
     calls = {
         "project": lambda: N.gs_project(Pd, n, cam, proj),
         "bin_sort": lambda: N.gs_bin_sort_batch([proj], n, [cam], ws, wsb, None, [vals], cap, [ranges], counts),
-        "render_fwd": lambda: N.gs_render_fwd(proj, n, vals, ranges, cam, None, img, Tf, nc),
+        "tile_order_fwd": lambda: N.gs_tile_order(ranges, None, T, order[0]),
+        "render_fwd": lambda: N.gs_render_fwd(proj, n, vals, ranges, cam, None, img, Tf, nc, tile_order=order[0],
+                                              tile_cost=tcost),
         "loss": lambda: N.gs_loss(img, tgt, W, H, 0.8, 0.2, 1.0, loss, False, dimg, lws, lws.numel()),
-        "render_bwd": lambda: N.gs_render_bwd(proj, n, vals, ranges, cam, None, Tf, nc, dimg, g2d),
+        "tile_order_bwd": lambda: N.gs_tile_order(None, tcost, T, order[1]),
+        "render_bwd": lambda: N.gs_render_bwd(proj, n, vals, ranges, cam, None, Tf, nc, dimg, g2d,
+                                              tile_order=order[1]),
     }
     # the batch's fused projection backward + Adam, every view with its own projection and a
     # copy of view 0's screen-space gradients

@@ -19,7 +19,7 @@ _NAMES = {1: "GS_ERR_INVALID", 2: "GS_ERR_CUDA", 3: "GS_ERR_CAPACITY", 4: "GS_ER
 # every symbol include/gs.h declares
 EXPORTS = ["gs_last_error", "gs_version", "gs_project", "gs_project_batch", "gs_bin_sort_workspace_size", "gs_bin_sort",
            "gs_bin_sort_batch_workspace_size", "gs_bin_sort_batch",
-           "gs_render_fwd", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
+           "gs_render_fwd", "gs_tile_order", "gs_loss_workspace_size", "gs_loss", "gs_loss_noalloc", "gs_render_bwd", "gs_project_bwd",
            "gs_visible_sets_workspace_size", "gs_visible_sets", "gs_sparse_adam", "gs_project_bwd_adam",
            "gs_tile_split", "gs_view_order", "gs_prune_workspace_size", "gs_prune", "gs_densify_workspace_size",
            "gs_densify", "gs_probe_ffma",
@@ -73,11 +73,12 @@ def load() -> C.CDLL:
         "gs_bin_sort": ([vp, i64, cp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
         "gs_bin_sort_batch_workspace_size": ([i32, i64, i64, vp], sz),
         "gs_bin_sort_batch": ([vp, i32, i64, vp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
-        "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
+        "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
+        "gs_tile_order": ([vp, vp, i64, vp, vp], i32),
         "gs_loss_workspace_size": ([i32, i32], sz),
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
         "gs_loss_noalloc": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp], i32),
-        "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp], i32),
+        "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_project_bwd": ([vp, i64, cp, vp, vp, vp, vp, vp], i32),
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -191,11 +192,17 @@ def gs_bin_sort_batch(projs, n, cams, workspace, workspace_bytes, keys, vals, ca
     return list(host) if sync else None
 
 
-def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, work=None, stream=None):
+def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, work=None, stream=None,
+                  tile_order=None, tile_cost=None):
     b = _floats3(bg)
     _check(load().gs_render_fwd(_ptr(proj), n, _ptr(vals), _ptr(ranges), _cam(cam), b[0] if b else None,
-                                _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(work), _stream(stream)),
-           "gs_render_fwd")
+                                _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(work), _ptr(tile_order),
+                                _ptr(tile_cost), _stream(stream)), "gs_render_fwd")
+
+
+def gs_tile_order(ranges, tile_cost, n_tiles, order, stream=None):
+    _check(load().gs_tile_order(_ptr(ranges), _ptr(tile_cost), n_tiles, _ptr(order), _stream(stream)),
+           "gs_tile_order")
 
 
 def gs_loss_workspace_size(width, height) -> int:
@@ -216,11 +223,12 @@ def gs_loss_noalloc(image, target, width, height, w_l1, w_ssim, scale, loss_dev,
                                   1 if accumulate else 0, _ptr(dL_dimage), _stream(stream)), "gs_loss_noalloc")
 
 
-def gs_render_bwd(proj, n, vals, ranges, cam, bg, T_final, n_contrib, dL_dimage, grad2d, stream=None):
+def gs_render_bwd(proj, n, vals, ranges, cam, bg, T_final, n_contrib, dL_dimage, grad2d, stream=None,
+                  tile_order=None):
     b = _floats3(bg)
     _check(load().gs_render_bwd(_ptr(proj), n, _ptr(vals), _ptr(ranges), _cam(cam), b[0] if b else None,
-                                _ptr(T_final), _ptr(n_contrib), _ptr(dL_dimage), _ptr(grad2d), _stream(stream)),
-           "gs_render_bwd")
+                                _ptr(T_final), _ptr(n_contrib), _ptr(dL_dimage), _ptr(grad2d), _ptr(tile_order),
+                                _stream(stream)), "gs_render_bwd")
 
 
 def gs_project_bwd(params, n, cam, proj, grad2d, grads, densify_stat=None, stream=None):

@@ -4,7 +4,9 @@
 // pixel composites the depth-sorted Gaussians of its 16x16 tile front to back; the backward
 // walks the same lists back to front.
 //
-// Layout: one 128-thread CTA per tile.  Warp w owns the 8x8 block at column band w % 2 and
+// Layout: one 128-thread CTA per tile.  The CTAs take the tiles in the order the caller
+// gives (gs_tile_order: heaviest first, so that no long tile starts last and runs alone at
+// the end of the launch) or, without one, in index order.  Warp w owns the 8x8 block at column band w % 2 and
 // row band w / 2 (a square block meets fewer footprints than a 16x4 one); lane l owns column
 // l % 8 of the block and its two rows 2 (l / 8) + {0, 1}.  The tile's list is walked in
 // batches of 256 Gaussians gathered into shared memory (2 per thread).  While gathering,
@@ -150,9 +152,12 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
                                                             int Tx, float3 bg, float* __restrict__ image,
                                                             float* __restrict__ T_final,
                                                             uint32_t* __restrict__ n_contrib,
-                                                            uint32_t* __restrict__ work) {
+                                                            uint32_t* __restrict__ work,
+                                                            const uint32_t* __restrict__ tile_order,
+                                                            uint32_t* __restrict__ tile_cost) {
   __shared__ BatchSmem S;
-  const int tile = blockIdx.x;
+  __shared__ uint32_t s_cost[kWarps];
+  const int tile = tile_order ? (int)__ldg(&tile_order[blockIdx.x]) : (int)blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
   const int px = tile_x0 + 8 * (warp & 1) + (lane & 7), py0 = tile_y0 + 8 * (warp >> 1) + 2 * (lane >> 3);
@@ -253,6 +258,20 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
     }
     __syncthreads();
   }
+  if (tile_cost) {  // the backward's walk over this tile: the largest n_contrib of its pixels
+    uint32_t lm = 0;
+#pragma unroll
+    for (int i = 0; i < kPPT; ++i) lm = max(lm, last[i]);
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, lm);
+    if (lane == 0) s_cost[warp] = wmax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) c = max(c, s_cost[w]);
+      tile_cost[tile] = c;
+    }
+  }
   const int64_t P = (int64_t)W * H;
 #pragma unroll
   for (int i = 0; i < kPPT; ++i) {
@@ -313,10 +332,11 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
                                                             int Tx, float3 bg, const float* __restrict__ T_final,
                                                             const uint32_t* __restrict__ n_contrib,
                                                             const float* __restrict__ dimg,
-                                                            float* __restrict__ grad2d) {
+                                                            float* __restrict__ grad2d,
+                                                            const uint32_t* __restrict__ tile_order) {
   __shared__ BatchSmem S;
   __shared__ uint32_t s_max_last;
-  const int tile = blockIdx.x;
+  const int tile = tile_order ? (int)__ldg(&tile_order[blockIdx.x]) : (int)blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tile_x0 = (tile % Tx) * gs::kTile, tile_y0 = (tile / Tx) * gs::kTile;
   const int px = tile_x0 + 8 * (warp & 1) + (lane & 7), py0 = tile_y0 + 8 * (warp >> 1) + 2 * (lane >> 3);
@@ -466,11 +486,68 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
   }
 }
 
+// Tile order, heaviest first.  A tile's cost is its list length (ranges) or the caller's
+// per-tile cost; tiles are ranked by a key with sixteen steps per octave of the cost
+// (0 for an empty tile), largest key first, in one CTA: a histogram of the keys, their
+// descending exclusive scan, a scatter.  Order within a key is unspecified.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderKeys = 1024;  // keys 0 .. 1 + 16 * 31 + 15
+
+__device__ __forceinline__ uint32_t cost_key(uint32_t c) {
+  if (c == 0u) return 0u;
+  const uint32_t hb = 31u - (uint32_t)__clz(c);
+  const uint32_t frac = hb >= 4u ? (c >> (hb - 4u)) & 15u : (c << (4u - hb)) & 15u;
+  return 1u + 16u * hb + frac;
+}
+
+__global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint32_t* __restrict__ ranges,
+                                                             const uint32_t* __restrict__ cost, int64_t T,
+                                                             uint32_t* __restrict__ order) {
+  __shared__ uint32_t cnt[kOrderKeys];
+  __shared__ uint32_t wsum[kOrderThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto key = [&](int64_t t) {
+    return cost_key(cost ? __ldg(&cost[t]) : __ldg(&ranges[2 * t + 1]) - __ldg(&ranges[2 * t]));
+  };
+  for (int i = tid; i < kOrderKeys; i += kOrderThreads) cnt[i] = 0u;
+  __syncthreads();
+  for (int64_t t = tid; t < T; t += kOrderThreads) atomicAdd(&cnt[key(t)], 1u);
+  __syncthreads();
+  // thread i takes key kOrderKeys - 1 - i: an exclusive scan in thread order is the
+  // descending one
+  static_assert(kOrderKeys == kOrderThreads, "one key per thread");
+  const int k = kOrderKeys - 1 - tid;
+  const uint32_t c = cnt[k];
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t woff = 0;
+  for (int w = 0; w < warp; ++w) woff += wsum[w];
+  cnt[k] = woff + incl - c;
+  __syncthreads();
+  for (int64_t t = tid; t < T; t += kOrderThreads) order[atomicAdd(&cnt[key(t)], 1u)] = (uint32_t)t;
+}
+
 }  // namespace
+
+extern "C" gs_status gs_tile_order(const uint32_t* ranges, const uint32_t* tile_cost, int64_t n_tiles,
+                                   uint32_t* order, void* stream) {
+  if (n_tiles < 0 || n_tiles > (int64_t)0xFFFFFFFFu) return gs::set_error(GS_ERR_INVALID, "gs_tile_order: bad n_tiles");
+  if (n_tiles == 0) return GS_OK;
+  if (!order || (!tile_cost && !ranges)) return gs::set_error(GS_ERR_INVALID, "gs_tile_order: NULL pointer");
+  k_tile_order<<<1, kOrderThreads, 0, gs::as_stream(stream)>>>(ranges, tile_cost, n_tiles, order);
+  return gs::check_launch("gs_tile_order");
+}
 
 extern "C" gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                                    const gs_camera* cam, const float* bg, float* image, float* T_final,
-                                   uint32_t* n_contrib, uint32_t* work, void* stream) {
+                                   uint32_t* n_contrib, uint32_t* work, const uint32_t* tile_order,
+                                   uint32_t* tile_cost, void* stream) {
   if (gs_status s = gs::check_camera(cam)) return s;
   if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_render_fwd: bad n");
   if (!ranges || !image || !T_final || !n_contrib || (n > 0 && (!proj || !vals)))
@@ -481,16 +558,17 @@ extern "C" gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t*
   cudaStream_t st = gs::as_stream(stream);
   if (work)
     k_render_fwd<true><<<k.Tx * k.Ty, kThreads, 0, st>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, image, T_final,
-                                                          n_contrib, work);
+                                                          n_contrib, work, tile_order, tile_cost);
   else
     k_render_fwd<false><<<k.Tx * k.Ty, kThreads, 0, st>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, image, T_final,
-                                                           n_contrib, work);
+                                                           n_contrib, work, tile_order, tile_cost);
   return gs::check_launch("gs_render_fwd");
 }
 
 extern "C" gs_status gs_render_bwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                                    const gs_camera* cam, const float* bg, const float* T_final,
-                                   const uint32_t* n_contrib, const float* dL_dimage, float* grad2d, void* stream) {
+                                   const uint32_t* n_contrib, const float* dL_dimage, float* grad2d,
+                                   const uint32_t* tile_order, void* stream) {
   if (gs_status s = gs::check_camera(cam)) return s;
   if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_render_bwd: bad n");
   if (!ranges || !T_final || !n_contrib || !dL_dimage || (n > 0 && (!proj || !vals || !grad2d)))
@@ -503,6 +581,6 @@ extern "C" gs_status gs_render_bwd(const float* proj, int64_t n, const uint32_t*
   if (n > 0 && cudaMemsetAsync(grad2d, 0, sizeof(float) * 12 * (size_t)n, st) != cudaSuccess)
     return gs::check_launch("gs_render_bwd memset");
   k_render_bwd<<<k.Tx * k.Ty, kThreads, 0, st>>>(proj, n, vals, ranges, k.W, k.H, k.Tx, b, T_final, n_contrib,
-                                                 dL_dimage, grad2d);
+                                                 dL_dimage, grad2d, tile_order);
   return gs::check_launch("gs_render_bwd");
 }

@@ -5,7 +5,7 @@ as torch tensors -- torch supplies memory and the stream, every computation is a
 kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
 training flow (训练流程): project every view (gs_project_batch), bin/sort them all (gs_bin_sort_batch: the
 views' depth sorts share one launch), then for each view composite -> loss -> composite
-backward; then the visible sets, and the projection backward of every view
+backward (both compositing calls issue their tiles heaviest first, gs_tile_order); then the visible sets, and the projection backward of every view
 with the visible-only Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch
 scaling) in one fused pass (gs_project_bwd_adam) whose gradients never leave the chip.
 ``step_async(..., adam=False)`` runs the per-view gs_project_bwd instead and leaves the
@@ -29,7 +29,7 @@ from . import _native as N
 
 # kernels each entry point launches (memset nodes are not counted)
 LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_bwd": 1, "visible_sets": 7,
-            "sparse_adam": 1, "project_bwd_adam": 1}
+            "sparse_adam": 1, "project_bwd_adam": 1, "tile_order": 1}
 
 
 MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
@@ -44,9 +44,9 @@ def tile_group(views: int, capacity: int) -> int:
 
 
 def bin_sort_launches(views: int, capacity: int) -> int:
-    # per group of up to 8 views: zeroing, the depth sorts (keys, tile-count grids, the four
-    # passes, the tiles-touched scans and the tile counts in one cooperative launch), the tile
-    # sorts (both passes of tile_group views per cooperative launch), ranges
+    # per group of up to 8 views: zeroing, the depth sorts (keys, the four passes and the
+    # tiles-touched scans in one cooperative launch), the tile sorts (both passes of tile_group
+    # views per cooperative launch), ranges
     total = 0
     for g0 in range(0, views, 8):
         gv = min(8, views - g0)
@@ -96,6 +96,11 @@ class Trainer:
         self.images = torch.zeros((batch, 3, height, width), dtype=f32, device=dev) if keep_views else None
         self.dimgs = torch.zeros((batch, 3, height, width), dtype=f32, device=dev) if keep_views else None
         self.ranges = torch.zeros((batch, tiles, 2), dtype=i32, device=dev)  # per view
+        # launch order of the compositing calls' tiles, heaviest first: [0] for the forward (by
+        # list length), [1] for the backward (by the forward's per-tile walk, tile_cost)
+        self.n_tiles = tiles
+        self.tile_order = torch.zeros((2, tiles), dtype=i32, device=dev)
+        self.tile_cost = torch.zeros(tiles, dtype=i32, device=dev)
         self.counts = torch.zeros((batch, 2), dtype=i64, device=dev)
         self.loss = torch.zeros(1, dtype=f32, device=dev)
         self.loss_ws = torch.empty(max(N.gs_loss_workspace_size(width, height), 256), dtype=torch.uint8, device=dev)
@@ -186,7 +191,9 @@ class Trainer:
         ws = self._sort_ws(cam)
         N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), None, self.vals[0], self.capacity, self.ranges[0],
                       self.counts[0])
-        N.gs_render_fwd(proj, self.n, self.vals[0], self.ranges[0], cam, self.bg, out, self.T_final, self.n_contrib)
+        N.gs_tile_order(self.ranges[0], None, self.n_tiles, self.tile_order[0])
+        N.gs_render_fwd(proj, self.n, self.vals[0], self.ranges[0], cam, self.bg, out, self.T_final, self.n_contrib,
+                        tile_order=self.tile_order[0])
         return out
 
     def prune(self, min_opacity: float) -> int:
@@ -292,16 +299,18 @@ class Trainer:
             work_buf = None
             if self.work is not None:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
+            T("tile_order", N.gs_tile_order, ranges, None, self.n_tiles, self.tile_order[0], stream=st)
             T("render_fwd", N.gs_render_fwd, proj, n, vals, ranges, cam, self.bg, image, self.T_final,
-              self.n_contrib, work_buf, stream=st)
+              self.n_contrib, work_buf, stream=st, tile_order=self.tile_order[0], tile_cost=self.tile_cost)
             if host_targets is not None and ready is None:  # after the first view's compositing
                 ready = self._upload(host_targets, B, step_start)
             if ready is not None:
                 torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
+            T("tile_order", N.gs_tile_order, None, self.tile_cost, self.n_tiles, self.tile_order[1], stream=st)
             T("render_bwd", N.gs_render_bwd, proj, n, vals, ranges, cam, self.bg, self.T_final,
-              self.n_contrib, dimg, self.grad2d[b], stream=st)
+              self.n_contrib, dimg, self.grad2d[b], stream=st, tile_order=self.tile_order[1])
             if not fused:
                 T("project_bwd", N.gs_project_bwd, self.params, n, cam, proj, self.grad2d[b], self.grads,
                   self.dstat if adam else None, stream=st)
@@ -311,7 +320,7 @@ class Trainer:
                 #  pairs the forward's warps evaluated)
                 self.work.append((int(work_buf[0].sum()), int(work_buf[1].sum()), int(self.n_contrib.sum()),
                                   int(work_buf[2].sum())))
-            launches += sum(LAUNCHES[k] for k in ("render_fwd", "loss", "render_bwd"))
+            launches += sum(LAUNCHES[k] for k in ("render_fwd", "loss", "render_bwd")) + 2 * LAUNCHES["tile_order"]
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
           self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard, stream=st)
         launches += LAUNCHES["visible_sets"]

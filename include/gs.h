@@ -157,10 +157,30 @@ gs_status gs_bin_sort_batch(const float* const* projs, int batch, int64_t n, con
  *   evaluated (through its termination point), work[1] = entries it accumulated, work[2] =
  *   entries its warp walked (the warp-culled list up to the point where all of the warp's
  *   pixels were done) -- the work counts behind the compositing kernels' roofline figures.
+ * tile_order is optional (NULL: tiles in index order), [Tx*Ty] uint32, a permutation of the
+ *   tile numbers (gs_tile_order): the order in which the tiles' thread blocks are issued.
+ *   It changes no result, only how evenly the tiles' unequal work spreads over the SMs.
+ * tile_cost is optional (NULL: not written), [Tx*Ty] uint32: per tile, the largest
+ *   n_contrib of its pixels (the length of the backward's walk), for gs_tile_order.
  */
 gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                         const gs_camera* cam, const float* bg, float* image, float* T_final,
-                        uint32_t* n_contrib, uint32_t* work, void* stream);
+                        uint32_t* n_contrib, uint32_t* work, const uint32_t* tile_order,
+                        uint32_t* tile_cost, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_tile_order -- the order in which the compositing calls issue a view's tiles, heaviest
+ * first.  Not a step of the method: a launch order for gs_render_fwd / gs_render_bwd (a
+ * long tile issued last would run alone at the end of the launch).  A tile's cost is
+ * tile_cost[t] if tile_cost is not NULL (gs_render_fwd's per-tile output, for the
+ * backward), else its list length ranges[t][1] - ranges[t][0] (for the forward).  Writes
+ * order [n_tiles] uint32, a permutation of 0 .. n_tiles-1 whose costs fall by key: key 0 for
+ * a zero cost, else 1 + 16 floor(log2 c) + the four bits of c below its leading one (steps of
+ * 1/16 octave); the largest key comes first, and the order among tiles of one key is
+ * unspecified.  One small launch; n_tiles < 2^32.
+ */
+gs_status gs_tile_order(const uint32_t* ranges, const uint32_t* tile_cost, int64_t n_tiles,
+                        uint32_t* order, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_loss -- L1 + SSIM image loss ("损失计算：L1 + SSIM 损失", Grendel-GS notes, 训练流程)
@@ -206,12 +226,14 @@ gs_status gs_loss_noalloc(const float* image, const float* target, int width, in
  * pixel's list back to front from n_contrib, recovering T by T / (1 - alpha), and
  * writes per-Gaussian screen-space gradients into grad2d [n][12] (the call clears
  * grad2d first; contributions of all pixels are summed with atomics, so the
- * summation order, and the last bits, vary from run to run).
+ * summation order, and the last bits, vary from run to run).  tile_order: as for
+ * gs_render_fwd (NULL: index order); the backward's is best made from gs_render_fwd's
+ * tile_cost.
  */
 gs_status gs_render_bwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                         const gs_camera* cam, const float* bg, const float* T_final,
                         const uint32_t* n_contrib, const float* dL_dimage, float* grad2d,
-                        void* stream);
+                        const uint32_t* tile_order, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_project_bwd -- reverse mode of gs_project: grad2d -> parameter gradients,

@@ -54,7 +54,13 @@ def test_host_side_argument_errors(lib):
                               None) == N.GS_ERR_INVALID
     bad = N.camera(scenes.make_cameras(0)[0])
     bad.width = 0
-    assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None, None,
+                             None) == N.GS_ERR_INVALID
+    # the tile launch order: n_tiles out of range, NULL pointers (no cost source, no output)
+    assert lib.gs_tile_order(None, None, -1, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 1 << 32, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 10, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 0, None, None) == N.GS_OK
     # misaligned workspace / capacity bounds for the sort
     assert lib.gs_bin_sort(None, 0, C.byref(cam), 8, 10, None, None, 1 << 30, 64, 64, None, None) == N.GS_ERR_INVALID
     # the scheduling helpers: parts, batch and unit out of range, NULL pointers

@@ -148,8 +148,10 @@ def test_project_batch_matches_per_view(case):
 
 # ------------------------------------------------------------------ binning + sort
 @pytest.mark.parametrize("cfg,n,view", [(0, None, 0), (0, 1, 0), (0, 2047, 0), (0, 2049, 0), (1, 300_000, 5),
-                                        (2, 200_000, 3)])
+                                        (2, 200_000, 3), (3, 2_000_003, 0)])
 def test_bin_sort_bit_exact(cfg, n, view):
+    # (3, 2_000_003): from 2M Gaussians on, the depth passes use the wide radix tiles; about
+    # 31 % of this view's Gaussians are culled and dropped by the first pass
     P, cam = scene(cfg, n, view)
     pr = oracle.project(P, cam)
     planes = proj_planes_from_oracle(pr)
@@ -236,12 +238,15 @@ def _batch_case(case):
     if case == "300k-4-views":  # fewer CTAs per view than radix tiles of the depth sort
         P = scenes.make_params(1, n=300_000)
         return P, [scenes.make_cameras(1)[v] for v in (0, 5, 11, 23)]
+    if case == "2m-2-views":  # wide depth radix tiles, views with different visible counts
+        P = scenes.make_params(3, n=2_000_003)
+        return P, [scenes.make_cameras(3)[v] for v in (0, 2)]
     # image sizes differ inside the batch (1236x820 and 1920x1080 cameras on one scene)
     P = scenes.make_params(1, n=50_000)
     return P, [scenes.make_cameras(1)[2], scenes.make_cameras(3)[0], scenes.make_cameras(1)[7]]
 
 
-@pytest.mark.parametrize("case", ["small-10-views", "300k-4-views", "mixed-sizes"])
+@pytest.mark.parametrize("case", ["small-10-views", "300k-4-views", "2m-2-views", "mixed-sizes"])
 def test_bin_sort_batch_bit_exact(case):
     P, cams = _batch_case(case)
     planes_list = [proj_planes_from_oracle(oracle.project(P, c)) for c in cams]
@@ -361,7 +366,8 @@ def test_loss_parity(H, W, scale):
 
 
 # ------------------------------------------------------------------ compositing backward
-def test_render_bwd_parity_config0():
+@pytest.mark.parametrize("ordered", [False, True], ids=["index-order", "heaviest-first"])
+def test_render_bwd_parity_config0(ordered):
     P, cam = scene(0)
     planes, (uvzo, conic, radius, rgb), keys, vals, ranges = oracle_stage_chain(P, cam)
     img_o, T_o, nc_o, mg = oracle.render_fwd(uvzo, conic, rgb, vals, ranges, cam.width, cam.height)
@@ -375,8 +381,16 @@ def test_render_bwd_parity_config0():
     g_o = oracle.render_bwd(uvzo, conic, rgb, vals, ranges, cam.width, cam.height, dimg32.astype(np.float64))
     n = P.shape[1]
     grad2d = torch.full((n, 12), 3.0, dtype=torch.float32, device="cuda")  # the call clears it
+    order = None
+    if ordered:  # the trainer's backward launch order: by each tile's largest n_contrib
+        Tn = cam.tiles_x * cam.tiles_y
+        pad = np.zeros((cam.tiles_y * 16, cam.tiles_x * 16), np.int64)
+        pad[:cam.height, :cam.width] = nc_o
+        cost = pad.reshape(cam.tiles_y, 16, cam.tiles_x, 16).max(axis=(1, 3)).ravel().astype(np.int32)
+        order = torch.zeros(Tn, dtype=torch.int32, device="cuda")
+        N.gs_tile_order(None, dev(cost), Tn, order)
     N.gs_render_bwd(dev(planes), n, dev(vals.view(np.int32)), dev(ranges.view(np.int32)), cam, None,
-                    dev(T_o.astype(np.float32)), dev(nc_o.view(np.int32)), dev(dimg32), grad2d)
+                    dev(T_o.astype(np.float32)), dev(nc_o.view(np.int32)), dev(dimg32), grad2d, tile_order=order)
     torch.cuda.synchronize()
     g = host(grad2d)
     # columns: oracle (du, dv, dA, dB, dC, dop, dr, dg, db) vs gs (du, dv, dop, 0, dA, dB, dC, 0, dr, dg, db, 0)
@@ -385,6 +399,72 @@ def test_render_bwd_parity_config0():
     bad = allclose_grad(gm, g_o)
     report("render_bwd cfg0 (every Gaussian)", int(bad.sum()), bad.size)
     assert bad.sum() == 0
+
+
+# ------------------------------------------------------------------ tile launch order
+def cost_key(c):
+    """gs_tile_order's documented ranking key: 0 for a zero cost, else 1 + 16 floor(log2 c)
+    plus the four bits of c below its leading one."""
+    c = np.asarray(c, np.int64)
+    hb = np.where(c > 0, np.floor(np.log2(np.maximum(c, 1))).astype(np.int64), 0)
+    frac = np.where(hb >= 4, (c >> np.maximum(hb - 4, 0)) & 15, (c << np.maximum(4 - hb, 0)) & 15)
+    return np.where(c > 0, 1 + 16 * hb + frac, 0)
+
+
+@pytest.mark.parametrize("T", [1, 5, 1023, 1024, 4056, 32400, 130_321])
+def test_tile_order_is_a_heaviest_first_permutation(T):
+    rng = np.random.default_rng(T)
+    cost = np.where(rng.random(T) < 0.2, 0, rng.integers(1, 1 << 20, T)).astype(np.int64)
+    cost[:3] = [0, (1 << 31) + 5, 1][:min(3, T)]  # a zero, a cost past 2^31, a one
+    starts = rng.integers(0, 1 << 30, T)
+    ranges = np.stack([starts, starts + cost], 1).astype(np.uint32)
+    for by_cost in (False, True):
+        order = torch.full((T,), -1, dtype=torch.int32, device="cuda")
+        N.gs_tile_order(None if by_cost else dev(ranges.view(np.int32)),
+                        dev(cost.astype(np.uint32).view(np.int32)) if by_cost else None, T, order)
+        torch.cuda.synchronize()
+        o = host(order).view(np.uint32).astype(np.int64)
+        assert np.array_equal(np.sort(o), np.arange(T))
+        k = cost_key(cost.astype(np.uint32).astype(np.int64))[o]
+        assert (np.diff(k) <= 0).all()
+    N.gs_tile_order(None, None, 0, None)  # nothing to order: no launch, no error
+
+
+def test_render_with_tile_order_matches_index_order():
+    """The launch order changes no forward result and the backward only by the order of its
+    atomic sums; tile_cost is the largest n_contrib of each tile."""
+    P, cam = scene(1, 300_000, 2)
+    planes, (uvzo, conic, radius, rgb), keys, vals, ranges = oracle_stage_chain(P, cam)
+    img0, T0, nc0 = gpu_render(planes, vals, ranges, cam)
+    n, H, W = P.shape[1], cam.height, cam.width
+    Tn = cam.tiles_x * cam.tiles_y
+    dv, dr, dp = dev(vals.view(np.int32)), dev(ranges.view(np.int32)), dev(planes)
+    order = torch.zeros((2, Tn), dtype=torch.int32, device="cuda")
+    tcost = torch.full((Tn,), 7, dtype=torch.int32, device="cuda")
+    img = torch.zeros((3, H, W), dtype=torch.float32, device="cuda")
+    Tf = torch.zeros((H, W), dtype=torch.float32, device="cuda")
+    nc = torch.zeros((H, W), dtype=torch.int32, device="cuda")
+    N.gs_tile_order(dr, None, Tn, order[0])
+    N.gs_render_fwd(dp, n, dv, dr, cam, None, img, Tf, nc, tile_order=order[0], tile_cost=tcost)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(img), img0) and np.array_equal(host(Tf), T0)
+    assert np.array_equal(host(nc).view(np.uint32), nc0)
+    pad = np.zeros((cam.tiles_y * 16, cam.tiles_x * 16), np.int64)
+    pad[:H, :W] = nc0
+    assert np.array_equal(host(tcost).astype(np.int64), pad.reshape(cam.tiles_y, 16, cam.tiles_x, 16).max(axis=(1, 3)).ravel())
+    N.gs_tile_order(None, tcost, Tn, order[1])
+    rng = np.random.default_rng(5)
+    dimg = dev(rng.normal(0, 1e-3, (3, H, W)).astype(np.float32))
+    g = [torch.zeros((n, 12), dtype=torch.float32, device="cuda") for _ in range(2)]
+    N.gs_render_bwd(dp, n, dv, dr, cam, None, Tf, nc, dimg, g[0])
+    N.gs_render_bwd(dp, n, dv, dr, cam, None, Tf, nc, dimg, g[1], tile_order=order[1])
+    torch.cuda.synchronize()
+    a, b = host(g[0]), host(g[1])
+    # the same fp32 terms summed in another order: a zero-mean image gradient makes many sums
+    # cancel, so the bound is relative to each column's largest magnitude
+    scale = np.abs(a).max(axis=0, keepdims=True)
+    assert (np.abs(a - b) <= 1e-5 * scale + 1e-12).all()
+    assert scale.max() > 0
 
 
 # ------------------------------------------------------------------ projection backward
