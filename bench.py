@@ -57,11 +57,12 @@ NCU_TRAFFIC = {
     ("render_bwd", "object-300k-1236x820"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
                                              "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
                                              "bytes": 38359552},
-    # one launch on a 10M-Gaussian 3840x2160 view of the city layout (55.2M instances): 1.875 GB
-    # read + 0.146 GB written, scaled by the instances to the 40M view's 216.2M (x 3.914)
+    # one launch on a 10M-Gaussian 3840x2160 view of the city layout (55.2M instances, tiles
+    # issued heaviest first): 5.052 GB read + 0.392 GB written, scaled by the instances to the
+    # 40M view's 216.2M (x 3.914)
     ("render_bwd", "city-40m-3840x2160"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                                           "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
-                                           "bytes": 7910000000, "scaled_from": "10M-Gaussian capture, by instances"},
+                                           "sha256": "7fa7ae656df2faf1e3668d9e4ebe5dc7a7e529b385c3bce0bb2578eb604d34f5",
+                                           "bytes": 21310000000, "scaled_from": "10M-Gaussian capture, by instances"},
 }
 
 
@@ -363,8 +364,9 @@ def log(msg: str):
 def kernels_mode(args):
     """One view of the workload's first camera (project, bin and sort, composite, loss,
     composite backward), every call timed on its own with CUDA events (best of --steps after
-    --warmup).  The scene can be drawn smaller (--gaussians) so that a profiler capture holds
-    a few GB on the device.  Prints one JSON line of per-call milliseconds."""
+    --warmup).  The scene can be drawn smaller (--gaussians) and the calls limited (--calls) so
+    that a profiler capture holds a few GB on the device.  Prints one JSON line of per-call
+    milliseconds."""
     import torch
     from gaussian_splatting_gb300 import _native as N
 
@@ -397,7 +399,7 @@ def kernels_mode(args):
     T = cam.tiles_x * cam.tiles_y
     order = torch.zeros((2, T), dtype=torch.int32, device="cuda")
     tcost = torch.zeros(T, dtype=torch.int32, device="cuda")
-    calls = {
+    per_view = {
         "project": lambda: N.gs_project(Pd, n, cam, proj),
         "bin_sort": lambda: N.gs_bin_sort_batch([proj], n, [cam], ws, wsb, None, [vals], cap, [ranges], counts),
         "tile_order_fwd": lambda: N.gs_tile_order(ranges, None, T, order[0]),
@@ -408,18 +410,25 @@ def kernels_mode(args):
         "render_bwd": lambda: N.gs_render_bwd(proj, n, vals, ranges, cam, None, Tf, nc, dimg, g2d,
                                               tile_order=order[1]),
     }
-    # the batch's fused projection backward + Adam, every view with its own projection and a
-    # copy of view 0's screen-space gradients
-    B = min(cfg.batch, 16)
-    bcams = scenes.make_cameras(args.config)[:B]
-    bprojs = [torch.zeros((3, n, 4), dtype=torch.float32, device="cuda") for _ in range(B)]
-    N.gs_project_batch(Pd, n, bcams, bprojs)
-    g2ds = [g2d.clone() for _ in range(B)]
-    m_, v_ = torch.zeros_like(Pd), torch.zeros_like(Pd)
-    Pu = Pd.clone()
-    stat = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
-    calls["project_bwd_adam"] = lambda: N.gs_project_bwd_adam(Pu, n, bcams, bprojs, g2ds, m_, v_, 1e-3, 0.9, 0.999,
-                                                              1e-15, 1, densify_stat=stat)
+    # one untimed pass of the view's calls prepares every call's inputs; --calls keeps only the
+    # named ones (and the buffers they need: a profiler capture then holds less)
+    for f in per_view.values():
+        f()
+    want = set(args.calls.split(",")) if args.calls else None
+    calls = {k: f for k, f in per_view.items() if want is None or k in want}
+    if want is None or "project_bwd_adam" in want:
+        # the batch's fused projection backward + Adam, every view with its own projection and
+        # a copy of view 0's screen-space gradients
+        B = min(cfg.batch, 16)
+        bcams = scenes.make_cameras(args.config)[:B]
+        bprojs = [torch.zeros((3, n, 4), dtype=torch.float32, device="cuda") for _ in range(B)]
+        N.gs_project_batch(Pd, n, bcams, bprojs)
+        g2ds = [g2d.clone() for _ in range(B)]
+        m_, v_ = torch.zeros_like(Pd), torch.zeros_like(Pd)
+        Pu = Pd.clone()
+        stat = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+        calls["project_bwd_adam"] = lambda: N.gs_project_bwd_adam(Pu, n, bcams, bprojs, g2ds, m_, v_, 1e-3, 0.9,
+                                                                  0.999, 1e-15, 1, densify_stat=stat)
     for _ in range(max(1, args.warmup)):
         for f in calls.values():
             f()
@@ -451,6 +460,7 @@ def main():
     ap.add_argument("--kernels", action="store_true",
                     help="time the stage calls of one view of the workload (for profiler captures)")
     ap.add_argument("--gaussians", type=int, default=0, help="with --kernels: draw this many Gaussians instead")
+    ap.add_argument("--calls", default="", help="with --kernels: comma-separated calls to time (default: all)")
     args = ap.parse_args()
     if args.kernels:
         return kernels_mode(args)

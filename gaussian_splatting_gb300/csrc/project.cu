@@ -514,7 +514,8 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 
 struct AdamSmem {
   float4 par[15][kAdamThreads];  // the CTA's parameter planes
-  float sh[48][kAdamThreads];    // SH-coefficient gradients, [3k + c][thread]
+  float4 sh[12][kAdamThreads];   // SH-coefficient gradients in the planes' layout: [q][thread] holds
+                                 // coefficients 3k + c = 4q .. 4q + 3 (one 16-byte access per four)
 };
 
 __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __restrict__ params, int64_t n,
@@ -534,9 +535,9 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
 #pragma unroll
   for (int pl = 0; pl < 15; ++pl) cp_async16(&S.par[pl][t], &P4[(int64_t)pl * n + i]);
   asm volatile("cp.async.commit_group;" ::: "memory");
-  float (*s_sh)[kAdamThreads] = S.sh;
+  float4 (*s_sh)[kAdamThreads] = S.sh;
 #pragma unroll
-  for (int f = 0; f < 48; ++f) s_sh[f][t] = 0.f;
+  for (int q = 0; q < 12; ++q) s_sh[q][t] = make_float4(0.f, 0.f, 0.f, 0.f);
   float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gl = ga, gq = ga;
   bool seen = false;
   float dsum = 0.f, dcnt = 0.f;  // densification statistic of the batch's views
@@ -562,7 +563,14 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
     gl.x += o.gls[0]; gl.y += o.gls[1]; gl.z += o.gls[2];
     gq.x += o.gq.x; gq.y += o.gq.y; gq.z += o.gq.z; gq.w += o.gq.w;
 #pragma unroll
-    for (int fidx = 0; fidx < 48; ++fidx) s_sh[fidx][t] += o.gcol[fidx % 3] * o.b.y[fidx / 3];
+    for (int q = 0; q < 12; ++q) {
+      float4 a = s_sh[q][t];
+      a.x += o.gcol[(4 * q) % 3] * o.b.y[(4 * q) / 3];
+      a.y += o.gcol[(4 * q + 1) % 3] * o.b.y[(4 * q + 1) / 3];
+      a.z += o.gcol[(4 * q + 2) % 3] * o.b.y[(4 * q + 2) / 3];
+      a.w += o.gcol[(4 * q + 3) % 3] * o.b.y[(4 * q + 3) / 3];
+      s_sh[q][t] = a;
+    }
   }
   if (!seen) return;  // not visible in any view of the batch: untouched
   if (stat) {
@@ -590,8 +598,7 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
       if (pl == 0) g = ga;
       else if (pl == 1) g = gl;
       else if (pl == 2) g = gq;
-      else g = make_float4(s_sh[4 * (pl - 3)][t], s_sh[4 * (pl - 3) + 1][t], s_sh[4 * (pl - 3) + 2][t],
-                           s_sh[4 * (pl - 3) + 3][t]);
+      else g = s_sh[pl - 3][t];
       adam4(pp[j], mm[j], vv[j], g, h);
       const int64_t e = (int64_t)pl * n + i;
       P[e] = pp[j];
