@@ -51,18 +51,20 @@ HBM_FALLBACK_GBS = 6800.0
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
 # keyed by entry point and workload, valid only for the kernel source it was measured on: when
-# the source file's hash differs the figure is reported as null.
+# the source file's hash differs the figure is reported as null.  (The render_bwd figures were
+# taken on these kernels while the tile-order kernel still shared their file.)
 NCU_TRAFFIC = {
-    # one launch on the 300K-Gaussian 1236x820 view: 38.308 MB read + 0.052 MB written
+    # one launch on the 300K-Gaussian 1236x820 view (tiles issued heaviest first): 38.226 MB
+    # read + 0.077 MB written
     ("render_bwd", "object-300k-1236x820"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                                             "sha256": "3c0bbb97eaee471b0ee5f280adceb1da17be6506676513b566ddb0ab45b0343e",
-                                             "bytes": 38359552},
+                                             "sha256": "abd192b664b0db3a609bc53b531e3c1bdb9d642d69cb07a748d0191c01cd6fca",
+                                             "bytes": 38302976},
     # one launch on a 10M-Gaussian 3840x2160 view of the city layout (55.2M instances, tiles
-    # issued heaviest first): 5.052 GB read + 0.392 GB written, scaled by the instances to the
+    # issued heaviest first): 5.055 GB read + 0.392 GB written, scaled by the instances to the
     # 40M view's 216.2M (x 3.914)
     ("render_bwd", "city-40m-3840x2160"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                                           "sha256": "7fa7ae656df2faf1e3668d9e4ebe5dc7a7e529b385c3bce0bb2578eb604d34f5",
-                                           "bytes": 21310000000, "scaled_from": "10M-Gaussian capture, by instances"},
+                                           "sha256": "abd192b664b0db3a609bc53b531e3c1bdb9d642d69cb07a748d0191c01cd6fca",
+                                           "bytes": 21320000000, "scaled_from": "10M-Gaussian capture, by instances"},
 }
 
 
@@ -369,6 +371,7 @@ def kernels_mode(args):
     milliseconds."""
     import torch
     from gaussian_splatting_gb300 import _native as N
+    from gaussian_splatting_gb300.trainer import ORDER_BLOCK
 
     cfg = scenes.CONFIGS[args.config]
     n = args.gaussians or cfg.n
@@ -402,11 +405,13 @@ def kernels_mode(args):
     per_view = {
         "project": lambda: N.gs_project(Pd, n, cam, proj),
         "bin_sort": lambda: N.gs_bin_sort_batch([proj], n, [cam], ws, wsb, None, [vals], cap, [ranges], counts),
-        "tile_order_fwd": lambda: N.gs_tile_order(ranges, None, T, order[0]),
+        "tile_order_fwd": lambda: N.gs_tile_order(ranges, None, cam.tiles_x, cam.tiles_y, order[0],
+                                                  block=ORDER_BLOCK[0]),
         "render_fwd": lambda: N.gs_render_fwd(proj, n, vals, ranges, cam, None, img, Tf, nc, tile_order=order[0],
                                               tile_cost=tcost),
         "loss": lambda: N.gs_loss(img, tgt, W, H, 0.8, 0.2, 1.0, loss, False, dimg, lws, lws.numel()),
-        "tile_order_bwd": lambda: N.gs_tile_order(None, tcost, T, order[1]),
+        "tile_order_bwd": lambda: N.gs_tile_order(None, tcost, cam.tiles_x, cam.tiles_y, order[1],
+                                                  block=ORDER_BLOCK[1]),
         "render_bwd": lambda: N.gs_render_bwd(proj, n, vals, ranges, cam, None, Tf, nc, dimg, g2d,
                                               tile_order=order[1]),
     }

@@ -74,7 +74,7 @@ def load() -> C.CDLL:
         "gs_bin_sort_batch_workspace_size": ([i32, i64, i64, vp], sz),
         "gs_bin_sort_batch": ([vp, i32, i64, vp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
         "gs_render_fwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
-        "gs_tile_order": ([vp, vp, i64, vp, vp], i32),
+        "gs_tile_order": ([vp, vp, i32, i32, i32, vp, vp], i32),
         "gs_loss_workspace_size": ([i32, i32], sz),
         "gs_loss": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp, sz, vp], i32),
         "gs_loss_noalloc": ([vp, vp, i32, i32, f32, f32, f32, vp, i32, vp, vp], i32),
@@ -200,9 +200,9 @@ def gs_render_fwd(proj, n, vals, ranges, cam, bg, image, T_final, n_contrib, wor
                                 _ptr(tile_cost), _stream(stream)), "gs_render_fwd")
 
 
-def gs_tile_order(ranges, tile_cost, n_tiles, order, stream=None):
-    _check(load().gs_tile_order(_ptr(ranges), _ptr(tile_cost), n_tiles, _ptr(order), _stream(stream)),
-           "gs_tile_order")
+def gs_tile_order(ranges, tile_cost, tiles_x, tiles_y, order, block=1, stream=None):
+    _check(load().gs_tile_order(_ptr(ranges), _ptr(tile_cost), tiles_x, tiles_y, block, _ptr(order),
+                                _stream(stream)), "gs_tile_order")
 
 
 def gs_loss_workspace_size(width, height) -> int:

@@ -614,6 +614,52 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, uin
   return true;
 }
 
+// Stable ranks of a warp's ITEMS x 32 keys by digit (key >> shift) & 255 within the warp, in
+// item-major order: peer masks of all items first, then the per-warp counts in item order
+// (rank[] holds the peer mask until it is replaced by the rank).  Peers: every lane ORs its
+// bit into its digit's word of a per-warp shared-memory table, reads the word back and clears
+// it.  kFull: every item takes part (a full radix tile: no masks, no divergence); otherwise
+// bit i of vbits says whether item i does.  Leaves the warp's digit counts in S.whist[warp].
+template <int ITEMS, bool kFull>
+__device__ __forceinline__ void rank_items(SortSmem<ITEMS>& S, const uint32_t (&k)[ITEMS], uint32_t vbits, int shift,
+                                           uint32_t (&rank)[ITEMS]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const bool valid = kFull || ((vbits >> i) & 1u);
+    const uint32_t d = (k[i] >> shift) & 255u;
+    if (valid) atomicOr(&S.peer[warp][d], 1u << lane);
+    __syncwarp();
+    rank[i] = valid ? S.peer[warp][d] : 0u;
+    __syncwarp();
+    if (valid) S.peer[warp][d] = 0u;
+    __syncwarp();
+  }
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const uint32_t d = (k[i] >> shift) & 255u;
+    const uint32_t peers = rank[i];
+    if (kFull) {
+      const uint32_t before = S.whist[warp][d];
+      __syncwarp();
+      if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
+      __syncwarp();
+      rank[i] = before + __popc(peers & lt_mask);
+    } else {
+      const bool valid = (vbits >> i) & 1u;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t before = S.whist[warp][d];
+        __syncwarp(vmask);
+        if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
+        __syncwarp(vmask);
+        rank[i] = before + __popc(peers & lt_mask);
+      }
+    }
+  }
+}
+
 // All passes of one sort, run by the G CTAs bid = 0 .. G-1 that the job owns.
 template <int ITEMS, bool kTileSort>
 __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, const uint32_t bid) {
@@ -624,7 +670,6 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
   int64_t M = J.n_host >= 0 ? J.n_host : min(J.count[0], J.cap);  // keys of the pass (depth: visible after pass 0)
   int64_t ntiles = sort_tiles<ITEMS>(M);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t lt_mask = (1u << lane) - 1u;
   for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.peer[0][0])[i] = 0u;
   uint32_t nbar = 0;
   for (int p = 0; p < J.passes; ++p) {
@@ -757,34 +802,8 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         const int li = wbase + i * 32 + lane;
         if (full || (li < nvalid && !(compact && k[i] == kCulledKey))) vbits |= 1u << i;
       }
-      // peer masks of all items first, then the per-warp counts in item order; rank[] holds
-      // the peer mask until it is replaced by the rank.  Peers: every lane ORs its bit into
-      // its digit's word of a per-warp shared-memory table, reads the word back and clears it.
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const bool valid = (vbits >> i) & 1u;
-        const uint32_t d = (k[i] >> shift) & 255u;
-        if (valid) atomicOr(&S.peer[warp][d], 1u << lane);
-        __syncwarp();
-        rank[i] = valid ? S.peer[warp][d] : 0u;
-        __syncwarp();
-        if (valid) S.peer[warp][d] = 0u;
-        __syncwarp();
-      }
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const bool valid = (vbits >> i) & 1u;
-        const uint32_t vmask = full ? 0xffffffffu : __ballot_sync(0xffffffffu, valid);
-        if (valid) {
-          const uint32_t d = (k[i] >> shift) & 255u;
-          const uint32_t peers = rank[i];
-          const uint32_t before = S.whist[warp][d];
-          __syncwarp(vmask);
-          if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
-          __syncwarp(vmask);
-          rank[i] = before + __popc(peers & lt_mask);
-        }
-      }
+      if (full) rank_items<ITEMS, true>(S, k, 0u, shift, rank);
+      else rank_items<ITEMS, false>(S, k, vbits, shift, rank);
       __syncthreads();
       {  // per digit (thread = digit): prefix over warps, the tile's offsets
         const int d = tid;

@@ -6,9 +6,9 @@
 //
 // Layout: one 128-thread CTA per tile.  The CTAs take the tiles in the order the caller
 // gives (gs_tile_order: heaviest first, so that no long tile starts last and runs alone at
-// the end of the launch) or, without one, in index order.  Warp w owns the 8x8 block at column band w % 2 and
-// row band w / 2 (a square block meets fewer footprints than a 16x4 one); lane l owns column
-// l % 8 of the block and its two rows 2 (l / 8) + {0, 1}.  The tile's list is walked in
+// the end of the launch) or, without one, in index order.  Warp w owns the 8x8 block at
+// column band w % 2 and row band w / 2 (a square block meets fewer footprints than a 16x4
+// one); lane l owns column l % 8 of the block and its two rows 2 (l / 8) + {0, 1}.  The tile's list is walked in
 // batches of 256 Gaussians gathered into shared memory (2 per thread).  While gathering,
 // each Gaussian gets a 4-bit mask of the warp blocks that its alpha >= 1/255 ellipse meets
 // (a box test, then the exact minimum of the quadratic form over the block, with a rounding
@@ -383,7 +383,10 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
       if (slot < cnt) gather_record(proj, n, __ldg(&vals[b0 + slot]), tile_x0, tile_y0, S, slot);
     }
     __syncthreads();
-    build_list(S, cnt, warp, lane);
+    // this warp's list stops at its own pixels' largest n_contrib: no pixel of the warp takes
+    // an entry at or past it (the tile's walk runs to the largest over all four warps)
+    const uint32_t wend = warp_max > (uint32_t)bb * kBatch ? warp_max - (uint32_t)bb * kBatch : 0u;
+    build_list(S, (int)min((uint32_t)cnt, wend), warp, lane);
     const int nl = (int)S.count[warp];
     // two entries per iteration, walked back to front: both candidate tests first (they do
     // not depend on the running state), then the entries in reverse list order
@@ -486,63 +489,7 @@ __global__ void __launch_bounds__(kThreads, 7) k_render_bwd(const float* __restr
   }
 }
 
-// Tile order, heaviest first.  A tile's cost is its list length (ranges) or the caller's
-// per-tile cost; tiles are ranked by a key with sixteen steps per octave of the cost
-// (0 for an empty tile), largest key first, in one CTA: a histogram of the keys, their
-// descending exclusive scan, a scatter.  Order within a key is unspecified.
-constexpr int kOrderThreads = 1024;
-constexpr int kOrderKeys = 1024;  // keys 0 .. 1 + 16 * 31 + 15
-
-__device__ __forceinline__ uint32_t cost_key(uint32_t c) {
-  if (c == 0u) return 0u;
-  const uint32_t hb = 31u - (uint32_t)__clz(c);
-  const uint32_t frac = hb >= 4u ? (c >> (hb - 4u)) & 15u : (c << (4u - hb)) & 15u;
-  return 1u + 16u * hb + frac;
-}
-
-__global__ void __launch_bounds__(kOrderThreads) k_tile_order(const uint32_t* __restrict__ ranges,
-                                                             const uint32_t* __restrict__ cost, int64_t T,
-                                                             uint32_t* __restrict__ order) {
-  __shared__ uint32_t cnt[kOrderKeys];
-  __shared__ uint32_t wsum[kOrderThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  auto key = [&](int64_t t) {
-    return cost_key(cost ? __ldg(&cost[t]) : __ldg(&ranges[2 * t + 1]) - __ldg(&ranges[2 * t]));
-  };
-  for (int i = tid; i < kOrderKeys; i += kOrderThreads) cnt[i] = 0u;
-  __syncthreads();
-  for (int64_t t = tid; t < T; t += kOrderThreads) atomicAdd(&cnt[key(t)], 1u);
-  __syncthreads();
-  // thread i takes key kOrderKeys - 1 - i: an exclusive scan in thread order is the
-  // descending one
-  static_assert(kOrderKeys == kOrderThreads, "one key per thread");
-  const int k = kOrderKeys - 1 - tid;
-  const uint32_t c = cnt[k];
-  uint32_t incl = c;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  uint32_t woff = 0;
-  for (int w = 0; w < warp; ++w) woff += wsum[w];
-  cnt[k] = woff + incl - c;
-  __syncthreads();
-  for (int64_t t = tid; t < T; t += kOrderThreads) order[atomicAdd(&cnt[key(t)], 1u)] = (uint32_t)t;
-}
-
 }  // namespace
-
-extern "C" gs_status gs_tile_order(const uint32_t* ranges, const uint32_t* tile_cost, int64_t n_tiles,
-                                   uint32_t* order, void* stream) {
-  if (n_tiles < 0 || n_tiles > (int64_t)0xFFFFFFFFu) return gs::set_error(GS_ERR_INVALID, "gs_tile_order: bad n_tiles");
-  if (n_tiles == 0) return GS_OK;
-  if (!order || (!tile_cost && !ranges)) return gs::set_error(GS_ERR_INVALID, "gs_tile_order: NULL pointer");
-  k_tile_order<<<1, kOrderThreads, 0, gs::as_stream(stream)>>>(ranges, tile_cost, n_tiles, order);
-  return gs::check_launch("gs_tile_order");
-}
 
 extern "C" gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, const uint32_t* ranges,
                                    const gs_camera* cam, const float* bg, float* image, float* T_final,

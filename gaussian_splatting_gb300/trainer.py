@@ -34,6 +34,11 @@ LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_
 
 MAX_FUSED_BATCH = 16  # views gs_project_bwd_adam takes in one call
 
+# edge of the square blocks of tiles that gs_tile_order ranks together (forward, backward):
+# single tiles measured fastest for both (blocks keep more Gaussians shared in L2, but the
+# kernels are issue-bound and lose more to the coarser schedule)
+ORDER_BLOCK = (1, 1)
+
 
 def tile_group(views: int, capacity: int) -> int:
     """Views whose tile sorts share one launch in gs_bin_sort_batch: as many as have their own
@@ -98,7 +103,7 @@ class Trainer:
         self.ranges = torch.zeros((batch, tiles, 2), dtype=i32, device=dev)  # per view
         # launch order of the compositing calls' tiles, heaviest first: [0] for the forward (by
         # list length), [1] for the backward (by the forward's per-tile walk, tile_cost)
-        self.n_tiles = tiles
+        self.tiles_x, self.tiles_y = (width + 15) // 16, (height + 15) // 16
         self.tile_order = torch.zeros((2, tiles), dtype=i32, device=dev)
         self.tile_cost = torch.zeros(tiles, dtype=i32, device=dev)
         self.counts = torch.zeros((batch, 2), dtype=i64, device=dev)
@@ -191,7 +196,7 @@ class Trainer:
         ws = self._sort_ws(cam)
         N.gs_bin_sort(proj, self.n, cam, ws, ws.numel(), None, self.vals[0], self.capacity, self.ranges[0],
                       self.counts[0])
-        N.gs_tile_order(self.ranges[0], None, self.n_tiles, self.tile_order[0])
+        N.gs_tile_order(self.ranges[0], None, self.tiles_x, self.tiles_y, self.tile_order[0], block=ORDER_BLOCK[0])
         N.gs_render_fwd(proj, self.n, self.vals[0], self.ranges[0], cam, self.bg, out, self.T_final, self.n_contrib,
                         tile_order=self.tile_order[0])
         return out
@@ -299,7 +304,8 @@ class Trainer:
             work_buf = None
             if self.work is not None:
                 work_buf = torch.zeros((3, H, W), dtype=torch.int32, device=self.params.device)
-            T("tile_order", N.gs_tile_order, ranges, None, self.n_tiles, self.tile_order[0], stream=st)
+            T("tile_order", N.gs_tile_order, ranges, None, self.tiles_x, self.tiles_y, self.tile_order[0],
+              block=ORDER_BLOCK[0], stream=st)
             T("render_fwd", N.gs_render_fwd, proj, n, vals, ranges, cam, self.bg, image, self.T_final,
               self.n_contrib, work_buf, stream=st, tile_order=self.tile_order[0], tile_cost=self.tile_cost)
             if host_targets is not None and ready is None:  # after the first view's compositing
@@ -308,7 +314,8 @@ class Trainer:
                 torch.cuda.current_stream().wait_event(ready[b])
             T("loss", N.gs_loss, image, targets[b], W, H, self.w_l1, self.w_ssim, inv_b, self.loss, b > 0,
               dimg, self.loss_ws, self.loss_ws.numel(), stream=st)
-            T("tile_order", N.gs_tile_order, None, self.tile_cost, self.n_tiles, self.tile_order[1], stream=st)
+            T("tile_order", N.gs_tile_order, None, self.tile_cost, self.tiles_x, self.tiles_y, self.tile_order[1],
+              block=ORDER_BLOCK[1], stream=st)
             T("render_bwd", N.gs_render_bwd, proj, n, vals, ranges, cam, self.bg, self.T_final,
               self.n_contrib, dimg, self.grad2d[b], stream=st, tile_order=self.tile_order[1])
             if not fused:

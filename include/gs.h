@@ -173,14 +173,18 @@ gs_status gs_render_fwd(const float* proj, int64_t n, const uint32_t* vals, cons
  * first.  Not a step of the method: a launch order for gs_render_fwd / gs_render_bwd (a
  * long tile issued last would run alone at the end of the launch).  A tile's cost is
  * tile_cost[t] if tile_cost is not NULL (gs_render_fwd's per-tile output, for the
- * backward), else its list length ranges[t][1] - ranges[t][0] (for the forward).  Writes
- * order [n_tiles] uint32, a permutation of 0 .. n_tiles-1 whose costs fall by key: key 0 for
- * a zero cost, else 1 + 16 floor(log2 c) + the four bits of c below its leading one (steps of
- * 1/16 octave); the largest key comes first, and the order among tiles of one key is
- * unspecified.  One small launch; n_tiles < 2^32.
+ * backward), else its list length ranges[t][1] - ranges[t][0] (for the forward).  The
+ * tiles_x x tiles_y grid is cut into square blocks of block x block tiles (block = 1..8;
+ * smaller at the right and bottom edges); a block's key is that of its largest cost c: 0 for
+ * c = 0, else
+ * 1 + 16 floor(log2 c) + the four bits of c below its leading one (steps of 1/16 octave).
+ * Writes order [tiles_x * tiles_y] uint32, a permutation of the tile numbers: blocks by
+ * falling key, each block's tiles together in row-major order (neighbouring tiles run at
+ * the same time and share Gaussians in L2); the order of blocks with equal keys is
+ * unspecified.  One small launch; tiles_x, tiles_y <= 65535.
  */
-gs_status gs_tile_order(const uint32_t* ranges, const uint32_t* tile_cost, int64_t n_tiles,
-                        uint32_t* order, void* stream);
+gs_status gs_tile_order(const uint32_t* ranges, const uint32_t* tile_cost, int tiles_x, int tiles_y,
+                        int block, uint32_t* order, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_loss -- L1 + SSIM image loss ("损失计算：L1 + SSIM 损失", Grendel-GS notes, 训练流程)

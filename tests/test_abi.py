@@ -57,10 +57,12 @@ def test_host_side_argument_errors(lib):
     assert lib.gs_render_fwd(None, 0, None, None, C.byref(bad), None, None, None, None, None, None, None,
                              None) == N.GS_ERR_INVALID
     # the tile launch order: n_tiles out of range, NULL pointers (no cost source, no output)
-    assert lib.gs_tile_order(None, None, -1, None, None) == N.GS_ERR_INVALID
-    assert lib.gs_tile_order(None, None, 1 << 32, None, None) == N.GS_ERR_INVALID
-    assert lib.gs_tile_order(None, None, 10, None, None) == N.GS_ERR_INVALID
-    assert lib.gs_tile_order(None, None, 0, None, None) == N.GS_OK
+    assert lib.gs_tile_order(None, None, -1, 4, 4, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 4, 65536, 4, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 4, 4, 0, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 4, 4, 9, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 10, 3, 4, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_tile_order(None, None, 0, 7, 4, None, None) == N.GS_OK
     # misaligned workspace / capacity bounds for the sort
     assert lib.gs_bin_sort(None, 0, C.byref(cam), 8, 10, None, None, 1 << 30, 64, 64, None, None) == N.GS_ERR_INVALID
     # the scheduling helpers: parts, batch and unit out of range, NULL pointers

@@ -388,7 +388,7 @@ def test_render_bwd_parity_config0(ordered):
         pad[:cam.height, :cam.width] = nc_o
         cost = pad.reshape(cam.tiles_y, 16, cam.tiles_x, 16).max(axis=(1, 3)).ravel().astype(np.int32)
         order = torch.zeros(Tn, dtype=torch.int32, device="cuda")
-        N.gs_tile_order(None, dev(cost), Tn, order)
+        N.gs_tile_order(None, dev(cost), cam.tiles_x, cam.tiles_y, order)
     N.gs_render_bwd(dev(planes), n, dev(vals.view(np.int32)), dev(ranges.view(np.int32)), cam, None,
                     dev(T_o.astype(np.float32)), dev(nc_o.view(np.int32)), dev(dimg32), grad2d, tile_order=order)
     torch.cuda.synchronize()
@@ -411,23 +411,35 @@ def cost_key(c):
     return np.where(c > 0, 1 + 16 * hb + frac, 0)
 
 
-@pytest.mark.parametrize("T", [1, 5, 1023, 1024, 4056, 32400, 130_321])
-def test_tile_order_is_a_heaviest_first_permutation(T):
+@pytest.mark.parametrize("tx,ty,block", [(1, 1, 4), (5, 3, 4), (77, 1, 4), (1, 77, 3), (78, 53, 4), (240, 135, 4),
+                                         (240, 135, 1), (361, 361, 8), (100, 70, 2)])
+def test_tile_order_is_a_heaviest_first_permutation(tx, ty, block):
+    T = tx * ty
     rng = np.random.default_rng(T)
     cost = np.where(rng.random(T) < 0.2, 0, rng.integers(1, 1 << 20, T)).astype(np.int64)
     cost[:3] = [0, (1 << 31) + 5, 1][:min(3, T)]  # a zero, a cost past 2^31, a one
     starts = rng.integers(0, 1 << 30, T)
     ranges = np.stack([starts, starts + cost], 1).astype(np.uint32)
+    ys, xs = np.divmod(np.arange(T), tx)
+    ux = (tx + block - 1) // block
+    blk = (ys // block) * ux + xs // block
+    bkey = np.zeros(blk.max() + 1, np.int64)
+    np.maximum.at(bkey, blk, cost_key(cost.astype(np.uint32).astype(np.int64)))
     for by_cost in (False, True):
         order = torch.full((T,), -1, dtype=torch.int32, device="cuda")
         N.gs_tile_order(None if by_cost else dev(ranges.view(np.int32)),
-                        dev(cost.astype(np.uint32).view(np.int32)) if by_cost else None, T, order)
+                        dev(cost.astype(np.uint32).view(np.int32)) if by_cost else None, tx, ty, order, block=block)
         torch.cuda.synchronize()
         o = host(order).view(np.uint32).astype(np.int64)
         assert np.array_equal(np.sort(o), np.arange(T))
-        k = cost_key(cost.astype(np.uint32).astype(np.int64))[o]
-        assert (np.diff(k) <= 0).all()
-    N.gs_tile_order(None, None, 0, None)  # nothing to order: no launch, no error
+        # square blocks of tiles, each contiguous and row-major inside, by falling key
+        b = blk[o]
+        starts_b = np.flatnonzero(np.r_[True, b[1:] != b[:-1]])
+        assert len(starts_b) == len(bkey)  # every block appears as one run
+        for s0, s1 in zip(starts_b, np.r_[starts_b[1:], T]):
+            assert np.array_equal(o[s0:s1], np.sort(o[s0:s1]))
+        assert (np.diff(bkey[b[starts_b]]) <= 0).all()
+    N.gs_tile_order(None, None, 0, 5, None, block=block)  # nothing to order: no launch, no error
 
 
 def test_render_with_tile_order_matches_index_order():
@@ -444,7 +456,7 @@ def test_render_with_tile_order_matches_index_order():
     img = torch.zeros((3, H, W), dtype=torch.float32, device="cuda")
     Tf = torch.zeros((H, W), dtype=torch.float32, device="cuda")
     nc = torch.zeros((H, W), dtype=torch.int32, device="cuda")
-    N.gs_tile_order(dr, None, Tn, order[0])
+    N.gs_tile_order(dr, None, cam.tiles_x, cam.tiles_y, order[0])
     N.gs_render_fwd(dp, n, dv, dr, cam, None, img, Tf, nc, tile_order=order[0], tile_cost=tcost)
     torch.cuda.synchronize()
     assert np.array_equal(host(img), img0) and np.array_equal(host(Tf), T0)
@@ -452,7 +464,7 @@ def test_render_with_tile_order_matches_index_order():
     pad = np.zeros((cam.tiles_y * 16, cam.tiles_x * 16), np.int64)
     pad[:H, :W] = nc0
     assert np.array_equal(host(tcost).astype(np.int64), pad.reshape(cam.tiles_y, 16, cam.tiles_x, 16).max(axis=(1, 3)).ravel())
-    N.gs_tile_order(None, tcost, Tn, order[1])
+    N.gs_tile_order(None, tcost, cam.tiles_x, cam.tiles_y, order[1])
     rng = np.random.default_rng(5)
     dimg = dev(rng.normal(0, 1e-3, (3, H, W)).astype(np.float32))
     g = [torch.zeros((n, 12), dtype=torch.float32, device="cuda") for _ in range(2)]
