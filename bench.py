@@ -238,8 +238,9 @@ class OracleSampler:
     height) views / wall time of the round."""
 
     # host memory the oracle's step holds per Gaussian it is given (double-precision parameters,
-    # moments and gradients, and its per-Gaussian records), with slack
-    BYTES_PER_GAUSSIAN = 7000
+    # moments and gradients, and its per-Gaussian records): a worker's peak resident set on a
+    # 16-row band of the 4K view is 4.8 KB per Gaussian; with slack
+    BYTES_PER_GAUSSIAN = 5500
     MAX_BAND_GAUSSIANS = 1_500_000
 
     def __init__(self, cfg_idx: int, P=None, cams=None, jit=None, workers: int | None = None):
