@@ -24,7 +24,8 @@
 //                 and an 8-byte tile-rectangle record per visible Gaussian; pass 0 leaves the
 //                 culled ones out, so the later passes move only the visible keys.  After the
 //                 passes the same launch runs the tiles-touched scan over the sorted visible
-//                 Gaussians (reduce, scan of the chunk sums, then each chunk's
+//                 Gaussians (each CTA a contiguous run of chunks: their sums, the CTAs'
+//                 totals, then each chunk's
 //                 records: first slot, rectangle, index; and for every radix tile of the tile
 //                 sort the Gaussian holding its first slot).
 //   k_tile_sort   the same passes for one view's instances by tile id: the first pass
@@ -43,6 +44,10 @@
 namespace {
 
 constexpr int kScanChunk = 1024;  // sorted Gaussians per chunk of the tiles-touched scan
+constexpr int kMaxScanCtas = 4096;  // CTAs per view of a depth-sort launch (their scan totals)
+// CTAs per view at least (as many as resident allow), however few the radix tiles: phase B
+// scans 256 digit columns, one CTA each at a time
+constexpr int64_t kMinSortCtas = 64;
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
@@ -72,7 +77,9 @@ constexpr uint32_t kCulledKey = 0xFFFFFFFFu;
 // layout of the small, memset-cleared block of the workspace (32-bit words)
 constexpr int kSmBarrier = 1;        // one arrival counter per sort (depth, tile)
 constexpr int kSmVisible = 3;        // the depth sort's count of visible Gaussians, for the tile sort
+constexpr int kSmTileCtr = 4;        // phase C's radix-tile counters: [sort][pass], kMaxTilePasses each
 constexpr int kSmHist = 32;          // kSlots * 256 digit totals (the column sums of phase B)
+static_assert(kDepthPasses <= kMaxTilePasses && kSmTileCtr + 2 * kMaxTilePasses <= kSmHist, "small-block layout");
 constexpr int kSmWords = kSmHist + kSlots * 256;
 
 struct Workspace {
@@ -80,7 +87,7 @@ struct Workspace {
   uint32_t* tval[2];               // instance Gaussian indices, ping-pong
   uint32_t* dkey[2];
   uint32_t* didx[2];
-  unsigned long long* chunk_tot;   // per scan chunk: tiles touched, then its first slot
+  unsigned long long* cta_tot;     // per CTA of the view's depth sort: tiles touched by its chunks
   uint32_t* hist_depth;            // [256][radix tiles of the depth sort]
   uint32_t* hist_tile;             // [256][radix tiles of the tile sort]
   uint2* rrec;                     // per Gaussian (index order): (x0 | y0 << 16, w | h << 16)
@@ -96,6 +103,10 @@ __host__ __device__ inline int64_t sort_tiles(int64_t m) {
   constexpr int kTile = kSortThreads * ITEMS;
   return (m + kTile - 1) / kTile;
 }
+
+// Row length of a [256][radix tiles] digit-count table: the tile count rounded up to a multiple
+// of four, so that every digit's row starts on a 16-byte boundary (phase B reads it as uint4).
+inline int64_t hist_cols(int64_t tiles) { return (tiles + 3) / 4 * 4; }
 
 int tile_bits(int64_t T) {
   int b = 0;
@@ -115,19 +126,18 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
     off += align256(std::max<size_t>(bytes, 1));
     return p;
   };
-  const int64_t chunks = (n + kScanChunk - 1) / kScanChunk;
   char* tk[kMaxSortViews][5];
   for (int t = 0; t < tile_slots; ++t) {
     for (int j = 0; j < 4; ++j) tk[t][j] = take(sizeof(uint32_t) * (size_t)cap);
-    tk[t][4] = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kTileItems>(cap));
+    tk[t][4] = take(sizeof(uint32_t) * 256 * (size_t)hist_cols(sort_tiles<kTileItems>(cap)));
   }
   for (int v = 0; v < views; ++v) {
     char* dk0 = take(sizeof(uint32_t) * (size_t)n);
     char* dk1 = take(sizeof(uint32_t) * (size_t)n);
     char* di0 = take(sizeof(uint32_t) * (size_t)n);
     char* di1 = take(sizeof(uint32_t) * (size_t)n);
-    char* ss = take(sizeof(unsigned long long) * (size_t)chunks);
-    char* lbd = take(sizeof(uint32_t) * 256 * (size_t)sort_tiles<kDepthItems>(n));
+    char* ss = take(sizeof(unsigned long long) * (size_t)kMaxScanCtas);
+    char* lbd = take(sizeof(uint32_t) * 256 * (size_t)hist_cols(sort_tiles<kDepthItems>(n)));
     char* rr = take(sizeof(uint2) * (size_t)n);
     char* rs = take(sizeof(uint32_t) * 2 * (size_t)n_tiles);
     char* go = take(sizeof(uint32_t) * (size_t)((cap + kSlice - 1) / kSlice));
@@ -145,7 +155,7 @@ size_t carve(Workspace* w, char* base, int views, int64_t n, int64_t cap, int64_
       x.dkey[1] = reinterpret_cast<uint32_t*>(dk1);
       x.didx[0] = reinterpret_cast<uint32_t*>(di0);
       x.didx[1] = reinterpret_cast<uint32_t*>(di1);
-      x.chunk_tot = reinterpret_cast<unsigned long long*>(ss);
+      x.cta_tot = reinterpret_cast<unsigned long long*>(ss);
       x.hist_depth = reinterpret_cast<uint32_t*>(lbd);
       x.rrec = reinterpret_cast<uint2*>(rr);
       x.rstage = reinterpret_cast<uint32_t*>(rs);
@@ -182,6 +192,7 @@ struct SortSmem {
   uint32_t dbase[256];  // the pass's digit bases
   uint32_t wsum[kSortWarps];
   uint32_t full;    // first tile pass, counts: full cycles of 256 digits
+  uint32_t nxt[2];  // phase C: the radix tiles taken from the counter (current, next)
   uint32_t total;   // the pass's key count (sum of the digit totals)
   uint32_t tvalid;  // phase C: keys of the current radix tile that take part in the pass
   int fail;
@@ -222,7 +233,7 @@ struct RadixJob {
   uint2* rrec;          // per Gaussian, index order: (x0 | y0 << 16, w | h << 16); 0 if culled
   // depth sort only, after the last pass: the tiles-touched scan over the depth-sorted
   // Gaussians
-  unsigned long long* chunk_tot;  // per scan chunk of kScanChunk sorted Gaussians
+  unsigned long long* cta_tot;    // per CTA of the job: tiles touched by its scan chunks
   uint4* grec;          // per sorted Gaussian: (first slot, x0 | y0 << 16, w | h << 16, index)
   uint32_t* slice_first;  // per radix tile of the tile sort: the Gaussian holding its first slot
   int64_t tcap;         // instance capacity
@@ -271,6 +282,18 @@ __device__ bool grid_barrier(SortSmem<ITEMS>& S, const RadixJob& J, uint32_t tar
   return S.fail == 0;
 }
 
+// Row and column of tile j of a rectangle w tiles wide (w >= 1): a float estimate of j / w,
+// within 1 of the quotient (its relative error is about 2^-21 and quotients stay below 2^16),
+// corrected by one step either way.
+__device__ __forceinline__ uint32_t rect_row(uint32_t j, uint32_t w, uint32_t& col) {
+  uint32_t row = (uint32_t)__fmul_rz((float)j, __fdividef(1.f, (float)w));
+  int rem = (int)j - (int)(row * w);
+  if (rem < 0) { --row; rem += (int)w; }
+  if (rem >= (int)w) { ++row; rem -= (int)w; }
+  col = (uint32_t)rem;
+  return row;
+}
+
 // 32-bit words of radix tile `tile` of an M-word array, warp-striped: item i of lane l of warp
 // w is slot w * ITEMS * 32 + i * 32 + l; slots past M read nothing and get 0.
 template <int ITEMS>
@@ -288,7 +311,9 @@ __device__ __forceinline__ void load_words(const uint32_t* in, int64_t tile, int
 
 // The keys (tile ids) and values (Gaussian indices) of radix tile `tile` of the first tile
 // pass, generated in the warp-striped order of load_words.  Slots past nvalid get key
-// 0xFFFFFFFF.
+// 0xFFFFFFFF.  The records of the first Gaussians from `first` on are kept in S.whist (free
+// until the ranking; the caller clears it afterwards), so most slots read their owner's
+// record from shared memory.
 template <int ITEMS>
 __device__ __forceinline__ void gen_tile(SortSmem<ITEMS>& S, const RadixJob& J, int64_t tile, int64_t base,
                                          int nvalid, uint32_t (&k)[ITEMS], uint32_t (&v)[ITEMS]) {
@@ -297,6 +322,8 @@ __device__ __forceinline__ void gen_tile(SortSmem<ITEMS>& S, const RadixJob& J, 
   const int wbase = warp * (ITEMS * 32);
   const bool full = nvalid == kTile;
   uint32_t* own = S.keys;  // free until the scatter
+  uint4* rc = reinterpret_cast<uint4*>(&S.whist[0][0]);
+  constexpr uint32_t kRecCache = sizeof(S.whist) / sizeof(uint4);
   const GenSource& G = J.gen;
   const int64_t gn = __ldg(&J.small[kSmVisible]);  // depth-ordered visible Gaussians (previous launch)
   const int64_t first = (int64_t)__ldg(&G.slice_first[tile]);
@@ -308,7 +335,9 @@ __device__ __forceinline__ void gen_tile(SortSmem<ITEMS>& S, const RadixJob& J, 
   const uint32_t end = (uint32_t)(base + nvalid);
   for (int e0 = 0;; e0 += kSortThreads) {
     const int64_t it = first + e0 + tid;
-    const uint32_t off = it < gn ? __ldg(&G.grec[it]).x : 0xFFFFFFFFu;
+    const uint4 r = it < gn ? __ldg(&G.grec[it]) : make_uint4(0xFFFFFFFFu, 0u, 0u, 0u);
+    const uint32_t off = r.x;
+    if ((uint32_t)(e0 + tid) < kRecCache) rc[e0 + tid] = r;
     const bool first_item = e0 + tid == 0;
     const bool in = first_item || off < end;
     if (in && it < gn) atomicMax(&own[first_item ? 0u : off - (uint32_t)base], (uint32_t)(e0 + tid) + 1u);
@@ -343,14 +372,11 @@ __device__ __forceinline__ void gen_tile(SortSmem<ITEMS>& S, const RadixJob& J, 
     const int li = wbase + i * 32 + lane;
     const uint32_t o = own[li];
     if ((full || li < nvalid) && o != 0u && first + o - 1u < gn) {
-      const uint4 rec = __ldg(&G.grec[first + o - 1u]);
-      const uint32_t j = (uint32_t)(base + li) - rec.x;  // tile index inside the rectangle
-      const uint32_t w = max(rec.z & 0xffffu, 1u);
-      uint32_t row = (uint32_t)__fmul_rz((float)j, __fdividef(1.f, (float)w));  // j / w within 1, corrected below
-      int rem = (int)j - (int)(row * w);
-      if (rem < 0) { --row; rem += (int)w; }
-      if (rem >= (int)w) { ++row; rem -= (int)w; }
-      k[i] = ((rec.y >> 16) + row) * (uint32_t)G.Tx + (rec.y & 0xffffu) + (uint32_t)rem;
+      const uint32_t e = o - 1u;
+      const uint4 rec = e < kRecCache ? rc[e] : __ldg(&G.grec[first + e]);
+      uint32_t col;
+      const uint32_t row = rect_row((uint32_t)(base + li) - rec.x, max(rec.z & 0xffffu, 1u), col);
+      k[i] = ((rec.y >> 16) + row) * (uint32_t)G.Tx + (rec.y & 0xffffu) + col;
       v[i] = rec.w;
     } else {
       k[i] = 0xFFFFFFFFu;
@@ -378,21 +404,25 @@ __device__ __forceinline__ void gen_digit_counts(SortSmem<ITEMS>& S, const Radix
   const uint32_t lo = (uint32_t)base, end = (uint32_t)(base + nvalid);
   for (int e0 = 0;; e0 += kSortThreads) {
     const int64_t it = first + e0 + tid;
+    const uint4 rec = it < gn ? __ldg(&G.grec[it]) : make_uint4(0xFFFFFFFFu, 0u, 0u, 0u);
+    const uint32_t off = rec.x;
+    // the next Gaussian's first slot: the next lane's record (one load per warp for lane 31)
+    uint32_t next = __shfl_down_sync(0xffffffffu, off, 1);
+    if (lane == 31 && it + 1 < gn) next = __ldg(&G.grec[it + 1]).x;
+    if (it + 1 >= gn) next = (uint32_t)M;
     bool more = false;
     if (it < gn) {
-      const uint4 rec = __ldg(&G.grec[it]);
-      const uint32_t off = rec.x;
       more = off < end;
       if (more || e0 + tid == 0) {
-        const uint32_t next = it + 1 < gn ? __ldg(&G.grec[it + 1]).x : (uint32_t)M;
         const uint32_t s_lo = max(off, lo), s_hi = min(next, end);
         const uint32_t w = max(rec.z & 0xffffu, 1u);
         if (s_lo < s_hi) {
           const uint32_t x0 = rec.y & 0xffffu, y0 = rec.y >> 16;
-          const uint32_t r0 = (s_lo - off) / w, r1 = (s_hi - 1u - off) / w;
+          uint32_t c0, c1;
+          const uint32_t r0 = rect_row(s_lo - off, w, c0), r1 = rect_row(s_hi - 1u - off, w, c1);
           for (uint32_t r = r0; r <= r1; ++r) {
-            const uint32_t j_lo = r == r0 ? s_lo - off - r * w : 0u;
-            const uint32_t j_hi = r == r1 ? s_hi - 1u - off - r * w : w - 1u;
+            const uint32_t j_lo = r == r0 ? c0 : 0u;
+            const uint32_t j_hi = r == r1 ? c1 : w - 1u;
             const uint32_t t_lo = (y0 + r) * (uint32_t)G.Tx + x0 + j_lo;
             const uint32_t len = j_hi - j_lo + 1u;
             if (len >> 8) atomicAdd(&S.full, len >> 8);
@@ -478,105 +508,61 @@ __device__ __forceinline__ uint32_t touched(const RadixJob& J, uint32_t g, uint4
   return (r.y & 0xffffu) * (r.y >> 16);
 }
 
-// Block-wide sum over the 256 threads (result in every thread).
-template <int ITEMS>
-__device__ __forceinline__ unsigned long long block_sum(SortSmem<ITEMS>& S, uint32_t v) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) S.wsum[warp] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kSortWarps; ++w) t += S.wsum[w];
-  return t;
-}
-
-// After the depth passes: the tiles-touched scan over the n sorted visible Gaussians.  S1: every sorted
-// Gaussian's record (gathered once, by index, from the rectangle records) and the sum of every
-// chunk of kScanChunk of them.  S2 (only for more than kDirectChunks chunks): CTA 0 turns the
-// sums into exclusive prefixes.  S3: every chunk's first slots (its prefix summed directly from
-// the chunk sums when there are few chunks), the records read back in order.  Returns false if
-// a barrier failed.
-constexpr int64_t kDirectChunks = 4096;
-
+// After the depth passes: the tiles-touched scan over the n sorted visible Gaussians, in chunks
+// of kScanChunk; CTA b owns a contiguous run of chunks.  S1: every sorted Gaussian's record
+// (gathered once, by index, from the rectangle records) and the sum of every chunk; the CTA's
+// total.  S3: the CTA's first slot (the totals of the CTAs before it), then every chunk's
+// first slots in order, the records read back and completed, and the first Gaussian of every
+// radix tile of the tile sort; the last CTA's end is M.  Returns false if a barrier failed.
 template <int ITEMS>
 __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, uint32_t G, uint32_t bid,
                            uint32_t& nbar) {
   constexpr int kPer = kScanChunk / kSortThreads;  // 4 consecutive Gaussians per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nchunks = (n + kScanChunk - 1) / kScanChunk;
-  const bool direct = nchunks <= kDirectChunks;
+  const int64_t per = (nchunks + G - 1) / G;
+  const int64_t c_begin = min((int64_t)bid * per, nchunks), c_end = min(c_begin + per, nchunks);
   const uint32_t* sidx = J.val[kDepthPasses & 1];
   unsigned long long* wsum64 = reinterpret_cast<unsigned long long*>(S.gbase);  // free in these phases
-  // S1: records and chunk sums (a thread keeps its kPer Gaussians for S3)
-  for (int64_t c = bid; c < nchunks; c += G) {
-    uint32_t sum = 0;
+  // S1: records and the CTA's total (a thread keeps its kPer Gaussians of every chunk for S3;
+  // no barrier per chunk, two chunks' gathers in flight)
+  unsigned long long tsum = 0;
+#pragma unroll 2
+  for (int64_t c = c_begin; c < c_end; ++c) {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int64_t i = c * kScanChunk + tid * kPer + j;
       if (i < n) {
         uint4 rec;
-        sum += touched(J, __ldcg(&sidx[i]), rec);
+        tsum += touched(J, __ldcg(&sidx[i]), rec);
         J.grec[i] = rec;
       }
     }
-    const unsigned long long t = block_sum(S, sum);
-    if (tid == 0) J.chunk_tot[c] = t;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
+  if (lane == 0) wsum64[warp] = tsum;
+  __syncthreads();
+  unsigned long long run = 0;
+  for (int w = 0; w < kSortWarps; ++w) run += wsum64[w];
+  if (tid == 0) J.cta_tot[bid] = run;
   if (!grid_barrier(S, J, ++nbar * G, true)) return false;
-  // S2: exclusive prefixes of the chunk sums and the instance count M (CTA 0)
-  if (!direct) {
-    if (bid == 0) {
-      unsigned long long carry = 0;
-      for (int64_t c0 = 0; c0 < nchunks; c0 += kSortThreads) {
-        const int64_t c = c0 + tid;
-        const unsigned long long v = c < nchunks ? J.chunk_tot[c] : 0ull;
-        unsigned long long in = v;
+  // S3: the CTA's first slot, then its chunks in order
+  unsigned long long part = 0;
+  for (uint32_t b2 = tid; b2 < bid; b2 += kSortThreads) part += __ldcg(&J.cta_tot[b2]);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long u = __shfl_up_sync(0xffffffffu, in, o);
-          if (lane >= o) in += u;
-        }
-        __syncthreads();
-        if (lane == 31) wsum64[warp] = in;
-        __syncthreads();
-        unsigned long long woff = 0, tot = 0;
-        for (int w = 0; w < kSortWarps; ++w) {
-          if (w < warp) woff += wsum64[w];
-          tot += wsum64[w];
-        }
-        if (c < nchunks) J.chunk_tot[c] = carry + woff + in - v;
-        carry += tot;
-      }
-      if (tid == 0) {
-        J.count[0] = (int64_t)carry;
-        if ((int64_t)carry > J.tcap) flag_status(J.count, gs::kStatusCapacity);
-      }
-    }
-    if (!grid_barrier(S, J, ++nbar * G, true)) return false;
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  __syncthreads();
+  if (lane == 0) wsum64[warp] = part;
+  __syncthreads();
+  unsigned long long prefix = 0;
+  for (int w = 0; w < kSortWarps; ++w) prefix += wsum64[w];
+  if (bid == G - 1 && tid == 0) {
+    const int64_t M = (int64_t)(prefix + run);
+    J.count[0] = M;
+    if (M > J.tcap) flag_status(J.count, gs::kStatusCapacity);
   }
-  // S3: every chunk's records and the first Gaussian of every radix tile of the tile sort
-  for (int64_t c = bid; c < nchunks; c += G) {
-    unsigned long long prefix;
-    if (direct) {  // sum of the chunk sums before c (and, for the last chunk, M)
-      unsigned long long part = 0;
-      for (int64_t c2 = tid; c2 < c; c2 += kSortThreads) part += J.chunk_tot[c2];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      __syncthreads();
-      if (lane == 0) wsum64[warp] = part;
-      __syncthreads();
-      prefix = 0;
-      for (int w = 0; w < kSortWarps; ++w) prefix += wsum64[w];
-      if (c == nchunks - 1 && tid == 0) {
-        const int64_t M = (int64_t)(prefix + J.chunk_tot[c]);
-        J.count[0] = M;
-        if (M > J.tcap) flag_status(J.count, gs::kStatusCapacity);
-      }
-    } else {
-      prefix = J.chunk_tot[c];
-    }
+  for (int64_t c = c_begin; c < c_end; ++c) {
     uint32_t cnt[kPer];
     uint4 rec[kPer];
     uint32_t sum = 0;
@@ -596,8 +582,12 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, uin
     __syncthreads();
     if (lane == 31) S.wsum[warp] = incl;
     __syncthreads();
-    uint32_t woff = 0;
-    for (int w = 0; w < warp; ++w) woff += S.wsum[w];
+    uint32_t woff = 0, total = 0;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t x = S.wsum[w];
+      if (w < warp) woff += x;
+      total += x;
+    }
     int64_t go = (int64_t)prefix + woff + incl - sum;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -610,6 +600,7 @@ __device__ bool depth_scan(SortSmem<ITEMS>& S, const RadixJob& J, int64_t n, uin
       }
       go += cnt[j];
     }
+    prefix += total;
   }
   return true;
 }
@@ -717,19 +708,32 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
     if (!grid_barrier(S, J, nbar * G, !(J.drop_arrival && nbar == 1 && bid == 0))) return;
     // ---- B: per digit, exclusive scan of its counts over the tiles; the column's sum is the
     // digit's total, from which phase C takes the digit bases
+    // (twelve counts per thread as three 16-byte loads, the next twelve in flight while these
+    // are scanned; counts past the last tile read as 0, and the row padding takes junk)
     for (uint32_t d = bid; d < 256; d += G) {
       uint32_t* col = J.hist + (int64_t)d * J.hist_stride;
       uint32_t carry = 0;
       constexpr int kPer = 12;
-      for (int64_t c0 = 0; c0 < ntiles; c0 += kSortThreads * kPer) {
-        uint32_t x[kPer];
+      constexpr int64_t kStep = kSortThreads * kPer;
+      auto load = [&](int64_t c0, uint32_t (&y)[kPer]) {
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q) {
+          const int64_t t = c0 + tid * kPer + 4 * q;
+          const uint4 v4 = t < ntiles ? __ldcg(reinterpret_cast<const uint4*>(col + t)) : make_uint4(0u, 0u, 0u, 0u);
+          y[4 * q] = v4.x;
+          y[4 * q + 1] = t + 1 < ntiles ? v4.y : 0u;
+          y[4 * q + 2] = t + 2 < ntiles ? v4.z : 0u;
+          y[4 * q + 3] = t + 3 < ntiles ? v4.w : 0u;
+        }
+      };
+      uint32_t x[kPer];
+      load(0, x);
+      for (int64_t c0 = 0; c0 < ntiles; c0 += kStep) {
+        uint32_t xn[kPer];
+        load(c0 + kStep, xn);
         uint32_t sum = 0;
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-          const int64_t t = c0 + tid * kPer + j;
-          x[j] = t < ntiles ? col[t] : 0u;
-          sum += x[j];
-        }
+        for (int j = 0; j < kPer; ++j) sum += x[j];
         uint32_t incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -744,14 +748,22 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
           if (w < warp) run += s;
           total += s;
         }
+        uint32_t out[kPer];
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-          const int64_t t = c0 + tid * kPer + j;
-          if (t < ntiles) col[t] = run;
+          out[j] = run;
           run += x[j];
+        }
+#pragma unroll
+        for (int q = 0; q < kPer / 4; ++q) {
+          const int64_t t = c0 + tid * kPer + 4 * q;
+          if (t < ntiles)
+            *reinterpret_cast<uint4*>(col + t) = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
         }
         carry += total;
         __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) x[j] = xn[j];
       }
       if (tid == 0) J.small[kSmHist + (J.slot0 + p) * 256 + d] = carry;
     }
@@ -776,13 +788,20 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       __syncthreads();
     }
     // ---- C: rank within the tile, scatter through shared memory, digit-contiguous writes
+    // The CTAs take radix tiles from a shared counter (the next one fetched while this one is
+    // processed), so a CTA whose tiles were cheaper takes more: the phase ends when the work
+    // does, not when the slowest CTA's fixed share does.  Thread 0 writes nxt[cur ^ 1] while
+    // every thread reads nxt[cur]; each iteration ends with a block barrier.
     uint32_t* kout = J.key[(p + 1) & 1];
     uint32_t* vout = fin ? J.vals_out : J.val[(p + 1) & 1];
-    for (int64_t tile = bid; tile < ntiles; tile += G) {
+    const int ctr = kSmTileCtr + J.sort_id * kMaxTilePasses + p;
+    if (tid == 0) S.nxt[0] = atomicAdd(&J.small[ctr], 1u);
+    __syncthreads();
+    uint32_t cur = 0;
+    for (uint32_t tile = S.nxt[0]; tile < ntiles; cur ^= 1u, tile = S.nxt[cur]) {
+      if (tid == 0) S.nxt[cur ^ 1u] = atomicAdd(&J.small[ctr], 1u);
       // this tile's global digit offsets, loaded now and used after the ranking
       const uint32_t tile_base = S.dbase[tid] + __ldcg(&J.hist[(int64_t)tid * J.hist_stride + tile]);
-      for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
-      __syncthreads();
       const int64_t base = tile * kTile;
       const int nvalid = (int)min((int64_t)kTile, M - base);
       const bool full = nvalid == kTile && !compact;
@@ -795,6 +814,8 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         load_words<ITEMS>(kin, tile, M, k);
         load_words<ITEMS>(vin, tile, M, v);
       }
+      for (int i = tid; i < kSortWarps * 256; i += kSortThreads) (&S.whist[0][0])[i] = 0u;
+      __syncthreads();
       const int wbase = warp * (ITEMS * 32);
       uint32_t vbits = 0;  // bit i: item i takes part (in range; in pass 0 of the depth sort, visible)
 #pragma unroll
@@ -1063,15 +1084,16 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
       dj.key[0] = w[v].dkey[0]; dj.key[1] = w[v].dkey[1];
       dj.val[0] = w[v].didx[0]; dj.val[1] = w[v].didx[1];
       dj.n_host = n; dj.cap = n; dj.passes = kDepthPasses; dj.slot0 = 0; dj.sort_id = 0;
-      dj.hist = w[v].hist_depth; dj.hist_stride = dtiles;
+      dj.hist = w[v].hist_depth; dj.hist_stride = hist_cols(dtiles);
       dj.small = w[v].small; dj.count = sv.count; dj.limit = limit; dj.drop_arrival = drop == 2 && g0 + v == 0;
       dj.proj = sv.proj; dj.Tx = sv.k.Tx; dj.Ty = sv.k.Ty; dj.rrec = w[v].rrec;
-      dj.chunk_tot = w[v].chunk_tot; dj.grec = w[v].grec; dj.slice_first = w[v].slice_first; dj.tcap = capacity;
+      dj.cta_tot = w[v].cta_tot; dj.grec = w[v].grec; dj.slice_first = w[v].slice_first; dj.tcap = capacity;
     }
     // CTAs per view: as many as the radix tiles if the group fits, else an equal share of the
     // resident CTAs
     const int64_t resident = (int64_t)sms * (wide ? radix_blocks_per_sm<2>(dsmem) : radix_blocks_per_sm<0>(dsmem));
-    const int64_t G = std::max<int64_t>(1, std::min<int64_t>(dtiles, resident / gv));
+    const int64_t G = std::max<int64_t>(1, std::min<int64_t>({std::max<int64_t>(dtiles, kMinSortCtas), resident / gv,
+                                                              (int64_t)kMaxScanCtas}));
     if (cudaError_t e = launch_depth_sort(db, (int)(G * gv), dsmem, st, wide))
       return gs::set_error(GS_ERR_CUDA, "gs_bin_sort depth sort: %s", cudaGetErrorString(e));
     if (gs_status s = gs::check_launch("gs_bin_sort depth sort")) return s;
@@ -1092,13 +1114,14 @@ gs_status run_sorts(const SortView* V, int views, int64_t n, int64_t capacity, c
         tj.val[0] = w[v].tval[0]; tj.val[1] = w[v].tval[1];
         tj.n_host = -1; tj.cap = capacity; tj.passes = tile_passes(sv.k);
         tj.slot0 = kDepthPasses; tj.sort_id = 1;
-        tj.hist = w[v].hist_tile; tj.hist_stride = sort_tiles<kTileItems>(capacity);
+        tj.hist = w[v].hist_tile; tj.hist_stride = hist_cols(sort_tiles<kTileItems>(capacity));
         tj.small = w[v].small; tj.count = sv.count; tj.limit = limit; tj.drop_arrival = drop == 1 && g0 + v == 0;
         tj.gen = GenSource{w[v].slice_first, w[v].grec, sv.k.Tx};
         tj.q0 = reinterpret_cast<const float4*>(sv.proj); tj.keys64 = sv.keys; tj.vals_out = sv.vals;
         tj.rstage = w[v].rstage;
       }
-      const int64_t TG = std::max<int64_t>(1, std::min<int64_t>(tresident / tv, sort_tiles<kTileItems>(capacity)));
+      const int64_t TG =
+          std::max<int64_t>(1, std::min<int64_t>(tresident / tv, std::max<int64_t>(sort_tiles<kTileItems>(capacity), kMinSortCtas)));
       if (cudaError_t e = launch_tile_sort(tb, (int)(TG * tv), tsmem, st))
         return gs::set_error(GS_ERR_CUDA, "gs_bin_sort tile sort: %s", cudaGetErrorString(e));
       if (gs_status s = gs::check_launch("gs_bin_sort tile sort")) return s;
