@@ -891,28 +891,46 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
   } else {
     // the staged ranges: tile t's run of sorted instances starts where the tile id changes
     // (the host zeroed them, so empty tiles keep [0, 0)).  Four sorted ids per thread in one
-    // 16-byte load (the buffer is 256-byte aligned and its padding covers the last group); a
-    // thread's neighbours come from the lanes beside it, a warp's edges from one more load.
+    // 16-byte load (the buffer is 256-byte aligned and its padding covers the last group), four
+    // such groups per round; a thread's neighbours come from the lanes beside it, a warp's
+    // edges from one more load.
     const uint32_t* skey = J.key[J.passes & 1];
     const uint4* sk4 = reinterpret_cast<const uint4*>(skey);
     const int64_t n4 = (M + 3) / 4;
     const int64_t span = (n4 + 31) / 32 * 32;  // whole warps, so the shuffles see every lane
-    for (int64_t q = (int64_t)bid * kSortThreads + tid; q < span; q += (int64_t)G * kSortThreads) {
-      const bool in = q < n4;
-      const uint4 v4 = in ? __ldcg(&sk4[q]) : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-      uint32_t e[6];
-      e[0] = __shfl_up_sync(0xffffffffu, v4.w, 1);
-      e[5] = __shfl_down_sync(0xffffffffu, v4.x, 1);
-      if (lane == 0) e[0] = in && q > 0 ? __ldcg(&skey[4 * q - 1]) : 0xFFFFFFFFu;
-      if (lane == 31) e[5] = in && 4 * q + 4 < M ? __ldcg(&skey[4 * q + 4]) : 0xFFFFFFFFu;
-      e[1] = v4.x; e[2] = v4.y; e[3] = v4.z; e[4] = v4.w;
+    const int64_t stride = (int64_t)G * kSortThreads;
+    constexpr int kU = 4;  // groups per thread per round, all of their loads in flight together
+    for (int64_t q0 = (int64_t)bid * kSortThreads + tid; q0 < span; q0 += kU * stride) {
+      uint4 v4[kU];
+      uint32_t edge[kU];  // lane 0: the id before its group; lane 31: the id after
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t g = 4 * q + j;
-        if (!in || g >= M) break;
-        const uint32_t t = e[j + 1];
-        if (g == 0 || e[j] != t) J.rstage[2 * (int64_t)t] = (uint32_t)g;
-        if (g == M - 1 || e[j + 2] != t) J.rstage[2 * (int64_t)t + 1] = (uint32_t)(g + 1);
+      for (int u = 0; u < kU; ++u) {
+        const int64_t q = q0 + u * stride;
+        const bool in = q < n4;
+        v4[u] = in ? __ldcg(&sk4[q]) : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+        edge[u] = 0xFFFFFFFFu;
+        if (lane == 0 && in && q > 0) edge[u] = __ldcg(&skey[4 * q - 1]);
+        if (lane == 31 && in && 4 * q + 4 < M) edge[u] = __ldcg(&skey[4 * q + 4]);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int64_t q = q0 + u * stride;
+        if (q >= span) break;  // the same for the whole warp: span and stride are whole warps
+        const bool in = q < n4;
+        uint32_t e[6];
+        e[0] = __shfl_up_sync(0xffffffffu, v4[u].w, 1);
+        e[5] = __shfl_down_sync(0xffffffffu, v4[u].x, 1);
+        if (lane == 0) e[0] = edge[u];
+        if (lane == 31) e[5] = edge[u];
+        e[1] = v4[u].x; e[2] = v4[u].y; e[3] = v4[u].z; e[4] = v4[u].w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t g = 4 * q + j;
+          if (!in || g >= M) break;
+          const uint32_t t = e[j + 1];
+          if (g == 0 || e[j] != t) J.rstage[2 * (int64_t)t] = (uint32_t)g;
+          if (g == M - 1 || e[j + 2] != t) J.rstage[2 * (int64_t)t + 1] = (uint32_t)(g + 1);
+        }
       }
     }
   }
