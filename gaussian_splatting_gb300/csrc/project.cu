@@ -262,11 +262,28 @@ struct ProjViews {
   int batch;
 };
 
-__global__ void __launch_bounds__(256) k_project_fwd_batch(const float* __restrict__ params, int64_t n,
-                                                           const __grid_constant__ ProjViews pv) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// The batch kernel's parameter source: planes 0-2 from global memory, the twelve SH planes
+// from the thread's shared-memory copy ([plane][thread]; every visible view reads them).
+constexpr int kProjThreads = 256;
+struct StagedSH {
+  const float* p;
+  int64_t n, i;
+  const float4* sh;
+  int t;
+  __device__ __forceinline__ float4 plane(int pl) const {
+    return pl < 3 ? ldg4(p, (int64_t)pl * n + i) : sh[(pl - 3) * kProjThreads + t];
+  }
+};
+
+__global__ void __launch_bounds__(kProjThreads) k_project_fwd_batch(const float* __restrict__ params, int64_t n,
+                                                                    const __grid_constant__ ProjViews pv) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float4* sh = reinterpret_cast<float4*>(smem_raw);  // [12][kProjThreads], thread-private slots
+  const int t = threadIdx.x;
+  const int64_t i = (int64_t)blockIdx.x * kProjThreads + t;
   if (i >= n) return;
   const GlobalParams src{params, n, i};
+  const StagedSH staged{params, n, i, sh, t};
   const float4 p0 = src.plane(0);
   Fwd f;
   bool intrinsics = false;
@@ -277,11 +294,14 @@ __global__ void __launch_bounds__(256) k_project_fwd_batch(const float* __restri
     if (pz > k.znear) {  // the near-plane cull needs only the mean
       if (!intrinsics) {
         project_intrinsics(src, f);
+        // the SH planes once per Gaussian, not once per visible view
+#pragma unroll
+        for (int pl = 0; pl < 12; ++pl) sh[pl * kProjThreads + t] = ldg4(params, (int64_t)(3 + pl) * n + i);
         intrinsics = true;
       }
       visible = project_view(src, k, f);
     }
-    if (visible) emit_projection(src, f, pv.campos[b], pv.proj[b], n, i);
+    if (visible) emit_projection(staged, f, pv.campos[b], pv.proj[b], n, i);
     else emit_culled(pv.proj[b], n, i);
   }
 }
@@ -645,8 +665,10 @@ extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_c
   if (n == 0) return GS_OK;
   if (!params || !gs::aligned16(params))
     return gs::set_error(GS_ERR_INVALID, "gs_project_batch: params NULL or misaligned");
-  const int threads = 256;
-  const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+  const unsigned blocks = (unsigned)((n + kProjThreads - 1) / kProjThreads);
+  const int smem = (int)(12 * kProjThreads * sizeof(float4));
+  const cudaError_t attr = gs::max_dynamic_smem((const void*)k_project_fwd_batch, smem);
+  if (attr != cudaSuccess) return gs::set_error(GS_ERR_CUDA, "gs_project_batch: %s", cudaGetErrorString(attr));
   for (int b0 = 0; b0 < batch; b0 += kMaxProjViews) {
     ProjViews pv{};
     pv.batch = std::min(kMaxProjViews, batch - b0);
@@ -655,7 +677,7 @@ extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_c
       pv.campos[b] = camera_centre(cams[b0 + b]);
       pv.proj[b] = projs[b0 + b];
     }
-    k_project_fwd_batch<<<blocks, threads, 0, gs::as_stream(stream)>>>(params, n, pv);
+    k_project_fwd_batch<<<blocks, kProjThreads, smem, gs::as_stream(stream)>>>(params, n, pv);
     if (gs_status s = gs::check_launch("gs_project_batch")) return s;
   }
   return GS_OK;
