@@ -142,7 +142,10 @@ __global__ void __launch_bounds__(kWordsPerBlock) k_vis_write(int B, int64_t nwo
                                                               const uint32_t* bits, const uint32_t* blkcnt,
                                                               const int64_t* offsets, uint32_t* indices,
                                                               uint32_t* union_idx) {
+  // each warp's indices (up to 32 per lane, in order) are staged in shared memory and then
+  // written to the output as consecutive words, instead of every lane storing its own run
   __shared__ uint32_t s[kWordsPerBlock / 32];
+  __shared__ uint32_t stage[kWordsPerBlock / 32][32 * 32];
   const int set = blockIdx.y;
   const int64_t word = (int64_t)blockIdx.x * kWordsPerBlock + threadIdx.x;
   const uint32_t m = word < nwords ? bits[(int64_t)set * nwords + word] : 0u;
@@ -158,17 +161,20 @@ __global__ void __launch_bounds__(kWordsPerBlock) k_vis_write(int B, int64_t nwo
   __syncthreads();
   uint32_t woff = 0;
   for (int w = 0; w < warp; ++w) woff += s[w];
-  int64_t pos = (int64_t)blkcnt[(int64_t)set * nblk + blockIdx.x] + woff + incl - c;
-  uint32_t* out = set < B ? indices + offsets[set] : union_idx;
+  const uint32_t wtotal = __shfl_sync(0xffffffffu, incl, 31);
+  uint32_t* st = stage[warp];
+  uint32_t k = incl - c;
   uint32_t mm = m;
   while (mm) {
     const int bit = __ffs(mm) - 1;
     mm &= mm - 1;
-    out[pos++] = (uint32_t)(word * 32 + bit);
+    st[k++] = (uint32_t)(word * 32 + bit);
   }
+  __syncwarp();
+  uint32_t* out = (set < B ? indices + offsets[set] : union_idx) + blkcnt[(int64_t)set * nblk + blockIdx.x] + woff;
+  for (uint32_t j = lane; j < wtotal; j += 32) out[j] = st[j];
 }
 
-// pairwise intersections: popcount of AND over a chunk of words staged in shared memory
 __global__ void __launch_bounds__(256) k_vis_inter(int B, int64_t nwords, const uint32_t* bits,
                                                    unsigned long long* inter) {
   extern __shared__ uint32_t s_words[];  // [B][256]
