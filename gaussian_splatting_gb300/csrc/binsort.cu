@@ -631,10 +631,11 @@ __device__ __forceinline__ void rank_items(SortSmem<ITEMS>& S, const uint32_t (&
   for (int i = 0; i < ITEMS; ++i) {
     const uint32_t d = (k[i] >> shift) & 255u;
     const uint32_t peers = rank[i];
+    // every peer stores the same new count (one of the identical stores lands)
     if (kFull) {
       const uint32_t before = S.whist[warp][d];
       __syncwarp();
-      if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
+      S.whist[warp][d] = before + __popc(peers);
       __syncwarp();
       rank[i] = before + __popc(peers & lt_mask);
     } else {
@@ -643,7 +644,7 @@ __device__ __forceinline__ void rank_items(SortSmem<ITEMS>& S, const uint32_t (&
       if (valid) {
         const uint32_t before = S.whist[warp][d];
         __syncwarp(vmask);
-        if (lane == 31 - __clz(peers)) S.whist[warp][d] = before + __popc(peers);
+        S.whist[warp][d] = before + __popc(peers);
         __syncwarp(vmask);
         rank[i] = before + __popc(peers & lt_mask);
       }
@@ -826,17 +827,13 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       if (full) rank_items<ITEMS, true>(S, k, 0u, shift, rank);
       else rank_items<ITEMS, false>(S, k, vbits, shift, rank);
       __syncthreads();
-      {  // per digit (thread = digit): prefix over warps, the tile's offsets
+      {  // per digit (thread = digit): the tile's offsets.  S.whist[w][d] becomes warp w's first
+         // staging slot for digit d, S.gbase[d] the output slot of staging slot 0 (mod 2^32)
         const int d = tid;
         uint32_t run = 0;
 #pragma unroll
-        for (int w = 0; w < kSortWarps; ++w) {
-          const uint32_t c = S.whist[w][d];
-          S.whist[w][d] = run;
-          run += c;
-        }
+        for (int w = 0; w < kSortWarps; ++w) run += S.whist[w][d];
         const uint32_t cnt = run;
-        S.gbase[d] = tile_base;
         uint32_t incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -847,7 +844,15 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         __syncthreads();
         uint32_t woff = 0;
         for (int w = 0; w < warp; ++w) woff += S.wsum[w];
-        S.tstart[d] = woff + incl - cnt;
+        const uint32_t ts = woff + incl - cnt;  // the digit's first staging slot
+        uint32_t r = ts;
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) {
+          const uint32_t c = S.whist[w][d];
+          S.whist[w][d] = r;
+          r += c;
+        }
+        S.gbase[d] = tile_base - ts;
         if (d == 255) S.tvalid = woff + incl;
       }
       __syncthreads();
@@ -855,7 +860,7 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
       for (int i = 0; i < ITEMS; ++i) {
         if ((vbits >> i) & 1u) {
           const uint32_t d = (k[i] >> shift) & 255u;
-          const uint32_t pos = S.tstart[d] + S.whist[warp][d] + rank[i];
+          const uint32_t pos = S.whist[warp][d] + rank[i];
           S.keys[pos] = k[i];
           S.vals[pos] = v[i];
         }
@@ -868,7 +873,7 @@ __device__ __forceinline__ void radix_body(const RadixJob& J, const uint32_t G, 
         if (q < (int)S.tvalid) {
           const uint32_t key = S.keys[q];
           const uint32_t d = (key >> shift) & 255u;
-          const uint32_t g = S.gbase[d] + (uint32_t)q - S.tstart[d];
+          const uint32_t g = S.gbase[d] + (uint32_t)q;
           if (g < (uint64_t)M) {  // always true unless a barrier gave up (status bit set)
             const uint32_t val = S.vals[q];
             kout[g] = key;  // the last tile pass keeps the sorted tile ids for the ranges
