@@ -20,7 +20,8 @@
 // The conic is stored scaled by -log2(e)/2 so that alpha = opacity * 2^p costs one ex2, and
 // a per-Gaussian threshold p_min = log2(1/(255 opacity)) rejects pairs below the 1/255 skip
 // before the ex2.  Forward and backward evaluate every (pixel, Gaussian) pair through the
-// same functions, so the backward's T / (1 - alpha) recovery retraces the forward exactly.
+// same functions, so both take the same entries with the same alpha; the backward recovers
+// each earlier transmittance as T / (1 - alpha) from the forward's final T.
 //
 // The backward takes two list entries per iteration: for each, a Gaussian's nine gradient
 // terms are summed over a thread's two pixels; then both entries' terms are summed over the
@@ -223,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
           float p[kPPT];
 #pragma unroll
           for (int i = 0; i < kPPT; ++i) {
-            hit[i] = (e ? h1[i] : h0[i]) && !done[i];  // a pixel may have finished on entry 0
+            // a pixel that finished before this pair has its row parked and fails the candidate
+            // test; one may have finished on entry 0 of the pair
+            hit[i] = e ? h1[i] && !done[i] : h0[i];
             p[i] = e ? p1[i] : p0[i];
           }
           if (!__any_sync(0xffffffffu, hit[0] || hit[1])) continue;  // warp-uniform skip
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
 #pragma unroll
           for (int i = 0; i < kPPT; ++i) {
             const float alpha = alpha_of(c.y, fast_exp2(p[i]));
-            const float Tn = __fmul_rn(T[i], __fsub_rn(1.f, alpha));
+            const float Tn = fmaf(-alpha, T[i], T[i]);  // T (1 - alpha), for the stop test
             const bool take = hit[i] && alpha >= kAlphaMin;
             const bool term = take && Tn < kTMin;  // stop before this entry
             const bool acc = take && !term;
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
             cr[i] = fmaf(w, col.x, cr[i]);
             cg[i] = fmaf(w, col.y, cg[i]);
             cb[i] = fmaf(w, col.z, cb[i]);
-            T[i] = acc ? Tn : T[i];
+            T[i] -= w;  // T (1 - alpha) if taken (within an ulp of Tn), else unchanged
             last[i] = acc ? pos + 1u : last[i];
             if (kCount) used[i] += acc ? 1u : 0u;
             if (term) {  // at most once per pixel: a branch that is almost never taken
