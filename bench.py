@@ -52,18 +52,19 @@ HBM_FALLBACK_GBS = 6800.0
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture,
 # keyed by entry point and workload, valid only for the kernel source it was measured on: when
 # the source file's hash differs the figure is reported as null.  (The render_bwd figures were
-# taken on these kernels while the tile-order kernel still shared their file.)
+# taken on this backward kernel; since then the tile-order kernel left the file and the
+# forward kernel's transmittance update and finished-pixel parking changed.)
 NCU_TRAFFIC = {
     # one launch on the 300K-Gaussian 1236x820 view (tiles issued heaviest first): 38.226 MB
     # read + 0.077 MB written
     ("render_bwd", "object-300k-1236x820"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                                             "sha256": "abd192b664b0db3a609bc53b531e3c1bdb9d642d69cb07a748d0191c01cd6fca",
+                                             "sha256": "32cf7c6a3f1dcace3465f1b26b0f0de88dece516b54b1115aa70d1feabfd7b7c",
                                              "bytes": 38302976},
     # one launch on a 10M-Gaussian 3840x2160 view of the city layout (55.2M instances, tiles
     # issued heaviest first): 5.055 GB read + 0.392 GB written, scaled by the instances to the
     # 40M view's 216.2M (x 3.914)
     ("render_bwd", "city-40m-3840x2160"): {"source": "gaussian_splatting_gb300/csrc/render.cu",
-                                           "sha256": "abd192b664b0db3a609bc53b531e3c1bdb9d642d69cb07a748d0191c01cd6fca",
+                                           "sha256": "32cf7c6a3f1dcace3465f1b26b0f0de88dece516b54b1115aa70d1feabfd7b7c",
                                            "bytes": 21320000000, "scaled_from": "10M-Gaussian capture, by instances"},
 }
 

@@ -143,8 +143,10 @@ __device__ __forceinline__ float alpha_of(float opacity, float G) {
 // written as |p - p_min/2| <= -p_min/2 (hm = p_min / 2)
 __device__ __forceinline__ bool candidate(float p, float hm) { return fabsf(__fsub_rn(p, hm)) <= -hm; }
 
-// A finished pixel's row coordinate is moved here: p becomes about -1e34, never a candidate.
-constexpr float kParkedRow = 1e17f;
+// A finished pixel's row coordinate is set to NaN: its power is NaN for every record, and a
+// NaN fails the candidate test (every comparison with it is false), so the pixel takes nothing
+// more however wide the Gaussian.
+__device__ __forceinline__ float parked_row() { return __int_as_float(0x7fc00000); }
 
 template <bool kCount>
 __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restrict__ proj, int64_t n,
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
   }
 #pragma unroll
   for (int i = 0; i < kPPT; ++i)
-    if (done[i]) fy[i] = kParkedRow;
+    if (done[i]) fy[i] = parked_row();
   bool warp_done = __all_sync(0xffffffffu, done[0] && done[1]);
   uint32_t walked = 0;  // entries of this warp's culled lists walked (the same in every lane)
   for (uint32_t b0 = start; b0 < end; b0 += kBatch) {
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 8) k_render_fwd(const float* __restr
             if (kCount) used[i] += acc ? 1u : 0u;
             if (term) {  // at most once per pixel: a branch that is almost never taken
               done[i] = true;
-              fy[i] = kParkedRow;
+              fy[i] = parked_row();
               stop[i] = pos + 1u;
               ended = true;
             }
