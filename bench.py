@@ -434,8 +434,16 @@ def kernels_mode(args):
         m_, v_ = torch.zeros_like(Pd), torch.zeros_like(Pd)
         Pu = Pd.clone()
         stat = torch.zeros((n, 2), dtype=torch.float32, device="cuda")
+        # the views' visibility bitsets, as the trainer hands them over from gs_visible_sets
+        vws = torch.empty(N.gs_visible_sets_workspace_size(B, n), dtype=torch.uint8, device="cuda")
+        i64 = dict(dtype=torch.int64, device="cuda")
+        N.gs_visible_sets(bprojs, B, n, vws, vws.numel(), torch.zeros(B + 1, **i64),
+                          torch.zeros(B * n, dtype=torch.int32, device="cuda"),
+                          torch.zeros(n, dtype=torch.int32, device="cuda"), torch.zeros(1, **i64),
+                          torch.zeros((B, B), **i64), torch.zeros((B, B), dtype=torch.float32, device="cuda"))
         calls["project_bwd_adam"] = lambda: N.gs_project_bwd_adam(Pu, n, bcams, bprojs, g2ds, m_, v_, 1e-3, 0.9,
-                                                                  0.999, 1e-15, 1, densify_stat=stat)
+                                                                  0.999, 1e-15, 1, densify_stat=stat,
+                                                                  visible_bits=vws, bits_stride=(n + 31) // 32)
     for _ in range(max(1, args.warmup)):
         for f in calls.values():
             f()
@@ -744,13 +752,14 @@ def main():
             others[k] = {"bound": "alu", "achieved_tflops": round(ach, 3), "frac": round(ach / FP32_PEAK_TFLOPS, 4),
                          "frac_of_measured": round(ach / fp32_meas, 4) if fp32_meas else None}
     if "project_bwd_adam" in avg:
-        # algorithmic bytes: every view's radius word (16 B per Gaussian) and its visible
-        # Gaussians' screen-space gradients (48 B); for the updated Gaussians, the parameters
-        # (240 B) and moments (480 B) read once and all three written (720 B)
+        # algorithmic bytes: every view's visibility bitset (one bit per Gaussian, the trainer
+        # hands over gs_visible_sets' bitsets) and its visible Gaussians' screen-space
+        # gradients (48 B); for the updated Gaussians, the parameters (240 B) and moments
+        # (480 B) read once and all three written (720 B)
         nu = int(tr.n_union.item())
         offs = tr.offsets.cpu().tolist()
         vis = sum(offs[b + 1] - offs[b] for b in range(cfg.batch))
-        nbytes = cfg.batch * tr.n * 16 + vis * 48 + nu * (240 + 480 + 720)
+        nbytes = cfg.batch * ((tr.n + 31) // 32) * 4 + vis * 48 + nu * (240 + 480 + 720)
         gbs = nbytes / (avg["project_bwd_adam"] / 1e3) / 1e9
         others["project_bwd_adam"] = {"bound": "hbm", "achieved_gbs": round(gbs, 1),
                                       "frac": round(gbs / peak_hbm, 4), "bytes": nbytes, "peak_source": hbm_src}

@@ -83,7 +83,8 @@ def load() -> C.CDLL:
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
         "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
-        "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp, vp], i32),
+        "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp, vp, i64, vp],
+                                i32),
         "gs_tile_split": ([vp, i32, i32, i32, vp, vp, vp, vp], i32),
         "gs_view_order": ([vp, i32, i32, vp, vp, vp], i32),
         "gs_prune_workspace_size": ([i64], sz),
@@ -256,7 +257,7 @@ def gs_sparse_adam(params, grads, exp_avg, exp_avg_sq, n, idx, n_idx, max_idx, l
 
 
 def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr, beta1, beta2, eps, step,
-                        counts=None, n_counts=0, densify_stat=None, stream=None):
+                        counts=None, n_counts=0, densify_stat=None, stream=None, visible_bits=None, bits_stride=0):
     batch = len(cams)
     carr = (Camera * batch)(*[c if isinstance(c, Camera) else camera(c) for c in cams])
     parr = (C.c_void_p * batch)(*[_ptr(p) for p in projs])
@@ -264,7 +265,8 @@ def gs_project_bwd_adam(params, n, cams, projs, grad2ds, exp_avg, exp_avg_sq, lr
     _check(load().gs_project_bwd_adam(_ptr(params), n, C.cast(carr, C.c_void_p), batch, C.cast(parr, C.c_void_p),
                                       C.cast(garr, C.c_void_p), _ptr(exp_avg), _ptr(exp_avg_sq), lr, beta1, beta2,
                                       eps, step, _ptr(counts), n_counts if counts is not None else 0,
-                                      _ptr(densify_stat), _stream(stream)), "gs_project_bwd_adam")
+                                      _ptr(densify_stat), _ptr(visible_bits), bits_stride if visible_bits is not None else 0,
+                                      _stream(stream)), "gs_project_bwd_adam")
 
 
 def gs_tile_split(cost_px, width, height, parts, tile_cost, cum, bounds, stream=None):

@@ -503,6 +503,8 @@ struct BatchViews {
   float3 campos[kMaxBatchViews];
   const float* proj[kMaxBatchViews];
   const float* grad2d[kMaxBatchViews];
+  const uint32_t* bits;  // optional visibility bitsets [batch][bits_stride]
+  int64_t bits_stride;
   int batch;
 };
 
@@ -561,9 +563,14 @@ __global__ void __launch_bounds__(kAdamThreads, 4) k_project_bwd_adam(float* __r
   float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gl = ga, gq = ga;
   bool seen = false;
   float dsum = 0.f, dcnt = 0.f;  // densification statistic of the batch's views
-  uint32_t vis = 0;  // views whose radius word is > 0, all read up front
-  for (int b = 0; b < bv.batch; ++b)
-    if (__float_as_int(__ldg(&reinterpret_cast<const float4*>(bv.proj[b])[n + i].w)) > 0) vis |= 1u << b;
+  uint32_t vis = 0;  // views whose radius word is > 0 (or visibility bit), all read up front
+  if (bv.bits) {
+    for (int b = 0; b < bv.batch; ++b)
+      vis |= ((__ldg(&bv.bits[b * bv.bits_stride + (i >> 5)]) >> (i & 31)) & 1u) << b;
+  } else {
+    for (int b = 0; b < bv.batch; ++b)
+      if (__float_as_int(__ldg(&reinterpret_cast<const float4*>(bv.proj[b])[n + i].w)) > 0) vis |= 1u << b;
+  }
   asm volatile("cp.async.wait_all;" ::: "memory");  // own copies only: no block barrier needed
   const SharedParams<kAdamThreads> src{&S.par[0][0], t};
   for (int b = 0; b < bv.batch; ++b) {
@@ -705,7 +712,8 @@ extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_came
                                          const float* const* proj_per_view, const float* const* grad2d_per_view,
                                          float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
                                          float eps, int64_t step, const int64_t* counts, int n_counts,
-                                         float* densify_stat, void* stream) {
+                                         float* densify_stat, const uint32_t* visible_bits, int64_t bits_stride,
+                                         void* stream) {
   if (batch < 1 || batch > kMaxBatchViews)
     return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: batch must be 1..%d", kMaxBatchViews);
   if (n < 0 || n > (int64_t(1) << 31)) return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: bad n");
@@ -718,8 +726,12 @@ extern "C" gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_came
   if (n_counts < 0 || !counts) n_counts = 0;
   if (!gs::aligned16(params) || !gs::aligned16(exp_avg) || !gs::aligned16(exp_avg_sq))
     return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: planes must be 16-byte aligned");
+  if (visible_bits && bits_stride < (n + 31) / 32)
+    return gs::set_error(GS_ERR_INVALID, "gs_project_bwd_adam: bits_stride %lld < ceil(n / 32)", (long long)bits_stride);
   BatchViews bv{};
   bv.batch = batch;
+  bv.bits = visible_bits;
+  bv.bits_stride = bits_stride;
   for (int b = 0; b < batch; ++b) {
     if (gs_status s = gs::check_camera(&cams[b])) return s;
     if (!proj_per_view[b] || !grad2d_per_view[b] || !gs::aligned16(proj_per_view[b]) ||

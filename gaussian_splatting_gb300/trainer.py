@@ -334,7 +334,8 @@ class Trainer:
         if fused:
             T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, ccams, [self.proj[b] for b in range(B)],
               [self.grad2d[b] for b in range(B)], self.exp_avg, self.exp_avg_sq, self.lr, self.betas[0],
-              self.betas[1], self.eps, self.t + 1, self.counts, B, self.dstat, stream=st)
+              self.betas[1], self.eps, self.t + 1, self.counts, B, self.dstat, stream=st,
+              visible_bits=self.vis_ws, bits_stride=(n + 31) // 32)  # gs_visible_sets' bitsets
             launches += LAUNCHES["project_bwd_adam"]
         elif adam:
             T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,

@@ -266,7 +266,10 @@ gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, c
  *   inter    [batch][batch] int64 = |V_i n V_j|.
  *   jaccard  [batch][batch] float = fp32 rounding of the exact ratio inter / |V_i u V_j|
  *            (computed in double from the integer counts), 0 when the union is empty.
- * workspace: gs_visible_sets_workspace_size(batch, n) bytes.  batch in [1, 64].
+ * workspace: gs_visible_sets_workspace_size(batch, n) bytes.  batch in [1, 64].  After the
+ *   call the workspace begins with the views' bitsets, [batch][ceil(n / 32)] uint32 (bit
+ *   i % 32 of word i / 32 of view b set iff i is in V_b), valid until the workspace is used
+ *   again (gs_project_bwd_adam can take them).
  */
 size_t gs_visible_sets_workspace_size(int batch, int64_t n);
 gs_status gs_visible_sets(const float* const* proj_per_view, int batch, int64_t n, void* workspace,
@@ -311,13 +314,20 @@ gs_status gs_sparse_adam(float* params, float* grads, float* exp_avg, float* exp
  *              (any nonzero status word skips the whole update).
  *   densify_stat  optional, as for gs_project_bwd, summed over the batch's views (in view
  *              order); not touched when the update is skipped.
+ *   visible_bits  optional (NULL: each view's radius words are read from its proj): the
+ *              views' visible sets as bitsets, [batch][bits_stride] uint32, bit i % 32 of
+ *              word i / 32 of view b set iff radius_b[i] > 0 -- what gs_visible_sets leaves
+ *              at the start of its workspace.  bits_stride >= ceil(n / 32).  The results
+ *              are the same; the bitsets replace 16 bytes of radius-word traffic per
+ *              Gaussian and view with a bit.
  * Gaussians visible in no view keep p, m and v bit-for-bit.
  */
 gs_status gs_project_bwd_adam(float* params, int64_t n, const gs_camera* cams, int batch,
                               const float* const* proj_per_view, const float* const* grad2d_per_view,
                               float* exp_avg, float* exp_avg_sq, float lr, float beta1, float beta2,
                               float eps, int64_t step, const int64_t* counts, int n_counts,
-                              float* densify_stat, void* stream);
+                              float* densify_stat, const uint32_t* visible_bits, int64_t bits_stride,
+                              void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_probe_ffma -- measurement utility with no counterpart in the method: `blocks` CTAs of

@@ -605,6 +605,30 @@ def test_project_bwd_adam_parity_and_skip():
     torch.cuda.synchronize()
     for t, b in zip((tp, tm, tv), before):
         assert (host(t) == b).all()
+    # the visible sets' bitsets (left at the start of gs_visible_sets' workspace) in place of
+    # the radius words: bit-identical results
+    B = len(cams)
+    ws = torch.empty(N.gs_visible_sets_workspace_size(B, n), dtype=torch.uint8, device="cuda")
+    offs = torch.zeros(B + 1, dtype=torch.int64, device="cuda")
+    idx = torch.zeros(B * n, dtype=torch.int32, device="cuda")
+    uni = torch.zeros(n, dtype=torch.int32, device="cuda")
+    nu = torch.zeros(1, dtype=torch.int64, device="cuda")
+    inter = torch.zeros((B, B), dtype=torch.int64, device="cuda")
+    jac = torch.zeros((B, B), dtype=torch.float32, device="cuda")
+    N.gs_visible_sets(dplanes, B, n, ws, ws.numel(), offs, idx, uni, nu, inter, jac)
+    counts[3, 1] = 0
+    outs = []
+    for bits in (None, ws):
+        p2, m2, v2 = dev(P), dev(M), dev(V)
+        N.gs_project_bwd_adam(p2, n, cams, dplanes, dg, m2, v2, 1e-3, 0.9, 0.999, 1e-15, 5, counts, B,
+                              visible_bits=bits, bits_stride=(n + 31) // 32)
+        torch.cuda.synchronize()
+        outs.append([host(t) for t in (p2, m2, v2)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    with pytest.raises(N.GSError):
+        N.gs_project_bwd_adam(tp, n, cams, dplanes, dg, tm, tv, 1e-3, 0.9, 0.999, 1e-15, 5, counts, B,
+                              visible_bits=ws, bits_stride=(n + 31) // 32 - 1)
 
 
 # ------------------------------------------------------------------ visible sets
