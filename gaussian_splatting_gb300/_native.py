@@ -68,7 +68,7 @@ def load() -> C.CDLL:
         "gs_last_error": ([], C.c_char_p),
         "gs_version": ([], C.c_int),
         "gs_project": ([vp, i64, cp, vp, vp], i32),
-        "gs_project_batch": ([vp, i64, vp, i32, vp, vp], i32),
+        "gs_project_batch": ([vp, i64, vp, i32, vp, vp, i64, vp], i32),
         "gs_bin_sort_workspace_size": ([i64, i64, cp], sz),
         "gs_bin_sort": ([vp, i64, cp, vp, sz, vp, vp, i64, vp, vp, vp, vp], i32),
         "gs_bin_sort_batch_workspace_size": ([i32, i64, i64, vp], sz),
@@ -81,7 +81,7 @@ def load() -> C.CDLL:
         "gs_render_bwd": ([vp, i64, vp, vp, cp, vp, vp, vp, vp, vp, vp, vp], i32),
         "gs_project_bwd": ([vp, i64, cp, vp, vp, vp, vp, vp], i32),
         "gs_visible_sets_workspace_size": ([i32, i64], sz),
-        "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp], i32),
+        "gs_visible_sets": ([vp, i32, i64, vp, sz, vp, vp, vp, vp, vp, vp, vp, i64, vp], i32),
         "gs_sparse_adam": ([vp, vp, vp, vp, i64, vp, vp, i64, f32, f32, f32, f32, i32, i64, vp, i32, vp], i32),
         "gs_project_bwd_adam": ([vp, i64, vp, i32, vp, vp, vp, vp, f32, f32, f32, f32, i64, vp, i32, vp, vp, i64, vp],
                                 i32),
@@ -144,10 +144,13 @@ def gs_project(params, n, cam, proj, stream=None):
     _check(load().gs_project(_ptr(params), n, _cam(cam), _ptr(proj), _stream(stream)), "gs_project")
 
 
-def gs_project_batch(params, n, cams, projs, stream=None):
-    """gs_project for len(cams) views; projs is a list of per-view [3][n][4] outputs."""
+def gs_project_batch(params, n, cams, projs, stream=None, visible_bits=None, bits_stride=0):
+    """gs_project for len(cams) views; projs is a list of per-view [3][n][4] outputs;
+    visible_bits (optional) receives the views' visibility bitsets."""
     c, p = _cams(cams), _ptrs(projs)
-    _check(load().gs_project_batch(_ptr(params), n, c[0], len(cams), p[0], _stream(stream)), "gs_project_batch")
+    _check(load().gs_project_batch(_ptr(params), n, c[0], len(cams), p[0], _ptr(visible_bits),
+                                   bits_stride if visible_bits is not None else 0, _stream(stream)),
+           "gs_project_batch")
 
 
 def gs_bin_sort_workspace_size(n, capacity, cam) -> int:
@@ -242,11 +245,12 @@ def gs_visible_sets_workspace_size(batch, n) -> int:
 
 
 def gs_visible_sets(projs, batch, n, workspace, workspace_bytes, offsets, indices, union_idx, n_union, inter,
-                    jaccard, stream=None):
-    arr = (C.c_void_p * batch)(*[_ptr(p) for p in projs])
-    _check(load().gs_visible_sets(C.cast(arr, C.c_void_p), batch, n, _ptr(workspace), workspace_bytes,
-                                  _ptr(offsets), _ptr(indices), _ptr(union_idx), _ptr(n_union), _ptr(inter),
-                                  _ptr(jaccard), _stream(stream)), "gs_visible_sets")
+                    jaccard, stream=None, visible_bits=None, bits_stride=0):
+    arr = (C.c_void_p * batch)(*[_ptr(p) for p in projs]) if projs is not None else None
+    _check(load().gs_visible_sets(C.cast(arr, C.c_void_p) if arr is not None else None, batch, n, _ptr(workspace),
+                                  workspace_bytes, _ptr(offsets), _ptr(indices), _ptr(union_idx), _ptr(n_union),
+                                  _ptr(inter), _ptr(jaccard), _ptr(visible_bits),
+                                  bits_stride if visible_bits is not None else 0, _stream(stream)), "gs_visible_sets")
 
 
 def gs_sparse_adam(params, grads, exp_avg, exp_avg_sq, n, idx, n_idx, max_idx, lr, beta1, beta2, eps, batch, step,

@@ -256,18 +256,21 @@ extern "C" size_t gs_visible_sets_workspace_size(int batch, int64_t n) {
 extern "C" gs_status gs_visible_sets(const float* const* proj_per_view, int batch, int64_t n, void* workspace,
                                      size_t workspace_bytes, int64_t* offsets, uint32_t* indices,
                                      uint32_t* union_idx, int64_t* n_union, int64_t* inter, float* jaccard,
-                                     void* stream) {
+                                     const uint32_t* visible_bits, int64_t bits_stride, void* stream) {
   if (batch < 1 || batch > kMaxViews) return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: batch must be 1..64");
   if (n < 0 || n >= (int64_t(1) << 32)) return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: bad n");
-  if (!proj_per_view || !workspace || !offsets || !n_union || !inter || !jaccard || (n > 0 && (!indices || !union_idx)))
+  if ((!proj_per_view && !visible_bits) || !workspace || !offsets || !n_union || !inter || !jaccard ||
+      (n > 0 && (!indices || !union_idx)))
     return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: NULL pointer");
+  if (visible_bits && bits_stride < (n + 31) / 32)
+    return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: bits_stride %lld < ceil(n / 32)", (long long)bits_stride);
   const size_t need = vis_carve(nullptr, nullptr, batch, n);
   if (workspace_bytes < need)
     return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: workspace must be 256-byte aligned");
   ViewPtrs vp{};
-  for (int b = 0; b < batch; ++b) {
+  for (int b = 0; b < batch && !visible_bits; ++b) {
     if (n > 0 && (!proj_per_view[b] || !gs::aligned16(proj_per_view[b])))
       return gs::set_error(GS_ERR_INVALID, "gs_visible_sets: view %d proj NULL or misaligned", b);
     vp.q[b] = proj_per_view[b];
@@ -280,8 +283,14 @@ extern "C" gs_status gs_visible_sets(const float* const* proj_per_view, int batc
   if (cudaMemsetAsync(inter, 0, sizeof(int64_t) * batch * batch, st) != cudaSuccess)
     return gs::check_launch("gs_visible_sets memset");
   if (n > 0) {
-    dim3 gb((unsigned)((nwords * 32 + 255) / 256), (unsigned)batch);
-    k_vis_bits<<<gb, 256, 0, st>>>(vp, n, nwords, w.bits);
+    if (visible_bits) {  // the caller's bitsets: copied into the workspace's sets
+      if (cudaMemcpy2DAsync(w.bits, sizeof(uint32_t) * nwords, visible_bits, sizeof(uint32_t) * bits_stride,
+                            sizeof(uint32_t) * nwords, (size_t)batch, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return gs::check_launch("gs_visible_sets bitsets");
+    } else {
+      dim3 gb((unsigned)((nwords * 32 + 255) / 256), (unsigned)batch);
+      k_vis_bits<<<gb, 256, 0, st>>>(vp, n, nwords, w.bits);
+    }
     dim3 gc((unsigned)nblk, (unsigned)(batch + 1));
     k_vis_count<<<gc, kWordsPerBlock, 0, st>>>(batch, nwords, nblk, w.bits, w.blkcnt);
   } else {

@@ -259,6 +259,9 @@ struct ProjViews {
   Cam k[kMaxProjViews];
   float3 campos[kMaxProjViews];
   float* proj[kMaxProjViews];
+  uint32_t* bits;        // optional visibility bitsets of the launch's views, [batch][bits_stride]
+  int64_t bits_stride;
+  int64_t bits_words;    // ceil(n / 32)
   int batch;
 };
 
@@ -275,34 +278,41 @@ struct StagedSH {
   }
 };
 
-__global__ void __launch_bounds__(kProjThreads) k_project_fwd_batch(const float* __restrict__ params, int64_t n,
+__global__ void __launch_bounds__(kProjThreads, 4) k_project_fwd_batch(const float* __restrict__ params, int64_t n,
                                                                     const __grid_constant__ ProjViews pv) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float4* sh = reinterpret_cast<float4*>(smem_raw);  // [12][kProjThreads], thread-private slots
   const int t = threadIdx.x;
   const int64_t i = (int64_t)blockIdx.x * kProjThreads + t;
-  if (i >= n) return;
+  const bool live = i < n;
+  if (!live && !pv.bits) return;  // (with bitsets every lane of a warp takes part in the ballot)
   const GlobalParams src{params, n, i};
   const StagedSH staged{params, n, i, sh, t};
-  const float4 p0 = src.plane(0);
+  const float4 p0 = live ? src.plane(0) : make_float4(0.f, 0.f, 0.f, 0.f);
   Fwd f;
   bool intrinsics = false;
   for (int b = 0; b < pv.batch; ++b) {
     const Cam& k = pv.k[b];
-    const float pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
     bool visible = false;
-    if (pz > k.znear) {  // the near-plane cull needs only the mean
-      if (!intrinsics) {
-        project_intrinsics(src, f);
-        // the SH planes once per Gaussian, not once per visible view
+    if (live) {
+      const float pz = k.R[6] * p0.x + k.R[7] * p0.y + k.R[8] * p0.z + k.t[2];
+      if (pz > k.znear) {  // the near-plane cull needs only the mean
+        if (!intrinsics) {
+          project_intrinsics(src, f);
+          // the SH planes once per Gaussian, not once per visible view
 #pragma unroll
-        for (int pl = 0; pl < 12; ++pl) sh[pl * kProjThreads + t] = ldg4(params, (int64_t)(3 + pl) * n + i);
-        intrinsics = true;
+          for (int pl = 0; pl < 12; ++pl) sh[pl * kProjThreads + t] = ldg4(params, (int64_t)(3 + pl) * n + i);
+          intrinsics = true;
+        }
+        visible = project_view(src, k, f);
       }
-      visible = project_view(src, k, f);
+      if (visible) emit_projection(staged, f, pv.campos[b], pv.proj[b], n, i);
+      else emit_culled(pv.proj[b], n, i);
     }
-    if (visible) emit_projection(staged, f, pv.campos[b], pv.proj[b], n, i);
-    else emit_culled(pv.proj[b], n, i);
+    if (pv.bits) {  // 32 consecutive Gaussians per warp: one bitset word per view
+      const uint32_t m = __ballot_sync(0xffffffffu, visible);
+      if ((t & 31) == 0 && (i >> 5) < pv.bits_words) pv.bits[b * pv.bits_stride + (i >> 5)] = m;
+    }
   }
 }
 
@@ -659,7 +669,8 @@ extern "C" gs_status gs_project(const float* params, int64_t n, const gs_camera*
 }
 
 extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_camera* cams, int batch,
-                                      float* const* projs, void* stream) {
+                                      float* const* projs, uint32_t* visible_bits, int64_t bits_stride,
+                                      void* stream) {
   if (batch < 1) return gs::set_error(GS_ERR_INVALID, "gs_project_batch: batch must be >= 1");
   if (n < 0 || n > (int64_t(1) << 31))
     return gs::set_error(GS_ERR_INVALID, "gs_project_batch: bad n %lld", (long long)n);
@@ -672,6 +683,8 @@ extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_c
   if (n == 0) return GS_OK;
   if (!params || !gs::aligned16(params))
     return gs::set_error(GS_ERR_INVALID, "gs_project_batch: params NULL or misaligned");
+  if (visible_bits && bits_stride < (n + 31) / 32)
+    return gs::set_error(GS_ERR_INVALID, "gs_project_batch: bits_stride %lld < ceil(n / 32)", (long long)bits_stride);
   const unsigned blocks = (unsigned)((n + kProjThreads - 1) / kProjThreads);
   const int smem = (int)(12 * kProjThreads * sizeof(float4));
   const cudaError_t attr = gs::max_dynamic_smem((const void*)k_project_fwd_batch, smem);
@@ -679,6 +692,9 @@ extern "C" gs_status gs_project_batch(const float* params, int64_t n, const gs_c
   for (int b0 = 0; b0 < batch; b0 += kMaxProjViews) {
     ProjViews pv{};
     pv.batch = std::min(kMaxProjViews, batch - b0);
+    pv.bits = visible_bits ? visible_bits + (int64_t)b0 * bits_stride : nullptr;
+    pv.bits_stride = bits_stride;
+    pv.bits_words = (n + 31) / 32;
     for (int b = 0; b < pv.batch; ++b) {
       pv.k[b] = gs::make_cam(cams[b0 + b]);
       pv.campos[b] = camera_centre(cams[b0 + b]);

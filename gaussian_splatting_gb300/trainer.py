@@ -28,7 +28,9 @@ import torch
 from . import _native as N
 
 # kernels each entry point launches (memset nodes are not counted)
-LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_bwd": 1, "visible_sets": 7,
+# (gs_visible_sets given the projection's bitsets: count, scan, offsets, write, intersections,
+# Jaccard; the bitset kernel is not launched)
+LAUNCHES = {"project": 1, "render_fwd": 1, "loss": 2, "render_bwd": 1, "project_bwd": 1, "visible_sets": 6,
             "sparse_adam": 1, "project_bwd_adam": 1, "tile_order": 1}
 
 
@@ -110,6 +112,10 @@ class Trainer:
         self.loss = torch.zeros(1, dtype=f32, device=dev)
         self.loss_ws = torch.empty(max(N.gs_loss_workspace_size(width, height), 256), dtype=torch.uint8, device=dev)
         self.vis_ws = torch.empty(max(N.gs_visible_sets_workspace_size(batch, n), 256), dtype=torch.uint8, device=dev)
+        # the views' visibility bitsets, written by the batched projection and read by the
+        # visible sets and the fused update instead of every view's radius words
+        self.bits_stride = max((n + 31) // 32, 1)
+        self.vis_bits = torch.zeros((batch, self.bits_stride), dtype=i32, device=dev)
         self.offsets = torch.zeros(batch + 1, dtype=i64, device=dev)
         self.indices = torch.zeros(max(batch * n, 1), dtype=i32, device=dev)
         self.union_idx = torch.zeros(max(n, 1), dtype=i32, device=dev)
@@ -261,6 +267,8 @@ class Trainer:
         self.proj = torch.zeros((batch, 3, n, 4), dtype=f32, device=dev)
         self.grad2d = torch.zeros((batch, n, 12), dtype=f32, device=dev)
         self.vis_ws = torch.empty(max(N.gs_visible_sets_workspace_size(batch, n), 256), dtype=torch.uint8, device=dev)
+        self.bits_stride = max((n + 31) // 32, 1)
+        self.vis_bits = torch.zeros((batch, self.bits_stride), dtype=i32, device=dev)
         self.indices = torch.zeros(max(batch * n, 1), dtype=i32, device=dev)
         self.union_idx = torch.zeros(max(n, 1), dtype=i32, device=dev)
         self.sort_ws = None
@@ -291,7 +299,8 @@ class Trainer:
         if host_targets is not None:  # marks the point the target uploads may start from
             step_start = torch.cuda.Event()
             step_start.record()
-        T("project", N.gs_project_batch, self.params, n, ccams, [self.proj[b] for b in range(B)], stream=st)
+        T("project", N.gs_project_batch, self.params, n, ccams, [self.proj[b] for b in range(B)], stream=st,
+          visible_bits=self.vis_bits, bits_stride=self.bits_stride)
         ws = self._sort_ws(ccams[0])
         T("bin_sort", N.gs_bin_sort_batch, [self.proj[b] for b in range(B)], n, ccams, ws, ws.numel(), None,
           [self.vals[b] for b in range(B)], self.capacity, [self.ranges[b] for b in range(B)], self.counts,
@@ -329,13 +338,14 @@ class Trainer:
                                   int(work_buf[2].sum())))
             launches += sum(LAUNCHES[k] for k in ("render_fwd", "loss", "render_bwd")) + 2 * LAUNCHES["tile_order"]
         T("visible_sets", N.gs_visible_sets, [self.proj[b] for b in range(B)], B, n, self.vis_ws, self.vis_ws.numel(),
-          self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard, stream=st)
+          self.offsets, self.indices, self.union_idx, self.n_union, self.inter, self.jaccard, stream=st,
+          visible_bits=self.vis_bits, bits_stride=self.bits_stride)
         launches += LAUNCHES["visible_sets"]
         if fused:
             T("project_bwd_adam", N.gs_project_bwd_adam, self.params, n, ccams, [self.proj[b] for b in range(B)],
               [self.grad2d[b] for b in range(B)], self.exp_avg, self.exp_avg_sq, self.lr, self.betas[0],
               self.betas[1], self.eps, self.t + 1, self.counts, B, self.dstat, stream=st,
-              visible_bits=self.vis_ws, bits_stride=(n + 31) // 32)  # gs_visible_sets' bitsets
+              visible_bits=self.vis_bits, bits_stride=self.bits_stride)  # the projection's bitsets
             launches += LAUNCHES["project_bwd_adam"]
         elif adam:
             T("sparse_adam", N.gs_sparse_adam, self.params, self.grads, self.exp_avg, self.exp_avg_sq, n,

@@ -86,10 +86,13 @@ gs_status gs_project(const float* params, int64_t n, const gs_camera* cam, float
  * (scales, opacity, rotation, 3-D covariance) once.
  *   cams   host array of `batch` cameras.
  *   projs  host array of `batch` device pointers, [3][n][4] each, 16-byte aligned.
+ *   visible_bits  optional (NULL: not written), [batch][bits_stride] uint32: bit i % 32 of
+ *          word i / 32 of view b set iff Gaussian i has radius > 0 in view b (bits past n
+ *          clear); bits_stride >= ceil(n / 32).  The visible sets' input (gs_visible_sets).
  * batch must be >= 1; n == 0 is a no-op.
  */
 gs_status gs_project_batch(const float* params, int64_t n, const gs_camera* cams, int batch,
-                           float* const* projs, void* stream);
+                           float* const* projs, uint32_t* visible_bits, int64_t bits_stride, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_bin_sort -- tile binning and depth sort ("find the Gaussians covering a pixel,
@@ -260,6 +263,9 @@ gs_status gs_project_bwd(const float* params, int64_t n, const gs_camera* cam, c
  * primitives after backward).
  *   proj_per_view  HOST array of `batch` device pointers to proj [3][n][4].
  *   V_b = {i : radius_b[i] > 0}.
+ *   visible_bits  optional: the same sets as bitsets, [batch][bits_stride] uint32 (as
+ *            gs_project_batch writes them); when given, the radius words are not read and
+ *            proj_per_view may be NULL.  bits_stride >= ceil(n / 32).
  *   offsets  [batch + 1] int64; indices [batch * n] uint32: V_b ascending at
  *            indices[offsets[b] .. offsets[b+1]).
  *   union_idx [n] uint32 ascending; *n_union (device int64) = |U|, U = union of V_b.
@@ -275,7 +281,7 @@ size_t gs_visible_sets_workspace_size(int batch, int64_t n);
 gs_status gs_visible_sets(const float* const* proj_per_view, int batch, int64_t n, void* workspace,
                           size_t workspace_bytes, int64_t* offsets, uint32_t* indices,
                           uint32_t* union_idx, int64_t* n_union, int64_t* inter, float* jaccard,
-                          void* stream);
+                          const uint32_t* visible_bits, int64_t bits_stride, void* stream);
 
 /* ---------------------------------------------------------------------------
  * gs_sparse_adam -- Adam on the listed Gaussians only, with the batch scaling rule of

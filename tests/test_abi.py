@@ -49,7 +49,10 @@ def test_host_side_argument_errors(lib):
     assert b"bad n" in lib.gs_last_error()
     assert lib.gs_project(None, 5, C.byref(cam), None, None) == N.GS_ERR_INVALID
     assert lib.gs_loss(None, None, 0, 4, 0.8, 0.2, 1.0, None, 0, None, None, 0, None) == N.GS_ERR_INVALID
-    assert lib.gs_visible_sets(None, 0, 10, None, 0, None, None, None, None, None, None, None) == N.GS_ERR_INVALID
+    assert lib.gs_visible_sets(None, 0, 10, None, 0, None, None, None, None, None, None, None, 0,
+                               None) == N.GS_ERR_INVALID
+    # the batched projection: a bitset stride below ceil(n / 32)
+    assert lib.gs_project_batch(None, 100, C.byref(cam), 1, None, None, 0, None) == N.GS_ERR_INVALID
     assert lib.gs_sparse_adam(None, None, None, None, 10, None, None, 10, 1e-3, 0.9, 0.999, 1e-15, 0, 1, None, 0,
                               None) == N.GS_ERR_INVALID
     bad = N.camera(scenes.make_cameras(0)[0])

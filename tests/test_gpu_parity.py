@@ -135,11 +135,20 @@ def test_project_batch_matches_per_view(case):
         cams = scenes.make_cameras(1)[:18]
     n = P.shape[1]
     projs = [torch.full((3, n, 4), 7.0, dtype=torch.float32, device="cuda") for _ in cams]
-    N.gs_project_batch(dev(P), n, cams, projs)
+    stride = (n + 31) // 32 + 3  # a padded row: the padding is never written
+    bits = torch.full((len(cams), stride), -1, dtype=torch.int32, device="cuda")
+    N.gs_project_batch(dev(P), n, cams, projs, visible_bits=bits, bits_stride=stride)
     torch.cuda.synchronize()
+    hb = host(bits).view(np.uint32)
     for b, cam in enumerate(cams):
         single = gpu_project(P, cam)
         assert np.array_equal(host(projs[b]).view(np.uint32), single.view(np.uint32)), b
+        # the visibility bitset: bit i of the view set iff its radius is > 0, bits past n clear
+        vis = np.zeros(stride * 32 - 96, bool)
+        vis[:n] = single[1, :, 3].view(np.int32) > 0
+        want = np.packbits(vis.reshape(-1, 32)[:, ::-1], axis=1).view(">u4").ravel().astype(np.uint32)
+        assert np.array_equal(hb[b, : stride - 3], want), b
+        assert (hb[b, stride - 3:] == 0xFFFFFFFF).all()
     # and the first view against the oracle's integer decisions
     pr = oracle.project(P, cams[0])
     ok = (pr["margin"] >= MARGIN) & (pr["rmargin"] >= MARGIN)
@@ -652,15 +661,28 @@ def test_visible_sets_bit_exact(B, n):
     nu = torch.zeros(1, dtype=torch.int64, device="cuda")
     inter = torch.zeros((B, B), dtype=torch.int64, device="cuda")
     jac = torch.zeros((B, B), dtype=torch.float32, device="cuda")
-    N.gs_visible_sets(projs, B, n, ws, ws_b, off, ind, uni, nu, inter, jac)
-    torch.cuda.synchronize()
     o_off, o_ind, o_uni, o_inter, o_jac = oracle.visible_sets(radii)
-    assert np.array_equal(host(off), o_off)
-    assert np.array_equal(host(ind)[: o_off[-1]].view(np.uint32), o_ind)
-    assert int(nu.item()) == len(o_uni)
-    assert np.array_equal(host(uni)[: len(o_uni)].view(np.uint32), o_uni)
-    assert np.array_equal(host(inter), o_inter)
-    assert np.array_equal(host(jac), o_jac)
+    # from the radius words, then from the same sets given as bitsets (no proj pointers)
+    stride = (n + 31) // 32 + 1
+    vis = np.zeros((B, stride * 32), bool)
+    vis[:, :n] = radii > 0
+    packed = np.packbits(vis.reshape(B, -1, 32)[:, :, ::-1], axis=2).view(">u4").reshape(B, stride)
+    bits = dev(packed.astype(np.uint32).view(np.int32))
+    for mode in ("radius", "bits"):
+        for t in (off, ind, uni, nu, inter, jac):
+            t.zero_()
+        if mode == "radius":
+            N.gs_visible_sets(projs, B, n, ws, ws_b, off, ind, uni, nu, inter, jac)
+        else:
+            N.gs_visible_sets(None, B, n, ws, ws_b, off, ind, uni, nu, inter, jac, visible_bits=bits,
+                              bits_stride=stride)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(off), o_off), mode
+        assert np.array_equal(host(ind)[: o_off[-1]].view(np.uint32), o_ind), mode
+        assert int(nu.item()) == len(o_uni), mode
+        assert np.array_equal(host(uni)[: len(o_uni)].view(np.uint32), o_uni), mode
+        assert np.array_equal(host(inter), o_inter), mode
+        assert np.array_equal(host(jac), o_jac), mode
 
 
 # ------------------------------------------------------------------ the whole step
