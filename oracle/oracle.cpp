@@ -36,8 +36,11 @@
 // per-pixel compositing, compositing invariants, central finite differences of
 // the whole forward (also from an oblique camera with a clamped Gaussian), SSIM
 // identities, Adam closed form at t = 1, set identities, balanced splits of known
-// cost profiles, worked view orders on block-structured weights.  A mutation
-// test plants mistakes in copies of this file and checks that the pins fail.
+// cost profiles, worked view orders on block-structured weights; closed forms of
+// one opaque Gaussian over a coloured background (forward and backward, the 0.99
+// cap), equal depth keys in the binning sort, Adam with a large epsilon and the
+// update set of a two-view step.  A mutation test plants mistakes in copies of
+// this file, in every stage, and checks that the pins fail.
 
 #include <algorithm>
 #include <cmath>
