@@ -34,9 +34,6 @@ import scenes  # noqa: E402
 METRIC = "train views/s (fwd+bwd+Adam) at N Gaussians x res; % of HBM/FP32 roofline"
 UNIT = "views/s"
 
-# Algorithmic FP32 work of the compositing kernels (FMA = 2 flops), per pixel-Gaussian pair:
-# every evaluated pair costs the offset and the quadratic form (9); an accumulated pair adds
-# the forward blend (10) or the backward chain rule and pixel sum (49).
 # Algorithmic flops per unit of work (FMA = 2): per pixel-Gaussian pair that the pixel itself
 # evaluates through its termination point, 15 for the forward compositing and 40 for the
 # backward (plus one ex2 each, not counted); about 1.3 kflop per pixel for the loss
@@ -197,7 +194,11 @@ def _reach(P, cam):
 
 def _band_reach(info, width, r0, rows):
     """Indices of every Gaussian whose tile rectangle can meet rows [r0, r0 + rows) (a
-    superset), so a band rendered from them alone equals those rows of the whole view."""
+    superset), so that the band's camera renders the same image from them alone as from the
+    whole scene.  (The band's camera is the view's with the principal point moved up by r0 and
+    an image `rows` high: its field of view, and with it the 1.3 tan(fov/2) clamp of the
+    projection's Jacobian in y, is the band's, so its image is close to, not equal to, those
+    rows of the whole view: a sample of the view's work, not of its pixels.)"""
     u, v, r, front = info
     hit = front & (u + r >= 0) & (u - r <= width) & (v + r >= r0) & (v - r <= r0 + rows)
     return np.nonzero(hit)[0]
@@ -232,11 +233,12 @@ def available_host_bytes() -> int:
 
 
 class OracleSampler:
-    """Times the CPU oracle, as it stands, on the host cores: one spawned process per core,
-    each running the oracle's whole step (batch 1) on its own band of `rows` image rows at full
-    width (consecutive bands of view 0, then of the next views), on the Gaussians that can
-    reach the band.  One round = every process takes one step; throughput = (bands x rows /
-    height) views / wall time of the round."""
+    """Times the CPU oracle, as it stands, on the host cores: one spawned process per core (as
+    many as the host memory holds), each running the oracle's whole step (batch 1) on its own
+    band of `rows` image rows at full width (one band in the middle of each equal share of view
+    0's rows, then of the next views), on the Gaussians that can reach the band.  One round =
+    every process takes one step; throughput = (bands x rows / height) views / wall time of the
+    round."""
 
     # host memory the oracle's step holds per Gaussian it is given (double-precision parameters,
     # moments and gradients, and its per-Gaussian records): a worker's peak resident set on a
@@ -257,11 +259,14 @@ class OracleSampler:
     def _band_idx(self, k):
         """Band k: its camera, its height and the indices of the Gaussians that can reach it."""
         H = self.cfg.height
-        # the processes' bands spread evenly over the image height (the content of a view is not
-        # uniform: the top rows of a city view see little), then over the next views
+        # the processes' bands spread evenly over the image height, each in the middle of its
+        # equal share of the rows (the content of a view is not uniform: the top rows of a city
+        # view see little, so a band at the top of each share would favour the empty sky), then
+        # over the next views
         per_view = max(1, min(H // self.rows, self.workers))
         view = (k // per_view) % len(self.cams)
-        r0 = min(((k % per_view) * H // per_view) // 16 * 16, max(0, H - self.rows))
+        mid = (2 * (k % per_view) + 1) * H // (2 * per_view)
+        r0 = min(max(0, mid - self.rows // 2) // 16 * 16, max(0, H - self.rows) // 16 * 16)
         rows = min(self.rows, H - r0)
         c = self.cams[view]
         cam = scenes.Camera(c.R, c.t, c.fx, c.fy, c.cx, c.cy - r0, c.znear, c.width, rows)
@@ -334,10 +339,11 @@ class OracleSampler:
         self.procs = []
 
     def describe(self, wall):
-        return (f"{self.workers} processes (one per host core), each the oracle's whole step (project, bin, "
-                f"composite, loss, backward, Adam; batch 1, double precision) on its own band of {self.rows} rows "
-                f"at full width (bands spread evenly over the height of view 0, then of the next views) with the "
-                f"Gaussians that can reach it; {wall:.1f} s per round")
+        return (f"{self.workers} processes (one per host core, as many as half the free host memory holds), "
+                f"each the oracle's whole step (project, bin, composite, loss, backward, Adam; batch 1, double "
+                f"precision) on its own band of {self.rows} rows at full width (one band in the middle of each "
+                f"equal share of view 0's height, then of the next views) with the Gaussians that can reach it; "
+                f"{wall:.1f} s per round")
 
 
 # ---------------------------------------------------------------------- main
