@@ -213,3 +213,34 @@ def test_step_updates_the_union_of_the_views_visible_sets():
     assert (res["params"][:, only_second] != P[:, only_second]).any()
     assert np.array_equal(res["params"][:, neither], P[:, neither])
     assert np.array_equal(res["m"][:, neither], m0[:, neither])
+
+
+# ------------------------------------------------------------------ clamped colour channel
+def test_clamped_colour_channel_passes_no_gradient():
+    """A colour channel whose SH sum + 0.5 is negative is clamped to 0, so near the parameters
+    the loss does not depend on that channel's 16 coefficients (their gradient is exactly 0)
+    and the view direction reaches the loss only through the other channels (the mean's
+    gradient matches central differences)."""
+    P, cam = scenes.tiny_scene(6, 14, width=32, height=32, focal=40.0)
+    P = P.astype(np.float64)
+    P[3, 0, 0] = -3.0  # sh[0][red]: 0.282 * -3 + 0.5 < 0
+    for kk in range(1, 16):
+        f = 3 * kk
+        P[3 + f // 4, 0, f % 4] = 0.05 * ((-1) ** kk)
+    pr = oracle.project(P, cam)
+    assert pr["radius"][0] > 0 and pr["raw"][0, 0] < -0.2 and pr["rgb"][0, 0] == 0.0
+    tgt = np.random.default_rng(114).uniform(0.0, 1.0, size=(1, 3, 32, 32))
+    res = oracle.step(P, np.zeros_like(P), np.zeros_like(P), [cam], tgt, do_adam=False)
+    G = res["grads"]
+    for kk in range(16):
+        f = 3 * kk
+        assert G[3 + f // 4, 0, f % 4] == 0.0, kk
+    assert np.abs(G[3:, 0]).max() > 0  # the other channels do get gradients
+    loss = lambda Q: oracle.step(Q, np.zeros_like(P), np.zeros_like(P), [cam], tgt, do_adam=False)["loss"]
+    for lane in range(3):
+        h = 1e-5 * max(1.0, abs(P[0, 0, lane]))
+        Pp, Pm = P.copy(), P.copy()
+        Pp[0, 0, lane] += h
+        Pm[0, 0, lane] -= h
+        num = (loss(Pp) - loss(Pm)) / (2 * h)
+        assert abs(num - G[0, 0, lane]) <= 1e-4 * abs(num) + 1e-9, (lane, num, G[0, 0, lane])

@@ -69,6 +69,41 @@ MUTATIONS = {
     # densification: a mean exactly at the threshold not selected
     "densify_threshold_strict": ("if (!(avg >= grad_threshold)) continue;", "if (!(avg > grad_threshold)) continue;"),
 
+    # backward: sign of the screen position's depth derivative
+    "bwd_u_depth_sign": ("dpc[2] += -du * k.fx * x / (z * z) - dv * k.fy * y / (z * z);",
+                         "dpc[2] += du * k.fx * x / (z * z) - dv * k.fy * y / (z * z);"),
+    # backward: d conic_A / d a with c in place of c^2
+    "bwd_conic_ga": ("const double ga = dconic[0] * (-c * c / d2)", "const double ga = dconic[0] * (-c / d2)"),
+    # backward: sign of a term of d conic_B / d b
+    "bwd_conic_gb": ("dconic[1] * (-1.0 / det - 2 * b * b / d2)", "dconic[1] * (-1.0 / det + 2 * b * b / d2)"),
+    # backward: the shared off-diagonal's gradient not split between the two entries
+    "bwd_offdiag_not_halved": ("const double G2[2][2] = {{ga, 0.5 * gb}, {0.5 * gb, gc}};",
+                               "const double G2[2][2] = {{ga, gb}, {gb, gc}};"),
+    # backward: d(T Sig T^T) / dT without its factor 2
+    "bwd_dTm_factor": ("acc += 2.0 * G2[ii][jj] * p.Tm[jj][m] * p.Sig[m][l];",
+                       "acc += G2[ii][jj] * p.Tm[jj][m] * p.Sig[m][l];"),
+    # backward: d(fx / z) / dz as -fx / z
+    "bwd_J00_depth": ("dpc[2] += dJ[0][0] * (-k.fx / (z * z)) + dJ[1][1] * (-k.fy / (z * z));",
+                      "dpc[2] += dJ[0][0] * (-k.fx / z) + dJ[1][1] * (-k.fy / (z * z));"),
+    # backward: d(-fx x / z^2) / dz without its factor 2
+    "bwd_J02_depth_factor": ("dpc[2] += dJ[0][2] * (2.0 * k.fx * x / (z * z * z));",
+                             "dpc[2] += dJ[0][2] * (k.fx * x / (z * z * z));"),
+    # backward: the y clamp's branches exchanged
+    "bwd_clamp_y_branches": ("if (p.cly) {", "if (!p.cly) {"),
+    # backward: d(M M^T) / dM not symmetrised
+    "bwd_sigma_not_symmetrised": ("acc += (dSig[l][n2] + dSig[n2][l]) * M[n2][m];", "acc += dSig[l][n2] * M[n2][m];"),
+    # backward: log-scale gradient without ds / dlog s = s
+    "bwd_scale_chain": ("dls[m] = acc * p.s[m];", "dls[m] = acc;"),
+    # backward: a sign in d R / d w
+    "bwd_quat_w_sign": ("dq[0] = 2 * (-qz * dRq[0][1]", "dq[0] = 2 * (qz * dRq[0][1]"),
+    # backward: the quaternion's normalisation left out of its gradient
+    "bwd_quat_no_normalisation": ("dqraw[l] = (dq[l] - p.qn[l] * dot) / p.qlen;", "dqraw[l] = dq[l] / p.qlen;"),
+    # backward: a colour channel clamped at 0 still passes gradients
+    "bwd_colour_mask": ("if (p.raw[ch] < 0) continue;", "(void)0;"),
+    # backward: sigmoid derivative without (1 - o)
+    "bwd_dlogit": ("const double dlogit = dopac * p.o * (1.0 - p.o);", "const double dlogit = dopac * p.o;"),
+    # backward: SH gradient written to the coefficient index instead of the (k, channel) float
+    "bwd_sh_layout": ("G(3 + f / 4, f % 4) += gch * p.Y[kk];", "G(3 + kk / 4, kk % 4) += gch * p.Y[kk];"),
     # compositing: sign of the exponent's cross term
     "power_cross_sign": ("const double power = -0.5 * (A * dx * dx + Cc * dy * dy) - B * dx * dy;",
                          "const double power = -0.5 * (A * dx * dx + Cc * dy * dy) + B * dx * dy;"),
