@@ -56,10 +56,6 @@ class Camera:
     def n_tiles(self) -> int:
         return self.tiles_x * self.tiles_y
 
-    @property
-    def n_pixels(self) -> int:
-        return self.width * self.height
-
 
 @dataclasses.dataclass
 class SceneConfig:
@@ -230,12 +226,6 @@ def make_cameras(cfg: SceneConfig | int, seed: int | None = None) -> list[Camera
             tgt = (0.0, -0.5, 0.0)
         cams.append(look_at(eye, tgt, W, H, f, cfg.znear))
     return cams
-
-
-def camera_array(cam: Camera) -> np.ndarray:
-    """Camera as 17 float64 values: R (row-major 9), t (3), fx, fy, cx, cy, znear."""
-    return np.concatenate([cam.R.astype(np.float64).ravel(), cam.t.astype(np.float64),
-                           np.array([cam.fx, cam.fy, cam.cx, cam.cy, cam.znear], dtype=np.float64)])
 
 
 def batch_views(cfg: SceneConfig, step: int) -> list[int]:
