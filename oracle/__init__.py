@@ -57,6 +57,8 @@ def lib():
         L.oracle_bin_sort.restype = i64
         L.oracle_render_fwd.argtypes = [dp, dp, dp, up, up, i32, i32, dp, dp, dp, up, dp]
         L.oracle_render_fwd.restype = None
+        L.oracle_render_counts.argtypes = [dp, dp, dp, up, up, i32, i32, up, up]
+        L.oracle_render_counts.restype = None
         L.oracle_render_bwd.argtypes = [dp, dp, dp, up, up, i32, i32, dp, dp, dp]
         L.oracle_render_bwd.restype = None
         L.oracle_loss.argtypes = [dp, dp, i32, i32, dbl, dbl, dbl, dp]
@@ -150,6 +152,22 @@ def render_fwd(uvzo, conic, rgb, vals, ranges, width, height, bg=(0.0, 0.0, 0.0)
                             _p(T, C.c_double), _p(nc, C.c_uint32), _p(mg, C.c_double))
     del P
     return img, T, nc, mg
+
+
+def render_counts(uvzo, conic, rgb, vals, ranges, width, height):
+    """Per-pixel work of the compositing walk, two [H][W] uint32 arrays: entries evaluated
+    (through the one that would take the transmittance below 1e-4, else the whole tile list)
+    and entries accumulated."""
+    U, Q, Cc = _d(uvzo), _d(conic), _d(rgb)
+    V = np.ascontiguousarray(vals, np.uint32)
+    if V.size == 0:
+        V = np.zeros(1, np.uint32)
+    Rg = np.ascontiguousarray(ranges, np.uint32)
+    n_eval = np.zeros((height, width), np.uint32)
+    n_used = np.zeros((height, width), np.uint32)
+    lib().oracle_render_counts(_p(U, C.c_double), _p(Q, C.c_double), _p(Cc, C.c_double), _p(V, C.c_uint32),
+                               _p(Rg, C.c_uint32), width, height, _p(n_eval, C.c_uint32), _p(n_used, C.c_uint32))
+    return n_eval, n_used
 
 
 def render_bwd(uvzo, conic, rgb, vals, ranges, width, height, dimg, bg=(0.0, 0.0, 0.0)):

@@ -33,7 +33,8 @@
 // pinhole map; hand-worked closed forms off the axis, for quarter turns and
 // beyond the field-of-view clamp; the view-dependent colour from two opposite
 // cameras; SH against scipy's complex harmonics and by quadrature, brute-force
-// per-pixel compositing, compositing invariants, central finite differences of
+// per-pixel compositing (image, transmittance and the walk's work counts),
+// compositing invariants, central finite differences of
 // the whole forward (also from an oblique camera with a clamped Gaussian), SSIM
 // identities, Adam closed form at t = 1, set identities, balanced splits of known
 // cost profiles, worked view orders on block-structured weights; closed forms of
@@ -346,6 +347,8 @@ struct PixelResult {
   double C[3];
   double T;
   uint32_t n_contrib;
+  uint32_t n_eval;  // list entries evaluated: through the terminating one, else the whole list
+  uint32_t n_used;  // list entries accumulated
   double margin;
   std::vector<Contrib> used;
 };
@@ -362,6 +365,8 @@ PixelResult composite_pixel(const View2D& in, const uint32_t* vals, uint32_t sta
   pr.C[0] = pr.C[1] = pr.C[2] = 0;
   pr.T = 1.0;
   pr.n_contrib = 0;
+  pr.n_eval = end - start;
+  pr.n_used = 0;
   pr.margin = 1e30;
   const float a_min = 1.0f / 255.0f, a_max = 0.99f, t_min = 1e-4f;
   for (uint32_t j = start; j < end; ++j) {
@@ -381,11 +386,15 @@ PixelResult composite_pixel(const View2D& in, const uint32_t* vals, uint32_t sta
     if (f32(alpha) < a_min) continue;
     const double Tn = pr.T * (1.0 - alpha);
     pr.margin = std::min(pr.margin, relm(Tn, t_min));
-    if (f32(Tn) < t_min) break;  // stop before this Gaussian
+    if (f32(Tn) < t_min) {  // stop before this Gaussian
+      pr.n_eval = j - start + 1;
+      break;
+    }
     for (int c = 0; c < 3; ++c) pr.C[c] += in.rgb[3 * g + c] * alpha * pr.T;
     if (keep) pr.used.push_back({g, alpha, pr.T, G, clamped, dx, dy});
     pr.T = Tn;
     pr.n_contrib = j - start + 1;
+    ++pr.n_used;
   }
   return pr;
 }
@@ -974,6 +983,23 @@ void oracle_render_fwd(const double* uvzo, const double* conic, const double* rg
   Cam k = load_cam(dummy, W, H);
   View2D in{uvzo, conic, rgb};
   render_fwd(in, vals, ranges, k, bg, img, T_final, n_contrib, margin);
+}
+
+// Per-pixel work of the compositing walk, [H][W] each: n_eval = list entries evaluated (through
+// the one whose transmittance would fall below 1e-4, else the whole tile list), n_used = entries
+// accumulated.
+void oracle_render_counts(const double* uvzo, const double* conic, const double* rgb, const uint32_t* vals,
+                          const uint32_t* ranges, int W, int H, uint32_t* n_eval, uint32_t* n_used) {
+  double dummy[17] = {0};
+  Cam k = load_cam(dummy, W, H);
+  View2D in{uvzo, conic, rgb};
+  for (int py = 0; py < H; ++py)
+    for (int px = 0; px < W; ++px) {
+      const int64_t t = (int64_t)(py / TILE) * k.Tx + px / TILE;
+      const PixelResult pr = composite_pixel(in, vals, ranges[2 * t], ranges[2 * t + 1], px, py, false);
+      n_eval[(int64_t)py * W + px] = pr.n_eval;
+      n_used[(int64_t)py * W + px] = pr.n_used;
+    }
 }
 
 // g2d: N x 9, accumulated (+=).

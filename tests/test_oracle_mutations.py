@@ -115,7 +115,12 @@ MUTATIONS = {
     # compositing: no skip of alphas below 1/255
     "no_alpha_skip": ("if (f32(alpha) < a_min) continue;", "if (f32(alpha) <= 0.0f) continue;"),
     # compositing: termination tested on the transmittance before the Gaussian
-    "termination_before": ("if (f32(Tn) < t_min) break;", "if (f32(pr.T) < t_min) break;"),
+    "termination_before": ("if (f32(Tn) < t_min) {  // stop before this Gaussian",
+                           "if (f32(pr.T) < t_min) {  // stop before this Gaussian"),
+    # work counts: the entry that ends the walk not counted as evaluated
+    "count_eval_terminator": ("pr.n_eval = j - start + 1;", "pr.n_eval = j - start;"),
+    # work counts: list positions counted as accumulated entries
+    "count_used_positions": ("++pr.n_used;", "pr.n_used = pr.n_contrib;"),
     # compositing: colour weighted by the transmittance after the Gaussian
     "weight_after": ("pr.C[c] += in.rgb[3 * g + c] * alpha * pr.T;", "pr.C[c] += in.rgb[3 * g + c] * alpha * Tn;"),
     # compositing: the background not attenuated by the final transmittance

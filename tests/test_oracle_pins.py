@@ -114,7 +114,8 @@ def test_single_isotropic_gaussian_closed_form(logs, logit, sh0):
 # ------------------------------------------------------------------ brute-force compositing
 def _brute_force_image(pr, W, H):
     """Every pixel: all r > 0 Gaussians whose tile square covers the pixel's tile,
-    sorted by (fp32 depth, index), composited front to back."""
+    sorted by (fp32 depth, index), composited front to back.  Also counts, per pixel, the
+    entries evaluated (through the one that ends the walk, else all) and accumulated."""
     N = pr["radius"].shape[0]
     u = pr["uvzo"][:, 0].astype(np.float32).astype(np.float64)
     v = pr["uvzo"][:, 1].astype(np.float32).astype(np.float64)
@@ -127,6 +128,8 @@ def _brute_force_image(pr, W, H):
     y1 = np.clip(np.floor((v + r) / 16) + 1, 0, ty)
     img = np.zeros((3, H, W))
     Tf = np.ones((H, W))
+    n_eval = np.zeros((H, W), np.uint32)
+    n_used = np.zeros((H, W), np.uint32)
     for py in range(H):
         for px in range(W):
             tX, tY = px // 16, py // 16
@@ -134,7 +137,8 @@ def _brute_force_image(pr, W, H):
             order = sorted(sel.tolist(), key=lambda i: (float(z32[i]), i))
             T = 1.0
             C = np.zeros(3)
-            for i in order:
+            n_eval[py, px] = len(order)
+            for pos, i in enumerate(order):
                 dx = px + 0.5 - pr["uvzo"][i, 0]
                 dy = py + 0.5 - pr["uvzo"][i, 1]
                 A, B, Cc = pr["conic"][i]
@@ -148,12 +152,14 @@ def _brute_force_image(pr, W, H):
                     continue
                 Tn = T * (1 - a)
                 if np.float32(Tn) < np.float32(1e-4):
+                    n_eval[py, px] = pos + 1
                     break
                 C += pr["rgb"][i] * a * T
                 T = Tn
+                n_used[py, px] += 1
             img[:, py, px] = C
             Tf[py, px] = T
-    return img, Tf
+    return img, Tf, n_eval, n_used
 
 
 @pytest.mark.parametrize("seed,n", [(3, 40), (4, 150)])
@@ -164,9 +170,19 @@ def test_tiled_compositing_equals_brute_force(seed, n):
     assert (pr["radius"] > 0).sum() > n // 2
     keys, vals, ranges = oracle.bin_sort(pr["uvzo"], pr["radius"], cam.width, cam.height)
     img, T, nc, _ = oracle.render_fwd(pr["uvzo"], pr["conic"], pr["rgb"], vals, ranges, cam.width, cam.height)
-    ref, Tref = _brute_force_image(pr, cam.width, cam.height)
+    ref, Tref, eval_ref, used_ref = _brute_force_image(pr, cam.width, cam.height)
     assert np.allclose(img, ref, atol=1e-12)
     assert np.allclose(T, Tref, atol=1e-12)
+    n_eval, n_used = oracle.render_counts(pr["uvzo"], pr["conic"], pr["rgb"], vals, ranges, cam.width, cam.height)
+    assert np.array_equal(n_eval, eval_ref) and np.array_equal(n_used, used_ref)
+    assert (n_used <= nc).all() and (nc <= n_eval).all()
+    tx = (cam.width + 15) // 16
+    ys, xs = np.mgrid[0:cam.height, 0:cam.width]
+    lens = (ranges[:, 1] - ranges[:, 0])[(ys // 16) * tx + xs // 16]
+    assert (n_eval <= lens).all()
+    if seed == 4:
+        assert (n_eval < lens).any()  # some walks end at the transmittance floor
+    assert (n_used < nc).any()  # some entries are skipped before a pixel's last accumulated one
 
 
 def test_binning_matches_python_stable_sort():
