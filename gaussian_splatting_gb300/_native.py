@@ -10,6 +10,8 @@ from __future__ import annotations
 import ctypes as C
 import os
 
+import numpy as np
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgs.so")
 
@@ -42,8 +44,8 @@ class Camera(C.Structure):
 def camera(cam) -> Camera:
     """gs_camera from any object with R, t, fx, fy, cx, cy, znear, width, height."""
     c = Camera()
-    R = [float(x) for x in __import__("numpy").asarray(cam.R, dtype="float32").ravel()]
-    t = [float(x) for x in __import__("numpy").asarray(cam.t, dtype="float32").ravel()]
+    R = [float(x) for x in np.asarray(cam.R, dtype=np.float32).ravel()]
+    t = [float(x) for x in np.asarray(cam.t, dtype=np.float32).ravel()]
     c.R[:] = R
     c.t[:] = t
     c.fx, c.fy, c.cx, c.cy, c.znear = cam.fx, cam.fy, cam.cx, cam.cy, cam.znear
