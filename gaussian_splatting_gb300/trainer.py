@@ -1,20 +1,19 @@
 """One 3D Gaussian Splatting training step on one GPU, driven through libgs.so.
 
-``Trainer`` owns the device state (parameters, gradients, Adam moments, per-view scratch)
-as torch tensors -- torch supplies memory and the stream, every computation is a libgs.so
-kernel -- and issues, per batch, the calls of the step in the order of the Grendel-GS
-training flow (训练流程): project every view (gs_project_batch), bin/sort them all (gs_bin_sort_batch: the
-views' depth sorts share one launch), then for each view composite -> loss -> composite
-backward (both compositing calls issue their tiles heaviest first, gs_tile_order); then the visible sets, and the projection backward of every view
-with the visible-only Adam update (Odin summary, 研究背景与动机; Grendel-GS notes §4.2 batch
-scaling) in one fused pass (gs_project_bwd_adam) whose gradients never leave the chip.
-``step_async(..., adam=False)`` runs the per-view gs_project_bwd instead and leaves the
-summed gradients in ``grads``.
+``Trainer`` owns the device state (parameters, gradients, Adam moments, per-view scratch) as
+torch tensors -- torch supplies memory and the stream, every computation is a libgs.so kernel
+-- and issues, per batch, the calls of the step in the order of the Grendel-GS training flow
+(训练流程): project every view (gs_project_batch), bin/sort them all (gs_bin_sort_batch: the views'
+depth sorts share one launch), then for each view composite -> loss -> composite backward (both
+compositing calls issue their tiles heaviest first, gs_tile_order); then the visible sets, and
+the projection backward of every view with the visible-only Adam update (Odin summary, 研究背景与动机;
+Grendel-GS notes §4.2 batch scaling) in one fused pass (gs_project_bwd_adam) whose gradients
+never leave the chip. ``step_async(..., adam=False)`` runs the per-view gs_project_bwd instead
+and leaves the summed gradients in ``grads``.
 
-The step never synchronises with the host.  The tile-instance buffers have a capacity;
-when a view overflows it, the update skips itself (it reads the per-view status words),
-``step`` notices on its one readback of the loss, grows the buffers and runs the batch
-again.
+The step never synchronises with the host. The tile-instance buffers have a capacity; when a
+view overflows it, the update skips itself (it reads the per-view status words), ``step``
+notices on its one readback of the loss, grows the buffers and runs the batch again.
 """
 from __future__ import annotations
 
